@@ -1,0 +1,379 @@
+"""Decode benchmark: the 32-layer Qwen3.5-4B-shape stack at batch 1.
+
+Workload (default): layer i is full attention when i % 4 == 3, else Gated
+DeltaNet; int8 group-64 synthetic weights (3.79 GB, larger than L2, so every
+step streams them from HBM); bf16 KV caches prefilled to 8192 tokens; GDN
+states N(0, 0.1); conv states zero. One step = one token through all 32 layers,
+replayed as one CUDA graph (qwen35_graph_*); the graph advances the device
+position, so the context grows by one token per step.
+
+Prints one JSON line. --impl reference times the CPU oracle on the same
+workload instead (bounded sample per step; see cpu_sample).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode tok/s (32-layer 4B-shape stack, batch 1); achieved HBM GB/s vs peak"
+PREFILL = 8192
+SEED = 0
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def algorithmic_bytes(cfg: dict, seq_len: int) -> dict:
+    """Bytes a decode step must move: every weight, scale and bias once, K/V rows
+    [0, seq_len) once per full-attention layer plus the appended row, GDN and conv
+    state read and written once, norm vectors and the small per-head vectors."""
+    from full_attention_decode_gb300 import synth
+    E, I, H, Hkv, D = cfg["hidden"], cfg["intermediate"], cfg["num_heads"], cfg["num_kv_heads"], cfg["head_dim"]
+    Hk, Hv, Dk, Dv, Kc = (cfg["num_k_heads_lin"], cfg["num_v_heads_lin"], cfg["k_head_dim_lin"],
+                          cfg["v_head_dim_lin"], cfg["conv_kernel_size"])
+    C = 2 * Hk * Dk + Hv * Dv
+
+    def q(n, k):
+        return n * k + 2 * n * (k // 64) * 2  # codes + bf16 scale + bf16 bias per group
+
+    mlp = q(I, E) * 2 + q(E, I)
+    fa_w = q(2 * H * D, E) + 2 * q(Hkv * D, E) + q(E, H * D) + mlp + 2 * (2 * E + 2 * D)
+    gdn_w = q(Hv, E) * 2 + q(C, E) + q(Hv * Dv, E) + q(E, Hv * Dv) + mlp + 2 * (2 * E + Dv) + \
+        Hv * (4 + 2) + C * Kc * 2
+    gdn_state = 2 * (Hv * Dk * Dv * 4 + C * Kc * 4)
+    kv = lambda S: 2 * S * Hkv * D * 2 + 2 * Hkv * D * 2  # noqa: E731
+    kinds = synth.layer_kinds(cfg)
+    n_fa = kinds.count("fa")
+    n_gdn = kinds.count("gdn")
+    weights = n_fa * fa_w + n_gdn * gdn_w
+    return {"weights": weights, "gemv_weights": n_fa * (q(2 * H * D, E) + 2 * q(Hkv * D, E) + q(E, H * D) + mlp)
+            + n_gdn * (q(Hv, E) * 2 + q(C, E) + q(Hv * Dv, E) + q(E, Hv * Dv) + mlp),
+            "step": weights + n_gdn * gdn_state + n_fa * kv(seq_len), "fa_layer_w": fa_w, "gdn_layer_w": gdn_w,
+            "gdn_state": gdn_state}
+
+
+# ---------------------------------------------------------------------- clocks
+
+
+class Clocks:
+    """Samples nvidia-smi SM clocks and throttle reasons while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.rows = []
+        if self.proc is None:
+            return
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) >= 9:
+                self.rows.append(f)
+
+    def summary(self) -> dict:
+        if not getattr(self, "rows", None):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[5 + i].lower() == "active"})
+        loaded = sorted(sm)[len(sm) // 2:] if sm else []
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------- GPU arm
+
+
+def run_gpu(args) -> dict | None:
+    import numpy as np
+    import torch
+
+    from full_attention_decode_gb300 import binding as B
+    from full_attention_decode_gb300 import synth
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    B.qwen35_init()
+
+    cfg = synth.config("4b")
+    c = B.make_config(cfg)
+    kinds = synth.layer_kinds(cfg)
+    cap = PREFILL + args.warmup + args.steps + 2 * (args.steps + 4) + 8
+    seed = SEED + rank  # each replica decodes its own sequence
+    t0 = time.time()
+    dev_layers, caches, entries = [], [], []
+    for i, kind in enumerate(kinds):
+        if kind == "fa":
+            dl = B.DeviceFaLayer(synth.fa_layer(seed, i, cfg))
+            kb, vb = synth.kv_cache(seed, i, cfg, cap, PREFILL)
+            cc = B.DeviceKv(kb, vb)
+        else:
+            dl = B.DeviceGdnLayer(synth.gdn_layer(seed, i, cfg))
+            conv, ssm = synth.gdn_state(seed, i, cfg, std=0.1)
+            cc = B.DeviceState(conv, ssm)
+        dev_layers.append(dl)
+        caches.append(cc)
+        entries.append(B.stack_layer(kind, dl, cc))
+    setup_s = time.time() - t0
+
+    stream = torch.cuda.Stream()
+    scratch = B.new_scratch(B.qwen35_stack_scratch_bytes(c), stream=stream)
+    x_in = torch.empty(cfg["hidden"], dtype=torch.int16, device="cuda")
+    x_out = torch.empty_like(x_in)
+    d_pos = torch.full((1,), PREFILL, dtype=torch.int32, device="cuda")
+    with torch.cuda.stream(stream):
+        x_in.copy_(B.to_device(synth.x_in(seed, 0, cfg)))
+    stream.synchronize()
+    with torch.cuda.stream(stream):
+        graph = B.Graph(c, entries, scratch, x_in, x_out, d_pos, cap)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # ---- device-resident timing: K graph replays
+    for _ in range(args.warmup):
+        graph.launch(stream)
+    barrier()
+    pos0 = PREFILL + args.warmup
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with Clocks(local) as clk:
+        ev0.record(stream)
+        for _ in range(args.steps):
+            graph.launch(stream)
+        ev1.record(stream)
+        stream.synchronize()
+    barrier()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    if dist is not None:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    status = B.qwen35_read_device_status(scratch, stream)
+
+    # ---- end to end through the C ABI with host buffers: H2D of the step's
+    # input vector, the graph, D2H of its output, every step
+    h_in = torch.empty_like(x_in, device="cpu").pin_memory()
+    h_out = torch.empty_like(x_out, device="cpu").pin_memory()
+    h_in.copy_(torch.from_numpy(synth.x_in(seed, 1, cfg).view(np.int16)))
+    barrier()
+    t_e0 = time.perf_counter()
+    for _ in range(args.steps):
+        with torch.cuda.stream(stream):
+            x_in.copy_(h_in, non_blocking=True)
+            graph.launch(stream)
+            h_out.copy_(x_out, non_blocking=True)
+        stream.synchronize()
+    e2e_ms = (time.perf_counter() - t_e0) * 1e3 / args.steps
+    barrier()
+    if dist is not None:
+        t = torch.tensor([e2e_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    # ---- dominant kernel alone: the quantised GEMV over every layer's gate_proj
+    # (9216 x 2560, 25.1 MB each) back to back, rotating through 32 distinct
+    # matrices so nothing is served from L2
+    mats = [dl.m["gate_proj"] for dl in dev_layers]
+    xv = torch.zeros(cfg["hidden"], dtype=torch.int16, device="cuda")
+    yv = torch.empty(cfg["intermediate"], dtype=torch.int16, device="cuda")
+    gs = B.new_scratch(4096, stream=stream)
+    cw = [m.c() for m in mats]
+    reps = 4
+    with torch.cuda.stream(stream):
+        for w in cw:
+            B.qwen35_gemv(w, xv, yv, gs, stream)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            for w in cw:
+                assert B.qwen35_gemv(w, xv, yv, gs, stream) == 0
+        e1.record(stream)
+    stream.synchronize()
+    gemv_ms = e0.elapsed_time(e1) / (reps * len(cw))
+    m0 = mats[0]
+    gemv_bytes = m0.n * m0.k + 2 * m0.n * (m0.k // 64) * 2
+    graph.close()
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return None
+
+    peak, peak_kind = _peaks()
+    seq_mid = pos0 + args.steps // 2 + 1
+    ab = algorithmic_bytes(cfg, seq_mid)
+    tok_s = 1000.0 / ms * world
+    step_gbs = ab["step"] / (ms * 1e-3) / 1e9
+    gemv_gbs = gemv_bytes / (gemv_ms * 1e-3) / 1e9
+    launches_per_step = sum(6 if k == "fa" else 5 for k in kinds) + 1
+    res = {
+        "metric": METRIC, "value": round(tok_s, 2), "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int8-weight/bf16-act/fp32-acc", "data": "synthetic",
+        "config": {"workload": "qwen3.5-4b-shape 32-layer decode stack, batch 1, KV prefilled to 8192",
+                   "layers": "24 gated-deltanet + 8 full-attention (i % 4 == 3)",
+                   "context": [pos0 + 1, pos0 + args.steps], "global_batch": world, "seq_len": seq_mid,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single gpu",
+                   "l2": "inputs larger than L2: 3.79 GB of weights streamed per step",
+                   "graph": "one CUDA graph per step", "seed": SEED,
+                   "bytes_per_step": ab["step"], "hbm_gbs_step": round(step_gbs, 1),
+                   "frac_step_of_peak": round(step_gbs / peak, 4), "peak_gbs": peak,
+                   "frac_step_of_8000": round(step_gbs / 8000.0, 4),
+                   "device_status": status, "setup_s": round(setup_s, 1)},
+        "roofline": {"bound": "hbm", "achieved": round(gemv_gbs, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(gemv_gbs / peak, 4), "traffic": None,
+                     "kernel": "gemv_q8g64_kernel (gate_proj 9216x2560, one launch)",
+                     "bytes_per_launch": gemv_bytes, "us_per_launch": round(gemv_ms * 1e3, 2),
+                     "peak_kind": peak_kind},
+        "e2e": {"value": round(1000.0 / e2e_ms * world, 2), "unit": "tok/s", "ms_per_step": round(e2e_ms, 4),
+                "h2d_bytes_per_step": cfg["hidden"] * 2, "d2h_bytes_per_step": cfg["hidden"] * 2},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+    }
+    if dist is not None:
+        dist.destroy_process_group()
+    return res
+
+
+# ---------------------------------------------------------------------- CPU oracle
+
+
+def cpu_sample(n_steps: int, per_step_layers: int = 1) -> dict:
+    """Time the oracle as it stands on a bounded sample of the workload.
+
+    The sample is the first four layers of the stack (three Gated DeltaNet layers
+    and the first full-attention layer at 8192 tokens of context), cycled one
+    layer per sample step; tok/s = 1 / (32 x mean layer time). Single-threaded
+    (BLAS threads pinned to 1 before numpy loads).
+    """
+    import numpy as np
+
+    from full_attention_decode_gb300 import synth
+    from oracle import qwen35_oracle as O
+    cfg = synth.config("4b")
+    kinds = synth.layer_kinds(cfg)[:4]
+    layers, caches = [], []
+    for i, kind in enumerate(kinds):
+        if kind == "fa":
+            layers.append(synth.fa_layer(SEED, i, cfg))
+            kb, vb = synth.kv_cache(SEED, i, cfg, PREFILL + n_steps + 8, PREFILL)
+            caches.append(O.kv_from_bits(kb, vb))
+        else:
+            layers.append(synth.gdn_layer(SEED, i, cfg))
+            conv, ssm = synth.gdn_state(SEED, i, cfg, std=0.1)
+            caches.append(O.state_from_arrays(conv, ssm))
+    x = O.bf16_to_f64(synth.x_in(SEED, 0, cfg))
+    times = []
+    pos = PREFILL
+    for s in range(n_steps):
+        i = s % 4
+        t0 = time.perf_counter()
+        if kinds[i] == "fa":
+            x = O.forward_full_attention(cfg, layers[i], caches[i], x, pos, pos + 1)
+            pos += 1
+        else:
+            x = O.forward_linear_attention(cfg, layers[i], caches[i], x)
+        times.append(time.perf_counter() - t0)
+    mean = float(np.mean(times))
+    return {"value": 1.0 / (32 * mean), "unit": "tok/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n_steps} single-layer forwards cycling the stack's first 4 layers "
+                      f"(3 GDN + 1 FA at 8192 context), float64 numpy; tok/s = 1/(32 x mean layer time); "
+                      f"mean {mean * 1e3:.1f} ms/layer (first pass of each layer includes its dequantisation)",
+            "layer_ms": round(mean * 1e3, 2), "host_cores": os.cpu_count()}
+
+
+def cpu_sample_subprocess(n_steps: int) -> dict | None:
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    try:
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-sample", str(n_steps)],
+                           env=env, capture_output=True, text=True, timeout=600)
+        return json.loads(r.stdout.strip().splitlines()[-1])
+    except Exception as e:  # reported, not fatal
+        return {"value": None, "unit": "tok/s", "cores": 1, "kind": "oracle", "sample": f"failed: {e}"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=512)
+    ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-sample", type=int, default=0, help=argparse.SUPPRESS)
+    ap.add_argument("--cpu-steps", type=int, default=24)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    if args.cpu_sample:
+        print(json.dumps(cpu_sample(args.cpu_sample)))
+        return
+
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        n = max(4, min(args.steps, 96))
+        s = cpu_sample_subprocess(n + args.warmup)
+        res = {"metric": METRIC, "value": s["value"], "unit": "tok/s", "n_gpus": args.gpus, "steps": args.steps,
+               "warmup": args.warmup, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+               "dtype": "f64", "data": "synthetic", "impl": "reference",
+               "config": {"workload": "qwen3.5-4b-shape 32-layer decode stack, batch 1, KV prefilled to 8192"},
+               "cpu_baseline": s,
+               "e2e": {"value": s["value"], "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(res))
+        return
+
+    res = run_gpu(args)
+    if res is None:
+        return
+    res["cpu_baseline"] = cpu_sample_subprocess(args.cpu_steps) if args.cpu_steps > 0 else None
+    print(json.dumps(res))
+
+
+if __name__ == "__main__":
+    main()

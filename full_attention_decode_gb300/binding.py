@@ -1,0 +1,347 @@
+"""Python binding of the C ABI in include/qwen35_decode.h.
+
+Argument marshalling only: the ctypes structs mirror the C structs, the
+functions carry the C names and forward torch tensors' device pointers and the
+current CUDA stream. Every step of the decode runs in the library's kernels.
+Loading fails loudly when the library has not been built (there is no fallback).
+
+Upload helpers turn the numpy weight dicts of `synth` into device tensors (torch
+owns the memory) and the matching C structs.
+"""
+
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libqwen35_decode.so")
+
+QWEN35_OK = 0
+QWEN35_ERR_INVALID_ARGUMENT = 1
+QWEN35_ERR_OUT_OF_RANGE = 2
+QWEN35_ERR_UNSUPPORTED = 3
+QWEN35_ERR_CUDA = 4
+QWEN35_ERR_DEVICE_TIMEOUT = 5
+QWEN35_ERR_DEVICE_RANGE = 6
+QWEN35_LAYER_FULL_ATTENTION = 0
+QWEN35_LAYER_LINEAR_ATTENTION = 1
+
+
+class Qwen35Error(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__(f"{fn} failed: {status} ({_status_string(status)})")
+
+
+class qwen35_config(C.Structure):
+    _fields_ = [("hidden", C.c_uint32), ("intermediate", C.c_uint32), ("num_layers", C.c_uint32),
+                ("vocab", C.c_uint32), ("group_size", C.c_uint32), ("rms_eps", C.c_float),
+                ("num_heads", C.c_uint32), ("num_kv_heads", C.c_uint32), ("head_dim", C.c_uint32),
+                ("rope_theta", C.c_float), ("rotary_dim", C.c_uint32),
+                ("num_k_heads_lin", C.c_uint32), ("num_v_heads_lin", C.c_uint32),
+                ("k_head_dim_lin", C.c_uint32), ("v_head_dim_lin", C.c_uint32),
+                ("conv_kernel_size", C.c_uint32)]
+
+
+class qwen35_qweight(C.Structure):
+    _fields_ = [("codes", C.c_void_p), ("scales", C.c_void_p), ("biases", C.c_void_p),
+                ("n", C.c_uint32), ("k", C.c_uint32)]
+
+
+class qwen35_fa_layer(C.Structure):
+    _fields_ = [("input_ln", C.c_void_p), ("q_norm", C.c_void_p), ("k_norm", C.c_void_p),
+                ("post_ln", C.c_void_p)] + \
+               [(n, qwen35_qweight) for n in ("q_proj", "k_proj", "v_proj", "o_proj", "gate_proj",
+                                              "up_proj", "down_proj")]
+
+
+class qwen35_gdn_layer(C.Structure):
+    _fields_ = [("input_ln", C.c_void_p), ("a_log", C.c_void_p), ("dt_bias", C.c_void_p),
+                ("conv1d_weight", C.c_void_p), ("in_proj_a", qwen35_qweight), ("in_proj_b", qwen35_qweight),
+                ("in_proj_qkv", qwen35_qweight), ("in_proj_z", qwen35_qweight), ("norm_weight", C.c_void_p),
+                ("out_proj", qwen35_qweight), ("post_ln", C.c_void_p), ("gate_proj", qwen35_qweight),
+                ("up_proj", qwen35_qweight), ("down_proj", qwen35_qweight)]
+
+
+class qwen35_kv_cache(C.Structure):
+    _fields_ = [("k", C.c_void_p), ("v", C.c_void_p), ("capacity", C.c_uint32)]
+
+
+class qwen35_gdn_state(C.Structure):
+    _fields_ = [("conv_state", C.c_void_p), ("gdn_state", C.c_void_p)]
+
+
+class qwen35_layer(C.Structure):
+    _fields_ = [("kind", C.c_int32), ("fa", C.POINTER(qwen35_fa_layer)), ("kv", C.POINTER(qwen35_kv_cache)),
+                ("gdn", C.POINTER(qwen35_gdn_layer)), ("state", C.POINTER(qwen35_gdn_state))]
+
+
+_P = C.c_void_p
+_U = C.c_uint32
+_SIGS = {
+    "qwen35_init": (C.c_int, []),
+    "qwen35_status_string": (C.c_char_p, [C.c_int]),
+    "qwen35_scratch_bytes": (C.c_size_t, [C.POINTER(qwen35_config), C.c_int]),
+    "qwen35_stack_scratch_bytes": (C.c_size_t, [C.POINTER(qwen35_config)]),
+    "qwen35_scratch_init": (C.c_int, [_P, C.c_size_t, _P]),
+    "qwen35_read_device_status": (C.c_int, [_P, C.POINTER(C.c_int32), _P]),
+    "qwen35_forward_full_attention": (C.c_int, [C.POINTER(qwen35_config), C.POINTER(qwen35_fa_layer), _P,
+                                                C.c_size_t, C.POINTER(qwen35_kv_cache), _P, _P, _U, _U, _P]),
+    "qwen35_forward_full_attention_dpos": (C.c_int, [C.POINTER(qwen35_config), C.POINTER(qwen35_fa_layer), _P,
+                                                     C.c_size_t, C.POINTER(qwen35_kv_cache), _P, _P, _P, _U, _P]),
+    "qwen35_forward_linear_attention": (C.c_int, [C.POINTER(qwen35_config), C.POINTER(qwen35_gdn_layer), _P,
+                                                  C.c_size_t, C.POINTER(qwen35_gdn_state), _P, _P, _P]),
+    "qwen35_decode_step": (C.c_int, [C.POINTER(qwen35_config), C.POINTER(qwen35_layer), _U, _P, C.c_size_t,
+                                     _P, _P, _P, _U, _P]),
+    "qwen35_graph_create": (C.c_int, [C.POINTER(qwen35_config), C.POINTER(qwen35_layer), _U, _P, C.c_size_t,
+                                      _P, _P, _P, _U, _P, C.POINTER(C.c_void_p)]),
+    "qwen35_graph_launch": (C.c_int, [_P, _P]),
+    "qwen35_graph_destroy": (C.c_int, [_P]),
+    "qwen35_gemv": (C.c_int, [C.POINTER(qwen35_qweight), _P, _P, _P, C.c_size_t, _P]),
+    "qwen35_dequant": (C.c_int, [C.POINTER(qwen35_qweight), _P, _P]),
+    "qwen35_debug_scratch_offset": (C.c_size_t, [C.POINTER(qwen35_config), C.c_int, C.c_char_p]),
+}
+
+_lib = None
+
+
+def lib():
+    """The loaded library, with prototypes declared. Raises if it is not built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"CUDA library not built: {LIB_PATH} is missing (run __graft_entry__.build())")
+        L = C.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def exported_symbols():
+    return list(_SIGS)
+
+
+def _status_string(s):
+    try:
+        return lib().qwen35_status_string(s).decode()
+    except Exception:
+        return "?"
+
+
+def _check(fn, status):
+    if status != QWEN35_OK:
+        raise Qwen35Error(fn, status)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+# ------------------------------------------------------------------ C calls
+
+
+def qwen35_init():
+    _check("qwen35_init", lib().qwen35_init())
+
+
+def make_config(cfg: dict) -> qwen35_config:
+    return qwen35_config(**{f: cfg[f] for f, _ in qwen35_config._fields_})
+
+
+def qwen35_scratch_bytes(cfg: qwen35_config, kind: int) -> int:
+    return lib().qwen35_scratch_bytes(C.byref(cfg), kind)
+
+
+def qwen35_stack_scratch_bytes(cfg: qwen35_config) -> int:
+    return lib().qwen35_stack_scratch_bytes(C.byref(cfg))
+
+
+def qwen35_scratch_init(scratch, stream=None):
+    _check("qwen35_scratch_init", lib().qwen35_scratch_init(_ptr(scratch), scratch.numel(), _stream(stream)))
+
+
+def qwen35_read_device_status(scratch, stream=None) -> int:
+    out = C.c_int32(0)
+    _check("qwen35_read_device_status", lib().qwen35_read_device_status(_ptr(scratch), C.byref(out),
+                                                                          _stream(stream)))
+    return out.value
+
+
+def qwen35_forward_full_attention(cfg, layer, scratch, kv, x_in, x_out, cache_pos, seq_len_attn, stream=None):
+    return lib().qwen35_forward_full_attention(C.byref(cfg), C.byref(layer), _ptr(scratch), scratch.numel(),
+                                               C.byref(kv), _ptr(x_in), _ptr(x_out), cache_pos, seq_len_attn,
+                                               _stream(stream))
+
+
+def qwen35_forward_full_attention_dpos(cfg, layer, scratch, kv, x_in, x_out, d_cache_pos, max_seq_len,
+                                       stream=None):
+    return lib().qwen35_forward_full_attention_dpos(C.byref(cfg), C.byref(layer), _ptr(scratch),
+                                                    scratch.numel(), C.byref(kv), _ptr(x_in), _ptr(x_out),
+                                                    _ptr(d_cache_pos), max_seq_len, _stream(stream))
+
+
+def qwen35_forward_linear_attention(cfg, layer, scratch, state, x_in, x_out, stream=None):
+    return lib().qwen35_forward_linear_attention(C.byref(cfg), C.byref(layer), _ptr(scratch), scratch.numel(),
+                                                 C.byref(state), _ptr(x_in), _ptr(x_out), _stream(stream))
+
+
+def qwen35_decode_step(cfg, layers, scratch, x_in, x_out, d_cache_pos, max_seq_len, stream=None):
+    arr = (qwen35_layer * len(layers))(*layers)
+    return lib().qwen35_decode_step(C.byref(cfg), arr, len(layers), _ptr(scratch), scratch.numel(), _ptr(x_in),
+                                    _ptr(x_out), _ptr(d_cache_pos), max_seq_len, _stream(stream))
+
+
+class Graph:
+    """A captured decode step (qwen35_graph_create); replay with launch()."""
+
+    def __init__(self, cfg, layers, scratch, x_in, x_out, d_cache_pos, max_seq_len, stream=None):
+        arr = (qwen35_layer * len(layers))(*layers)
+        h = C.c_void_p(0)
+        _check("qwen35_graph_create",
+               lib().qwen35_graph_create(C.byref(cfg), arr, len(layers), _ptr(scratch), scratch.numel(),
+                                         _ptr(x_in), _ptr(x_out), _ptr(d_cache_pos), max_seq_len,
+                                         _stream(stream), C.byref(h)))
+        self.handle = h
+
+    def launch(self, stream=None):
+        _check("qwen35_graph_launch", lib().qwen35_graph_launch(self.handle, _stream(stream)))
+
+    def close(self):
+        if self.handle:
+            lib().qwen35_graph_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def qwen35_gemv(w, x, y, scratch, stream=None):
+    return lib().qwen35_gemv(C.byref(w), _ptr(x), _ptr(y), _ptr(scratch), scratch.numel(), _stream(stream))
+
+
+def qwen35_debug_scratch_offset(cfg, kind, name: str) -> int:
+    return lib().qwen35_debug_scratch_offset(C.byref(cfg), kind, name.encode())
+
+
+def scratch_view(scratch: torch.Tensor, cfg, kind, name: str, n: int) -> torch.Tensor:
+    """The bf16 intermediate `name` (n elements) inside a layer's scratch, as int16 bits."""
+    off = qwen35_debug_scratch_offset(cfg, kind, name)
+    if off == C.c_size_t(-1).value:
+        raise KeyError(name)
+    return scratch[off:off + 2 * n].view(torch.int16)
+
+
+def qwen35_dequant(w, out, stream=None):
+    return lib().qwen35_dequant(C.byref(w), _ptr(out), _stream(stream))
+
+
+# ------------------------------------------------------------------ device uploads
+
+
+def to_device(a: np.ndarray, device="cuda") -> torch.Tensor:
+    """numpy array -> device tensor of the same bits (uint16 stays int16 storage)."""
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        t = torch.from_numpy(a.view(np.int16))
+    else:
+        t = torch.from_numpy(a)
+    return t.to(device)
+
+
+class DeviceQWeight:
+    def __init__(self, qw: dict, device="cuda"):
+        self.codes = to_device(qw["codes"], device)
+        self.scales = to_device(qw["scales"], device)
+        self.biases = to_device(qw["biases"], device)
+        self.n, self.k = qw["n"], qw["k"]
+
+    def c(self) -> qwen35_qweight:
+        return qwen35_qweight(self.codes.data_ptr(), self.scales.data_ptr(), self.biases.data_ptr(), self.n, self.k)
+
+
+_FA_VEC = ("input_ln", "q_norm", "k_norm", "post_ln")
+_FA_MAT = ("q_proj", "k_proj", "v_proj", "o_proj", "gate_proj", "up_proj", "down_proj")
+_GDN_VEC = ("input_ln", "a_log", "dt_bias", "conv1d_weight", "norm_weight", "post_ln")
+_GDN_MAT = ("in_proj_a", "in_proj_b", "in_proj_qkv", "in_proj_z", "out_proj", "gate_proj", "up_proj",
+            "down_proj")
+
+
+class DeviceFaLayer:
+    """Device copy of a full-attention layer's weights plus its C struct."""
+
+    def __init__(self, layer: dict, device="cuda"):
+        self.t = {n: to_device(layer[n], device) for n in _FA_VEC}
+        self.m = {n: DeviceQWeight(layer[n], device) for n in _FA_MAT}
+        self.struct = qwen35_fa_layer(*[self.t[n].data_ptr() for n in _FA_VEC],
+                                      *[self.m[n].c() for n in _FA_MAT])
+
+
+class DeviceGdnLayer:
+    """Device copy of a linear-attention layer's weights plus its C struct."""
+
+    def __init__(self, layer: dict, device="cuda"):
+        self.t = {n: to_device(layer[n], device) for n in _GDN_VEC}
+        self.m = {n: DeviceQWeight(layer[n], device) for n in _GDN_MAT}
+        t, m = self.t, self.m
+        self.struct = qwen35_gdn_layer(
+            t["input_ln"].data_ptr(), t["a_log"].data_ptr(), t["dt_bias"].data_ptr(), t["conv1d_weight"].data_ptr(),
+            m["in_proj_a"].c(), m["in_proj_b"].c(), m["in_proj_qkv"].c(), m["in_proj_z"].c(),
+            t["norm_weight"].data_ptr(), m["out_proj"].c(), t["post_ln"].data_ptr(), m["gate_proj"].c(),
+            m["up_proj"].c(), m["down_proj"].c())
+
+
+class DeviceKv:
+    def __init__(self, k: np.ndarray, v: np.ndarray, device="cuda"):
+        self.k = to_device(k, device)
+        self.v = to_device(v, device)
+        self.struct = qwen35_kv_cache(self.k.data_ptr(), self.v.data_ptr(), k.shape[0])
+
+
+class DeviceState:
+    def __init__(self, conv: np.ndarray, ssm: np.ndarray, device="cuda"):
+        self.conv = to_device(conv, device)
+        self.ssm = to_device(ssm, device)
+        self.struct = qwen35_gdn_state(self.conv.data_ptr(), self.ssm.data_ptr())
+
+
+def stack_layer(kind: str, dev_layer, cache) -> qwen35_layer:
+    """A qwen35_layer entry; the caller keeps dev_layer and cache alive."""
+    if kind == "fa":
+        return qwen35_layer(QWEN35_LAYER_FULL_ATTENTION, C.pointer(dev_layer.struct), C.pointer(cache.struct),
+                            None, None)
+    return qwen35_layer(QWEN35_LAYER_LINEAR_ATTENTION, None, None, C.pointer(dev_layer.struct),
+                        C.pointer(cache.struct))
+
+
+def new_scratch(nbytes: int, device="cuda", stream=None) -> torch.Tensor:
+    """A scratch buffer (uint8, 256-byte aligned by the allocator) with its status word zeroed."""
+    s = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    qwen35_scratch_init(s, stream)
+    return s
+
+
+def bf16_tensor_bits(t: torch.Tensor) -> np.ndarray:
+    """Device int16/bf16 tensor -> numpy uint16 bit patterns."""
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)

@@ -1,0 +1,255 @@
+/*
+ * qwen35_decode.h — C ABI of the GB300 (sm_103a) single-token decode library for
+ * Qwen3.5 decoder layers: the gated full-attention layer and the Gated DeltaNet
+ * (linear-attention) layer.
+ *
+ * The calls follow the problem statement of the pages "full_attention.rs"
+ * (forward_full_attention: config, layer weights, scratch, KV cache, x_in,
+ * cache_pos, seq_len_attn, stream) and "linear_attention.rs"
+ * (forward_linear_attention: config, layer weights, persistent conv/SSM state,
+ * scratch, x_in, stream), with the structs of "mod.rs".
+ *
+ * Conventions for every call:
+ *  - All tensor pointers are DEVICE pointers unless a comment says otherwise, and
+ *    must be 16-byte aligned. bf16 values travel as uint16_t bit patterns.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream). Calls only enqueue
+ *    work: they never synchronise, except qwen35_read_device_status.
+ *  - The caller owns and allocates everything (weights, caches, states, scratch);
+ *    the library allocates nothing on the forward path and keeps no pointer after
+ *    a call returns (a captured graph keeps them: see qwen35_graph_create).
+ *  - Return value: QWEN35_OK or an error code. Argument errors are reported
+ *    before anything is enqueued. Errors of asynchronous device work surface at the
+ *    caller's next synchronisation (CUDA error) or in the device status word.
+ *  - Device status word: the first 4 bytes of every scratch buffer hold an int32
+ *    status that kernels set (never clear) when a bounded wait gives up
+ *    (QWEN35_ERR_DEVICE_TIMEOUT) or a device-resident position is out of range
+ *    (QWEN35_ERR_DEVICE_RANGE; that kernel then skips its work). The caller zeroes
+ *    it when the scratch is created (qwen35_scratch_init) and may read it with
+ *    qwen35_read_device_status.
+ */
+#ifndef QWEN35_DECODE_H
+#define QWEN35_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define QWEN35_API __attribute__((visibility("default")))
+#else
+#define QWEN35_API
+#endif
+
+typedef uint16_t qwen35_bf16;
+
+enum qwen35_status {
+    QWEN35_OK = 0,
+    QWEN35_ERR_INVALID_ARGUMENT = 1, /* null/misaligned pointer, bad dims, scratch too small */
+    QWEN35_ERR_OUT_OF_RANGE = 2,     /* cache_pos >= capacity, seq_len_attn not in [1, cache_pos+1] */
+    QWEN35_ERR_UNSUPPORTED = 3,      /* dims beyond the compiled kernels' limits */
+    QWEN35_ERR_CUDA = 4,             /* a CUDA runtime call or launch failed */
+    QWEN35_ERR_DEVICE_TIMEOUT = 5,   /* device status only: a bounded wait gave up */
+    QWEN35_ERR_DEVICE_RANGE = 6      /* device status only: device position out of range */
+};
+
+enum qwen35_layer_kind {
+    QWEN35_LAYER_FULL_ATTENTION = 0,
+    QWEN35_LAYER_LINEAR_ATTENTION = 1
+};
+
+/* Dimensions of a checkpoint: the Qwen35ForwardConfig struct of "mod.rs" (its 4B
+ * preset is qwen3_5_4b_mlx_int8). vocab is carried but unused (no embedding or
+ * lm_head here). group_size must be 64. */
+typedef struct qwen35_config {
+    uint32_t hidden, intermediate, num_layers, vocab, group_size;
+    float rms_eps;
+    uint32_t num_heads, num_kv_heads, head_dim;
+    float rope_theta;
+    uint32_t rotary_dim;
+    uint32_t num_k_heads_lin, num_v_heads_lin, k_head_dim_lin, v_head_dim_lin;
+    uint32_t conv_kernel_size;
+} qwen35_config;
+
+/* An int8 group-64 affine matrix W [n][k] (the QuantWeights type the pages use;
+ * its format is not printed there, this is the MLX-8bit layout):
+ *   codes  uint8 [n][k] row-major;
+ *   scales bf16  [n][gstride], biases bf16 [n][gstride], gstride = round_up(k/64, 8)
+ *   (the padding keeps every row 16-byte aligned; padded entries are never read);
+ *   W[r][c] = scales[r][c/64] * codes[r][c] + biases[r][c/64].
+ * k must be a multiple of 64 and at most 12288. Borrowed, never written. */
+typedef struct qwen35_qweight {
+    const uint8_t* codes;
+    const qwen35_bf16* scales;
+    const qwen35_bf16* biases;
+    uint32_t n, k;
+} qwen35_qweight;
+
+/* Full-attention layer weights (FullAttentionLayer, "mod.rs"). Norm vectors are
+ * bf16: input_ln/post_ln [hidden], q_norm/k_norm [head_dim]. q_proj is
+ * [2*num_heads*head_dim][hidden] with each head's rows ordered [Q_h | gate_h];
+ * k_proj, v_proj [num_kv_heads*head_dim][hidden]; o_proj [hidden][num_heads*head_dim];
+ * gate_proj, up_proj [intermediate][hidden]; down_proj [hidden][intermediate]. */
+typedef struct qwen35_fa_layer {
+    const qwen35_bf16 *input_ln, *q_norm, *k_norm, *post_ln;
+    qwen35_qweight q_proj, k_proj, v_proj, o_proj, gate_proj, up_proj, down_proj;
+} qwen35_fa_layer;
+
+/* Linear-attention layer weights (LinearAttentionLayer, "mod.rs"): a_log fp32
+ * [Hv]; dt_bias bf16 [Hv]; conv1d_weight bf16 [C][conv_kernel_size] with
+ * C = 2*Hk*Dk + Hv*Dv; norm_weight bf16 [Dv]; in_proj_a/b [Hv][hidden];
+ * in_proj_qkv [C][hidden] with channels ordered [Q | K | V]; in_proj_z
+ * [Hv*Dv][hidden]; out_proj [hidden][Hv*Dv]; MLP as in the full-attention layer. */
+typedef struct qwen35_gdn_layer {
+    const qwen35_bf16* input_ln;
+    const float* a_log;
+    const qwen35_bf16 *dt_bias, *conv1d_weight;
+    qwen35_qweight in_proj_a, in_proj_b, in_proj_qkv, in_proj_z;
+    const qwen35_bf16* norm_weight;
+    qwen35_qweight out_proj;
+    const qwen35_bf16* post_ln;
+    qwen35_qweight gate_proj, up_proj, down_proj;
+} qwen35_gdn_layer;
+
+/* bf16 KV cache of one full-attention layer and one sequence (LayerKvCache with
+ * the Bf16 format, "mod.rs"): k and v are [capacity][num_kv_heads][head_dim]. A
+ * forward writes exactly row cache_pos of each and reads rows [0, seq_len_attn). */
+typedef struct qwen35_kv_cache {
+    qwen35_bf16* k;
+    qwen35_bf16* v;
+    uint32_t capacity;
+} qwen35_kv_cache;
+
+/* Persistent state of one linear-attention layer (LinearAttentionState,
+ * "mod.rs"): conv_state fp32 [C][conv_kernel_size] (newest input in the last
+ * slot), gdn_state fp32 [Hv][Dk][Dv]. Caller-allocated and zeroed before the
+ * first token; updated in place by every forward. */
+typedef struct qwen35_gdn_state {
+    float* conv_state;
+    float* gdn_state;
+} qwen35_gdn_state;
+
+/* One layer of a decode stack: kind selects fa+kv or gdn+state. */
+typedef struct qwen35_layer {
+    int32_t kind;
+    const qwen35_fa_layer* fa;
+    const qwen35_kv_cache* kv;
+    const qwen35_gdn_layer* gdn;
+    const qwen35_gdn_state* state;
+} qwen35_layer;
+
+/* Once per process and device, before any forward: queries the device and sets
+ * kernel attributes (the counterpart of Qwen35Kernels::resolve in "mod.rs",
+ * which looks every kernel up once at startup). Returns QWEN35_ERR_CUDA without a
+ * usable sm_103 device. */
+QWEN35_API int qwen35_init(void);
+
+/* Static description of a status code (never NULL). */
+QWEN35_API const char* qwen35_status_string(int status);
+
+/* Bytes of scratch a forward of `layer_kind` needs (the FullAttentionScratch /
+ * LinearAttentionScratch buffers of "mod.rs", plus the device status word and the
+ * split-KV attention partials). qwen35_stack_scratch_bytes covers every layer of a
+ * stack. 0 for an invalid config. */
+QWEN35_API size_t qwen35_scratch_bytes(const qwen35_config* cfg, int layer_kind);
+QWEN35_API size_t qwen35_stack_scratch_bytes(const qwen35_config* cfg);
+
+/* Zero the device status word and the internal counters of a scratch buffer
+ * (enqueued on `stream`). Call once after allocating scratch. */
+QWEN35_API int qwen35_scratch_init(void* scratch, size_t scratch_bytes, void* stream);
+
+/* Synchronise `stream`, then copy the device status word of `scratch` into
+ * *host_status (host pointer). */
+QWEN35_API int qwen35_read_device_status(const void* scratch, int32_t* host_status, void* stream);
+
+/* Single-token full-attention decoder forward ("full_attention.rs",
+ * forward_full_attention): input RMSNorm, q_proj with its [Q_h | gate_h] split,
+ * k/v projections, per-head q/k RMSNorm, RoPE on the first rotary_dim dims at
+ * position cache_pos, KV append at row cache_pos, GQA attention over tokens
+ * [0, seq_len_attn), sigmoid(gate) gating, o_proj, residual + post RMSNorm, and the
+ * SiLU-gated MLP with its residual. x_in, x_out: bf16 [hidden]; x_out may equal
+ * x_in (no other aliasing). Errors: INVALID_ARGUMENT, OUT_OF_RANGE
+ * (cache_pos >= kv->capacity, seq_len_attn == 0 or > cache_pos + 1), UNSUPPORTED
+ * (head_dim not 64/128/256, rotary_dim odd or > head_dim, num_kv_heads > 8), CUDA. */
+QWEN35_API int qwen35_forward_full_attention(const qwen35_config* cfg, const qwen35_fa_layer* layer,
+                                  void* scratch, size_t scratch_bytes,
+                                  const qwen35_kv_cache* kv,
+                                  const qwen35_bf16* x_in, qwen35_bf16* x_out,
+                                  uint32_t cache_pos, uint32_t seq_len_attn, void* stream);
+
+/* The same forward with the position in device memory, for graph capture:
+ * cache_pos = *d_cache_pos, seq_len_attn = cache_pos + 1, read by the kernels when
+ * they run. The split-KV work partition is sized for max_seq_len tokens at
+ * enqueue time. A device position outside [0, min(capacity, max_seq_len)) sets
+ * QWEN35_ERR_DEVICE_RANGE in the status word and the layer's attention is skipped. */
+QWEN35_API int qwen35_forward_full_attention_dpos(const qwen35_config* cfg, const qwen35_fa_layer* layer,
+                                       void* scratch, size_t scratch_bytes,
+                                       const qwen35_kv_cache* kv,
+                                       const qwen35_bf16* x_in, qwen35_bf16* x_out,
+                                       const int32_t* d_cache_pos, uint32_t max_seq_len,
+                                       void* stream);
+
+/* Single-token Gated DeltaNet decoder forward ("linear_attention.rs",
+ * forward_linear_attention): input RMSNorm, in_proj_a/b/qkv/z, causal conv1d
+ * update + SiLU with per-head L2 norm on the Q/K channels, gate =
+ * exp(softplus(dt + dt_bias) * -exp(A_log)), beta = sigmoid(b), the gated
+ * delta-rule state update and readout scaled by 1/sqrt(k_head_dim_lin), the
+ * per-head RMSNorm gated by silu(z), out_proj, residual + post RMSNorm and the MLP.
+ * The page copies x_final into a separate x_buf; here the last kernel writes x_out
+ * directly, and x_out may equal x_in. Errors: INVALID_ARGUMENT, UNSUPPORTED
+ * (k/v head dims not 32/64/128, num_v_heads_lin % num_k_heads_lin != 0), CUDA. */
+QWEN35_API int qwen35_forward_linear_attention(const qwen35_config* cfg, const qwen35_gdn_layer* layer,
+                                    void* scratch, size_t scratch_bytes,
+                                    const qwen35_gdn_state* state,
+                                    const qwen35_bf16* x_in, qwen35_bf16* x_out, void* stream);
+
+/* One decode step of a layer stack: layer i's output is layer i+1's input (the
+ * caller's layer loop, which the module page leaves to the caller). Full-attention
+ * layers use the device position *d_cache_pos (as in the _dpos forward); after
+ * the last layer a final kernel advances *d_cache_pos by one, so the same enqueued
+ * sequence (or a graph of it) decodes consecutive tokens. x_in [hidden] is read by
+ * layer 0; x_out [hidden] receives every layer's output in turn (it may equal
+ * x_in). Scratch: qwen35_stack_scratch_bytes. */
+QWEN35_API int qwen35_decode_step(const qwen35_config* cfg, const qwen35_layer* layers, uint32_t num_layers,
+                       void* scratch, size_t scratch_bytes,
+                       const qwen35_bf16* x_in, qwen35_bf16* x_out,
+                       int32_t* d_cache_pos, uint32_t max_seq_len, void* stream);
+
+/* A CUDA graph of one qwen35_decode_step, captured on `stream` (which must not be
+ * capturing already). The graph keeps every pointer given here: the buffers must
+ * outlive it. Replaying it decodes one token and advances *d_cache_pos. */
+typedef struct qwen35_graph qwen35_graph;
+QWEN35_API int qwen35_graph_create(const qwen35_config* cfg, const qwen35_layer* layers, uint32_t num_layers,
+                        void* scratch, size_t scratch_bytes,
+                        const qwen35_bf16* x_in, qwen35_bf16* x_out,
+                        int32_t* d_cache_pos, uint32_t max_seq_len, void* stream,
+                        qwen35_graph** out_graph);
+QWEN35_API int qwen35_graph_launch(qwen35_graph* graph, void* stream);
+QWEN35_API int qwen35_graph_destroy(qwen35_graph* graph);
+
+/* The quantised GEMV on its own (QuantWeights::gemv): y[n] = bf16(W x), x bf16 [k]. */
+QWEN35_API int qwen35_gemv(const qwen35_qweight* w, const qwen35_bf16* x, qwen35_bf16* y, void* scratch,
+                size_t scratch_bytes, void* stream);
+
+/* Byte offset inside a layer's scratch of a named intermediate the last forward of
+ * that kind left there, or (size_t)-1 for an unknown name: the counterpart of the
+ * intra_dump hook of "linear_attention.rs" (named buffers readable after a stream
+ * synchronise). bf16 buffers, by kind:
+ *   full attention:   q_full [2*H*D], k, v [Hkv*D], gated_attn [H*D], o, x_resid [hidden],
+ *                     gate_act, up_act [intermediate]
+ *   linear attention: dt_raw, b_raw [Hv], qkv [C], z, y [Hv*Dv], out, x_resid [hidden],
+ *                     gate_act, up_act [intermediate]
+ * (x_norm, x_norm2 and qkv_smooth exist only inside the fused kernels.) */
+QWEN35_API size_t qwen35_debug_scratch_offset(const qwen35_config* cfg, int layer_kind, const char* name);
+
+/* Dequantised weights of `w`, fp32 [n][k], each element fmaf(scale, code, bias) rounded
+ * once: a check of the code/scale/bias indexing the GEMV uses. */
+QWEN35_API int qwen35_dequant(const qwen35_qweight* w, float* out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QWEN35_DECODE_H */

@@ -1,0 +1,160 @@
+"""The C-ABI library without a GPU: it loads, exports every declared symbol, its
+structs have the C layout, and argument errors are reported before any launch."""
+
+import ctypes as C
+import os
+import re
+import subprocess
+
+import pytest
+
+from full_attention_decode_gb300 import binding as B
+from full_attention_decode_gb300 import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qwen35_decode.h")
+
+
+def _declared():
+    txt = open(HEADER).read()
+    return sorted(set(re.findall(r"QWEN35_API\s+[\w\s\*]+?\b(qwen35_\w+)\s*\(", txt)))
+
+
+def test_library_exports_every_declared_symbol():
+    L = B.lib()
+    names = _declared()
+    assert len(names) >= 16
+    for n in names:
+        assert hasattr(L, n), n
+    out = subprocess.run(["nm", "-D", "--defined-only", B.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (qwen35_\w+)", out))
+    assert set(names) <= exported
+    # the binding declares a prototype for each of them
+    assert set(names) == set(B.exported_symbols())
+
+
+def test_struct_layout_matches_c_compiler(tmp_path):
+    src = tmp_path / "layout.c"
+    fields = {
+        "qwen35_config": [f for f, _ in B.qwen35_config._fields_],
+        "qwen35_qweight": [f for f, _ in B.qwen35_qweight._fields_],
+        "qwen35_fa_layer": [f for f, _ in B.qwen35_fa_layer._fields_],
+        "qwen35_gdn_layer": [f for f, _ in B.qwen35_gdn_layer._fields_],
+        "qwen35_kv_cache": [f for f, _ in B.qwen35_kv_cache._fields_],
+        "qwen35_gdn_state": [f for f, _ in B.qwen35_gdn_state._fields_],
+        "qwen35_layer": [f for f, _ in B.qwen35_layer._fields_],
+    }
+    lines = ['#include <stdio.h>', '#include <stddef.h>', f'#include "{HEADER}"', "int main(void) {"]
+    for s, fs in fields.items():
+        lines.append(f'printf("{s} %zu\\n", sizeof({s}));')
+        for f in fs:
+            lines.append(f'printf("{s}.{f} %zu\\n", offsetof({s}, {f}));')
+    lines.append("return 0; }")
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", str(src), "-o", str(exe)], check=True)
+    got = dict(l.split() for l in subprocess.run([str(exe)], capture_output=True, text=True).stdout.splitlines())
+    for s, fs in fields.items():
+        cls = getattr(B, s)
+        assert int(got[s]) == C.sizeof(cls), s
+        for f in fs:
+            assert int(got[f"{s}.{f}"]) == getattr(cls, f).offset, (s, f)
+
+
+def test_scratch_sizes():
+    c4 = B.make_config(synth.config("4b"))
+    fa = B.qwen35_scratch_bytes(c4, B.QWEN35_LAYER_FULL_ATTENTION)
+    gdn = B.qwen35_scratch_bytes(c4, B.QWEN35_LAYER_LINEAR_ATTENTION)
+    assert fa > 0 and gdn > 0
+    assert B.qwen35_stack_scratch_bytes(c4) == max(fa, gdn)
+    assert B.qwen35_scratch_bytes(c4, 7) == 0
+    bad = synth.config("4b")
+    bad["group_size"] = 32
+    assert B.qwen35_scratch_bytes(B.make_config(bad), 0) == 0
+    bad = synth.config("4b")
+    bad["head_dim"] = 96
+    assert B.qwen35_scratch_bytes(B.make_config(bad), 0) == 0
+    assert B.qwen35_scratch_bytes(B.make_config(bad), 1) > 0  # the GDN layer does not use head_dim
+
+
+def test_debug_offsets():
+    c = B.make_config(synth.config("tiny"))
+    none = C.c_size_t(-1).value
+    for n in ["q_full", "k", "v", "gated_attn", "o", "x_resid", "gate_act", "up_act"]:
+        assert B.qwen35_debug_scratch_offset(c, 0, n) != none, n
+    for n in ["dt_raw", "b_raw", "qkv", "z", "y", "out", "x_resid", "gate_act", "up_act"]:
+        assert B.qwen35_debug_scratch_offset(c, 1, n) != none, n
+    assert B.qwen35_debug_scratch_offset(c, 0, "qkv") == none
+    assert B.qwen35_debug_scratch_offset(c, 1, "nope") == none
+
+
+# ---- argument validation with fake (never dereferenced) aligned pointers
+
+_FAKE = 0x10000
+
+
+def _fake_qw(n, k, base):
+    return B.qwen35_qweight(base, base + 0x1000000, base + 0x2000000, n, k)
+
+
+def _fake_fa(cfg):
+    E, I, H, Hkv, D = cfg["hidden"], cfg["intermediate"], cfg["num_heads"], cfg["num_kv_heads"], cfg["head_dim"]
+    shapes = [(2 * H * D, E), (Hkv * D, E), (Hkv * D, E), (E, H * D), (I, E), (I, E), (E, I)]
+    qws = [_fake_qw(n, k, _FAKE * (i + 10) * 0x100) for i, (n, k) in enumerate(shapes)]
+    return B.qwen35_fa_layer(_FAKE, _FAKE * 2, _FAKE * 3, _FAKE * 4, *qws)
+
+
+class _FakeScratch:
+    def __init__(self, n):
+        self.n = n
+
+    def numel(self):
+        return self.n
+
+    def data_ptr(self):
+        return 0x7000000
+
+
+def test_full_attention_argument_errors_precede_launch():
+    cfg = synth.config("tiny")
+    c = B.make_config(cfg)
+    lay = _fake_fa(cfg)
+    kv = B.qwen35_kv_cache(0x5000000, 0x6000000, 16)
+    sb = B.qwen35_scratch_bytes(c, 0)
+    S = _FakeScratch(sb)
+    x, y = 0x8000000, 0x9000000
+    f = B.qwen35_forward_full_attention
+    assert f(c, lay, S, kv, x, y, 16, 17, 0) == B.QWEN35_ERR_OUT_OF_RANGE  # cache_pos >= capacity
+    assert f(c, lay, S, kv, x, y, 3, 0, 0) == B.QWEN35_ERR_OUT_OF_RANGE    # empty attention
+    assert f(c, lay, S, kv, x, y, 3, 5, 0) == B.QWEN35_ERR_OUT_OF_RANGE    # beyond cache_pos + 1
+    assert f(c, lay, _FakeScratch(sb - 1), kv, x, y, 3, 4, 0) == B.QWEN35_ERR_INVALID_ARGUMENT
+    assert f(c, lay, S, kv, x + 2, y, 3, 4, 0) == B.QWEN35_ERR_INVALID_ARGUMENT  # misaligned
+    bad = _fake_fa(cfg)
+    bad.down_proj.k = 256
+    assert f(c, bad, S, kv, x, y, 3, 4, 0) == B.QWEN35_ERR_INVALID_ARGUMENT  # wrong shape
+    bad = _fake_fa(cfg)
+    bad.q_norm = None
+    assert f(c, bad, S, kv, x, y, 3, 4, 0) == B.QWEN35_ERR_INVALID_ARGUMENT
+    cb = synth.config("tiny")
+    cb["rotary_dim"] = 15
+    assert f(B.make_config(cb), lay, S, kv, x, y, 3, 4, 0) == B.QWEN35_ERR_INVALID_ARGUMENT
+    cb = synth.config("tiny")
+    cb["num_kv_heads"] = 3
+    assert f(B.make_config(cb), lay, S, kv, x, y, 3, 4, 0) == B.QWEN35_ERR_INVALID_ARGUMENT
+
+
+def test_linear_attention_and_stack_argument_errors():
+    cfg = synth.config("tiny")
+    c = B.make_config(cfg)
+    g = B.qwen35_gdn_layer()
+    st = B.qwen35_gdn_state(0x5000000, 0x6000000)
+    S = _FakeScratch(B.qwen35_scratch_bytes(c, 1))
+    assert B.qwen35_forward_linear_attention(c, g, S, st, 0x8000000, 0x9000000, 0) == B.QWEN35_ERR_INVALID_ARGUMENT
+    cb = synth.config("tiny")
+    cb["k_head_dim_lin"] = 48
+    assert B.qwen35_forward_linear_attention(B.make_config(cb), g, S, st, 0x8000000, 0x9000000, 0) == \
+        B.QWEN35_ERR_UNSUPPORTED
+    bad_layer = B.qwen35_layer(9, None, None, None, None)
+    assert B.qwen35_decode_step(c, [bad_layer], S, 0x8000000, 0x9000000, 0x100, 16, 0) == \
+        B.QWEN35_ERR_INVALID_ARGUMENT
+    assert B.lib().qwen35_status_string(2) == b"position out of range"

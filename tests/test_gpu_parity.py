@@ -1,0 +1,228 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Tolerances: bit-exact for dequantised weights, KV-append positions and the
+[Q_h | gate_h] split; relative L2 <= 1e-2 on every layer output (bf16
+activations) and <= 2e-3 on the fp32 Gated DeltaNet state after 64 steps.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from full_attention_decode_gb300 import binding as B
+from full_attention_decode_gb300 import synth
+from oracle import qwen35_oracle as O
+
+from harness import FaRunner, GdnRunner, bf16_ulps, bits, f32, f64, init, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+TOL_X = 1e-2
+TOL_STATE = 2e-3
+
+
+# ------------------------------------------------------------------ GEMV
+
+
+@pytest.mark.parametrize("n,k", [(300, 2560), (77, 4096), (50, 9216), (8, 256), (3, 128), (37, 192),
+                                 (1, 12288), (1031, 320)])
+def test_dequant_bit_exact(n, k):
+    init()
+    qw = synth.qweight(11, ("dq", n, k), n, k)
+    if k == 192:  # a general affine bias, not tied to the scale
+        qw["biases"][:, :3] = synth.to_bf16_bits(np.random.default_rng(1).standard_normal((n, 3)) * 1e-2)
+    d = B.DeviceQWeight(qw)
+    out = torch.empty((n, k), dtype=torch.float32, device="cuda")
+    assert B.qwen35_dequant(d.c(), out) == 0
+    ref = O.dequant(qw).astype(np.float32)  # exact values, rounded once to fp32
+    np.testing.assert_array_equal(out.cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("n,k", [(300, 2560), (77, 4096), (50, 9216), (8, 256), (3, 128), (37, 192),
+                                 (5, 12288), (1031, 320), (18432, 2560)])
+def test_gemv_matches_oracle(n, k):
+    init()
+    qw = synth.qweight(5, ("gv", n, k), n, k)
+    x = synth.to_bf16_bits(np.random.default_rng(n + k).standard_normal(k))
+    d = B.DeviceQWeight(qw)
+    y = torch.empty(n, dtype=torch.int16, device="cuda")
+    scratch = B.new_scratch(4096)
+    assert B.qwen35_gemv(d.c(), B.to_device(x), y, scratch) == 0
+    got = f64(y)
+    ref = O.bf16_round(O.gemv(qw, O.bf16_to_f64(x)))
+    assert rel_l2(got, ref) <= 2e-3
+    assert bf16_ulps(got, ref).max() <= 2
+    assert B.qwen35_read_device_status(scratch) == 0
+
+
+# ------------------------------------------------------------------ layers, tiny
+
+
+def test_gdn_layer_tiny_16_steps():
+    r = GdnRunner("tiny")
+    for t in range(16):
+        tr = {}
+        got, ref = r.step(t, tr)
+        assert rel_l2(got, ref) <= TOL_X, t
+        assert rel_l2(r.view("qkv", len(tr["qkv"])), tr["qkv"]) <= TOL_X
+        assert rel_l2(r.view("y", len(tr["y"])), tr["y"]) <= TOL_X
+    assert rel_l2(f32(r.state.ssm), r.ostate["ssm"]) <= TOL_STATE
+    assert rel_l2(f32(r.state.conv), r.ostate["conv"]) <= TOL_STATE
+    assert B.qwen35_read_device_status(r.scratch) == 0
+
+
+def test_fa_layer_tiny_16_steps_and_append_rows():
+    cap = 20
+    r = FaRunner("tiny", cap, 0)
+    sentinel = torch.full_like(r.kv.k, 0x7F7F)  # a bf16 pattern no computed value takes
+    r.kv.k.copy_(sentinel)
+    r.kv.v.copy_(sentinel)
+    r.okv["k"][:] = O.bf16_to_f64(np.full(r.okv["k"].shape, 0x7F7F, np.uint16))
+    r.okv["v"][:] = r.okv["k"]
+    for t in range(16):
+        tr = {}
+        got, ref = r.step(t, t, trace=tr)
+        assert rel_l2(got, ref) <= TOL_X, t
+        # rows above the newest append are untouched, bit for bit
+        kb = bits(r.kv.k)
+        assert np.all(kb[t + 1:] == 0x7F7F)
+        assert not np.any(kb[t] == 0x7F7F)
+        np.testing.assert_array_less(bf16_ulps(O.bf16_to_f64(kb[t]), tr["k_rope"]), 3)
+        np.testing.assert_array_less(bf16_ulps(f64(r.kv.v)[t], tr["v"].reshape(kb[t].shape)), 3)
+    assert B.qwen35_read_device_status(r.scratch) == 0
+
+
+def test_fa_seq1_is_gated_v_and_split_is_exact():
+    # zero gate rows of q_proj: gate = 0, sigmoid = 1/2, so at one token the gated
+    # attention output is exactly v / 2 of the head's kv-head
+    cfg = synth.config("tiny")
+    r = FaRunner("tiny", 8, 0)
+    H, Hkv, D = cfg["num_heads"], cfg["num_kv_heads"], cfg["head_dim"]
+    codes = r.layer["q_proj"]["codes"]
+    for h in range(H):
+        codes[h * 2 * D + D:(h + 1) * 2 * D] = 128
+    r.dev = B.DeviceFaLayer(r.layer)
+    r.layer.pop("_deq_q_proj", None)
+    got, ref = r.step(0, 0)
+    assert rel_l2(got, ref) <= TOL_X
+    v = r.view("v", Hkv * D).reshape(Hkv, D)
+    ga = r.view("gated_attn", H * D).reshape(H, D)
+    for h in range(H):
+        np.testing.assert_array_equal(ga[h], v[h // (H // Hkv)] / 2)
+    qf = r.view("q_full", 2 * H * D).reshape(H, 2 * D)
+    assert not np.any(qf[:, D:])
+
+
+def test_fa_prefix_attention_and_last_row():
+    # seq_len_attn below cache_pos + 1 (the new row is appended but not attended),
+    # and an append at the last row of the cache
+    cap = 12
+    r = FaRunner("tiny", cap, 11)
+    got, ref = r.step(0, 11, seq_len=7)
+    assert rel_l2(got, ref) <= TOL_X
+    got, ref = r.step(1, cap - 1)
+    assert rel_l2(got, ref) <= TOL_X
+    assert rel_l2(f64(r.kv.k), r.okv["k"]) <= TOL_X
+
+
+def test_device_position_out_of_range_sets_status_and_skips():
+    r = FaRunner("tiny", 8, 4)
+    before = bits(r.kv.k).copy()
+    dpos = torch.full((1,), 8, dtype=torch.int32, device="cuda")  # == capacity
+    rc = B.qwen35_forward_full_attention_dpos(r.c, r.dev.struct, r.scratch, r.kv.struct, r.x_in, r.x_out, dpos, 8)
+    assert rc == 0
+    assert B.qwen35_read_device_status(r.scratch) == B.QWEN35_ERR_DEVICE_RANGE
+    np.testing.assert_array_equal(bits(r.kv.k), before)
+    B.qwen35_scratch_init(r.scratch)
+    dpos.fill_(-1)
+    rc = B.qwen35_forward_full_attention_dpos(r.c, r.dev.struct, r.scratch, r.kv.struct, r.x_in, r.x_out, dpos, 8)
+    assert rc == 0
+    assert B.qwen35_read_device_status(r.scratch) == B.QWEN35_ERR_DEVICE_RANGE
+    np.testing.assert_array_equal(bits(r.kv.k), before)
+
+
+def test_fa_device_position_matches_host_position():
+    r = FaRunner("tiny", 16, 0)
+    dpos = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for t in range(6):
+        got, ref = r.step(t, t, dpos=dpos)
+        assert rel_l2(got, ref) <= TOL_X, t
+    assert B.qwen35_read_device_status(r.scratch) == 0
+
+
+# ------------------------------------------------------------------ tiny stack (config 0)
+
+
+def _tiny_stack(seed=0):
+    cfg = synth.config("tiny")
+    kinds = synth.layer_kinds(cfg)
+    layers = [synth.gdn_layer(seed, 0, cfg), synth.fa_layer(seed, 1, cfg)]
+    conv, ssm = synth.gdn_state(seed, 0, cfg)
+    kb, vb = synth.kv_cache(seed, 1, cfg, 16, 0)
+    dev = [B.DeviceGdnLayer(layers[0]), B.DeviceFaLayer(layers[1])]
+    caches = [B.DeviceState(conv, ssm), B.DeviceKv(kb, vb)]
+    ocaches = [O.state_from_arrays(conv, ssm), O.kv_from_bits(kb, vb)]
+    return cfg, kinds, layers, dev, caches, ocaches
+
+
+@pytest.mark.parametrize("use_graph", [False, True])
+def test_tiny_stack_16_steps(use_graph):
+    init()
+    cfg, kinds, layers, dev, caches, ocaches = _tiny_stack()
+    c = B.make_config(cfg)
+    entries = [B.stack_layer(k, l, cc) for k, l, cc in zip(kinds, dev, caches)]
+    scratch = B.new_scratch(B.qwen35_stack_scratch_bytes(c))
+    x_in = torch.empty(cfg["hidden"], dtype=torch.int16, device="cuda")
+    x_out = torch.empty_like(x_in)
+    d_pos = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.Stream()
+    g = None
+    if use_graph:
+        with torch.cuda.stream(stream):
+            g = B.Graph(c, entries, scratch, x_in, x_out, d_pos, 16)
+    for t in range(16):
+        x = synth.x_in(0, t, cfg)
+        with torch.cuda.stream(stream):
+            x_in.copy_(B.to_device(x))
+            if g is not None:
+                g.launch()
+            else:
+                assert B.qwen35_decode_step(c, entries, scratch, x_in, x_out, d_pos, 16) == 0
+        ref = O.decode_step(cfg, kinds, layers, ocaches, O.bf16_to_f64(x), t)
+        stream.synchronize()
+        assert rel_l2(f64(x_out), ref) <= TOL_X, t
+    assert int(d_pos.item()) == 16
+    assert rel_l2(f32(caches[0].ssm), ocaches[0]["ssm"]) <= TOL_STATE
+    assert rel_l2(f64(caches[1].k), ocaches[1]["k"]) <= TOL_X
+    assert B.qwen35_read_device_status(scratch, stream) == 0
+    if g is not None:
+        g.close()
+
+
+# ------------------------------------------------------------------ 4B-shape layers (configs 1, 2)
+
+
+def test_gdn_layer_4b_64_steps():
+    r = GdnRunner("4b")
+    worst = 0.0
+    for t in range(64):
+        got, ref = r.step(t)
+        worst = max(worst, rel_l2(got, ref))
+        assert worst <= TOL_X, (t, worst)
+    err = rel_l2(f32(r.state.ssm), r.ostate["ssm"])
+    assert err <= TOL_STATE, err
+    assert rel_l2(f32(r.state.conv), r.ostate["conv"]) <= TOL_STATE
+    assert B.qwen35_read_device_status(r.scratch) == 0
+
+
+@pytest.mark.parametrize("cache_pos", [511, 4095, 16383])
+def test_fa_layer_4b(cache_pos):
+    r = FaRunner("4b", cache_pos + 8, cache_pos)
+    tr = {}
+    got, ref = r.step(0, cache_pos, trace=tr)
+    assert rel_l2(got, ref) <= TOL_X
+    kb = f64(r.kv.k)
+    assert rel_l2(kb[cache_pos], tr["k_rope"]) <= TOL_X
+    assert not np.any(bits(r.kv.k)[cache_pos + 1:])  # rows above the append stay zero
+    np.testing.assert_array_equal(bits(r.kv.k)[:cache_pos], O.bf16_bits(r.okv["k"][:cache_pos]))
+    assert B.qwen35_read_device_status(r.scratch) == 0
