@@ -363,9 +363,6 @@ int qwen35_init(void) {
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return QWEN35_ERR_CUDA;
   if (major != 10 || minor != 3) return QWEN35_ERR_CUDA;  // built for sm_103a only
-  const char* mode = std::getenv("QWEN35_GEMV_DOT");
-  if (mode && std::strcmp(mode, "fp32") == 0) g_gemv_mode = 0;
-  if (mode && std::strcmp(mode, "dp4a") == 0) g_gemv_mode = 1;
   if (gemv_set_attributes() != cudaSuccess || attn_set_attributes() != cudaSuccess) return QWEN35_ERR_CUDA;
   g_num_sms[dev] = sms;
   return QWEN35_OK;

@@ -22,6 +22,10 @@ __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w &
 
 __device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + expf(-x)); }
 __device__ __forceinline__ float siluf_(float x) { return x / (1.0f + expf(-x)); }
+// SiLU with the fast exponential and division intrinsics (relative error ~1e-6,
+// far below the bf16 rounding of every value it feeds); used where it runs per
+// element of a GEMV input.
+__device__ __forceinline__ float silu_fast(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -62,12 +66,14 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
                : "memory");
 }
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+// Test the phase; the thread may sleep in hardware until the phase completes or
+// about `hint_ns` pass, so waiting warps do not spin on the issue slots.
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity, uint32_t hint_ns = 1000000) {
   uint32_t ok;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
       : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
       : "memory");
   return ok != 0;
 }
@@ -105,6 +111,17 @@ __device__ __forceinline__ void bulk_g2s_stream(void* dst, const void* src, uint
       "%4;" ::"r"(smem_addr(dst)),
       "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
       : "memory");
+}
+// Pull [src, src + bytes) toward L2 without staging it anywhere (16-byte aligned,
+// bytes % 16 == 0); issued in pieces of at most 64 KiB.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint64_t bytes) {
+  const char* p = static_cast<const char*>(src);
+  while (bytes > 0) {
+    const uint32_t n = bytes > 65536 ? 65536u : (uint32_t)bytes;
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(n) : "memory");
+    p += n;
+    bytes -= n;
+  }
 }
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;

@@ -7,12 +7,20 @@
 // Each CTA owns a contiguous, balanced range of rows. A producer warp streams the
 // rows' codes, scales and biases through a ring of shared-memory stages with bulk
 // (TMA-engine) copies and mbarriers; the first stages are issued before the
-// kernel waits on its predecessor, since weights never depend on it. Eight
-// consumer warps each keep their slice of x in registers for the whole kernel and
-// reduce rows with the group identity
-//     sum_k (s_g c_k + b_g) x_k = s_g * sum_k c_k x_k + b_g * sum_k x_k,
-// so each weight costs one byte-to-float conversion and one FMA (or, in the
-// integer mode, a quarter of a dp4a on 16-bit fixed-point x).
+// kernel waits on its predecessor, since weights never depend on it.
+//
+// Eight consumer warps keep their slice of x in registers for the whole kernel,
+// as 16-bit fixed point per 16-element chunk (x ~= q * 2^(e-15), q = 256 hi + lo,
+// a power-of-two scale per chunk; exact for every element within 2^8 of its
+// chunk's largest, since bf16 carries 8 significant bits). A 16-code chunk then
+// costs eight dp4a, which give sum (c - 128) q exactly in int32, and the group
+// identity
+//     sum_k (s_g c_k + b_g) x_k = s_g * sum_k (c_k - 128) x_k + (b_g + 128 s_g) * sum_k x_k
+// applies the scale and bias once per chunk. The -128 offset keeps the two terms
+// from cancelling when b is close to -128 s (the usual affine 8-bit format).
+// Each warp accumulates four tiles' rows in registers and reduces them together
+// with one transposed warp reduction (6 shuffles per 4 rows).
+//
 // The prologue forms x from the preceding kernel's outputs (RMSNorm, residual
 // add + RMSNorm, SiLU gating, per-head RMSNorm with SiLU(z) gating) and the
 // epilogue optionally adds a residual, so the pages' separate rms_norm,
@@ -21,8 +29,6 @@
 #include "kernels.h"
 
 namespace q35 {
-
-int g_gemv_mode = 1;
 
 namespace {
 
@@ -52,74 +58,17 @@ __device__ __forceinline__ void unpack8(const uint4 u, float* x) {
   x[4] = bf16lo(u.z); x[5] = bf16hi(u.z);
   x[6] = bf16lo(u.w); x[7] = bf16hi(u.w);
 }
-
-// x values of the 16 inputs k0 .. k0+15 as the prologue defines them.
-template <int PRO>
-__device__ __forceinline__ void x_chunk(const GemvArgs& a, uint32_t k0, float inv, const float* hinv,
-                                        float* v) {
-  float xa[16];
-  unpack8(*reinterpret_cast<const uint4*>(a.a + k0), xa);
-  unpack8(*reinterpret_cast<const uint4*>(a.a + k0 + 8), xa + 8);
-  if constexpr (PRO == kProPlain) {
-#pragma unroll
-    for (int j = 0; j < 16; ++j) v[j] = xa[j];
-  } else if constexpr (PRO == kProRmsNorm) {
-    float w[16];
-    unpack8(*reinterpret_cast<const uint4*>(a.nw + k0), w);
-    unpack8(*reinterpret_cast<const uint4*>(a.nw + k0 + 8), w + 8);
-#pragma unroll
-    for (int j = 0; j < 16; ++j) v[j] = round_bf16(xa[j] * inv * w[j]);
-  } else if constexpr (PRO == kProAddRmsNorm) {
-    float xb[16], w[16];
-    unpack8(*reinterpret_cast<const uint4*>(a.b + k0), xb);
-    unpack8(*reinterpret_cast<const uint4*>(a.b + k0 + 8), xb + 8);
-    unpack8(*reinterpret_cast<const uint4*>(a.nw + k0), w);
-    unpack8(*reinterpret_cast<const uint4*>(a.nw + k0 + 8), w + 8);
-#pragma unroll
-    for (int j = 0; j < 16; ++j) v[j] = round_bf16(round_bf16(xa[j] + xb[j]) * inv * w[j]);
-  } else if constexpr (PRO == kProSiluMul) {
-    float xb[16];
-    unpack8(*reinterpret_cast<const uint4*>(a.b + k0), xb);
-    unpack8(*reinterpret_cast<const uint4*>(a.b + k0 + 8), xb + 8);
-#pragma unroll
-    for (int j = 0; j < 16; ++j) v[j] = siluf_(xa[j]) * xb[j];
-  } else {  // kProHeadNormSilu: a = y, b = z
-    float xb[16], w[16];
-    const uint32_t d0 = k0 % a.head_dim;
-    const float hi = hinv[k0 / a.head_dim];
-    unpack8(*reinterpret_cast<const uint4*>(a.b + k0), xb);
-    unpack8(*reinterpret_cast<const uint4*>(a.b + k0 + 8), xb + 8);
-    unpack8(*reinterpret_cast<const uint4*>(a.nw + d0), w);
-    unpack8(*reinterpret_cast<const uint4*>(a.nw + d0 + 8), w + 8);
-#pragma unroll
-    for (int j = 0; j < 16; ++j) v[j] = siluf_(xb[j]) * round_bf16(xa[j] * hi * w[j]);
-  }
+__device__ __forceinline__ void load16(const uint16_t* p, float* x) {
+  unpack8(*reinterpret_cast<const uint4*>(p), x);
+  unpack8(*reinterpret_cast<const uint4*>(p + 8), x + 8);
 }
 
-// ---- fp32 dot: a code byte becomes a float by placing it in the mantissa of
-// 2^23 and subtracting 2^23 (exact), then one FMA; four partial sums.
-__device__ __forceinline__ float code_f(uint32_t word, uint32_t sel) {
-  return __uint_as_float(__byte_perm(word, 0x4B000000u, sel)) - 8388608.0f;
-}
-__device__ __forceinline__ float dot16_f32(const uint4 w, const float* x) {
-  const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    a0 = fmaf(code_f(ws[j], 0x7650u), x[4 * j + 0], a0);
-    a1 = fmaf(code_f(ws[j], 0x7651u), x[4 * j + 1], a1);
-    a2 = fmaf(code_f(ws[j], 0x7652u), x[4 * j + 2], a2);
-    a3 = fmaf(code_f(ws[j], 0x7653u), x[4 * j + 3], a3);
-  }
-  return (a0 + a1) + (a2 + a3);
-}
-
-// ---- integer dot: x as 16-bit fixed point per chunk (x ~= q * 2^(e-15), q =
-// 256*hi + lo, hi signed byte, lo unsigned byte), sum c*q exact in int32 by dp4a.
 struct XQ {
   uint32_t hi[4], lo[4];
-  float scale;
+  int qsum128;  // 128 * sum q
+  float scale;  // 2^(e-15)
 };
+
 __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
   int d;
   asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
@@ -130,55 +79,81 @@ __device__ __forceinline__ uint32_t dp4a_uu(uint32_t a, uint32_t b, uint32_t c) 
   asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
   return d;
 }
+
 __device__ __forceinline__ void quantize16(const float* v, XQ& q) {
   float amax = 0.f;
 #pragma unroll
   for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(v[j]));
-  int e = 0;
-  if (amax > 0.f) frexpf(amax, &e);  // amax = m * 2^e, 0.5 <= m < 1
-  const float up = ldexpf(1.0f, 15 - e);
-  q.scale = amax > 0.f ? ldexpf(1.0f, e - 15) : 0.f;
+  // amax = m * 2^e with 0.5 <= m < 1, e = E - 126 for the biased exponent E; the
+  // scale is 2^(e-15). Chunks whose largest element is below 2^-112 count as zero.
+  const uint32_t E = __float_as_uint(amax) >> 23;
+  const bool nz = E >= 15;
+  const float up = __uint_as_float((268u - (nz ? E : 15u)) << 23);  // 2^(15-e)
+  q.scale = nz ? __uint_as_float((E - 14u) << 23) : 0.f;             // 2^(e-15)
+  int qs = 0;
 #pragma unroll
   for (int w = 0; w < 4; ++w) {
     uint32_t hi = 0, lo = 0;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      int t = amax > 0.f ? __float2int_rn(v[4 * w + j] * up) : 0;
+      int t = nz ? __float2int_rn(v[4 * w + j] * up) : 0;
       t = max(-32768, min(32767, t));
+      qs += t;
       hi |= (uint32_t)((t >> 8) & 0xFF) << (8 * j);
       lo |= (uint32_t)(t & 0xFF) << (8 * j);
     }
     q.hi[w] = hi;
     q.lo[w] = lo;
   }
+  q.qsum128 = 128 * qs;
 }
-__device__ __forceinline__ float dot16_dp4a(const uint4 w, const XQ& q) {
+
+// sum over the 16 codes of one chunk of (c - 128) * x, from dp4a on 16-bit x.
+__device__ __forceinline__ float dot16(const uint4 w, const XQ& q) {
   int ah = 0;
-  uint32_t al = 0;
+  uint32_t al = (uint32_t)(-q.qsum128);
   ah = dp4a_us(w.x, q.hi[0], ah);
-  ah = dp4a_us(w.y, q.hi[1], ah);
-  ah = dp4a_us(w.z, q.hi[2], ah);
-  ah = dp4a_us(w.w, q.hi[3], ah);
   al = dp4a_uu(w.x, q.lo[0], al);
+  ah = dp4a_us(w.y, q.hi[1], ah);
   al = dp4a_uu(w.y, q.lo[1], al);
+  ah = dp4a_us(w.z, q.hi[2], ah);
   al = dp4a_uu(w.z, q.lo[2], al);
+  ah = dp4a_us(w.w, q.hi[3], ah);
   al = dp4a_uu(w.w, q.lo[3], al);
   return (float)(ah * 256 + (int)al) * q.scale;
 }
 
-template <int PRO, int EPI, int MODE>
+// Sum over the 32 lanes of v[0..3]; lane L ends with the total of v[2*b4 + b3]
+// (b4, b3 = bits 4 and 3 of L).
+__device__ __forceinline__ float reduce4(const float* v, uint32_t lane) {
+  const bool b4 = lane & 16, b3 = lane & 8;
+  const float w0 = (b4 ? v[2] : v[0]) + __shfl_xor_sync(0xffffffffu, b4 ? v[0] : v[2], 16);
+  const float w1 = (b4 ? v[3] : v[1]) + __shfl_xor_sync(0xffffffffu, b4 ? v[1] : v[3], 16);
+  float z = (b3 ? w1 : w0) + __shfl_xor_sync(0xffffffffu, b3 ? w0 : w1, 8);
+  z += __shfl_xor_sync(0xffffffffu, z, 4);
+  z += __shfl_xor_sync(0xffffffffu, z, 2);
+  z += __shfl_xor_sync(0xffffffffu, z, 1);
+  return z;
+}
+
+template <typename T>
+__device__ __forceinline__ T sel4(const T* v, uint32_t j) {
+  return j == 0 ? v[0] : j == 1 ? v[1] : j == 2 ? v[2] : v[3];
+}
+
+template <int PRO, int EPI, int CPL>
 __global__ void __launch_bounds__(kGemvThreads, 2) gemv_q8g64_kernel(const __grid_constant__ GemvArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + a.bar_off);
   uint64_t* empty = full + a.nstage;
-  float* red = reinterpret_cast<float*>(empty + a.nstage);  // [2][8] cross-warp partials
-  float* pro = red + 16;                                    // [128] prologue statistics
+  float* red = reinterpret_cast<float*>(empty + a.nstage);  // [2][4 tiles][8 warps]
+  float* pro = red + 64;                                    // [8] prologue partial sums
 
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t G = gridDim.x, bid = blockIdx.x;
   const uint32_t rb = (uint32_t)(((uint64_t)a.total_rows * bid) / G);
   const uint32_t re = (uint32_t)(((uint64_t)a.total_rows * (bid + 1)) / G);
-  const uint32_t R = kGemvConsumerWarps / a.W;
+  const uint32_t W = a.W, R = kGemvConsumerWarps / W;
 
   if (threadIdx.x == 0) {
     for (uint32_t s = 0; s < a.nstage; ++s) {
@@ -192,6 +167,18 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_q8g64_kernel(const __gri
   if (warp == kGemvConsumerWarps) {
     // ------------------------------------------------ producer
     if (lane == 0) {
+      // Pull this CTA's whole weight range toward L2 first: under programmatic
+      // dependent launch this overlaps the predecessor, so HBM stays busy across
+      // the kernel boundary and the ring below refills from L2.
+      for (uint32_t sg = 0; sg < a.nseg; ++sg) {
+        const GemvSeg& s = a.seg[sg];
+        const uint32_t lo = max(rb, s.row0), hi = min(re, s.row0 + s.rows);
+        if (lo >= hi) continue;
+        const uint32_t l0 = lo - s.row0, n = hi - lo;
+        prefetch_l2(s.codes + (size_t)l0 * a.K, (uint64_t)n * a.K);
+        prefetch_l2(s.scales + (size_t)l0 * a.gstride, (uint64_t)n * a.gstride * 2);
+        prefetch_l2(s.biases + (size_t)l0 * a.gstride, (uint64_t)n * a.gstride * 2);
+      }
       const uint64_t pol = policy_evict_first();
       TileIter it{rb, re, R, 0};
       Tile t;
@@ -237,133 +224,177 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_q8g64_kernel(const __gri
   pdl_wait();
   pdl_launch();
 
+  const uint32_t kp = warp % W, rs = warp / W, nchunks = a.K / 16;
+  // chunk c of this lane: index lane + 32 (kp + W c); chunks past the row end are
+  // read at index 0 (valid memory) against x = 0, so every loop is branch-free.
+  uint32_t chk[CPL];
+  bool valid[CPL];
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) {
+    const uint32_t ch = lane + 32 * (kp + W * c);
+    valid[c] = ch < nchunks;
+    chk[c] = valid[c] ? ch : 0;
+  }
+
+  // ---- per-CTA statistics of the prologue
   float inv = 0.f;
   if constexpr (PRO == kProRmsNorm || PRO == kProAddRmsNorm) {
     float ss = 0.f;
-    for (uint32_t k = threadIdx.x * 8; k < a.K; k += kGemvConsumerWarps * 32 * 8) {
-      float x[8];
-      unpack8(*reinterpret_cast<const uint4*>(a.a + k), x);
-      if constexpr (PRO == kProAddRmsNorm) {
-        float xb[8];
-        unpack8(*reinterpret_cast<const uint4*>(a.b + k), xb);
-        uint32_t packed[4];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) x[j] = round_bf16(x[j] + xb[j]);
+    for (int c = 0; c < CPL; ++c) {
+      if (valid[c]) {
+        float xa[16];
+        load16(a.a + chk[c] * 16, xa);
+        if constexpr (PRO == kProAddRmsNorm) {
+          float xb[16];
+          load16(a.b + chk[c] * 16, xb);
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          packed[j] = (uint32_t)to_bf16(x[2 * j]) | ((uint32_t)to_bf16(x[2 * j + 1]) << 16);
-        if (bid == 0) *reinterpret_cast<uint4*>(a.resid_out + k) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-      }
+          for (int j = 0; j < 16; ++j) xa[j] = round_bf16(xa[j] + xb[j]);
+          if (bid == 0 && rs == 0) {  // the rows-0 warps of CTA 0 cover x once: store x_resid
+            uint32_t pk[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) ss = fmaf(x[j], x[j], ss);
-    }
-    ss = warp_sum(ss);
-    if (lane == 0) pro[warp] = ss;
-    named_barrier(1, kGemvConsumerWarps * 32);
-    float tot = 0.f;
-#pragma unroll
-    for (int w = 0; w < kGemvConsumerWarps; ++w) tot += pro[w];
-    inv = rsqrtf(tot / (float)a.K + a.eps);
-  }
-  if constexpr (PRO == kProHeadNormSilu) {
-    const uint32_t nh = a.K / a.head_dim;
-    for (uint32_t h = warp; h < nh; h += kGemvConsumerWarps) {
-      float ss = 0.f;
-      for (uint32_t d = lane; d < a.head_dim; d += 32) {
-        const float y = bf16f(a.a[h * a.head_dim + d]);
-        ss = fmaf(y, y, ss);
-      }
-      ss = warp_sum(ss);
-      if (lane == 0) pro[h] = rsqrtf(ss / (float)a.head_dim + a.eps);
-    }
-    named_barrier(1, kGemvConsumerWarps * 32);
-  }
-
-  // Each lane's chunks of x, kept in registers for every row of the kernel.
-  const uint32_t kp = warp % a.W, rs = warp / a.W, nchunks = a.K / 16, cpl = a.cpl;
-  constexpr int CPL = MODE == 0 ? kGemvCplMaxF32 : kGemvCplMax;
-  float xs[CPL];
-  float xr[MODE == 0 ? CPL : 1][16];
-  XQ xq[MODE == 1 ? CPL : 1];
-#pragma unroll
-  for (int c = 0; c < CPL; ++c) {
-    xs[c] = 0.f;
-    if (c < (int)cpl) {
-      const uint32_t ch = lane + 32 * (kp + a.W * c);
-      float v[16];
-      if (ch < nchunks) {
-        x_chunk<PRO>(a, ch * 16, inv, pro, v);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] = 0.f;
-      }
-#pragma unroll
-      for (int j = 0; j < 16; ++j) xs[c] += v[j];
-      if constexpr (MODE == 0) {
-#pragma unroll
-        for (int j = 0; j < 16; ++j) xr[c][j] = v[j];
-      } else {
-        quantize16(v, xq[c]);
-      }
-    }
-  }
-
-  TileIter it{rb, re, R, 0};
-  Tile t;
-  uint32_t i = 0;
-  bool dead = false;  // a wait gave up: keep joining the barriers, compute nothing
-  while (it.next(a, t)) {
-    const uint32_t st = i % a.nstage;
-    if (!dead && !mbar_wait(&full[st], (i / a.nstage) & 1)) {
-      set_status(a.status, kStatusTimeout);
-      dead = true;
-    }
-    const uint8_t* sbase = smem + st * a.stage_stride;
-    float acc = 0.f;
-    if (rs < t.nr && !dead) {
-      const uint8_t* crow = sbase + rs * a.K;
-      const uint16_t* srow = reinterpret_cast<const uint16_t*>(sbase + a.stage_scale_off) + rs * a.gstride;
-      const uint16_t* brow = reinterpret_cast<const uint16_t*>(sbase + a.stage_bias_off) + rs * a.gstride;
-#pragma unroll
-      for (int c = 0; c < CPL; ++c) {
-        if (c < (int)cpl) {
-          const uint32_t ch = lane + 32 * (kp + a.W * c);
-          if (ch < nchunks) {
-            const uint4 w = *reinterpret_cast<const uint4*>(crow + ch * 16);
-            const float s = bf16f(srow[ch >> 2]), b = bf16f(brow[ch >> 2]);
-            float d;
-            if constexpr (MODE == 0) d = dot16_f32(w, xr[c]);
-            else d = dot16_dp4a(w, xq[c]);
-            acc = fmaf(s, d, acc);
-            acc = fmaf(b, xs[c], acc);
+            for (int j = 0; j < 8; ++j)
+              pk[j] = (uint32_t)to_bf16(xa[2 * j]) | ((uint32_t)to_bf16(xa[2 * j + 1]) << 16);
+            uint4* dst = reinterpret_cast<uint4*>(a.resid_out + chk[c] * 16);
+            dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
           }
         }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) ss = fmaf(xa[j], xa[j], ss);
       }
-      acc = warp_sum(acc);
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[st]);  // this warp is done reading the stage
-
-    bool store = false;
-    if (a.W == 1) {
-      store = rs < t.nr && lane == 0;
-    } else {
-      if (lane == 0) red[(i & 1) * kGemvConsumerWarps + warp] = acc;
+    ss = warp_sum(ss);
+    if (W > 1) {  // the W warps of a row group hold disjoint parts of x
+      if (lane == 0) pro[warp] = ss;
       named_barrier(1, kGemvConsumerWarps * 32);
-      if (kp == 0 && lane == 0 && rs < t.nr) {
-        acc = 0.f;
-        for (uint32_t j = 0; j < a.W; ++j) acc += red[(i & 1) * kGemvConsumerWarps + rs * a.W + j];
+      ss = 0.f;
+      for (uint32_t w = 0; w < W; ++w) ss += pro[rs * W + w];
+    }
+    inv = rsqrtf(ss / (float)a.K + a.eps);
+  }
+
+  // ---- this lane's x chunks, quantised
+  XQ xq[CPL];
+  float xs[CPL];
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) {
+    float v[16];
+    const uint32_t k0 = chk[c] * 16;
+    float xa[16];
+    load16(a.a + k0, xa);
+    if constexpr (PRO == kProPlain) {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[j] = xa[j];
+    } else if constexpr (PRO == kProRmsNorm) {
+      float w[16];
+      load16(a.nw + k0, w);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[j] = round_bf16(xa[j] * inv * w[j]);
+    } else if constexpr (PRO == kProAddRmsNorm) {
+      float xb[16], w[16];
+      load16(a.b + k0, xb);
+      load16(a.nw + k0, w);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[j] = round_bf16(round_bf16(xa[j] + xb[j]) * inv * w[j]);
+    } else if constexpr (PRO == kProSiluMul) {
+      float xb[16];
+      load16(a.b + k0, xb);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[j] = silu_fast(xa[j]) * xb[j];
+    } else {  // kProHeadNormSilu: a = y, b = z; the head's chunks sit on adjacent lanes
+      float ss = 0.f;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) ss = fmaf(xa[j], xa[j], ss);
+      for (uint32_t o = 1; o < a.head_dim / 16; o <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      const float hi = rsqrtf(ss / (float)a.head_dim + a.eps);
+      float xb[16], w[16];
+      load16(a.b + k0, xb);
+      load16(a.nw + k0 % a.head_dim, w);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[j] = silu_fast(xb[j]) * round_bf16(xa[j] * hi * w[j]);
+    }
+    if (!valid[c]) {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[j] = 0.f;
+    }
+    xs[c] = 0.f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) xs[c] += v[j];
+    quantize16(v, xq[c]);
+  }
+
+  // ---- main loop: batches of four tiles, one row per warp per tile
+  TileIter it{rb, re, R, 0};
+  uint32_t i = 0, batch = 0;
+  bool dead = false;  // a wait gave up: keep joining the barriers, compute nothing
+  const uint32_t jl = ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1);  // tile whose total this lane ends with
+  while (true) {
+    float acc[4];
+    uint32_t trow[4], tcnt[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      acc[j] = 0.f;
+      trow[j] = 0;
+      tcnt[j] = 0;
+      Tile t;
+      if (it.next(a, t)) {
+        trow[j] = t.r;
+        tcnt[j] = t.nr;
+        const uint32_t st = i % a.nstage;
+        if (!dead && !mbar_wait(&full[st], (i / a.nstage) & 1)) {
+          set_status(a.status, kStatusTimeout);
+          dead = true;
+        }
+        if (!dead && rs < t.nr) {
+          const uint8_t* sbase = smem + st * a.stage_stride;
+          const uint8_t* crow = sbase + rs * a.K;
+          const uint16_t* srow = reinterpret_cast<const uint16_t*>(sbase + a.stage_scale_off) + rs * a.gstride;
+          const uint16_t* brow = reinterpret_cast<const uint16_t*>(sbase + a.stage_bias_off) + rs * a.gstride;
+          float part[CPL];
+#pragma unroll
+          for (int c = 0; c < CPL; ++c) {
+            const uint4 w = *reinterpret_cast<const uint4*>(crow + chk[c] * 16);
+            const float s = bf16f(srow[chk[c] >> 2]);
+            const float b = fmaf(128.0f, s, bf16f(brow[chk[c] >> 2]));
+            part[c] = fmaf(s, dot16(w, xq[c]), b * xs[c]);
+          }
+#pragma unroll
+          for (int c = 1; c < CPL; ++c) part[0] += part[c];
+          acc[j] = part[0];
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);  // this warp is done reading the stage
+        ++i;
+      }
+    }
+    if (tcnt[0] == 0) break;
+    const float tot = reduce4(acc, lane);
+    const uint32_t r0 = sel4(trow, jl), n0 = sel4(tcnt, jl);
+    bool store = false;
+    float y = tot;
+    if (W == 1) {
+      store = (lane & 7) == 0 && rs < n0;
+    } else {
+      float* buf = red + (batch & 1) * 32;
+      if ((lane & 7) == 0) buf[jl * 8 + warp] = tot;
+      named_barrier(1, kGemvConsumerWarps * 32);
+      if (kp == 0 && (lane & 7) == 0 && rs < n0) {
+        y = 0.f;
+        for (uint32_t w = 0; w < W; ++w) y += buf[jl * 8 + rs * W + w];
         store = true;
       }
     }
     if (store && !dead) {
-      const GemvSeg& s = a.seg[t.seg];
-      const uint32_t local = t.r + rs - s.row0;
-      float y = acc;
+      const uint32_t row = r0 + rs;
+      uint32_t sg = 0;
+      while (row >= a.seg[sg].row0 + a.seg[sg].rows) ++sg;
+      const uint32_t local = row - a.seg[sg].row0;
       if constexpr (EPI == kEpiResid) y += bf16f(a.resid_in[local]);
-      s.out[local] = to_bf16(y);
+      a.seg[sg].out[local] = to_bf16(y);
     }
-    ++i;
+    ++batch;
+    if (tcnt[3] == 0) break;
   }
 }
 
@@ -381,20 +412,29 @@ __global__ void dequant_kernel(const uint8_t* codes, const uint16_t* scales, con
 
 using GemvKernel = void (*)(GemvArgs);
 
-template <int MODE>
-GemvKernel pick(int pro, int epi) {
-  if (epi == kEpiResid) return pro == kProSiluMul ? gemv_q8g64_kernel<kProSiluMul, kEpiResid, MODE> : nullptr;
+template <int CPL>
+GemvKernel pick_cpl(int pro, int epi) {
+  if (epi == kEpiResid) return pro == kProSiluMul ? gemv_q8g64_kernel<kProSiluMul, kEpiResid, CPL> : nullptr;
   switch (pro) {
-    case kProPlain: return gemv_q8g64_kernel<kProPlain, kEpiStore, MODE>;
-    case kProRmsNorm: return gemv_q8g64_kernel<kProRmsNorm, kEpiStore, MODE>;
-    case kProAddRmsNorm: return gemv_q8g64_kernel<kProAddRmsNorm, kEpiStore, MODE>;
-    case kProSiluMul: return gemv_q8g64_kernel<kProSiluMul, kEpiStore, MODE>;
-    case kProHeadNormSilu: return gemv_q8g64_kernel<kProHeadNormSilu, kEpiStore, MODE>;
+    case kProPlain: return gemv_q8g64_kernel<kProPlain, kEpiStore, CPL>;
+    case kProRmsNorm: return gemv_q8g64_kernel<kProRmsNorm, kEpiStore, CPL>;
+    case kProAddRmsNorm: return gemv_q8g64_kernel<kProAddRmsNorm, kEpiStore, CPL>;
+    case kProSiluMul: return gemv_q8g64_kernel<kProSiluMul, kEpiStore, CPL>;
+    case kProHeadNormSilu: return gemv_q8g64_kernel<kProHeadNormSilu, kEpiStore, CPL>;
   }
   return nullptr;
 }
 
-GemvKernel pick_kernel(int pro, int epi, int mode) { return mode ? pick<1>(pro, epi) : pick<0>(pro, epi); }
+GemvKernel pick_kernel(int pro, int epi, uint32_t cpl) {
+  switch (cpl) {
+    case 1: return pick_cpl<1>(pro, epi);
+    case 2: return pick_cpl<2>(pro, epi);
+    case 3: return pick_cpl<3>(pro, epi);
+    case 4: return pick_cpl<4>(pro, epi);
+    case 5: return pick_cpl<5>(pro, epi);
+  }
+  return nullptr;
+}
 
 }  // namespace
 
@@ -402,11 +442,10 @@ bool gemv_plan(GemvPlan& p, int num_sms) {
   GemvArgs& a = p.args;
   if (a.K == 0 || a.K % 64 != 0 || a.K > (uint32_t)kGemvMaxK || a.nseg == 0 || a.nseg > kGemvMaxSegs) return false;
   const uint32_t nchunks = a.K / 16;
-  const uint32_t cpl_max = g_gemv_mode ? kGemvCplMax : kGemvCplMaxF32;
   a.W = 0;
   for (uint32_t W = 1; W <= 8; W *= 2) {
     const uint32_t cpl = (nchunks + 32 * W - 1) / (32 * W);
-    if (cpl <= cpl_max) {
+    if (cpl <= (uint32_t)kGemvCplMax) {
       a.W = W;
       a.cpl = cpl;
       break;
@@ -423,7 +462,7 @@ bool gemv_plan(GemvPlan& p, int num_sms) {
   if (a.nstage > 8) a.nstage = 8;
   if (a.nstage < 2) return false;
   a.bar_off = a.nstage * a.stage_stride;
-  p.smem = a.bar_off + 2 * a.nstage * 8 + 16 * 4 + 128 * 4;
+  p.smem = a.bar_off + 2 * a.nstage * 8 + 64 * 4 + 8 * 4;
   uint32_t total = 0;
   for (uint32_t s = 0; s < a.nseg; ++s) {
     a.seg[s].row0 = total;
@@ -431,15 +470,17 @@ bool gemv_plan(GemvPlan& p, int num_sms) {
   }
   a.total_rows = total;
   if (total == 0) return false;
-  if (p.prologue == kProHeadNormSilu && (a.head_dim == 0 || a.head_dim % 16 || a.K % a.head_dim ||
-                                         a.K / a.head_dim > 128))
-    return false;
+  if (p.prologue == kProHeadNormSilu) {
+    // a head's chunks must sit on adjacent lanes of one warp
+    const uint32_t m = a.head_dim / 16;
+    if (a.head_dim % 16 || m == 0 || m > 32 || (m & (m - 1)) || a.K % a.head_dim) return false;
+  }
   p.grid = total < (uint32_t)num_sms ? total : (uint32_t)num_sms;
-  return pick_kernel(p.prologue, p.epilogue, 0) != nullptr;
+  return pick_kernel(p.prologue, p.epilogue, a.cpl) != nullptr;
 }
 
 cudaError_t gemv_launch(const GemvPlan& p, cudaStream_t stream, bool pdl) {
-  GemvKernel k = pick_kernel(p.prologue, p.epilogue, g_gemv_mode);
+  GemvKernel k = pick_kernel(p.prologue, p.epilogue, p.args.cpl);
   if (!k) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.grid);
@@ -456,10 +497,10 @@ cudaError_t gemv_launch(const GemvPlan& p, cudaStream_t stream, bool pdl) {
 
 cudaError_t gemv_set_attributes() {
   const int pros[5] = {kProPlain, kProRmsNorm, kProAddRmsNorm, kProSiluMul, kProHeadNormSilu};
-  for (int mode = 0; mode < 2; ++mode)
+  for (uint32_t cpl = 1; cpl <= (uint32_t)kGemvCplMax; ++cpl)
     for (int epi = 0; epi < 2; ++epi)
       for (int pi = 0; pi < 5; ++pi) {
-        GemvKernel k = pick_kernel(pros[pi], epi, mode);
+        GemvKernel k = pick_kernel(pros[pi], epi, cpl);
         if (!k) continue;
         cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              kGemvSmemBudget + 4096);

@@ -12,9 +12,8 @@ namespace q35 {
 constexpr int kGemvConsumerWarps = 8;
 constexpr int kGemvThreads = (kGemvConsumerWarps + 1) * 32;  // + one producer warp
 constexpr int kGemvMaxSegs = 4;
-constexpr int kGemvCplMax = 5;      // 16-byte code chunks per lane and row (integer mode)
-constexpr int kGemvCplMaxF32 = 3;   // the fp32 mode keeps 16 floats per chunk in registers
-constexpr int kGemvMaxK = 8 * 32 * kGemvCplMaxF32 * 16;  // 12288: both modes support it
+constexpr int kGemvCplMax = 5;      // 16-byte code chunks per lane and row
+constexpr int kGemvMaxK = 12288;    // x in registers: at most 8 warps x 32 lanes x 5 chunks x 16
 constexpr int kGemvSmemBudget = 96 * 1024;  // pipeline stages per CTA
 
 // How the GEMV input vector x is formed from the preceding kernel's outputs.
@@ -66,7 +65,6 @@ struct GemvPlan {
 bool gemv_plan(GemvPlan& p, int num_sms);
 cudaError_t gemv_launch(const GemvPlan& p, cudaStream_t stream, bool pdl);
 cudaError_t gemv_set_attributes();
-extern int g_gemv_mode;  // 0 = fp32 FMA dot, 1 = integer dp4a dot
 
 // Dequantise one matrix to fp32 (bit-exact check of the GEMV's indexing).
 cudaError_t dequant_launch(const uint8_t* codes, const uint16_t* scales, const uint16_t* biases,
@@ -79,6 +77,7 @@ constexpr int kAttnThreads = (kAttnConsumerWarps + 1) * 32;
 constexpr int kAttnMaxSplits = 512;
 constexpr int kAttnMaxHalfRot = 128;
 constexpr int kAttnSmemBudget = 96 * 1024;
+constexpr int kAttnTile = 8;  // tokens per pipeline stage
 
 struct AttnArgs {
   const uint16_t* q_full;  // [H][2D]: [Q_h | gate_h]
