@@ -95,6 +95,8 @@ _SIGS = {
                                                      C.c_size_t, C.POINTER(qwen35_kv_cache), _P, _P, _P, _U, _P]),
     "qwen35_forward_linear_attention": (C.c_int, [C.POINTER(qwen35_config), C.POINTER(qwen35_gdn_layer), _P,
                                                   C.c_size_t, C.POINTER(qwen35_gdn_state), _P, _P, _P]),
+    "qwen35_forward_linear_attention_static": (C.c_int, [C.POINTER(qwen35_config), C.POINTER(qwen35_gdn_layer),
+                                                         C.POINTER(qwen35_gdn_state), _P, _P, _P]),
     "qwen35_decode_step": (C.c_int, [C.POINTER(qwen35_config), C.POINTER(qwen35_layer), _U, _P, C.c_size_t,
                                      _P, _P, _P, _U, _P]),
     "qwen35_graph_create": (C.c_int, [C.POINTER(qwen35_config), C.POINTER(qwen35_layer), _U, _P, C.c_size_t,
@@ -202,6 +204,12 @@ def qwen35_forward_full_attention_dpos(cfg, layer, scratch, kv, x_in, x_out, d_c
 def qwen35_forward_linear_attention(cfg, layer, scratch, state, x_in, x_out, stream=None):
     return lib().qwen35_forward_linear_attention(C.byref(cfg), C.byref(layer), _ptr(scratch), scratch.numel(),
                                                  C.byref(state), _ptr(x_in), _ptr(x_out), _stream(stream))
+
+
+def qwen35_forward_linear_attention_static(cfg, layer, state, x_in, x_out, stream=None):
+    """The linear-attention forward on the library's static scratch (nothing allocated)."""
+    return lib().qwen35_forward_linear_attention_static(C.byref(cfg), C.byref(layer), C.byref(state),
+                                                        _ptr(x_in), _ptr(x_out), _stream(stream))
 
 
 def qwen35_decode_step(cfg, layers, scratch, x_in, x_out, d_cache_pos, max_seq_len, stream=None):

@@ -352,6 +352,12 @@ int gdn_forward(const qwen35_config* cfg, const qwen35_gdn_layer* layer, void* s
 
 }  // namespace
 
+// Scratch of qwen35_forward_linear_attention_static: one array per device that
+// loads the library. Host code must not use the symbol as an address; the device
+// address is looked up per device and cached below.
+static __device__ __align__(256) uint8_t g_static_scratch[QWEN35_STATIC_SCRATCH_BYTES];
+static void* g_static_scratch_ptr[kMaxDevices] = {nullptr};
+
 extern "C" {
 
 int qwen35_init(void) {
@@ -433,6 +439,26 @@ int qwen35_forward_linear_attention(const qwen35_config* cfg, const qwen35_gdn_l
                                     size_t scratch_bytes, const qwen35_gdn_state* state, const qwen35_bf16* x_in,
                                     qwen35_bf16* x_out, void* stream) {
   return gdn_forward(cfg, layer, scratch, scratch_bytes, state, x_in, x_out, (cudaStream_t)stream);
+}
+
+int qwen35_forward_linear_attention_static(const qwen35_config* cfg, const qwen35_gdn_layer* layer,
+                                           const qwen35_gdn_state* state, const qwen35_bf16* x_in,
+                                           qwen35_bf16* x_out, void* stream) {
+  const size_t need = qwen35_scratch_bytes(cfg, QWEN35_LAYER_LINEAR_ATTENTION);
+  if (need == 0) return QWEN35_ERR_INVALID_ARGUMENT;
+  if (need > QWEN35_STATIC_SCRATCH_BYTES) return QWEN35_ERR_UNSUPPORTED;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QWEN35_ERR_CUDA;
+  if (!g_static_scratch_ptr[dev]) {  // once per device, with that device current
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return QWEN35_ERR_CUDA;
+    g_static_scratch_ptr[dev] = p;
+  }
+  void* scratch = g_static_scratch_ptr[dev];
+  cudaStream_t st = (cudaStream_t)stream;
+  // the array keeps the previous call's contents: the status word must start at zero
+  if (cudaMemsetAsync(scratch, 0, 256, st) != cudaSuccess) return QWEN35_ERR_CUDA;
+  return gdn_forward(cfg, layer, scratch, QWEN35_STATIC_SCRATCH_BYTES, state, x_in, x_out, st);
 }
 
 int qwen35_decode_step(const qwen35_config* cfg, const qwen35_layer* layers, uint32_t num_layers, void* scratch,

@@ -205,6 +205,29 @@ QWEN35_API int qwen35_forward_linear_attention(const qwen35_config* cfg, const q
                                     const qwen35_gdn_state* state,
                                     const qwen35_bf16* x_in, qwen35_bf16* x_out, void* stream);
 
+/* The linear-attention forward above for callers that cannot allocate device
+ * memory: a plug-in that lives inside a host framework which owns every device
+ * allocation, a process whose memory budget is fixed once at start-up, or a
+ * latency-critical path where cudaMalloc's device-wide synchronisation is not
+ * acceptable. No counterpart on the pages (their forwards take caller-owned
+ * scratch); it exists for those callers only.
+ * Instead of caller scratch it uses one static device array of 128 KiB inside
+ * the library (QWEN35_STATIC_SCRATCH_BYTES), which every GPU that loads the
+ * library keeps until the process exits. Configs whose linear-attention scratch
+ * (qwen35_scratch_bytes) exceeds it are rejected with QWEN35_ERR_UNSUPPORTED.
+ * The first call on a device looks the array's device address up (once per
+ * device, with that device current); make that first call before any stream
+ * capture. Every call shares the array and each call clears its status word
+ * first, so calls whose work overlaps on the GPU (other streams, other host
+ * threads) race on it: serialise them. Arguments and errors otherwise as
+ * qwen35_forward_linear_attention. Allocates nothing (no cudaMalloc/cudaFree). */
+#define QWEN35_STATIC_SCRATCH_BYTES (128u * 1024u)
+QWEN35_API int qwen35_forward_linear_attention_static(const qwen35_config* cfg,
+                                                      const qwen35_gdn_layer* layer,
+                                                      const qwen35_gdn_state* state,
+                                                      const qwen35_bf16* x_in, qwen35_bf16* x_out,
+                                                      void* stream);
+
 /* One decode step of a layer stack: layer i's output is layer i+1's input (the
  * caller's layer loop, which the module page leaves to the caller). Full-attention
  * layers use the device position *d_cache_pos (as in the _dpos forward); after
