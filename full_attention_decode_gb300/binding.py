@@ -106,6 +106,7 @@ _SIGS = {
     "qwen35_gemv": (C.c_int, [C.POINTER(qwen35_qweight), _P, _P, _P, C.c_size_t, _P]),
     "qwen35_dequant": (C.c_int, [C.POINTER(qwen35_qweight), _P, _P]),
     "qwen35_debug_scratch_offset": (C.c_size_t, [C.POINTER(qwen35_config), C.c_int, C.c_char_p]),
+    "qwen35_debug_trace": (C.c_int, [_P, C.c_uint32]),
 }
 
 _lib = None
@@ -259,6 +260,11 @@ def scratch_view(scratch: torch.Tensor, cfg, kind, name: str, n: int) -> torch.T
     if off == C.c_size_t(-1).value:
         raise KeyError(name)
     return scratch[off:off + 2 * n].view(torch.int16)
+
+
+def qwen35_debug_trace(buf, max_phases: int):
+    """Record the phase timeline of later launches into buf (int64 device tensor), or stop (None, 0)."""
+    return lib().qwen35_debug_trace(_ptr(buf), max_phases)
 
 
 def qwen35_dequant(w, out, stream=None):

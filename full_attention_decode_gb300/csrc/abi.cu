@@ -1,26 +1,18 @@
 // C ABI of the decode library (include/qwen35_decode.h): argument validation,
-// scratch layout, and the kernel sequence of each layer kind.
+// scratch layout, and the programs the persistent decode kernel runs.
 //
-// Full-attention layer ("full_attention.rs", forward_full_attention), 6 launches:
-//   1 GEMV  [q_proj | k_proj | v_proj] with the input RMSNorm in its prologue
-//   2 attention partials (q/k RMSNorm, RoPE, KV append, split-KV softmax)
-//   3 combine + sigmoid(gate)
-//   4 GEMV  o_proj
-//   5 GEMV  [gate_proj | up_proj] with residual add + post RMSNorm in its prologue
-//   6 GEMV  down_proj with silu(gate) * up in its prologue and the residual add
-// Linear-attention layer ("linear_attention.rs", forward_linear_attention), 5:
-//   1 GEMV  [in_proj_a | in_proj_b | in_proj_qkv | in_proj_z] + input RMSNorm
-//   2 Gated DeltaNet step (conv1d + SiLU + L2 norm, gate, beta, delta rule)
-//   3 GEMV  out_proj with per-head RMSNorm and silu(z) gating in its prologue
-//   4, 5 as 5, 6 above.
-// Every launch after the first of a call is a programmatic dependent launch, so
-// each kernel's weight stream starts while its predecessor finishes.
+// Every forward is one launch of decode_kernel (decode.cu) over a program of
+// layers: one layer for qwen35_forward_full_attention / _dpos /
+// qwen35_forward_linear_attention, every layer of the stack for
+// qwen35_decode_step. A launch is preceded by a 4-byte memset of its grid-barrier
+// counter, so a captured decode step is two graph nodes.
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
+#include <new>
 
-#include "../../include/qwen35_decode.h"
-#include "kernels.h"
+#include "qwen35_decode.h"  // include/ (on the include path)
+#include "decode.h"
 
 using namespace q35;
 
@@ -53,19 +45,21 @@ int check_config(const qwen35_config* c, Dims& d) {
   if (c->group_size != 64) return QWEN35_ERR_INVALID_ARGUMENT;
   if (!(c->rms_eps >= 0.f) || !std::isfinite(c->rms_eps)) return QWEN35_ERR_INVALID_ARGUMENT;
   if (d.E == 0 || d.I == 0 || d.E % 64 || d.I % 64) return QWEN35_ERR_INVALID_ARGUMENT;
-  if (d.E > (uint32_t)kGemvMaxK || d.I > (uint32_t)kGemvMaxK) return QWEN35_ERR_UNSUPPORTED;
+  if (d.E > 12288 || d.I > 12288) return QWEN35_ERR_UNSUPPORTED;
   return QWEN35_OK;
 }
 
 int check_fa_dims(const qwen35_config* c, const Dims& d) {
   if (d.H == 0 || d.Hkv == 0 || d.H % d.Hkv) return QWEN35_ERR_INVALID_ARGUMENT;
   if (d.R % 2 || d.R > d.D || d.R == 0) return QWEN35_ERR_INVALID_ARGUMENT;
-  if (d.D != 64 && d.D != 128 && d.D != 256) return QWEN35_ERR_UNSUPPORTED;
-  if (d.Hkv > 8 || (d.H > 8 && d.H % 8) || (d.H > 8 && d.H / 8 > 4) ||
-      (d.H > 8 && d.H / 8 > d.H / d.Hkv))
-    return QWEN35_ERR_UNSUPPORTED;
-  if (d.H * d.D > (uint32_t)kGemvMaxK) return QWEN35_ERR_UNSUPPORTED;
   if (!(c->rope_theta > 0.f)) return QWEN35_ERR_INVALID_ARGUMENT;
+  if (d.D != 64 && d.D != 128 && d.D != 256) return QWEN35_ERR_UNSUPPORTED;
+  if (d.Hkv > 8 || d.H * d.D > 12288 || d.H * d.D % 64) return QWEN35_ERR_UNSUPPORTED;
+  if (d.R / 2 > 128) return QWEN35_ERR_UNSUPPORTED;
+  // attention warps: the consumer warps hold the q-heads in groups of 1 or 2
+  const bool two = (d.H / d.Hkv) % 2 == 0 && d.H / 2 <= (uint32_t)kDecConsumerWarps;
+  const bool one = d.H <= (uint32_t)kDecConsumerWarps;
+  if (!two && !one) return QWEN35_ERR_UNSUPPORTED;
   return QWEN35_OK;
 }
 
@@ -74,8 +68,7 @@ int check_gdn_dims(const Dims& d) {
   if ((d.Dk != 32 && d.Dk != 64 && d.Dk != 128) || (d.Dv != 32 && d.Dv != 64 && d.Dv != 128))
     return QWEN35_ERR_UNSUPPORTED;
   if (d.Kc == 0 || d.Kc > 8) return QWEN35_ERR_UNSUPPORTED;
-  if ((d.Hv / d.Hk) * (d.Dv / 32) > 8) return QWEN35_ERR_UNSUPPORTED;  // one cluster per k-head
-  if (d.Z > (uint32_t)kGemvMaxK || d.Z / d.Dv > 128) return QWEN35_ERR_UNSUPPORTED;
+  if (d.Z > 12288) return QWEN35_ERR_UNSUPPORTED;
   return QWEN35_OK;
 }
 
@@ -85,99 +78,63 @@ bool qw_ok(const qwen35_qweight& w, uint32_t n, uint32_t k) {
 
 // ---------------------------------------------------------------- scratch layout
 
+// [0, 4) device status word; [4, 8) grid-barrier counter; intermediates from 256.
 struct Layout {
-  size_t q_full, k, v, ga, o, part_o, part_ml;      // full attention
-  size_t dt_raw, b_raw, qkv, z, y, out;             // linear attention
-  size_t x_resid, g, u;                             // both (MLP)
+  ScratchMap m;
   size_t total;
 };
 
 struct Bump {
-  size_t off = 256;  // [0, 4): device status word
-  size_t take(size_t bytes) {
+  size_t off = 256;
+  uint32_t take(size_t bytes) {
     const size_t o = off;
     off += (bytes + 255) / 256 * 256;
-    return o;
+    return (uint32_t)o;
   }
 };
 
 Layout layout(const Dims& d, int kind) {
   Layout L = {};
   Bump b;
-  L.x_resid = b.take(d.E * 2);
-  L.g = b.take(d.I * 2);
-  L.u = b.take(d.I * 2);
+  L.m.x_resid = b.take(d.E * 2);
+  L.m.g = b.take(d.I * 2);
+  L.m.u = b.take(d.I * 2);
   if (kind == QWEN35_LAYER_FULL_ATTENTION) {
-    L.q_full = b.take((size_t)2 * d.H * d.D * 2);
-    L.k = b.take((size_t)d.Hkv * d.D * 2);
-    L.v = b.take((size_t)d.Hkv * d.D * 2);
-    L.ga = b.take((size_t)d.H * d.D * 2);
-    L.o = b.take((size_t)d.E * 2);
-    L.part_o = b.take((size_t)kAttnMaxSplits * d.H * d.D * 4);
-    L.part_ml = b.take((size_t)kAttnMaxSplits * d.H * 2 * 4);
+    L.m.q_full = b.take((size_t)2 * d.H * d.D * 2);
+    L.m.k = b.take((size_t)d.Hkv * d.D * 2);
+    L.m.v = b.take((size_t)d.Hkv * d.D * 2);
+    L.m.ga = b.take((size_t)d.H * d.D * 2);
+    L.m.o = b.take((size_t)d.E * 2);
+    L.m.part_o = b.take((size_t)kDecMaxSplits * d.H * d.D * 4);
+    L.m.part_ml = b.take((size_t)kDecMaxSplits * d.H * 2 * 4);
   } else {
-    L.dt_raw = b.take(d.Hv * 2);
-    L.b_raw = b.take(d.Hv * 2);
-    L.qkv = b.take((size_t)d.C * 2);
-    L.z = b.take((size_t)d.Z * 2);
-    L.y = b.take((size_t)d.Z * 2);
-    L.out = b.take((size_t)d.E * 2);
+    L.m.dt_raw = b.take(d.Hv * 2);
+    L.m.b_raw = b.take(d.Hv * 2);
+    L.m.qkv = b.take((size_t)d.C * 2);
+    L.m.z = b.take((size_t)d.Z * 2);
+    L.m.y = b.take((size_t)d.Z * 2);
+    L.m.out = b.take((size_t)d.E * 2);
   }
   L.total = b.off;
   return L;
 }
 
-template <typename T>
-T* at(void* base, size_t off) {
-  return reinterpret_cast<T*>(static_cast<uint8_t*>(base) + off);
+// Both kinds' intermediates in one map (they share the buffer; the phases that use
+// them never overlap).
+ScratchMap stack_map(const Dims& d) {
+  ScratchMap a = layout(d, QWEN35_LAYER_FULL_ATTENTION).m, b = layout(d, QWEN35_LAYER_LINEAR_ATTENTION).m;
+  a.dt_raw = b.dt_raw; a.b_raw = b.b_raw; a.qkv = b.qkv; a.z = b.z; a.y = b.y; a.out = b.out;
+  return a;
 }
 
-GemvSeg seg_of(const qwen35_qweight& w, uint16_t* out) {
-  GemvSeg s = {};
-  s.codes = w.codes;
-  s.scales = w.scales;
-  s.biases = w.biases;
-  s.out = out;
-  s.rows = w.n;
-  return s;
-}
-
-int launch_gemv(GemvPlan& p, cudaStream_t st, bool pdl) {
-  if (!gemv_plan(p, num_sms())) return QWEN35_ERR_UNSUPPORTED;
-  return gemv_launch(p, st, pdl) == cudaSuccess ? QWEN35_OK : QWEN35_ERR_CUDA;
-}
-
-// MLP tail shared by both layer kinds: [gate | up] with residual + post norm, then down.
-int mlp(const Dims& d, float eps, const uint16_t* post_ln, const qwen35_qweight& gate_w,
-        const qwen35_qweight& up_w, const qwen35_qweight& down_w, const uint16_t* x_in, const uint16_t* delta,
-        const Layout& L, void* scratch, uint16_t* x_out, cudaStream_t st) {
-  int* status = at<int>(scratch, 0);
-  GemvPlan p = {};
-  p.prologue = kProAddRmsNorm;
-  p.epilogue = kEpiStore;
-  p.args.nseg = 2;
-  p.args.seg[0] = seg_of(gate_w, at<uint16_t>(scratch, L.g));
-  p.args.seg[1] = seg_of(up_w, at<uint16_t>(scratch, L.u));
-  p.args.K = d.E;
-  p.args.a = x_in;
-  p.args.b = delta;
-  p.args.nw = post_ln;
-  p.args.eps = eps;
-  p.args.resid_out = at<uint16_t>(scratch, L.x_resid);
-  p.args.status = status;
-  int r = launch_gemv(p, st, true);
-  if (r) return r;
-  GemvPlan q = {};
-  q.prologue = kProSiluMul;
-  q.epilogue = kEpiResid;
-  q.args.nseg = 1;
-  q.args.seg[0] = seg_of(down_w, x_out);
-  q.args.K = d.I;
-  q.args.a = at<uint16_t>(scratch, L.g);
-  q.args.b = at<uint16_t>(scratch, L.u);
-  q.args.resid_in = at<uint16_t>(scratch, L.x_resid);
-  q.args.status = status;
-  return launch_gemv(q, st, true);
+QMat qm(const qwen35_qweight& w) {
+  QMat m;
+  m.codes = w.codes;
+  m.scales = w.scales;
+  m.biases = w.biases;
+  m.n = w.n;
+  m.pad = 0;
+  return m;
 }
 
 int check_fa_layer(const qwen35_fa_layer* l, const Dims& d) {
@@ -205,7 +162,85 @@ int check_gdn_layer(const qwen35_gdn_layer* l, const Dims& d) {
   return QWEN35_OK;
 }
 
-// The full-attention sequence; d_pos == nullptr selects the host position.
+void fill_fa(LayerDesc& L, const qwen35_fa_layer* l, const qwen35_kv_cache* kv) {
+  L.kind = kLayerFA;
+  L.capacity = kv->capacity;
+  L.m[0] = qm(l->q_proj);
+  L.m[1] = qm(l->k_proj);
+  L.m[2] = qm(l->v_proj);
+  L.m[3] = qm(l->o_proj);
+  L.m[4] = qm(l->gate_proj);
+  L.m[5] = qm(l->up_proj);
+  L.m[6] = qm(l->down_proj);
+  L.input_ln = l->input_ln;
+  L.post_ln = l->post_ln;
+  L.q_norm = l->q_norm;
+  L.k_norm = l->k_norm;
+  L.kc = kv->k;
+  L.vc = kv->v;
+}
+
+void fill_gdn(LayerDesc& L, const qwen35_gdn_layer* l, const qwen35_gdn_state* st) {
+  L.kind = kLayerGDN;
+  L.m[0] = qm(l->in_proj_a);
+  L.m[1] = qm(l->in_proj_b);
+  L.m[2] = qm(l->in_proj_qkv);
+  L.m[3] = qm(l->in_proj_z);
+  L.m[4] = qm(l->gate_proj);
+  L.m[5] = qm(l->up_proj);
+  L.m[6] = qm(l->down_proj);
+  L.m[7] = qm(l->out_proj);
+  L.input_ln = l->input_ln;
+  L.post_ln = l->post_ln;
+  L.norm_weight = l->norm_weight;
+  L.dt_bias = l->dt_bias;
+  L.conv_w = l->conv1d_weight;
+  L.a_log = l->a_log;
+  L.conv_state = st->conv_state;
+  L.ssm = st->gdn_state;
+}
+
+// The program header shared by every call; the caller fills the layers.
+Program* new_program(const qwen35_config* cfg, const Dims& d, void* scratch) {
+  Program* p = new (std::nothrow) Program();
+  if (!p) return nullptr;
+  p->E = d.E; p->I = d.I; p->H = d.H; p->Hkv = d.Hkv; p->D = d.D; p->R = d.R;
+  p->Hk = d.Hk; p->Hv = d.Hv; p->Dk = d.Dk; p->Dv = d.Dv; p->Kc = d.Kc; p->C = d.C; p->Z = d.Z;
+  p->eps = cfg->rms_eps;
+  p->scale_log2 = d.D ? (float)(1.0 / std::sqrt((double)d.D) * 1.4426950408889634) : 0.f;
+  p->gdn_out_scale = d.Dk ? (float)(1.0 / std::sqrt((double)d.Dk)) : 0.f;
+  p->l2_eps = 1e-6f;
+  p->scratch = static_cast<uint8_t*>(scratch);
+  p->sm = stack_map(d);
+  p->status = reinterpret_cast<int*>(scratch);
+  p->barrier = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(scratch) + 4);
+  // inv_freq[i] = theta^(-2i/R), computed in double and kept as fp32
+  for (uint32_t i = 0; i < d.R / 2 && i < 128; ++i)
+    p->inv_freq[i] = (float)std::pow((double)cfg->rope_theta, -2.0 * (double)i / (double)d.R);
+  return p;
+}
+
+// Phase timeline of the next launches (qwen35_debug_trace); off when null.
+unsigned long long* g_trace = nullptr;
+uint32_t g_trace_phases = 0;
+
+uint32_t splits_for(uint32_t span) {
+  uint32_t P = (span + 31) / 32;
+  if (P > (uint32_t)num_sms()) P = num_sms();
+  if (P > (uint32_t)kDecMaxSplits) P = kDecMaxSplits;
+  return P == 0 ? 1 : P;
+}
+
+int launch(Program* p, bool has_fa, bool has_gdn, cudaStream_t st) {
+  p->trace = g_trace;
+  p->trace_phases = g_trace_phases;
+  int r = QWEN35_OK;
+  if (!decode_dims_ok(*p, has_fa, has_gdn)) r = QWEN35_ERR_UNSUPPORTED;
+  else if (decode_launch(*p, num_sms(), st) != cudaSuccess) r = QWEN35_ERR_CUDA;
+  delete p;
+  return r;
+}
+
 int fa_forward(const qwen35_config* cfg, const qwen35_fa_layer* layer, void* scratch, size_t scratch_bytes,
                const qwen35_kv_cache* kv, const uint16_t* x_in, uint16_t* x_out, uint32_t cache_pos,
                uint32_t seq_len, const int32_t* d_pos, uint32_t max_seq, cudaStream_t st) {
@@ -216,75 +251,25 @@ int fa_forward(const qwen35_config* cfg, const qwen35_fa_layer* layer, void* scr
   if ((r = check_fa_layer(layer, d))) return r;
   if (!kv || !aligned16(kv->k) || !aligned16(kv->v) || kv->capacity == 0) return QWEN35_ERR_INVALID_ARGUMENT;
   if (!aligned16(x_in) || !aligned16(x_out) || !aligned16(scratch)) return QWEN35_ERR_INVALID_ARGUMENT;
-  const Layout L = layout(d, QWEN35_LAYER_FULL_ATTENTION);
-  if (scratch_bytes < L.total) return QWEN35_ERR_INVALID_ARGUMENT;
+  if (scratch_bytes < layout(d, QWEN35_LAYER_FULL_ATTENTION).total) return QWEN35_ERR_INVALID_ARGUMENT;
   if (d_pos) {
     if (max_seq == 0) return QWEN35_ERR_INVALID_ARGUMENT;
   } else if (cache_pos >= kv->capacity || seq_len == 0 || seq_len > cache_pos + 1) {
     return QWEN35_ERR_OUT_OF_RANGE;
   }
   if (num_sms() <= 0) return QWEN35_ERR_CUDA;
-  int* status = at<int>(scratch, 0);
-
-  GemvPlan p = {};
-  p.prologue = kProRmsNorm;
-  p.epilogue = kEpiStore;
-  p.args.nseg = 3;
-  p.args.seg[0] = seg_of(layer->q_proj, at<uint16_t>(scratch, L.q_full));
-  p.args.seg[1] = seg_of(layer->k_proj, at<uint16_t>(scratch, L.k));
-  p.args.seg[2] = seg_of(layer->v_proj, at<uint16_t>(scratch, L.v));
-  p.args.K = d.E;
-  p.args.a = x_in;
-  p.args.nw = layer->input_ln;
-  p.args.eps = cfg->rms_eps;
-  p.args.status = status;
-  if ((r = launch_gemv(p, st, true))) return r;
-
-  AttnPlan ap = {};
-  AttnArgs& a = ap.args;
-  a.q_full = at<uint16_t>(scratch, L.q_full);
-  a.k_new = at<uint16_t>(scratch, L.k);
-  a.v_new = at<uint16_t>(scratch, L.v);
-  a.q_norm = layer->q_norm;
-  a.k_norm = layer->k_norm;
-  a.kc = kv->k;
-  a.vc = kv->v;
-  a.capacity = kv->capacity;
-  a.H = d.H; a.Hkv = d.Hkv; a.D = d.D; a.R = d.R;
-  a.eps = cfg->rms_eps;
-  a.scale_log2 = (float)(1.0 / std::sqrt((double)d.D) * 1.4426950408889634);
-  a.cache_pos = cache_pos;
-  a.S = seq_len;
-  a.d_pos = d_pos;
-  a.max_seq = max_seq;
-  const uint32_t span = d_pos ? max_seq : seq_len;
-  uint32_t P = (span + 31) / 32;
-  if (P > (uint32_t)num_sms()) P = num_sms();
-  if (P > (uint32_t)kAttnMaxSplits) P = kAttnMaxSplits;
-  if (P == 0) P = 1;
-  a.P = P;
-  a.part_o = at<float>(scratch, L.part_o);
-  a.part_ml = at<float>(scratch, L.part_ml);
-  a.ga = at<uint16_t>(scratch, L.ga);
-  a.status = status;
-  // inv_freq[i] = theta^(-2i/R), computed in double and kept as fp32
-  for (uint32_t i = 0; i < d.R / 2; ++i)
-    a.inv_freq[i] = (float)std::pow((double)cfg->rope_theta, -2.0 * (double)i / (double)d.R);
-  if (!attn_plan(ap)) return QWEN35_ERR_UNSUPPORTED;
-  if (attn_launch(ap, st, true) != cudaSuccess) return QWEN35_ERR_CUDA;
-
-  GemvPlan o = {};
-  o.prologue = kProPlain;
-  o.epilogue = kEpiStore;
-  o.args.nseg = 1;
-  o.args.seg[0] = seg_of(layer->o_proj, at<uint16_t>(scratch, L.o));
-  o.args.K = d.H * d.D;
-  o.args.a = at<uint16_t>(scratch, L.ga);
-  o.args.status = status;
-  if ((r = launch_gemv(o, st, true))) return r;
-
-  return mlp(d, cfg->rms_eps, layer->post_ln, layer->gate_proj, layer->up_proj, layer->down_proj, x_in,
-             at<uint16_t>(scratch, L.o), L, scratch, x_out, st);
+  Program* p = new_program(cfg, d, scratch);
+  if (!p) return QWEN35_ERR_CUDA;
+  p->n_layers = 1;
+  p->x_in = x_in;
+  p->x_out = x_out;
+  p->pos = cache_pos;
+  p->S = seq_len;
+  p->d_pos = d_pos;
+  p->max_seq = max_seq;
+  p->P = splits_for(d_pos ? max_seq : seq_len);
+  fill_fa(p->layers[0], layer, kv);
+  return launch(p, true, false, st);
 }
 
 int gdn_forward(const qwen35_config* cfg, const qwen35_gdn_layer* layer, void* scratch, size_t scratch_bytes,
@@ -296,58 +281,15 @@ int gdn_forward(const qwen35_config* cfg, const qwen35_gdn_layer* layer, void* s
   if ((r = check_gdn_layer(layer, d))) return r;
   if (!state || !aligned16(state->conv_state) || !aligned16(state->gdn_state)) return QWEN35_ERR_INVALID_ARGUMENT;
   if (!aligned16(x_in) || !aligned16(x_out) || !aligned16(scratch)) return QWEN35_ERR_INVALID_ARGUMENT;
-  const Layout L = layout(d, QWEN35_LAYER_LINEAR_ATTENTION);
-  if (scratch_bytes < L.total) return QWEN35_ERR_INVALID_ARGUMENT;
+  if (scratch_bytes < layout(d, QWEN35_LAYER_LINEAR_ATTENTION).total) return QWEN35_ERR_INVALID_ARGUMENT;
   if (num_sms() <= 0) return QWEN35_ERR_CUDA;
-  int* status = at<int>(scratch, 0);
-
-  GemvPlan p = {};
-  p.prologue = kProRmsNorm;
-  p.epilogue = kEpiStore;
-  p.args.nseg = 4;
-  p.args.seg[0] = seg_of(layer->in_proj_a, at<uint16_t>(scratch, L.dt_raw));
-  p.args.seg[1] = seg_of(layer->in_proj_b, at<uint16_t>(scratch, L.b_raw));
-  p.args.seg[2] = seg_of(layer->in_proj_qkv, at<uint16_t>(scratch, L.qkv));
-  p.args.seg[3] = seg_of(layer->in_proj_z, at<uint16_t>(scratch, L.z));
-  p.args.K = d.E;
-  p.args.a = x_in;
-  p.args.nw = layer->input_ln;
-  p.args.eps = cfg->rms_eps;
-  p.args.status = status;
-  if ((r = launch_gemv(p, st, true))) return r;
-
-  GdnArgs g = {};
-  g.qkv = at<uint16_t>(scratch, L.qkv);
-  g.dt_raw = at<uint16_t>(scratch, L.dt_raw);
-  g.b_raw = at<uint16_t>(scratch, L.b_raw);
-  g.a_log = layer->a_log;
-  g.dt_bias = layer->dt_bias;
-  g.conv_w = layer->conv1d_weight;
-  g.conv_state = state->conv_state;
-  g.ssm = state->gdn_state;
-  g.y = at<uint16_t>(scratch, L.y);
-  g.Hk = d.Hk; g.Hv = d.Hv; g.Dk = d.Dk; g.Dv = d.Dv; g.Kc = d.Kc;
-  g.l2_eps = 1e-6f;
-  g.out_scale = (float)(1.0 / std::sqrt((double)d.Dk));
-  g.status = status;
-  if (gdn_launch(g, st, true) != cudaSuccess) return QWEN35_ERR_CUDA;
-
-  GemvPlan o = {};
-  o.prologue = kProHeadNormSilu;
-  o.epilogue = kEpiStore;
-  o.args.nseg = 1;
-  o.args.seg[0] = seg_of(layer->out_proj, at<uint16_t>(scratch, L.out));
-  o.args.K = d.Z;
-  o.args.a = at<uint16_t>(scratch, L.y);
-  o.args.b = at<uint16_t>(scratch, L.z);
-  o.args.nw = layer->norm_weight;
-  o.args.eps = cfg->rms_eps;
-  o.args.head_dim = d.Dv;
-  o.args.status = status;
-  if ((r = launch_gemv(o, st, true))) return r;
-
-  return mlp(d, cfg->rms_eps, layer->post_ln, layer->gate_proj, layer->up_proj, layer->down_proj, x_in,
-             at<uint16_t>(scratch, L.out), L, scratch, x_out, st);
+  Program* p = new_program(cfg, d, scratch);
+  if (!p) return QWEN35_ERR_CUDA;
+  p->n_layers = 1;
+  p->x_in = x_in;
+  p->x_out = x_out;
+  fill_gdn(p->layers[0], layer, state);
+  return launch(p, false, true, st);
 }
 
 }  // namespace
@@ -363,13 +305,14 @@ extern "C" {
 int qwen35_init(void) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QWEN35_ERR_CUDA;
-  int major = 0, minor = 0, sms = 0;
+  int major = 0, minor = 0, sms = 0, coop = 0;
   if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess)
     return QWEN35_ERR_CUDA;
-  if (major != 10 || minor != 3) return QWEN35_ERR_CUDA;  // built for sm_103a only
-  if (gemv_set_attributes() != cudaSuccess || attn_set_attributes() != cudaSuccess) return QWEN35_ERR_CUDA;
+  if (major != 10 || minor != 3 || !coop) return QWEN35_ERR_CUDA;  // built for sm_103a only
+  if (decode_set_attributes() != cudaSuccess) return QWEN35_ERR_CUDA;
   g_num_sms[dev] = sms;
   return QWEN35_OK;
 }
@@ -464,27 +407,50 @@ int qwen35_forward_linear_attention_static(const qwen35_config* cfg, const qwen3
 int qwen35_decode_step(const qwen35_config* cfg, const qwen35_layer* layers, uint32_t num_layers, void* scratch,
                        size_t scratch_bytes, const qwen35_bf16* x_in, qwen35_bf16* x_out, int32_t* d_cache_pos,
                        uint32_t max_seq_len, void* stream) {
-  if (!layers || num_layers == 0 || !d_cache_pos || ((uintptr_t)d_cache_pos % 4)) return QWEN35_ERR_INVALID_ARGUMENT;
+  if (!layers || num_layers == 0 || num_layers > (uint32_t)kMaxLayers || !d_cache_pos ||
+      ((uintptr_t)d_cache_pos % 4) || max_seq_len == 0)
+    return QWEN35_ERR_INVALID_ARGUMENT;
+  Dims d;
+  int r = check_config(cfg, d);
+  if (r) return r;
+  bool has_fa = false, has_gdn = false;
   for (uint32_t i = 0; i < num_layers; ++i) {
     const qwen35_layer& l = layers[i];
     if (l.kind == QWEN35_LAYER_FULL_ATTENTION) {
-      if (!l.fa || !l.kv) return QWEN35_ERR_INVALID_ARGUMENT;
+      if (!l.fa || !l.kv || !aligned16(l.kv->k) || !aligned16(l.kv->v) || l.kv->capacity == 0)
+        return QWEN35_ERR_INVALID_ARGUMENT;
+      if ((r = check_fa_dims(cfg, d)) || (r = check_fa_layer(l.fa, d))) return r;
+      has_fa = true;
     } else if (l.kind == QWEN35_LAYER_LINEAR_ATTENTION) {
-      if (!l.gdn || !l.state) return QWEN35_ERR_INVALID_ARGUMENT;
+      if (!l.gdn || !l.state || !aligned16(l.state->conv_state) || !aligned16(l.state->gdn_state))
+        return QWEN35_ERR_INVALID_ARGUMENT;
+      if ((r = check_gdn_dims(d)) || (r = check_gdn_layer(l.gdn, d))) return r;
+      has_gdn = true;
     } else {
       return QWEN35_ERR_INVALID_ARGUMENT;
     }
   }
-  cudaStream_t st = (cudaStream_t)stream;
+  if (!aligned16(x_in) || !aligned16(x_out) || !aligned16(scratch)) return QWEN35_ERR_INVALID_ARGUMENT;
+  size_t need = 0;
+  if (has_fa) need = layout(d, QWEN35_LAYER_FULL_ATTENTION).total;
+  if (has_gdn && layout(d, QWEN35_LAYER_LINEAR_ATTENTION).total > need)
+    need = layout(d, QWEN35_LAYER_LINEAR_ATTENTION).total;
+  if (scratch_bytes < need) return QWEN35_ERR_INVALID_ARGUMENT;
+  if (num_sms() <= 0) return QWEN35_ERR_CUDA;
+  Program* p = new_program(cfg, d, scratch);
+  if (!p) return QWEN35_ERR_CUDA;
+  p->n_layers = num_layers;
+  p->x_in = x_in;
+  p->x_out = x_out;
+  p->d_pos = d_cache_pos;
+  p->max_seq = max_seq_len;
+  p->P = splits_for(max_seq_len);
+  p->advance = d_cache_pos;
   for (uint32_t i = 0; i < num_layers; ++i) {
-    const qwen35_layer& l = layers[i];
-    const qwen35_bf16* src = i == 0 ? x_in : x_out;
-    int r = l.kind == QWEN35_LAYER_FULL_ATTENTION
-                ? fa_forward(cfg, l.fa, scratch, scratch_bytes, l.kv, src, x_out, 0, 0, d_cache_pos, max_seq_len, st)
-                : gdn_forward(cfg, l.gdn, scratch, scratch_bytes, l.state, src, x_out, st);
-    if (r) return r;
+    if (layers[i].kind == QWEN35_LAYER_FULL_ATTENTION) fill_fa(p->layers[i], layers[i].fa, layers[i].kv);
+    else fill_gdn(p->layers[i], layers[i].gdn, layers[i].state);
   }
-  return advance_pos_launch(d_cache_pos, st, true) == cudaSuccess ? QWEN35_OK : QWEN35_ERR_CUDA;
+  return launch(p, has_fa, has_gdn, (cudaStream_t)stream);
 }
 
 struct qwen35_graph {
@@ -514,7 +480,12 @@ int qwen35_graph_create(const qwen35_config* cfg, const qwen35_layer* layers, ui
     cudaGraphDestroy(g);
     return QWEN35_ERR_CUDA;
   }
-  qwen35_graph* out = new qwen35_graph{g, ex};
+  qwen35_graph* out = new (std::nothrow) qwen35_graph{g, ex};
+  if (!out) {
+    cudaGraphExecDestroy(ex);
+    cudaGraphDestroy(g);
+    return QWEN35_ERR_CUDA;
+  }
   *out_graph = out;
   return QWEN35_OK;
 }
@@ -537,18 +508,18 @@ size_t qwen35_debug_scratch_offset(const qwen35_config* cfg, int kind, const cha
   if (!name || qwen35_scratch_bytes(cfg, kind) == 0) return none;
   Dims d;
   check_config(cfg, d);
-  const Layout L = layout(d, kind);
+  const ScratchMap m = layout(d, kind).m;
   struct Named {
     const char* n;
-    size_t off;
+    uint32_t off;
     int kind;
   };
   const int F = QWEN35_LAYER_FULL_ATTENTION, G = QWEN35_LAYER_LINEAR_ATTENTION;
-  const Named tab[] = {{"q_full", L.q_full, F}, {"k", L.k, F},         {"v", L.v, F},
-                       {"gated_attn", L.ga, F}, {"o", L.o, F},         {"dt_raw", L.dt_raw, G},
-                       {"b_raw", L.b_raw, G},   {"qkv", L.qkv, G},     {"z", L.z, G},
-                       {"y", L.y, G},           {"out", L.out, G},     {"x_resid", L.x_resid, -1},
-                       {"gate_act", L.g, -1},   {"up_act", L.u, -1}};
+  const Named tab[] = {{"q_full", m.q_full, F}, {"k", m.k, F},         {"v", m.v, F},
+                       {"gated_attn", m.ga, F}, {"o", m.o, F},         {"dt_raw", m.dt_raw, G},
+                       {"b_raw", m.b_raw, G},   {"qkv", m.qkv, G},     {"z", m.z, G},
+                       {"y", m.y, G},           {"out", m.out, G},     {"x_resid", m.x_resid, -1},
+                       {"gate_act", m.g, -1},   {"up_act", m.u, -1}};
   for (const Named& e : tab)
     if ((e.kind == kind || e.kind == -1) && std::strcmp(e.n, name) == 0) return e.off;
   return none;
@@ -556,19 +527,31 @@ size_t qwen35_debug_scratch_offset(const qwen35_config* cfg, int kind, const cha
 
 int qwen35_gemv(const qwen35_qweight* w, const qwen35_bf16* x, qwen35_bf16* y, void* scratch, size_t scratch_bytes,
                 void* stream) {
-  if (!w || !aligned16(x) || !y || !aligned16(scratch) || scratch_bytes < 256) return QWEN35_ERR_INVALID_ARGUMENT;
+  if (!w || !aligned16(x) || !aligned16(y) || !aligned16(scratch) || scratch_bytes < 256)
+    return QWEN35_ERR_INVALID_ARGUMENT;
   if (!qw_ok(*w, w->n, w->k) || w->n == 0 || w->k == 0 || w->k % 64) return QWEN35_ERR_INVALID_ARGUMENT;
-  if (w->k > (uint32_t)kGemvMaxK) return QWEN35_ERR_UNSUPPORTED;
+  if (w->k > 12288) return QWEN35_ERR_UNSUPPORTED;
   if (num_sms() <= 0) return QWEN35_ERR_CUDA;
-  GemvPlan p = {};
-  p.prologue = kProPlain;
-  p.epilogue = kEpiStore;
-  p.args.nseg = 1;
-  p.args.seg[0] = seg_of(*w, y);
-  p.args.K = w->k;
-  p.args.a = x;
-  p.args.status = at<int>(scratch, 0);
-  return launch_gemv(p, (cudaStream_t)stream, true);
+  qwen35_config cfg = {};
+  cfg.group_size = 64;
+  Dims d = {};
+  d.E = w->k;
+  d.I = w->k;
+  Program* p = new_program(&cfg, d, scratch);
+  if (!p) return QWEN35_ERR_CUDA;
+  p->n_layers = 1;
+  p->x_in = x;
+  p->x_out = y;
+  p->layers[0].kind = kLayerGemv;
+  p->layers[0].m[0] = qm(*w);
+  return launch(p, false, false, (cudaStream_t)stream);
+}
+
+int qwen35_debug_trace(unsigned long long* d_trace, uint32_t max_phases) {
+  if ((d_trace == nullptr) != (max_phases == 0)) return QWEN35_ERR_INVALID_ARGUMENT;
+  g_trace = d_trace;
+  g_trace_phases = max_phases;
+  return QWEN35_OK;
 }
 
 int qwen35_dequant(const qwen35_qweight* w, float* out, void* stream) {

@@ -66,15 +66,27 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
                : "memory");
 }
-// Test the phase; the thread may sleep in hardware until the phase completes or
-// about `hint_ns` pass, so waiting warps do not spin on the issue slots.
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity, uint32_t hint_ns = 1000000) {
+// Test the phase. With a nonzero QWEN35_WAIT_HINT_NS the thread may sleep in
+// hardware until the phase completes or about that many ns pass; with 0 it uses
+// the instruction's own (short) time limit.
+#ifndef QWEN35_WAIT_HINT_NS
+#define QWEN35_WAIT_HINT_NS 0
+#endif
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
+#if QWEN35_WAIT_HINT_NS > 0
   asm volatile(
       "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
       : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
+      : "r"(smem_addr(bar)), "r"(parity), "r"((uint32_t)QWEN35_WAIT_HINT_NS)
       : "memory");
+#else
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+#endif
   return ok != 0;
 }
 __device__ __forceinline__ uint64_t global_ns() {

@@ -1,0 +1,1392 @@
+// Persistent single-token decode kernel for Qwen3.5 decoder layers on sm_103a.
+//
+// One launch runs a program of layers: a single layer for the per-layer forwards
+// of the pages "full_attention.rs" (forward_full_attention) and
+// "linear_attention.rs" (forward_linear_attention), or the whole stack for a
+// decode step. Each layer is a sequence of phases:
+//   full attention:   [q|k|v GEMV + input RMSNorm] [split-KV attention with q/k
+//                     norm, partial RoPE, KV append] [combine + sigmoid gate]
+//                     [o_proj] [gate|up GEMV + residual + post RMSNorm]
+//                     [down GEMV + SiLU gate + residual]
+//   linear attention: [a|b|qkv|z GEMV + input RMSNorm] [conv1d + SiLU + L2 norm,
+//                     gate, beta, gated delta rule] [out_proj + per-head RMSNorm
+//                     + SiLU(z) gate] [gate|up ...] [down ...]
+//
+// The grid is one CTA per SM (a cooperative launch, so all CTAs are resident):
+// one producer warp and twelve consumer warps. The producer walks the CTA's
+// whole schedule of the launch, every weight tile of every GEMV phase and every
+// K/V tile of every attention phase, and streams them with bulk (TMA-engine)
+// copies into a four-stage, 176 KiB shared-memory ring, never waiting for a
+// phase boundary: weights and old cache rows do not depend on the phases before
+// them. Consumers run the phases in order with a grid barrier between dependent
+// phases; while they wait at a barrier or form a phase's input, the ring keeps
+// filling, so HBM stays busy across phase boundaries.
+//
+// Phase functions are kept out of line so that each gets the full register budget
+// (one call per phase; the call costs nothing next to the phase).
+//
+// GEMV phases (the int8 group-64 affine QuantWeights::gemv family): each CTA owns
+// a balanced contiguous range of rows of the phase's concatenated matrices. The
+// input vector is formed once per CTA (RMSNorm, residual add + RMSNorm, SiLU
+// gating, per-head RMSNorm with SiLU(z) gating) and kept in shared memory as
+// 16-bit fixed point per 16-element chunk (x ~= q 2^(e-15), q = 256 hi + lo, a
+// power-of-two scale per chunk: exact for every element within 2^8 of its chunk's
+// largest, since bf16 carries 8 significant bits). Each consumer lane holds its
+// chunks in registers; a 16-code chunk costs eight dp4a giving sum (c - 128) q
+// exactly in int32, and the group identity
+//   sum_k (s c_k + b) x_k = s sum_k (c_k - 128) x_k + (b + 128 s) sum_k x_k
+// applies scale and bias once per chunk (the -128 offset avoids cancelling two
+// terms ~128x larger than the result when b is close to -128 s). Warps reduce four
+// tiles' rows at once with a transposed warp reduction.
+#include <cstddef>
+
+#include "common.cuh"
+#include "decode.h"
+
+namespace q35 {
+namespace {
+
+constexpr int NCW = kDecConsumerWarps;
+constexpr int NCT = NCW * 32;
+constexpr uint32_t FULLMASK = 0xffffffffu;
+constexpr int kTS = 8;      // tokens per attention tile
+constexpr int kMaxKc = 8;
+
+enum PhaseType { kPhGemv = 0, kPhAttn = 1, kPhCombine = 2, kPhGdn = 3 };
+enum Pro { kPlain = 0, kRms = 1, kAddRms = 2, kSiluMul = 3, kHeadNormSilu = 4 };
+
+__device__ __forceinline__ int n_phases(int kind) { return kind == kLayerFA ? 6 : kind == kLayerGDN ? 5 : 1; }
+__device__ __forceinline__ int phase_type(int kind, int p) {
+  if (kind == kLayerFA) return p == 1 ? kPhAttn : p == 2 ? kPhCombine : kPhGemv;
+  if (kind == kLayerGDN) return p == 1 ? kPhGdn : kPhGemv;
+  return kPhGemv;
+}
+
+// ------------------------------------------------------------------ shared memory
+
+extern __shared__ __align__(1024) uint8_t smem_raw[];
+
+struct Smem {
+  uint8_t* ring;
+  uint64_t* full;
+  uint64_t* empty;
+  float* misc;   // 256 floats (1 KiB): reductions, gate/beta
+  uint8_t* uni;  // per-phase buffer (kDecUnion bytes)
+};
+
+__device__ __forceinline__ Smem smem_map(uint8_t* base) {
+  Smem s;
+  s.ring = base;
+  s.full = reinterpret_cast<uint64_t*>(base + kDecStages * kDecStage);
+  s.empty = s.full + kDecStages;
+  s.misc = reinterpret_cast<float*>(s.empty + kDecStages);
+  s.uni = reinterpret_cast<uint8_t*>(s.misc + 256);
+  return s;
+}
+
+__device__ __forceinline__ void consumer_sync() { named_barrier(1, NCT); }
+
+// misc[255]: the device position, read once per CTA when the launch starts (every
+// phase of the launch sees the same value although CTA 0 advances it at the end)
+__device__ __forceinline__ int32_t launch_pos() {
+  return reinterpret_cast<const int32_t*>(smem_map(smem_raw).misc)[255];
+}
+
+// ------------------------------------------------------------------ grid barrier
+
+// All CTAs' consumers: arrive on a counter that starts at zero for the launch and
+// wait until it reaches `target` (G per barrier passed). Bounded to 1 s; on expiry
+// the status word records a timeout and the CTA continues (its results are then
+// meaningless, but nothing hangs).
+__device__ __forceinline__ void grid_sync(const Program& P, uint32_t target) {
+  consumer_sync();
+  if (threadIdx.x == 0) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(P.barrier) : "memory");
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(P.barrier) : "memory");
+    if (v < target) {
+      const uint64_t t0 = global_ns();
+      while (true) {
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(P.barrier) : "memory");
+        if (v >= target) break;
+        if (global_ns() - t0 > kWaitNs) {
+          set_status(P.status, kStatusTimeout);
+          break;
+        }
+        __nanosleep(32);
+      }
+    }
+  }
+  consumer_sync();
+}
+
+// ------------------------------------------------------------------ bf16 helpers
+
+__device__ __forceinline__ void unpack8(const uint4 u, float* x) {
+  x[0] = bf16lo(u.x); x[1] = bf16hi(u.x);
+  x[2] = bf16lo(u.y); x[3] = bf16hi(u.y);
+  x[4] = bf16lo(u.z); x[5] = bf16hi(u.z);
+  x[6] = bf16lo(u.w); x[7] = bf16hi(u.w);
+}
+__device__ __forceinline__ void load16(const uint16_t* p, float* x) {
+  unpack8(*reinterpret_cast<const uint4*>(p), x);
+  unpack8(*reinterpret_cast<const uint4*>(p + 8), x + 8);
+}
+template <int EPL>
+__device__ __forceinline__ void load_row(const uint16_t* p, float* x) {
+  if constexpr (EPL == 8) {
+    unpack8(*reinterpret_cast<const uint4*>(p), x);
+  } else if constexpr (EPL == 4) {
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    x[0] = bf16lo(u.x); x[1] = bf16hi(u.x); x[2] = bf16lo(u.y); x[3] = bf16hi(u.y);
+  } else {
+    const uint32_t u = *reinterpret_cast<const uint32_t*>(p);
+    x[0] = bf16lo(u); x[1] = bf16hi(u);
+  }
+}
+
+// ------------------------------------------------------------------ GEMV phases
+
+struct XQ {
+  uint32_t hi[4], lo[4];
+  int qsum128;  // 128 * sum q
+  float scale;  // 2^(e-15)
+};
+
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ uint32_t dp4a_uu(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+__device__ __forceinline__ void quantize16(const float* v, XQ& q) {
+  float amax = 0.f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(v[j]));
+  // amax = m 2^e, 0.5 <= m < 1, e = E - 126 for the biased exponent E; scale 2^(e-15).
+  // A chunk whose largest element is below 2^-112 counts as zero.
+  const uint32_t E = __float_as_uint(amax) >> 23;
+  const bool nz = E >= 15;
+  const float up = __uint_as_float((268u - (nz ? E : 15u)) << 23);  // 2^(15-e)
+  q.scale = nz ? __uint_as_float((E - 14u) << 23) : 0.f;
+  int qs = 0;
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    uint32_t hi = 0, lo = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      int t = nz ? __float2int_rn(v[4 * w + j] * up) : 0;
+      t = max(-32768, min(32767, t));
+      qs += t;
+      hi |= (uint32_t)((t >> 8) & 0xFF) << (8 * j);
+      lo |= (uint32_t)(t & 0xFF) << (8 * j);
+    }
+    q.hi[w] = hi;
+    q.lo[w] = lo;
+  }
+  q.qsum128 = 128 * qs;
+}
+
+__device__ __forceinline__ float dot16(const uint4 w, const XQ& q) {
+  int ah = 0;
+  uint32_t al = (uint32_t)(-q.qsum128);
+  ah = dp4a_us(w.x, q.hi[0], ah);
+  al = dp4a_uu(w.x, q.lo[0], al);
+  ah = dp4a_us(w.y, q.hi[1], ah);
+  al = dp4a_uu(w.y, q.lo[1], al);
+  ah = dp4a_us(w.z, q.hi[2], ah);
+  al = dp4a_uu(w.z, q.lo[2], al);
+  ah = dp4a_us(w.w, q.hi[3], ah);
+  al = dp4a_uu(w.w, q.lo[3], al);
+  return (float)(ah * 256 + (int)al) * q.scale;
+}
+
+// Sum over the 32 lanes of v[0..3]; lane L ends with the total of v[2*b4 + b3].
+__device__ __forceinline__ float reduce4(const float* v, uint32_t lane) {
+  const bool b4 = lane & 16, b3 = lane & 8;
+  const float w0 = (b4 ? v[2] : v[0]) + __shfl_xor_sync(FULLMASK, b4 ? v[0] : v[2], 16);
+  const float w1 = (b4 ? v[3] : v[1]) + __shfl_xor_sync(FULLMASK, b4 ? v[1] : v[3], 16);
+  float z = (b3 ? w1 : w0) + __shfl_xor_sync(FULLMASK, b3 ? w0 : w1, 8);
+  z += __shfl_xor_sync(FULLMASK, z, 4);
+  z += __shfl_xor_sync(FULLMASK, z, 2);
+  z += __shfl_xor_sync(FULLMASK, z, 1);
+  return z;
+}
+template <typename T>
+__device__ __forceinline__ T sel4(const T* v, uint32_t j) {
+  return j == 0 ? v[0] : j == 1 ? v[1] : j == 2 ? v[2] : v[3];
+}
+
+// Warps per row W (a divisor of the consumer warps) and 16-element chunks per lane
+// (at most 5): the fewest wasted chunk slots, then the fewest warps per row.
+__host__ __device__ inline void pick_split(uint32_t nch, uint32_t& W, uint32_t& cpl) {
+  const uint32_t divs[6] = {1, 2, 3, 4, 6, 12};
+  W = 0;
+  cpl = 0;
+  uint32_t best = 0xffffffffu;
+  for (uint32_t i = 0; i < 6; ++i) {
+    const uint32_t w = divs[i], c = (nch + 32 * w - 1) / (32 * w);
+    if (c > 5) continue;
+    const uint32_t waste = c * 32 * w - nch;
+    if (waste < best) {
+      best = waste;
+      W = w;
+      cpl = c;
+    }
+  }
+}
+
+struct Gemv {
+  QMat seg[4];
+  uint16_t* out[4];
+  uint32_t row0[5];  // prefix sums of the segments' rows
+  uint32_t nseg, K;
+  int pro, epi;
+  const uint16_t *a, *b, *nw;
+  uint16_t* resid_out;
+  const uint16_t* resid_in;
+  uint32_t head_dim;
+  uint32_t W, cpl, R, gstride, scale_off, bias_off;
+};
+
+__device__ __forceinline__ void gemv_add(Gemv& g, const QMat& m, uint16_t* out) {
+  g.seg[g.nseg] = m;
+  g.out[g.nseg] = out;
+  g.row0[g.nseg + 1] = g.row0[g.nseg] + m.n;
+  ++g.nseg;
+}
+
+// The GEMV of phase p of layer l.
+__device__ __noinline__ Gemv gemv_of(const Program& P, const LayerDesc& L, uint32_t l, int p) {
+  Gemv g;
+  g.nseg = 0;
+  g.row0[0] = 0;
+  g.b = nullptr;
+  g.nw = nullptr;
+  g.resid_out = nullptr;
+  g.resid_in = nullptr;
+  g.head_dim = 0;
+  g.epi = 0;
+  uint8_t* S = P.scratch;
+  const ScratchMap& m = P.sm;
+  const uint16_t* xin = l == 0 ? P.x_in : P.x_out;
+  auto at = [&](uint32_t off) { return reinterpret_cast<uint16_t*>(S + off); };
+  const bool fa = L.kind == kLayerFA;
+  const int mlp0 = fa ? 4 : 3;  // the gate|up phase
+  if (L.kind == kLayerGemv) {
+    g.K = P.E;
+    g.pro = kPlain;
+    g.a = P.x_in;
+    gemv_add(g, L.m[0], P.x_out);
+  } else if (p == 0) {
+    g.K = P.E;
+    g.pro = kRms;
+    g.a = xin;
+    g.nw = L.input_ln;
+    if (fa) {
+      gemv_add(g, L.m[0], at(m.q_full));
+      gemv_add(g, L.m[1], at(m.k));
+      gemv_add(g, L.m[2], at(m.v));
+    } else {
+      gemv_add(g, L.m[0], at(m.dt_raw));
+      gemv_add(g, L.m[1], at(m.b_raw));
+      gemv_add(g, L.m[2], at(m.qkv));
+      gemv_add(g, L.m[3], at(m.z));
+    }
+  } else if (p == mlp0) {
+    g.K = P.E;
+    g.pro = kAddRms;
+    g.a = xin;
+    g.b = at(fa ? m.o : m.out);
+    g.nw = L.post_ln;
+    g.resid_out = at(m.x_resid);
+    gemv_add(g, L.m[4], at(m.g));
+    gemv_add(g, L.m[5], at(m.u));
+  } else if (p == mlp0 + 1) {
+    g.K = P.I;
+    g.pro = kSiluMul;
+    g.epi = 1;
+    g.a = at(m.g);
+    g.b = at(m.u);
+    g.resid_in = at(m.x_resid);
+    gemv_add(g, L.m[6], P.x_out);
+  } else if (fa) {  // p == 3: o_proj
+    g.K = P.H * P.D;
+    g.pro = kPlain;
+    g.a = at(m.ga);
+    gemv_add(g, L.m[3], at(m.o));
+  } else {  // p == 2: out_proj on silu(z) * RMSNorm_head(y)
+    g.K = P.Z;
+    g.pro = kHeadNormSilu;
+    g.a = at(m.y);
+    g.b = at(m.z);
+    g.nw = L.norm_weight;
+    g.head_dim = P.Dv;
+    gemv_add(g, L.m[7], at(m.out));
+  }
+  pick_split(g.K / 16, g.W, g.cpl);
+  g.R = NCW / g.W;
+  g.gstride = ((g.K / 64 + 7) / 8) * 8;
+  g.scale_off = (g.R * g.K + 15) / 16 * 16;
+  g.bias_off = g.scale_off + g.R * g.gstride * 2;
+  return g;
+}
+
+struct Tile {
+  uint32_t r, nr, seg;
+};
+// The CTA's rows [r, re) cut into tiles of at most R rows, never across a segment end.
+__device__ __forceinline__ bool next_tile(const Gemv& g, uint32_t& r, uint32_t re, uint32_t& seg, Tile& t) {
+  if (r >= re) return false;
+  while (r >= g.row0[seg + 1]) ++seg;
+  const uint32_t end = min(re, g.row0[seg + 1]);
+  t.r = r;
+  t.nr = min(g.R, end - r);
+  t.seg = seg;
+  r += t.nr;
+  return true;
+}
+
+__device__ __forceinline__ void cta_rows(uint32_t total, uint32_t& rb, uint32_t& re) {
+  rb = (uint32_t)(((uint64_t)total * blockIdx.x) / gridDim.x);
+  re = (uint32_t)(((uint64_t)total * (blockIdx.x + 1)) / gridDim.x);
+}
+
+// Form the phase's input vector once per CTA and store it, quantised, in shared
+// memory: chunk c at hi[c], lo[c] (uint4 each) and aux[c] = {qsum128, scale, sum x}.
+__device__ __noinline__ void gemv_prologue(const Program& P, const Gemv& g, const Smem& sh) {
+  const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t nch = g.K / 16;
+  uint4* qhi = reinterpret_cast<uint4*>(sh.uni);
+  uint4* qlo = qhi + nch;
+  float4* aux = reinterpret_cast<float4*>(qlo + nch);
+  float raw[2][16];
+  float ss = 0.f;
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const uint32_t c = tid + q * NCT;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) raw[q][j] = 0.f;
+    if (c < nch) {
+      load16(g.a + c * 16, raw[q]);
+      if (g.pro == kAddRms) {
+        float xb[16];
+        load16(g.b + c * 16, xb);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) raw[q][j] = round_bf16(raw[q][j] + xb[j]);
+        if (blockIdx.x == 0) {  // one CTA keeps x_resid for the down projection's residual
+          uint32_t pk[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            pk[j] = (uint32_t)to_bf16(raw[q][2 * j]) | ((uint32_t)to_bf16(raw[q][2 * j + 1]) << 16);
+          uint4* dst = reinterpret_cast<uint4*>(g.resid_out + c * 16);
+          dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) ss = fmaf(raw[q][j], raw[q][j], ss);
+    }
+  }
+  float inv = 0.f;
+  if (g.pro == kRms || g.pro == kAddRms) {
+    ss = warp_sum(ss);
+    if (lane == 0) sh.misc[warp] = ss;
+    consumer_sync();
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < NCW; ++w) tot += sh.misc[w];
+    inv = rsqrtf(tot / (float)g.K + P.eps);
+  }
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const uint32_t c = tid + q * NCT;
+    if (q == 1 && NCT >= nch) break;  // (uniform) no second chunk anywhere
+    float v[16];
+    if (g.pro == kHeadNormSilu) {
+      // a head's chunks sit on adjacent lanes: reduce its sum of squares there
+      float hs = 0.f;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) hs = fmaf(raw[q][j], raw[q][j], hs);
+      for (uint32_t o = 1; o < g.head_dim / 16; o <<= 1) hs += __shfl_xor_sync(FULLMASK, hs, o);
+      const float hi = rsqrtf(hs / (float)g.head_dim + P.eps);
+      if (c < nch) {
+        float xb[16], w[16];
+        load16(g.b + c * 16, xb);
+        load16(g.nw + (c * 16) % g.head_dim, w);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = silu_fast(xb[j]) * round_bf16(raw[q][j] * hi * w[j]);
+      }
+    } else if (c < nch) {
+      if (g.pro == kPlain) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = raw[q][j];
+      } else if (g.pro == kSiluMul) {
+        float xb[16];
+        load16(g.b + c * 16, xb);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = silu_fast(raw[q][j]) * xb[j];
+      } else {  // RMSNorm (plain or after the residual add)
+        float w[16];
+        load16(g.nw + c * 16, w);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = round_bf16(raw[q][j] * inv * w[j]);
+      }
+    }
+    if (c < nch) {
+      XQ x;
+      quantize16(v, x);
+      float s = 0.f;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) s += v[j];
+      qhi[c] = make_uint4(x.hi[0], x.hi[1], x.hi[2], x.hi[3]);
+      qlo[c] = make_uint4(x.lo[0], x.lo[1], x.lo[2], x.lo[3]);
+      aux[c] = make_float4(__int_as_float(x.qsum128), x.scale, s, 0.f);
+    }
+  }
+  consumer_sync();
+}
+
+// The row loop of a GEMV phase. The description is copied into registers first:
+// the mbarrier operations' memory clobbers would otherwise reload it from shared
+// memory on every tile.
+constexpr bool kEarlyRelease = false;
+template <int CPL>
+__device__ __noinline__ void gemv_main(const Gemv& gs, const Smem& sh, uint32_t& it, int* status, bool& dead) {
+  const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t K = gs.K, W = gs.W, R = gs.R, gstride = gs.gstride, soff = gs.scale_off, boff = gs.bias_off;
+  const uint32_t nseg = gs.nseg, epi = gs.epi;
+  uint32_t row0[5];
+#pragma unroll
+  for (int i = 0; i < 5; ++i) row0[i] = gs.row0[i];
+  const uint32_t kp = warp % W, rs = warp / W, nch = K / 16;
+  const uint4* qhi = reinterpret_cast<const uint4*>(sh.uni);
+  const uint4* qlo = qhi + nch;
+  const float4* aux = reinterpret_cast<const float4*>(qlo + nch);
+  // chunk c of this lane is ch0 + c * cstep; chunks past the row end read chunk 0
+  // (valid memory) against x = 0, so the loops are branch-free
+  const uint32_t ch0 = lane + 32 * kp, cstep = 32 * W;
+  auto chk = [&](int c) { const uint32_t ch = ch0 + c * cstep; return ch < nch ? ch : 0u; };
+  XQ xq[CPL];
+  float xs[CPL];
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) {
+    const bool valid = ch0 + c * cstep < nch;
+    const uint4 h = qhi[chk(c)], l = qlo[chk(c)];
+    const float4 x = aux[chk(c)];
+    xq[c].hi[0] = valid ? h.x : 0u; xq[c].hi[1] = valid ? h.y : 0u;
+    xq[c].hi[2] = valid ? h.z : 0u; xq[c].hi[3] = valid ? h.w : 0u;
+    xq[c].lo[0] = valid ? l.x : 0u; xq[c].lo[1] = valid ? l.y : 0u;
+    xq[c].lo[2] = valid ? l.z : 0u; xq[c].lo[3] = valid ? l.w : 0u;
+    xq[c].qsum128 = valid ? __float_as_int(x.x) : 0;
+    xq[c].scale = valid ? x.y : 0.f;
+    xs[c] = valid ? x.z : 0.f;
+  }
+  const uint32_t total = row0[nseg];
+  const uint32_t rb = (uint32_t)(((uint64_t)total * blockIdx.x) / gridDim.x);
+  const uint32_t re = (uint32_t)(((uint64_t)total * (blockIdx.x + 1)) / gridDim.x);
+  uint32_t r = rb, batch = 0;
+  const uint32_t jl = ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1);
+  float* red = sh.misc + 32;  // [2][4][NCW]
+  while (true) {
+    float acc[4];
+    uint32_t tile[4];  // row start | rows << 24 (rows <= 12; row starts < 2^24)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      acc[j] = 0.f;
+      tile[j] = 0;
+      if (r < re) {
+        // the tile: up to R rows, never across a segment end
+        uint32_t sg = 0;
+#pragma unroll
+        for (int i = 1; i < 4; ++i) sg += (i < (int)nseg && r >= row0[i]) ? 1u : 0u;
+        const uint32_t end = min(re, sg == 0 ? row0[1] : sg == 1 ? row0[2] : sg == 2 ? row0[3] : row0[4]);
+        const uint32_t nr = min(R, end - r);
+        tile[j] = r | (nr << 24);
+        r += nr;
+        const uint32_t st = it % kDecStages;
+        if (!dead && !mbar_wait(&sh.full[st], (it / kDecStages) & 1)) {
+          set_status(status, kStatusTimeout);
+          dead = true;
+        }
+        if (!dead && rs < nr) {
+          const uint8_t* sb = sh.ring + st * kDecStage;
+          const uint8_t* crow = sb + rs * K;
+          const uint16_t* srow = reinterpret_cast<const uint16_t*>(sb + soff) + rs * gstride;
+          const uint16_t* brow = reinterpret_cast<const uint16_t*>(sb + boff) + rs * gstride;
+          uint4 w[CPL];
+          float s[CPL], b[CPL];
+#pragma unroll
+          for (int c = 0; c < CPL; ++c) {  // all shared-memory loads first
+            w[c] = *reinterpret_cast<const uint4*>(crow + chk(c) * 16);
+            s[c] = bf16f(srow[chk(c) >> 2]);
+            b[c] = bf16f(brow[chk(c) >> 2]);
+          }
+          if (kEarlyRelease) {  // the row is in registers: release the stage before the arithmetic
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh.empty[st]);
+          }
+          float part[CPL];
+#pragma unroll
+          for (int c = 0; c < CPL; ++c) part[c] = fmaf(s[c], dot16(w[c], xq[c]), fmaf(128.0f, s[c], b[c]) * xs[c]);
+#pragma unroll
+          for (int c = 1; c < CPL; ++c) part[0] += part[c];
+          acc[j] = part[0];
+          if (!kEarlyRelease) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh.empty[st]);
+          }
+        } else {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sh.empty[st]);
+        }
+        ++it;
+      }
+    }
+    if (tile[0] == 0) break;
+    const float tot = reduce4(acc, lane);
+    const uint32_t tl = sel4(tile, jl), r0 = tl & 0xFFFFFFu, n0 = tl >> 24;
+    bool store = false;
+    float y = tot;
+    if (W == 1) {
+      store = (lane & 7) == 0 && rs < n0;
+    } else {
+      float* buf = red + (batch & 1) * 4 * NCW;
+      if ((lane & 7) == 0) buf[jl * NCW + warp] = tot;
+      consumer_sync();
+      if (kp == 0 && (lane & 7) == 0 && rs < n0) {
+        y = 0.f;
+        for (uint32_t w2 = 0; w2 < W; ++w2) y += buf[jl * NCW + rs * W + w2];
+        store = true;
+      }
+    }
+    if (store && !dead) {
+      const uint32_t row = r0 + rs;
+      uint32_t sg = 0;
+#pragma unroll
+      for (int i = 1; i < 4; ++i) sg += (i < (int)nseg && row >= row0[i]) ? 1u : 0u;
+      const uint32_t base = sg == 0 ? row0[0] : sg == 1 ? row0[1] : sg == 2 ? row0[2] : row0[3];
+      const uint32_t local = row - base;
+      if (epi == 1) y += bf16f(gs.resid_in[local]);
+      gs.out[sg][local] = to_bf16(y);
+    }
+    ++batch;
+    if (tile[3] == 0) break;
+  }
+}
+
+__device__ void gemv_rows(const Program& P, const Gemv& g, const Smem& sh, uint32_t& it, bool& dead) {
+  switch (g.cpl) {
+    case 1: gemv_main<1>(g, sh, it, P.status, dead); break;
+    case 2: gemv_main<2>(g, sh, it, P.status, dead); break;
+    case 3: gemv_main<3>(g, sh, it, P.status, dead); break;
+    case 4: gemv_main<4>(g, sh, it, P.status, dead); break;
+    default: gemv_main<5>(g, sh, it, P.status, dead); break;
+  }
+  consumer_sync();  // the x chunks in shared memory are free again
+}
+
+// ------------------------------------------------------------------ attention phases
+
+struct Span {
+  uint32_t pos, S, t0, t1, tc_end, ntiles;
+  bool ok, has_fresh;
+};
+
+// The device position as this CTA read it at kernel start (shared memory).
+__device__ __forceinline__ int32_t launch_pos();
+
+__device__ __forceinline__ Span attn_span(const Program& P, uint32_t capacity) {
+  Span sp;
+  if (P.d_pos) {
+    const int32_t p = launch_pos();
+    const uint32_t lim = min(capacity, P.max_seq);
+    sp.ok = p >= 0 && (uint32_t)p < lim;
+    sp.pos = sp.ok ? (uint32_t)p : 0;
+    sp.S = sp.pos + 1;
+  } else {
+    sp.ok = P.pos < capacity;
+    sp.pos = P.pos;
+    sp.S = P.S;
+  }
+  const uint32_t s = blockIdx.x;
+  const bool mine = s < P.P && sp.ok;
+  sp.t0 = mine ? (uint32_t)(((uint64_t)sp.S * s) / P.P) : 0;
+  sp.t1 = mine ? (uint32_t)(((uint64_t)sp.S * (s + 1)) / P.P) : 0;
+  sp.has_fresh = mine && sp.S == sp.pos + 1 && sp.pos >= sp.t0 && sp.pos < sp.t1;
+  sp.tc_end = sp.has_fresh ? sp.pos : sp.t1;
+  sp.ntiles = (mine && sp.tc_end > sp.t0) ? (sp.tc_end - sp.t0 + kTS - 1) / kTS : 0;
+  return sp;
+}
+
+// RMSNorm over one head (this lane's EPL elements at d = lane*EPL), rounded to bf16,
+// then RoPE on dims [0, R) with rotate-half pairing, rounded to bf16.
+template <int EPL>
+__device__ __forceinline__ void norm_rope(float* x, const uint16_t* w, const Program& P, uint32_t pos, float* buf,
+                                          uint32_t lane) {
+  const uint32_t D = EPL * 32, R = P.R, half = R / 2;
+  float ss = 0.f;
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) ss = fmaf(x[e], x[e], ss);
+  ss = warp_sum(ss);
+  const float inv = rsqrtf(ss / (float)D + P.eps);
+  float wv[EPL];
+  load_row<EPL>(w + lane * EPL, wv);
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) {
+    x[e] = round_bf16(x[e] * inv * wv[e]);
+    buf[lane * EPL + e] = x[e];
+  }
+  __syncwarp();
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) {
+    const uint32_t d = lane * EPL + e;
+    if (d < R) {
+      const uint32_t i = d < half ? d : d - half;
+      float sn, cs;
+      sincosf((float)pos * P.inv_freq[i], &sn, &cs);
+      x[e] = d < half ? round_bf16(buf[d] * cs - buf[d + half] * sn) : round_bf16(buf[d] * cs + buf[d - half] * sn);
+    }
+  }
+  __syncwarp();
+}
+
+// Sum over the 32 lanes of v[0..NV-1] (NV = 8, 16 or 32), each step handing half of
+// the remaining values to the partner lane; lane L ends with the total of
+// v[L >> (5 - log2 NV)].
+template <int NV>
+__device__ __forceinline__ float reduce_transposed(float* v, uint32_t lane) {
+  int n = NV;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    if (n > 1) {
+      const bool up = lane & o;
+      const int h = n / 2;
+#pragma unroll
+      for (int i = 0; i < NV / 2; ++i) {
+        if (i < h) {
+          const float keep = up ? v[i + h] : v[i];
+          const float send = up ? v[i] : v[i + h];
+          v[i] = keep + __shfl_xor_sync(FULLMASK, send, o);
+        }
+      }
+      n = h;
+    } else {
+      v[0] += __shfl_xor_sync(FULLMASK, v[0], o);
+    }
+  }
+  return v[0];
+}
+
+// Split-KV attention of one split (CTA). Warp w serves the HPW consecutive q-heads
+// of head group w % NG (one kv-head) and every TI-th tile, TI = 16 / NG; the TI
+// partial softmax states of a head group are merged in shared memory at the end.
+template <int D, int HPW>
+__device__ __noinline__ void attn_consume(const Program& P, const LayerDesc& L, const Smem& sh, uint32_t& it, bool& dead) {
+  constexpr int EPL = D / 32;
+  constexpr int NV = HPW * kTS;
+  constexpr int SH = NV == 8 ? 2 : NV == 16 ? 1 : 0;
+  const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t s = blockIdx.x;
+  const Span sp = attn_span(P, L.capacity);
+  const uint32_t H = P.H, Hkv = P.Hkv, rowh = Hkv * D, rowbytes = rowh * 2;
+  const uint32_t NG = H / HPW, TI = NCW / NG;  // warps beyond NG * TI only keep the ring moving
+  if (!sp.ok) {
+    if (s == 0 && threadIdx.x == 0) set_status(P.status, kStatusRange);
+    return;
+  }
+  if (s >= P.P) return;
+  float* fresh = reinterpret_cast<float*>(sh.uni);    // k then v, [Hkv][D] each
+  float* buf = fresh + 2 * rowh;                      // per-warp [D] for RoPE, then merge space
+  // the new token's k (normed, rotated) and v: appended by exactly one CTA
+  const bool appender = sp.has_fresh || (sp.S != sp.pos + 1 && s == 0);
+  if (appender) {
+    for (uint32_t g = warp; g < Hkv; g += NCW) {
+      float kx[EPL], vx[EPL];
+      load_row<EPL>(reinterpret_cast<const uint16_t*>(P.scratch + P.sm.k) + g * D + lane * EPL, kx);
+      load_row<EPL>(reinterpret_cast<const uint16_t*>(P.scratch + P.sm.v) + g * D + lane * EPL, vx);
+      norm_rope<EPL>(kx, L.k_norm, P, sp.pos, buf + warp * D, lane);
+      uint16_t* kd = L.kc + (size_t)sp.pos * rowh + g * D + lane * EPL;
+      uint16_t* vd = L.vc + (size_t)sp.pos * rowh + g * D + lane * EPL;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) {
+        fresh[g * D + lane * EPL + e] = kx[e];
+        fresh[rowh + g * D + lane * EPL + e] = vx[e];
+        kd[e] = to_bf16(kx[e]);
+        vd[e] = to_bf16(vx[e]);
+      }
+    }
+  }
+  const uint32_t hg = warp % NG, ti = warp / NG;
+  const bool active = ti < TI;
+  const uint32_t h0 = hg * HPW, g = h0 / (H / Hkv);
+  float q[HPW][EPL], m[HPW], l[HPW], acc[HPW][EPL];
+  const uint16_t* qf = reinterpret_cast<const uint16_t*>(P.scratch + P.sm.q_full);
+#pragma unroll
+  for (int j = 0; j < HPW; ++j) {
+    m[j] = -INFINITY;
+    l[j] = 0.f;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) acc[j][e] = 0.f;
+    load_row<EPL>(qf + (size_t)(h0 + j) * 2 * D + lane * EPL, q[j]);
+    if (active) norm_rope<EPL>(q[j], L.q_norm, P, sp.pos, buf + warp * D, lane);
+  }
+  consumer_sync();  // the fresh row is visible to every warp; the RoPE buffers are free
+
+  const uint32_t midx = lane >> SH, mj = midx / kTS, mt = midx % kTS;
+  for (uint32_t i = 0; i < sp.ntiles; ++i) {
+    const uint32_t st = it % kDecStages;
+    const bool mine = active && (i % TI) == ti;
+    // every warp waits for every tile before releasing it, so no warp can run a
+    // ring round ahead and complete a slot's release early
+    if (!dead && !mbar_wait(&sh.full[st], (it / kDecStages) & 1)) {
+      set_status(P.status, kStatusTimeout);
+      dead = true;
+    }
+    if (mine && !dead) {
+      const uint8_t* base = sh.ring + st * kDecStage;
+      const uint32_t n = min((uint32_t)kTS, sp.tc_end - (sp.t0 + i * kTS));
+      float d[NV];
+#pragma unroll
+      for (int t = 0; t < kTS; ++t) {  // rows t >= n hold stale data: their scores are masked
+        float kf[EPL];
+        load_row<EPL>(reinterpret_cast<const uint16_t*>(base + t * rowbytes) + g * D + lane * EPL, kf);
+#pragma unroll
+        for (int j = 0; j < HPW; ++j) {
+          float x = 0.f;
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) x = fmaf(q[j][e], kf[e], x);
+          d[j * kTS + t] = x;
+        }
+      }
+      float sc = reduce_transposed<NV>(d, lane) * P.scale_log2;
+      sc = mt < n ? sc : -INFINITY;
+      float mx = sc;
+#pragma unroll
+      for (int o = 1 << SH; o < (kTS << SH); o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(FULLMASK, mx, o));
+      float mold = m[0];
+#pragma unroll
+      for (int j = 1; j < HPW; ++j) mold = mj == (uint32_t)j ? m[j] : mold;
+      const float mnew = fmaxf(mold, mx);
+      const float p = exp2f(sc - mnew);
+      float ps = p;
+#pragma unroll
+      for (int o = 1 << SH; o < (kTS << SH); o <<= 1) ps += __shfl_xor_sync(FULLMASK, ps, o);
+#pragma unroll
+      for (int j = 0; j < HPW; ++j) {
+        const float mn = __shfl_sync(FULLMASK, mnew, (j * kTS) << SH);
+        const float sum = __shfl_sync(FULLMASK, ps, (j * kTS) << SH);
+        const float corr = exp2f(m[j] - mn);
+        l[j] = fmaf(l[j], corr, sum);
+        m[j] = mn;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) acc[j][e] *= corr;
+      }
+      for (uint32_t t = 0; t < n; ++t) {
+        float vf[EPL];
+        load_row<EPL>(reinterpret_cast<const uint16_t*>(base + (kTS + t) * rowbytes) + g * D + lane * EPL, vf);
+#pragma unroll
+        for (int j = 0; j < HPW; ++j) {
+          const float pj = __shfl_sync(FULLMASK, p, (j * kTS + t) << SH);
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) acc[j][e] = fmaf(pj, vf[e], acc[j][e]);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sh.empty[st]);  // every warp releases every tile
+    ++it;
+  }
+  if (sp.has_fresh && ti == 0) {
+    float kf[EPL], vf[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+      kf[e] = fresh[g * D + lane * EPL + e];
+      vf[e] = fresh[rowh + g * D + lane * EPL + e];
+    }
+#pragma unroll
+    for (int j = 0; j < HPW; ++j) {
+      float x = 0.f;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) x = fmaf(q[j][e], kf[e], x);
+      const float sc = warp_sum(x) * P.scale_log2;
+      const float mn = fmaxf(m[j], sc);
+      const float corr = exp2f(m[j] - mn), pp = exp2f(sc - mn);
+      l[j] = fmaf(l[j], corr, pp);
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) acc[j][e] = fmaf(acc[j][e], corr, pp * vf[e]);
+      m[j] = mn;
+    }
+  }
+  // merge the TI partial states of each head group (warps ti > 0 hand theirs over)
+  float* mb = buf;  // [(TI-1) * NG warps][HPW][D + 2]
+  if (active && ti > 0) {
+    float* dst = mb + ((ti - 1) * NG + hg) * HPW * (D + 2);
+#pragma unroll
+    for (int j = 0; j < HPW; ++j) {
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) dst[j * (D + 2) + lane * EPL + e] = acc[j][e];
+      if (lane == 0) {
+        dst[j * (D + 2) + D] = m[j];
+        dst[j * (D + 2) + D + 1] = l[j];
+      }
+    }
+  }
+  consumer_sync();
+  if (ti == 0) {
+    for (uint32_t u = 1; u < TI; ++u) {
+      const float* src = mb + ((u - 1) * NG + hg) * HPW * (D + 2);
+#pragma unroll
+      for (int j = 0; j < HPW; ++j) {
+        const float mu = src[j * (D + 2) + D], lu = src[j * (D + 2) + D + 1];
+        if (mu == -INFINITY) continue;
+        const float mn = fmaxf(m[j], mu);
+        const float c0 = exp2f(m[j] - mn), c1 = exp2f(mu - mn);
+        l[j] = l[j] * c0 + lu * c1;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) acc[j][e] = acc[j][e] * c0 + src[j * (D + 2) + lane * EPL + e] * c1;
+        m[j] = mn;
+      }
+    }
+    float* part_o = reinterpret_cast<float*>(P.scratch + P.sm.part_o);
+    float* part_ml = reinterpret_cast<float*>(P.scratch + P.sm.part_ml);
+#pragma unroll
+    for (int j = 0; j < HPW; ++j) {
+      const uint32_t h = h0 + j;
+      float* po = part_o + ((size_t)s * H + h) * D + lane * EPL;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) po[e] = acc[j][e];
+      if (lane == 0) {
+        part_ml[((size_t)s * H + h) * 2] = m[j];
+        part_ml[((size_t)s * H + h) * 2 + 1] = l[j];
+      }
+    }
+  }
+  consumer_sync();  // the merge space is free again
+}
+
+// Merge of the P partials of (head h, 32 dims) per CTA, then the output gate:
+// ga = bf16(bf16(attn) * sigmoid(gate)).
+__device__ __noinline__ void combine_consume(const Program& P, const LayerDesc& L, const Smem& sh) {
+  const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t nd = P.D / 32, item = blockIdx.x;
+  const Span sp = attn_span(P, L.capacity);
+  if (item >= P.H * nd) return;
+  const uint32_t h = item / nd, d = (item % nd) * 32 + lane;
+  uint16_t* ga = reinterpret_cast<uint16_t*>(P.scratch + P.sm.ga);
+  if (!sp.ok) {
+    if (warp == 0) ga[(size_t)h * P.D + d] = 0;
+    return;
+  }
+  const float* part_o = reinterpret_cast<const float*>(P.scratch + P.sm.part_o);
+  const float* part_ml = reinterpret_cast<const float*>(P.scratch + P.sm.part_ml);
+  float M = -INFINITY, Ls = 0.f, O = 0.f;
+  for (uint32_t base = 0; base < P.P; base += NCW * 4) {
+    float ms[4], ls[4], os[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t sp_ = base + warp + NCW * k;
+      const bool ok = sp_ < P.P;
+      ms[k] = ok ? part_ml[((size_t)sp_ * P.H + h) * 2] : -INFINITY;
+      ls[k] = ok ? part_ml[((size_t)sp_ * P.H + h) * 2 + 1] : 0.f;
+      os[k] = ok ? part_o[((size_t)sp_ * P.H + h) * P.D + d] : 0.f;
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (ms[k] == -INFINITY) continue;  // a split with no tokens
+      const float mn = fmaxf(M, ms[k]);
+      const float c0 = exp2f(M - mn), c1 = exp2f(ms[k] - mn);
+      Ls = Ls * c0 + ls[k] * c1;
+      O = O * c0 + os[k] * c1;
+      M = mn;
+    }
+  }
+  float* part = reinterpret_cast<float*>(sh.uni);  // [3][16][32]
+  part[(0 * NCW + warp) * 32 + lane] = M;
+  part[(1 * NCW + warp) * 32 + lane] = Ls;
+  part[(2 * NCW + warp) * 32 + lane] = O;
+  consumer_sync();
+  if (warp == 0) {
+    M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < NCW; ++w) M = fmaxf(M, part[w * 32 + lane]);
+    Ls = 0.f;
+    O = 0.f;
+#pragma unroll
+    for (int w = 0; w < NCW; ++w) {
+      const float mw = part[w * 32 + lane];
+      if (mw == -INFINITY) continue;
+      const float c = exp2f(mw - M);
+      Ls = fmaf(part[(NCW + w) * 32 + lane], c, Ls);
+      O = fmaf(part[(2 * NCW + w) * 32 + lane], c, O);
+    }
+    const float attn = round_bf16(O / Ls);
+    const uint16_t* qf = reinterpret_cast<const uint16_t*>(P.scratch + P.sm.q_full);
+    const float gate = bf16f(qf[(size_t)h * 2 * P.D + P.D + d]);
+    ga[(size_t)h * P.D + d] = to_bf16(attn * sigmoidf_(gate));
+  }
+  consumer_sync();
+}
+
+// ------------------------------------------------------------------ Gated DeltaNet phase
+
+// Work item (v-head h, 32 state columns j) per CTA. Given the head's q, k, gate and
+// beta, state columns are independent:
+//   u_v = sum_i (g S[i][v]) k_i,  S[i][v] <- g S[i][v] + k_i beta (v_v - u_v),
+//   y_v = sum_i S[i][v] q_i / sqrt(Dk),
+// so the [Dk][32] fp32 slice is read into registers once (before the phase's grid
+// barrier: nothing before it writes the state), updated, and written once.
+constexpr int kGdnWarps = 8;  // warps holding state rows (Dk / 8 rows each)
+
+template <int DK>
+struct GdnPre {
+  float st[DK / kGdnWarps];
+  float cst[kMaxKc], cw[kMaxKc];
+  float alog, dtb;
+  uint32_t ch;
+  bool item, chan;
+};
+
+template <int DK>
+__device__ __forceinline__ void gdn_pre(const Program& P, const LayerDesc& L, GdnPre<DK>& pr) {
+  constexpr int RPT = DK / kGdnWarps;
+  const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+  const uint32_t nsl = P.Dv / 32, item = blockIdx.x;
+  pr.item = item < P.Hv * nsl;
+  pr.chan = false;
+  if (!pr.item) return;
+  const uint32_t h = item / nsl, j = item % nsl, grp = P.Hv / P.Hk, hk = h / grp, v0 = j * 32;
+  if (warp < kGdnWarps) {
+    const float* sp = L.ssm + ((size_t)h * DK + warp * RPT) * P.Dv + v0 + lane;
+#pragma unroll
+    for (int r = 0; r < RPT; ++r) pr.st[r] = sp[(size_t)r * P.Dv];
+  }
+  const uint32_t nch = 2 * DK + 32;
+  if (tid < nch) {
+    pr.chan = true;
+    pr.ch = tid < DK ? hk * DK + tid
+          : tid < 2 * DK ? P.Hk * DK + hk * DK + (tid - DK)
+                         : 2 * P.Hk * DK + h * P.Dv + v0 + (tid - 2 * DK);
+#pragma unroll
+    for (int t = 0; t < kMaxKc; ++t) {
+      pr.cst[t] = t < (int)P.Kc ? L.conv_state[(size_t)pr.ch * P.Kc + t] : 0.f;
+      pr.cw[t] = t < (int)P.Kc ? bf16f(L.conv_w[(size_t)pr.ch * P.Kc + t]) : 0.f;
+    }
+  }
+  pr.alog = L.a_log[h];
+  pr.dtb = bf16f(L.dt_bias[h]);
+}
+
+template <int DK>
+__device__ __noinline__ void gdn_consume(const Program& P, const LayerDesc& L, const Smem& sh, GdnPre<DK>& pr) {
+  constexpr int RPT = DK / kGdnWarps;
+  const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+  if (!pr.item) return;
+  const uint32_t nsl = P.Dv / 32, item = blockIdx.x;
+  const uint32_t h = item / nsl, j = item % nsl, grp = P.Hv / P.Hk, v0 = j * 32;
+  const uint32_t Kc = P.Kc;
+  float* act = reinterpret_cast<float*>(sh.uni);  // [2 Dk + 32]
+  float* red = act + 2 * DK + 32;                 // [2][NCW][32]
+  const uint16_t* qkv = reinterpret_cast<const uint16_t*>(P.scratch + P.sm.qkv);
+  // causal conv update + SiLU
+  if (pr.chan) {
+    const float x = bf16f(qkv[pr.ch]);
+    float o = 0.f;
+#pragma unroll
+    for (int t = 0; t < kMaxKc; ++t) {
+      if (t < (int)Kc) {
+        const float sv = (t + 1 < (int)Kc) ? pr.cst[t + 1] : x;  // shift left, newest last
+        pr.cst[t] = sv;
+        o = fmaf(pr.cw[t], sv, o);
+      }
+    }
+    act[tid] = siluf_(o);
+    // v channels belong to this CTA alone; the q/k channels of a k-head are read by
+    // every CTA of its v-heads, all before the grid barrier that opened this phase,
+    // so one of them may write them now
+    if (tid >= 2 * DK || ((h % grp) == 0 && j == 0)) {
+#pragma unroll
+      for (int t = 0; t < kMaxKc; ++t)
+        if (t < (int)Kc) L.conv_state[(size_t)pr.ch * Kc + t] = pr.cst[t];
+    }
+  }
+  const uint16_t* dtr = reinterpret_cast<const uint16_t*>(P.scratch + P.sm.dt_raw);
+  const uint16_t* brw = reinterpret_cast<const uint16_t*>(P.scratch + P.sm.b_raw);
+  if (tid == 0) {
+    // gate = exp(softplus(dt + dt_bias) * -exp(A_log)); beta = sigmoid(b)
+    const float x = bf16f(dtr[h]) + pr.dtb;
+    const float spl = x > 20.f ? x : log1pf(expf(x));
+    sh.misc[0] = expf(spl * -expf(pr.alog));
+    sh.misc[1] = sigmoidf_(bf16f(brw[h]));
+  }
+  consumer_sync();
+  // per-head L2 norm of q and k (eps 1e-6), then bf16 as qkv_smooth is
+  {
+    float sq = 0.f, sk = 0.f;
+    for (uint32_t i = tid; i < DK; i += NCT) {
+      sq = fmaf(act[i], act[i], sq);
+      sk = fmaf(act[DK + i], act[DK + i], sk);
+    }
+    sq = warp_sum(sq);
+    sk = warp_sum(sk);
+    if (lane == 0) {
+      red[warp] = sq;
+      red[32 + warp] = sk;
+    }
+    consumer_sync();
+    float tq = 0.f, tk = 0.f;
+#pragma unroll
+    for (int w = 0; w < NCW; ++w) {
+      tq += red[w];
+      tk += red[32 + w];
+    }
+    const float iq = rsqrtf(tq + P.l2_eps), ik = rsqrtf(tk + P.l2_eps);
+    consumer_sync();
+    for (uint32_t i = tid; i < 2 * DK + 32; i += NCT) {
+      const float v = act[i];
+      act[i] = round_bf16(i < DK ? v * iq : (i < 2 * DK ? v * ik : v));
+    }
+    consumer_sync();
+  }
+  // delta rule on the slice: thread (warp, lane) of the first 8 warps holds rows
+  // warp*RPT + r of column lane
+  const float g = sh.misc[0], beta = sh.misc[1];
+  const float* qv = act;
+  const float* kv = act + DK;
+  const bool holder = warp < kGdnWarps;
+  float u = 0.f;
+  if (holder) {
+#pragma unroll
+    for (int r = 0; r < RPT; ++r) {
+      pr.st[r] *= g;
+      u = fmaf(pr.st[r], kv[warp * RPT + r], u);
+    }
+    red[warp * 32 + lane] = u;
+  }
+  consumer_sync();
+  u = 0.f;
+#pragma unroll
+  for (int w = 0; w < kGdnWarps; ++w) u += red[w * 32 + lane];
+  const float delta = beta * (act[2 * DK + lane] - u);
+  float y = 0.f;
+  if (holder) {
+#pragma unroll
+    for (int r = 0; r < RPT; ++r) {
+      pr.st[r] = fmaf(kv[warp * RPT + r], delta, pr.st[r]);
+      y = fmaf(pr.st[r], qv[warp * RPT + r], y);
+    }
+    float* sp = L.ssm + ((size_t)h * DK + warp * RPT) * P.Dv + v0 + lane;
+#pragma unroll
+    for (int r = 0; r < RPT; ++r) sp[(size_t)r * P.Dv] = pr.st[r];
+    red[kGdnWarps * 32 + warp * 32 + lane] = y;
+  }
+  consumer_sync();
+  if (warp == 0) {
+    y = 0.f;
+#pragma unroll
+    for (int w = 0; w < kGdnWarps; ++w) y += red[kGdnWarps * 32 + w * 32 + lane];
+    uint16_t* yo = reinterpret_cast<uint16_t*>(P.scratch + P.sm.y);
+    yo[(size_t)h * P.Dv + v0 + lane] = to_bf16(y * P.gdn_out_scale);
+  }
+  consumer_sync();
+}
+
+// ------------------------------------------------------------------ producer schedule
+
+// A walk over the CTA's tiles of the whole launch, phase after phase, in the order
+// the consumers take them. It lives in shared memory: the producer thread's local
+// memory would compete for the small L1 left beside the ring, and a walk step that
+// misses L1 costs several L2 round trips per tile.
+struct Cursor {
+  uint32_t l, lc;  // position; the layer whose description L holds
+  int p;
+  bool open;
+  int ty;
+  LayerDesc L;
+  Gemv g;
+  uint32_t r, re, seg;
+  Span sp;
+  uint32_t i;
+};
+
+// Advance to the next tile and issue its bulk copies into `dst`, completing on
+// `full`; false when the launch has no tiles left (nothing issued).
+__device__ __forceinline__ bool issue_next(const Program& P, const LayerDesc* layers, Cursor& c, uint8_t* dst,
+                                           uint64_t* full, uint64_t pol) {
+  while (c.l < P.n_layers) {
+    if (c.lc != c.l) {
+      c.L = layers[c.l];
+      c.lc = c.l;
+    }
+    if (!c.open) {
+      c.ty = phase_type(c.L.kind, c.p);
+      if (c.ty == kPhGemv) {
+        c.g = gemv_of(P, c.L, c.l, c.p);
+        cta_rows(c.g.row0[c.g.nseg], c.r, c.re);
+        c.seg = 0;
+      } else if (c.ty == kPhAttn) {
+        c.sp = attn_span(P, c.L.capacity);
+        c.i = 0;
+      }
+      c.open = true;
+    }
+    if (c.ty == kPhGemv) {
+      uint32_t r = c.r, seg = c.seg;
+      Tile t;
+      if (next_tile(c.g, r, c.re, seg, t)) {
+        c.r = r;
+        c.seg = seg;
+        const QMat& m = c.g.seg[t.seg];
+        const uint32_t K = c.g.K, gstride = c.g.gstride, local = t.r - c.g.row0[t.seg];
+        const uint32_t cb = t.nr * K, sb = t.nr * gstride * 2;
+        mbar_arrive_expect_tx(full, cb + 2 * sb);
+        bulk_g2s_stream(dst, m.codes + (size_t)local * K, cb, full, pol);
+        bulk_g2s_stream(dst + c.g.scale_off, m.scales + (size_t)local * gstride, sb, full, pol);
+        bulk_g2s_stream(dst + c.g.bias_off, m.biases + (size_t)local * gstride, sb, full, pol);
+        return true;
+      }
+    } else if (c.ty == kPhAttn) {
+      if (c.i < c.sp.ntiles) {
+        const uint32_t rowh = P.Hkv * P.D, rowbytes = rowh * 2;
+        const uint32_t tt = c.sp.t0 + c.i * kTS;
+        const uint32_t n = min((uint32_t)kTS, c.sp.tc_end - tt);
+        mbar_arrive_expect_tx(full, 2 * n * rowbytes);
+        bulk_g2s(dst, c.L.kc + (size_t)tt * rowh, n * rowbytes, full);
+        bulk_g2s(dst + kTS * rowbytes, c.L.vc + (size_t)tt * rowh, n * rowbytes, full);
+        ++c.i;
+        return true;
+      }
+    }
+    c.open = false;
+    if (++c.p >= n_phases(c.L.kind)) {
+      c.p = 0;
+      ++c.l;
+    }
+  }
+  return false;
+}
+
+__device__ __noinline__ void produce_all(const Program& P, const LayerDesc* layers, const Smem& sh, Cursor& c) {
+  const uint64_t pol = policy_evict_first();
+  c.l = 0;
+  c.lc = 0xffffffffu;
+  c.p = 0;
+  c.open = false;
+  uint32_t it = 0;
+  bool dead = false;
+  while (!dead) {
+    const uint32_t st = it % kDecStages;
+    // the stage's previous tile must be consumed; after the last tile this wait
+    // still ends, since the consumers take every tile issued
+    if (it >= (uint32_t)kDecStages && !mbar_wait(&sh.empty[st], ((it / kDecStages) - 1) & 1)) {
+      set_status(P.status, kStatusTimeout);
+      dead = true;
+      break;
+    }
+    if (!issue_next(P, layers, c, sh.ring + st * kDecStage, &sh.full[st], pol)) return;
+    ++it;
+  }
+  // let the copies still in flight land before the CTA can exit
+  const uint32_t first = it > (uint32_t)kDecStages ? it - kDecStages : 0;
+  for (uint32_t j = first; j < it; ++j) mbar_wait(&sh.full[j % kDecStages], (j / kDecStages) & 1);
+}
+
+// ------------------------------------------------------------------ the kernel
+
+// The program's header (everything before the layer table) is copied into shared
+// memory when the launch starts and each layer's description when the consumers
+// reach it: the phase loops then never read the (large) parameter block, whose
+// generic-address reads would miss the constant cache.
+constexpr uint32_t kHeadBytes = (offsetof(Program, layers) + 3) / 4 * 4;
+static_assert(offsetof(Program, layers) % 8 == 0, "layer table alignment");
+
+template <int D, int HPW, int DK>
+__global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_constant__ Program Pk) {
+  __shared__ Gemv gdesc;
+  __shared__ __align__(16) uint8_t head_raw[kHeadBytes];
+  __shared__ LayerDesc Lcur;
+  __shared__ Cursor pcur;  // the producer's walk
+  const Smem sh = smem_map(smem_raw);
+  const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (uint32_t i = threadIdx.x; i < kHeadBytes / 4; i += blockDim.x)  // 4-byte words: the
+    reinterpret_cast<uint32_t*>(head_raw)[i] = reinterpret_cast<const uint32_t*>(&Pk)[i];  // block is 8-aligned
+  const Program& P = *reinterpret_cast<const Program*>(head_raw);  // header fields only
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kDecStages; ++s) {
+      mbar_init(&sh.full[s], 1);
+      mbar_init(&sh.empty[s], NCW);
+    }
+    mbar_fence_init();
+    reinterpret_cast<int32_t*>(sh.misc)[255] = Pk.d_pos ? *Pk.d_pos : 0;
+  }
+  __syncthreads();
+
+  if (warp == NCW) {
+    // ------------------------------------------------ producer: the whole schedule
+    if (lane == 0) produce_all(P, Pk.layers, sh, pcur);
+    return;
+  }
+
+  // -------------------------------------------------- consumers: the phases in order
+  uint32_t it = 0, nbar = 0, ph = 0;
+  bool dead = false;
+  auto mark = [&](uint32_t k) {
+    if (P.trace && threadIdx.x == 0 && ph < P.trace_phases)
+      P.trace[((size_t)blockIdx.x * P.trace_phases + ph) * 4 + k] = global_ns();
+  };
+  for (uint32_t l = 0; l < P.n_layers; ++l) {
+    if (threadIdx.x == 0) Lcur = Pk.layers[l];
+    consumer_sync();
+    const LayerDesc& L = Lcur;
+    const int np = n_phases(L.kind);
+    for (int p = 0; p < np; ++p, ++ph) {
+      const int ty = phase_type(L.kind, p);
+      const bool first = l == 0 && p == 0;
+      mark(0);
+      if (ty == kPhGdn) {
+        GdnPre<DK> pr;
+        gdn_pre<DK>(P, L, pr);  // issued before the barrier: the state is not written before
+        grid_sync(P, ++nbar * gridDim.x);
+        mark(1);
+        gdn_consume<DK>(P, L, sh, pr);
+        mark(2);
+        continue;
+      }
+      if (!first) grid_sync(P, ++nbar * gridDim.x);
+      mark(1);
+      if (ty == kPhGemv) {
+        // the phase's GEMV description, once per CTA, in shared memory
+        if (threadIdx.x == 0) gdesc = gemv_of(P, L, l, p);
+        consumer_sync();
+        gemv_prologue(P, gdesc, sh);
+        mark(3);
+        gemv_rows(P, gdesc, sh, it, dead);
+      }
+      else if (ty == kPhAttn) attn_consume<D, HPW>(P, L, sh, it, dead);
+      else combine_consume(P, L, sh);
+      mark(2);
+    }
+  }
+  consumer_sync();  // Lcur is read to the end of the last phase
+  if (P.advance && blockIdx.x == 0 && threadIdx.x == 0) *P.advance += 1;
+}
+
+using DecodeKernel = void (*)(Program);
+
+template <int D, int HPW>
+DecodeKernel pick_dk(uint32_t Dk) {
+  switch (Dk) {
+    case 32: return decode_kernel<D, HPW, 32>;
+    case 64: return decode_kernel<D, HPW, 64>;
+    case 128: return decode_kernel<D, HPW, 128>;
+  }
+  return nullptr;
+}
+template <int D>
+DecodeKernel pick_h(uint32_t hpw, uint32_t Dk) {
+  switch (hpw) {
+    case 1: return pick_dk<D, 1>(Dk);
+    case 2: return pick_dk<D, 2>(Dk);
+  }
+  return nullptr;
+}
+DecodeKernel pick(uint32_t D, uint32_t hpw, uint32_t Dk) {
+  switch (D) {
+    case 64: return pick_h<64>(hpw, Dk);
+    case 128: return pick_h<128>(hpw, Dk);
+    case 256: return pick_h<256>(hpw, Dk);
+  }
+  return nullptr;
+}
+
+// q-heads per attention warp: 2 when the heads pair up within a kv-head, else 1;
+// there must be no more head groups (H / HPW) than consumer warps.
+uint32_t attn_hpw(uint32_t H, uint32_t Hkv) {
+  if (Hkv && H % Hkv == 0 && (H / Hkv) % 2 == 0 && H / 2 <= (uint32_t)NCW) return 2;
+  if (H <= (uint32_t)NCW) return 1;
+  return 0;
+}
+
+}  // namespace
+
+bool decode_dims_ok(const Program& p, bool has_fa, bool has_gdn) {
+  auto gemv_ok = [](uint32_t K) {
+    if (K == 0 || K % 64 || K > 12288) return false;
+    const uint32_t nch = K / 16;
+    uint32_t W, cpl;
+    pick_split(nch, W, cpl);
+    if (W == 0) return false;
+    const uint32_t R = NCW / W, gs = ((K / 64 + 7) / 8) * 8;
+    const uint32_t stage = (R * K + 15) / 16 * 16 + 2 * R * gs * 2;
+    return stage <= (uint32_t)kDecStage && nch * 48 <= (uint32_t)kDecUnion;
+  };
+  if (!gemv_ok(p.E) || !gemv_ok(p.I)) return false;
+  if (has_fa) {
+    if (p.D != 64 && p.D != 128 && p.D != 256) return false;
+    const uint32_t hpw = attn_hpw(p.H, p.Hkv);
+    if (hpw == 0 || p.Hkv > 8) return false;
+    if (!gemv_ok(p.H * p.D)) return false;
+    const uint32_t rowbytes = p.Hkv * p.D * 2;
+    if (2 * kTS * rowbytes > (uint32_t)kDecStage) return false;
+    const uint32_t NG = p.H / hpw, TI = NCW / NG;
+    if (TI == 0) return false;
+    const uint32_t fresh = 2 * p.Hkv * p.D * 4;
+    const uint32_t rope = NCW * p.D * 4, merge = (TI - 1) * NG * hpw * (p.D + 2) * 4;
+    if (fresh + (rope > merge ? rope : merge) > (uint32_t)kDecUnion) return false;
+    if (3 * NCW * 32 * 4 > kDecUnion) return false;
+    if (p.P == 0 || p.P > (uint32_t)kDecMaxSplits) return false;
+    if (p.H * (p.D / 32) == 0) return false;
+  }
+  if (has_gdn) {
+    if (p.Dk != 32 && p.Dk != 64 && p.Dk != 128) return false;
+    if (p.Dv % 32 || p.Dv == 0 || p.Kc == 0 || p.Kc > (uint32_t)kMaxKc) return false;
+    if (!gemv_ok(p.Z)) return false;
+    const uint32_t m = p.Dv / 16;
+    if (m > 32 || (m & (m - 1))) return false;  // a head's chunks on adjacent lanes
+    if ((2 * p.Dk + 32) > (uint32_t)NCT) return false;
+  }
+  return true;
+}
+
+cudaError_t decode_set_attributes() {
+  const uint32_t Ds[3] = {64, 128, 256}, Hs[2] = {1, 2}, Dks[3] = {32, 64, 128};
+  for (uint32_t d : Ds)
+    for (uint32_t h : Hs)
+      for (uint32_t k : Dks) {
+        DecodeKernel f = pick(d, h, k);
+        if (!f) continue;
+        cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmem);
+        if (e != cudaSuccess) return e;
+      }
+  return cudaSuccess;
+}
+
+cudaError_t decode_launch(const Program& p, int num_sms, cudaStream_t stream) {
+  // the head dims select the attention and GDN phase code; a program without those
+  // phases (a GEMV alone) runs on any instantiation
+  const uint32_t hpw = attn_hpw(p.H, p.Hkv);
+  const uint32_t D = (p.D == 64 || p.D == 128 || p.D == 256) ? p.D : 256;
+  const uint32_t Dk = (p.Dk == 32 || p.Dk == 64 || p.Dk == 128) ? p.Dk : 128;
+  DecodeKernel f = pick(D, hpw ? hpw : 1, Dk);
+  if (!f) return cudaErrorInvalidValue;
+  cudaError_t e = cudaMemsetAsync(p.barrier, 0, sizeof(uint32_t), stream);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_sms);
+  cfg.blockDim = dim3(kDecThreads);
+  cfg.dynamicSmemBytes = kDecSmem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, f, p);
+}
+
+}  // namespace q35

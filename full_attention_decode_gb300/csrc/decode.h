@@ -1,0 +1,86 @@
+// The persistent decode kernel: one launch runs a program of layers (one layer
+// for the per-layer forwards, the whole stack for a decode step).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace q35 {
+
+constexpr int kMaxLayers = 64;
+constexpr int kDecMaxSplits = 512;  // split-KV partials the scratch holds
+
+// One quantised matrix: codes [n][k] u8, scales/biases [n][gstride] bf16.
+struct QMat {
+  const uint8_t* codes;
+  const uint16_t* scales;
+  const uint16_t* biases;
+  uint32_t n, pad;
+};
+
+// kLayerGemv: a single GEMV phase, x_out = bf16(m[0] x_in) (the component entry point).
+enum LayerKind : int32_t { kLayerFA = 0, kLayerGDN = 1, kLayerGemv = 2 };
+
+// Matrix slots of a layer.
+//   full attention:   0 q_proj, 1 k_proj, 2 v_proj, 3 o_proj, 4 gate, 5 up, 6 down
+//   linear attention: 0 in_proj_a, 1 in_proj_b, 2 in_proj_qkv, 3 in_proj_z, 4 gate,
+//                     5 up, 6 down, 7 out_proj
+struct LayerDesc {
+  int32_t kind;
+  uint32_t capacity;  // KV rows (full attention)
+  QMat m[8];
+  const uint16_t *input_ln, *post_ln, *q_norm, *k_norm, *norm_weight, *dt_bias, *conv_w;
+  const float* a_log;
+  uint16_t *kc, *vc;
+  float *conv_state, *ssm;
+};
+
+// Byte offsets of the intermediates inside the scratch buffer.
+struct ScratchMap {
+  uint32_t q_full, k, v, ga, o, part_o, part_ml;  // full attention
+  uint32_t dt_raw, b_raw, qkv, z, y, out;         // linear attention
+  uint32_t x_resid, g, u;                         // both
+};
+
+struct Program {
+  // dims
+  uint32_t E, I, H, Hkv, D, R, Hk, Hv, Dk, Dv, Kc, C, Z;
+  float eps, scale_log2, gdn_out_scale, l2_eps;
+  uint32_t n_layers;
+  const uint16_t* x_in;
+  uint16_t* x_out;
+  uint8_t* scratch;
+  ScratchMap sm;
+  int* status;
+  uint32_t* barrier;  // grid-barrier counter, zero at launch
+  // position: host values, or *d_pos (seq_len = *d_pos + 1) bounded by max_seq
+  uint32_t pos, S, max_seq, P;
+  const int32_t* d_pos;
+  int32_t* advance;  // incremented by one after the last layer, or null
+  float inv_freq[128];
+  // optional phase timeline: trace[(cta * trace_phases + phase) * 4 + k], k = 0
+  // barrier arrival, 1 barrier release, 2 phase end, 3 GEMV input formed
+  // (globaltimer ns); null = off
+  unsigned long long* trace;
+  uint32_t trace_phases;
+  LayerDesc layers[kMaxLayers];
+};
+
+// Launch geometry and attributes.
+constexpr int kDecConsumerWarps = 12;
+constexpr int kDecThreads = (kDecConsumerWarps + 1) * 32;
+constexpr int kDecStage = 45056;  // 44 KiB
+constexpr int kDecStages = 4;
+constexpr int kDecUnion = 36864;  // per-phase shared buffer (x chunks / attention / GDN)
+constexpr int kDecSmem = kDecStages * kDecStage + 2 * kDecStages * 8 + 1024 + kDecUnion;
+
+cudaError_t decode_set_attributes();
+// Dequantise one matrix to fp32 [n][k]: fmaf(scale, code, bias), one rounding.
+cudaError_t dequant_launch(const uint8_t* codes, const uint16_t* scales, const uint16_t* biases,
+                           uint32_t n, uint32_t k, uint32_t gstride, float* out, cudaStream_t stream);
+// Zeroes the barrier counter, then launches the program (cooperative, one CTA per SM).
+cudaError_t decode_launch(const Program& p, int num_sms, cudaStream_t stream);
+// Host check of the dims the kernel supports; false if unsupported.
+bool decode_dims_ok(const Program& p, bool has_fa, bool has_gdn);
+
+}  // namespace q35

@@ -267,6 +267,16 @@ QWEN35_API int qwen35_gemv(const qwen35_qweight* w, const qwen35_bf16* x, qwen35
  * (x_norm, x_norm2 and qkv_smooth exist only inside the fused kernels.) */
 QWEN35_API size_t qwen35_debug_scratch_offset(const qwen35_config* cfg, int layer_kind, const char* name);
 
+/* Debug timeline of the forwards launched after this call (until it is called
+ * again with NULL, 0): each CTA c (one per SM) writes, for phase f of a launch,
+ * globaltimer readings (ns) at d_trace[(c * max_phases + f) * 4 + k]: k = 0
+ * when it reaches the grid barrier before the phase, 1 when it leaves it, 2 when
+ * it finishes the phase, 3 (projection phases only) when the phase's input
+ * vector is formed and quantised. A phase is one step of a layer (6 per
+ * full-attention layer, 5 per linear-attention layer). d_trace is a device
+ * buffer of #SMs * max_phases * 4 entries. Not thread-safe; for profiling. */
+QWEN35_API int qwen35_debug_trace(unsigned long long* d_trace, uint32_t max_phases);
+
 /* Dequantised weights of `w`, fp32 [n][k], each element fmaf(scale, code, bias) rounded
  * once: a check of the code/scale/bias indexing the GEMV uses. */
 QWEN35_API int qwen35_dequant(const qwen35_qweight* w, float* out, void* stream);
