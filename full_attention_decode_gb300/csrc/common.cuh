@@ -126,7 +126,9 @@ __device__ __forceinline__ void bulk_g2s_stream(void* dst, const void* src, uint
 }
 // Pull [src, src + bytes) toward L2 without staging it anywhere (16-byte aligned,
 // bytes % 16 == 0); issued in pieces of at most 64 KiB.
+// A hint: a request that is not 16-byte aligned in address and size is dropped.
 __device__ __forceinline__ void prefetch_l2(const void* src, uint64_t bytes) {
+  if ((reinterpret_cast<uintptr_t>(src) | bytes) & 15) return;
   const char* p = static_cast<const char*>(src);
   while (bytes > 0) {
     const uint32_t n = bytes > 65536 ? 65536u : (uint32_t)bytes;

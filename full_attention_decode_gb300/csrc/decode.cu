@@ -70,21 +70,38 @@ struct Smem {
   uint8_t* ring;
   uint64_t* full;
   uint64_t* empty;
-  float* misc;   // 256 floats (1 KiB): reductions, gate/beta
-  uint8_t* uni;  // per-phase buffer (kDecUnion bytes)
+  uint32_t* toff;   // ring offset of the tile in each slot (written before its copies)
+  uint32_t* tmeta;  // GEMV tiles: first row | rows << 24
+  float* misc;     // 256 floats (1 KiB): reductions, gate/beta
+  uint8_t* uni;    // per-phase buffer (kDecUnion bytes)
 };
 
 __device__ __forceinline__ Smem smem_map(uint8_t* base) {
   Smem s;
   s.ring = base;
-  s.full = reinterpret_cast<uint64_t*>(base + kDecStages * kDecStage);
-  s.empty = s.full + kDecStages;
-  s.misc = reinterpret_cast<float*>(s.empty + kDecStages);
+  s.full = reinterpret_cast<uint64_t*>(base + kDecRing);
+  s.empty = s.full + kDecSlots;
+  s.toff = reinterpret_cast<uint32_t*>(s.empty + kDecSlots);
+  s.tmeta = s.toff + kDecSlots;
+  s.misc = reinterpret_cast<float*>(s.tmeta + kDecSlots);
   s.uni = reinterpret_cast<uint8_t*>(s.misc + 256);
   return s;
 }
+// The tile the consumers take as their it-th: its slot and the slot's phase parity.
+__device__ __forceinline__ uint32_t slot_of(uint32_t it) { return it % kDecSlots; }
+__device__ __forceinline__ uint32_t parity_of(uint32_t it) { return (it / kDecSlots) & 1; }
 
 __device__ __forceinline__ void consumer_sync() { named_barrier(1, NCT); }
+
+// Per-CTA state in static shared memory, addressed directly by every phase
+// function (a shared-space address instead of a generic pointer parameter):
+// the program's header (everything before the layer table, copied when the
+// launch starts) and the current layer's description.
+constexpr uint32_t kHeadBytes = (offsetof(Program, layers) + 3) / 4 * 4;
+static_assert(offsetof(Program, layers) % 8 == 0, "layer table alignment");
+__shared__ __align__(16) uint8_t s_head[kHeadBytes];
+__shared__ LayerDesc s_layer;
+__device__ __forceinline__ const Program& prog() { return *reinterpret_cast<const Program*>(s_head); }
 
 // misc[255]: the device position, read once per CTA when the launch starts (every
 // phase of the launch sees the same value although CTA 0 advances it at the end)
@@ -98,10 +115,17 @@ __device__ __forceinline__ int32_t launch_pos() {
 // wait until it reaches `target` (G per barrier passed). Bounded to 1 s; on expiry
 // the status word records a timeout and the CTA continues (its results are then
 // meaningless, but nothing hangs).
-__device__ __forceinline__ void grid_sync(const Program& P, uint32_t target) {
+// The grid barrier in two halves, run by lane 0 of the last consumer warp (a warp
+// that issues none of the loads placed between the halves). Arrival is a release
+// add after the consumers' own barrier; it waits for that thread's earlier memory
+// operations, so loads that do not depend on the other CTAs go between the halves.
+constexpr uint32_t kBarThread = (NCW - 1) * 32;
+__device__ __forceinline__ void grid_arrive(const Program& P) {
   consumer_sync();
-  if (threadIdx.x == 0) {
-    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(P.barrier) : "memory");
+  if (threadIdx.x == kBarThread) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(P.barrier) : "memory");
+}
+__device__ __forceinline__ void grid_wait(const Program& P, uint32_t target) {
+  if (threadIdx.x == kBarThread) {
     uint32_t v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(P.barrier) : "memory");
     if (v < target) {
@@ -127,10 +151,6 @@ __device__ __forceinline__ void unpack8(const uint4 u, float* x) {
   x[2] = bf16lo(u.y); x[3] = bf16hi(u.y);
   x[4] = bf16lo(u.z); x[5] = bf16hi(u.z);
   x[6] = bf16lo(u.w); x[7] = bf16hi(u.w);
-}
-__device__ __forceinline__ void load16(const uint16_t* p, float* x) {
-  unpack8(*reinterpret_cast<const uint4*>(p), x);
-  unpack8(*reinterpret_cast<const uint4*>(p + 8), x + 8);
 }
 template <int EPL>
 __device__ __forceinline__ void load_row(const uint16_t* p, float* x) {
@@ -192,7 +212,8 @@ __device__ __forceinline__ void quantize16(const float* v, XQ& q) {
   q.qsum128 = 128 * qs;
 }
 
-__device__ __forceinline__ float dot16(const uint4 w, const XQ& q) {
+// sum over the chunk of (c - 128) * q, exact: 256 * sum(c * hi) + sum(c * lo) - 128 * sum(q)
+__device__ __forceinline__ int dot16i(const uint4 w, const XQ& q) {
   int ah = 0;
   uint32_t al = (uint32_t)(-q.qsum128);
   ah = dp4a_us(w.x, q.hi[0], ah);
@@ -203,24 +224,9 @@ __device__ __forceinline__ float dot16(const uint4 w, const XQ& q) {
   al = dp4a_uu(w.z, q.lo[2], al);
   ah = dp4a_us(w.w, q.hi[3], ah);
   al = dp4a_uu(w.w, q.lo[3], al);
-  return (float)(ah * 256 + (int)al) * q.scale;
+  return ah * 256 + (int)al;
 }
 
-// Sum over the 32 lanes of v[0..3]; lane L ends with the total of v[2*b4 + b3].
-__device__ __forceinline__ float reduce4(const float* v, uint32_t lane) {
-  const bool b4 = lane & 16, b3 = lane & 8;
-  const float w0 = (b4 ? v[2] : v[0]) + __shfl_xor_sync(FULLMASK, b4 ? v[0] : v[2], 16);
-  const float w1 = (b4 ? v[3] : v[1]) + __shfl_xor_sync(FULLMASK, b4 ? v[1] : v[3], 16);
-  float z = (b3 ? w1 : w0) + __shfl_xor_sync(FULLMASK, b3 ? w0 : w1, 8);
-  z += __shfl_xor_sync(FULLMASK, z, 4);
-  z += __shfl_xor_sync(FULLMASK, z, 2);
-  z += __shfl_xor_sync(FULLMASK, z, 1);
-  return z;
-}
-template <typename T>
-__device__ __forceinline__ T sel4(const T* v, uint32_t j) {
-  return j == 0 ? v[0] : j == 1 ? v[1] : j == 2 ? v[2] : v[3];
-}
 
 // Warps per row W (a divisor of the consumer warps) and 16-element chunks per lane
 // (at most 5): the fewest wasted chunk slots, then the fewest warps per row.
@@ -254,6 +260,8 @@ struct Gemv {
   uint32_t W, cpl, R, gstride, scale_off, bias_off;
 };
 
+__shared__ Gemv s_gemv;  // the current GEMV phase (written by thread 0 inside the barrier)
+
 __device__ __forceinline__ void gemv_add(Gemv& g, const QMat& m, uint16_t* out) {
   g.seg[g.nseg] = m;
   g.out[g.nseg] = out;
@@ -261,9 +269,9 @@ __device__ __forceinline__ void gemv_add(Gemv& g, const QMat& m, uint16_t* out) 
   ++g.nseg;
 }
 
-// The GEMV of phase p of layer l.
-__device__ __noinline__ Gemv gemv_of(const Program& P, const LayerDesc& L, uint32_t l, int p) {
-  Gemv g;
+// The GEMV of phase p of layer l, written into g (shared memory: a returned struct
+// would go through local memory).
+__device__ __noinline__ void gemv_of(const Program& P, const LayerDesc& L, uint32_t l, int p, Gemv& g) {
   g.nseg = 0;
   g.row0[0] = 0;
   g.b = nullptr;
@@ -334,7 +342,6 @@ __device__ __noinline__ Gemv gemv_of(const Program& P, const LayerDesc& L, uint3
   g.gstride = ((g.K / 64 + 7) / 8) * 8;
   g.scale_off = (g.R * g.K + 15) / 16 * 16;
   g.bias_off = g.scale_off + g.R * g.gstride * 2;
-  return g;
 }
 
 struct Tile {
@@ -357,41 +364,81 @@ __device__ __forceinline__ void cta_rows(uint32_t total, uint32_t& rb, uint32_t&
   re = (uint32_t)(((uint64_t)total * (blockIdx.x + 1)) / gridDim.x);
 }
 
+// The CTA's partial row sums of a GEMV phase ([W][rows], one slice per K-part of
+// a row) and, for the down projection, its residual rows ([rows]): shared memory
+// after the input chunks.
+__device__ __forceinline__ float* gemv_partials(const Smem& sh, uint32_t nch) {
+  return reinterpret_cast<float*>(sh.uni + nch * 48);
+}
+
 // Form the phase's input vector once per CTA and store it, quantised, in shared
 // memory: chunk c at hi[c], lo[c] (uint4 each) and aux[c] = {qsum128, scale, sum x}.
-__device__ __noinline__ void gemv_prologue(const Program& P, const Gemv& g, const Smem& sh) {
+__device__ __noinline__ void gemv_prologue() {
+  const Program& P = prog();
+  const Gemv& g = s_gemv;
+  const Smem sh = smem_map(smem_raw);
   const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t nch = g.K / 16;
   uint4* qhi = reinterpret_cast<uint4*>(sh.uni);
   uint4* qlo = qhi + nch;
   float4* aux = reinterpret_cast<float4*>(qlo + nch);
+  const bool has_b = g.pro == kAddRms || g.pro == kSiluMul || g.pro == kHeadNormSilu;
+  const bool has_w = g.pro == kAddRms || g.pro == kRms || g.pro == kHeadNormSilu;
+  // every global load of the prologue is issued before any is used: one round trip
+  uint4 pa[2][2], pb[2][2], pw[2][2];
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const uint32_t c = tid + q * NCT;
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+    pa[q][0] = pa[q][1] = pb[q][0] = pb[q][1] = pw[q][0] = pw[q][1] = z;
+    if (c < nch) {
+      const uint4* ap = reinterpret_cast<const uint4*>(g.a + c * 16);
+      pa[q][0] = ap[0];
+      pa[q][1] = ap[1];
+      if (has_b) {
+        const uint4* bp = reinterpret_cast<const uint4*>(g.b + c * 16);
+        pb[q][0] = bp[0];
+        pb[q][1] = bp[1];
+      }
+      if (has_w) {
+        const uint32_t wi = g.pro == kHeadNormSilu ? (c * 16) % g.head_dim : c * 16;
+        const uint4* wp = reinterpret_cast<const uint4*>(g.nw + wi);
+        pw[q][0] = wp[0];
+        pw[q][1] = wp[1];
+      }
+    }
+  }
+  if (g.epi == 1) {  // the down projection's residual rows, for the epilogue
+    uint32_t rb, re;
+    cta_rows(g.row0[g.nseg], rb, re);
+    float* resid = gemv_partials(sh, nch) + g.W * (re - rb);
+    for (uint32_t i = tid; i < re - rb; i += NCT) resid[i] = bf16f(g.resid_in[rb + i]);
+  }
   float raw[2][16];
   float ss = 0.f;
 #pragma unroll
   for (int q = 0; q < 2; ++q) {
     const uint32_t c = tid + q * NCT;
+    unpack8(pa[q][0], raw[q]);
+    unpack8(pa[q][1], raw[q] + 8);
+    if (g.pro == kAddRms) {
+      float xb[16];
+      unpack8(pb[q][0], xb);
+      unpack8(pb[q][1], xb + 8);
 #pragma unroll
-    for (int j = 0; j < 16; ++j) raw[q][j] = 0.f;
-    if (c < nch) {
-      load16(g.a + c * 16, raw[q]);
-      if (g.pro == kAddRms) {
-        float xb[16];
-        load16(g.b + c * 16, xb);
+      for (int j = 0; j < 16; ++j) raw[q][j] = round_bf16(raw[q][j] + xb[j]);
+      if (blockIdx.x == 0 && c < nch) {  // one CTA keeps x_resid for the down projection's residual
+        uint32_t pk[8];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) raw[q][j] = round_bf16(raw[q][j] + xb[j]);
-        if (blockIdx.x == 0) {  // one CTA keeps x_resid for the down projection's residual
-          uint32_t pk[8];
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            pk[j] = (uint32_t)to_bf16(raw[q][2 * j]) | ((uint32_t)to_bf16(raw[q][2 * j + 1]) << 16);
-          uint4* dst = reinterpret_cast<uint4*>(g.resid_out + c * 16);
-          dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-        }
+        for (int j = 0; j < 8; ++j)
+          pk[j] = (uint32_t)to_bf16(raw[q][2 * j]) | ((uint32_t)to_bf16(raw[q][2 * j + 1]) << 16);
+        uint4* dst = reinterpret_cast<uint4*>(g.resid_out + c * 16);
+        dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
       }
-#pragma unroll
-      for (int j = 0; j < 16; ++j) ss = fmaf(raw[q][j], raw[q][j], ss);
     }
+#pragma unroll
+    for (int j = 0; j < 16; ++j) ss = fmaf(raw[q][j], raw[q][j], ss);  // zero past the end
   }
   float inv = 0.f;
   if (g.pro == kRms || g.pro == kAddRms) {
@@ -407,7 +454,11 @@ __device__ __noinline__ void gemv_prologue(const Program& P, const Gemv& g, cons
   for (int q = 0; q < 2; ++q) {
     const uint32_t c = tid + q * NCT;
     if (q == 1 && NCT >= nch) break;  // (uniform) no second chunk anywhere
-    float v[16];
+    float v[16], xb[16], w[16];
+    unpack8(pb[q][0], xb);
+    unpack8(pb[q][1], xb + 8);
+    unpack8(pw[q][0], w);
+    unpack8(pw[q][1], w + 8);
     if (g.pro == kHeadNormSilu) {
       // a head's chunks sit on adjacent lanes: reduce its sum of squares there
       float hs = 0.f;
@@ -415,28 +466,17 @@ __device__ __noinline__ void gemv_prologue(const Program& P, const Gemv& g, cons
       for (int j = 0; j < 16; ++j) hs = fmaf(raw[q][j], raw[q][j], hs);
       for (uint32_t o = 1; o < g.head_dim / 16; o <<= 1) hs += __shfl_xor_sync(FULLMASK, hs, o);
       const float hi = rsqrtf(hs / (float)g.head_dim + P.eps);
-      if (c < nch) {
-        float xb[16], w[16];
-        load16(g.b + c * 16, xb);
-        load16(g.nw + (c * 16) % g.head_dim, w);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] = silu_fast(xb[j]) * round_bf16(raw[q][j] * hi * w[j]);
-      }
-    } else if (c < nch) {
-      if (g.pro == kPlain) {
+      for (int j = 0; j < 16; ++j) v[j] = silu_fast(xb[j]) * round_bf16(raw[q][j] * hi * w[j]);
+    } else if (g.pro == kPlain) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] = raw[q][j];
-      } else if (g.pro == kSiluMul) {
-        float xb[16];
-        load16(g.b + c * 16, xb);
+      for (int j = 0; j < 16; ++j) v[j] = raw[q][j];
+    } else if (g.pro == kSiluMul) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] = silu_fast(raw[q][j]) * xb[j];
-      } else {  // RMSNorm (plain or after the residual add)
-        float w[16];
-        load16(g.nw + c * 16, w);
+      for (int j = 0; j < 16; ++j) v[j] = silu_fast(raw[q][j]) * xb[j];
+    } else {  // RMSNorm (plain or after the residual add)
 #pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] = round_bf16(raw[q][j] * inv * w[j]);
-      }
+      for (int j = 0; j < 16; ++j) v[j] = round_bf16(raw[q][j] * inv * w[j]);
     }
     if (c < nch) {
       XQ x;
@@ -452,18 +492,19 @@ __device__ __noinline__ void gemv_prologue(const Program& P, const Gemv& g, cons
   consumer_sync();
 }
 
-// The row loop of a GEMV phase. The description is copied into registers first:
-// the mbarrier operations' memory clobbers would otherwise reload it from shared
-// memory on every tile.
-constexpr bool kEarlyRelease = false;
+// The row loop of a GEMV phase. Warp (rs, kp) computes row rs of every tile over
+// the chunks kp, kp + W, ... of each lane, reduces it across the warp and leaves
+// the sum in the partials; the producer publishes each tile's first row and row
+// count beside its ring offset, so the loop only counts its tiles. Per chunk the
+// lane keeps x as hi/lo bytes, 128 * sum(q) and the power-of-two scale: the row's
+// part is scale * (s * sum((c - 128) q) + (b / 128 + s) * 128 sum(q)), the first
+// sum exact in integers, the bias term on the quantised chunk sum.
 template <int CPL>
-__device__ __noinline__ void gemv_main(const Gemv& gs, const Smem& sh, uint32_t& it, int* status, bool& dead) {
+__device__ __noinline__ void gemv_main(uint32_t& it_io, bool& dead_io, unsigned long long* tr) {
+  const Gemv& g = s_gemv;
+  const Smem sh = smem_map(smem_raw);
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t K = gs.K, W = gs.W, R = gs.R, gstride = gs.gstride, soff = gs.scale_off, boff = gs.bias_off;
-  const uint32_t nseg = gs.nseg, epi = gs.epi;
-  uint32_t row0[5];
-#pragma unroll
-  for (int i = 0; i < 5; ++i) row0[i] = gs.row0[i];
+  const uint32_t K = g.K, W = g.W, R = g.R, gstride = g.gstride, soff = g.scale_off, boff = g.bias_off;
   const uint32_t kp = warp % W, rs = warp / W, nch = K / 16;
   const uint4* qhi = reinterpret_cast<const uint4*>(sh.uni);
   const uint4* qlo = qhi + nch;
@@ -473,7 +514,6 @@ __device__ __noinline__ void gemv_main(const Gemv& gs, const Smem& sh, uint32_t&
   const uint32_t ch0 = lane + 32 * kp, cstep = 32 * W;
   auto chk = [&](int c) { const uint32_t ch = ch0 + c * cstep; return ch < nch ? ch : 0u; };
   XQ xq[CPL];
-  float xs[CPL];
 #pragma unroll
   for (int c = 0; c < CPL; ++c) {
     const bool valid = ch0 + c * cstep < nch;
@@ -485,110 +525,91 @@ __device__ __noinline__ void gemv_main(const Gemv& gs, const Smem& sh, uint32_t&
     xq[c].lo[2] = valid ? l.z : 0u; xq[c].lo[3] = valid ? l.w : 0u;
     xq[c].qsum128 = valid ? __float_as_int(x.x) : 0;
     xq[c].scale = valid ? x.y : 0.f;
-    xs[c] = valid ? x.z : 0.f;
   }
-  const uint32_t total = row0[nseg];
-  const uint32_t rb = (uint32_t)(((uint64_t)total * blockIdx.x) / gridDim.x);
-  const uint32_t re = (uint32_t)(((uint64_t)total * (blockIdx.x + 1)) / gridDim.x);
-  uint32_t r = rb, batch = 0;
-  const uint32_t jl = ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1);
-  float* red = sh.misc + 32;  // [2][4][NCW]
-  while (true) {
-    float acc[4];
-    uint32_t tile[4];  // row start | rows << 24 (rows <= 12; row starts < 2^24)
+  // the CTA's tiles: per segment, its rows cut into R-row tiles (the producer's walk)
+  uint32_t rb, re, ntiles = 0;
+  cta_rows(g.row0[g.nseg], rb, re);
+  for (uint32_t sg = 0; sg < g.nseg; ++sg) {
+    const uint32_t lo = max(rb, g.row0[sg]), hi = min(re, g.row0[sg + 1]);
+    if (hi > lo) ntiles += (hi - lo + R - 1) / R;
+  }
+  float* part = gemv_partials(sh, nch) + kp * (re - rb);  // indexed by row - rb
+  uint32_t it = it_io;
+  bool dead = dead_io;
+  int* status = prog().status;
+  for (uint32_t t = 0; t < ntiles; ++t) {
+    const uint32_t st = slot_of(it);
+    if (!dead && !mbar_wait(&sh.full[st], parity_of(it))) {
+      set_status(status, kStatusTimeout);
+      dead = true;
+    }
+    if (tr && threadIdx.x == 0) {
+      if (t == 0) tr[4] = global_ns();
+      if (t + 1 == ntiles) tr[5] = global_ns();
+    }
+    const uint32_t meta = dead ? 0u : sh.tmeta[st];
+    float sum = 0.f;
+    const bool mine = rs < (meta >> 24);
+    if (mine) {
+      const uint8_t* sb = sh.ring + sh.toff[st];
+      const uint8_t* crow = sb + rs * K;
+      const uint16_t* srow = reinterpret_cast<const uint16_t*>(sb + soff) + rs * gstride;
+      const uint16_t* brow = reinterpret_cast<const uint16_t*>(sb + boff) + rs * gstride;
+      uint4 w[CPL];
+      float sc[CPL], bi[CPL];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      acc[j] = 0.f;
-      tile[j] = 0;
-      if (r < re) {
-        // the tile: up to R rows, never across a segment end
-        uint32_t sg = 0;
+      for (int c = 0; c < CPL; ++c) {  // all shared-memory loads first
+        w[c] = *reinterpret_cast<const uint4*>(crow + chk(c) * 16);
+        sc[c] = bf16f(srow[chk(c) >> 2]);
+        bi[c] = bf16f(brow[chk(c) >> 2]);
+      }
 #pragma unroll
-        for (int i = 1; i < 4; ++i) sg += (i < (int)nseg && r >= row0[i]) ? 1u : 0u;
-        const uint32_t end = min(re, sg == 0 ? row0[1] : sg == 1 ? row0[2] : sg == 2 ? row0[3] : row0[4]);
-        const uint32_t nr = min(R, end - r);
-        tile[j] = r | (nr << 24);
-        r += nr;
-        const uint32_t st = it % kDecStages;
-        if (!dead && !mbar_wait(&sh.full[st], (it / kDecStages) & 1)) {
-          set_status(status, kStatusTimeout);
-          dead = true;
-        }
-        if (!dead && rs < nr) {
-          const uint8_t* sb = sh.ring + st * kDecStage;
-          const uint8_t* crow = sb + rs * K;
-          const uint16_t* srow = reinterpret_cast<const uint16_t*>(sb + soff) + rs * gstride;
-          const uint16_t* brow = reinterpret_cast<const uint16_t*>(sb + boff) + rs * gstride;
-          uint4 w[CPL];
-          float s[CPL], b[CPL];
-#pragma unroll
-          for (int c = 0; c < CPL; ++c) {  // all shared-memory loads first
-            w[c] = *reinterpret_cast<const uint4*>(crow + chk(c) * 16);
-            s[c] = bf16f(srow[chk(c) >> 2]);
-            b[c] = bf16f(brow[chk(c) >> 2]);
-          }
-          if (kEarlyRelease) {  // the row is in registers: release the stage before the arithmetic
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sh.empty[st]);
-          }
-          float part[CPL];
-#pragma unroll
-          for (int c = 0; c < CPL; ++c) part[c] = fmaf(s[c], dot16(w[c], xq[c]), fmaf(128.0f, s[c], b[c]) * xs[c]);
-#pragma unroll
-          for (int c = 1; c < CPL; ++c) part[0] += part[c];
-          acc[j] = part[0];
-          if (!kEarlyRelease) {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sh.empty[st]);
-          }
-        } else {
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sh.empty[st]);
-        }
-        ++it;
+      for (int c = 0; c < CPL; ++c) {
+        const float q128 = (float)xq[c].qsum128;
+        sum = fmaf(xq[c].scale, fmaf(sc[c], (float)dot16i(w[c], xq[c]), fmaf(bi[c], 0.0078125f, sc[c]) * q128), sum);
       }
     }
-    if (tile[0] == 0) break;
-    const float tot = reduce4(acc, lane);
-    const uint32_t tl = sel4(tile, jl), r0 = tl & 0xFFFFFFu, n0 = tl >> 24;
-    bool store = false;
-    float y = tot;
-    if (W == 1) {
-      store = (lane & 7) == 0 && rs < n0;
-    } else {
-      float* buf = red + (batch & 1) * 4 * NCW;
-      if ((lane & 7) == 0) buf[jl * NCW + warp] = tot;
-      consumer_sync();
-      if (kp == 0 && (lane & 7) == 0 && rs < n0) {
-        y = 0.f;
-        for (uint32_t w2 = 0; w2 < W; ++w2) y += buf[jl * NCW + rs * W + w2];
-        store = true;
-      }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sh.empty[st]);  // the row is in registers
+    ++it;
+    if (mine) {
+      sum = warp_sum(sum);
+      if (lane == 0) part[(meta & 0xFFFFFFu) + rs - rb] = sum;
     }
-    if (store && !dead) {
-      const uint32_t row = r0 + rs;
-      uint32_t sg = 0;
-#pragma unroll
-      for (int i = 1; i < 4; ++i) sg += (i < (int)nseg && row >= row0[i]) ? 1u : 0u;
-      const uint32_t base = sg == 0 ? row0[0] : sg == 1 ? row0[1] : sg == 2 ? row0[2] : row0[3];
-      const uint32_t local = row - base;
-      if (epi == 1) y += bf16f(gs.resid_in[local]);
-      gs.out[sg][local] = to_bf16(y);
-    }
-    ++batch;
-    if (tile[3] == 0) break;
   }
+  if (tr && threadIdx.x == 0) tr[6] = global_ns();
+  it_io = it;
+  dead_io = dead;
 }
 
-__device__ void gemv_rows(const Program& P, const Gemv& g, const Smem& sh, uint32_t& it, bool& dead) {
-  switch (g.cpl) {
-    case 1: gemv_main<1>(g, sh, it, P.status, dead); break;
-    case 2: gemv_main<2>(g, sh, it, P.status, dead); break;
-    case 3: gemv_main<3>(g, sh, it, P.status, dead); break;
-    case 4: gemv_main<4>(g, sh, it, P.status, dead); break;
-    default: gemv_main<5>(g, sh, it, P.status, dead); break;
+// The rows of a GEMV phase, then its outputs: the K-parts of each row summed in a
+// fixed order, the residual added for the down projection, bf16 stores by
+// consecutive threads.
+__device__ void gemv_rows(uint32_t& it, bool& dead, unsigned long long* tr) {
+  switch (s_gemv.cpl) {
+    case 1: gemv_main<1>(it, dead, tr); break;
+    case 2: gemv_main<2>(it, dead, tr); break;
+    case 3: gemv_main<3>(it, dead, tr); break;
+    case 4: gemv_main<4>(it, dead, tr); break;
+    default: gemv_main<5>(it, dead, tr); break;
   }
-  consumer_sync();  // the x chunks in shared memory are free again
+  consumer_sync();
+  const Gemv& g = s_gemv;
+  const Smem sh = smem_map(smem_raw);
+  uint32_t rb, re;
+  cta_rows(g.row0[g.nseg], rb, re);
+  const uint32_t rows = re - rb, W = g.W;
+  const float* part = gemv_partials(sh, g.K / 16);
+  const float* resid = part + W * rows;
+  for (uint32_t i = threadIdx.x; i < rows; i += NCT) {
+    float y = 0.f;
+    for (uint32_t w = 0; w < W; ++w) y += part[w * rows + i];
+    if (g.epi == 1) y += resid[i];
+    const uint32_t row = rb + i;
+    uint32_t sg = 0;
+    while (sg + 1 < g.nseg && row >= g.row0[sg + 1]) ++sg;
+    g.out[sg][row - g.row0[sg]] = to_bf16(y);
+  }
 }
 
 // ------------------------------------------------------------------ attention phases
@@ -687,7 +708,10 @@ __device__ __forceinline__ float reduce_transposed(float* v, uint32_t lane) {
 // of head group w % NG (one kv-head) and every TI-th tile, TI = 16 / NG; the TI
 // partial softmax states of a head group are merged in shared memory at the end.
 template <int D, int HPW>
-__device__ __noinline__ void attn_consume(const Program& P, const LayerDesc& L, const Smem& sh, uint32_t& it, bool& dead) {
+__device__ __noinline__ void attn_consume(uint32_t& it, bool& dead) {
+  const Program& P = prog();
+  const LayerDesc& L = s_layer;
+  const Smem sh = smem_map(smem_raw);
   constexpr int EPL = D / 32;
   constexpr int NV = HPW * kTS;
   constexpr int SH = NV == 8 ? 2 : NV == 16 ? 1 : 0;
@@ -740,16 +764,16 @@ __device__ __noinline__ void attn_consume(const Program& P, const LayerDesc& L, 
 
   const uint32_t midx = lane >> SH, mj = midx / kTS, mt = midx % kTS;
   for (uint32_t i = 0; i < sp.ntiles; ++i) {
-    const uint32_t st = it % kDecStages;
+    const uint32_t st = slot_of(it);
     const bool mine = active && (i % TI) == ti;
     // every warp waits for every tile before releasing it, so no warp can run a
     // ring round ahead and complete a slot's release early
-    if (!dead && !mbar_wait(&sh.full[st], (it / kDecStages) & 1)) {
+    if (!dead && !mbar_wait(&sh.full[st], parity_of(it))) {
       set_status(P.status, kStatusTimeout);
       dead = true;
     }
     if (mine && !dead) {
-      const uint8_t* base = sh.ring + st * kDecStage;
+      const uint8_t* base = sh.ring + sh.toff[st];
       const uint32_t n = min((uint32_t)kTS, sp.tc_end - (sp.t0 + i * kTS));
       float d[NV];
 #pragma unroll
@@ -872,7 +896,10 @@ __device__ __noinline__ void attn_consume(const Program& P, const LayerDesc& L, 
 
 // Merge of the P partials of (head h, 32 dims) per CTA, then the output gate:
 // ga = bf16(bf16(attn) * sigmoid(gate)).
-__device__ __noinline__ void combine_consume(const Program& P, const LayerDesc& L, const Smem& sh) {
+__device__ __noinline__ void combine_consume() {
+  const Program& P = prog();
+  const LayerDesc& L = s_layer;
+  const Smem sh = smem_map(smem_raw);
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t nd = P.D / 32, item = blockIdx.x;
   const Span sp = attn_span(P, L.capacity);
@@ -982,13 +1009,38 @@ __device__ __forceinline__ void gdn_pre(const Program& P, const LayerDesc& L, Gd
   pr.dtb = bf16f(L.dt_bias[h]);
 }
 
+// The convolution state of the q/k channels, shifted by one token (newest last):
+// the linear-attention phase reads it in every CTA of the channel's v-heads, so it
+// is written one grid barrier later, in the output projection phase, each CTA
+// taking a share of the channels (one warp).
+__device__ __noinline__ void conv_shift_qk() {
+  const Program& P = prog();
+  const LayerDesc& L = s_layer;
+  const uint32_t lane = threadIdx.x & 31, Kc = P.Kc;
+  const uint32_t nqk = 2 * P.Hk * P.Dk, per = (nqk + gridDim.x - 1) / gridDim.x;
+  const uint32_t c0 = blockIdx.x * per, c1 = min(nqk, c0 + per);
+  const uint16_t* qkv = reinterpret_cast<const uint16_t*>(P.scratch + P.sm.qkv);
+  for (uint32_t ch = c0 + lane; ch < c1; ch += 32) {
+    float* cs = L.conv_state + (size_t)ch * Kc;
+    float v[kMaxKc];
+#pragma unroll
+    for (int t = 0; t < kMaxKc; ++t) v[t] = t + 1 < (int)Kc ? cs[t + 1] : bf16f(qkv[ch]);
+#pragma unroll
+    for (int t = 0; t < kMaxKc; ++t)
+      if (t < (int)Kc) cs[t] = v[t];
+  }
+}
+
 template <int DK>
-__device__ __noinline__ void gdn_consume(const Program& P, const LayerDesc& L, const Smem& sh, GdnPre<DK>& pr) {
+__device__ __noinline__ void gdn_consume(GdnPre<DK>& pr) {
+  const Program& P = prog();
+  const LayerDesc& L = s_layer;
+  const Smem sh = smem_map(smem_raw);
   constexpr int RPT = DK / kGdnWarps;
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
   if (!pr.item) return;
   const uint32_t nsl = P.Dv / 32, item = blockIdx.x;
-  const uint32_t h = item / nsl, j = item % nsl, grp = P.Hv / P.Hk, v0 = j * 32;
+  const uint32_t h = item / nsl, j = item % nsl, v0 = j * 32;
   const uint32_t Kc = P.Kc;
   float* act = reinterpret_cast<float*>(sh.uni);  // [2 Dk + 32]
   float* red = act + 2 * DK + 32;                 // [2][NCW][32]
@@ -1007,9 +1059,9 @@ __device__ __noinline__ void gdn_consume(const Program& P, const LayerDesc& L, c
     }
     act[tid] = siluf_(o);
     // v channels belong to this CTA alone; the q/k channels of a k-head are read by
-    // every CTA of its v-heads, all before the grid barrier that opened this phase,
-    // so one of them may write them now
-    if (tid >= 2 * DK || ((h % grp) == 0 && j == 0)) {
+    // every CTA of its v-heads during this phase, so conv_shift_qk shifts them in
+    // the next one
+    if (tid >= 2 * DK) {
 #pragma unroll
       for (int t = 0; t < kMaxKc; ++t)
         if (t < (int)Kc) L.conv_state[(size_t)pr.ch * Kc + t] = pr.cst[t];
@@ -1112,12 +1164,25 @@ struct Cursor {
   uint32_t r, re, seg;
   Span sp;
   uint32_t i;
+  uint32_t ph;  // phases opened (the timeline's phase index + 1)
+  bool fresh;   // no tile of the open phase issued yet
+  uint32_t vstart[kDecSlots];  // ring placement of the tiles in flight (see produce_all)
 };
 
-// Advance to the next tile and issue its bulk copies into `dst`, completing on
-// `full`; false when the launch has no tiles left (nothing issued).
-__device__ __forceinline__ bool issue_next(const Program& P, const LayerDesc* layers, Cursor& c, uint8_t* dst,
-                                           uint64_t* full, uint64_t pol) {
+__shared__ Cursor s_cursor;
+
+// One tile: up to three contiguous global ranges, where they land in the tile, and
+// the bytes the tile takes in the ring.
+struct TileCopy {
+  const void* src[3];
+  uint32_t off[3], bytes[3];
+  uint32_t n, total, span;
+  uint32_t meta;  // GEMV: first row | rows << 24
+  bool weights;   // streamed once per step: evict-first in L2
+};
+
+// Advance to the next tile; false when the launch has no tiles left.
+__device__ __forceinline__ bool next_copy(const Program& P, const LayerDesc* layers, Cursor& c, TileCopy& tc) {
   while (c.l < P.n_layers) {
     if (c.lc != c.l) {
       c.L = layers[c.l];
@@ -1126,7 +1191,7 @@ __device__ __forceinline__ bool issue_next(const Program& P, const LayerDesc* la
     if (!c.open) {
       c.ty = phase_type(c.L.kind, c.p);
       if (c.ty == kPhGemv) {
-        c.g = gemv_of(P, c.L, c.l, c.p);
+        gemv_of(P, c.L, c.l, c.p, c.g);
         cta_rows(c.g.row0[c.g.nseg], c.r, c.re);
         c.seg = 0;
       } else if (c.ty == kPhAttn) {
@@ -1134,6 +1199,8 @@ __device__ __forceinline__ bool issue_next(const Program& P, const LayerDesc* la
         c.i = 0;
       }
       c.open = true;
+      c.fresh = true;
+      ++c.ph;
     }
     if (c.ty == kPhGemv) {
       uint32_t r = c.r, seg = c.seg;
@@ -1144,10 +1211,19 @@ __device__ __forceinline__ bool issue_next(const Program& P, const LayerDesc* la
         const QMat& m = c.g.seg[t.seg];
         const uint32_t K = c.g.K, gstride = c.g.gstride, local = t.r - c.g.row0[t.seg];
         const uint32_t cb = t.nr * K, sb = t.nr * gstride * 2;
-        mbar_arrive_expect_tx(full, cb + 2 * sb);
-        bulk_g2s_stream(dst, m.codes + (size_t)local * K, cb, full, pol);
-        bulk_g2s_stream(dst + c.g.scale_off, m.scales + (size_t)local * gstride, sb, full, pol);
-        bulk_g2s_stream(dst + c.g.bias_off, m.biases + (size_t)local * gstride, sb, full, pol);
+        tc.n = 3;
+        tc.src[0] = m.codes + (size_t)local * K;
+        tc.src[1] = m.scales + (size_t)local * gstride;
+        tc.src[2] = m.biases + (size_t)local * gstride;
+        tc.off[0] = 0;
+        tc.off[1] = c.g.scale_off;
+        tc.off[2] = c.g.bias_off;
+        tc.bytes[0] = cb;
+        tc.bytes[1] = tc.bytes[2] = sb;
+        tc.total = cb + 2 * sb;
+        tc.span = c.g.bias_off + c.g.R * gstride * 2;
+        tc.meta = t.r | (t.nr << 24);
+        tc.weights = true;
         return true;
       }
     } else if (c.ty == kPhAttn) {
@@ -1155,9 +1231,16 @@ __device__ __forceinline__ bool issue_next(const Program& P, const LayerDesc* la
         const uint32_t rowh = P.Hkv * P.D, rowbytes = rowh * 2;
         const uint32_t tt = c.sp.t0 + c.i * kTS;
         const uint32_t n = min((uint32_t)kTS, c.sp.tc_end - tt);
-        mbar_arrive_expect_tx(full, 2 * n * rowbytes);
-        bulk_g2s(dst, c.L.kc + (size_t)tt * rowh, n * rowbytes, full);
-        bulk_g2s(dst + kTS * rowbytes, c.L.vc + (size_t)tt * rowh, n * rowbytes, full);
+        tc.n = 2;
+        tc.src[0] = c.L.kc + (size_t)tt * rowh;
+        tc.src[1] = c.L.vc + (size_t)tt * rowh;
+        tc.off[0] = 0;
+        tc.off[1] = kTS * rowbytes;
+        tc.bytes[0] = tc.bytes[1] = n * rowbytes;
+        tc.total = 2 * n * rowbytes;
+        tc.span = 2 * kTS * rowbytes;  // rows past n are read (masked) by the consumers
+        tc.meta = 0;
+        tc.weights = false;
         ++c.i;
         return true;
       }
@@ -1171,53 +1254,80 @@ __device__ __forceinline__ bool issue_next(const Program& P, const LayerDesc* la
   return false;
 }
 
-__device__ __noinline__ void produce_all(const Program& P, const LayerDesc* layers, const Smem& sh, Cursor& c) {
+// The producer. Tile i takes slot i % kDecSlots and the ring bytes
+// [v_i, v_i + span_i) of a virtual byte stream, placed at v_i mod kDecRing; a tile
+// that would cross the ring's end starts at the next multiple of kDecRing. It may
+// be written once every tile that started more than kDecRing - span_i bytes before
+// its end is consumed, and once the slot's previous tile (i - kDecSlots) is.
+// Consumption is in order, so `vcons` (the start of the oldest unconsumed tile)
+// and `tail` (its index) describe all of it.
+__device__ __noinline__ void produce_all(const LayerDesc* layers) {
+  const Program& P = prog();
+  const Smem sh = smem_map(smem_raw);
+  Cursor& c = s_cursor;
   const uint64_t pol = policy_evict_first();
   c.l = 0;
   c.lc = 0xffffffffu;
   c.p = 0;
   c.open = false;
-  uint32_t it = 0;
+  c.ph = 0;
+  uint32_t i = 0, tail = 0, vnext = 0, vcons = 0;
   bool dead = false;
-  while (!dead) {
-    const uint32_t st = it % kDecStages;
-    // the stage's previous tile must be consumed; after the last tile this wait
-    // still ends, since the consumers take every tile issued
-    if (it >= (uint32_t)kDecStages && !mbar_wait(&sh.empty[st], ((it / kDecStages) - 1) & 1)) {
-      set_status(P.status, kStatusTimeout);
-      dead = true;
-      break;
+  TileCopy tc;
+  while (!dead && next_copy(P, layers, c, tc)) {
+    const uint32_t span = (tc.span + 127) & ~127u;
+    uint32_t v = vnext, ph = v % kDecRing;
+    if (ph + span > (uint32_t)kDecRing) {
+      v += kDecRing - ph;
+      ph = 0;
     }
-    if (!issue_next(P, layers, c, sh.ring + st * kDecStage, &sh.full[st], pol)) return;
-    ++it;
+    while (tail < i && (i - tail >= (uint32_t)kDecSlots || v + span - vcons > (uint32_t)kDecRing)) {
+      if (!mbar_wait(&sh.empty[slot_of(tail)], parity_of(tail))) {
+        set_status(P.status, kStatusTimeout);
+        dead = true;
+        break;
+      }
+      ++tail;
+      vcons = tail < i ? c.vstart[slot_of(tail)] : v;
+    }
+    if (dead) break;
+    if (c.fresh) {  // timeline: when the phase's first tile is issued
+      c.fresh = false;
+      if (P.trace && c.ph - 1 < P.trace_phases)
+        P.trace[((size_t)blockIdx.x * P.trace_phases + c.ph - 1) * kTraceSlots + 7] = global_ns();
+    }
+    const uint32_t st = slot_of(i);
+    c.vstart[st] = v;
+    sh.toff[st] = ph;
+    sh.tmeta[st] = tc.meta;
+    uint8_t* dst = sh.ring + ph;
+    mbar_arrive_expect_tx(&sh.full[st], tc.total);
+    for (uint32_t j = 0; j < tc.n; ++j) {
+      const uint8_t* src = static_cast<const uint8_t*>(tc.src[j]);
+      if (tc.weights) bulk_g2s_stream(dst + tc.off[j], src, tc.bytes[j], &sh.full[st], pol);
+      else bulk_g2s(dst + tc.off[j], src, tc.bytes[j], &sh.full[st]);
+    }
+    vnext = v + span;
+    ++i;
   }
-  // let the copies still in flight land before the CTA can exit
-  const uint32_t first = it > (uint32_t)kDecStages ? it - kDecStages : 0;
-  for (uint32_t j = first; j < it; ++j) mbar_wait(&sh.full[j % kDecStages], (j / kDecStages) & 1);
+  if (dead) {  // let the copies still in flight land before the CTA can exit
+    for (uint32_t j = tail; j < i; ++j) mbar_wait(&sh.full[slot_of(j)], parity_of(j));
+  }
 }
 
 // ------------------------------------------------------------------ the kernel
 
-// The program's header (everything before the layer table) is copied into shared
-// memory when the launch starts and each layer's description when the consumers
-// reach it: the phase loops then never read the (large) parameter block, whose
-// generic-address reads would miss the constant cache.
-constexpr uint32_t kHeadBytes = (offsetof(Program, layers) + 3) / 4 * 4;
-static_assert(offsetof(Program, layers) % 8 == 0, "layer table alignment");
-
 template <int D, int HPW, int DK>
 __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_constant__ Program Pk) {
-  __shared__ Gemv gdesc;
-  __shared__ __align__(16) uint8_t head_raw[kHeadBytes];
-  __shared__ LayerDesc Lcur;
-  __shared__ Cursor pcur;  // the producer's walk
   const Smem sh = smem_map(smem_raw);
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (uint32_t i = threadIdx.x; i < kHeadBytes / 4; i += blockDim.x)  // 4-byte words: the
-    reinterpret_cast<uint32_t*>(head_raw)[i] = reinterpret_cast<const uint32_t*>(&Pk)[i];  // block is 8-aligned
-  const Program& P = *reinterpret_cast<const Program*>(head_raw);  // header fields only
+  // the program's header into shared memory: 4-byte words (the parameter block is
+  // 8-byte aligned); the phase loops then never read the large parameter block
+  for (uint32_t i = threadIdx.x; i < kHeadBytes / 4; i += blockDim.x)
+    reinterpret_cast<uint32_t*>(s_head)[i] = reinterpret_cast<const uint32_t*>(&Pk)[i];
+  const Program& P = prog();
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kDecStages; ++s) {
+    for (int s = 0; s < kDecSlots; ++s) {
       mbar_init(&sh.full[s], 1);
       mbar_init(&sh.empty[s], NCW);
     }
@@ -1228,51 +1338,71 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
 
   if (warp == NCW) {
     // ------------------------------------------------ producer: the whole schedule
-    if (lane == 0) produce_all(P, Pk.layers, sh, pcur);
+    if (lane == 0) produce_all(Pk.layers);
     return;
   }
 
   // -------------------------------------------------- consumers: the phases in order
+  // Between the two halves of each grid barrier thread 0 fetches the coming phase's
+  // descriptions (the layer's, the GEMV's) and a GDN phase issues its state loads:
+  // neither depends on the other CTAs, and the wait hides them.
   uint32_t it = 0, nbar = 0, ph = 0;
   bool dead = false;
   auto mark = [&](uint32_t k) {
     if (P.trace && threadIdx.x == 0 && ph < P.trace_phases)
-      P.trace[((size_t)blockIdx.x * P.trace_phases + ph) * 4 + k] = global_ns();
+      P.trace[((size_t)blockIdx.x * P.trace_phases + ph) * kTraceSlots + k] = global_ns();
   };
+  auto slots = [&]() -> unsigned long long* {
+    return P.trace && ph < P.trace_phases ? P.trace + ((size_t)blockIdx.x * P.trace_phases + ph) * kTraceSlots
+                                          : nullptr;
+  };
+  auto describe = [&](uint32_t l, int p) {  // thread 0
+    if (p == 0) s_layer = Pk.layers[l];
+    if (phase_type(s_layer.kind, p) == kPhGemv) gemv_of(P, s_layer, l, p, s_gemv);
+  };
+  if (threadIdx.x == 0 && P.n_layers > 0) describe(0, 0);
   for (uint32_t l = 0; l < P.n_layers; ++l) {
-    if (threadIdx.x == 0) Lcur = Pk.layers[l];
-    consumer_sync();
-    const LayerDesc& L = Lcur;
-    const int np = n_phases(L.kind);
-    for (int p = 0; p < np; ++p, ++ph) {
-      const int ty = phase_type(L.kind, p);
-      const bool first = l == 0 && p == 0;
-      mark(0);
-      if (ty == kPhGdn) {
+    for (int p = 0;; ++p, ++ph) {
+      if (l > 0 || p > 0) {
+        mark(0);
+        const bool gdn = p == 1 && s_layer.kind == kLayerGDN;  // same layer: s_layer is current
         GdnPre<DK> pr;
-        gdn_pre<DK>(P, L, pr);  // issued before the barrier: the state is not written before
-        grid_sync(P, ++nbar * gridDim.x);
+        grid_arrive(P);
+        if (threadIdx.x == 0) describe(l, p);
+        if (gdn) gdn_pre<DK>(P, s_layer, pr);  // no other CTA writes this state
+        grid_wait(P, ++nbar * gridDim.x);
         mark(1);
-        gdn_consume<DK>(P, L, sh, pr);
-        mark(2);
-        continue;
-      }
-      if (!first) grid_sync(P, ++nbar * gridDim.x);
-      mark(1);
-      if (ty == kPhGemv) {
-        // the phase's GEMV description, once per CTA, in shared memory
-        if (threadIdx.x == 0) gdesc = gemv_of(P, L, l, p);
+        if (gdn) {
+          gdn_consume<DK>(pr);
+          mark(2);
+          goto next;
+        }
+      } else {
         consumer_sync();
-        gemv_prologue(P, gdesc, sh);
-        mark(3);
-        gemv_rows(P, gdesc, sh, it, dead);
+        mark(1);
       }
-      else if (ty == kPhAttn) attn_consume<D, HPW>(P, L, sh, it, dead);
-      else combine_consume(P, L, sh);
-      mark(2);
+      {
+        const int ty = phase_type(s_layer.kind, p);
+        if (s_layer.kind == kLayerGDN && p == 2 && warp == NCW - 1) conv_shift_qk();
+        if (ty == kPhGemv) {
+          gemv_prologue();
+          mark(3);
+          gemv_rows(it, dead, slots());
+        } else if (ty == kPhAttn) {
+          attn_consume<D, HPW>(it, dead);
+        } else {
+          combine_consume();
+        }
+        mark(2);
+      }
+    next:
+      if (p + 1 >= n_phases(s_layer.kind)) {
+        ++ph;
+        break;
+      }
     }
   }
-  consumer_sync();  // Lcur is read to the end of the last phase
+  consumer_sync();
   if (P.advance && blockIdx.x == 0 && threadIdx.x == 0) *P.advance += 1;
 }
 
@@ -1314,25 +1444,43 @@ uint32_t attn_hpw(uint32_t H, uint32_t Hkv) {
 
 }  // namespace
 
-bool decode_dims_ok(const Program& p, bool has_fa, bool has_gdn) {
-  auto gemv_ok = [](uint32_t K) {
-    if (K == 0 || K % 64 || K > 12288) return false;
+bool decode_dims_ok(const Program& p, bool has_fa, bool has_gdn, int num_sms) {
+  // a GEMV phase of K columns and N rows: its tile fits a ring tile, its input
+  // chunks, the CTA's partial sums and residual rows fit the phase buffer
+  auto gemv_ok = [&](uint32_t K, uint32_t N) {
+    if (K == 0 || K % 64 || K > 12288 || N == 0 || N >= (1u << 24) || num_sms <= 0) return false;
     const uint32_t nch = K / 16;
     uint32_t W, cpl;
     pick_split(nch, W, cpl);
     if (W == 0) return false;
     const uint32_t R = NCW / W, gs = ((K / 64 + 7) / 8) * 8;
     const uint32_t stage = (R * K + 15) / 16 * 16 + 2 * R * gs * 2;
-    return stage <= (uint32_t)kDecStage && nch * 48 <= (uint32_t)kDecUnion;
+    const uint32_t rows = (N + num_sms - 1) / num_sms;
+    return stage <= (uint32_t)kDecTileMax && nch * 48 + (W + 1) * rows * 4 <= (uint32_t)kDecUnion;
   };
-  if (!gemv_ok(p.E) || !gemv_ok(p.I)) return false;
+  for (uint32_t l = 0; l < p.n_layers; ++l) {
+    const LayerDesc& L = p.layers[l];
+    auto n = [&](int i) { return L.m[i].n; };
+    bool ok = true;
+    if (L.kind == kLayerGemv) {
+      ok = gemv_ok(p.E, n(0));
+    } else if (L.kind == kLayerFA) {
+      ok = gemv_ok(p.E, n(0) + n(1) + n(2)) && gemv_ok(p.H * p.D, n(3)) && gemv_ok(p.E, n(4) + n(5)) &&
+           gemv_ok(p.I, n(6));
+    } else if (L.kind == kLayerGDN) {
+      ok = gemv_ok(p.E, n(0) + n(1) + n(2) + n(3)) && gemv_ok(p.Z, n(7)) && gemv_ok(p.E, n(4) + n(5)) &&
+           gemv_ok(p.I, n(6));
+    } else {
+      ok = false;
+    }
+    if (!ok) return false;
+  }
   if (has_fa) {
     if (p.D != 64 && p.D != 128 && p.D != 256) return false;
     const uint32_t hpw = attn_hpw(p.H, p.Hkv);
     if (hpw == 0 || p.Hkv > 8) return false;
-    if (!gemv_ok(p.H * p.D)) return false;
     const uint32_t rowbytes = p.Hkv * p.D * 2;
-    if (2 * kTS * rowbytes > (uint32_t)kDecStage) return false;
+    if (2 * kTS * rowbytes > (uint32_t)kDecTileMax) return false;
     const uint32_t NG = p.H / hpw, TI = NCW / NG;
     if (TI == 0) return false;
     const uint32_t fresh = 2 * p.Hkv * p.D * 4;
@@ -1345,7 +1493,6 @@ bool decode_dims_ok(const Program& p, bool has_fa, bool has_gdn) {
   if (has_gdn) {
     if (p.Dk != 32 && p.Dk != 64 && p.Dk != 128) return false;
     if (p.Dv % 32 || p.Dv == 0 || p.Kc == 0 || p.Kc > (uint32_t)kMaxKc) return false;
-    if (!gemv_ok(p.Z)) return false;
     const uint32_t m = p.Dv / 16;
     if (m > 32 || (m & (m - 1))) return false;  // a head's chunks on adjacent lanes
     if ((2 * p.Dk + 32) > (uint32_t)NCT) return false;

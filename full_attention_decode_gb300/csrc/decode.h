@@ -8,6 +8,7 @@
 namespace q35 {
 
 constexpr int kMaxLayers = 64;
+constexpr int kTraceSlots = 8;  // timeline entries per CTA and phase
 constexpr int kDecMaxSplits = 512;  // split-KV partials the scratch holds
 
 // One quantised matrix: codes [n][k] u8, scales/biases [n][gstride] bf16.
@@ -58,9 +59,10 @@ struct Program {
   const int32_t* d_pos;
   int32_t* advance;  // incremented by one after the last layer, or null
   float inv_freq[128];
-  // optional phase timeline: trace[(cta * trace_phases + phase) * 4 + k], k = 0
-  // barrier arrival, 1 barrier release, 2 phase end, 3 GEMV input formed
-  // (globaltimer ns); null = off
+  // optional phase timeline: trace[(cta * trace_phases + phase) * kTraceSlots + k],
+  // k = 0 barrier arrival, 1 barrier release, 2 phase end, 3 GEMV input formed,
+  // 4 first tile in shared memory, 5 last tile in shared memory, 6 rows done
+  // (globaltimer ns, thread 0), 7 first tile issued (the producer); null = off
   unsigned long long* trace;
   uint32_t trace_phases;
   LayerDesc layers[kMaxLayers];
@@ -69,10 +71,14 @@ struct Program {
 // Launch geometry and attributes.
 constexpr int kDecConsumerWarps = 12;
 constexpr int kDecThreads = (kDecConsumerWarps + 1) * 32;
-constexpr int kDecStage = 45056;  // 44 KiB
-constexpr int kDecStages = 4;
-constexpr int kDecUnion = 36864;  // per-phase shared buffer (x chunks / attention / GDN)
-constexpr int kDecSmem = kDecStages * kDecStage + 2 * kDecStages * 8 + 1024 + kDecUnion;
+// The tile ring: tiles of any size up to kDecTileMax sit at increasing offsets of
+// one circular buffer, at most kDecSlots in flight (one full/empty barrier pair
+// and one offset word per slot).
+constexpr int kDecRing = 135168;    // 132 KiB
+constexpr int kDecTileMax = 45056;  // 44 KiB
+constexpr int kDecSlots = 16;
+constexpr int kDecUnion = 65536;  // per-phase shared buffer (x chunks + partials / attention / GDN)
+constexpr int kDecSmem = kDecRing + 2 * kDecSlots * 8 + 2 * kDecSlots * 4 + 1024 + kDecUnion;
 
 cudaError_t decode_set_attributes();
 // Dequantise one matrix to fp32 [n][k]: fmaf(scale, code, bias), one rounding.
@@ -80,7 +86,8 @@ cudaError_t dequant_launch(const uint8_t* codes, const uint16_t* scales, const u
                            uint32_t n, uint32_t k, uint32_t gstride, float* out, cudaStream_t stream);
 // Zeroes the barrier counter, then launches the program (cooperative, one CTA per SM).
 cudaError_t decode_launch(const Program& p, int num_sms, cudaStream_t stream);
-// Host check of the dims the kernel supports; false if unsupported.
-bool decode_dims_ok(const Program& p, bool has_fa, bool has_gdn);
+// Host check of the dims the kernel supports on a grid of num_sms CTAs; false if
+// unsupported.
+bool decode_dims_ok(const Program& p, bool has_fa, bool has_gdn, int num_sms);
 
 }  // namespace q35

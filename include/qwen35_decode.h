@@ -269,12 +269,15 @@ QWEN35_API size_t qwen35_debug_scratch_offset(const qwen35_config* cfg, int laye
 
 /* Debug timeline of the forwards launched after this call (until it is called
  * again with NULL, 0): each CTA c (one per SM) writes, for phase f of a launch,
- * globaltimer readings (ns) at d_trace[(c * max_phases + f) * 4 + k]: k = 0
+ * globaltimer readings (ns) at d_trace[(c * max_phases + f) * 8 + k]: k = 0
  * when it reaches the grid barrier before the phase, 1 when it leaves it, 2 when
- * it finishes the phase, 3 (projection phases only) when the phase's input
- * vector is formed and quantised. A phase is one step of a layer (6 per
- * full-attention layer, 5 per linear-attention layer). d_trace is a device
- * buffer of #SMs * max_phases * 4 entries. Not thread-safe; for profiling. */
+ * it finishes the phase; projection phases also write 3 when the phase's input
+ * vector is formed and quantised, 4 and 5 when the first and the last of the
+ * CTA's weight tiles is in shared memory, 6 when its rows are done; phases
+ * that stream tiles write 7 when the first is requested. Entries a
+ * phase does not write keep their contents. A phase is one step of a layer (6
+ * per full-attention layer, 5 per linear-attention layer). d_trace is a device
+ * buffer of #SMs * max_phases * 8 entries. Not thread-safe; for profiling. */
 QWEN35_API int qwen35_debug_trace(unsigned long long* d_trace, uint32_t max_phases);
 
 /* Dequantised weights of `w`, fp32 [n][k], each element fmaf(scale, code, bias) rounded
