@@ -334,10 +334,21 @@ class DeviceKv:
 
 
 class DeviceState:
+    """A linear-attention state on the device. `ssm` is given as [Hv][Dk][Dv] and
+    stored in the library's column-block layout [Hv][Dv/32][Dk][32]."""
+
     def __init__(self, conv: np.ndarray, ssm: np.ndarray, device="cuda"):
+        hv, dk, dv = ssm.shape
+        self.shape = (hv, dk, dv)
+        blocked = np.ascontiguousarray(ssm.reshape(hv, dk, dv // 32, 32).transpose(0, 2, 1, 3))
         self.conv = to_device(conv, device)
-        self.ssm = to_device(ssm, device)
+        self.ssm = to_device(blocked, device)
         self.struct = qwen35_gdn_state(self.conv.data_ptr(), self.ssm.data_ptr())
+
+    def ssm_matrix(self):
+        """The state as [Hv][Dk][Dv] (a device tensor)."""
+        hv, dk, dv = self.shape
+        return self.ssm.view(hv, dv // 32, dk, 32).permute(0, 2, 1, 3).reshape(hv, dk, dv)
 
 
 def stack_layer(kind: str, dev_layer, cache) -> qwen35_layer:

@@ -152,8 +152,7 @@ int check_fa_layer(const qwen35_fa_layer* l, const Dims& d) {
 int check_gdn_layer(const qwen35_gdn_layer* l, const Dims& d) {
   if (!l) return QWEN35_ERR_INVALID_ARGUMENT;
   if (!aligned16(l->input_ln) || !aligned16(l->post_ln) || !aligned16(l->norm_weight) || !l->a_log ||
-      !l->dt_bias || !l->conv1d_weight || ((uintptr_t)l->a_log % 4) || ((uintptr_t)l->dt_bias % 2) ||
-      ((uintptr_t)l->conv1d_weight % 2))
+      !l->dt_bias || !aligned16(l->conv1d_weight) || ((uintptr_t)l->a_log % 4) || ((uintptr_t)l->dt_bias % 2))
     return QWEN35_ERR_INVALID_ARGUMENT;
   if (!qw_ok(l->in_proj_a, d.Hv, d.E) || !qw_ok(l->in_proj_b, d.Hv, d.E) ||
       !qw_ok(l->in_proj_qkv, d.C, d.E) || !qw_ok(l->in_proj_z, d.Z, d.E) || !qw_ok(l->out_proj, d.E, d.Z) ||

@@ -70,7 +70,9 @@ struct Smem {
   uint8_t* ring;
   uint64_t* full;
   uint64_t* empty;
-  uint32_t* toff;   // ring offset of the tile in each slot (written before its copies)
+  uint64_t* gfull;   // linear-attention staging: filled (producer, tx count)
+  uint64_t* gempty;  // linear-attention staging: consumed (thread 0)
+  uint32_t* toff;    // ring offset of the tile in each slot (written before its copies)
   uint32_t* tmeta;  // GEMV tiles: first row | rows << 24
   float* misc;     // 256 floats (1 KiB): reductions, gate/beta
   uint8_t* uni;    // per-phase buffer (kDecUnion bytes)
@@ -81,7 +83,9 @@ __device__ __forceinline__ Smem smem_map(uint8_t* base) {
   s.ring = base;
   s.full = reinterpret_cast<uint64_t*>(base + kDecRing);
   s.empty = s.full + kDecSlots;
-  s.toff = reinterpret_cast<uint32_t*>(s.empty + kDecSlots);
+  s.gfull = s.empty + kDecSlots;
+  s.gempty = s.gfull + 1;
+  s.toff = reinterpret_cast<uint32_t*>(s.gempty + 1);
   s.tmeta = s.toff + kDecSlots;
   s.misc = reinterpret_cast<float*>(s.tmeta + kDecSlots);
   s.uni = reinterpret_cast<uint8_t*>(s.misc + 256);
@@ -184,6 +188,11 @@ __device__ __forceinline__ uint32_t dp4a_uu(uint32_t a, uint32_t b, uint32_t c) 
   return d;
 }
 
+__device__ __forceinline__ int sat16(float x) {  // round to nearest even, saturate to int16
+  short r;
+  asm("cvt.rni.sat.s16.f32 %0, %1;" : "=h"(r) : "f"(x));
+  return r;
+}
 __device__ __forceinline__ void quantize16(const float* v, XQ& q) {
   float amax = 0.f;
 #pragma unroll
@@ -192,22 +201,20 @@ __device__ __forceinline__ void quantize16(const float* v, XQ& q) {
   // A chunk whose largest element is below 2^-112 counts as zero.
   const uint32_t E = __float_as_uint(amax) >> 23;
   const bool nz = E >= 15;
-  const float up = __uint_as_float((268u - (nz ? E : 15u)) << 23);  // 2^(15-e)
+  const float up = nz ? __uint_as_float((268u - E) << 23) : 0.f;  // 2^(15-e)
   q.scale = nz ? __uint_as_float((E - 14u) << 23) : 0.f;
   int qs = 0;
 #pragma unroll
   for (int w = 0; w < 4; ++w) {
-    uint32_t hi = 0, lo = 0;
+    int t[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      int t = nz ? __float2int_rn(v[4 * w + j] * up) : 0;
-      t = max(-32768, min(32767, t));
-      qs += t;
-      hi |= (uint32_t)((t >> 8) & 0xFF) << (8 * j);
-      lo |= (uint32_t)(t & 0xFF) << (8 * j);
+      t[j] = sat16(v[4 * w + j] * up);
+      qs += t[j];
     }
-    q.hi[w] = hi;
-    q.lo[w] = lo;
+    // byte j of lo / hi = the low / high byte of element 4w + j
+    q.lo[w] = __byte_perm(__byte_perm(t[0], t[1], 0x0040), __byte_perm(t[2], t[3], 0x0040), 0x5410);
+    q.hi[w] = __byte_perm(__byte_perm(t[0], t[1], 0x0051), __byte_perm(t[2], t[3], 0x0051), 0x5410);
   }
   q.qsum128 = 128 * qs;
 }
@@ -258,6 +265,7 @@ struct Gemv {
   const uint16_t* resid_in;
   uint32_t head_dim;
   uint32_t W, cpl, R, gstride, scale_off, bias_off;
+  uint32_t rb, re, ntiles;  // this CTA's rows [rb, re) and its tile count
 };
 
 __shared__ Gemv s_gemv;  // the current GEMV phase (written by thread 0 inside the barrier)
@@ -342,6 +350,15 @@ __device__ __noinline__ void gemv_of(const Program& P, const LayerDesc& L, uint3
   g.gstride = ((g.K / 64 + 7) / 8) * 8;
   g.scale_off = (g.R * g.K + 15) / 16 * 16;
   g.bias_off = g.scale_off + g.R * g.gstride * 2;
+  // a balanced contiguous range of rows per CTA, cut into R-row tiles per segment
+  const uint32_t total = g.row0[g.nseg];
+  g.rb = (uint32_t)(((uint64_t)total * blockIdx.x) / gridDim.x);
+  g.re = (uint32_t)(((uint64_t)total * (blockIdx.x + 1)) / gridDim.x);
+  g.ntiles = 0;
+  for (uint32_t sg = 0; sg < g.nseg; ++sg) {
+    const uint32_t lo = max(g.rb, g.row0[sg]), hi = min(g.re, g.row0[sg + 1]);
+    if (hi > lo) g.ntiles += (hi - lo + g.R - 1) / g.R;
+  }
 }
 
 struct Tile {
@@ -359,10 +376,6 @@ __device__ __forceinline__ bool next_tile(const Gemv& g, uint32_t& r, uint32_t r
   return true;
 }
 
-__device__ __forceinline__ void cta_rows(uint32_t total, uint32_t& rb, uint32_t& re) {
-  rb = (uint32_t)(((uint64_t)total * blockIdx.x) / gridDim.x);
-  re = (uint32_t)(((uint64_t)total * (blockIdx.x + 1)) / gridDim.x);
-}
 
 // The CTA's partial row sums of a GEMV phase ([W][rows], one slice per K-part of
 // a row) and, for the down projection, its residual rows ([rows]): shared memory
@@ -373,7 +386,7 @@ __device__ __forceinline__ float* gemv_partials(const Smem& sh, uint32_t nch) {
 
 // Form the phase's input vector once per CTA and store it, quantised, in shared
 // memory: chunk c at hi[c], lo[c] (uint4 each) and aux[c] = {qsum128, scale, sum x}.
-__device__ __noinline__ void gemv_prologue() {
+__device__ __noinline__ void gemv_prologue(unsigned long long* tr) {
   const Program& P = prog();
   const Gemv& g = s_gemv;
   const Smem sh = smem_map(smem_raw);
@@ -409,10 +422,9 @@ __device__ __noinline__ void gemv_prologue() {
     }
   }
   if (g.epi == 1) {  // the down projection's residual rows, for the epilogue
-    uint32_t rb, re;
-    cta_rows(g.row0[g.nseg], rb, re);
-    float* resid = gemv_partials(sh, nch) + g.W * (re - rb);
-    for (uint32_t i = tid; i < re - rb; i += NCT) resid[i] = bf16f(g.resid_in[rb + i]);
+    const uint32_t rb = g.rb, rows = g.re - g.rb;
+    float* resid = gemv_partials(sh, nch) + g.W * rows;
+    for (uint32_t i = tid; i < rows; i += NCT) resid[i] = bf16f(g.resid_in[rb + i]);
   }
   float raw[2][16];
   float ss = 0.f;
@@ -440,6 +452,7 @@ __device__ __noinline__ void gemv_prologue() {
 #pragma unroll
     for (int j = 0; j < 16; ++j) ss = fmaf(raw[q][j], raw[q][j], ss);  // zero past the end
   }
+  if (tr && tid == 0 && raw[0][0] != 12345.f) tr[8] = global_ns();  // thread 0's loads have landed
   float inv = 0.f;
   if (g.pro == kRms || g.pro == kAddRms) {
     ss = warp_sum(ss);
@@ -489,6 +502,7 @@ __device__ __noinline__ void gemv_prologue() {
       aux[c] = make_float4(__int_as_float(x.qsum128), x.scale, s, 0.f);
     }
   }
+  if (tr && tid == 0) tr[9] = global_ns();
   consumer_sync();
 }
 
@@ -499,12 +513,13 @@ __device__ __noinline__ void gemv_prologue() {
 // lane keeps x as hi/lo bytes, 128 * sum(q) and the power-of-two scale: the row's
 // part is scale * (s * sum((c - 128) q) + (b / 128 + s) * 128 sum(q)), the first
 // sum exact in integers, the bias term on the quantised chunk sum.
+// The tile loop for CPL chunks per lane (one instantiation per chunk count, all in
+// one out-of-line function so every projection phase enters the same code).
 template <int CPL>
-__device__ __noinline__ void gemv_main(uint32_t& it_io, bool& dead_io, unsigned long long* tr) {
-  const Gemv& g = s_gemv;
-  const Smem sh = smem_map(smem_raw);
+__device__ __forceinline__ void gemv_tiles(const Gemv& g, const Smem& sh, uint32_t& it, bool& dead,
+                                           unsigned long long* tr) {
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t K = g.K, W = g.W, R = g.R, gstride = g.gstride, soff = g.scale_off, boff = g.bias_off;
+  const uint32_t K = g.K, W = g.W, gstride = g.gstride, soff = g.scale_off, boff = g.bias_off;
   const uint32_t kp = warp % W, rs = warp / W, nch = K / 16;
   const uint4* qhi = reinterpret_cast<const uint4*>(sh.uni);
   const uint4* qlo = qhi + nch;
@@ -526,17 +541,10 @@ __device__ __noinline__ void gemv_main(uint32_t& it_io, bool& dead_io, unsigned 
     xq[c].qsum128 = valid ? __float_as_int(x.x) : 0;
     xq[c].scale = valid ? x.y : 0.f;
   }
-  // the CTA's tiles: per segment, its rows cut into R-row tiles (the producer's walk)
-  uint32_t rb, re, ntiles = 0;
-  cta_rows(g.row0[g.nseg], rb, re);
-  for (uint32_t sg = 0; sg < g.nseg; ++sg) {
-    const uint32_t lo = max(rb, g.row0[sg]), hi = min(re, g.row0[sg + 1]);
-    if (hi > lo) ntiles += (hi - lo + R - 1) / R;
-  }
-  float* part = gemv_partials(sh, nch) + kp * (re - rb);  // indexed by row - rb
-  uint32_t it = it_io;
-  bool dead = dead_io;
+  const uint32_t rb = g.rb, ntiles = g.ntiles;
+  float* part = gemv_partials(sh, nch) + kp * (g.re - rb);  // indexed by row - rb
   int* status = prog().status;
+  if (tr && threadIdx.x == 0) tr[11] = global_ns();
   for (uint32_t t = 0; t < ntiles; ++t) {
     const uint32_t st = slot_of(it);
     if (!dead && !mbar_wait(&sh.full[st], parity_of(it))) {
@@ -577,6 +585,21 @@ __device__ __noinline__ void gemv_main(uint32_t& it_io, bool& dead_io, unsigned 
       if (lane == 0) part[(meta & 0xFFFFFFu) + rs - rb] = sum;
     }
   }
+}
+
+__device__ __noinline__ void gemv_main(uint32_t& it_io, bool& dead_io, unsigned long long* tr) {
+  const Gemv& g = s_gemv;
+  const Smem sh = smem_map(smem_raw);
+  if (tr && threadIdx.x == 0) tr[10] = global_ns();
+  uint32_t it = it_io;
+  bool dead = dead_io;
+  switch (g.cpl) {
+    case 1: gemv_tiles<1>(g, sh, it, dead, tr); break;
+    case 2: gemv_tiles<2>(g, sh, it, dead, tr); break;
+    case 3: gemv_tiles<3>(g, sh, it, dead, tr); break;
+    case 4: gemv_tiles<4>(g, sh, it, dead, tr); break;
+    default: gemv_tiles<5>(g, sh, it, dead, tr); break;
+  }
   if (tr && threadIdx.x == 0) tr[6] = global_ns();
   it_io = it;
   dead_io = dead;
@@ -586,19 +609,12 @@ __device__ __noinline__ void gemv_main(uint32_t& it_io, bool& dead_io, unsigned 
 // fixed order, the residual added for the down projection, bf16 stores by
 // consecutive threads.
 __device__ void gemv_rows(uint32_t& it, bool& dead, unsigned long long* tr) {
-  switch (s_gemv.cpl) {
-    case 1: gemv_main<1>(it, dead, tr); break;
-    case 2: gemv_main<2>(it, dead, tr); break;
-    case 3: gemv_main<3>(it, dead, tr); break;
-    case 4: gemv_main<4>(it, dead, tr); break;
-    default: gemv_main<5>(it, dead, tr); break;
-  }
+  gemv_main(it, dead, tr);
   consumer_sync();
+  if (tr && threadIdx.x == 0) tr[12] = global_ns();
   const Gemv& g = s_gemv;
   const Smem sh = smem_map(smem_raw);
-  uint32_t rb, re;
-  cta_rows(g.row0[g.nseg], rb, re);
-  const uint32_t rows = re - rb, W = g.W;
+  const uint32_t rb = g.rb, rows = g.re - g.rb, W = g.W;
   const float* part = gemv_partials(sh, g.K / 16);
   const float* resid = part + W * rows;
   for (uint32_t i = threadIdx.x; i < rows; i += NCT) {
@@ -969,44 +985,53 @@ __device__ __noinline__ void combine_consume() {
 // so the [Dk][32] fp32 slice is read into registers once (before the phase's grid
 // barrier: nothing before it writes the state), updated, and written once.
 constexpr int kGdnWarps = 8;  // warps holding state rows (Dk / 8 rows each)
+// The linear-attention phase's inputs that do not depend on the step's earlier
+// phases (the CTA's state slice [Dk][32] fp32, its channels' convolution state
+// [2 Dk + 32][Kc] fp32 and weights [2 Dk + 32][Kc] bf16) are staged here, in the
+// upper half of the phase buffer, by asynchronous copies issued when the layer's
+// input projection phase starts: they land while that phase streams.
+constexpr uint32_t kGdnStageOff = kDecUnion / 2;
 
-template <int DK>
-struct GdnPre {
-  float st[DK / kGdnWarps];
-  float cst[kMaxKc], cw[kMaxKc];
-  float alog, dtb;
-  uint32_t ch;
-  bool item, chan;
+// The CTA's linear-attention work item: v-head h, columns [v0, v0 + 32) of its state.
+struct GdnItem {
+  bool ok;
+  uint32_t h, j, hk, v0;
 };
+__device__ __forceinline__ GdnItem gdn_item(const Program& P) {
+  GdnItem it;
+  const uint32_t nsl = P.Dv / 32;
+  it.ok = blockIdx.x < P.Hv * nsl;
+  it.h = it.ok ? blockIdx.x / nsl : 0;
+  it.j = it.ok ? blockIdx.x % nsl : 0;
+  it.hk = it.h / (P.Hv / P.Hk);
+  it.v0 = it.j * 32;
+  return it;
+}
 
-template <int DK>
-__device__ __forceinline__ void gdn_pre(const Program& P, const LayerDesc& L, GdnPre<DK>& pr) {
-  constexpr int RPT = DK / kGdnWarps;
-  const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
-  const uint32_t nsl = P.Dv / 32, item = blockIdx.x;
-  pr.item = item < P.Hv * nsl;
-  pr.chan = false;
-  if (!pr.item) return;
-  const uint32_t h = item / nsl, j = item % nsl, grp = P.Hv / P.Hk, hk = h / grp, v0 = j * 32;
-  if (warp < kGdnWarps) {
-    const float* sp = L.ssm + ((size_t)h * DK + warp * RPT) * P.Dv + v0 + lane;
-#pragma unroll
-    for (int r = 0; r < RPT; ++r) pr.st[r] = sp[(size_t)r * P.Dv];
+// The producer's copies of a work item's staged inputs (completing on gfull): the
+// state block (contiguous: the state is stored in column blocks of 32), then three
+// channel blocks (the k-head's q channels, its k channels, the slice's v channels)
+// of convolution state and of convolution weights. False if the previous staging
+// was not consumed in time.
+__device__ __forceinline__ bool stage_gdn(const Program& P, const LayerDesc& L, const Smem& sh, uint32_t n) {
+  const GdnItem w = gdn_item(P);
+  if (!w.ok) return true;
+  if (n > 0 && !mbar_wait(sh.gempty, (n - 1) & 1)) return false;
+  const uint32_t Dk = P.Dk, Kc = P.Kc, nch = 2 * Dk + 32;
+  uint8_t* base = sh.uni + kGdnStageOff;
+  uint8_t* cs = base + Dk * 128;
+  uint8_t* cw = cs + nch * Kc * 4;
+  mbar_arrive_expect_tx(sh.gfull, Dk * 128 + nch * Kc * 6);
+  bulk_g2s(base, L.ssm + (size_t)blockIdx.x * Dk * 32, Dk * 128, sh.gfull);
+  const uint32_t ch[3] = {w.hk * Dk, P.Hk * Dk + w.hk * Dk, 2 * P.Hk * Dk + w.h * P.Dv + w.v0};
+  const uint32_t nc[3] = {Dk, Dk, 32};
+  uint32_t done = 0;
+  for (int b = 0; b < 3; ++b) {
+    bulk_g2s(cs + done * Kc * 4, L.conv_state + (size_t)ch[b] * Kc, nc[b] * Kc * 4, sh.gfull);
+    bulk_g2s(cw + done * Kc * 2, L.conv_w + (size_t)ch[b] * Kc, nc[b] * Kc * 2, sh.gfull);
+    done += nc[b];
   }
-  const uint32_t nch = 2 * DK + 32;
-  if (tid < nch) {
-    pr.chan = true;
-    pr.ch = tid < DK ? hk * DK + tid
-          : tid < 2 * DK ? P.Hk * DK + hk * DK + (tid - DK)
-                         : 2 * P.Hk * DK + h * P.Dv + v0 + (tid - 2 * DK);
-#pragma unroll
-    for (int t = 0; t < kMaxKc; ++t) {
-      pr.cst[t] = t < (int)P.Kc ? L.conv_state[(size_t)pr.ch * P.Kc + t] : 0.f;
-      pr.cw[t] = t < (int)P.Kc ? bf16f(L.conv_w[(size_t)pr.ch * P.Kc + t]) : 0.f;
-    }
-  }
-  pr.alog = L.a_log[h];
-  pr.dtb = bf16f(L.dt_bias[h]);
+  return true;
 }
 
 // The convolution state of the q/k channels, shifted by one token (newest last):
@@ -1032,29 +1057,43 @@ __device__ __noinline__ void conv_shift_qk() {
 }
 
 template <int DK>
-__device__ __noinline__ void gdn_consume(GdnPre<DK>& pr) {
+__device__ __noinline__ void gdn_consume(uint32_t n) {
   const Program& P = prog();
   const LayerDesc& L = s_layer;
   const Smem sh = smem_map(smem_raw);
   constexpr int RPT = DK / kGdnWarps;
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
-  if (!pr.item) return;
-  const uint32_t nsl = P.Dv / 32, item = blockIdx.x;
-  const uint32_t h = item / nsl, j = item % nsl, v0 = j * 32;
-  const uint32_t Kc = P.Kc;
+  const GdnItem w = gdn_item(P);
+  if (!w.ok) return;  // (uniform over the CTA)
+  const uint32_t h = w.h, v0 = w.v0, Kc = P.Kc;
   float* act = reinterpret_cast<float*>(sh.uni);  // [2 Dk + 32]
   float* red = act + 2 * DK + 32;                 // [2][NCW][32]
+  const float* st_s = reinterpret_cast<const float*>(sh.uni + kGdnStageOff);
+  const float* cs_s = st_s + DK * 32;
+  const uint16_t* cw_s = reinterpret_cast<const uint16_t*>(cs_s + (2 * DK + 32) * Kc);
   const uint16_t* qkv = reinterpret_cast<const uint16_t*>(P.scratch + P.sm.qkv);
+  // this channel (thread < 2 Dk + 32): q, k of the k-head, v of the slice
+  const bool chan = tid < 2 * DK + 32;
+  const uint32_t ch = tid < DK ? w.hk * DK + tid
+                    : tid < 2 * DK ? P.Hk * DK + w.hk * DK + (tid - DK)
+                                   : 2 * P.Hk * DK + h * P.Dv + v0 + (tid - 2 * DK);
+  const float x = chan ? bf16f(qkv[ch]) : 0.f;
+  float alog = 0.f, dtb = 0.f;
+  if (tid == 0) {
+    alog = L.a_log[h];
+    dtb = bf16f(L.dt_bias[h]);
+  }
+  if (!mbar_wait(sh.gfull, n & 1)) set_status(P.status, kStatusTimeout);  // the staged inputs
   // causal conv update + SiLU
-  if (pr.chan) {
-    const float x = bf16f(qkv[pr.ch]);
+  if (chan) {
+    float cst[kMaxKc];
     float o = 0.f;
 #pragma unroll
     for (int t = 0; t < kMaxKc; ++t) {
       if (t < (int)Kc) {
-        const float sv = (t + 1 < (int)Kc) ? pr.cst[t + 1] : x;  // shift left, newest last
-        pr.cst[t] = sv;
-        o = fmaf(pr.cw[t], sv, o);
+        const float sv = (t + 1 < (int)Kc) ? cs_s[tid * Kc + t + 1] : x;  // shift left, newest last
+        cst[t] = sv;
+        o = fmaf(bf16f(cw_s[tid * Kc + t]), sv, o);
       }
     }
     act[tid] = siluf_(o);
@@ -1064,16 +1103,16 @@ __device__ __noinline__ void gdn_consume(GdnPre<DK>& pr) {
     if (tid >= 2 * DK) {
 #pragma unroll
       for (int t = 0; t < kMaxKc; ++t)
-        if (t < (int)Kc) L.conv_state[(size_t)pr.ch * Kc + t] = pr.cst[t];
+        if (t < (int)Kc) L.conv_state[(size_t)ch * Kc + t] = cst[t];
     }
   }
   const uint16_t* dtr = reinterpret_cast<const uint16_t*>(P.scratch + P.sm.dt_raw);
   const uint16_t* brw = reinterpret_cast<const uint16_t*>(P.scratch + P.sm.b_raw);
   if (tid == 0) {
     // gate = exp(softplus(dt + dt_bias) * -exp(A_log)); beta = sigmoid(b)
-    const float x = bf16f(dtr[h]) + pr.dtb;
-    const float spl = x > 20.f ? x : log1pf(expf(x));
-    sh.misc[0] = expf(spl * -expf(pr.alog));
+    const float xd = bf16f(dtr[h]) + dtb;
+    const float spl = xd > 20.f ? xd : log1pf(expf(xd));
+    sh.misc[0] = expf(spl * -expf(alog));
     sh.misc[1] = sigmoidf_(bf16f(brw[h]));
   }
   consumer_sync();
@@ -1111,16 +1150,18 @@ __device__ __noinline__ void gdn_consume(GdnPre<DK>& pr) {
   const float* qv = act;
   const float* kv = act + DK;
   const bool holder = warp < kGdnWarps;
+  float st[RPT];
   float u = 0.f;
   if (holder) {
 #pragma unroll
     for (int r = 0; r < RPT; ++r) {
-      pr.st[r] *= g;
-      u = fmaf(pr.st[r], kv[warp * RPT + r], u);
+      st[r] = st_s[(warp * RPT + r) * 32 + lane] * g;
+      u = fmaf(st[r], kv[warp * RPT + r], u);
     }
     red[warp * 32 + lane] = u;
   }
   consumer_sync();
+  if (tid == 0) mbar_arrive(sh.gempty);  // the staged inputs are read
   u = 0.f;
 #pragma unroll
   for (int w = 0; w < kGdnWarps; ++w) u += red[w * 32 + lane];
@@ -1129,12 +1170,12 @@ __device__ __noinline__ void gdn_consume(GdnPre<DK>& pr) {
   if (holder) {
 #pragma unroll
     for (int r = 0; r < RPT; ++r) {
-      pr.st[r] = fmaf(kv[warp * RPT + r], delta, pr.st[r]);
-      y = fmaf(pr.st[r], qv[warp * RPT + r], y);
+      st[r] = fmaf(kv[warp * RPT + r], delta, st[r]);
+      y = fmaf(st[r], qv[warp * RPT + r], y);
     }
-    float* sp = L.ssm + ((size_t)h * DK + warp * RPT) * P.Dv + v0 + lane;
+    float* sp = L.ssm + ((size_t)blockIdx.x * DK + warp * RPT) * 32 + lane;  // block (h, v0 / 32)
 #pragma unroll
-    for (int r = 0; r < RPT; ++r) sp[(size_t)r * P.Dv] = pr.st[r];
+    for (int r = 0; r < RPT; ++r) sp[r * 32] = st[r];
     red[kGdnWarps * 32 + warp * 32 + lane] = y;
   }
   consumer_sync();
@@ -1164,7 +1205,9 @@ struct Cursor {
   uint32_t r, re, seg;
   Span sp;
   uint32_t i;
-  uint32_t ph;  // phases opened (the timeline's phase index + 1)
+  uint32_t ph;      // phases opened (the timeline's phase index + 1)
+  uint32_t nstage;  // linear-attention stagings issued
+  bool stage_dead;  // a staging wait ran out
   bool fresh;   // no tile of the open phase issued yet
   uint32_t vstart[kDecSlots];  // ring placement of the tiles in flight (see produce_all)
 };
@@ -1192,7 +1235,8 @@ __device__ __forceinline__ bool next_copy(const Program& P, const LayerDesc* lay
       c.ty = phase_type(c.L.kind, c.p);
       if (c.ty == kPhGemv) {
         gemv_of(P, c.L, c.l, c.p, c.g);
-        cta_rows(c.g.row0[c.g.nseg], c.r, c.re);
+        c.r = c.g.rb;
+        c.re = c.g.re;
         c.seg = 0;
       } else if (c.ty == kPhAttn) {
         c.sp = attn_span(P, c.L.capacity);
@@ -1201,6 +1245,11 @@ __device__ __forceinline__ bool next_copy(const Program& P, const LayerDesc* lay
       c.open = true;
       c.fresh = true;
       ++c.ph;
+      // a linear-attention layer's staged inputs, ahead of its input projection
+      if (c.L.kind == kLayerGDN && c.p == 0) {
+        if (!stage_gdn(P, c.L, smem_map(smem_raw), c.nstage)) c.stage_dead = true;
+        ++c.nstage;
+      }
     }
     if (c.ty == kPhGemv) {
       uint32_t r = c.r, seg = c.seg;
@@ -1271,10 +1320,17 @@ __device__ __noinline__ void produce_all(const LayerDesc* layers) {
   c.p = 0;
   c.open = false;
   c.ph = 0;
+  c.nstage = 0;
+  c.stage_dead = false;
   uint32_t i = 0, tail = 0, vnext = 0, vcons = 0;
   bool dead = false;
   TileCopy tc;
   while (!dead && next_copy(P, layers, c, tc)) {
+    if (c.stage_dead) {
+      set_status(P.status, kStatusTimeout);
+      dead = true;
+      break;
+    }
     const uint32_t span = (tc.span + 127) & ~127u;
     uint32_t v = vnext, ph = v % kDecRing;
     if (ph + span > (uint32_t)kDecRing) {
@@ -1331,6 +1387,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
       mbar_init(&sh.full[s], 1);
       mbar_init(&sh.empty[s], NCW);
     }
+    mbar_init(sh.gfull, 1);
+    mbar_init(sh.gempty, 1);
     mbar_fence_init();
     reinterpret_cast<int32_t*>(sh.misc)[255] = Pk.d_pos ? *Pk.d_pos : 0;
   }
@@ -1346,7 +1404,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
   // Between the two halves of each grid barrier thread 0 fetches the coming phase's
   // descriptions (the layer's, the GEMV's) and a GDN phase issues its state loads:
   // neither depends on the other CTAs, and the wait hides them.
-  uint32_t it = 0, nbar = 0, ph = 0;
+  uint32_t it = 0, nbar = 0, ph = 0, nstage = 0;
   bool dead = false;
   auto mark = [&](uint32_t k) {
     if (P.trace && threadIdx.x == 0 && ph < P.trace_phases)
@@ -1365,18 +1423,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
     for (int p = 0;; ++p, ++ph) {
       if (l > 0 || p > 0) {
         mark(0);
-        const bool gdn = p == 1 && s_layer.kind == kLayerGDN;  // same layer: s_layer is current
-        GdnPre<DK> pr;
         grid_arrive(P);
         if (threadIdx.x == 0) describe(l, p);
-        if (gdn) gdn_pre<DK>(P, s_layer, pr);  // no other CTA writes this state
         grid_wait(P, ++nbar * gridDim.x);
         mark(1);
-        if (gdn) {
-          gdn_consume<DK>(pr);
-          mark(2);
-          goto next;
-        }
       } else {
         consumer_sync();
         mark(1);
@@ -1385,17 +1435,18 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
         const int ty = phase_type(s_layer.kind, p);
         if (s_layer.kind == kLayerGDN && p == 2 && warp == NCW - 1) conv_shift_qk();
         if (ty == kPhGemv) {
-          gemv_prologue();
+          gemv_prologue(slots());
           mark(3);
           gemv_rows(it, dead, slots());
         } else if (ty == kPhAttn) {
           attn_consume<D, HPW>(it, dead);
+        } else if (ty == kPhGdn) {
+          gdn_consume<DK>(nstage++);
         } else {
           combine_consume();
         }
         mark(2);
       }
-    next:
       if (p + 1 >= n_phases(s_layer.kind)) {
         ++ph;
         break;
@@ -1447,6 +1498,9 @@ uint32_t attn_hpw(uint32_t H, uint32_t Hkv) {
 bool decode_dims_ok(const Program& p, bool has_fa, bool has_gdn, int num_sms) {
   // a GEMV phase of K columns and N rows: its tile fits a ring tile, its input
   // chunks, the CTA's partial sums and residual rows fit the phase buffer
+  // with linear-attention layers the upper half of the phase buffer holds staged
+  // inputs that the producer may write during any earlier phase
+  const uint32_t room = has_gdn ? kGdnStageOff : (uint32_t)kDecUnion;
   auto gemv_ok = [&](uint32_t K, uint32_t N) {
     if (K == 0 || K % 64 || K > 12288 || N == 0 || N >= (1u << 24) || num_sms <= 0) return false;
     const uint32_t nch = K / 16;
@@ -1456,7 +1510,7 @@ bool decode_dims_ok(const Program& p, bool has_fa, bool has_gdn, int num_sms) {
     const uint32_t R = NCW / W, gs = ((K / 64 + 7) / 8) * 8;
     const uint32_t stage = (R * K + 15) / 16 * 16 + 2 * R * gs * 2;
     const uint32_t rows = (N + num_sms - 1) / num_sms;
-    return stage <= (uint32_t)kDecTileMax && nch * 48 + (W + 1) * rows * 4 <= (uint32_t)kDecUnion;
+    return stage <= (uint32_t)kDecTileMax && nch * 48 + (W + 1) * rows * 4 <= room;
   };
   for (uint32_t l = 0; l < p.n_layers; ++l) {
     const LayerDesc& L = p.layers[l];
@@ -1485,8 +1539,8 @@ bool decode_dims_ok(const Program& p, bool has_fa, bool has_gdn, int num_sms) {
     if (TI == 0) return false;
     const uint32_t fresh = 2 * p.Hkv * p.D * 4;
     const uint32_t rope = NCW * p.D * 4, merge = (TI - 1) * NG * hpw * (p.D + 2) * 4;
-    if (fresh + (rope > merge ? rope : merge) > (uint32_t)kDecUnion) return false;
-    if (3 * NCW * 32 * 4 > kDecUnion) return false;
+    if (fresh + (rope > merge ? rope : merge) > room) return false;
+    if (3 * NCW * 32 * 4 > room) return false;
     if (p.P == 0 || p.P > (uint32_t)kDecMaxSplits) return false;
     if (p.H * (p.D / 32) == 0) return false;
   }
@@ -1496,6 +1550,7 @@ bool decode_dims_ok(const Program& p, bool has_fa, bool has_gdn, int num_sms) {
     const uint32_t m = p.Dv / 16;
     if (m > 32 || (m & (m - 1))) return false;  // a head's chunks on adjacent lanes
     if ((2 * p.Dk + 32) > (uint32_t)NCT) return false;
+    if (p.Dk * 128 + (2 * p.Dk + 32) * p.Kc * 6 > (uint32_t)(kDecUnion - kGdnStageOff)) return false;
   }
   return true;
 }

@@ -8,7 +8,7 @@
 namespace q35 {
 
 constexpr int kMaxLayers = 64;
-constexpr int kTraceSlots = 8;  // timeline entries per CTA and phase
+constexpr int kTraceSlots = 16;  // timeline entries per CTA and phase
 constexpr int kDecMaxSplits = 512;  // split-KV partials the scratch holds
 
 // One quantised matrix: codes [n][k] u8, scales/biases [n][gstride] bf16.
@@ -62,7 +62,9 @@ struct Program {
   // optional phase timeline: trace[(cta * trace_phases + phase) * kTraceSlots + k],
   // k = 0 barrier arrival, 1 barrier release, 2 phase end, 3 GEMV input formed,
   // 4 first tile in shared memory, 5 last tile in shared memory, 6 rows done
-  // (globaltimer ns, thread 0), 7 first tile issued (the producer); null = off
+  // (globaltimer ns, thread 0), 7 first tile issued (the producer), 8 input loads
+  // landed, 9 input stored, 10 row loop entered, 11 tile loop entered, 12 rows
+  // reduced; null = off
   unsigned long long* trace;
   uint32_t trace_phases;
   LayerDesc layers[kMaxLayers];
@@ -78,7 +80,7 @@ constexpr int kDecRing = 135168;    // 132 KiB
 constexpr int kDecTileMax = 45056;  // 44 KiB
 constexpr int kDecSlots = 16;
 constexpr int kDecUnion = 65536;  // per-phase shared buffer (x chunks + partials / attention / GDN)
-constexpr int kDecSmem = kDecRing + 2 * kDecSlots * 8 + 2 * kDecSlots * 4 + 1024 + kDecUnion;
+constexpr int kDecSmem = kDecRing + 2 * kDecSlots * 8 + 16 + 2 * kDecSlots * 4 + 1024 + kDecUnion;
 
 cudaError_t decode_set_attributes();
 // Dequantise one matrix to fp32 [n][k]: fmaf(scale, code, bias), one rounding.

@@ -124,8 +124,11 @@ typedef struct qwen35_kv_cache {
 
 /* Persistent state of one linear-attention layer (LinearAttentionState,
  * "mod.rs"): conv_state fp32 [C][conv_kernel_size] (newest input in the last
- * slot), gdn_state fp32 [Hv][Dk][Dv]. Caller-allocated and zeroed before the
- * first token; updated in place by every forward. */
+ * slot); gdn_state fp32, the per-head Dk x Dv matrices S_h stored in column
+ * blocks of 32: [Hv][Dv/32][Dk][32], S_h[k][v] at
+ * ((h * (Dv/32) + v/32) * Dk + k) * 32 + v % 32 (each block is the contiguous
+ * working set of one CTA). Caller-allocated and zeroed before the first token;
+ * updated in place by every forward. */
 typedef struct qwen35_gdn_state {
     float* conv_state;
     float* gdn_state;
@@ -269,15 +272,17 @@ QWEN35_API size_t qwen35_debug_scratch_offset(const qwen35_config* cfg, int laye
 
 /* Debug timeline of the forwards launched after this call (until it is called
  * again with NULL, 0): each CTA c (one per SM) writes, for phase f of a launch,
- * globaltimer readings (ns) at d_trace[(c * max_phases + f) * 8 + k]: k = 0
+ * globaltimer readings (ns) at d_trace[(c * max_phases + f) * 16 + k]: k = 0
  * when it reaches the grid barrier before the phase, 1 when it leaves it, 2 when
  * it finishes the phase; projection phases also write 3 when the phase's input
  * vector is formed and quantised, 4 and 5 when the first and the last of the
  * CTA's weight tiles is in shared memory, 6 when its rows are done; phases
- * that stream tiles write 7 when the first is requested. Entries a
+ * that stream tiles write 7 when the first is requested; 8..12 mark steps inside
+ * a projection phase (input loads landed, input stored, row loop entered, tile
+ * loop entered, rows reduced). Entries a
  * phase does not write keep their contents. A phase is one step of a layer (6
  * per full-attention layer, 5 per linear-attention layer). d_trace is a device
- * buffer of #SMs * max_phases * 8 entries. Not thread-safe; for profiling. */
+ * buffer of #SMs * max_phases * 16 entries. Not thread-safe; for profiling. */
 QWEN35_API int qwen35_debug_trace(unsigned long long* d_trace, uint32_t max_phases);
 
 /* Dequantised weights of `w`, fp32 [n][k], each element fmaf(scale, code, bias) rounded

@@ -68,7 +68,7 @@ def test_gdn_layer_tiny_16_steps():
         assert rel_l2(got, ref) <= TOL_X, t
         assert rel_l2(r.view("qkv", len(tr["qkv"])), tr["qkv"]) <= TOL_X
         assert rel_l2(r.view("y", len(tr["y"])), tr["y"]) <= TOL_X
-    assert rel_l2(f32(r.state.ssm), r.ostate["ssm"]) <= TOL_STATE
+    assert rel_l2(f32(r.state.ssm_matrix()), r.ostate["ssm"]) <= TOL_STATE
     assert rel_l2(f32(r.state.conv), r.ostate["conv"]) <= TOL_STATE
     assert B.qwen35_read_device_status(r.scratch) == 0
 
@@ -194,7 +194,7 @@ def test_tiny_stack_16_steps(use_graph):
         stream.synchronize()
         assert rel_l2(f64(x_out), ref) <= TOL_X, t
     assert int(d_pos.item()) == 16
-    assert rel_l2(f32(caches[0].ssm), ocaches[0]["ssm"]) <= TOL_STATE
+    assert rel_l2(f32(caches[0].ssm_matrix()), ocaches[0]["ssm"]) <= TOL_STATE
     assert rel_l2(f64(caches[1].k), ocaches[1]["k"]) <= TOL_X
     assert B.qwen35_read_device_status(scratch, stream) == 0
     if g is not None:
@@ -211,7 +211,7 @@ def test_gdn_layer_4b_64_steps():
         got, ref = r.step(t)
         worst = max(worst, rel_l2(got, ref))
         assert worst <= TOL_X, (t, worst)
-    err = rel_l2(f32(r.state.ssm), r.ostate["ssm"])
+    err = rel_l2(f32(r.state.ssm_matrix()), r.ostate["ssm"])
     assert err <= TOL_STATE, err
     assert rel_l2(f32(r.state.conv), r.ostate["conv"]) <= TOL_STATE
     assert B.qwen35_read_device_status(r.scratch) == 0

@@ -38,7 +38,7 @@ def test_static_scratch_forward_matches_regular_forward_twice(cfg_name):
         assert B.qwen35_forward_linear_attention_static(c, dev.struct, st_new.struct, x_in, y_new) == 0
         torch.cuda.synchronize()
         assert rel_l2(f64(y_new), f64(y_ref)) <= TOL_X, t
-        assert rel_l2(f32(st_new.ssm), f32(st_ref.ssm)) <= TOL_STATE, t
+        assert rel_l2(f32(st_new.ssm_matrix()), f32(st_ref.ssm_matrix())) <= TOL_STATE, t
         assert rel_l2(f32(st_new.conv), f32(st_ref.conv)) <= TOL_STATE, t
     assert B.qwen35_read_device_status(scratch) == 0
 
