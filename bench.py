@@ -29,6 +29,42 @@ PREFILL = 8192
 SEED = 0
 
 
+KERNEL_SOURCES = ["full_attention_decode_gb300/csrc/decode.cu", "full_attention_decode_gb300/csrc/decode.h",
+                  "full_attention_decode_gb300/csrc/common.cuh"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_kernel_stack_dram_traffic.txt")
+
+
+def kernel_sha() -> str:
+    """sha256 over the decode kernel's sources (ties a profile to the kernel it measured)."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def profiled_traffic(step_bytes: int):
+    """DRAM bytes (read + write) per launch of the decode kernel from the committed
+    ncu capture, scaled from the captured stack to this launch by algorithmic bytes
+    (traffic grows with the layers streamed); None when the kernel's sources have
+    changed since the capture or no capture is committed."""
+    try:
+        kv = {}
+        with open(TRAFFIC_FILE) as f:
+            for line in f:
+                if "=" in line and not line.lstrip().startswith("#"):
+                    k, v = line.split("=", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("kernel_sources_sha256") != kernel_sha():
+            return None, "stale: the kernel changed since the capture"
+        dram = float(kv["dram_bytes_per_launch"])
+        alg = float(kv["algorithmic_bytes_per_launch"])
+        return int(round(dram * step_bytes / alg)), f"scaled from the {kv.get('captured')} capture ({dram / alg:.4f} x algorithmic)"
+    except Exception:
+        return None, "no capture committed"
+
+
 def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -38,7 +74,7 @@ def _peaks():
         return 6800.0, "fallback"
 
 
-def algorithmic_bytes(cfg: dict, seq_len: int) -> dict:
+def algorithmic_bytes(cfg: dict, seq_len: int, kinds: list | None = None) -> dict:
     """Bytes a decode step must move: every weight, scale and bias once, K/V rows
     [0, seq_len) once per full-attention layer plus the appended row, GDN and conv
     state read and written once, norm vectors and the small per-head vectors."""
@@ -57,7 +93,7 @@ def algorithmic_bytes(cfg: dict, seq_len: int) -> dict:
         Hv * (4 + 2) + C * Kc * 2
     gdn_state = 2 * (Hv * Dk * Dv * 4 + C * Kc * 4)
     kv = lambda S: 2 * S * Hkv * D * 2 + 2 * Hkv * D * 2  # noqa: E731
-    kinds = synth.layer_kinds(cfg)
+    kinds = kinds if kinds is not None else synth.layer_kinds(cfg)
     n_fa = kinds.count("fa")
     n_gdn = kinds.count("gdn")
     weights = n_fa * fa_w + n_gdn * gdn_w
@@ -139,8 +175,9 @@ def run_gpu(args) -> dict | None:
     B.qwen35_init()
 
     cfg = synth.config("4b")
+    kinds = synth.layer_kinds(cfg)[:args.layers]
+    cfg = dict(cfg, num_layers=len(kinds))
     c = B.make_config(cfg)
-    kinds = synth.layer_kinds(cfg)
     cap = PREFILL + args.warmup + args.steps + 2 * (args.steps + 4) + 8
     seed = SEED + rank  # each replica decodes its own sequence
     t0 = time.time()
@@ -194,6 +231,9 @@ def run_gpu(args) -> dict | None:
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
     status = B.qwen35_read_device_status(scratch, stream)
+    if args.stack_only:  # profiling runs: the graph replays alone
+        graph.close()
+        return {"ms_per_step": ms, "status": status, "layers": len(kinds)} if rank == 0 else None
 
     # ---- end to end through the C ABI with host buffers: H2D of the step's
     # input vector, the graph, D2H of its output, every step
@@ -245,7 +285,8 @@ def run_gpu(args) -> dict | None:
 
     peak, peak_kind = _peaks()
     seq_mid = pos0 + args.steps // 2 + 1
-    ab = algorithmic_bytes(cfg, seq_mid)
+    ab = algorithmic_bytes(cfg, seq_mid, kinds)
+    traffic, traffic_note = profiled_traffic(ab["step"])
     tok_s = 1000.0 / ms * world
     step_gbs = ab["step"] / (ms * 1e-3) / 1e9
     gemv_gbs = gemv_bytes / (gemv_ms * 1e-3) / 1e9
@@ -265,7 +306,7 @@ def run_gpu(args) -> dict | None:
                                         "us": round(gemv_ms * 1e3, 2), "gbs": round(gemv_gbs, 1)},
                    "device_status": status, "setup_s": round(setup_s, 1)},
         "roofline": {"bound": "hbm", "achieved": round(step_gbs, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(step_gbs / peak, 4), "traffic": None,
+                     "frac": round(step_gbs / peak, 4), "traffic": traffic, "traffic_source": traffic_note,
                      "kernel": "decode_kernel (one launch = the whole 32-layer step)",
                      "bytes_per_launch": ab["step"], "us_per_launch": round(ms * 1e3, 2),
                      "peak_kind": peak_kind},
@@ -345,6 +386,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-sample", type=int, default=0, help=argparse.SUPPRESS)
     ap.add_argument("--cpu-steps", type=int, default=24)
+    ap.add_argument("--layers", type=int, default=32, help="first N layers of the stack (profiling a small case)")
+    ap.add_argument("--stack-only", action="store_true", help="graph replays only (for ncu captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -370,6 +413,9 @@ def main():
 
     res = run_gpu(args)
     if res is None:
+        return
+    if args.stack_only:
+        print(json.dumps(res))
         return
     res["cpu_baseline"] = cpu_sample_subprocess(args.cpu_steps) if args.cpu_steps > 0 else None
     print(json.dumps(res))
