@@ -16,14 +16,15 @@
 // one producer warp and twelve consumer warps. The producer walks the CTA's
 // whole schedule of the launch, every weight tile of every GEMV phase and every
 // K/V tile of every attention phase, and streams them with bulk (TMA-engine)
-// copies into a four-stage, 176 KiB shared-memory ring, never waiting for a
-// phase boundary: weights and old cache rows do not depend on the phases before
-// them. Consumers run the phases in order with a grid barrier between dependent
-// phases; while they wait at a barrier or form a phase's input, the ring keeps
-// filling, so HBM stays busy across phase boundaries.
+// copies into a byte-addressed shared-memory ring, never waiting for a phase
+// boundary: weights and old cache rows do not depend on the phases before them.
+// It also stages each linear-attention layer's state block and conv inputs while
+// that layer's input projection streams. Consumers run the phases in order with
+// a grid barrier between dependent phases.
 //
-// Phase functions are kept out of line so that each gets the full register budget
-// (one call per phase; the call costs nothing next to the phase).
+// Phase functions are kept out of line (one call per phase) and read the
+// program header, the current layer and the current GEMV from static shared
+// memory.
 //
 // GEMV phases (the int8 group-64 affine QuantWeights::gemv family): each CTA owns
 // a balanced contiguous range of rows of the phase's concatenated matrices. The
@@ -36,8 +37,9 @@
 // exactly in int32, and the group identity
 //   sum_k (s c_k + b) x_k = s sum_k (c_k - 128) x_k + (b + 128 s) sum_k x_k
 // applies scale and bias once per chunk (the -128 offset avoids cancelling two
-// terms ~128x larger than the result when b is close to -128 s). Warps reduce four
-// tiles' rows at once with a transposed warp reduction.
+// terms ~128x larger than the result when b is close to -128 s). Each tile's row
+// is reduced across its warp into shared partial sums; one epilogue per phase
+// stores the rows.
 #include <cstddef>
 
 #include "common.cuh"
