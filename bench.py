@@ -35,12 +35,19 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_kernel_stack_dram_traffic.
 
 
 def kernel_sha() -> str:
-    """sha256 over the decode kernel's sources (ties a profile to the kernel it measured)."""
+    """sha256 over the decode kernel's sources without comments and blank lines
+    (ties a profile to the code it measured, not to its commentary)."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, f)) as fh:
+            for line in fh:
+                if '"' not in line:
+                    line = re.sub(r"//.*$", "", line)
+                line = line.strip()
+                if line:
+                    h.update(line.encode() + b"\n")
     return h.hexdigest()
 
 
