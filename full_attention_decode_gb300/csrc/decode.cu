@@ -663,10 +663,11 @@ __device__ __forceinline__ Span attn_span(const Program& P, uint32_t capacity) {
   return sp;
 }
 
-// RMSNorm over one head (this lane's EPL elements at d = lane*EPL), rounded to bf16,
-// then RoPE on dims [0, R) with rotate-half pairing, rounded to bf16.
+// RMSNorm over one head (this lane's EPL elements at d = lane*EPL, weights wv),
+// rounded to bf16, then RoPE on dims [0, R) with rotate-half pairing, rounded to
+// bf16; cs[i] = (cos, sin) of the position's angle for frequency i < R/2.
 template <int EPL>
-__device__ __forceinline__ void norm_rope(float* x, const uint16_t* w, const Program& P, uint32_t pos, float* buf,
+__device__ __forceinline__ void norm_rope(float* x, const float* wv, const Program& P, const float2* cs, float* buf,
                                           uint32_t lane) {
   const uint32_t D = EPL * 32, R = P.R, half = R / 2;
   float ss = 0.f;
@@ -674,8 +675,6 @@ __device__ __forceinline__ void norm_rope(float* x, const uint16_t* w, const Pro
   for (int e = 0; e < EPL; ++e) ss = fmaf(x[e], x[e], ss);
   ss = warp_sum(ss);
   const float inv = rsqrtf(ss / (float)D + P.eps);
-  float wv[EPL];
-  load_row<EPL>(w + lane * EPL, wv);
 #pragma unroll
   for (int e = 0; e < EPL; ++e) {
     x[e] = round_bf16(x[e] * inv * wv[e]);
@@ -686,10 +685,8 @@ __device__ __forceinline__ void norm_rope(float* x, const uint16_t* w, const Pro
   for (int e = 0; e < EPL; ++e) {
     const uint32_t d = lane * EPL + e;
     if (d < R) {
-      const uint32_t i = d < half ? d : d - half;
-      float sn, cs;
-      sincosf((float)pos * P.inv_freq[i], &sn, &cs);
-      x[e] = d < half ? round_bf16(buf[d] * cs - buf[d + half] * sn) : round_bf16(buf[d] * cs + buf[d - half] * sn);
+      const float2 c = cs[d < half ? d : d - half];
+      x[e] = d < half ? round_bf16(buf[d] * c.x - buf[d + half] * c.y) : round_bf16(buf[d] * c.x + buf[d - half] * c.y);
     }
   }
   __syncwarp();
@@ -723,10 +720,10 @@ __device__ __forceinline__ float reduce_transposed(float* v, uint32_t lane) {
 }
 
 // Split-KV attention of one split (CTA). Warp w serves the HPW consecutive q-heads
-// of head group w % NG (one kv-head) and every TI-th tile, TI = 16 / NG; the TI
+// of head group w % NG (one kv-head) and every TI-th tile, TI = 12 / NG; the TI
 // partial softmax states of a head group are merged in shared memory at the end.
 template <int D, int HPW>
-__device__ __noinline__ void attn_consume(uint32_t& it, bool& dead) {
+__device__ __noinline__ void attn_consume(uint32_t& it, bool& dead, unsigned long long* tr) {
   const Program& P = prog();
   const LayerDesc& L = s_layer;
   const Smem sh = smem_map(smem_raw);
@@ -743,42 +740,56 @@ __device__ __noinline__ void attn_consume(uint32_t& it, bool& dead) {
     return;
   }
   if (s >= P.P) return;
-  float* fresh = reinterpret_cast<float*>(sh.uni);    // k then v, [Hkv][D] each
-  float* buf = fresh + 2 * rowh;                      // per-warp [D] for RoPE, then merge space
-  // the new token's k (normed, rotated) and v: appended by exactly one CTA
-  const bool appender = sp.has_fresh || (sp.S != sp.pos + 1 && s == 0);
-  if (appender) {
-    for (uint32_t g = warp; g < Hkv; g += NCW) {
-      float kx[EPL], vx[EPL];
-      load_row<EPL>(reinterpret_cast<const uint16_t*>(P.scratch + P.sm.k) + g * D + lane * EPL, kx);
-      load_row<EPL>(reinterpret_cast<const uint16_t*>(P.scratch + P.sm.v) + g * D + lane * EPL, vx);
-      norm_rope<EPL>(kx, L.k_norm, P, sp.pos, buf + warp * D, lane);
-      uint16_t* kd = L.kc + (size_t)sp.pos * rowh + g * D + lane * EPL;
-      uint16_t* vd = L.vc + (size_t)sp.pos * rowh + g * D + lane * EPL;
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) {
-        fresh[g * D + lane * EPL + e] = kx[e];
-        fresh[rowh + g * D + lane * EPL + e] = vx[e];
-        kd[e] = to_bf16(kx[e]);
-        vd[e] = to_bf16(vx[e]);
-      }
-    }
+  float2* cs = reinterpret_cast<float2*>(sh.uni);        // RoPE (cos, sin), [R/2]
+  float* fresh = reinterpret_cast<float*>(sh.uni) + 256;  // k then v, [Hkv][D] each
+  float* buf = fresh + 2 * rowh;                          // per-warp [D] for RoPE, then merge space
+  // the position's rotation angles, once per CTA: fp32 angle, accurate sin/cos
+  if (threadIdx.x < P.R / 2) {
+    float sn, cn;
+    sincosf((float)sp.pos * P.inv_freq[threadIdx.x], &sn, &cn);
+    cs[threadIdx.x] = make_float2(cn, sn);
   }
+  // every load of the phase's inputs in one batch: this warp's q-heads and their
+  // norm weights; for the appending CTA, the new token's k and v rows
+  const bool appender = sp.has_fresh || (sp.S != sp.pos + 1 && s == 0);
   const uint32_t hg = warp % NG, ti = warp / NG;
   const bool active = ti < TI;
   const uint32_t h0 = hg * HPW, g = h0 / (H / Hkv);
-  float q[HPW][EPL], m[HPW], l[HPW], acc[HPW][EPL];
+  float q[HPW][EPL], m[HPW], l[HPW], acc[HPW][EPL], qw[EPL];
   const uint16_t* qf = reinterpret_cast<const uint16_t*>(P.scratch + P.sm.q_full);
+#pragma unroll
+  for (int j = 0; j < HPW; ++j) load_row<EPL>(qf + (size_t)(h0 + j) * 2 * D + lane * EPL, q[j]);
+  load_row<EPL>(L.q_norm + lane * EPL, qw);
+  const bool kv_warp = appender && warp < Hkv;
+  float kx[EPL], vx[EPL], kw[EPL];
+  if (kv_warp) {
+    load_row<EPL>(reinterpret_cast<const uint16_t*>(P.scratch + P.sm.k) + warp * D + lane * EPL, kx);
+    load_row<EPL>(reinterpret_cast<const uint16_t*>(P.scratch + P.sm.v) + warp * D + lane * EPL, vx);
+    load_row<EPL>(L.k_norm + lane * EPL, kw);
+  }
+  consumer_sync();  // the angle table
+  if (kv_warp) {  // the new token's k (normed, rotated) and v: appended by exactly one CTA
+    norm_rope<EPL>(kx, kw, P, cs, buf + warp * D, lane);
+    uint16_t* kd = L.kc + (size_t)sp.pos * rowh + warp * D + lane * EPL;
+    uint16_t* vd = L.vc + (size_t)sp.pos * rowh + warp * D + lane * EPL;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+      fresh[warp * D + lane * EPL + e] = kx[e];
+      fresh[rowh + warp * D + lane * EPL + e] = vx[e];
+      kd[e] = to_bf16(kx[e]);
+      vd[e] = to_bf16(vx[e]);
+    }
+  }
 #pragma unroll
   for (int j = 0; j < HPW; ++j) {
     m[j] = -INFINITY;
     l[j] = 0.f;
 #pragma unroll
     for (int e = 0; e < EPL; ++e) acc[j][e] = 0.f;
-    load_row<EPL>(qf + (size_t)(h0 + j) * 2 * D + lane * EPL, q[j]);
-    if (active) norm_rope<EPL>(q[j], L.q_norm, P, sp.pos, buf + warp * D, lane);
+    if (active) norm_rope<EPL>(q[j], qw, P, cs, buf + warp * D, lane);
   }
   consumer_sync();  // the fresh row is visible to every warp; the RoPE buffers are free
+  if (tr && threadIdx.x == 0) tr[3] = global_ns();
 
   const uint32_t midx = lane >> SH, mj = midx / kTS, mt = midx % kTS;
   for (uint32_t i = 0; i < sp.ntiles; ++i) {
@@ -789,6 +800,10 @@ __device__ __noinline__ void attn_consume(uint32_t& it, bool& dead) {
     if (!dead && !mbar_wait(&sh.full[st], parity_of(it))) {
       set_status(P.status, kStatusTimeout);
       dead = true;
+    }
+    if (tr && threadIdx.x == 0) {
+      if (i == 0) tr[4] = global_ns();
+      if (i + 1 == sp.ntiles) tr[5] = global_ns();
     }
     if (mine && !dead) {
       const uint8_t* base = sh.ring + sh.toff[st];
@@ -865,24 +880,26 @@ __device__ __noinline__ void attn_consume(uint32_t& it, bool& dead) {
       m[j] = mn;
     }
   }
-  // merge the TI partial states of each head group (warps ti > 0 hand theirs over)
-  float* mb = buf;  // [(TI-1) * NG warps][HPW][D + 2]
-  if (active && ti > 0) {
-    float* dst = mb + ((ti - 1) * NG + hg) * HPW * (D + 2);
+  if (tr && threadIdx.x == 0) tr[6] = global_ns();
+  // merge the TI partial states of each head group: the warps of token split u
+  // hand theirs over one split at a time ([NG][HPW][D + 2] floats)
+  float* mb = buf;
+  for (uint32_t u = 1; u < TI; ++u) {
+    if (active && ti == u) {
+      float* dst = mb + hg * HPW * (D + 2);
 #pragma unroll
-    for (int j = 0; j < HPW; ++j) {
+      for (int j = 0; j < HPW; ++j) {
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) dst[j * (D + 2) + lane * EPL + e] = acc[j][e];
-      if (lane == 0) {
-        dst[j * (D + 2) + D] = m[j];
-        dst[j * (D + 2) + D + 1] = l[j];
+        for (int e = 0; e < EPL; ++e) dst[j * (D + 2) + lane * EPL + e] = acc[j][e];
+        if (lane == 0) {
+          dst[j * (D + 2) + D] = m[j];
+          dst[j * (D + 2) + D + 1] = l[j];
+        }
       }
     }
-  }
-  consumer_sync();
-  if (ti == 0) {
-    for (uint32_t u = 1; u < TI; ++u) {
-      const float* src = mb + ((u - 1) * NG + hg) * HPW * (D + 2);
+    consumer_sync();
+    if (ti == 0) {
+      const float* src = mb + hg * HPW * (D + 2);
 #pragma unroll
       for (int j = 0; j < HPW; ++j) {
         const float mu = src[j * (D + 2) + D], lu = src[j * (D + 2) + D + 1];
@@ -895,6 +912,9 @@ __device__ __noinline__ void attn_consume(uint32_t& it, bool& dead) {
         m[j] = mn;
       }
     }
+    consumer_sync();
+  }
+  if (ti == 0) {
     float* part_o = reinterpret_cast<float*>(P.scratch + P.sm.part_o);
     float* part_ml = reinterpret_cast<float*>(P.scratch + P.sm.part_ml);
 #pragma unroll
@@ -990,9 +1010,10 @@ constexpr int kGdnWarps = 8;  // warps holding state rows (Dk / 8 rows each)
 // The linear-attention phase's inputs that do not depend on the step's earlier
 // phases (the CTA's state slice [Dk][32] fp32, its channels' convolution state
 // [2 Dk + 32][Kc] fp32 and weights [2 Dk + 32][Kc] bf16) are staged here, in the
-// upper half of the phase buffer, by asynchronous copies issued when the layer's
+// top 24 KiB of the phase buffer, by bulk copies issued when the layer's
 // input projection phase starts: they land while that phase streams.
-constexpr uint32_t kGdnStageOff = kDecUnion / 2;
+constexpr uint32_t kGdnStageBytes = 24576;
+constexpr uint32_t kGdnStageOff = kDecUnion - kGdnStageBytes;
 
 // The CTA's linear-attention work item: v-head h, columns [v0, v0 + 32) of its state.
 struct GdnItem {
@@ -1441,7 +1462,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
           mark(3);
           gemv_rows(it, dead, slots());
         } else if (ty == kPhAttn) {
-          attn_consume<D, HPW>(it, dead);
+          attn_consume<D, HPW>(it, dead, slots());
         } else if (ty == kPhGdn) {
           gdn_consume<DK>(nstage++);
         } else {
@@ -1487,11 +1508,15 @@ DecodeKernel pick(uint32_t D, uint32_t hpw, uint32_t Dk) {
   return nullptr;
 }
 
-// q-heads per attention warp: 2 when the heads pair up within a kv-head, else 1;
-// there must be no more head groups (H / HPW) than consumer warps.
+// q-heads per attention warp: 2 when they pair up within a kv-head's group, else
+// 1, with no more head groups (H / HPW) than consumer warps; the remaining warps
+// split the tokens (TI = 12 / (H / HPW) warps per head group). (Four heads per
+// warp measured slower at head dim 256: register pressure.)
 uint32_t attn_hpw(uint32_t H, uint32_t Hkv) {
-  if (Hkv && H % Hkv == 0 && (H / Hkv) % 2 == 0 && H / 2 <= (uint32_t)NCW) return 2;
-  if (H <= (uint32_t)NCW) return 1;
+  if (Hkv == 0 || H % Hkv) return 0;
+  const uint32_t grp = H / Hkv;
+  for (uint32_t hpw : {2u, 1u})
+    if (grp % hpw == 0 && H / hpw <= (uint32_t)NCW) return hpw;
   return 0;
 }
 
@@ -1500,7 +1525,7 @@ uint32_t attn_hpw(uint32_t H, uint32_t Hkv) {
 bool decode_dims_ok(const Program& p, bool has_fa, bool has_gdn, int num_sms) {
   // a GEMV phase of K columns and N rows: its tile fits a ring tile, its input
   // chunks, the CTA's partial sums and residual rows fit the phase buffer
-  // with linear-attention layers the upper half of the phase buffer holds staged
+  // with linear-attention layers the top of the phase buffer holds staged
   // inputs that the producer may write during any earlier phase
   const uint32_t room = has_gdn ? kGdnStageOff : (uint32_t)kDecUnion;
   auto gemv_ok = [&](uint32_t K, uint32_t N) {
@@ -1540,8 +1565,8 @@ bool decode_dims_ok(const Program& p, bool has_fa, bool has_gdn, int num_sms) {
     const uint32_t NG = p.H / hpw, TI = NCW / NG;
     if (TI == 0) return false;
     const uint32_t fresh = 2 * p.Hkv * p.D * 4;
-    const uint32_t rope = NCW * p.D * 4, merge = (TI - 1) * NG * hpw * (p.D + 2) * 4;
-    if (fresh + (rope > merge ? rope : merge) > room) return false;
+    const uint32_t rope = NCW * p.D * 4, merge = TI > 1 ? NG * hpw * (p.D + 2) * 4 : 0;
+    if (1024 + fresh + (rope > merge ? rope : merge) > room) return false;  // angle table, new row, buffers
     if (3 * NCW * 32 * 4 > room) return false;
     if (p.P == 0 || p.P > (uint32_t)kDecMaxSplits) return false;
     if (p.H * (p.D / 32) == 0) return false;
@@ -1552,7 +1577,7 @@ bool decode_dims_ok(const Program& p, bool has_fa, bool has_gdn, int num_sms) {
     const uint32_t m = p.Dv / 16;
     if (m > 32 || (m & (m - 1))) return false;  // a head's chunks on adjacent lanes
     if ((2 * p.Dk + 32) > (uint32_t)NCT) return false;
-    if (p.Dk * 128 + (2 * p.Dk + 32) * p.Kc * 6 > (uint32_t)(kDecUnion - kGdnStageOff)) return false;
+    if (p.Dk * 128 + (2 * p.Dk + 32) * p.Kc * 6 > kGdnStageBytes) return false;
   }
   return true;
 }

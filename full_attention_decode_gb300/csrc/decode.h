@@ -76,10 +76,10 @@ constexpr int kDecThreads = (kDecConsumerWarps + 1) * 32;
 // The tile ring: tiles of any size up to kDecTileMax sit at increasing offsets of
 // one circular buffer, at most kDecSlots in flight (one full/empty barrier pair
 // and one offset word per slot).
-constexpr int kDecRing = 135168;    // 132 KiB
+constexpr int kDecRing = 174080;    // 170 KiB
 constexpr int kDecTileMax = 45056;  // 44 KiB
 constexpr int kDecSlots = 16;
-constexpr int kDecUnion = 65536;  // per-phase shared buffer (x chunks + partials / attention / GDN)
+constexpr int kDecUnion = 53248;  // per-phase shared buffer (x chunks + partials / attention / GDN)
 constexpr int kDecSmem = kDecRing + 2 * kDecSlots * 8 + 16 + 2 * kDecSlots * 4 + 1024 + kDecUnion;
 
 cudaError_t decode_set_attributes();
