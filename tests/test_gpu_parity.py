@@ -228,3 +228,83 @@ def test_fa_layer_4b(cache_pos):
     assert not np.any(bits(r.kv.k)[cache_pos + 1:])  # rows above the append stay zero
     np.testing.assert_array_equal(bits(r.kv.k)[:cache_pos], O.bf16_bits(r.okv["k"][:cache_pos]))
     assert B.qwen35_read_device_status(r.scratch) == 0
+
+
+# ------------------------------------------------------------------ long context (config 4a)
+
+
+def test_fa_layer_4b_long_context():
+    # 131072 tokens of context: the appended row is the cache's 131072nd
+    cache_pos = 131071
+    r = FaRunner("4b", cache_pos + 8, cache_pos)
+    tr = {}
+    got, ref = r.step(0, cache_pos, trace=tr)
+    assert rel_l2(got, ref) <= TOL_X
+    assert rel_l2(f64(r.kv.k)[cache_pos], tr["k_rope"]) <= TOL_X
+    assert rel_l2(f64(r.kv.v)[cache_pos], tr["v"].reshape(-1, r.cfg["head_dim"])) <= TOL_X
+    assert B.qwen35_read_device_status(r.scratch) == 0
+
+
+# ------------------------------------------------------------------ the 32-layer stack (config 3)
+
+
+def test_stack_4b_teacher_forced_per_layer():
+    """One decode step of the 32-layer 4B-shape stack at 8192 tokens of context,
+    checked layer by layer: the GPU runs the stack's prefixes [0, i] from the same
+    states; the oracle applies layer i to the GPU's own input of that layer, and its
+    output, its new state (GDN) or appended row (FA) must match."""
+    init()
+    cfg = synth.config("4b")
+    kinds = synth.layer_kinds(cfg)
+    c = B.make_config(cfg)
+    prefill, cap = 8192, 8192 + 8
+    dev, caches, entries, layers, ocaches = [], [], [], [], []
+    for i, kind in enumerate(kinds):
+        if kind == "fa":
+            layers.append(synth.fa_layer(0, i, cfg))
+            kb, vb = synth.kv_cache(0, i, cfg, cap, prefill)
+            dev.append(B.DeviceFaLayer(layers[-1]))
+            caches.append(B.DeviceKv(kb, vb))
+            ocaches.append(O.kv_from_bits(kb, vb))
+        else:
+            layers.append(synth.gdn_layer(0, i, cfg))
+            conv, ssm = synth.gdn_state(0, i, cfg, std=0.1)
+            dev.append(B.DeviceGdnLayer(layers[-1]))
+            caches.append(B.DeviceState(conv, ssm))
+            ocaches.append(O.state_from_arrays(conv, ssm))
+        entries.append(B.stack_layer(kind, dev[-1], caches[-1]))
+    saved = [(cc.conv.clone(), cc.ssm.clone()) for cc in caches if isinstance(cc, B.DeviceState)]
+    scratch = B.new_scratch(B.qwen35_stack_scratch_bytes(c))
+    x_in = torch.empty(cfg["hidden"], dtype=torch.int16, device="cuda")
+    x_out = torch.empty_like(x_in)
+    d_pos = torch.empty(1, dtype=torch.int32, device="cuda")
+    x0 = synth.x_in(0, 0, cfg)
+    x_layer = O.bf16_to_f64(x0)  # the GPU's input of layer i
+    worst = 0.0
+    for i, kind in enumerate(kinds):
+        j = 0
+        for cc in caches:  # every linear-attention state back to its initial value
+            if isinstance(cc, B.DeviceState):
+                cc.conv.copy_(saved[j][0])
+                cc.ssm.copy_(saved[j][1])
+                j += 1
+        d_pos.fill_(prefill)
+        x_in.copy_(B.to_device(x0))
+        assert B.qwen35_decode_step(c, entries[:i + 1], scratch, x_in, x_out, d_pos, cap) == 0
+        torch.cuda.synchronize()
+        got = f64(x_out)
+        tr = {}
+        if kind == "fa":
+            ref = O.forward_full_attention(cfg, layers[i], ocaches[i], x_layer, prefill, prefill + 1, tr)
+            assert rel_l2(f64(caches[i].k)[prefill], tr["k_rope"]) <= TOL_X, i
+        else:
+            ref = O.forward_linear_attention(cfg, layers[i], ocaches[i], x_layer, tr)
+            assert rel_l2(f32(caches[i].ssm_matrix()), ocaches[i]["ssm"]) <= TOL_STATE, i
+        for key in [k for k in layers[i] if k.startswith("_deq_")]:
+            del layers[i][key]  # the oracle's dequantised weights, one layer at a time
+        err = rel_l2(got, ref)
+        worst = max(worst, err)
+        assert err <= TOL_X, (i, kind, err)
+        x_layer = got
+    assert int(d_pos.item()) == prefill + 1
+    assert B.qwen35_read_device_status(scratch) == 0
