@@ -87,6 +87,7 @@ _SIGS = {
     "qwen35_status_string": (C.c_char_p, [C.c_int]),
     "qwen35_scratch_bytes": (C.c_size_t, [C.POINTER(qwen35_config), C.c_int]),
     "qwen35_stack_scratch_bytes": (C.c_size_t, [C.POINTER(qwen35_config)]),
+    "qwen35_stack_scratch_bytes_batched": (C.c_size_t, [C.POINTER(qwen35_config), _U]),
     "qwen35_scratch_init": (C.c_int, [_P, C.c_size_t, _P]),
     "qwen35_read_device_status": (C.c_int, [_P, C.POINTER(C.c_int32), _P]),
     "qwen35_forward_full_attention": (C.c_int, [C.POINTER(qwen35_config), C.POINTER(qwen35_fa_layer), _P,
@@ -101,6 +102,10 @@ _SIGS = {
                                      _P, _P, _P, _U, _P]),
     "qwen35_graph_create": (C.c_int, [C.POINTER(qwen35_config), C.POINTER(qwen35_layer), _U, _P, C.c_size_t,
                                       _P, _P, _P, _U, _P, C.POINTER(C.c_void_p)]),
+    "qwen35_decode_step_batched": (C.c_int, [C.POINTER(qwen35_config), C.POINTER(qwen35_layer), _U, _U, _P,
+                                             C.c_size_t, _P, _P, _P, _U, _P]),
+    "qwen35_graph_create_batched": (C.c_int, [C.POINTER(qwen35_config), C.POINTER(qwen35_layer), _U, _U, _P,
+                                              C.c_size_t, _P, _P, _P, _U, _P, C.POINTER(C.c_void_p)]),
     "qwen35_graph_launch": (C.c_int, [_P, _P]),
     "qwen35_graph_destroy": (C.c_int, [_P]),
     "qwen35_gemv": (C.c_int, [C.POINTER(qwen35_qweight), _P, _P, _P, C.c_size_t, _P]),
@@ -178,6 +183,10 @@ def qwen35_stack_scratch_bytes(cfg: qwen35_config) -> int:
     return lib().qwen35_stack_scratch_bytes(C.byref(cfg))
 
 
+def qwen35_stack_scratch_bytes_batched(cfg: qwen35_config, batch: int) -> int:
+    return lib().qwen35_stack_scratch_bytes_batched(C.byref(cfg), batch)
+
+
 def qwen35_scratch_init(scratch, stream=None):
     _check("qwen35_scratch_init", lib().qwen35_scratch_init(_ptr(scratch), scratch.numel(), _stream(stream)))
 
@@ -219,16 +228,30 @@ def qwen35_decode_step(cfg, layers, scratch, x_in, x_out, d_cache_pos, max_seq_l
                                     _ptr(x_out), _ptr(d_cache_pos), max_seq_len, _stream(stream))
 
 
-class Graph:
-    """A captured decode step (qwen35_graph_create); replay with launch()."""
+def qwen35_decode_step_batched(cfg, layers, batch, scratch, x_in, x_out, d_cache_pos, max_seq_len, stream=None):
+    arr = (qwen35_layer * len(layers))(*layers)
+    return lib().qwen35_decode_step_batched(C.byref(cfg), arr, len(layers), batch, _ptr(scratch), scratch.numel(),
+                                            _ptr(x_in), _ptr(x_out), _ptr(d_cache_pos), max_seq_len,
+                                            _stream(stream))
 
-    def __init__(self, cfg, layers, scratch, x_in, x_out, d_cache_pos, max_seq_len, stream=None):
+
+class Graph:
+    """A captured decode step (qwen35_graph_create, or qwen35_graph_create_batched
+    for batch > 1); replay with launch()."""
+
+    def __init__(self, cfg, layers, scratch, x_in, x_out, d_cache_pos, max_seq_len, stream=None, batch: int = 1):
         arr = (qwen35_layer * len(layers))(*layers)
         h = C.c_void_p(0)
-        _check("qwen35_graph_create",
-               lib().qwen35_graph_create(C.byref(cfg), arr, len(layers), _ptr(scratch), scratch.numel(),
-                                         _ptr(x_in), _ptr(x_out), _ptr(d_cache_pos), max_seq_len,
-                                         _stream(stream), C.byref(h)))
+        if batch == 1:
+            _check("qwen35_graph_create",
+                   lib().qwen35_graph_create(C.byref(cfg), arr, len(layers), _ptr(scratch), scratch.numel(),
+                                             _ptr(x_in), _ptr(x_out), _ptr(d_cache_pos), max_seq_len,
+                                             _stream(stream), C.byref(h)))
+        else:
+            _check("qwen35_graph_create_batched",
+                   lib().qwen35_graph_create_batched(C.byref(cfg), arr, len(layers), batch, _ptr(scratch),
+                                                     scratch.numel(), _ptr(x_in), _ptr(x_out), _ptr(d_cache_pos),
+                                                     max_seq_len, _stream(stream), C.byref(h)))
         self.handle = h
 
     def launch(self, stream=None):
@@ -349,6 +372,32 @@ class DeviceState:
         """The state as [Hv][Dk][Dv] (a device tensor)."""
         hv, dk, dv = self.shape
         return self.ssm.view(hv, dv // 32, dk, 32).permute(0, 2, 1, 3).reshape(hv, dk, dv)
+
+
+class DeviceKvBatch:
+    """KV caches of a batch of sequences, [B][capacity][Hkv][D] (one capacity)."""
+
+    def __init__(self, ks: list, vs: list, device="cuda"):
+        self.k = to_device(np.stack(ks), device)
+        self.v = to_device(np.stack(vs), device)
+        self.struct = qwen35_kv_cache(self.k.data_ptr(), self.v.data_ptr(), ks[0].shape[0])
+
+
+class DeviceStateBatch:
+    """Linear-attention states of a batch: conv [B][C][Kc], ssm in the column-block
+    layout [B][Hv][Dv/32][Dk][32] (given per sequence as [Hv][Dk][Dv])."""
+
+    def __init__(self, convs: list, ssms: list, device="cuda"):
+        hv, dk, dv = ssms[0].shape
+        self.shape = (hv, dk, dv)
+        blocked = [np.ascontiguousarray(s.reshape(hv, dk, dv // 32, 32).transpose(0, 2, 1, 3)) for s in ssms]
+        self.conv = to_device(np.stack(convs), device)
+        self.ssm = to_device(np.stack(blocked), device)
+        self.struct = qwen35_gdn_state(self.conv.data_ptr(), self.ssm.data_ptr())
+
+    def ssm_matrix(self, b: int):
+        hv, dk, dv = self.shape
+        return self.ssm[b].view(hv, dv // 32, dk, 32).permute(0, 2, 1, 3).reshape(hv, dk, dv)
 
 
 def stack_layer(kind: str, dev_layer, cache) -> qwen35_layer:

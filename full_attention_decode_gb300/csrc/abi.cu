@@ -213,6 +213,8 @@ Program* new_program(const qwen35_config* cfg, const Dims& d, void* scratch) {
   p->sm = stack_map(d);
   p->status = reinterpret_cast<int*>(scratch);
   p->barrier = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(scratch) + 4);
+  p->batch = 1;
+  p->seq_stride = 0;
   // inv_freq[i] = theta^(-2i/R), computed in double and kept as fp32
   for (uint32_t i = 0; i < d.R / 2 && i < 128; ++i)
     p->inv_freq[i] = (float)std::pow((double)cfg->rope_theta, -2.0 * (double)i / (double)d.R);
@@ -403,11 +405,25 @@ int qwen35_forward_linear_attention_static(const qwen35_config* cfg, const qwen3
   return gdn_forward(cfg, layer, scratch, QWEN35_STATIC_SCRATCH_BYTES, state, x_in, x_out, st);
 }
 
-int qwen35_decode_step(const qwen35_config* cfg, const qwen35_layer* layers, uint32_t num_layers, void* scratch,
-                       size_t scratch_bytes, const qwen35_bf16* x_in, qwen35_bf16* x_out, int32_t* d_cache_pos,
-                       uint32_t max_seq_len, void* stream) {
+namespace {
+
+// Scratch of one sequence's intermediates in a stack program (both layer kinds'
+// maps share it), and of a batch: the status word and barrier counter, then one
+// block per sequence.
+size_t stack_need(const Dims& d, bool has_fa, bool has_gdn) {
+  size_t need = 256;
+  if (has_fa) need = layout(d, QWEN35_LAYER_FULL_ATTENTION).total;
+  if (has_gdn && layout(d, QWEN35_LAYER_LINEAR_ATTENTION).total > need)
+    need = layout(d, QWEN35_LAYER_LINEAR_ATTENTION).total;
+  return need;
+}
+size_t batch_need(size_t one, uint32_t batch) { return 256 + (size_t)batch * (one - 256); }
+
+int decode_step(const qwen35_config* cfg, const qwen35_layer* layers, uint32_t num_layers, uint32_t batch,
+                void* scratch, size_t scratch_bytes, const qwen35_bf16* x_in, qwen35_bf16* x_out,
+                int32_t* d_cache_pos, uint32_t max_seq_len, cudaStream_t stream) {
   if (!layers || num_layers == 0 || num_layers > (uint32_t)kMaxLayers || !d_cache_pos ||
-      ((uintptr_t)d_cache_pos % 4) || max_seq_len == 0)
+      ((uintptr_t)d_cache_pos % 4) || max_seq_len == 0 || batch == 0 || batch > (uint32_t)kMaxBatch)
     return QWEN35_ERR_INVALID_ARGUMENT;
   Dims d;
   int r = check_config(cfg, d);
@@ -430,11 +446,8 @@ int qwen35_decode_step(const qwen35_config* cfg, const qwen35_layer* layers, uin
     }
   }
   if (!aligned16(x_in) || !aligned16(x_out) || !aligned16(scratch)) return QWEN35_ERR_INVALID_ARGUMENT;
-  size_t need = 0;
-  if (has_fa) need = layout(d, QWEN35_LAYER_FULL_ATTENTION).total;
-  if (has_gdn && layout(d, QWEN35_LAYER_LINEAR_ATTENTION).total > need)
-    need = layout(d, QWEN35_LAYER_LINEAR_ATTENTION).total;
-  if (scratch_bytes < need) return QWEN35_ERR_INVALID_ARGUMENT;
+  const size_t one = stack_need(d, has_fa, has_gdn);
+  if (scratch_bytes < batch_need(one, batch)) return QWEN35_ERR_INVALID_ARGUMENT;
   if (num_sms() <= 0) return QWEN35_ERR_CUDA;
   Program* p = new_program(cfg, d, scratch);
   if (!p) return QWEN35_ERR_CUDA;
@@ -445,11 +458,35 @@ int qwen35_decode_step(const qwen35_config* cfg, const qwen35_layer* layers, uin
   p->max_seq = max_seq_len;
   p->P = splits_for(max_seq_len);
   p->advance = d_cache_pos;
+  p->batch = batch;
+  p->seq_stride = (uint32_t)(one - 256);
   for (uint32_t i = 0; i < num_layers; ++i) {
     if (layers[i].kind == QWEN35_LAYER_FULL_ATTENTION) fill_fa(p->layers[i], layers[i].fa, layers[i].kv);
     else fill_gdn(p->layers[i], layers[i].gdn, layers[i].state);
   }
-  return launch(p, has_fa, has_gdn, (cudaStream_t)stream);
+  return launch(p, has_fa, has_gdn, stream);
+}
+
+}  // namespace
+
+int qwen35_decode_step(const qwen35_config* cfg, const qwen35_layer* layers, uint32_t num_layers, void* scratch,
+                       size_t scratch_bytes, const qwen35_bf16* x_in, qwen35_bf16* x_out, int32_t* d_cache_pos,
+                       uint32_t max_seq_len, void* stream) {
+  return decode_step(cfg, layers, num_layers, 1, scratch, scratch_bytes, x_in, x_out, d_cache_pos, max_seq_len,
+                     (cudaStream_t)stream);
+}
+
+int qwen35_decode_step_batched(const qwen35_config* cfg, const qwen35_layer* layers, uint32_t num_layers,
+                               uint32_t batch, void* scratch, size_t scratch_bytes, const qwen35_bf16* x_in,
+                               qwen35_bf16* x_out, int32_t* d_cache_pos, uint32_t max_seq_len, void* stream) {
+  return decode_step(cfg, layers, num_layers, batch, scratch, scratch_bytes, x_in, x_out, d_cache_pos, max_seq_len,
+                     (cudaStream_t)stream);
+}
+
+size_t qwen35_stack_scratch_bytes_batched(const qwen35_config* cfg, uint32_t batch) {
+  Dims d;
+  if (!cfg || batch == 0 || batch > (uint32_t)kMaxBatch || check_config(cfg, d) != QWEN35_OK) return 0;
+  return batch_need(stack_need(d, true, true), batch);
 }
 
 struct qwen35_graph {
@@ -457,16 +494,17 @@ struct qwen35_graph {
   cudaGraphExec_t exec;
 };
 
-int qwen35_graph_create(const qwen35_config* cfg, const qwen35_layer* layers, uint32_t num_layers, void* scratch,
-                        size_t scratch_bytes, const qwen35_bf16* x_in, qwen35_bf16* x_out, int32_t* d_cache_pos,
-                        uint32_t max_seq_len, void* stream, qwen35_graph** out_graph) {
+namespace {
+int graph_create(const qwen35_config* cfg, const qwen35_layer* layers, uint32_t num_layers, uint32_t batch,
+                 void* scratch, size_t scratch_bytes, const qwen35_bf16* x_in, qwen35_bf16* x_out,
+                 int32_t* d_cache_pos, uint32_t max_seq_len, void* stream, qwen35_graph** out_graph) {
   if (!out_graph) return QWEN35_ERR_INVALID_ARGUMENT;
   *out_graph = nullptr;
   cudaStream_t st = (cudaStream_t)stream;
   if (st == nullptr) return QWEN35_ERR_INVALID_ARGUMENT;  // the legacy stream cannot be captured
   if (cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal) != cudaSuccess) return QWEN35_ERR_CUDA;
-  int r = qwen35_decode_step(cfg, layers, num_layers, scratch, scratch_bytes, x_in, x_out, d_cache_pos,
-                             max_seq_len, stream);
+  int r = decode_step(cfg, layers, num_layers, batch, scratch, scratch_bytes, x_in, x_out, d_cache_pos, max_seq_len,
+                      st);
   cudaGraph_t g = nullptr;
   cudaError_t e = cudaStreamEndCapture(st, &g);
   if (r != QWEN35_OK) {
@@ -487,6 +525,22 @@ int qwen35_graph_create(const qwen35_config* cfg, const qwen35_layer* layers, ui
   }
   *out_graph = out;
   return QWEN35_OK;
+}
+}  // namespace
+
+int qwen35_graph_create(const qwen35_config* cfg, const qwen35_layer* layers, uint32_t num_layers, void* scratch,
+                        size_t scratch_bytes, const qwen35_bf16* x_in, qwen35_bf16* x_out, int32_t* d_cache_pos,
+                        uint32_t max_seq_len, void* stream, qwen35_graph** out_graph) {
+  return graph_create(cfg, layers, num_layers, 1, scratch, scratch_bytes, x_in, x_out, d_cache_pos, max_seq_len,
+                      stream, out_graph);
+}
+
+int qwen35_graph_create_batched(const qwen35_config* cfg, const qwen35_layer* layers, uint32_t num_layers,
+                                uint32_t batch, void* scratch, size_t scratch_bytes, const qwen35_bf16* x_in,
+                                qwen35_bf16* x_out, int32_t* d_cache_pos, uint32_t max_seq_len, void* stream,
+                                qwen35_graph** out_graph) {
+  return graph_create(cfg, layers, num_layers, batch, scratch, scratch_bytes, x_in, x_out, d_cache_pos, max_seq_len,
+                      stream, out_graph);
 }
 
 int qwen35_graph_launch(qwen35_graph* graph, void* stream) {

@@ -72,8 +72,6 @@ struct Smem {
   uint8_t* ring;
   uint64_t* full;
   uint64_t* empty;
-  uint64_t* gfull;   // linear-attention staging: filled (producer, tx count)
-  uint64_t* gempty;  // linear-attention staging: consumed (thread 0)
   uint32_t* toff;    // ring offset of the tile in each slot (written before its copies)
   uint32_t* tmeta;  // GEMV tiles: first row | rows << 24
   float* misc;     // 256 floats (1 KiB): reductions, gate/beta
@@ -85,9 +83,7 @@ __device__ __forceinline__ Smem smem_map(uint8_t* base) {
   s.ring = base;
   s.full = reinterpret_cast<uint64_t*>(base + kDecRing);
   s.empty = s.full + kDecSlots;
-  s.gfull = s.empty + kDecSlots;
-  s.gempty = s.gfull + 1;
-  s.toff = reinterpret_cast<uint32_t*>(s.gempty + 1);
+  s.toff = reinterpret_cast<uint32_t*>(s.empty + kDecSlots);
   s.tmeta = s.toff + kDecSlots;
   s.misc = reinterpret_cast<float*>(s.tmeta + kDecSlots);
   s.uni = reinterpret_cast<uint8_t*>(s.misc + 256);
@@ -107,13 +103,39 @@ constexpr uint32_t kHeadBytes = (offsetof(Program, layers) + 3) / 4 * 4;
 static_assert(offsetof(Program, layers) % 8 == 0, "layer table alignment");
 __shared__ __align__(16) uint8_t s_head[kHeadBytes];
 __shared__ LayerDesc s_layer;
+__shared__ LayerDesc s_layer0;  // the current layer as the program gives it (sequence 0's caches)
 __device__ __forceinline__ const Program& prog() { return *reinterpret_cast<const Program*>(s_head); }
+
+// The sequence the consumers are working on (a batch runs each phase for its
+// sequences back to back): its scratch block, input and output vectors. The
+// layer's cache pointers in s_layer are rebased to it as well.
+struct SeqCtx {
+  uint8_t* scratch;
+  const uint16_t* x_in;
+  uint16_t* x_out;
+  uint32_t b;
+};
+__shared__ SeqCtx s_seq;
+__shared__ int32_t s_pos[kMaxBatch];  // each sequence's device position, read at launch
+
+// Sequence b's scratch block and its caches in layer L (the caller's [B][...] arrays).
+__device__ __forceinline__ uint8_t* seq_scratch(const Program& P, uint32_t b) {
+  return P.scratch + (size_t)b * P.seq_stride;
+}
+__device__ __forceinline__ void seq_caches(const Program& P, LayerDesc& L, uint32_t b) {
+  if (L.kind == kLayerFA) {
+    const size_t kv = (size_t)L.capacity * P.Hkv * P.D * b;
+    L.kc += kv;
+    L.vc += kv;
+  } else if (L.kind == kLayerGDN) {
+    L.conv_state += (size_t)P.C * P.Kc * b;
+    L.ssm += (size_t)P.Hv * P.Dk * P.Dv * b;
+  }
+}
 
 // misc[255]: the device position, read once per CTA when the launch starts (every
 // phase of the launch sees the same value although CTA 0 advances it at the end)
-__device__ __forceinline__ int32_t launch_pos() {
-  return reinterpret_cast<const int32_t*>(smem_map(smem_raw).misc)[255];
-}
+__device__ __forceinline__ int32_t launch_pos(uint32_t b) { return s_pos[b]; }
 
 // ------------------------------------------------------------------ grid barrier
 
@@ -281,7 +303,7 @@ __device__ __forceinline__ void gemv_add(Gemv& g, const QMat& m, uint16_t* out) 
 
 // The GEMV of phase p of layer l, written into g (shared memory: a returned struct
 // would go through local memory).
-__device__ __noinline__ void gemv_of(const Program& P, const LayerDesc& L, uint32_t l, int p, Gemv& g) {
+__device__ __noinline__ void gemv_of(const Program& P, const LayerDesc& L, uint32_t l, int p, uint32_t sq, Gemv& g) {
   g.nseg = 0;
   g.row0[0] = 0;
   g.b = nullptr;
@@ -290,17 +312,19 @@ __device__ __noinline__ void gemv_of(const Program& P, const LayerDesc& L, uint3
   g.resid_in = nullptr;
   g.head_dim = 0;
   g.epi = 0;
-  uint8_t* S = P.scratch;
+  uint8_t* S = seq_scratch(P, sq);
   const ScratchMap& m = P.sm;
-  const uint16_t* xin = l == 0 ? P.x_in : P.x_out;
+  const uint16_t* x_in = P.x_in + (size_t)sq * P.E;
+  uint16_t* x_out = P.x_out + (size_t)sq * P.E;
+  const uint16_t* xin = l == 0 ? x_in : x_out;
   auto at = [&](uint32_t off) { return reinterpret_cast<uint16_t*>(S + off); };
   const bool fa = L.kind == kLayerFA;
   const int mlp0 = fa ? 4 : 3;  // the gate|up phase
   if (L.kind == kLayerGemv) {
     g.K = P.E;
     g.pro = kPlain;
-    g.a = P.x_in;
-    gemv_add(g, L.m[0], P.x_out);
+    g.a = x_in;
+    gemv_add(g, L.m[0], x_out);
   } else if (p == 0) {
     g.K = P.E;
     g.pro = kRms;
@@ -332,7 +356,7 @@ __device__ __noinline__ void gemv_of(const Program& P, const LayerDesc& L, uint3
     g.a = at(m.g);
     g.b = at(m.u);
     g.resid_in = at(m.x_resid);
-    gemv_add(g, L.m[6], P.x_out);
+    gemv_add(g, L.m[6], x_out);
   } else if (fa) {  // p == 3: o_proj
     g.K = P.H * P.D;
     g.pro = kPlain;
@@ -638,12 +662,11 @@ struct Span {
 };
 
 // The device position as this CTA read it at kernel start (shared memory).
-__device__ __forceinline__ int32_t launch_pos();
 
-__device__ __forceinline__ Span attn_span(const Program& P, uint32_t capacity) {
+__device__ __forceinline__ Span attn_span(const Program& P, uint32_t capacity, uint32_t b) {
   Span sp;
   if (P.d_pos) {
-    const int32_t p = launch_pos();
+    const int32_t p = launch_pos(b);
     const uint32_t lim = min(capacity, P.max_seq);
     sp.ok = p >= 0 && (uint32_t)p < lim;
     sp.pos = sp.ok ? (uint32_t)p : 0;
@@ -732,7 +755,7 @@ __device__ __noinline__ void attn_consume(uint32_t& it, bool& dead, unsigned lon
   constexpr int SH = NV == 8 ? 2 : NV == 16 ? 1 : 0;
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t s = blockIdx.x;
-  const Span sp = attn_span(P, L.capacity);
+  const Span sp = attn_span(P, L.capacity, s_seq.b);
   const uint32_t H = P.H, Hkv = P.Hkv, rowh = Hkv * D, rowbytes = rowh * 2;
   const uint32_t NG = H / HPW, TI = NCW / NG;  // warps beyond NG * TI only keep the ring moving
   if (!sp.ok) {
@@ -756,15 +779,15 @@ __device__ __noinline__ void attn_consume(uint32_t& it, bool& dead, unsigned lon
   const bool active = ti < TI;
   const uint32_t h0 = hg * HPW, g = h0 / (H / Hkv);
   float q[HPW][EPL], m[HPW], l[HPW], acc[HPW][EPL], qw[EPL];
-  const uint16_t* qf = reinterpret_cast<const uint16_t*>(P.scratch + P.sm.q_full);
+  const uint16_t* qf = reinterpret_cast<const uint16_t*>(s_seq.scratch + P.sm.q_full);
 #pragma unroll
   for (int j = 0; j < HPW; ++j) load_row<EPL>(qf + (size_t)(h0 + j) * 2 * D + lane * EPL, q[j]);
   load_row<EPL>(L.q_norm + lane * EPL, qw);
   const bool kv_warp = appender && warp < Hkv;
   float kx[EPL], vx[EPL], kw[EPL];
   if (kv_warp) {
-    load_row<EPL>(reinterpret_cast<const uint16_t*>(P.scratch + P.sm.k) + warp * D + lane * EPL, kx);
-    load_row<EPL>(reinterpret_cast<const uint16_t*>(P.scratch + P.sm.v) + warp * D + lane * EPL, vx);
+    load_row<EPL>(reinterpret_cast<const uint16_t*>(s_seq.scratch + P.sm.k) + warp * D + lane * EPL, kx);
+    load_row<EPL>(reinterpret_cast<const uint16_t*>(s_seq.scratch + P.sm.v) + warp * D + lane * EPL, vx);
     load_row<EPL>(L.k_norm + lane * EPL, kw);
   }
   consumer_sync();  // the angle table
@@ -915,8 +938,8 @@ __device__ __noinline__ void attn_consume(uint32_t& it, bool& dead, unsigned lon
     consumer_sync();
   }
   if (ti == 0) {
-    float* part_o = reinterpret_cast<float*>(P.scratch + P.sm.part_o);
-    float* part_ml = reinterpret_cast<float*>(P.scratch + P.sm.part_ml);
+    float* part_o = reinterpret_cast<float*>(s_seq.scratch + P.sm.part_o);
+    float* part_ml = reinterpret_cast<float*>(s_seq.scratch + P.sm.part_ml);
 #pragma unroll
     for (int j = 0; j < HPW; ++j) {
       const uint32_t h = h0 + j;
@@ -940,16 +963,16 @@ __device__ __noinline__ void combine_consume() {
   const Smem sh = smem_map(smem_raw);
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t nd = P.D / 32, item = blockIdx.x;
-  const Span sp = attn_span(P, L.capacity);
+  const Span sp = attn_span(P, L.capacity, s_seq.b);
   if (item >= P.H * nd) return;
   const uint32_t h = item / nd, d = (item % nd) * 32 + lane;
-  uint16_t* ga = reinterpret_cast<uint16_t*>(P.scratch + P.sm.ga);
+  uint16_t* ga = reinterpret_cast<uint16_t*>(s_seq.scratch + P.sm.ga);
   if (!sp.ok) {
     if (warp == 0) ga[(size_t)h * P.D + d] = 0;
     return;
   }
-  const float* part_o = reinterpret_cast<const float*>(P.scratch + P.sm.part_o);
-  const float* part_ml = reinterpret_cast<const float*>(P.scratch + P.sm.part_ml);
+  const float* part_o = reinterpret_cast<const float*>(s_seq.scratch + P.sm.part_o);
+  const float* part_ml = reinterpret_cast<const float*>(s_seq.scratch + P.sm.part_ml);
   float M = -INFINITY, Ls = 0.f, O = 0.f;
   for (uint32_t base = 0; base < P.P; base += NCW * 4) {
     float ms[4], ls[4], os[4];
@@ -991,7 +1014,7 @@ __device__ __noinline__ void combine_consume() {
       O = fmaf(part[(2 * NCW + w) * 32 + lane], c, O);
     }
     const float attn = round_bf16(O / Ls);
-    const uint16_t* qf = reinterpret_cast<const uint16_t*>(P.scratch + P.sm.q_full);
+    const uint16_t* qf = reinterpret_cast<const uint16_t*>(s_seq.scratch + P.sm.q_full);
     const float gate = bf16f(qf[(size_t)h * 2 * P.D + P.D + d]);
     ga[(size_t)h * P.D + d] = to_bf16(attn * sigmoidf_(gate));
   }
@@ -1008,12 +1031,10 @@ __device__ __noinline__ void combine_consume() {
 // barrier: nothing before it writes the state), updated, and written once.
 constexpr int kGdnWarps = 8;  // warps holding state rows (Dk / 8 rows each)
 // The linear-attention phase's inputs that do not depend on the step's earlier
-// phases (the CTA's state slice [Dk][32] fp32, its channels' convolution state
-// [2 Dk + 32][Kc] fp32 and weights [2 Dk + 32][Kc] bf16) are staged here, in the
-// top 24 KiB of the phase buffer, by bulk copies issued when the layer's
-// input projection phase starts: they land while that phase streams.
-constexpr uint32_t kGdnStageBytes = 24576;
-constexpr uint32_t kGdnStageOff = kDecUnion - kGdnStageBytes;
+// phases (the CTA's state block [Dk][32] fp32, its channels' convolution state
+// [2 Dk + 32][Kc] fp32 and weights [2 Dk + 32][Kc] bf16) come as one ring tile per
+// sequence, right after the layer's input projection tiles.
+__host__ __device__ inline uint32_t gdn_tile_bytes(uint32_t Dk, uint32_t Kc) { return Dk * 128 + (2 * Dk + 32) * Kc * 6; }
 
 // The CTA's linear-attention work item: v-head h, columns [v0, v0 + 32) of its state.
 struct GdnItem {
@@ -1031,32 +1052,6 @@ __device__ __forceinline__ GdnItem gdn_item(const Program& P) {
   return it;
 }
 
-// The producer's copies of a work item's staged inputs (completing on gfull): the
-// state block (contiguous: the state is stored in column blocks of 32), then three
-// channel blocks (the k-head's q channels, its k channels, the slice's v channels)
-// of convolution state and of convolution weights. False if the previous staging
-// was not consumed in time.
-__device__ __forceinline__ bool stage_gdn(const Program& P, const LayerDesc& L, const Smem& sh, uint32_t n) {
-  const GdnItem w = gdn_item(P);
-  if (!w.ok) return true;
-  if (n > 0 && !mbar_wait(sh.gempty, (n - 1) & 1)) return false;
-  const uint32_t Dk = P.Dk, Kc = P.Kc, nch = 2 * Dk + 32;
-  uint8_t* base = sh.uni + kGdnStageOff;
-  uint8_t* cs = base + Dk * 128;
-  uint8_t* cw = cs + nch * Kc * 4;
-  mbar_arrive_expect_tx(sh.gfull, Dk * 128 + nch * Kc * 6);
-  bulk_g2s(base, L.ssm + (size_t)blockIdx.x * Dk * 32, Dk * 128, sh.gfull);
-  const uint32_t ch[3] = {w.hk * Dk, P.Hk * Dk + w.hk * Dk, 2 * P.Hk * Dk + w.h * P.Dv + w.v0};
-  const uint32_t nc[3] = {Dk, Dk, 32};
-  uint32_t done = 0;
-  for (int b = 0; b < 3; ++b) {
-    bulk_g2s(cs + done * Kc * 4, L.conv_state + (size_t)ch[b] * Kc, nc[b] * Kc * 4, sh.gfull);
-    bulk_g2s(cw + done * Kc * 2, L.conv_w + (size_t)ch[b] * Kc, nc[b] * Kc * 2, sh.gfull);
-    done += nc[b];
-  }
-  return true;
-}
-
 // The convolution state of the q/k channels, shifted by one token (newest last):
 // the linear-attention phase reads it in every CTA of the channel's v-heads, so it
 // is written one grid barrier later, in the output projection phase, each CTA
@@ -1067,7 +1062,7 @@ __device__ __noinline__ void conv_shift_qk() {
   const uint32_t lane = threadIdx.x & 31, Kc = P.Kc;
   const uint32_t nqk = 2 * P.Hk * P.Dk, per = (nqk + gridDim.x - 1) / gridDim.x;
   const uint32_t c0 = blockIdx.x * per, c1 = min(nqk, c0 + per);
-  const uint16_t* qkv = reinterpret_cast<const uint16_t*>(P.scratch + P.sm.qkv);
+  const uint16_t* qkv = reinterpret_cast<const uint16_t*>(s_seq.scratch + P.sm.qkv);
   for (uint32_t ch = c0 + lane; ch < c1; ch += 32) {
     float* cs = L.conv_state + (size_t)ch * Kc;
     float v[kMaxKc];
@@ -1080,7 +1075,7 @@ __device__ __noinline__ void conv_shift_qk() {
 }
 
 template <int DK>
-__device__ __noinline__ void gdn_consume(uint32_t n) {
+__device__ __noinline__ void gdn_consume(uint32_t& it, bool& dead) {
   const Program& P = prog();
   const LayerDesc& L = s_layer;
   const Smem sh = smem_map(smem_raw);
@@ -1091,10 +1086,15 @@ __device__ __noinline__ void gdn_consume(uint32_t n) {
   const uint32_t h = w.h, v0 = w.v0, Kc = P.Kc;
   float* act = reinterpret_cast<float*>(sh.uni);  // [2 Dk + 32]
   float* red = act + 2 * DK + 32;                 // [2][NCW][32]
-  const float* st_s = reinterpret_cast<const float*>(sh.uni + kGdnStageOff);
+  const uint32_t slot = slot_of(it);
+  if (!dead && !mbar_wait(&sh.full[slot], parity_of(it))) {
+    set_status(P.status, kStatusTimeout);
+    dead = true;
+  }
+  const float* st_s = reinterpret_cast<const float*>(sh.ring + sh.toff[slot]);
   const float* cs_s = st_s + DK * 32;
   const uint16_t* cw_s = reinterpret_cast<const uint16_t*>(cs_s + (2 * DK + 32) * Kc);
-  const uint16_t* qkv = reinterpret_cast<const uint16_t*>(P.scratch + P.sm.qkv);
+  const uint16_t* qkv = reinterpret_cast<const uint16_t*>(s_seq.scratch + P.sm.qkv);
   // this channel (thread < 2 Dk + 32): q, k of the k-head, v of the slice
   const bool chan = tid < 2 * DK + 32;
   const uint32_t ch = tid < DK ? w.hk * DK + tid
@@ -1106,7 +1106,6 @@ __device__ __noinline__ void gdn_consume(uint32_t n) {
     alog = L.a_log[h];
     dtb = bf16f(L.dt_bias[h]);
   }
-  if (!mbar_wait(sh.gfull, n & 1)) set_status(P.status, kStatusTimeout);  // the staged inputs
   // causal conv update + SiLU
   if (chan) {
     float cst[kMaxKc];
@@ -1129,8 +1128,8 @@ __device__ __noinline__ void gdn_consume(uint32_t n) {
         if (t < (int)Kc) L.conv_state[(size_t)ch * Kc + t] = cst[t];
     }
   }
-  const uint16_t* dtr = reinterpret_cast<const uint16_t*>(P.scratch + P.sm.dt_raw);
-  const uint16_t* brw = reinterpret_cast<const uint16_t*>(P.scratch + P.sm.b_raw);
+  const uint16_t* dtr = reinterpret_cast<const uint16_t*>(s_seq.scratch + P.sm.dt_raw);
+  const uint16_t* brw = reinterpret_cast<const uint16_t*>(s_seq.scratch + P.sm.b_raw);
   if (tid == 0) {
     // gate = exp(softplus(dt + dt_bias) * -exp(A_log)); beta = sigmoid(b)
     const float xd = bf16f(dtr[h]) + dtb;
@@ -1184,7 +1183,8 @@ __device__ __noinline__ void gdn_consume(uint32_t n) {
     red[warp * 32 + lane] = u;
   }
   consumer_sync();
-  if (tid == 0) mbar_arrive(sh.gempty);  // the staged inputs are read
+  if (lane == 0) mbar_arrive(&sh.empty[slot]);  // the tile is read (every warp releases it)
+  ++it;
   u = 0.f;
 #pragma unroll
   for (int w = 0; w < kGdnWarps; ++w) u += red[w * 32 + lane];
@@ -1206,7 +1206,7 @@ __device__ __noinline__ void gdn_consume(uint32_t n) {
     y = 0.f;
 #pragma unroll
     for (int w = 0; w < kGdnWarps; ++w) y += red[kGdnWarps * 32 + w * 32 + lane];
-    uint16_t* yo = reinterpret_cast<uint16_t*>(P.scratch + P.sm.y);
+    uint16_t* yo = reinterpret_cast<uint16_t*>(s_seq.scratch + P.sm.y);
     yo[(size_t)h * P.Dv + v0 + lane] = to_bf16(y * P.gdn_out_scale);
   }
   consumer_sync();
@@ -1214,13 +1214,15 @@ __device__ __noinline__ void gdn_consume(uint32_t n) {
 
 // ------------------------------------------------------------------ producer schedule
 
-// A walk over the CTA's tiles of the whole launch, phase after phase, in the order
-// the consumers take them. It lives in shared memory: the producer thread's local
-// memory would compete for the small L1 left beside the ring, and a walk step that
-// misses L1 costs several L2 round trips per tile.
+// A walk over the CTA's tiles of the whole launch, phase after phase and, within a
+// phase, sequence after sequence, in the order the consumers take them. It lives
+// in shared memory: the producer thread's local memory would compete for the
+// small L1 left beside the ring, and a walk step that misses L1 costs several L2
+// round trips per tile.
 struct Cursor {
   uint32_t l, lc;  // position; the layer whose description L holds
   int p;
+  uint32_t b;  // the sequence within the phase
   bool open;
   int ty;
   LayerDesc L;
@@ -1228,27 +1230,39 @@ struct Cursor {
   uint32_t r, re, seg;
   Span sp;
   uint32_t i;
-  uint32_t ph;      // phases opened (the timeline's phase index + 1)
-  uint32_t nstage;  // linear-attention stagings issued
-  bool stage_dead;  // a staging wait ran out
+  uint32_t ph;  // phases opened (the timeline's phase index + 1)
   bool fresh;   // no tile of the open phase issued yet
   uint32_t vstart[kDecSlots];  // ring placement of the tiles in flight (see produce_all)
 };
-
 __shared__ Cursor s_cursor;
 
-// One tile: up to three contiguous global ranges, where they land in the tile, and
+// One tile: up to seven contiguous global ranges, where they land in the tile, and
 // the bytes the tile takes in the ring.
 struct TileCopy {
-  const void* src[3];
-  uint32_t off[3], bytes[3];
+  const void* src[7];
+  uint32_t off[7], bytes[7];
   uint32_t n, total, span;
-  uint32_t meta;  // GEMV: first row | rows << 24
-  bool weights;   // streamed once per step: evict-first in L2
+  uint32_t meta;    // GEMV: first row | rows << 24
+  uint64_t policy;  // L2 policy of weight copies; 0 = none
 };
 
-// Advance to the next tile; false when the launch has no tiles left.
-__device__ __forceinline__ bool next_copy(const Program& P, const LayerDesc* layers, Cursor& c, TileCopy& tc) {
+// Open (phase, sequence) of the cursor: the tile walk of that sequence.
+__device__ __forceinline__ void open_seq(const Program& P, Cursor& c) {
+  c.i = 0;
+  if (c.ty == kPhGemv) {
+    c.r = c.g.rb;
+    c.re = c.g.re;
+    c.seg = 0;
+  } else if (c.ty == kPhAttn) {
+    c.sp = attn_span(P, c.L.capacity, c.b);
+  }
+}
+
+// Advance to the next tile; false when the launch has no tiles left. Weights are
+// read from HBM by a batch's first pass over a phase and kept in L2 for the others
+// (evict-last), the last pass marking them evict-first.
+__device__ __forceinline__ bool next_copy(const Program& P, const LayerDesc* layers, Cursor& c, TileCopy& tc,
+                                          uint64_t keep, uint64_t stream) {
   while (c.l < P.n_layers) {
     if (c.lc != c.l) {
       c.L = layers[c.l];
@@ -1256,23 +1270,12 @@ __device__ __forceinline__ bool next_copy(const Program& P, const LayerDesc* lay
     }
     if (!c.open) {
       c.ty = phase_type(c.L.kind, c.p);
-      if (c.ty == kPhGemv) {
-        gemv_of(P, c.L, c.l, c.p, c.g);
-        c.r = c.g.rb;
-        c.re = c.g.re;
-        c.seg = 0;
-      } else if (c.ty == kPhAttn) {
-        c.sp = attn_span(P, c.L.capacity);
-        c.i = 0;
-      }
+      if (c.ty == kPhGemv) gemv_of(P, c.L, c.l, c.p, 0, c.g);
+      c.b = 0;
+      open_seq(P, c);
       c.open = true;
       c.fresh = true;
       ++c.ph;
-      // a linear-attention layer's staged inputs, ahead of its input projection
-      if (c.L.kind == kLayerGDN && c.p == 0) {
-        if (!stage_gdn(P, c.L, smem_map(smem_raw), c.nstage)) c.stage_dead = true;
-        ++c.nstage;
-      }
     }
     if (c.ty == kPhGemv) {
       uint32_t r = c.r, seg = c.seg;
@@ -1295,27 +1298,63 @@ __device__ __forceinline__ bool next_copy(const Program& P, const LayerDesc* lay
         tc.total = cb + 2 * sb;
         tc.span = c.g.bias_off + c.g.R * gstride * 2;
         tc.meta = t.r | (t.nr << 24);
-        tc.weights = true;
+        tc.policy = c.b + 1 < P.batch ? keep : stream;
         return true;
       }
     } else if (c.ty == kPhAttn) {
       if (c.i < c.sp.ntiles) {
+        LayerDesc q = c.L;
+        seq_caches(P, q, c.b);
         const uint32_t rowh = P.Hkv * P.D, rowbytes = rowh * 2;
         const uint32_t tt = c.sp.t0 + c.i * kTS;
         const uint32_t n = min((uint32_t)kTS, c.sp.tc_end - tt);
         tc.n = 2;
-        tc.src[0] = c.L.kc + (size_t)tt * rowh;
-        tc.src[1] = c.L.vc + (size_t)tt * rowh;
+        tc.src[0] = q.kc + (size_t)tt * rowh;
+        tc.src[1] = q.vc + (size_t)tt * rowh;
         tc.off[0] = 0;
         tc.off[1] = kTS * rowbytes;
         tc.bytes[0] = tc.bytes[1] = n * rowbytes;
         tc.total = 2 * n * rowbytes;
         tc.span = 2 * kTS * rowbytes;  // rows past n are read (masked) by the consumers
         tc.meta = 0;
-        tc.weights = false;
+        tc.policy = 0;
         ++c.i;
         return true;
       }
+    } else if (c.ty == kPhGdn) {
+      const GdnItem w = gdn_item(P);
+      if (c.i == 0 && w.ok) {  // the work item's state block, conv state and weights
+        LayerDesc q = c.L;
+        seq_caches(P, q, c.b);
+        const uint32_t Dk = P.Dk, Kc = P.Kc, nch = 2 * Dk + 32;
+        const uint32_t ch[3] = {w.hk * Dk, P.Hk * Dk + w.hk * Dk, 2 * P.Hk * Dk + w.h * P.Dv + w.v0};
+        const uint32_t nc[3] = {Dk, Dk, 32};
+        tc.n = 7;
+        tc.src[0] = q.ssm + (size_t)blockIdx.x * Dk * 32;
+        tc.off[0] = 0;
+        tc.bytes[0] = Dk * 128;
+        uint32_t done = 0;
+        for (int j = 0; j < 3; ++j) {
+          tc.src[1 + j] = q.conv_state + (size_t)ch[j] * Kc;
+          tc.off[1 + j] = Dk * 128 + done * Kc * 4;
+          tc.bytes[1 + j] = nc[j] * Kc * 4;
+          tc.src[4 + j] = q.conv_w + (size_t)ch[j] * Kc;
+          tc.off[4 + j] = Dk * 128 + nch * Kc * 4 + done * Kc * 2;
+          tc.bytes[4 + j] = nc[j] * Kc * 2;
+          done += nc[j];
+        }
+        tc.total = gdn_tile_bytes(Dk, Kc);
+        tc.span = tc.total;
+        tc.meta = 0;
+        tc.policy = 0;
+        c.i = 1;
+        return true;
+      }
+    }
+    // this sequence's walk of the phase is done: the next sequence, or the next phase
+    if (++c.b < P.batch) {
+      open_seq(P, c);
+      continue;
     }
     c.open = false;
     if (++c.p >= n_phases(c.L.kind)) {
@@ -1337,23 +1376,16 @@ __device__ __noinline__ void produce_all(const LayerDesc* layers) {
   const Program& P = prog();
   const Smem sh = smem_map(smem_raw);
   Cursor& c = s_cursor;
-  const uint64_t pol = policy_evict_first();
+  const uint64_t stream = policy_evict_first(), keep = policy_evict_last();
   c.l = 0;
   c.lc = 0xffffffffu;
   c.p = 0;
   c.open = false;
   c.ph = 0;
-  c.nstage = 0;
-  c.stage_dead = false;
   uint32_t i = 0, tail = 0, vnext = 0, vcons = 0;
   bool dead = false;
   TileCopy tc;
-  while (!dead && next_copy(P, layers, c, tc)) {
-    if (c.stage_dead) {
-      set_status(P.status, kStatusTimeout);
-      dead = true;
-      break;
-    }
+  while (!dead && next_copy(P, layers, c, tc, keep, stream)) {
     const uint32_t span = (tc.span + 127) & ~127u;
     uint32_t v = vnext, ph = v % kDecRing;
     if (ph + span > (uint32_t)kDecRing) {
@@ -1383,7 +1415,7 @@ __device__ __noinline__ void produce_all(const LayerDesc* layers) {
     mbar_arrive_expect_tx(&sh.full[st], tc.total);
     for (uint32_t j = 0; j < tc.n; ++j) {
       const uint8_t* src = static_cast<const uint8_t*>(tc.src[j]);
-      if (tc.weights) bulk_g2s_stream(dst + tc.off[j], src, tc.bytes[j], &sh.full[st], pol);
+      if (tc.policy) bulk_g2s_stream(dst + tc.off[j], src, tc.bytes[j], &sh.full[st], tc.policy);
       else bulk_g2s(dst + tc.off[j], src, tc.bytes[j], &sh.full[st]);
     }
     vnext = v + span;
@@ -1396,7 +1428,7 @@ __device__ __noinline__ void produce_all(const LayerDesc* layers) {
 
 // ------------------------------------------------------------------ the kernel
 
-template <int D, int HPW, int DK>
+template <int D, int HPW, int DK, bool BATCHED>
 __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_constant__ Program Pk) {
   const Smem sh = smem_map(smem_raw);
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1410,11 +1442,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
       mbar_init(&sh.full[s], 1);
       mbar_init(&sh.empty[s], NCW);
     }
-    mbar_init(sh.gfull, 1);
-    mbar_init(sh.gempty, 1);
     mbar_fence_init();
-    reinterpret_cast<int32_t*>(sh.misc)[255] = Pk.d_pos ? *Pk.d_pos : 0;
   }
+  if (threadIdx.x < Pk.batch) s_pos[threadIdx.x] = Pk.d_pos ? Pk.d_pos[threadIdx.x] : 0;
   __syncthreads();
 
   if (warp == NCW) {
@@ -1424,10 +1454,11 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
   }
 
   // -------------------------------------------------- consumers: the phases in order
-  // Between the two halves of each grid barrier thread 0 fetches the coming phase's
-  // descriptions (the layer's, the GEMV's) and a GDN phase issues its state loads:
-  // neither depends on the other CTAs, and the wait hides them.
-  uint32_t it = 0, nbar = 0, ph = 0, nstage = 0;
+  // Each phase runs for the batch's sequences back to back (they are independent);
+  // dependent phases are separated by a grid barrier. Between its two halves
+  // thread 0 fetches the coming phase's descriptions (the layer's, rebased to the
+  // first sequence, and the GEMV's): they do not depend on the other CTAs.
+  uint32_t it = 0, nbar = 0, ph = 0;
   bool dead = false;
   auto mark = [&](uint32_t k) {
     if (P.trace && threadIdx.x == 0 && ph < P.trace_phases)
@@ -1437,25 +1468,41 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
     return P.trace && ph < P.trace_phases ? P.trace + ((size_t)blockIdx.x * P.trace_phases + ph) * kTraceSlots
                                           : nullptr;
   };
-  auto describe = [&](uint32_t l, int p) {  // thread 0
-    if (p == 0) s_layer = Pk.layers[l];
-    if (phase_type(s_layer.kind, p) == kPhGemv) gemv_of(P, s_layer, l, p, s_gemv);
+  auto set_seq = [&](uint32_t l, int p, uint32_t b) {  // thread 0
+    if (p == 0 && b == 0) {  // once per layer from the parameter block
+      s_layer0 = Pk.layers[l];
+      s_layer = s_layer0;
+    } else if (BATCHED) {
+      s_layer = s_layer0;
+      seq_caches(P, s_layer, b);
+    }
+    s_seq.scratch = seq_scratch(P, b);
+    s_seq.x_in = P.x_in + (size_t)b * P.E;
+    s_seq.x_out = P.x_out + (size_t)b * P.E;
+    s_seq.b = b;
+    if (phase_type(s_layer.kind, p) == kPhGemv) gemv_of(P, s_layer, l, p, b, s_gemv);
   };
-  if (threadIdx.x == 0 && P.n_layers > 0) describe(0, 0);
+  if (threadIdx.x == 0 && P.n_layers > 0) set_seq(0, 0, 0);
   for (uint32_t l = 0; l < P.n_layers; ++l) {
     for (int p = 0;; ++p, ++ph) {
       if (l > 0 || p > 0) {
         mark(0);
         grid_arrive(P);
-        if (threadIdx.x == 0) describe(l, p);
+        if (threadIdx.x == 0) set_seq(l, p, 0);
         grid_wait(P, ++nbar * gridDim.x);
         mark(1);
       } else {
         consumer_sync();
         mark(1);
       }
-      {
-        const int ty = phase_type(s_layer.kind, p);
+      const int ty = phase_type(s_layer.kind, p);
+      const uint32_t nb = BATCHED ? P.batch : 1u;
+      for (uint32_t b = 0; b < nb; ++b) {
+        if (b > 0) {  // the next sequence: its descriptions, once every warp is done with the last
+          consumer_sync();
+          if (threadIdx.x == 0) set_seq(l, p, b);
+          consumer_sync();
+        }
         if (s_layer.kind == kLayerGDN && p == 2 && warp == NCW - 1) conv_shift_qk();
         if (ty == kPhGemv) {
           gemv_prologue(slots());
@@ -1464,12 +1511,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
         } else if (ty == kPhAttn) {
           attn_consume<D, HPW>(it, dead, slots());
         } else if (ty == kPhGdn) {
-          gdn_consume<DK>(nstage++);
+          gdn_consume<DK>(it, dead);
         } else {
           combine_consume();
         }
-        mark(2);
       }
+      mark(2);
       if (p + 1 >= n_phases(s_layer.kind)) {
         ++ph;
         break;
@@ -1477,33 +1524,36 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
     }
   }
   consumer_sync();
-  if (P.advance && blockIdx.x == 0 && threadIdx.x == 0) *P.advance += 1;
+  if (P.advance && blockIdx.x == 0 && threadIdx.x < P.batch) P.advance[threadIdx.x] += 1;
 }
 
 using DecodeKernel = void (*)(Program);
 
-template <int D, int HPW>
+template <int D, int HPW, bool BT>
 DecodeKernel pick_dk(uint32_t Dk) {
   switch (Dk) {
-    case 32: return decode_kernel<D, HPW, 32>;
-    case 64: return decode_kernel<D, HPW, 64>;
-    case 128: return decode_kernel<D, HPW, 128>;
+    case 32: return decode_kernel<D, HPW, 32, BT>;
+    case 64: return decode_kernel<D, HPW, 64, BT>;
+    case 128: return decode_kernel<D, HPW, 128, BT>;
   }
   return nullptr;
 }
 template <int D>
-DecodeKernel pick_h(uint32_t hpw, uint32_t Dk) {
+DecodeKernel pick_h(uint32_t hpw, uint32_t Dk, bool batched) {
   switch (hpw) {
-    case 1: return pick_dk<D, 1>(Dk);
-    case 2: return pick_dk<D, 2>(Dk);
+    case 1: return batched ? pick_dk<D, 1, true>(Dk) : pick_dk<D, 1, false>(Dk);
+    case 2: return batched ? pick_dk<D, 2, true>(Dk) : pick_dk<D, 2, false>(Dk);
   }
   return nullptr;
 }
-DecodeKernel pick(uint32_t D, uint32_t hpw, uint32_t Dk) {
+// The instantiation for a program: attention head dim and q-heads per warp, GDN
+// key head dim, and whether it decodes a batch of sequences (the single-sequence
+// kernel has no sequence loop).
+DecodeKernel pick(uint32_t D, uint32_t hpw, uint32_t Dk, bool batched) {
   switch (D) {
-    case 64: return pick_h<64>(hpw, Dk);
-    case 128: return pick_h<128>(hpw, Dk);
-    case 256: return pick_h<256>(hpw, Dk);
+    case 64: return pick_h<64>(hpw, Dk, batched);
+    case 128: return pick_h<128>(hpw, Dk, batched);
+    case 256: return pick_h<256>(hpw, Dk, batched);
   }
   return nullptr;
 }
@@ -1525,9 +1575,7 @@ uint32_t attn_hpw(uint32_t H, uint32_t Hkv) {
 bool decode_dims_ok(const Program& p, bool has_fa, bool has_gdn, int num_sms) {
   // a GEMV phase of K columns and N rows: its tile fits a ring tile, its input
   // chunks, the CTA's partial sums and residual rows fit the phase buffer
-  // with linear-attention layers the top of the phase buffer holds staged
-  // inputs that the producer may write during any earlier phase
-  const uint32_t room = has_gdn ? kGdnStageOff : (uint32_t)kDecUnion;
+  const uint32_t room = kDecUnion;
   auto gemv_ok = [&](uint32_t K, uint32_t N) {
     if (K == 0 || K % 64 || K > 12288 || N == 0 || N >= (1u << 24) || num_sms <= 0) return false;
     const uint32_t nch = K / 16;
@@ -1577,7 +1625,7 @@ bool decode_dims_ok(const Program& p, bool has_fa, bool has_gdn, int num_sms) {
     const uint32_t m = p.Dv / 16;
     if (m > 32 || (m & (m - 1))) return false;  // a head's chunks on adjacent lanes
     if ((2 * p.Dk + 32) > (uint32_t)NCT) return false;
-    if (p.Dk * 128 + (2 * p.Dk + 32) * p.Kc * 6 > kGdnStageBytes) return false;
+    if (gdn_tile_bytes(p.Dk, p.Kc) > (uint32_t)kDecTileMax) return false;  // one ring tile
   }
   return true;
 }
@@ -1586,12 +1634,13 @@ cudaError_t decode_set_attributes() {
   const uint32_t Ds[3] = {64, 128, 256}, Hs[2] = {1, 2}, Dks[3] = {32, 64, 128};
   for (uint32_t d : Ds)
     for (uint32_t h : Hs)
-      for (uint32_t k : Dks) {
-        DecodeKernel f = pick(d, h, k);
-        if (!f) continue;
-        cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmem);
-        if (e != cudaSuccess) return e;
-      }
+      for (uint32_t k : Dks)
+        for (bool bt : {false, true}) {
+          DecodeKernel f = pick(d, h, k, bt);
+          if (!f) continue;
+          cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmem);
+          if (e != cudaSuccess) return e;
+        }
   return cudaSuccess;
 }
 
@@ -1601,7 +1650,7 @@ cudaError_t decode_launch(const Program& p, int num_sms, cudaStream_t stream) {
   const uint32_t hpw = attn_hpw(p.H, p.Hkv);
   const uint32_t D = (p.D == 64 || p.D == 128 || p.D == 256) ? p.D : 256;
   const uint32_t Dk = (p.Dk == 32 || p.Dk == 64 || p.Dk == 128) ? p.Dk : 128;
-  DecodeKernel f = pick(D, hpw ? hpw : 1, Dk);
+  DecodeKernel f = pick(D, hpw ? hpw : 1, Dk, p.batch > 1);
   if (!f) return cudaErrorInvalidValue;
   cudaError_t e = cudaMemsetAsync(p.barrier, 0, sizeof(uint32_t), stream);
   if (e != cudaSuccess) return e;

@@ -8,6 +8,7 @@
 namespace q35 {
 
 constexpr int kMaxLayers = 64;
+constexpr int kMaxBatch = 8;  // sequences decoded together (their own caches, shared weights)
 constexpr int kTraceSlots = 16;  // timeline entries per CTA and phase
 constexpr int kDecMaxSplits = 512;  // split-KV partials the scratch holds
 
@@ -54,10 +55,13 @@ struct Program {
   ScratchMap sm;
   int* status;
   uint32_t* barrier;  // grid-barrier counter, zero at launch
-  // position: host values, or *d_pos (seq_len = *d_pos + 1) bounded by max_seq
+  // position: host values, or d_pos[b] (seq_len = d_pos[b] + 1) bounded by max_seq
   uint32_t pos, S, max_seq, P;
   const int32_t* d_pos;
-  int32_t* advance;  // incremented by one after the last layer, or null
+  int32_t* advance;  // advance[b] incremented by one after the last layer, or null
+  // batch: sequence b's intermediates at scratch + b * seq_stride, vectors at
+  // x_in/x_out + b * E, caches at the layer's pointers + b * (one sequence's size)
+  uint32_t batch, seq_stride;
   float inv_freq[128];
   // optional phase timeline: trace[(cta * trace_phases + phase) * kTraceSlots + k],
   // k = 0 barrier arrival, 1 barrier release, 2 phase end, 3 GEMV input formed,

@@ -234,7 +234,7 @@ QWEN35_API int qwen35_forward_linear_attention_static(const qwen35_config* cfg,
 /* One decode step of a layer stack: layer i's output is layer i+1's input (the
  * caller's layer loop, which the module page leaves to the caller). Full-attention
  * layers use the device position *d_cache_pos (as in the _dpos forward); after
- * the last layer a final kernel advances *d_cache_pos by one, so the same enqueued
+ * the last layer the kernel advances *d_cache_pos by one, so the same enqueued
  * sequence (or a graph of it) decodes consecutive tokens. x_in [hidden] is read by
  * layer 0; x_out [hidden] receives every layer's output in turn (it may equal
  * x_in). Scratch: qwen35_stack_scratch_bytes. */
@@ -254,6 +254,34 @@ QWEN35_API int qwen35_graph_create(const qwen35_config* cfg, const qwen35_layer*
                         qwen35_graph** out_graph);
 QWEN35_API int qwen35_graph_launch(qwen35_graph* graph, void* stream);
 QWEN35_API int qwen35_graph_destroy(qwen35_graph* graph);
+
+/* Several independent sequences decoded in one step (multi-sequence decode: each
+ * sequence has its own position, KV caches and linear-attention states; the
+ * weights are shared and streamed from HBM once per step, the batch's later
+ * passes over a layer's weights being served from L2). Every phase of the
+ * stack runs for the batch's sequences back to back, so the grid barriers are
+ * shared by the batch.
+ *  - batch: 1..8 sequences.
+ *  - x_in, x_out: [batch][hidden]; d_cache_pos: [batch] int32 (each advanced by
+ *    one after the last layer); max_seq_len bounds every sequence's position.
+ *  - layers: as for qwen35_decode_step, with every cache holding the batch's
+ *    sequences contiguously, sequence b at the given pointer plus b times one
+ *    sequence's size: kv->k and kv->v [batch][capacity][Hkv][D] (capacity shared);
+ *    conv_state [batch][C][conv_kernel_size]; gdn_state [batch][Hv][Dv/32][Dk][32].
+ *  - scratch: qwen35_stack_scratch_bytes_batched(cfg, batch).
+ * Errors as qwen35_decode_step; batch outside 1..8 is INVALID_ARGUMENT. Sequence b
+ * computes exactly what qwen35_decode_step computes for it alone. */
+QWEN35_API size_t qwen35_stack_scratch_bytes_batched(const qwen35_config* cfg, uint32_t batch);
+QWEN35_API int qwen35_decode_step_batched(const qwen35_config* cfg, const qwen35_layer* layers,
+                       uint32_t num_layers, uint32_t batch, void* scratch, size_t scratch_bytes,
+                       const qwen35_bf16* x_in, qwen35_bf16* x_out,
+                       int32_t* d_cache_pos, uint32_t max_seq_len, void* stream);
+/* A CUDA graph of one qwen35_decode_step_batched (as qwen35_graph_create). */
+QWEN35_API int qwen35_graph_create_batched(const qwen35_config* cfg, const qwen35_layer* layers,
+                        uint32_t num_layers, uint32_t batch, void* scratch, size_t scratch_bytes,
+                        const qwen35_bf16* x_in, qwen35_bf16* x_out,
+                        int32_t* d_cache_pos, uint32_t max_seq_len, void* stream,
+                        qwen35_graph** out_graph);
 
 /* The quantised GEMV on its own (QuantWeights::gemv): y[n] = bf16(W x), x bf16 [k]. */
 QWEN35_API int qwen35_gemv(const qwen35_qweight* w, const qwen35_bf16* x, qwen35_bf16* y, void* scratch,

@@ -308,3 +308,126 @@ def test_stack_4b_teacher_forced_per_layer():
         x_layer = got
     assert int(d_pos.item()) == prefill + 1
     assert B.qwen35_read_device_status(scratch) == 0
+
+
+# ------------------------------------------------------------------ multi-sequence batch (config 4b)
+
+
+def _batch_case(cfg_name, n_layers, positions, cap, seeds):
+    """Layers shared by the batch; per sequence its own caches at its own position."""
+    cfg = synth.config(cfg_name)
+    kinds = synth.layer_kinds(cfg)[:n_layers]
+    cfg = dict(cfg, num_layers=len(kinds))
+    layers, dev = [], []
+    per_seq = [[] for _ in positions]  # per sequence: its numpy caches per layer
+    for i, kind in enumerate(kinds):
+        if kind == "fa":
+            layers.append(synth.fa_layer(0, i, cfg))
+            dev.append(B.DeviceFaLayer(layers[-1]))
+            for s, (pos, sd) in enumerate(zip(positions, seeds)):
+                per_seq[s].append(synth.kv_cache(sd, i, cfg, cap, pos))
+        else:
+            layers.append(synth.gdn_layer(0, i, cfg))
+            dev.append(B.DeviceGdnLayer(layers[-1]))
+            for s, sd in enumerate(seeds):
+                per_seq[s].append(synth.gdn_state(sd, i, cfg, std=0.1))
+    return cfg, kinds, layers, dev, per_seq
+
+
+@pytest.mark.parametrize("cfg_name,n_layers,positions,use_graph",
+                         [("tiny", 2, [0, 5, 11], False), ("tiny", 2, [3, 0, 7], True),
+                          ("4b", 4, [1000, 3100, 257, 2048], False)])
+def test_batch_equals_single_sequence_decodes(cfg_name, n_layers, positions, use_graph):
+    init()
+    nb, steps = len(positions), 3
+    cap = max(positions) + steps + 8
+    seeds = [10 + s for s in range(nb)]
+    cfg, kinds, layers, dev, per_seq = _batch_case(cfg_name, n_layers, positions, cap, seeds)
+    c = B.make_config(cfg)
+    E = cfg["hidden"]
+    # the batch: caches stacked per layer
+    bcaches = []
+    for i, kind in enumerate(kinds):
+        if kind == "fa":
+            bcaches.append(B.DeviceKvBatch([per_seq[s][i][0] for s in range(nb)], [per_seq[s][i][1] for s in range(nb)]))
+        else:
+            bcaches.append(B.DeviceStateBatch([per_seq[s][i][0] for s in range(nb)],
+                                              [per_seq[s][i][1] for s in range(nb)]))
+    bent = [B.stack_layer(k, d, cc) for k, d, cc in zip(kinds, dev, bcaches)]
+    bscr = B.new_scratch(B.qwen35_stack_scratch_bytes_batched(c, nb))
+    bx_in = torch.empty(nb * E, dtype=torch.int16, device="cuda")
+    bx_out = torch.empty_like(bx_in)
+    bpos = torch.tensor(positions, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.Stream()
+    g = None
+    if use_graph:
+        with torch.cuda.stream(stream):
+            g = B.Graph(c, bent, bscr, bx_in, bx_out, bpos, cap, batch=nb)
+    # the same sequences one at a time
+    singles = []
+    for s in range(nb):
+        caches = []
+        for i, kind in enumerate(kinds):
+            caches.append(B.DeviceKv(*per_seq[s][i]) if kind == "fa" else B.DeviceState(*per_seq[s][i]))
+        ent = [B.stack_layer(k, d, cc) for k, d, cc in zip(kinds, dev, caches)]
+        singles.append(dict(caches=caches, ent=ent, scr=B.new_scratch(B.qwen35_stack_scratch_bytes(c)),
+                            x_in=torch.empty(E, dtype=torch.int16, device="cuda"),
+                            x_out=torch.empty(E, dtype=torch.int16, device="cuda"),
+                            pos=torch.tensor([positions[s]], dtype=torch.int32, device="cuda")))
+    for t in range(steps):
+        xs = [synth.x_in(seeds[s], t, cfg) for s in range(nb)]
+        with torch.cuda.stream(stream):
+            bx_in.copy_(B.to_device(np.concatenate(xs)))
+            if g is not None:
+                g.launch(stream)
+            else:
+                assert B.qwen35_decode_step_batched(c, bent, nb, bscr, bx_in, bx_out, bpos, cap, stream) == 0
+            for s, sg in enumerate(singles):
+                sg["x_in"].copy_(B.to_device(xs[s]))
+                assert B.qwen35_decode_step(c, sg["ent"], sg["scr"], sg["x_in"], sg["x_out"], sg["pos"], cap,
+                                            stream) == 0
+        stream.synchronize()
+        bo = bits(bx_out).reshape(nb, E)
+        for s, sg in enumerate(singles):
+            np.testing.assert_array_equal(bo[s], bits(sg["x_out"]), err_msg=f"step {t} sequence {s}")
+    assert bpos.tolist() == [p + steps for p in positions]
+    for i, kind in enumerate(kinds):
+        for s, sg in enumerate(singles):
+            if kind == "fa":
+                np.testing.assert_array_equal(bits(bcaches[i].k)[s], bits(sg["caches"][i].k))
+                np.testing.assert_array_equal(bits(bcaches[i].v)[s], bits(sg["caches"][i].v))
+            else:
+                assert torch.equal(bcaches[i].ssm_matrix(s), sg["caches"][i].ssm_matrix())
+                assert torch.equal(bcaches[i].conv[s], sg["caches"][i].conv)
+    assert B.qwen35_read_device_status(bscr, stream) == 0
+    if g is not None:
+        g.close()
+
+
+def test_batch_sequence_matches_oracle():
+    # a batched sequence against the oracle stack (tiny dims, 3 sequences, 8 steps)
+    init()
+    positions, steps = [2, 0, 6], 8
+    nb, cap = len(positions), 6 + steps + 4
+    seeds = [20, 21, 22]
+    cfg, kinds, layers, dev, per_seq = _batch_case("tiny", 2, positions, cap, seeds)
+    c = B.make_config(cfg)
+    E = cfg["hidden"]
+    bcaches = [B.DeviceStateBatch([per_seq[s][0][0] for s in range(nb)], [per_seq[s][0][1] for s in range(nb)]),
+               B.DeviceKvBatch([per_seq[s][1][0] for s in range(nb)], [per_seq[s][1][1] for s in range(nb)])]
+    bent = [B.stack_layer(k, d, cc) for k, d, cc in zip(kinds, dev, bcaches)]
+    bscr = B.new_scratch(B.qwen35_stack_scratch_bytes_batched(c, nb))
+    bx_in = torch.empty(nb * E, dtype=torch.int16, device="cuda")
+    bx_out = torch.empty_like(bx_in)
+    bpos = torch.tensor(positions, dtype=torch.int32, device="cuda")
+    s = 2  # the sequence checked against the oracle
+    oc = [O.state_from_arrays(*per_seq[s][0]), O.kv_from_bits(*per_seq[s][1])]
+    for t in range(steps):
+        xs = [synth.x_in(seeds[q], t, cfg) for q in range(nb)]
+        bx_in.copy_(B.to_device(np.concatenate(xs)))
+        assert B.qwen35_decode_step_batched(c, bent, nb, bscr, bx_in, bx_out, bpos, cap) == 0
+        ref = O.decode_step(cfg, kinds, layers, oc, O.bf16_to_f64(xs[s]), positions[s] + t)
+        torch.cuda.synchronize()
+        assert rel_l2(O.bf16_to_f64(bits(bx_out).reshape(nb, E)[s]), ref) <= TOL_X, t
+    assert rel_l2(f32(bcaches[0].ssm_matrix(s)), oc[0]["ssm"]) <= TOL_STATE
+    assert B.qwen35_read_device_status(bscr) == 0
