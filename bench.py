@@ -107,7 +107,7 @@ def algorithmic_bytes(cfg: dict, seq_len: int, kinds: list | None = None) -> dic
     return {"weights": weights, "gemv_weights": n_fa * (q(2 * H * D, E) + 2 * q(Hkv * D, E) + q(E, H * D) + mlp)
             + n_gdn * (q(Hv, E) * 2 + q(C, E) + q(Hv * Dv, E) + q(E, Hv * Dv) + mlp),
             "step": weights + n_gdn * gdn_state + n_fa * kv(seq_len), "fa_layer_w": fa_w, "gdn_layer_w": gdn_w,
-            "gdn_state": gdn_state}
+            "gdn_state": gdn_state, "gdn_state_all": n_gdn * gdn_state}
 
 
 # ---------------------------------------------------------------------- clocks
@@ -185,34 +185,54 @@ def run_gpu(args) -> dict | None:
     kinds = synth.layer_kinds(cfg)[:args.layers]
     cfg = dict(cfg, num_layers=len(kinds))
     c = B.make_config(cfg)
-    cap = PREFILL + args.warmup + args.steps + 2 * (args.steps + 4) + 8
-    seed = SEED + rank  # each replica decodes its own sequence
+    nb = args.batch
+    seed = SEED + rank  # each replica decodes its own sequences
+    if nb > 1:  # each sequence at its own position, U{1024..65536}, seeded
+        positions = [int(p) for p in np.random.default_rng([seed, 4242]).integers(1024, 65537, size=nb)]
+    else:
+        positions = [args.prefill]
+    grow = args.warmup + args.steps + 2 * (args.steps + 4) + 8
+    cap = max(positions) + grow
     t0 = time.time()
     dev_layers, caches, entries = [], [], []
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(seed)
+    device_fill = nb > 1 or args.prefill != PREFILL  # large caches: filled on the device (seeded)
     for i, kind in enumerate(kinds):
         if kind == "fa":
             dl = B.DeviceFaLayer(synth.fa_layer(seed, i, cfg))
-            kb, vb = synth.kv_cache(seed, i, cfg, cap, PREFILL)
-            cc = B.DeviceKv(kb, vb)
+            if device_fill:
+                shape = (nb, cap, cfg["num_kv_heads"], cfg["head_dim"])
+                cc = B.DeviceKvBatch.__new__(B.DeviceKvBatch)
+                cc.k = torch.randn(shape, generator=gen, device="cuda", dtype=torch.bfloat16).view(torch.int16)
+                cc.v = torch.randn(shape, generator=gen, device="cuda", dtype=torch.bfloat16).view(torch.int16)
+                cc.struct = B.qwen35_kv_cache(cc.k.data_ptr(), cc.v.data_ptr(), cap)
+            else:
+                kb, vb = synth.kv_cache(seed, i, cfg, cap, PREFILL)
+                cc = B.DeviceKv(kb, vb)
         else:
             dl = B.DeviceGdnLayer(synth.gdn_layer(seed, i, cfg))
-            conv, ssm = synth.gdn_state(seed, i, cfg, std=0.1)
-            cc = B.DeviceState(conv, ssm)
+            if nb > 1:
+                conv, ssm = synth.gdn_state(seed, i, cfg, std=0.1)
+                cc = B.DeviceStateBatch([conv] * nb, [ssm] * nb)
+            else:
+                conv, ssm = synth.gdn_state(seed, i, cfg, std=0.1)
+                cc = B.DeviceState(conv, ssm)
         dev_layers.append(dl)
         caches.append(cc)
         entries.append(B.stack_layer(kind, dl, cc))
     setup_s = time.time() - t0
 
     stream = torch.cuda.Stream()
-    scratch = B.new_scratch(B.qwen35_stack_scratch_bytes(c), stream=stream)
-    x_in = torch.empty(cfg["hidden"], dtype=torch.int16, device="cuda")
+    scratch = B.new_scratch(B.qwen35_stack_scratch_bytes_batched(c, nb), stream=stream)
+    x_in = torch.empty(nb * cfg["hidden"], dtype=torch.int16, device="cuda")
     x_out = torch.empty_like(x_in)
-    d_pos = torch.full((1,), PREFILL, dtype=torch.int32, device="cuda")
+    d_pos = torch.tensor(positions, dtype=torch.int32, device="cuda")
     with torch.cuda.stream(stream):
-        x_in.copy_(B.to_device(synth.x_in(seed, 0, cfg)))
+        x_in.copy_(B.to_device(np.concatenate([synth.x_in(seed + 97 * b, 0, cfg) for b in range(nb)])))
     stream.synchronize()
     with torch.cuda.stream(stream):
-        graph = B.Graph(c, entries, scratch, x_in, x_out, d_pos, cap)
+        graph = B.Graph(c, entries, scratch, x_in, x_out, d_pos, cap, batch=nb)
 
     def barrier():
         if dist is not None:
@@ -223,7 +243,7 @@ def run_gpu(args) -> dict | None:
     for _ in range(args.warmup):
         graph.launch(stream)
     barrier()
-    pos0 = PREFILL + args.warmup
+    pos0 = positions[0] + args.warmup
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with Clocks(local) as clk:
         ev0.record(stream)
@@ -246,7 +266,7 @@ def run_gpu(args) -> dict | None:
     # input vector, the graph, D2H of its output, every step
     h_in = torch.empty_like(x_in, device="cpu").pin_memory()
     h_out = torch.empty_like(x_out, device="cpu").pin_memory()
-    h_in.copy_(torch.from_numpy(synth.x_in(seed, 1, cfg).view(np.int16)))
+    h_in.copy_(torch.from_numpy(np.concatenate([synth.x_in(seed + 97 * b, 1, cfg) for b in range(nb)]).view(np.int16)))
     barrier()
     t_e0 = time.perf_counter()
     for _ in range(args.steps):
@@ -291,17 +311,24 @@ def run_gpu(args) -> dict | None:
         return None
 
     peak, peak_kind = _peaks()
-    seq_mid = pos0 + args.steps // 2 + 1
-    ab = algorithmic_bytes(cfg, seq_mid, kinds)
-    traffic, traffic_note = profiled_traffic(ab["step"])
-    tok_s = 1000.0 / ms * world
+    mid = args.warmup + args.steps // 2 + 1  # tokens each sequence gained by mid-run
+    per_seq = [algorithmic_bytes(cfg, p + mid, kinds) for p in positions]
+    kv_seq = [a["step"] - a["weights"] - a["gdn_state_all"] for a in per_seq]
+    ab = dict(per_seq[0])
+    ab["step"] = per_seq[0]["weights"] + sum(kv_seq) + nb * per_seq[0]["gdn_state_all"]
+    seq_mid = positions[0] + mid
+    traffic, traffic_note = profiled_traffic(ab["step"]) if nb == 1 and args.prefill == PREFILL else (None, "not captured")
+    tok_s = 1000.0 / ms * world * nb
     step_gbs = ab["step"] / (ms * 1e-3) / 1e9
     gemv_gbs = gemv_bytes / (gemv_ms * 1e-3) / 1e9
     res = {
         "metric": METRIC, "value": round(tok_s, 2), "unit": "tok/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int8-weight/bf16-act/fp32-acc", "data": "synthetic",
-        "config": {"workload": "qwen3.5-4b-shape 32-layer decode stack, batch 1, KV prefilled to 8192",
+        "config": {"workload": ("qwen3.5-4b-shape 32-layer decode stack, batch 1, KV prefilled to 8192" if nb == 1
+                                and args.prefill == PREFILL else
+                                f"qwen3.5-4b-shape 32-layer decode stack, batch {nb}, KV prefilled to {positions}"),
+                   "batch": nb, "positions": positions,
                    "layers": "24 gated-deltanet + 8 full-attention (i % 4 == 3)",
                    "context": [pos0 + 1, pos0 + args.steps], "global_batch": world, "seq_len": seq_mid,
                    "parallelism": f"replicas x{world}" if world > 1 else "single gpu",
@@ -317,8 +344,8 @@ def run_gpu(args) -> dict | None:
                      "kernel": "decode_kernel (one launch = the whole 32-layer step)",
                      "bytes_per_launch": ab["step"], "us_per_launch": round(ms * 1e3, 2),
                      "peak_kind": peak_kind},
-        "e2e": {"value": round(1000.0 / e2e_ms * world, 2), "unit": "tok/s", "ms_per_step": round(e2e_ms, 4),
-                "h2d_bytes_per_step": cfg["hidden"] * 2, "d2h_bytes_per_step": cfg["hidden"] * 2},
+        "e2e": {"value": round(1000.0 / e2e_ms * world * nb, 2), "unit": "tok/s", "ms_per_step": round(e2e_ms, 4),
+                "h2d_bytes_per_step": nb * cfg["hidden"] * 2, "d2h_bytes_per_step": nb * cfg["hidden"] * 2},
         "gpu_launches": args.steps,
         "clocks": clk.summary(),
     }
@@ -395,6 +422,8 @@ def main():
     ap.add_argument("--cpu-steps", type=int, default=24)
     ap.add_argument("--layers", type=int, default=32, help="first N layers of the stack (profiling a small case)")
     ap.add_argument("--stack-only", action="store_true", help="graph replays only (for ncu captures)")
+    ap.add_argument("--batch", type=int, default=1, help="sequences per step (multi-sequence workload)")
+    ap.add_argument("--prefill", type=int, default=PREFILL, help="KV tokens before the first step (batch 1)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

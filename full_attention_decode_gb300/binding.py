@@ -125,6 +125,8 @@ def lib():
             raise RuntimeError(f"CUDA library not built: {LIB_PATH} is missing (run __graft_entry__.build())")
         L = C.CDLL(LIB_PATH)
         for name, (res, args) in _SIGS.items():
+            if not hasattr(L, name):  # a library without this entry fails when it is called
+                continue
             f = getattr(L, name)
             f.restype = res
             f.argtypes = args

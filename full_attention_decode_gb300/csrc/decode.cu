@@ -89,6 +89,10 @@ __device__ __forceinline__ Smem smem_map(uint8_t* base) {
   s.uni = reinterpret_cast<uint8_t*>(s.misc + 256);
   return s;
 }
+// The consumers' ring position travels through the phase functions by value: the
+// count of tiles taken, with kDeadBit set once a wait has run out (a reference
+// would put it in local memory).
+constexpr uint32_t kDeadBit = 0x80000000u;
 // The tile the consumers take as their it-th: its slot and the slot's phase parity.
 __device__ __forceinline__ uint32_t slot_of(uint32_t it) { return it % kDecSlots; }
 __device__ __forceinline__ uint32_t parity_of(uint32_t it) { return (it / kDecSlots) & 1; }
@@ -613,12 +617,12 @@ __device__ __forceinline__ void gemv_tiles(const Gemv& g, const Smem& sh, uint32
   }
 }
 
-__device__ __noinline__ void gemv_main(uint32_t& it_io, bool& dead_io, unsigned long long* tr) {
+__device__ __noinline__ uint32_t gemv_main(uint32_t itd, unsigned long long* tr) {
   const Gemv& g = s_gemv;
   const Smem sh = smem_map(smem_raw);
   if (tr && threadIdx.x == 0) tr[10] = global_ns();
-  uint32_t it = it_io;
-  bool dead = dead_io;
+  uint32_t it = itd & ~kDeadBit;
+  bool dead = (itd & kDeadBit) != 0;
   switch (g.cpl) {
     case 1: gemv_tiles<1>(g, sh, it, dead, tr); break;
     case 2: gemv_tiles<2>(g, sh, it, dead, tr); break;
@@ -627,15 +631,14 @@ __device__ __noinline__ void gemv_main(uint32_t& it_io, bool& dead_io, unsigned 
     default: gemv_tiles<5>(g, sh, it, dead, tr); break;
   }
   if (tr && threadIdx.x == 0) tr[6] = global_ns();
-  it_io = it;
-  dead_io = dead;
+  return it | (dead ? kDeadBit : 0u);
 }
 
 // The rows of a GEMV phase, then its outputs: the K-parts of each row summed in a
 // fixed order, the residual added for the down projection, bf16 stores by
 // consecutive threads.
-__device__ void gemv_rows(uint32_t& it, bool& dead, unsigned long long* tr) {
-  gemv_main(it, dead, tr);
+__device__ uint32_t gemv_rows(uint32_t itd, unsigned long long* tr) {
+  itd = gemv_main(itd, tr);
   consumer_sync();
   if (tr && threadIdx.x == 0) tr[12] = global_ns();
   const Gemv& g = s_gemv;
@@ -652,6 +655,7 @@ __device__ void gemv_rows(uint32_t& it, bool& dead, unsigned long long* tr) {
     while (sg + 1 < g.nseg && row >= g.row0[sg + 1]) ++sg;
     g.out[sg][row - g.row0[sg]] = to_bf16(y);
   }
+  return itd;
 }
 
 // ------------------------------------------------------------------ attention phases
@@ -746,7 +750,9 @@ __device__ __forceinline__ float reduce_transposed(float* v, uint32_t lane) {
 // of head group w % NG (one kv-head) and every TI-th tile, TI = 12 / NG; the TI
 // partial softmax states of a head group are merged in shared memory at the end.
 template <int D, int HPW>
-__device__ __noinline__ void attn_consume(uint32_t& it, bool& dead, unsigned long long* tr) {
+__device__ __noinline__ uint32_t attn_consume(uint32_t itd, unsigned long long* tr) {
+  uint32_t it = itd & ~kDeadBit;
+  bool dead = (itd & kDeadBit) != 0;
   const Program& P = prog();
   const LayerDesc& L = s_layer;
   const Smem sh = smem_map(smem_raw);
@@ -760,9 +766,9 @@ __device__ __noinline__ void attn_consume(uint32_t& it, bool& dead, unsigned lon
   const uint32_t NG = H / HPW, TI = NCW / NG;  // warps beyond NG * TI only keep the ring moving
   if (!sp.ok) {
     if (s == 0 && threadIdx.x == 0) set_status(P.status, kStatusRange);
-    return;
+    return itd;
   }
-  if (s >= P.P) return;
+  if (s >= P.P) return itd;
   float2* cs = reinterpret_cast<float2*>(sh.uni);        // RoPE (cos, sin), [R/2]
   float* fresh = reinterpret_cast<float*>(sh.uni) + 256;  // k then v, [Hkv][D] each
   float* buf = fresh + 2 * rowh;                          // per-warp [D] for RoPE, then merge space
@@ -953,6 +959,7 @@ __device__ __noinline__ void attn_consume(uint32_t& it, bool& dead, unsigned lon
     }
   }
   consumer_sync();  // the merge space is free again
+  return it | (dead ? kDeadBit : 0u);
 }
 
 // Merge of the P partials of (head h, 32 dims) per CTA, then the output gate:
@@ -1075,21 +1082,21 @@ __device__ __noinline__ void conv_shift_qk() {
 }
 
 template <int DK>
-__device__ __noinline__ void gdn_consume(uint32_t& it, bool& dead) {
+__device__ __noinline__ uint32_t gdn_consume(uint32_t itd) {
   const Program& P = prog();
   const LayerDesc& L = s_layer;
   const Smem sh = smem_map(smem_raw);
   constexpr int RPT = DK / kGdnWarps;
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
   const GdnItem w = gdn_item(P);
-  if (!w.ok) return;  // (uniform over the CTA)
+  if (!w.ok) return itd;  // (uniform over the CTA)
   const uint32_t h = w.h, v0 = w.v0, Kc = P.Kc;
   float* act = reinterpret_cast<float*>(sh.uni);  // [2 Dk + 32]
   float* red = act + 2 * DK + 32;                 // [2][NCW][32]
-  const uint32_t slot = slot_of(it);
-  if (!dead && !mbar_wait(&sh.full[slot], parity_of(it))) {
+  const uint32_t slot = slot_of(itd & ~kDeadBit);
+  if (!(itd & kDeadBit) && !mbar_wait(&sh.full[slot], parity_of(itd & ~kDeadBit))) {
     set_status(P.status, kStatusTimeout);
-    dead = true;
+    itd |= kDeadBit;
   }
   const float* st_s = reinterpret_cast<const float*>(sh.ring + sh.toff[slot]);
   const float* cs_s = st_s + DK * 32;
@@ -1108,25 +1115,17 @@ __device__ __noinline__ void gdn_consume(uint32_t& it, bool& dead) {
   }
   // causal conv update + SiLU
   if (chan) {
-    float cst[kMaxKc];
+    // v channels belong to this CTA alone and are written here; the q/k channels of
+    // a k-head are read by every CTA of its v-heads during this phase, so
+    // conv_shift_qk shifts them in the next one
+    float* cnew = tid >= 2 * DK ? L.conv_state + (size_t)ch * Kc : nullptr;
     float o = 0.f;
-#pragma unroll
-    for (int t = 0; t < kMaxKc; ++t) {
-      if (t < (int)Kc) {
-        const float sv = (t + 1 < (int)Kc) ? cs_s[tid * Kc + t + 1] : x;  // shift left, newest last
-        cst[t] = sv;
-        o = fmaf(bf16f(cw_s[tid * Kc + t]), sv, o);
-      }
+    for (uint32_t t = 0; t < Kc; ++t) {
+      const float sv = t + 1 < Kc ? cs_s[tid * Kc + t + 1] : x;  // shift left, newest last
+      o = fmaf(bf16f(cw_s[tid * Kc + t]), sv, o);
+      if (cnew) cnew[t] = sv;
     }
     act[tid] = siluf_(o);
-    // v channels belong to this CTA alone; the q/k channels of a k-head are read by
-    // every CTA of its v-heads during this phase, so conv_shift_qk shifts them in
-    // the next one
-    if (tid >= 2 * DK) {
-#pragma unroll
-      for (int t = 0; t < kMaxKc; ++t)
-        if (t < (int)Kc) L.conv_state[(size_t)ch * Kc + t] = cst[t];
-    }
   }
   const uint16_t* dtr = reinterpret_cast<const uint16_t*>(s_seq.scratch + P.sm.dt_raw);
   const uint16_t* brw = reinterpret_cast<const uint16_t*>(s_seq.scratch + P.sm.b_raw);
@@ -1184,7 +1183,7 @@ __device__ __noinline__ void gdn_consume(uint32_t& it, bool& dead) {
   }
   consumer_sync();
   if (lane == 0) mbar_arrive(&sh.empty[slot]);  // the tile is read (every warp releases it)
-  ++it;
+  ++itd;
   u = 0.f;
 #pragma unroll
   for (int w = 0; w < kGdnWarps; ++w) u += red[w * 32 + lane];
@@ -1210,6 +1209,7 @@ __device__ __noinline__ void gdn_consume(uint32_t& it, bool& dead) {
     yo[(size_t)h * P.Dv + v0 + lane] = to_bf16(y * P.gdn_out_scale);
   }
   consumer_sync();
+  return itd;
 }
 
 // ------------------------------------------------------------------ producer schedule
@@ -1458,8 +1458,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
   // dependent phases are separated by a grid barrier. Between its two halves
   // thread 0 fetches the coming phase's descriptions (the layer's, rebased to the
   // first sequence, and the GEMV's): they do not depend on the other CTAs.
-  uint32_t it = 0, nbar = 0, ph = 0;
-  bool dead = false;
+  uint32_t itd = 0, nbar = 0, ph = 0;  // ring position | kDeadBit
   auto mark = [&](uint32_t k) {
     if (P.trace && threadIdx.x == 0 && ph < P.trace_phases)
       P.trace[((size_t)blockIdx.x * P.trace_phases + ph) * kTraceSlots + k] = global_ns();
@@ -1507,11 +1506,11 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
         if (ty == kPhGemv) {
           gemv_prologue(slots());
           mark(3);
-          gemv_rows(it, dead, slots());
+          itd = gemv_rows(itd, slots());
         } else if (ty == kPhAttn) {
-          attn_consume<D, HPW>(it, dead, slots());
+          itd = attn_consume<D, HPW>(itd, slots());
         } else if (ty == kPhGdn) {
-          gdn_consume<DK>(it, dead);
+          itd = gdn_consume<DK>(itd);
         } else {
           combine_consume();
         }
