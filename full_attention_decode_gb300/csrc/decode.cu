@@ -42,6 +42,8 @@
 // stores the rows.
 #include <cstddef>
 
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 #include "decode.h"
 
@@ -282,6 +284,39 @@ __host__ __device__ inline void pick_split(uint32_t nch, uint32_t& W, uint32_t& 
   }
 }
 
+// A batch's projections run on the tensor cores as m16n8k16 f16 products with fp32
+// sums: m = up to 16 weight rows of a tile (codes converted exactly to f16), n = the
+// pass's sequences, each sequence's input staged in f16 with a power-of-two scale
+// per 64-column group. Tiles hold up to kBatchRowsMax rows of the full K; rows of
+// the staged inputs are padded by kXPadH elements (16 bytes: a quarter-warp's lanes
+// then read distinct banks). Teams of warps take the tiles in turn: the warps of a
+// team share a tile's column groups and add their row sums in a fixed order.
+constexpr uint32_t kBatchRowsMax = 16;
+constexpr uint32_t kXPadH = 8;
+constexpr uint32_t kBatchPart = NCW * 128 * 4;  // each warp's 16 x 8 partial sums
+#ifndef QWEN35_TEAM_SLACK
+#define QWEN35_TEAM_SLACK 1
+#endif
+__host__ __device__ inline uint32_t batch_rows(uint32_t K) {
+  const uint32_t gs = ((K / 64 + 7) / 8) * 8;
+  uint32_t r = kBatchRowsMax;
+  while (r > 1 && (r * K + 15) / 16 * 16 + 4 * r * gs > (uint32_t)kDecTileMax) r /= 2;
+  return r;
+}
+// Phase-buffer bytes per sequence of a pass: the staged f16 input and the group
+// scales and sums.
+__host__ __device__ inline uint32_t batch_seq_bytes(uint32_t K) { return 2 * (K + kXPadH) + 8 * (K / 64); }
+// Teams per CTA: a divisor of the consumer warps, at most the tiles the ring holds at
+// once less a slack (tiles in flight while every team computes), at most the tiles.
+__host__ __device__ inline uint32_t batch_teams(uint32_t span, uint32_t ntiles) {
+  const uint32_t fit = (uint32_t)kDecRing / span;
+  uint32_t cap = fit > QWEN35_TEAM_SLACK ? fit - QWEN35_TEAM_SLACK : 1u;
+  if (ntiles < cap) cap = ntiles > 0 ? ntiles : 1u;
+  for (uint32_t d = cap; d > 1; --d)
+    if (NCW % d == 0) return d;
+  return 1;
+}
+
 struct Gemv {
   QMat seg[4];
   uint16_t* out[4];
@@ -294,13 +329,18 @@ struct Gemv {
   uint32_t head_dim;
   uint32_t W, cpl, R, gstride, scale_off, bias_off;
   uint32_t rb, re, ntiles;  // this CTA's rows [rb, re) and its tile count
+  // a batch: sequence b's vectors at the pointers above + b * these strides
+  // (elements), bs sequences per pass over the weights, npass passes
+  uint32_t sa, sb, sres_in, sres_out, sout[4];
+  uint32_t bs, npass, T;  // T: teams of warps per CTA (a batch)
 };
 
 __shared__ Gemv s_gemv;  // the current GEMV phase (written by thread 0 inside the barrier)
 
-__device__ __forceinline__ void gemv_add(Gemv& g, const QMat& m, uint16_t* out) {
+__device__ __forceinline__ void gemv_add(Gemv& g, const QMat& m, uint16_t* out, uint32_t stride) {
   g.seg[g.nseg] = m;
   g.out[g.nseg] = out;
+  g.sout[g.nseg] = stride;
   g.row0[g.nseg + 1] = g.row0[g.nseg] + m.n;
   ++g.nseg;
 }
@@ -316,67 +356,81 @@ __device__ __noinline__ void gemv_of(const Program& P, const LayerDesc& L, uint3
   g.resid_in = nullptr;
   g.head_dim = 0;
   g.epi = 0;
+  g.sa = g.sb = g.sres_in = g.sres_out = 0;
   uint8_t* S = seq_scratch(P, sq);
   const ScratchMap& m = P.sm;
   const uint16_t* x_in = P.x_in + (size_t)sq * P.E;
   uint16_t* x_out = P.x_out + (size_t)sq * P.E;
   const uint16_t* xin = l == 0 ? x_in : x_out;
   auto at = [&](uint32_t off) { return reinterpret_cast<uint16_t*>(S + off); };
+  const uint32_t SS = P.seq_stride / 2, SX = P.E;  // per-sequence strides: scratch, vectors
   const bool fa = L.kind == kLayerFA;
   const int mlp0 = fa ? 4 : 3;  // the gate|up phase
   if (L.kind == kLayerGemv) {
     g.K = P.E;
     g.pro = kPlain;
     g.a = x_in;
-    gemv_add(g, L.m[0], x_out);
+    g.sa = SX;
+    gemv_add(g, L.m[0], x_out, SX);
   } else if (p == 0) {
     g.K = P.E;
     g.pro = kRms;
     g.a = xin;
+    g.sa = SX;
     g.nw = L.input_ln;
     if (fa) {
-      gemv_add(g, L.m[0], at(m.q_full));
-      gemv_add(g, L.m[1], at(m.k));
-      gemv_add(g, L.m[2], at(m.v));
+      gemv_add(g, L.m[0], at(m.q_full), SS);
+      gemv_add(g, L.m[1], at(m.k), SS);
+      gemv_add(g, L.m[2], at(m.v), SS);
     } else {
-      gemv_add(g, L.m[0], at(m.dt_raw));
-      gemv_add(g, L.m[1], at(m.b_raw));
-      gemv_add(g, L.m[2], at(m.qkv));
-      gemv_add(g, L.m[3], at(m.z));
+      gemv_add(g, L.m[0], at(m.dt_raw), SS);
+      gemv_add(g, L.m[1], at(m.b_raw), SS);
+      gemv_add(g, L.m[2], at(m.qkv), SS);
+      gemv_add(g, L.m[3], at(m.z), SS);
     }
   } else if (p == mlp0) {
     g.K = P.E;
     g.pro = kAddRms;
     g.a = xin;
+    g.sa = SX;
     g.b = at(fa ? m.o : m.out);
+    g.sb = SS;
     g.nw = L.post_ln;
     g.resid_out = at(m.x_resid);
-    gemv_add(g, L.m[4], at(m.g));
-    gemv_add(g, L.m[5], at(m.u));
+    g.sres_out = SS;
+    gemv_add(g, L.m[4], at(m.g), SS);
+    gemv_add(g, L.m[5], at(m.u), SS);
   } else if (p == mlp0 + 1) {
     g.K = P.I;
     g.pro = kSiluMul;
     g.epi = 1;
     g.a = at(m.g);
+    g.sa = SS;
     g.b = at(m.u);
+    g.sb = SS;
     g.resid_in = at(m.x_resid);
-    gemv_add(g, L.m[6], x_out);
+    g.sres_in = SS;
+    gemv_add(g, L.m[6], x_out, SX);
   } else if (fa) {  // p == 3: o_proj
     g.K = P.H * P.D;
     g.pro = kPlain;
     g.a = at(m.ga);
-    gemv_add(g, L.m[3], at(m.o));
+    g.sa = SS;
+    gemv_add(g, L.m[3], at(m.o), SS);
   } else {  // p == 2: out_proj on silu(z) * RMSNorm_head(y)
     g.K = P.Z;
     g.pro = kHeadNormSilu;
     g.a = at(m.y);
+    g.sa = SS;
     g.b = at(m.z);
+    g.sb = SS;
     g.nw = L.norm_weight;
     g.head_dim = P.Dv;
-    gemv_add(g, L.m[7], at(m.out));
+    gemv_add(g, L.m[7], at(m.out), SS);
   }
   pick_split(g.K / 16, g.W, g.cpl);
   g.R = NCW / g.W;
+  if (P.batch > 1) g.R = batch_rows(g.K);  // tensor-core tiles
   g.gstride = ((g.K / 64 + 7) / 8) * 8;
   g.scale_off = (g.R * g.K + 15) / 16 * 16;
   g.bias_off = g.scale_off + g.R * g.gstride * 2;
@@ -389,6 +443,11 @@ __device__ __noinline__ void gemv_of(const Program& P, const LayerDesc& L, uint3
     const uint32_t lo = max(g.rb, g.row0[sg]), hi = min(g.re, g.row0[sg + 1]);
     if (hi > lo) g.ntiles += (hi - lo + g.R - 1) / g.R;
   }
+  // a batch: as many sequences per pass over the weights as their staged inputs
+  // fit in the phase buffer beside the teams' partial sums
+  g.bs = P.batch > 1 ? min(P.batch, ((uint32_t)kDecUnion - kBatchPart) / batch_seq_bytes(g.K)) : 1u;
+  g.npass = (P.batch + g.bs - 1) / g.bs;
+  g.T = P.batch > 1 ? batch_teams(g.bias_off + g.R * g.gstride * 2, g.ntiles) : 1u;
 }
 
 struct Tile {
@@ -656,6 +715,419 @@ __device__ uint32_t gemv_rows(uint32_t itd, unsigned long long* tr) {
     g.out[sg][row - g.row0[sg]] = to_bf16(y);
   }
   return itd;
+}
+
+// ------------------------------------------------------------------ a batch's projections
+
+// The phase buffer of a batched projection pass (bs sequences): the staged inputs
+// [bs][K + kXPadH] (f16, or the raw bf16 rows between the two halves of an RMS
+// prologue), per sequence and 64-column group {scale, scale * sum of the group's f16
+// values} [bs][K/64], and the warps' partial sums [NCW][16 rows][8 sequences].
+struct BatchBuf {
+  uint16_t* xf;
+  float2* xsq;
+  float* part;
+  uint32_t stride;  // elements
+};
+__device__ __forceinline__ BatchBuf batch_buf(const Smem& sh, uint32_t K, uint32_t bs) {
+  BatchBuf b;
+  b.stride = K + kXPadH;
+  b.xf = reinterpret_cast<uint16_t*>(sh.uni);
+  b.xsq = reinterpret_cast<float2*>(sh.uni + (size_t)bs * b.stride * 2);
+  b.part = reinterpret_cast<float*>(b.xsq + (size_t)bs * (K / 64));
+  return b;
+}
+
+// Two weight codes (the bytes that sel picks) as f16 values code - 128, exactly:
+// the f16 with bits 0x64XX is 1024 + XX, and 1024 + XX - 1152 = XX - 128.
+__device__ __forceinline__ uint32_t codes_f16x2(uint32_t w, uint32_t sel) {
+  const uint32_t h = __byte_perm(w, 0x64646464u, sel);
+  uint32_t r;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(0x64806480u));
+  return r;
+}
+constexpr uint32_t kLoPair = 0x5140u, kHiPair = 0x5342u;  // bytes 0,1 and 2,3 of a word
+
+// f16 pair {lo, hi} (round to nearest) and back.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// bf16 pair {lo, hi} (round to nearest).
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ void unpack_words(const uint32_t (&pk)[8], float* x) {
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    x[2 * k] = bf16lo(pk[k]);
+    x[2 * k + 1] = bf16hi(pk[k]);
+  }
+}
+
+// D += A B for A 16x16 (row-major fragments a0..a3), B 16x8 (b0, b1), f16 in, fp32 sums.
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Stage 16 input values (chunk c of sequence s; the four chunks of a 64-column
+// group sit on a lane quad, every lane takes part): f16 with the group's factor
+// 2^(14-e), 2^e <= group max < 2^(e+1), so the largest stays below 2^15; the group's
+// scale 2^(e-14) and the sum of its values for the constant term (bf16 inputs are
+// exact in f16 at that factor; others differ from their f16 forms by f16 rounding).
+__device__ __forceinline__ void stage16(const BatchBuf& bb, uint32_t ng, const float* v, uint32_t s, uint32_t c,
+                                        bool ok) {
+  float amax = 0.f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(v[j]));
+  amax = fmaxf(amax, __shfl_xor_sync(FULLMASK, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(FULLMASK, amax, 2));
+  const uint32_t E = __float_as_uint(amax) >> 23;
+  const bool nz = E >= 15;
+  const float up = nz ? __uint_as_float((268u - E) << 23) : 0.f;     // 2^(14-e)
+  const float scale = nz ? __uint_as_float((E - 14u) << 23) : 0.f;  // 2^(e-14)
+  uint32_t h[8];
+  float gsum = 0.f;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    h[k] = pack_f16x2(v[2 * k] * up, v[2 * k + 1] * up);
+    gsum += v[2 * k] + v[2 * k + 1];
+  }
+  gsum += __shfl_xor_sync(FULLMASK, gsum, 1);
+  gsum += __shfl_xor_sync(FULLMASK, gsum, 2);
+  if (ok) {
+    uint4* dst = reinterpret_cast<uint4*>(bb.xf + s * bb.stride + c * 16);
+    dst[0] = make_uint4(h[0], h[1], h[2], h[3]);
+    dst[1] = make_uint4(h[4], h[5], h[6], h[7]);
+    if ((c & 3) == 0) bb.xsq[s * ng + c / 4] = make_float2(scale, gsum);
+  }
+}
+
+// Form and stage the inputs of sequences [b0, b0 + nb) of a batched projection pass
+// (the same forms as gemv_prologue, per sequence). Chunk c of sequence s is item
+// s * nch + c; a thread takes items tid + u * NCT, so consecutive items sit on
+// consecutive lanes, and nch is a multiple of 4 (of a head's chunks): a group's four
+// chunks share a lane quad and a head's chunks an aligned lane group. The loads of a
+// round of NI items are issued before any is used (NI sized so that they stay in
+// registers). RMS kinds keep the raw rows (bf16) in the staging buffer until the
+// sums of squares are in.
+template <int PRO>
+__device__ __noinline__ void prologue_b_kind(uint32_t b0, uint32_t nb, unsigned long long* tr) {
+  constexpr bool kTwo = PRO == kAddRms || PRO == kSiluMul || PRO == kHeadNormSilu;
+  constexpr bool kRmsKind = PRO == kRms || PRO == kAddRms;
+  constexpr uint32_t NI = kTwo ? 2 : 4;
+  const Program& P = prog();
+  const Gemv& g = s_gemv;
+  const Smem sh = smem_map(smem_raw);
+  const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t K = g.K, nch = K / 16, ng = K / 64, items = nb * nch;
+  const BatchBuf bb = batch_buf(sh, K, g.bs);
+  float ssb[kRmsKind ? kMaxBatch : 1];
+#pragma unroll
+  for (int b = 0; b < (kRmsKind ? kMaxBatch : 1); ++b) ssb[b] = 0.f;
+  for (uint32_t i0 = 0; i0 < items; i0 += NI * NCT) {
+    uint4 a[NI][2], x2[kTwo ? NI : 1][2];
+#pragma unroll
+    for (uint32_t u = 0; u < NI; ++u) {
+      const uint32_t i = i0 + u * NCT + tid;
+      const bool ok = i < items;  // past the end: sequence 0's chunk 0 (valid memory, unused)
+      const uint32_t s = ok ? i / nch : 0, c = ok ? i % nch : 0;
+      const uint4* ap = reinterpret_cast<const uint4*>(g.a + (size_t)(b0 + s) * g.sa + c * 16);
+      a[u][0] = ap[0];
+      a[u][1] = ap[1];
+      if constexpr (kTwo) {
+        const uint4* bp = reinterpret_cast<const uint4*>(g.b + (size_t)(b0 + s) * g.sb + c * 16);
+        x2[u][0] = bp[0];
+        x2[u][1] = bp[1];
+      }
+    }
+    if (tr && tid == 0 && i0 == 0 && a[0][0].x != 0x12345678u) tr[8] = global_ns();  // loads landed
+#pragma unroll
+    for (uint32_t u = 0; u < NI; ++u) {
+      const uint32_t i = i0 + u * NCT + tid;
+      const bool ok = i < items;
+      const uint32_t s = ok ? i / nch : 0, c = ok ? i % nch : 0;
+      float raw[16], v[16];
+      unpack8(a[u][0], raw);
+      unpack8(a[u][1], raw + 8);
+      if constexpr (kRmsKind) {
+        uint32_t pk[8] = {a[u][0].x, a[u][0].y, a[u][0].z, a[u][0].w, a[u][1].x, a[u][1].y, a[u][1].z, a[u][1].w};
+        if constexpr (PRO == kAddRms) {
+          float xb[16];
+          unpack8(x2[u][0], xb);
+          unpack8(x2[u][1], xb + 8);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) pk[k] = pack_bf16x2(raw[2 * k] + xb[2 * k], raw[2 * k + 1] + xb[2 * k + 1]);
+          unpack_words(pk, raw);
+        }
+        float ss = 0.f;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) ss = fmaf(raw[j], raw[j], ss);
+        if (ok) {
+#pragma unroll
+          for (int b = 0; b < kMaxBatch; ++b) ssb[b] += s == (uint32_t)b ? ss : 0.f;
+          uint4* dst = reinterpret_cast<uint4*>(bb.xf + s * bb.stride + c * 16);
+          dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          if (PRO == kAddRms && blockIdx.x == 0) {  // one CTA stores x_resid
+            uint4* rd = reinterpret_cast<uint4*>(g.resid_out + (size_t)(b0 + s) * g.sres_out + c * 16);
+            rd[0] = dst[0];
+            rd[1] = dst[1];
+          }
+        }
+      } else {
+        if constexpr (PRO == kSiluMul) {
+          float xb[16];
+          unpack8(x2[u][0], xb);
+          unpack8(x2[u][1], xb + 8);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] = silu_fast(raw[j]) * xb[j];
+        } else if constexpr (PRO == kHeadNormSilu) {
+          float hs = 0.f;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) hs = fmaf(raw[j], raw[j], hs);
+          for (uint32_t o = 1; o < g.head_dim / 16; o <<= 1) hs += __shfl_xor_sync(FULLMASK, hs, o);
+          const float hi = rsqrtf(hs / (float)g.head_dim + P.eps);
+          float xb[16], w[16];
+          unpack8(x2[u][0], xb);
+          unpack8(x2[u][1], xb + 8);
+          const uint4* wp = reinterpret_cast<const uint4*>(g.nw + (c * 16) % g.head_dim);
+          unpack8(wp[0], w);
+          unpack8(wp[1], w + 8);
+          uint32_t pk[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            pk[k] = pack_bf16x2(raw[2 * k] * hi * w[2 * k], raw[2 * k + 1] * hi * w[2 * k + 1]);
+          unpack_words(pk, v);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] *= silu_fast(xb[j]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] = raw[j];
+        }
+        stage16(bb, ng, v, s, c, ok);
+      }
+    }
+  }
+  if (tr && tid == 0) tr[9] = global_ns();
+  if constexpr (kRmsKind) {
+    // each sequence's sum of squares: per thread, per warp, then over the warps in a
+    // fixed order; then the staged raw rows normalised and converted in place
+    float* part = sh.misc;  // [kMaxBatch][NCW]
+#pragma unroll
+    for (int b = 0; b < kMaxBatch; ++b) {
+      const float w = warp_sum(ssb[b]);
+      if (lane == 0) part[b * NCW + warp] = w;
+    }
+    consumer_sync();
+    float inv_all[kMaxBatch];
+#pragma unroll
+    for (int b = 0; b < kMaxBatch; ++b) {
+      float tot = 0.f;
+#pragma unroll
+      for (int w = 0; w < NCW; ++w) tot += part[b * NCW + w];
+      inv_all[b] = rsqrtf(tot / (float)K + P.eps);
+    }
+    if (tr && tid == 0) tr[10] = global_ns();
+    for (uint32_t i0 = 0; i0 < items; i0 += 4 * NCT) {
+      uint4 r[4][2], wv[4][2];
+#pragma unroll
+      for (uint32_t u = 0; u < 4; ++u) {
+        const uint32_t i = i0 + u * NCT + tid;
+        const bool ok = i < items;
+        const uint32_t s = ok ? i / nch : 0, c = ok ? i % nch : 0;
+        const uint4* src = reinterpret_cast<const uint4*>(bb.xf + s * bb.stride + c * 16);
+        r[u][0] = src[0];
+        r[u][1] = src[1];
+        const uint4* wp = reinterpret_cast<const uint4*>(g.nw + c * 16);
+        wv[u][0] = wp[0];
+        wv[u][1] = wp[1];
+      }
+#pragma unroll
+      for (uint32_t u = 0; u < 4; ++u) {
+        const uint32_t i = i0 + u * NCT + tid;
+        const bool ok = i < items;
+        const uint32_t s = ok ? i / nch : 0, c = ok ? i % nch : 0;
+        float raw[16], w[16], v[16];
+        unpack8(r[u][0], raw);
+        unpack8(r[u][1], raw + 8);
+        unpack8(wv[u][0], w);
+        unpack8(wv[u][1], w + 8);
+        float inv = inv_all[0];
+#pragma unroll
+        for (int q = 1; q < kMaxBatch; ++q) inv = s == (uint32_t)q ? inv_all[q] : inv;
+        uint32_t pk[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) pk[k] = pack_bf16x2(raw[2 * k] * inv * w[2 * k], raw[2 * k + 1] * inv * w[2 * k + 1]);
+        unpack_words(pk, v);
+        stage16(bb, ng, v, s, c, ok);
+      }
+    }
+  }
+  if (tr && tid == 0) tr[11] = global_ns();
+  consumer_sync();
+}
+
+__device__ __forceinline__ void gemv_prologue_b(uint32_t b0, uint32_t nb, unsigned long long* tr) {
+  switch (s_gemv.pro) {
+    case kRms: prologue_b_kind<kRms>(b0, nb, tr); break;
+    case kAddRms: prologue_b_kind<kAddRms>(b0, nb, tr); break;
+    case kSiluMul: prologue_b_kind<kSiluMul>(b0, nb, tr); break;
+    case kHeadNormSilu: prologue_b_kind<kHeadNormSilu>(b0, nb, tr); break;
+    default: prologue_b_kind<kPlain>(b0, nb, tr); break;
+  }
+}
+
+template <bool TWO>
+struct GroupOps {
+  const uint8_t *wa, *wb;
+  const uint16_t *sc, *bi, *xrow;
+  const float2 *sqa, *sqb;
+  uint32_t ra, rb, gstride;
+  // the group's four products as two chains (columns 0-31, 32-63 of the slice
+  // pattern), summed at the end: rows g, g + 8 x sequences 2t, 2t + 1
+  __device__ __forceinline__ void sums(uint32_t gr, float (&acc)[4]) const {
+    const uint4 xa = *reinterpret_cast<const uint4*>(xrow + gr * 64);
+    const uint4 xb = *reinterpret_cast<const uint4*>(xrow + gr * 64 + 8);
+    const uint4 u = *reinterpret_cast<const uint4*>(wa + gr * 64);
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (TWO) v = *reinterpret_cast<const uint4*>(wb + gr * 64);
+    float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+    mma_f16(c0, codes_f16x2(u.x, kLoPair), TWO ? codes_f16x2(v.x, kLoPair) : 0u, codes_f16x2(u.x, kHiPair),
+            TWO ? codes_f16x2(v.x, kHiPair) : 0u, xa.x, xa.y);
+    mma_f16(c1, codes_f16x2(u.z, kLoPair), TWO ? codes_f16x2(v.z, kLoPair) : 0u, codes_f16x2(u.z, kHiPair),
+            TWO ? codes_f16x2(v.z, kHiPair) : 0u, xb.x, xb.y);
+    mma_f16(c0, codes_f16x2(u.y, kLoPair), TWO ? codes_f16x2(v.y, kLoPair) : 0u, codes_f16x2(u.y, kHiPair),
+            TWO ? codes_f16x2(v.y, kHiPair) : 0u, xa.z, xa.w);
+    mma_f16(c1, codes_f16x2(u.w, kLoPair), TWO ? codes_f16x2(v.w, kLoPair) : 0u, codes_f16x2(u.w, kHiPair),
+            TWO ? codes_f16x2(v.w, kHiPair) : 0u, xb.z, xb.w);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) acc[k] = c0[k] + c1[k];
+  }
+  // y += scale_row * scale_seq * sums + (bias_row + 128 scale_row) * sum_seq
+  __device__ __forceinline__ void add(uint32_t gr, const float (&acc)[4], float (&y)[2][2]) const {
+    const float2 qa = sqa[gr], qb = sqb[gr];
+    const float sA = bf16f(sc[ra * gstride + gr]), tA = fmaf(sA, 128.f, bf16f(bi[ra * gstride + gr]));
+    y[0][0] = fmaf(sA * qa.x, acc[0], fmaf(tA, qa.y, y[0][0]));
+    y[0][1] = fmaf(sA * qb.x, acc[1], fmaf(tA, qb.y, y[0][1]));
+    if (TWO) {
+      const float sB = bf16f(sc[rb * gstride + gr]), tB = fmaf(sB, 128.f, bf16f(bi[rb * gstride + gr]));
+      y[1][0] = fmaf(sB * qa.x, acc[2], fmaf(tB, qa.y, y[1][0]));
+      y[1][1] = fmaf(sB * qb.x, acc[3], fmaf(tB, qb.y, y[1][1]));
+    }
+  }
+};
+
+// One warp's share of a batched tile: the column groups j, j + W, ... of tile rows
+// g and g + 8 (TWO) against the pass's sequences, two groups at a time (added in
+// column order). Per 64-column group, four m16n8k16 products: thread (g = lane/4,
+// t = lane%4) supplies the codes of rows g (and g + 8) and sequence g's input for
+// the 16 columns at 16t of the group, the same permutation of k in both operands
+// (columns 4m..4m+3 of that slice in product m), and receives rows g, g + 8 of
+// sequences 2t, 2t + 1. Each group's sums are scaled by the row's and the
+// sequence's group scales, the affine constant term taken against the group's
+// input sum.
+template <bool TWO>
+__device__ __forceinline__ void batch_tile_groups(const uint8_t* tile, uint32_t nr, uint32_t K, uint32_t gstride,
+                                                  uint32_t scale_off, uint32_t bias_off, uint32_t j, uint32_t W,
+                                                  const uint16_t* xrow, const float2* sqa, const float2* sqb,
+                                                  float (&y)[2][2]) {
+  const uint32_t lane = threadIdx.x & 31, gq = lane >> 2, t = lane & 3, ng = K / 64;
+  GroupOps<TWO> op;
+  op.ra = min(gq, nr - 1);
+  op.rb = min(gq + 8, nr - 1);
+  op.wa = tile + op.ra * K + t * 16;
+  op.wb = tile + op.rb * K + t * 16;
+  op.sc = reinterpret_cast<const uint16_t*>(tile + scale_off);
+  op.bi = reinterpret_cast<const uint16_t*>(tile + bias_off);
+  op.xrow = xrow;
+  op.sqa = sqa;
+  op.sqb = sqb;
+  op.gstride = gstride;
+  uint32_t gr = j;
+  for (; gr + W < ng; gr += 2 * W) {
+    float a0[4], a1[4];
+    op.sums(gr, a0);
+    op.sums(gr + W, a1);
+    op.add(gr, a0, y);
+    op.add(gr + W, a1, y);
+  }
+  if (gr < ng) {
+    float a0[4];
+    op.sums(gr, a0);
+    op.add(gr, a0, y);
+  }
+}
+
+// The tiles of a batched projection pass. Team `team` (warps team*W .. team*W+W-1)
+// takes the CTA's tiles team, team + T, ...; its warps release a tile with T
+// arrivals each (T teams x W warps = every consumer warp's count), write their
+// partial sums, and the team adds them in warp order and writes the rows of each
+// sequence (+ residual) as bf16. Tiles of other teams are skipped unread.
+__device__ __noinline__ uint32_t gemv_tiles_b(uint32_t itd, uint32_t b0, uint32_t nb, unsigned long long* tr) {
+  const Gemv& g = s_gemv;
+  const Smem sh = smem_map(smem_raw);
+  const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gq = lane >> 2, t = lane & 3;
+  const uint32_t K = g.K, ng = K / 64, T = g.T, W = NCW / T;
+  const uint32_t team = warp / W, j = warp - team * W;
+  const BatchBuf bb = batch_buf(sh, K, g.bs);
+  int* status = prog().status;
+  uint32_t it = itd & ~kDeadBit;
+  bool dead = (itd & kDeadBit) != 0;
+  // inputs of sequence g (B operand) and group scales of sequences 2t, 2t + 1 (the
+  // outputs); sequences past the pass read sequence 0's (their results are unused)
+  const uint16_t* xrow = bb.xf + (gq < nb ? gq : 0) * bb.stride + t * 16;
+  const float2* sqa = bb.xsq + (2 * t < nb ? 2 * t : 0) * ng;
+  const float2* sqb = bb.xsq + (2 * t + 1 < nb ? 2 * t + 1 : 0) * ng;
+  float* mine = bb.part + warp * 128;         // [16 rows][8 sequences]
+  const float* tp = bb.part + team * W * 128;  // the team's partials
+  for (uint32_t tl = 0; tl < g.ntiles; ++tl, ++it) {
+    if (tl % T != team) continue;
+    const uint32_t st = slot_of(it);
+    if (!dead && !mbar_wait(&sh.full[st], parity_of(it))) {
+      set_status(status, kStatusTimeout);
+      dead = true;
+    }
+    if (tr && threadIdx.x == 0) {
+      if (tl == 0) tr[4] = global_ns();
+      if (tl + T >= g.ntiles) tr[5] = global_ns();
+    }
+    const uint32_t meta = dead ? 0u : sh.tmeta[st];
+    const uint32_t r0 = meta & 0xFFFFFFu, nr = meta >> 24;
+    float y[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+    if (nr > 8) {
+      batch_tile_groups<true>(sh.ring + sh.toff[st], nr, K, g.gstride, g.scale_off, g.bias_off, j, W, xrow, sqa,
+                              sqb, y);
+    } else if (nr) {
+      batch_tile_groups<false>(sh.ring + sh.toff[st], nr, K, g.gstride, g.scale_off, g.bias_off, j, W, xrow, sqa,
+                               sqb, y);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive_n(&sh.empty[st], T);
+    mine[gq * 8 + 2 * t] = y[0][0];
+    mine[gq * 8 + 2 * t + 1] = y[0][1];
+    mine[(gq + 8) * 8 + 2 * t] = y[1][0];
+    mine[(gq + 8) * 8 + 2 * t + 1] = y[1][1];
+    named_barrier(2 + team, W * 32);
+    for (uint32_t e = j * 32 + lane; e < nr * nb; e += W * 32) {
+      const uint32_t rho = e / nb, s = e - rho * nb, row = r0 + rho;
+      float acc = 0.f;
+      for (uint32_t jj = 0; jj < W; ++jj) acc += tp[jj * 128 + rho * 8 + s];
+      if (g.epi == 1) acc += bf16f(g.resid_in[(size_t)(b0 + s) * g.sres_in + row]);
+      uint32_t sg = 0;
+      while (sg + 1 < g.nseg && row >= g.row0[sg + 1]) ++sg;
+      g.out[sg][(size_t)(b0 + s) * g.sout[sg] + row - g.row0[sg]] = to_bf16(acc);
+    }
+    named_barrier(2 + team, W * 32);  // the partials are read before the next tile's
+  }
+  if (tr && threadIdx.x == 0) tr[6] = global_ns();
+  return it | (dead ? kDeadBit : 0u);
 }
 
 // ------------------------------------------------------------------ attention phases
@@ -1063,15 +1535,14 @@ __device__ __forceinline__ GdnItem gdn_item(const Program& P) {
 // the linear-attention phase reads it in every CTA of the channel's v-heads, so it
 // is written one grid barrier later, in the output projection phase, each CTA
 // taking a share of the channels (one warp).
-__device__ __noinline__ void conv_shift_qk() {
+__device__ __noinline__ void conv_shift_qk(float* conv_state, const uint8_t* scratch) {
   const Program& P = prog();
-  const LayerDesc& L = s_layer;
   const uint32_t lane = threadIdx.x & 31, Kc = P.Kc;
   const uint32_t nqk = 2 * P.Hk * P.Dk, per = (nqk + gridDim.x - 1) / gridDim.x;
   const uint32_t c0 = blockIdx.x * per, c1 = min(nqk, c0 + per);
-  const uint16_t* qkv = reinterpret_cast<const uint16_t*>(s_seq.scratch + P.sm.qkv);
+  const uint16_t* qkv = reinterpret_cast<const uint16_t*>(scratch + P.sm.qkv);
   for (uint32_t ch = c0 + lane; ch < c1; ch += 32) {
-    float* cs = L.conv_state + (size_t)ch * Kc;
+    float* cs = conv_state + (size_t)ch * Kc;
     float v[kMaxKc];
 #pragma unroll
     for (int t = 0; t < kMaxKc; ++t) v[t] = t + 1 < (int)Kc ? cs[t + 1] : bf16f(qkv[ch]);
@@ -1298,7 +1769,7 @@ __device__ __forceinline__ bool next_copy(const Program& P, const LayerDesc* lay
         tc.total = cb + 2 * sb;
         tc.span = c.g.bias_off + c.g.R * gstride * 2;
         tc.meta = t.r | (t.nr << 24);
-        tc.policy = c.b + 1 < P.batch ? keep : stream;
+        tc.policy = c.b + 1 < c.g.npass ? keep : stream;
         return true;
       }
     } else if (c.ty == kPhAttn) {
@@ -1352,7 +1823,7 @@ __device__ __forceinline__ bool next_copy(const Program& P, const LayerDesc* lay
       }
     }
     // this sequence's walk of the phase is done: the next sequence, or the next phase
-    if (++c.b < P.batch) {
+    if (++c.b < (c.ty == kPhGemv && P.batch > 1 ? c.g.npass : P.batch)) {
       open_seq(P, c);
       continue;
     }
@@ -1495,6 +1966,26 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
         mark(1);
       }
       const int ty = phase_type(s_layer.kind, p);
+      if (BATCHED && ty == kPhGemv) {  // every sequence in passes over the weights, on tensor cores
+        if (s_layer.kind == kLayerGDN && p == 2 && warp == NCW - 1)
+          for (uint32_t b = 0; b < P.batch; ++b)
+            conv_shift_qk(s_layer0.conv_state + (size_t)P.C * P.Kc * b, seq_scratch(P, b));
+        const uint32_t bs = s_gemv.bs, npass = s_gemv.npass;
+        for (uint32_t pass = 0; pass < npass; ++pass) {
+          const uint32_t b0 = pass * bs, nb = min(bs, P.batch - b0);
+          if (pass > 0) consumer_sync();  // every team is done with the last pass's inputs
+          gemv_prologue_b(b0, nb, pass == 0 ? slots() : nullptr);
+          if (pass == 0) mark(3);
+          itd = gemv_tiles_b(itd, b0, nb, pass == 0 ? slots() : nullptr);
+          if (pass == 0) mark(12);
+        }
+        mark(2);
+        if (p + 1 >= n_phases(s_layer.kind)) {
+          ++ph;
+          break;
+        }
+        continue;
+      }
       const uint32_t nb = BATCHED ? P.batch : 1u;
       for (uint32_t b = 0; b < nb; ++b) {
         if (b > 0) {  // the next sequence: its descriptions, once every warp is done with the last
@@ -1502,7 +1993,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
           if (threadIdx.x == 0) set_seq(l, p, b);
           consumer_sync();
         }
-        if (s_layer.kind == kLayerGDN && p == 2 && warp == NCW - 1) conv_shift_qk();
+        if (s_layer.kind == kLayerGDN && p == 2 && warp == NCW - 1) conv_shift_qk(s_layer.conv_state, s_seq.scratch);
         if (ty == kPhGemv) {
           gemv_prologue(slots());
           mark(3);
@@ -1577,6 +2068,11 @@ bool decode_dims_ok(const Program& p, bool has_fa, bool has_gdn, int num_sms) {
   const uint32_t room = kDecUnion;
   auto gemv_ok = [&](uint32_t K, uint32_t N) {
     if (K == 0 || K % 64 || K > 12288 || N == 0 || N >= (1u << 24) || num_sms <= 0) return false;
+    if (p.batch > 1) {  // tensor-core passes: one sequence's staged input fits; a tile fits
+      const uint32_t R = batch_rows(K), gs = ((K / 64 + 7) / 8) * 8;
+      return batch_seq_bytes(K) + kBatchPart <= (uint32_t)kDecUnion &&
+             (R * K + 15) / 16 * 16 + 4 * R * gs <= (uint32_t)kDecTileMax;
+    }
     const uint32_t nch = K / 16;
     uint32_t W, cpl;
     pick_split(nch, W, cpl);

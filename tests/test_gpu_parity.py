@@ -337,7 +337,15 @@ def _batch_case(cfg_name, n_layers, positions, cap, seeds):
 @pytest.mark.parametrize("cfg_name,n_layers,positions,use_graph",
                          [("tiny", 2, [0, 5, 11], False), ("tiny", 2, [3, 0, 7], True),
                           ("4b", 4, [1000, 3100, 257, 2048], False)])
-def test_batch_equals_single_sequence_decodes(cfg_name, n_layers, positions, use_graph):
+def test_batch_matches_single_sequence_decodes(cfg_name, n_layers, positions, use_graph):
+    # the batch's projections run on tensor cores with inputs quantised per 64
+    # columns (16-bit), the single path per 16: each sequence of the batch is held
+    # to the oracle at the per-layer tolerances, and batch and single path, both
+    # within those of the oracle, to twice them of each other. Only the first
+    # layer's state sees the exact input; a deeper layer's input carries the
+    # earlier layers' output error (<= TOL_X), which its decay gate passes on to
+    # the state, so deeper states are held to TOL_X here and to TOL_STATE in the
+    # teacher-forced test below
     init()
     nb, steps = len(positions), 3
     cap = max(positions) + steps + 8
@@ -374,8 +382,12 @@ def test_batch_equals_single_sequence_decodes(cfg_name, n_layers, positions, use
                             x_in=torch.empty(E, dtype=torch.int16, device="cuda"),
                             x_out=torch.empty(E, dtype=torch.int16, device="cuda"),
                             pos=torch.tensor([positions[s]], dtype=torch.int32, device="cuda")))
+    ocaches = [[O.kv_from_bits(*per_seq[s][i]) if kind == "fa" else O.state_from_arrays(*per_seq[s][i])
+                for i, kind in enumerate(kinds)] for s in range(nb)]
     for t in range(steps):
         xs = [synth.x_in(seeds[s], t, cfg) for s in range(nb)]
+        refs = [O.decode_step(cfg, kinds, layers, ocaches[s], O.bf16_to_f64(xs[s]), positions[s] + t)
+                for s in range(nb)]
         with torch.cuda.stream(stream):
             bx_in.copy_(B.to_device(np.concatenate(xs)))
             if g is not None:
@@ -387,21 +399,81 @@ def test_batch_equals_single_sequence_decodes(cfg_name, n_layers, positions, use
                 assert B.qwen35_decode_step(c, sg["ent"], sg["scr"], sg["x_in"], sg["x_out"], sg["pos"], cap,
                                             stream) == 0
         stream.synchronize()
-        bo = bits(bx_out).reshape(nb, E)
+        bo = O.bf16_to_f64(bits(bx_out).reshape(nb, E))
         for s, sg in enumerate(singles):
-            np.testing.assert_array_equal(bo[s], bits(sg["x_out"]), err_msg=f"step {t} sequence {s}")
+            assert rel_l2(bo[s], refs[s]) <= TOL_X, (t, s)
+            assert rel_l2(bo[s], f64(sg["x_out"])) <= 2 * TOL_X, (t, s)
     assert bpos.tolist() == [p + steps for p in positions]
     for i, kind in enumerate(kinds):
         for s, sg in enumerate(singles):
             if kind == "fa":
-                np.testing.assert_array_equal(bits(bcaches[i].k)[s], bits(sg["caches"][i].k))
-                np.testing.assert_array_equal(bits(bcaches[i].v)[s], bits(sg["caches"][i].v))
+                assert rel_l2(f64(bcaches[i].k)[s], ocaches[s][i]["k"]) <= TOL_X, (i, s)
+                assert rel_l2(f64(bcaches[i].v)[s], ocaches[s][i]["v"]) <= TOL_X, (i, s)
+                assert rel_l2(f64(bcaches[i].k)[s], f64(sg["caches"][i].k)) <= 2 * TOL_X, (i, s)
             else:
-                assert torch.equal(bcaches[i].ssm_matrix(s), sg["caches"][i].ssm_matrix())
-                assert torch.equal(bcaches[i].conv[s], sg["caches"][i].conv)
+                tol = TOL_STATE if i == 0 else TOL_X
+                assert rel_l2(f32(bcaches[i].ssm_matrix(s)), ocaches[s][i]["ssm"]) <= tol, (i, s)
+                assert rel_l2(f32(bcaches[i].conv[s]), ocaches[s][i]["conv"]) <= tol, (i, s)
+                assert rel_l2(f32(bcaches[i].ssm_matrix(s)), f32(sg["caches"][i].ssm_matrix())) <= 2 * tol, (i, s)
     assert B.qwen35_read_device_status(bscr, stream) == 0
     if g is not None:
         g.close()
+
+
+def test_batch_4b_teacher_forced_per_layer():
+    """One batched step of a 4-layer 4B-shape stack (3 linear-attention layers, then
+    full attention), 4 sequences at their own positions, checked layer by layer:
+    the GPU runs the prefixes [0, i] from the same caches; the oracle applies layer i
+    to each sequence's GPU input of that layer; output, new state or appended row
+    must match at the per-layer tolerances."""
+    init()
+    positions = [1000, 3100, 257, 2048]
+    nb, cap = len(positions), max(positions) + 8
+    seeds = [30 + s for s in range(nb)]
+    cfg, kinds, layers, dev, per_seq = _batch_case("4b", 4, positions, cap, seeds)
+    c = B.make_config(cfg)
+    E = cfg["hidden"]
+    bcaches = []
+    for i, kind in enumerate(kinds):
+        if kind == "fa":
+            bcaches.append(B.DeviceKvBatch([per_seq[s][i][0] for s in range(nb)], [per_seq[s][i][1] for s in range(nb)]))
+        else:
+            bcaches.append(B.DeviceStateBatch([per_seq[s][i][0] for s in range(nb)],
+                                              [per_seq[s][i][1] for s in range(nb)]))
+    saved = [(cc.conv.clone(), cc.ssm.clone()) if kind == "gdn" else None for kind, cc in zip(kinds, bcaches)]
+    bent = [B.stack_layer(k, d, cc) for k, d, cc in zip(kinds, dev, bcaches)]
+    bscr = B.new_scratch(B.qwen35_stack_scratch_bytes_batched(c, nb))
+    bx_in = torch.empty(nb * E, dtype=torch.int16, device="cuda")
+    bx_out = torch.empty_like(bx_in)
+    bpos = torch.empty(nb, dtype=torch.int32, device="cuda")
+    xs = [synth.x_in(seeds[s], 0, cfg) for s in range(nb)]
+    x_layer = [O.bf16_to_f64(x) for x in xs]  # each sequence's GPU input of layer i
+    for i, kind in enumerate(kinds):
+        for sv, cc in zip(saved, bcaches):
+            if sv is not None:
+                cc.conv.copy_(sv[0])
+                cc.ssm.copy_(sv[1])
+        bpos.copy_(torch.tensor(positions, dtype=torch.int32))
+        bx_in.copy_(B.to_device(np.concatenate(xs)))
+        assert B.qwen35_decode_step_batched(c, bent[:i + 1], nb, bscr, bx_in, bx_out, bpos, cap) == 0
+        torch.cuda.synchronize()
+        got = O.bf16_to_f64(bits(bx_out).reshape(nb, E))
+        for s in range(nb):
+            tr = {}
+            if kind == "fa":
+                okv = O.kv_from_bits(*per_seq[s][i])
+                ref = O.forward_full_attention(cfg, layers[i], okv, x_layer[s], positions[s], positions[s] + 1, tr)
+                assert rel_l2(f64(bcaches[i].k)[s][positions[s]], tr["k_rope"]) <= TOL_X, (i, s)
+                assert rel_l2(f64(bcaches[i].v)[s][positions[s]], tr["v"].reshape(-1, cfg["head_dim"])) <= TOL_X
+            else:
+                ost = O.state_from_arrays(*per_seq[s][i])
+                ref = O.forward_linear_attention(cfg, layers[i], ost, x_layer[s], tr)
+                assert rel_l2(f32(bcaches[i].ssm_matrix(s)), ost["ssm"]) <= TOL_STATE, (i, s)
+                assert rel_l2(f32(bcaches[i].conv[s]), ost["conv"]) <= TOL_STATE, (i, s)
+            assert rel_l2(got[s], ref) <= TOL_X, (i, s)
+        x_layer = list(got)
+    assert bpos.tolist() == [p + 1 for p in positions]
+    assert B.qwen35_read_device_status(bscr) == 0
 
 
 def test_batch_sequence_matches_oracle():
