@@ -236,7 +236,7 @@ int launch(Program* p, bool has_fa, bool has_gdn, cudaStream_t st) {
   p->trace = g_trace;
   p->trace_phases = g_trace_phases;
   int r = QWEN35_OK;
-  if (!decode_dims_ok(*p, has_fa, has_gdn, num_sms())) r = QWEN35_ERR_UNSUPPORTED;
+  if (!decode_pick_split(*p, has_fa, has_gdn, num_sms())) r = QWEN35_ERR_UNSUPPORTED;
   else if (decode_launch(*p, num_sms(), st) != cudaSuccess) r = QWEN35_ERR_CUDA;
   delete p;
   return r;

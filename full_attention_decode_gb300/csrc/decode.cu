@@ -80,10 +80,10 @@ struct Smem {
   uint8_t* uni;    // per-phase buffer (kDecUnion bytes)
 };
 
-__device__ __forceinline__ Smem smem_map(uint8_t* base) {
+__device__ __forceinline__ Smem smem_map(uint8_t* base, uint32_t ring_bytes) {
   Smem s;
   s.ring = base;
-  s.full = reinterpret_cast<uint64_t*>(base + kDecRing);
+  s.full = reinterpret_cast<uint64_t*>(base + ring_bytes);
   s.empty = s.full + kDecSlots;
   s.toff = reinterpret_cast<uint32_t*>(s.empty + kDecSlots);
   s.tmeta = s.toff + kDecSlots;
@@ -111,6 +111,7 @@ __shared__ __align__(16) uint8_t s_head[kHeadBytes];
 __shared__ LayerDesc s_layer;
 __shared__ LayerDesc s_layer0;  // the current layer as the program gives it (sequence 0's caches)
 __device__ __forceinline__ const Program& prog() { return *reinterpret_cast<const Program*>(s_head); }
+__device__ __forceinline__ Smem smem_map(uint8_t* base) { return smem_map(base, prog().ring_bytes); }
 
 // The sequence the consumers are working on (a batch runs each phase for its
 // sequences back to back): its scratch block, input and output vectors. The
@@ -197,6 +198,33 @@ __device__ __forceinline__ void load_row(const uint16_t* p, float* x) {
     const uint32_t u = *reinterpret_cast<const uint32_t*>(p);
     x[0] = bf16lo(u); x[1] = bf16hi(u);
   }
+}
+
+// Sum over the 32 lanes of v[0..NV-1] (NV a power of two up to 32), each step handing half of
+// the remaining values to the partner lane; lane L ends with the total of
+// v[L >> (5 - log2 NV)].
+template <int NV>
+__device__ __forceinline__ float reduce_transposed(float* v, uint32_t lane) {
+  int n = NV;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    if (n > 1) {
+      const bool up = lane & o;
+      const int h = n / 2;
+#pragma unroll
+      for (int i = 0; i < NV / 2; ++i) {
+        if (i < h) {
+          const float keep = up ? v[i + h] : v[i];
+          const float send = up ? v[i] : v[i + h];
+          v[i] = keep + __shfl_xor_sync(FULLMASK, send, o);
+        }
+      }
+      n = h;
+    } else {
+      v[0] += __shfl_xor_sync(FULLMASK, v[0], o);
+    }
+  }
+  return v[0];
 }
 
 // ------------------------------------------------------------------ GEMV phases
@@ -308,8 +336,8 @@ __host__ __device__ inline uint32_t batch_rows(uint32_t K) {
 __host__ __device__ inline uint32_t batch_seq_bytes(uint32_t K) { return 2 * (K + kXPadH) + 8 * (K / 64); }
 // Teams per CTA: a divisor of the consumer warps, at most the tiles the ring holds at
 // once less a slack (tiles in flight while every team computes), at most the tiles.
-__host__ __device__ inline uint32_t batch_teams(uint32_t span, uint32_t ntiles) {
-  const uint32_t fit = (uint32_t)kDecRing / span;
+__host__ __device__ inline uint32_t batch_teams(uint32_t span, uint32_t ntiles, uint32_t ring_bytes) {
+  const uint32_t fit = ring_bytes / span;
   uint32_t cap = fit > QWEN35_TEAM_SLACK ? fit - QWEN35_TEAM_SLACK : 1u;
   if (ntiles < cap) cap = ntiles > 0 ? ntiles : 1u;
   for (uint32_t d = cap; d > 1; --d)
@@ -445,26 +473,10 @@ __device__ __noinline__ void gemv_of(const Program& P, const LayerDesc& L, uint3
   }
   // a batch: as many sequences per pass over the weights as their staged inputs
   // fit in the phase buffer beside the teams' partial sums
-  g.bs = P.batch > 1 ? min(P.batch, ((uint32_t)kDecUnion - kBatchPart) / batch_seq_bytes(g.K)) : 1u;
+  g.bs = P.batch > 1 ? min(P.batch, (P.union_bytes - kBatchPart) / batch_seq_bytes(g.K)) : 1u;
   g.npass = (P.batch + g.bs - 1) / g.bs;
-  g.T = P.batch > 1 ? batch_teams(g.bias_off + g.R * g.gstride * 2, g.ntiles) : 1u;
+  g.T = P.batch > 1 ? batch_teams(g.bias_off + g.R * g.gstride * 2, g.ntiles, P.ring_bytes) : 1u;
 }
-
-struct Tile {
-  uint32_t r, nr, seg;
-};
-// The CTA's rows [r, re) cut into tiles of at most R rows, never across a segment end.
-__device__ __forceinline__ bool next_tile(const Gemv& g, uint32_t& r, uint32_t re, uint32_t& seg, Tile& t) {
-  if (r >= re) return false;
-  while (r >= g.row0[seg + 1]) ++seg;
-  const uint32_t end = min(re, g.row0[seg + 1]);
-  t.r = r;
-  t.nr = min(g.R, end - r);
-  t.seg = seg;
-  r += t.nr;
-  return true;
-}
-
 
 // The CTA's partial row sums of a GEMV phase ([W][rows], one slice per K-part of
 // a row) and, for the down projection, its residual rows ([rows]): shared memory
@@ -634,6 +646,8 @@ __device__ __forceinline__ void gemv_tiles(const Gemv& g, const Smem& sh, uint32
   float* part = gemv_partials(sh, nch) + kp * (g.re - rb);  // indexed by row - rb
   int* status = prog().status;
   if (tr && threadIdx.x == 0) tr[11] = global_ns();
+  float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;  // sums of the last tiles' rows
+  uint32_t pr0 = ~0u, pr1 = ~0u, pr2 = ~0u, pr3 = ~0u;  // their places in part (~0u: none)
   for (uint32_t t = 0; t < ntiles; ++t) {
     const uint32_t st = slot_of(it);
     if (!dead && !mbar_wait(&sh.full[st], parity_of(it))) {
@@ -645,8 +659,8 @@ __device__ __forceinline__ void gemv_tiles(const Gemv& g, const Smem& sh, uint32
       if (t + 1 == ntiles) tr[5] = global_ns();
     }
     const uint32_t meta = dead ? 0u : sh.tmeta[st];
-    float sum = 0.f;
     const bool mine = rs < (meta >> 24);
+    float sum = 0.f;
     if (mine) {
       const uint8_t* sb = sh.ring + sh.toff[st];
       const uint8_t* crow = sb + rs * K;
@@ -660,18 +674,32 @@ __device__ __forceinline__ void gemv_tiles(const Gemv& g, const Smem& sh, uint32
         sc[c] = bf16f(srow[chk(c) >> 2]);
         bi[c] = bf16f(brow[chk(c) >> 2]);
       }
+      // the warp's part of the tile is in registers: the slot goes back to the
+      // producer before the arithmetic
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.empty[st]);
 #pragma unroll
       for (int c = 0; c < CPL; ++c) {
         const float q128 = (float)xq[c].qsum128;
         sum = fmaf(xq[c].scale, fmaf(sc[c], (float)dot16i(w[c], xq[c]), fmaf(bi[c], 0.0078125f, sc[c]) * q128), sum);
       }
+    } else {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.empty[st]);
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sh.empty[st]);  // the row is in registers
     ++it;
-    if (mine) {
-      sum = warp_sum(sum);
-      if (lane == 0) part[(meta & 0xFFFFFFu) + rs - rb] = sum;
+    // the lanes' sums of the last four tiles' rows are reduced across the warp
+    // together (one transposed reduction instead of four)
+    acc3 = acc2; acc2 = acc1; acc1 = acc0; acc0 = sum;
+    pr3 = pr2; pr2 = pr1; pr1 = pr0; pr0 = mine ? (meta & 0xFFFFFFu) + rs - rb : ~0u;
+    if ((t & 3) == 3 || t + 1 == ntiles) {
+      float v[4] = {acc0, acc1, acc2, acc3};
+      const float tot = reduce_transposed<4>(v, lane);  // lane L: the total of v[L / 8]
+      const uint32_t q = lane >> 3;
+      const uint32_t pr = q == 0 ? pr0 : q == 1 ? pr1 : q == 2 ? pr2 : pr3;
+      if ((lane & 7) == 0 && pr != ~0u) part[pr] = tot;
+      acc0 = acc1 = acc2 = acc3 = 0.f;
+      pr0 = pr1 = pr2 = pr3 = ~0u;
     }
   }
 }
@@ -1191,32 +1219,6 @@ __device__ __forceinline__ void norm_rope(float* x, const float* wv, const Progr
   __syncwarp();
 }
 
-// Sum over the 32 lanes of v[0..NV-1] (NV = 8, 16 or 32), each step handing half of
-// the remaining values to the partner lane; lane L ends with the total of
-// v[L >> (5 - log2 NV)].
-template <int NV>
-__device__ __forceinline__ float reduce_transposed(float* v, uint32_t lane) {
-  int n = NV;
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) {
-    if (n > 1) {
-      const bool up = lane & o;
-      const int h = n / 2;
-#pragma unroll
-      for (int i = 0; i < NV / 2; ++i) {
-        if (i < h) {
-          const float keep = up ? v[i + h] : v[i];
-          const float send = up ? v[i] : v[i + h];
-          v[i] = keep + __shfl_xor_sync(FULLMASK, send, o);
-        }
-      }
-      n = h;
-    } else {
-      v[0] += __shfl_xor_sync(FULLMASK, v[0], o);
-    }
-  }
-  return v[0];
-}
 
 // Split-KV attention of one split (CTA). Warp w serves the HPW consecutive q-heads
 // of head group w % NG (one kv-head) and every TI-th tile, TI = 12 / NG; the TI
@@ -1685,223 +1687,171 @@ __device__ __noinline__ uint32_t gdn_consume(uint32_t itd) {
 
 // ------------------------------------------------------------------ producer schedule
 
-// A walk over the CTA's tiles of the whole launch, phase after phase and, within a
-// phase, sequence after sequence, in the order the consumers take them. It lives
-// in shared memory: the producer thread's local memory would compete for the
-// small L1 left beside the ring, and a walk step that misses L1 costs several L2
-// round trips per tile.
-struct Cursor {
-  uint32_t l, lc;  // position; the layer whose description L holds
-  int p;
-  uint32_t b;  // the sequence within the phase
-  bool open;
-  int ty;
+// The producer walks the CTA's tiles of the whole launch, phase after phase and,
+// within a phase, sequence after sequence (a batch's projections: pass after
+// pass), in the order the consumers take them. Everything that changes per tile
+// lives in registers; the current layer and GEMV descriptions and the ring
+// placement of the tiles in flight sit in shared memory and are read once per
+// phase or segment (a walk that keeps its cursor in memory costs a chain of
+// dependent loads per tile, and the producer's issue rate bounds the stream).
+struct ProdShared {
   LayerDesc L;
   Gemv g;
-  uint32_t r, re, seg;
-  Span sp;
-  uint32_t i;
-  uint32_t ph;  // phases opened (the timeline's phase index + 1)
-  bool fresh;   // no tile of the open phase issued yet
-  uint32_t vstart[kDecSlots];  // ring placement of the tiles in flight (see produce_all)
+  uint32_t vstart[kDecSlots];  // ring placement of the tiles in flight
 };
-__shared__ Cursor s_cursor;
+__shared__ ProdShared s_prod;
 
-// One tile: up to seven contiguous global ranges, where they land in the tile, and
-// the bytes the tile takes in the ring.
-struct TileCopy {
-  const void* src[7];
-  uint32_t off[7], bytes[7];
-  uint32_t n, total, span;
-  uint32_t meta;    // GEMV: first row | rows << 24
-  uint64_t policy;  // L2 policy of weight copies; 0 = none
+// Tile i takes slot i % kDecSlots and the ring bytes [v_i, v_i + span_i) of a
+// virtual byte stream, placed at v_i mod the ring's size; a tile that would cross
+// the ring's end starts at the next multiple of the size. It may be written once
+// every tile that started more than size - span_i bytes before its end is consumed,
+// and once the slot's previous tile (i - kDecSlots) is. Consumption is in order, so
+// `vcons` (the start of the oldest unconsumed tile) and `tail` (its index) describe
+// all of it.
+struct Ring {
+  uint32_t i, tail, vnext, vcons, size;  // size: the ring's bytes
+  bool dead;
 };
 
-// Open (phase, sequence) of the cursor: the tile walk of that sequence.
-__device__ __forceinline__ void open_seq(const Program& P, Cursor& c) {
-  c.i = 0;
-  if (c.ty == kPhGemv) {
-    c.r = c.g.rb;
-    c.re = c.g.re;
-    c.seg = 0;
-  } else if (c.ty == kPhAttn) {
-    c.sp = attn_span(P, c.L.capacity, c.b);
+// Room for tile rg.i (span bytes in the ring, `total` bytes arriving): waits
+// (bounded) until the tiles it overwrites are consumed, publishes its ring offset
+// and GEMV rows, and arms its slot's full barrier. Null once a wait has run out.
+__device__ __forceinline__ uint8_t* ring_claim(Ring& rg, const Smem& sh, uint32_t span, uint32_t total,
+                                               uint32_t meta, int* status) {
+  span = (span + 127) & ~127u;
+  uint32_t v = rg.vnext, ph = v % rg.size;
+  if (ph + span > rg.size) {
+    v += rg.size - ph;
+    ph = 0;
   }
+  while (rg.tail < rg.i && (rg.i - rg.tail >= (uint32_t)kDecSlots || v + span - rg.vcons > rg.size)) {
+    if (!mbar_wait(&sh.empty[slot_of(rg.tail)], parity_of(rg.tail))) {
+      set_status(status, kStatusTimeout);
+      rg.dead = true;
+      return nullptr;
+    }
+    ++rg.tail;
+    rg.vcons = rg.tail < rg.i ? s_prod.vstart[slot_of(rg.tail)] : v;
+  }
+  const uint32_t st = slot_of(rg.i);
+  s_prod.vstart[st] = v;
+  sh.toff[st] = ph;
+  sh.tmeta[st] = meta;
+  mbar_arrive_expect_tx(&sh.full[st], total);
+  rg.vnext = v + span;
+  return sh.ring + ph;
 }
 
-// Advance to the next tile; false when the launch has no tiles left. Weights are
-// read from HBM by a batch's first pass over a phase and kept in L2 for the others
-// (evict-last), the last pass marking them evict-first.
-__device__ __forceinline__ bool next_copy(const Program& P, const LayerDesc* layers, Cursor& c, TileCopy& tc,
-                                          uint64_t keep, uint64_t stream) {
-  while (c.l < P.n_layers) {
-    if (c.lc != c.l) {
-      c.L = layers[c.l];
-      c.lc = c.l;
-    }
-    if (!c.open) {
-      c.ty = phase_type(c.L.kind, c.p);
-      if (c.ty == kPhGemv) gemv_of(P, c.L, c.l, c.p, 0, c.g);
-      c.b = 0;
-      open_seq(P, c);
-      c.open = true;
-      c.fresh = true;
-      ++c.ph;
-    }
-    if (c.ty == kPhGemv) {
-      uint32_t r = c.r, seg = c.seg;
-      Tile t;
-      if (next_tile(c.g, r, c.re, seg, t)) {
-        c.r = r;
-        c.seg = seg;
-        const QMat& m = c.g.seg[t.seg];
-        const uint32_t K = c.g.K, gstride = c.g.gstride, local = t.r - c.g.row0[t.seg];
-        const uint32_t cb = t.nr * K, sb = t.nr * gstride * 2;
-        tc.n = 3;
-        tc.src[0] = m.codes + (size_t)local * K;
-        tc.src[1] = m.scales + (size_t)local * gstride;
-        tc.src[2] = m.biases + (size_t)local * gstride;
-        tc.off[0] = 0;
-        tc.off[1] = c.g.scale_off;
-        tc.off[2] = c.g.bias_off;
-        tc.bytes[0] = cb;
-        tc.bytes[1] = tc.bytes[2] = sb;
-        tc.total = cb + 2 * sb;
-        tc.span = c.g.bias_off + c.g.R * gstride * 2;
-        tc.meta = t.r | (t.nr << 24);
-        tc.policy = c.b + 1 < c.g.npass ? keep : stream;
-        return true;
-      }
-    } else if (c.ty == kPhAttn) {
-      if (c.i < c.sp.ntiles) {
-        LayerDesc q = c.L;
-        seq_caches(P, q, c.b);
-        const uint32_t rowh = P.Hkv * P.D, rowbytes = rowh * 2;
-        const uint32_t tt = c.sp.t0 + c.i * kTS;
-        const uint32_t n = min((uint32_t)kTS, c.sp.tc_end - tt);
-        tc.n = 2;
-        tc.src[0] = q.kc + (size_t)tt * rowh;
-        tc.src[1] = q.vc + (size_t)tt * rowh;
-        tc.off[0] = 0;
-        tc.off[1] = kTS * rowbytes;
-        tc.bytes[0] = tc.bytes[1] = n * rowbytes;
-        tc.total = 2 * n * rowbytes;
-        tc.span = 2 * kTS * rowbytes;  // rows past n are read (masked) by the consumers
-        tc.meta = 0;
-        tc.policy = 0;
-        ++c.i;
-        return true;
-      }
-    } else if (c.ty == kPhGdn) {
-      const GdnItem w = gdn_item(P);
-      if (c.i == 0 && w.ok) {  // the work item's state block, conv state and weights
-        LayerDesc q = c.L;
-        seq_caches(P, q, c.b);
-        const uint32_t Dk = P.Dk, Kc = P.Kc, nch = 2 * Dk + 32;
-        const uint32_t ch[3] = {w.hk * Dk, P.Hk * Dk + w.hk * Dk, 2 * P.Hk * Dk + w.h * P.Dv + w.v0};
-        const uint32_t nc[3] = {Dk, Dk, 32};
-        tc.n = 7;
-        tc.src[0] = q.ssm + (size_t)blockIdx.x * Dk * 32;
-        tc.off[0] = 0;
-        tc.bytes[0] = Dk * 128;
-        uint32_t done = 0;
-        for (int j = 0; j < 3; ++j) {
-          tc.src[1 + j] = q.conv_state + (size_t)ch[j] * Kc;
-          tc.off[1 + j] = Dk * 128 + done * Kc * 4;
-          tc.bytes[1 + j] = nc[j] * Kc * 4;
-          tc.src[4 + j] = q.conv_w + (size_t)ch[j] * Kc;
-          tc.off[4 + j] = Dk * 128 + nch * Kc * 4 + done * Kc * 2;
-          tc.bytes[4 + j] = nc[j] * Kc * 2;
-          done += nc[j];
-        }
-        tc.total = gdn_tile_bytes(Dk, Kc);
-        tc.span = tc.total;
-        tc.meta = 0;
-        tc.policy = 0;
-        c.i = 1;
-        return true;
-      }
-    }
-    // this sequence's walk of the phase is done: the next sequence, or the next phase
-    if (++c.b < (c.ty == kPhGemv && P.batch > 1 ? c.g.npass : P.batch)) {
-      open_seq(P, c);
-      continue;
-    }
-    c.open = false;
-    if (++c.p >= n_phases(c.L.kind)) {
-      c.p = 0;
-      ++c.l;
-    }
-  }
-  return false;
-}
-
-// The producer. Tile i takes slot i % kDecSlots and the ring bytes
-// [v_i, v_i + span_i) of a virtual byte stream, placed at v_i mod kDecRing; a tile
-// that would cross the ring's end starts at the next multiple of kDecRing. It may
-// be written once every tile that started more than kDecRing - span_i bytes before
-// its end is consumed, and once the slot's previous tile (i - kDecSlots) is.
-// Consumption is in order, so `vcons` (the start of the oldest unconsumed tile)
-// and `tail` (its index) describe all of it.
+// The producer (one thread). Weights are read from HBM by a batch's first pass
+// over a phase and kept in L2 for the others (evict-last), the last pass marking
+// them evict-first.
 __device__ __noinline__ void produce_all(const LayerDesc* layers) {
   const Program& P = prog();
   const Smem sh = smem_map(smem_raw);
-  Cursor& c = s_cursor;
   const uint64_t stream = policy_evict_first(), keep = policy_evict_last();
-  c.l = 0;
-  c.lc = 0xffffffffu;
-  c.p = 0;
-  c.open = false;
-  c.ph = 0;
-  uint32_t i = 0, tail = 0, vnext = 0, vcons = 0;
-  bool dead = false;
-  TileCopy tc;
-  while (!dead && next_copy(P, layers, c, tc, keep, stream)) {
-    const uint32_t span = (tc.span + 127) & ~127u;
-    uint32_t v = vnext, ph = v % kDecRing;
-    if (ph + span > (uint32_t)kDecRing) {
-      v += kDecRing - ph;
-      ph = 0;
+  int* const status = P.status;
+  unsigned long long* const trace = P.trace;
+  const uint32_t trace_phases = P.trace_phases, n_layers = P.n_layers, batch = P.batch;
+  Ring rg = {0u, 0u, 0u, 0u, P.ring_bytes, false};
+  uint32_t phc = 0;  // phases opened (the timeline's phase index + 1)
+  bool fresh = false;
+  // timeline: when the phase's first tile is issued
+  auto issued = [&]() {
+    if (fresh) {
+      fresh = false;
+      if (trace && phc - 1 < trace_phases) trace[((size_t)blockIdx.x * trace_phases + phc - 1) * kTraceSlots + 7] = global_ns();
     }
-    while (tail < i && (i - tail >= (uint32_t)kDecSlots || v + span - vcons > (uint32_t)kDecRing)) {
-      if (!mbar_wait(&sh.empty[slot_of(tail)], parity_of(tail))) {
-        set_status(P.status, kStatusTimeout);
-        dead = true;
-        break;
+    ++rg.i;
+  };
+  for (uint32_t l = 0; l < n_layers; ++l) {
+    s_prod.L = layers[l];
+    const LayerDesc& L = s_prod.L;
+    const int np = n_phases(L.kind);
+    for (int p = 0; p < np; ++p) {
+      ++phc;
+      fresh = true;
+      const int ty = phase_type(L.kind, p);
+      if (ty == kPhGemv) {
+        gemv_of(P, L, l, p, 0, s_prod.g);
+        const Gemv& g = s_prod.g;
+        const uint32_t K = g.K, gs = g.gstride, R = g.R, soff = g.scale_off, boff = g.bias_off;
+        const uint32_t span = boff + R * gs * 2, rb = g.rb, re = g.re, nseg = g.nseg;
+        const uint32_t npass = batch > 1 ? g.npass : 1u;
+        for (uint32_t pass = 0; pass < npass; ++pass) {
+          const uint64_t pol = pass + 1 < npass ? keep : stream;
+          for (uint32_t sg = 0; sg < nseg; ++sg) {
+            const uint32_t base = g.row0[sg], lo = max(rb, base), hi = min(re, g.row0[sg + 1]);
+            if (lo >= hi) continue;
+            const uint8_t* codes = g.seg[sg].codes;
+            const uint16_t* scales = g.seg[sg].scales;
+            const uint16_t* biases = g.seg[sg].biases;
+            for (uint32_t r = lo; r < hi; r += R) {
+              const uint32_t nr = min(R, hi - r), local = r - base, cb = nr * K, sb = nr * gs * 2;
+              uint8_t* dst = ring_claim(rg, sh, span, cb + 2 * sb, r | (nr << 24), status);
+              if (!dst) goto drain;
+              uint64_t* fb = &sh.full[slot_of(rg.i)];
+              bulk_g2s_stream(dst, codes + (size_t)local * K, cb, fb, pol);
+              bulk_g2s_stream(dst + soff, scales + (size_t)local * gs, sb, fb, pol);
+              bulk_g2s_stream(dst + boff, biases + (size_t)local * gs, sb, fb, pol);
+              issued();
+            }
+          }
+        }
+      } else if (ty == kPhAttn) {
+        const uint32_t rowh = P.Hkv * P.D, rowbytes = rowh * 2;
+        for (uint32_t b = 0; b < batch; ++b) {
+          const size_t seq_off = (size_t)L.capacity * rowh * b;
+          const uint16_t* kc = L.kc + seq_off;
+          const uint16_t* vc = L.vc + seq_off;
+          const Span sp = attn_span(P, L.capacity, b);
+          for (uint32_t t = 0; t < sp.ntiles; ++t) {
+            const uint32_t tt = sp.t0 + t * kTS, n = min((uint32_t)kTS, sp.tc_end - tt);
+            // rows past n are read (masked) by the consumers
+            uint8_t* dst = ring_claim(rg, sh, 2 * kTS * rowbytes, 2 * n * rowbytes, 0u, status);
+            if (!dst) goto drain;
+            uint64_t* fb = &sh.full[slot_of(rg.i)];
+            bulk_g2s(dst, kc + (size_t)tt * rowh, n * rowbytes, fb);
+            bulk_g2s(dst + kTS * rowbytes, vc + (size_t)tt * rowh, n * rowbytes, fb);
+            issued();
+          }
+        }
+      } else if (ty == kPhGdn) {
+        // the work item's state block, conv state and conv weights, one tile per sequence
+        const GdnItem w = gdn_item(P);
+        if (!w.ok) continue;
+        const uint32_t Dk = P.Dk, Kc = P.Kc, nch = 2 * Dk + 32;
+        const uint32_t ch[3] = {w.hk * Dk, P.Hk * Dk + w.hk * Dk, 2 * P.Hk * Dk + w.h * P.Dv + w.v0};
+        const uint32_t nc[3] = {Dk, Dk, 32};
+        const uint32_t bytes = gdn_tile_bytes(Dk, Kc);
+        for (uint32_t b = 0; b < batch; ++b) {
+          const float* ssm = L.ssm + (size_t)P.Hv * P.Dk * P.Dv * b;
+          const float* conv = L.conv_state + (size_t)P.C * Kc * b;
+          uint8_t* dst = ring_claim(rg, sh, bytes, bytes, 0u, status);
+          if (!dst) goto drain;
+          uint64_t* fb = &sh.full[slot_of(rg.i)];
+          bulk_g2s(dst, ssm + (size_t)blockIdx.x * Dk * 32, Dk * 128, fb);
+          uint32_t done = 0;
+#pragma unroll
+          for (int j = 0; j < 3; ++j) {
+            bulk_g2s(dst + Dk * 128 + done * Kc * 4, conv + (size_t)ch[j] * Kc, nc[j] * Kc * 4, fb);
+            bulk_g2s(dst + Dk * 128 + nch * Kc * 4 + done * Kc * 2, L.conv_w + (size_t)ch[j] * Kc, nc[j] * Kc * 2, fb);
+            done += nc[j];
+          }
+          issued();
+        }
       }
-      ++tail;
-      vcons = tail < i ? c.vstart[slot_of(tail)] : v;
     }
-    if (dead) break;
-    if (c.fresh) {  // timeline: when the phase's first tile is issued
-      c.fresh = false;
-      if (P.trace && c.ph - 1 < P.trace_phases)
-        P.trace[((size_t)blockIdx.x * P.trace_phases + c.ph - 1) * kTraceSlots + 7] = global_ns();
-    }
-    const uint32_t st = slot_of(i);
-    c.vstart[st] = v;
-    sh.toff[st] = ph;
-    sh.tmeta[st] = tc.meta;
-    uint8_t* dst = sh.ring + ph;
-    mbar_arrive_expect_tx(&sh.full[st], tc.total);
-    for (uint32_t j = 0; j < tc.n; ++j) {
-      const uint8_t* src = static_cast<const uint8_t*>(tc.src[j]);
-      if (tc.policy) bulk_g2s_stream(dst + tc.off[j], src, tc.bytes[j], &sh.full[st], tc.policy);
-      else bulk_g2s(dst + tc.off[j], src, tc.bytes[j], &sh.full[st]);
-    }
-    vnext = v + span;
-    ++i;
   }
-  if (dead) {  // let the copies still in flight land before the CTA can exit
-    for (uint32_t j = tail; j < i; ++j) mbar_wait(&sh.full[slot_of(j)], parity_of(j));
-  }
+  return;
+drain:  // a wait ran out: let the copies still in flight land before the CTA can exit
+  for (uint32_t j = rg.tail; j < rg.i; ++j) mbar_wait(&sh.full[slot_of(j)], parity_of(j));
 }
 
 // ------------------------------------------------------------------ the kernel
 
 template <int D, int HPW, int DK, bool BATCHED>
 __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_constant__ Program Pk) {
-  const Smem sh = smem_map(smem_raw);
+  const Smem sh = smem_map(smem_raw, Pk.ring_bytes);
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // the program's header into shared memory: 4-byte words (the parameter block is
   // 8-byte aligned); the phase loops then never read the large parameter block
@@ -2065,12 +2015,15 @@ uint32_t attn_hpw(uint32_t H, uint32_t Hkv) {
 bool decode_dims_ok(const Program& p, bool has_fa, bool has_gdn, int num_sms) {
   // a GEMV phase of K columns and N rows: its tile fits a ring tile, its input
   // chunks, the CTA's partial sums and residual rows fit the phase buffer
-  const uint32_t room = kDecUnion;
+  const uint32_t room = p.union_bytes;
+  if (p.ring_bytes + p.union_bytes + kDecFixed != (uint32_t)kDecSmem || p.ring_bytes % 128 ||
+      p.ring_bytes < (uint32_t)kDecTileMax)
+    return false;
   auto gemv_ok = [&](uint32_t K, uint32_t N) {
     if (K == 0 || K % 64 || K > 12288 || N == 0 || N >= (1u << 24) || num_sms <= 0) return false;
     if (p.batch > 1) {  // tensor-core passes: one sequence's staged input fits; a tile fits
       const uint32_t R = batch_rows(K), gs = ((K / 64 + 7) / 8) * 8;
-      return batch_seq_bytes(K) + kBatchPart <= (uint32_t)kDecUnion &&
+      return batch_seq_bytes(K) + kBatchPart <= room &&
              (R * K + 15) / 16 * 16 + 4 * R * gs <= (uint32_t)kDecTileMax;
     }
     const uint32_t nch = K / 16;
@@ -2123,6 +2076,17 @@ bool decode_dims_ok(const Program& p, bool has_fa, bool has_gdn, int num_sms) {
     if (gdn_tile_bytes(p.Dk, p.Kc) > (uint32_t)kDecTileMax) return false;  // one ring tile
   }
   return true;
+}
+
+bool decode_pick_split(Program& p, bool has_fa, bool has_gdn, int num_sms) {
+  if (p.batch <= 1) {
+    p.ring_bytes = kDecRingLarge;
+    p.union_bytes = kDecUnionSmall;
+    if (decode_dims_ok(p, has_fa, has_gdn, num_sms)) return true;
+  }
+  p.ring_bytes = kDecRing;
+  p.union_bytes = kDecUnion;
+  return decode_dims_ok(p, has_fa, has_gdn, num_sms);
 }
 
 cudaError_t decode_set_attributes() {

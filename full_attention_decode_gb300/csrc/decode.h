@@ -71,6 +71,9 @@ struct Program {
   // reduced; null = off
   unsigned long long* trace;
   uint32_t trace_phases;
+  // shared memory split of this launch: the tile ring's bytes and the per-phase
+  // buffer's (ring_bytes + union_bytes + kDecFixed = kDecSmem)
+  uint32_t ring_bytes, union_bytes;
   LayerDesc layers[kMaxLayers];
 };
 
@@ -80,11 +83,19 @@ constexpr int kDecThreads = (kDecConsumerWarps + 1) * 32;
 // The tile ring: tiles of any size up to kDecTileMax sit at increasing offsets of
 // one circular buffer, at most kDecSlots in flight (one full/empty barrier pair
 // and one offset word per slot).
+// Two splits of the same dynamic shared memory between the ring and the per-phase
+// buffer (x chunks + partial sums / attention / GDN work area): a batch's
+// tensor-core passes stage several sequences' inputs in the larger buffer; a single
+// sequence needs at most about 28 KiB there and takes the larger ring (six 4B-shape
+// 12-row tiles of 2560 columns, ten 2-row tiles of 9216).
 constexpr int kDecRing = 174080;    // 170 KiB
 constexpr int kDecTileMax = 45056;  // 44 KiB
 constexpr int kDecSlots = 16;
-constexpr int kDecUnion = 53248;  // per-phase shared buffer (x chunks + partials / attention / GDN)
-constexpr int kDecSmem = kDecRing + 2 * kDecSlots * 8 + 16 + 2 * kDecSlots * 4 + 1024 + kDecUnion;
+constexpr int kDecUnion = 53248;
+constexpr int kDecFixed = 2 * kDecSlots * 8 + 16 + 2 * kDecSlots * 4 + 1024;  // barriers, slot words, misc
+constexpr int kDecSmem = kDecRing + kDecFixed + kDecUnion;
+constexpr int kDecRingLarge = 195840;
+constexpr int kDecUnionSmall = kDecSmem - kDecFixed - kDecRingLarge;
 
 cudaError_t decode_set_attributes();
 // Dequantise one matrix to fp32 [n][k]: fmaf(scale, code, bias), one rounding.
@@ -95,5 +106,8 @@ cudaError_t decode_launch(const Program& p, int num_sms, cudaStream_t stream);
 // Host check of the dims the kernel supports on a grid of num_sms CTAs; false if
 // unsupported.
 bool decode_dims_ok(const Program& p, bool has_fa, bool has_gdn, int num_sms);
+// Picks the launch's shared-memory split (the larger ring when every phase fits the
+// smaller buffer), then checks the dims; false if unsupported.
+bool decode_pick_split(Program& p, bool has_fa, bool has_gdn, int num_sms);
 
 }  // namespace q35
