@@ -164,15 +164,15 @@ __device__ __forceinline__ void grid_wait(const Program& P, uint32_t target) {
     uint32_t v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(P.barrier) : "memory");
     if (v < target) {
+      // back-to-back polls (each is an L2 round trip); the clock is read every 8th
       const uint64_t t0 = global_ns();
-      while (true) {
+      for (uint32_t n = 1;; ++n) {
         asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(P.barrier) : "memory");
         if (v >= target) break;
-        if (global_ns() - t0 > kWaitNs) {
+        if ((n & 7) == 0 && global_ns() - t0 > kWaitNs) {
           set_status(P.status, kStatusTimeout);
           break;
         }
-        __nanosleep(32);
       }
     }
   }
@@ -607,6 +607,11 @@ __device__ __noinline__ void gemv_prologue(unsigned long long* tr) {
   consumer_sync();
 }
 
+// Rows computed whole by one warp with nothing added after the sum (one K-part, no
+// residual) are stored by the row loop itself; the others go through the partial
+// sums and the epilogue.
+__device__ __forceinline__ bool gemv_direct(const Gemv& g) { return g.W == 1 && g.epi == 0; }
+
 // The row loop of a GEMV phase. Warp (rs, kp) computes row rs of every tile over
 // the chunks kp, kp + W, ... of each lane, reduces it across the warp and leaves
 // the sum in the partials; the producer publishes each tile's first row and row
@@ -644,6 +649,7 @@ __device__ __forceinline__ void gemv_tiles(const Gemv& g, const Smem& sh, uint32
   }
   const uint32_t rb = g.rb, ntiles = g.ntiles;
   float* part = gemv_partials(sh, nch) + kp * (g.re - rb);  // indexed by row - rb
+  const bool direct = gemv_direct(g);
   int* status = prog().status;
   if (tr && threadIdx.x == 0) tr[11] = global_ns();
   float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;  // sums of the last tiles' rows
@@ -697,7 +703,16 @@ __device__ __forceinline__ void gemv_tiles(const Gemv& g, const Smem& sh, uint32
       const float tot = reduce_transposed<4>(v, lane);  // lane L: the total of v[L / 8]
       const uint32_t q = lane >> 3;
       const uint32_t pr = q == 0 ? pr0 : q == 1 ? pr1 : q == 2 ? pr2 : pr3;
-      if ((lane & 7) == 0 && pr != ~0u) part[pr] = tot;
+      if ((lane & 7) == 0 && pr != ~0u) {
+        if (direct) {  // a whole row: its output, straight from the loop
+          const uint32_t row = rb + pr;
+          uint32_t sg = 0;
+          while (sg + 1 < g.nseg && row >= g.row0[sg + 1]) ++sg;
+          g.out[sg][row - g.row0[sg]] = to_bf16(tot);
+        } else {
+          part[pr] = tot;
+        }
+      }
       acc0 = acc1 = acc2 = acc3 = 0.f;
       pr0 = pr1 = pr2 = pr3 = ~0u;
     }
@@ -721,11 +736,12 @@ __device__ __noinline__ uint32_t gemv_main(uint32_t itd, unsigned long long* tr)
   return it | (dead ? kDeadBit : 0u);
 }
 
-// The rows of a GEMV phase, then its outputs: the K-parts of each row summed in a
-// fixed order, the residual added for the down projection, bf16 stores by
-// consecutive threads.
+// The rows of a GEMV phase, then (unless the row loop stored them) its outputs: the
+// K-parts of each row summed in a fixed order, the residual added for the down
+// projection, bf16 stores by consecutive threads.
 __device__ uint32_t gemv_rows(uint32_t itd, unsigned long long* tr) {
   itd = gemv_main(itd, tr);
+  if (gemv_direct(s_gemv)) return itd;
   consumer_sync();
   if (tr && threadIdx.x == 0) tr[12] = global_ns();
   const Gemv& g = s_gemv;
@@ -1347,14 +1363,18 @@ __device__ __noinline__ uint32_t attn_consume(uint32_t itd, unsigned long long* 
 #pragma unroll
         for (int e = 0; e < EPL; ++e) acc[j][e] *= corr;
       }
-      for (uint32_t t = 0; t < n; ++t) {
+      // unrolled over the tile's rows (independent loads); rows t >= n hold stale
+      // bytes that may not even be finite, so they are selected out, not weighted by 0
+#pragma unroll
+      for (uint32_t t = 0; t < (uint32_t)kTS; ++t) {
         float vf[EPL];
         load_row<EPL>(reinterpret_cast<const uint16_t*>(base + (kTS + t) * rowbytes) + g * D + lane * EPL, vf);
+        const bool live = t < n;
 #pragma unroll
         for (int j = 0; j < HPW; ++j) {
           const float pj = __shfl_sync(FULLMASK, p, (j * kTS + t) << SH);
 #pragma unroll
-          for (int e = 0; e < EPL; ++e) acc[j][e] = fmaf(pj, vf[e], acc[j][e]);
+          for (int e = 0; e < EPL; ++e) acc[j][e] = live ? fmaf(pj, vf[e], acc[j][e]) : acc[j][e];
         }
       }
     }
@@ -1888,27 +1908,36 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
     return P.trace && ph < P.trace_phases ? P.trace + ((size_t)blockIdx.x * P.trace_phases + ph) * kTraceSlots
                                           : nullptr;
   };
-  auto set_seq = [&](uint32_t l, int p, uint32_t b) {  // thread 0
-    if (p == 0 && b == 0) {  // once per layer from the parameter block
-      s_layer0 = Pk.layers[l];
-      s_layer = s_layer0;
-    } else if (BATCHED) {
+  auto set_seq = [&](uint32_t l, int p, uint32_t b) {  // warp 0
+    if (p == 0 && b == 0) {  // once per layer from the parameter block, a few words per lane
+      const uint32_t* src = reinterpret_cast<const uint32_t*>(&Pk.layers[l]);
+      uint32_t* d0 = reinterpret_cast<uint32_t*>(&s_layer0);
+      uint32_t* d1 = reinterpret_cast<uint32_t*>(&s_layer);
+      for (uint32_t i = lane; i < sizeof(LayerDesc) / 4; i += 32) {
+        const uint32_t v = src[i];
+        d0[i] = v;
+        d1[i] = v;
+      }
+      __syncwarp();
+    } else if (BATCHED && lane == 0) {
       s_layer = s_layer0;
       seq_caches(P, s_layer, b);
     }
-    s_seq.scratch = seq_scratch(P, b);
-    s_seq.x_in = P.x_in + (size_t)b * P.E;
-    s_seq.x_out = P.x_out + (size_t)b * P.E;
-    s_seq.b = b;
-    if (phase_type(s_layer.kind, p) == kPhGemv) gemv_of(P, s_layer, l, p, b, s_gemv);
+    if (lane == 0) {
+      s_seq.scratch = seq_scratch(P, b);
+      s_seq.x_in = P.x_in + (size_t)b * P.E;
+      s_seq.x_out = P.x_out + (size_t)b * P.E;
+      s_seq.b = b;
+      if (phase_type(s_layer.kind, p) == kPhGemv) gemv_of(P, s_layer, l, p, b, s_gemv);
+    }
   };
-  if (threadIdx.x == 0 && P.n_layers > 0) set_seq(0, 0, 0);
+  if (warp == 0 && P.n_layers > 0) set_seq(0, 0, 0);
   for (uint32_t l = 0; l < P.n_layers; ++l) {
     for (int p = 0;; ++p, ++ph) {
       if (l > 0 || p > 0) {
         mark(0);
         grid_arrive(P);
-        if (threadIdx.x == 0) set_seq(l, p, 0);
+        if (warp == 0) set_seq(l, p, 0);
         grid_wait(P, ++nbar * gridDim.x);
         mark(1);
       } else {
@@ -1940,7 +1969,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
       for (uint32_t b = 0; b < nb; ++b) {
         if (b > 0) {  // the next sequence: its descriptions, once every warp is done with the last
           consumer_sync();
-          if (threadIdx.x == 0) set_seq(l, p, b);
+          if (warp == 0) set_seq(l, p, b);
           consumer_sync();
         }
         if (s_layer.kind == kLayerGDN && p == 2 && warp == NCW - 1) conv_shift_qk(s_layer.conv_state, s_seq.scratch);
