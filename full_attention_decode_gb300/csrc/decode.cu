@@ -296,12 +296,12 @@ __device__ __forceinline__ int dot16i(const uint4 w, const XQ& q) {
 // Warps per row W (a divisor of the consumer warps) and 16-element chunks per lane
 // (at most 5): the fewest wasted chunk slots, then the fewest warps per row.
 __host__ __device__ inline void pick_split(uint32_t nch, uint32_t& W, uint32_t& cpl) {
-  const uint32_t divs[6] = {1, 2, 3, 4, 6, 12};
   W = 0;
   cpl = 0;
   uint32_t best = 0xffffffffu;
-  for (uint32_t i = 0; i < 6; ++i) {
-    const uint32_t w = divs[i], c = (nch + 32 * w - 1) / (32 * w);
+  for (uint32_t w = 1; w <= (uint32_t)NCW; ++w) {
+    if (NCW % w) continue;
+    const uint32_t c = (nch + 32 * w - 1) / (32 * w);
     if (c > 5) continue;
     const uint32_t waste = c * 32 * w - nch;
     if (waste < best) {
