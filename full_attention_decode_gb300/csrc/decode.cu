@@ -364,6 +364,11 @@ struct Gemv {
 };
 
 __shared__ Gemv s_gemv;  // the current GEMV phase (written by thread 0 inside the barrier)
+// Per ring slot: where a GEMV tile's first row is stored, as an element offset
+// from the phase's first output (a phase's outputs are consecutive buffers of one
+// scratch block in segment order, or a single output), written by the producer with
+// the tile's other words; the row loop stores whole rows without a segment lookup.
+__shared__ uint32_t s_tout[kDecSlots];
 
 __device__ __forceinline__ void gemv_add(Gemv& g, const QMat& m, uint16_t* out, uint32_t stride) {
   g.seg[g.nseg] = m;
@@ -650,10 +655,12 @@ __device__ __forceinline__ void gemv_tiles(const Gemv& g, const Smem& sh, uint32
   const uint32_t rb = g.rb, ntiles = g.ntiles;
   float* part = gemv_partials(sh, nch) + kp * (g.re - rb);  // indexed by row - rb
   const bool direct = gemv_direct(g);
+  uint16_t* const obase = g.out[0];
   int* status = prog().status;
   if (tr && threadIdx.x == 0) tr[11] = global_ns();
   float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;  // sums of the last tiles' rows
-  uint32_t pr0 = ~0u, pr1 = ~0u, pr2 = ~0u, pr3 = ~0u;  // their places in part (~0u: none)
+  // their places: in part, or for whole rows in the outputs from obase (~0u: none)
+  uint32_t pr0 = ~0u, pr1 = ~0u, pr2 = ~0u, pr3 = ~0u;
   for (uint32_t t = 0; t < ntiles; ++t) {
     const uint32_t st = slot_of(it);
     if (!dead && !mbar_wait(&sh.full[st], parity_of(it))) {
@@ -665,6 +672,7 @@ __device__ __forceinline__ void gemv_tiles(const Gemv& g, const Smem& sh, uint32
       if (t + 1 == ntiles) tr[5] = global_ns();
     }
     const uint32_t meta = dead ? 0u : sh.tmeta[st];
+    const uint32_t tout = s_tout[st];
     const bool mine = rs < (meta >> 24);
     float sum = 0.f;
     if (mine) {
@@ -697,21 +705,15 @@ __device__ __forceinline__ void gemv_tiles(const Gemv& g, const Smem& sh, uint32
     // the lanes' sums of the last four tiles' rows are reduced across the warp
     // together (one transposed reduction instead of four)
     acc3 = acc2; acc2 = acc1; acc1 = acc0; acc0 = sum;
-    pr3 = pr2; pr2 = pr1; pr1 = pr0; pr0 = mine ? (meta & 0xFFFFFFu) + rs - rb : ~0u;
+    pr3 = pr2; pr2 = pr1; pr1 = pr0; pr0 = !mine ? ~0u : direct ? tout + rs : (meta & 0xFFFFFFu) + rs - rb;
     if ((t & 3) == 3 || t + 1 == ntiles) {
       float v[4] = {acc0, acc1, acc2, acc3};
       const float tot = reduce_transposed<4>(v, lane);  // lane L: the total of v[L / 8]
       const uint32_t q = lane >> 3;
       const uint32_t pr = q == 0 ? pr0 : q == 1 ? pr1 : q == 2 ? pr2 : pr3;
       if ((lane & 7) == 0 && pr != ~0u) {
-        if (direct) {  // a whole row: its output, straight from the loop
-          const uint32_t row = rb + pr;
-          uint32_t sg = 0;
-          while (sg + 1 < g.nseg && row >= g.row0[sg + 1]) ++sg;
-          g.out[sg][row - g.row0[sg]] = to_bf16(tot);
-        } else {
-          part[pr] = tot;
-        }
+        if (direct) obase[pr] = to_bf16(tot);  // a whole row: its output, straight from the loop
+        else part[pr] = tot;
       }
       acc0 = acc1 = acc2 = acc3 = 0.f;
       pr0 = pr1 = pr2 = pr3 = ~0u;
@@ -1737,7 +1739,7 @@ struct Ring {
 // (bounded) until the tiles it overwrites are consumed, publishes its ring offset
 // and GEMV rows, and arms its slot's full barrier. Null once a wait has run out.
 __device__ __forceinline__ uint8_t* ring_claim(Ring& rg, const Smem& sh, uint32_t span, uint32_t total,
-                                               uint32_t meta, int* status) {
+                                               uint32_t meta, uint32_t tout, int* status) {
   span = (span + 127) & ~127u;
   uint32_t v = rg.vnext, ph = v % rg.size;
   if (ph + span > rg.size) {
@@ -1757,6 +1759,7 @@ __device__ __forceinline__ uint8_t* ring_claim(Ring& rg, const Smem& sh, uint32_
   s_prod.vstart[st] = v;
   sh.toff[st] = ph;
   sh.tmeta[st] = meta;
+  s_tout[st] = tout;
   mbar_arrive_expect_tx(&sh.full[st], total);
   rg.vnext = v + span;
   return sh.ring + ph;
@@ -1802,12 +1805,13 @@ __device__ __noinline__ void produce_all(const LayerDesc* layers) {
           for (uint32_t sg = 0; sg < nseg; ++sg) {
             const uint32_t base = g.row0[sg], lo = max(rb, base), hi = min(re, g.row0[sg + 1]);
             if (lo >= hi) continue;
+            const uint32_t obase = (uint32_t)(g.out[sg] - g.out[0]);
             const uint8_t* codes = g.seg[sg].codes;
             const uint16_t* scales = g.seg[sg].scales;
             const uint16_t* biases = g.seg[sg].biases;
             for (uint32_t r = lo; r < hi; r += R) {
               const uint32_t nr = min(R, hi - r), local = r - base, cb = nr * K, sb = nr * gs * 2;
-              uint8_t* dst = ring_claim(rg, sh, span, cb + 2 * sb, r | (nr << 24), status);
+              uint8_t* dst = ring_claim(rg, sh, span, cb + 2 * sb, r | (nr << 24), obase + local, status);
               if (!dst) goto drain;
               uint64_t* fb = &sh.full[slot_of(rg.i)];
               bulk_g2s_stream(dst, codes + (size_t)local * K, cb, fb, pol);
@@ -1827,7 +1831,7 @@ __device__ __noinline__ void produce_all(const LayerDesc* layers) {
           for (uint32_t t = 0; t < sp.ntiles; ++t) {
             const uint32_t tt = sp.t0 + t * kTS, n = min((uint32_t)kTS, sp.tc_end - tt);
             // rows past n are read (masked) by the consumers
-            uint8_t* dst = ring_claim(rg, sh, 2 * kTS * rowbytes, 2 * n * rowbytes, 0u, status);
+            uint8_t* dst = ring_claim(rg, sh, 2 * kTS * rowbytes, 2 * n * rowbytes, 0u, 0u, status);
             if (!dst) goto drain;
             uint64_t* fb = &sh.full[slot_of(rg.i)];
             bulk_g2s(dst, kc + (size_t)tt * rowh, n * rowbytes, fb);
@@ -1846,7 +1850,7 @@ __device__ __noinline__ void produce_all(const LayerDesc* layers) {
         for (uint32_t b = 0; b < batch; ++b) {
           const float* ssm = L.ssm + (size_t)P.Hv * P.Dk * P.Dv * b;
           const float* conv = L.conv_state + (size_t)P.C * Kc * b;
-          uint8_t* dst = ring_claim(rg, sh, bytes, bytes, 0u, status);
+          uint8_t* dst = ring_claim(rg, sh, bytes, bytes, 0u, 0u, status);
           if (!dst) goto drain;
           uint64_t* fb = &sh.full[slot_of(rg.i)];
           bulk_g2s(dst, ssm + (size_t)blockIdx.x * Dk * 32, Dk * 128, fb);
