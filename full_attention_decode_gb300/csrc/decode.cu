@@ -77,7 +77,7 @@ struct Smem {
   uint32_t* toff;    // ring offset of the tile in each slot (written before its copies)
   uint32_t* tmeta;  // GEMV tiles: first row | rows << 24
   float* misc;     // 256 floats (1 KiB): reductions, gate/beta
-  uint8_t* uni;    // per-phase buffer (kDecUnion bytes)
+  uint8_t* uni;    // per-phase buffer (the launch's union_bytes)
 };
 
 __device__ __forceinline__ Smem smem_map(uint8_t* base, uint32_t ring_bytes) {
