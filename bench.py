@@ -161,6 +161,32 @@ class Clocks:
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(sm)}
 
 
+# ---------------------------------------------------------------------- the job across ranks
+
+
+def max_over_ranks(value: float, dist=None, device="cpu") -> float:
+    """The largest of the ranks' values: the job takes as long as its slowest rank.
+    `dist` is torch.distributed (or None for one process); `device` the device a
+    rank's collectives use (cuda under NCCL, cpu under gloo)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tok_s(ms_per_step: float, world: int, batch: int) -> float:
+    """Whole-job decode throughput: every rank decodes `batch` sequences of its own
+    (independent replicas), one token each per step."""
+    return 1000.0 / ms_per_step * world * batch
+
+
+def replica_seed(rank: int) -> int:
+    """Each replica decodes its own synthetic sequences."""
+    return SEED + rank
+
+
 # ---------------------------------------------------------------------- GPU arm
 
 
@@ -186,7 +212,7 @@ def run_gpu(args) -> dict | None:
     cfg = dict(cfg, num_layers=len(kinds))
     c = B.make_config(cfg)
     nb = args.batch
-    seed = SEED + rank  # each replica decodes its own sequences
+    seed = replica_seed(rank)
     if nb > 1:  # each sequence at its own position, U{1024..65536}, seeded
         positions = [int(p) for p in np.random.default_rng([seed, 4242]).integers(1024, 65537, size=nb)]
     else:
@@ -252,11 +278,7 @@ def run_gpu(args) -> dict | None:
         ev1.record(stream)
         stream.synchronize()
     barrier()
-    ms = ev0.elapsed_time(ev1) / args.steps
-    if dist is not None:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, dist, "cuda")
     status = B.qwen35_read_device_status(scratch, stream)
     if args.stack_only:  # profiling runs: the graph replays alone
         graph.close()
@@ -277,10 +299,7 @@ def run_gpu(args) -> dict | None:
         stream.synchronize()
     e2e_ms = (time.perf_counter() - t_e0) * 1e3 / args.steps
     barrier()
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, dist, "cuda")
 
     # ---- the quantised GEMV phase alone (the same kernel on a one-GEMV program):
     # every layer's gate_proj (9216 x 2560, 25.1 MB) back to back, 32 distinct
@@ -318,7 +337,7 @@ def run_gpu(args) -> dict | None:
     ab["step"] = per_seq[0]["weights"] + sum(kv_seq) + nb * per_seq[0]["gdn_state_all"]
     seq_mid = positions[0] + mid
     traffic, traffic_note = profiled_traffic(ab["step"]) if nb == 1 and args.prefill == PREFILL else (None, "not captured")
-    tok_s = 1000.0 / ms * world * nb
+    tok_s = job_tok_s(ms, world, nb)
     step_gbs = ab["step"] / (ms * 1e-3) / 1e9
     gemv_gbs = gemv_bytes / (gemv_ms * 1e-3) / 1e9
     res = {
@@ -344,7 +363,7 @@ def run_gpu(args) -> dict | None:
                      "kernel": "decode_kernel (one launch = the whole 32-layer step)",
                      "bytes_per_launch": ab["step"], "us_per_launch": round(ms * 1e3, 2),
                      "peak_kind": peak_kind},
-        "e2e": {"value": round(1000.0 / e2e_ms * world * nb, 2), "unit": "tok/s", "ms_per_step": round(e2e_ms, 4),
+        "e2e": {"value": round(job_tok_s(e2e_ms, world, nb), 2), "unit": "tok/s", "ms_per_step": round(e2e_ms, 4),
                 "h2d_bytes_per_step": nb * cfg["hidden"] * 2, "d2h_bytes_per_step": nb * cfg["hidden"] * 2},
         "gpu_launches": args.steps,
         "clocks": clk.summary(),

@@ -201,6 +201,45 @@ def test_tiny_stack_16_steps(use_graph):
         g.close()
 
 
+def test_resume_from_snapshot_is_bit_exact():
+    """Checkpoint and resume: the caller owns the KV cache, the linear-attention
+    state and the device position, so copying them mid-run and restoring them later
+    reproduces the uninterrupted run bit for bit (every reduction of the decode runs
+    in a fixed order)."""
+    init()
+    cfg, kinds, layers, dev, caches, _ = _tiny_stack()
+    c = B.make_config(cfg)
+    entries = [B.stack_layer(k, l, cc) for k, l, cc in zip(kinds, dev, caches)]
+    scratch = B.new_scratch(B.qwen35_stack_scratch_bytes(c))
+    x_in = torch.empty(cfg["hidden"], dtype=torch.int16, device="cuda")
+    x_out = torch.empty_like(x_in)
+    d_pos = torch.zeros(1, dtype=torch.int32, device="cuda")
+    persistent = [caches[0].conv, caches[0].ssm, caches[1].k, caches[1].v, d_pos]
+
+    def run(t0, t1):
+        outs = []
+        for t in range(t0, t1):
+            x_in.copy_(B.to_device(synth.x_in(0, t, cfg)))
+            assert B.qwen35_decode_step(c, entries, scratch, x_in, x_out, d_pos, 16) == 0
+            outs.append(x_out.clone())
+        torch.cuda.synchronize()
+        return outs
+
+    run(0, 6)
+    snapshot = [b.clone() for b in persistent]
+    uninterrupted = run(6, 12)
+    final = [b.clone() for b in persistent]
+    for b, s in zip(persistent, snapshot):
+        b.copy_(s)
+    resumed = run(6, 12)
+    for t, (a, b) in enumerate(zip(uninterrupted, resumed)):
+        assert torch.equal(a, b), t
+    for a, b in zip(final, persistent):
+        assert torch.equal(a, b)
+    assert int(d_pos.item()) == 12
+    assert B.qwen35_read_device_status(scratch) == 0
+
+
 # ------------------------------------------------------------------ 4B-shape layers (configs 1, 2)
 
 
