@@ -323,6 +323,30 @@ def run_gpu(args) -> dict | None:
     gemv_ms = e0.elapsed_time(e1) / (reps * len(cw))
     m0 = mats[0]
     gemv_bytes = m0.n * m0.k + 2 * m0.n * (m0.k // 64) * 2
+
+    # ---- the output head after the stack: final norm + lm_head GEMV over the full
+    # vocabulary + greedy token (qwen35_lm_head_greedy), back to back
+    head = synth.head(seed, cfg)
+    vocab, E = cfg["vocab"], cfg["hidden"]
+    h_nw = B.to_device(head["final_norm"])
+    h_w = B.DeviceQWeight(head["lm_head"])
+    h_logits = torch.empty(vocab, dtype=torch.int16, device="cuda")
+    h_tok = torch.zeros(1, dtype=torch.int32, device="cuda")
+    h_scr = B.new_scratch(4096, stream=stream)
+    h_x = x_out[:E]
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            assert B.qwen35_lm_head_greedy(c, h_nw, h_w.c(), h_x, h_logits, h_tok, h_scr, stream) == 0
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(10):
+            assert B.qwen35_lm_head_greedy(c, h_nw, h_w.c(), h_x, h_logits, h_tok, h_scr, stream) == 0
+        e1.record(stream)
+    stream.synchronize()
+    head_ms = e0.elapsed_time(e1) / 10
+    head_bytes = vocab * E + 2 * vocab * (E // 64) * 2 + E * 2
+    head_status = B.qwen35_read_device_status(h_scr, stream)
+    del h_w
     graph.close()
     if rank != 0:
         if dist is not None:
@@ -357,6 +381,12 @@ def run_gpu(args) -> dict | None:
                    "frac_step_of_8000": round(step_gbs / 8000.0, 4),
                    "gemv_phase_alone": {"matrix": "9216x2560", "bytes": gemv_bytes,
                                         "us": round(gemv_ms * 1e3, 2), "gbs": round(gemv_gbs, 1)},
+                   "lm_head_greedy": {"vocab": vocab, "bytes": head_bytes, "us": round(head_ms * 1e3, 2),
+                                      "gbs": round(head_bytes / (head_ms * 1e-3) / 1e9, 1),
+                                      "frac_of_peak": round(head_bytes / (head_ms * 1e-3) / 1e9 / peak, 4),
+                                      "tok_s_stack_plus_head": round(1000.0 / (ms + head_ms) * world * nb, 2)
+                                      if nb == 1 else None,
+                                      "device_status": head_status},
                    "device_status": status, "setup_s": round(setup_s, 1)},
         "roofline": {"bound": "hbm", "achieved": round(step_gbs, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(step_gbs / peak, 4), "traffic": traffic, "traffic_source": traffic_note,

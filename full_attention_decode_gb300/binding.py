@@ -110,6 +110,8 @@ _SIGS = {
     "qwen35_graph_destroy": (C.c_int, [_P]),
     "qwen35_gemv": (C.c_int, [C.POINTER(qwen35_qweight), _P, _P, _P, C.c_size_t, _P]),
     "qwen35_dequant": (C.c_int, [C.POINTER(qwen35_qweight), _P, _P]),
+    "qwen35_lm_head_greedy": (C.c_int, [C.POINTER(qwen35_config), _P, C.POINTER(qwen35_qweight), _P, _P, _P, _P,
+                                        C.c_size_t, _P]),
     "qwen35_debug_scratch_offset": (C.c_size_t, [C.POINTER(qwen35_config), C.c_int, C.c_char_p]),
     "qwen35_debug_trace": (C.c_int, [_P, C.c_uint32]),
 }
@@ -273,6 +275,11 @@ class Graph:
 
 def qwen35_gemv(w, x, y, scratch, stream=None):
     return lib().qwen35_gemv(C.byref(w), _ptr(x), _ptr(y), _ptr(scratch), scratch.numel(), _stream(stream))
+
+
+def qwen35_lm_head_greedy(cfg, final_norm, lm_head, x, logits, token, scratch, stream=None):
+    return lib().qwen35_lm_head_greedy(C.byref(cfg), _ptr(final_norm), C.byref(lm_head), _ptr(x), _ptr(logits),
+                                       _ptr(token), _ptr(scratch), scratch.numel(), _stream(stream))
 
 
 def qwen35_debug_scratch_offset(cfg, kind, name: str) -> int:

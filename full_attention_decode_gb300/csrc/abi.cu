@@ -607,6 +607,34 @@ int qwen35_debug_trace(unsigned long long* d_trace, uint32_t max_phases) {
   return QWEN35_OK;
 }
 
+int qwen35_lm_head_greedy(const qwen35_config* cfg, const qwen35_bf16* final_norm, const qwen35_qweight* lm_head,
+                          const qwen35_bf16* x, qwen35_bf16* logits, int32_t* token, void* scratch,
+                          size_t scratch_bytes, void* stream) {
+  if (!cfg || !lm_head || !aligned16(final_norm) || !aligned16(x) || !aligned16(logits) || !token ||
+      ((uintptr_t)token % 4) || !aligned16(scratch) || scratch_bytes < 256)
+    return QWEN35_ERR_INVALID_ARGUMENT;
+  const uint32_t E = cfg->hidden;
+  if (E == 0 || E % 64 || cfg->group_size != 64 || !(cfg->rms_eps >= 0.f)) return QWEN35_ERR_INVALID_ARGUMENT;
+  if (lm_head->n == 0 || !qw_ok(*lm_head, lm_head->n, E)) return QWEN35_ERR_INVALID_ARGUMENT;
+  if (E > 12288) return QWEN35_ERR_UNSUPPORTED;
+  if (num_sms() <= 0) return QWEN35_ERR_CUDA;
+  Dims d = {};
+  d.E = E;
+  d.I = E;
+  Program* p = new_program(cfg, d, scratch);
+  if (!p) return QWEN35_ERR_CUDA;
+  p->n_layers = 1;
+  p->x_in = x;
+  p->x_out = logits;
+  p->layers[0].kind = kLayerHead;
+  p->layers[0].m[0] = qm(*lm_head);
+  p->layers[0].input_ln = final_norm;
+  const cudaStream_t st = (cudaStream_t)stream;
+  const int r = launch(p, false, false, st);
+  if (r != QWEN35_OK) return r;
+  return argmax_bf16_launch(logits, lm_head->n, token, st) == cudaSuccess ? QWEN35_OK : QWEN35_ERR_CUDA;
+}
+
 int qwen35_dequant(const qwen35_qweight* w, float* out, void* stream) {
   if (!w || !out || !qw_ok(*w, w->n, w->k) || w->n == 0 || w->k == 0 || w->k % 64)
     return QWEN35_ERR_INVALID_ARGUMENT;

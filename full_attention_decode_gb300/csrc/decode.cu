@@ -399,11 +399,12 @@ __device__ __noinline__ void gemv_of(const Program& P, const LayerDesc& L, uint3
   const uint32_t SS = P.seq_stride / 2, SX = P.E;  // per-sequence strides: scratch, vectors
   const bool fa = L.kind == kLayerFA;
   const int mlp0 = fa ? 4 : 3;  // the gate|up phase
-  if (L.kind == kLayerGemv) {
+  if (L.kind == kLayerGemv || L.kind == kLayerHead) {
     g.K = P.E;
-    g.pro = kPlain;
+    g.pro = L.kind == kLayerHead ? kRms : kPlain;
     g.a = x_in;
     g.sa = SX;
+    g.nw = L.input_ln;
     gemv_add(g, L.m[0], x_out, SX);
   } else if (p == 0) {
     g.K = P.E;
@@ -2072,7 +2073,7 @@ bool decode_dims_ok(const Program& p, bool has_fa, bool has_gdn, int num_sms) {
     const LayerDesc& L = p.layers[l];
     auto n = [&](int i) { return L.m[i].n; };
     bool ok = true;
-    if (L.kind == kLayerGemv) {
+    if (L.kind == kLayerGemv || L.kind == kLayerHead) {
       ok = gemv_ok(p.E, n(0));
     } else if (L.kind == kLayerFA) {
       ok = gemv_ok(p.E, n(0) + n(1) + n(2)) && gemv_ok(p.H * p.D, n(3)) && gemv_ok(p.E, n(4) + n(5)) &&

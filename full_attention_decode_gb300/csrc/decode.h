@@ -21,7 +21,9 @@ struct QMat {
 };
 
 // kLayerGemv: a single GEMV phase, x_out = bf16(m[0] x_in) (the component entry point).
-enum LayerKind : int32_t { kLayerFA = 0, kLayerGDN = 1, kLayerGemv = 2 };
+// kLayerHead: the output head's GEMV, x_out = bf16(m[0] bf16(RMSNorm(x_in) * input_ln))
+// (input_ln holds the final norm's weights; x_out receives the logits).
+enum LayerKind : int32_t { kLayerFA = 0, kLayerGDN = 1, kLayerGemv = 2, kLayerHead = 3 };
 
 // Matrix slots of a layer.
 //   full attention:   0 q_proj, 1 k_proj, 2 v_proj, 3 o_proj, 4 gate, 5 up, 6 down
@@ -101,6 +103,9 @@ cudaError_t decode_set_attributes();
 // Dequantise one matrix to fp32 [n][k]: fmaf(scale, code, bias), one rounding.
 cudaError_t dequant_launch(const uint8_t* codes, const uint16_t* scales, const uint16_t* biases,
                            uint32_t n, uint32_t k, uint32_t gstride, float* out, cudaStream_t stream);
+// Index of the largest of n bf16 values (the lowest index among equal ones) into
+// *out: one block of 1024 threads.
+cudaError_t argmax_bf16_launch(const uint16_t* v, uint32_t n, int32_t* out, cudaStream_t stream);
 // Zeroes the barrier counter, then launches the program (cooperative, one CTA per SM).
 cudaError_t decode_launch(const Program& p, int num_sms, cudaStream_t stream);
 // Host check of the dims the kernel supports on a grid of num_sms CTAs; false if

@@ -152,6 +152,14 @@ def gdn_layer(seed: int, layer: int, cfg: dict) -> dict:
     }
 
 
+def head(seed: int, cfg: dict, vocab: int | None = None) -> dict:
+    """The model's output head: the final norm's weights (1 + N(0, 0.1)) and the
+    lm_head matrix [vocab][hidden], int8 group-64 like every projection."""
+    v = cfg["vocab"] if vocab is None else vocab
+    return {"final_norm": _norm_w(seed, ("final_norm",), cfg["hidden"]),
+            "lm_head": qweight(seed, ("lm_head",), v, cfg["hidden"])}
+
+
 def x_in(seed: int, step: int, cfg: dict, seq: int = 0) -> np.ndarray:
     """The layer-0 hidden vector of one decode step, bf16 N(0, 1)."""
     return to_bf16_bits(_rng(seed, "x_in", seq, step).standard_normal(cfg["hidden"]))

@@ -287,6 +287,26 @@ QWEN35_API int qwen35_graph_create_batched(const qwen35_config* cfg, const qwen3
 QWEN35_API int qwen35_gemv(const qwen35_qweight* w, const qwen35_bf16* x, qwen35_bf16* y, void* scratch,
                 size_t scratch_bytes, void* stream);
 
+/* The model's output head after the last decoder layer, with greedy token choice.
+ * The pages stop at the decoder layers and leave the final norm, the lm_head and
+ * sampling to the caller (page "Module qwen3_5": non-goals); this entry is that
+ * tail in the pages' conventions:
+ *   x_norm = bf16(RMSNorm(x) * final_norm), eps = cfg->rms_eps (as every rms_norm);
+ *   logits[v] = bf16(sum_k W[v][k] x_norm[k]) for v < lm_head->n (the vocabulary);
+ *   *token = the index of the largest logit, the lowest index among equal ones
+ *            (NaN logits are never chosen; -1 if every logit is NaN).
+ * x, final_norm: bf16 [hidden]; lm_head: [vocab][hidden] in the QuantWeights format
+ * of qwen35_qweight (k = hidden, a multiple of 64, at most 12288); logits: bf16
+ * [vocab], written; token: one int32 in device memory, written. All device
+ * pointers, caller-owned, 16-byte aligned (token 4-byte aligned); scratch: at least
+ * 256 bytes (its status word and barrier counter). Runs the quantised GEMV with
+ * the norm in its prologue, then a one-block argmax, on `stream`. Errors:
+ * QWEN35_ERR_INVALID_ARGUMENT (null or misaligned pointer, shape mismatch),
+ * QWEN35_ERR_UNSUPPORTED (hidden > 12288), QWEN35_ERR_CUDA (launch failure). */
+QWEN35_API int qwen35_lm_head_greedy(const qwen35_config* cfg, const qwen35_bf16* final_norm,
+                                     const qwen35_qweight* lm_head, const qwen35_bf16* x, qwen35_bf16* logits,
+                                     int32_t* token, void* scratch, size_t scratch_bytes, void* stream);
+
 /* Byte offset inside a layer's scratch of a named intermediate the last forward of
  * that kind left there, or (size_t)-1 for an unknown name: the counterpart of the
  * intra_dump hook of "linear_attention.rs" (named buffers readable after a stream

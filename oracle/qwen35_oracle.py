@@ -395,6 +395,37 @@ def decode_step(cfg: dict, kinds: list, layers: list, caches: list, x_in, cache_
     return x
 
 
+# ----------------------------------------------------------------------------
+# Output head
+# ----------------------------------------------------------------------------
+
+
+def lm_head_greedy(cfg: dict, head: dict, x_in, rows_per_chunk: int = 4096) -> tuple:
+    """The model's tail after the last decoder layer: final RMSNorm, the lm_head
+    GEMV and the greedy token. Returns (logits, token).
+
+    Reading: the pages stop at the decoder layers and leave the final norm, the
+    lm_head and sampling to the caller (page "Module qwen3_5"); this is the plain
+    tail of the model in the pages' conventions: x_norm = bf16(RMSNorm(x) * w) with
+    eps = rms_eps (the same rms_norm as every other norm), logits = bf16(W_lm x_norm)
+    (a bf16 GEMV output, like q_full or z), and the token is the index of the largest
+    bf16 logit, the lowest such index on a tie. The matrix is dequantised a block of
+    rows at a time (a full 248 320-row matrix in float64 would take 5 GB).
+    """
+    eps = cfg["rms_eps"]
+    x_norm = bf16_round(rms_norm(np.asarray(x_in, dtype=np.float64), bf16_to_f64(head["final_norm"]), eps))
+    w = head["lm_head"]
+    n = w["n"]
+    logits = np.empty(n, dtype=np.float64)
+    for r0 in range(0, n, rows_per_chunk):
+        r1 = min(n, r0 + rows_per_chunk)
+        part = {"codes": w["codes"][r0:r1], "scales": w["scales"][r0:r1], "biases": w["biases"][r0:r1],
+                "n": r1 - r0, "k": w["k"]}
+        logits[r0:r1] = bf16_round(gemv(part, x_norm))
+    token = int(np.argmax(logits))  # numpy returns the first index of the maximum
+    return logits, token
+
+
 def kv_from_bits(k_bits, v_bits) -> dict:
     return {"k": bf16_to_f64(k_bits), "v": bf16_to_f64(v_bits)}
 

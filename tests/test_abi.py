@@ -158,3 +158,25 @@ def test_linear_attention_and_stack_argument_errors():
     assert B.qwen35_decode_step(c, [bad_layer], S, 0x8000000, 0x9000000, 0x100, 16, 0) == \
         B.QWEN35_ERR_INVALID_ARGUMENT
     assert B.lib().qwen35_status_string(2) == b"position out of range"
+
+
+def test_lm_head_argument_errors_precede_launch():
+    cfg = synth.config("tiny")
+    c = B.make_config(cfg)
+    E = cfg["hidden"]
+    w = B.qwen35_qweight(0x1000000, 0x2000000, 0x3000000, 1000, E)
+    S = _FakeScratch(4096)
+    nw, x, logits, tok = 0x4000000, 0x5000000, 0x6000000, 0x7000000
+    f = B.qwen35_lm_head_greedy
+    assert f(c, nw, w, x + 2, logits, tok, S, 0) == B.QWEN35_ERR_INVALID_ARGUMENT  # misaligned x
+    assert f(c, nw, w, x, logits, tok + 2, S, 0) == B.QWEN35_ERR_INVALID_ARGUMENT  # misaligned token
+    assert f(c, None, w, x, logits, tok, S, 0) == B.QWEN35_ERR_INVALID_ARGUMENT  # no final norm
+    assert f(c, nw, w, x, logits, tok, _FakeScratch(255), 0) == B.QWEN35_ERR_INVALID_ARGUMENT
+    bad = B.qwen35_qweight(0x1000000, 0x2000000, 0x3000000, 1000, E + 64)
+    assert f(c, nw, bad, x, logits, tok, S, 0) == B.QWEN35_ERR_INVALID_ARGUMENT  # k != hidden
+    empty = B.qwen35_qweight(0x1000000, 0x2000000, 0x3000000, 0, E)
+    assert f(c, nw, empty, x, logits, tok, S, 0) == B.QWEN35_ERR_INVALID_ARGUMENT  # no vocabulary
+    big = synth.config("tiny")
+    big["hidden"] = 12288 + 64
+    wbig = B.qwen35_qweight(0x1000000, 0x2000000, 0x3000000, 1000, 12288 + 64)
+    assert f(B.make_config(big), nw, wbig, x, logits, tok, S, 0) == B.QWEN35_ERR_UNSUPPORTED

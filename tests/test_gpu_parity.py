@@ -240,6 +240,57 @@ def test_resume_from_snapshot_is_bit_exact():
     assert B.qwen35_read_device_status(scratch) == 0
 
 
+# ------------------------------------------------------------------ output head (lm_head, greedy token)
+
+
+def _run_head(cfg, head, x_bits):
+    init()
+    c = B.make_config(cfg)
+    nw = B.to_device(head["final_norm"])
+    w = B.DeviceQWeight(head["lm_head"])
+    x = B.to_device(x_bits)
+    logits = torch.empty(head["lm_head"]["n"], dtype=torch.int16, device="cuda")
+    tok = torch.full((1,), -7, dtype=torch.int32, device="cuda")
+    scratch = B.new_scratch(4096)
+    assert B.qwen35_lm_head_greedy(c, nw, w.c(), x, logits, tok, scratch) == 0
+    torch.cuda.synchronize()
+    assert B.qwen35_read_device_status(scratch) == 0
+    return f64(logits), int(tok.item())
+
+
+@pytest.mark.parametrize("name,vocab", [("tiny", 1000), ("4b", None)])
+def test_lm_head_greedy_matches_oracle(name, vocab):
+    cfg = synth.config(name)
+    head = synth.head(7, cfg, vocab)  # 4b: the full 248 320-token vocabulary
+    x_bits = synth.x_in(7, 0, cfg)
+    got, tok = _run_head(cfg, head, x_bits)
+    ref, _ = O.lm_head_greedy(cfg, head, O.bf16_to_f64(x_bits))
+    assert rel_l2(got, ref) <= TOL_X
+    # the token is decided on the kernel's own bf16 logits: their first maximal index
+    assert tok == int(np.argmax(got))
+
+
+def test_lm_head_ties_and_planted_winner():
+    cfg = synth.config("tiny")
+    x_bits = synth.x_in(6, 0, cfg)
+
+    def head_with_identical_rows(winner=None, factor=1.0):
+        h = synth.head(6, cfg, 1000)
+        w = h["lm_head"]
+        for key in ("codes", "scales", "biases"):
+            w[key][:] = w[key][0]
+        if winner is not None:
+            for key in ("scales", "biases"):
+                w[key][winner] = synth.to_bf16_bits(synth.bf16_bits_to_f32(w[key][winner]) * factor)
+        return h
+
+    got, tok = _run_head(cfg, head_with_identical_rows(), x_bits)
+    assert np.all(got == got[0]) and tok == 0  # equal logits: the lowest index
+    factor = 2.0 if got[0] > 0 else 0.5
+    got2, tok2 = _run_head(cfg, head_with_identical_rows(winner=637, factor=factor), x_bits)
+    assert tok2 == 637 and got2[637] == got[0] * factor
+
+
 # ------------------------------------------------------------------ 4B-shape layers (configs 1, 2)
 
 

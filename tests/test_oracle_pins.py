@@ -407,3 +407,52 @@ def test_stack_step_chains_layers():
     y1 = O.forward_linear_attention(CFG, layers[0], st, x)
     y2 = O.forward_full_attention(CFG, layers[1], kv, y1, 0, 1)
     np.testing.assert_array_equal(y2, y)
+
+
+# ---------------------------------------------------------------- output head
+
+def _head_with_identical_rows(seed, cfg, vocab, winner=None, factor=1.0):
+    """Every row of the lm_head a copy of row 0; row `winner` (if any) with its
+    scales and biases multiplied by `factor` (a power of two: exact in bf16)."""
+    h = synth.head(seed, cfg, vocab)
+    w = h["lm_head"]
+    for key in ("codes", "scales", "biases"):
+        w[key][:] = w[key][0]
+    if winner is not None:
+        for key in ("scales", "biases"):
+            w[key][winner] = synth.to_bf16_bits(synth.bf16_bits_to_f32(w[key][winner]) * factor)
+    return h
+
+
+def test_lm_head_greedy_against_library_and_brute_force():
+    cfg = synth.config("tiny")
+    head = synth.head(5, cfg, 300)
+    x = O.bf16_to_f64(synth.x_in(5, 0, cfg)) * 3.0
+    logits, tok = O.lm_head_greedy(cfg, head, x, rows_per_chunk=128)  # chunks: 128, 128, 44
+    # the norm through a library routine, the GEMV as an explicit dequantised matmul
+    w = torch.from_numpy(O.bf16_to_f64(head["final_norm"]))
+    xn = F.rms_norm(torch.from_numpy(x), (cfg["hidden"],), w, eps=cfg["rms_eps"])
+    xn = xn.to(torch.bfloat16).to(torch.float64)
+    qw = head["lm_head"]
+    g = qw["k"] // 64
+    s = torch.from_numpy(O.bf16_to_f64(qw["scales"])[:, :g]).repeat_interleave(64, dim=1)
+    b = torch.from_numpy(O.bf16_to_f64(qw["biases"])[:, :g]).repeat_interleave(64, dim=1)
+    W = torch.from_numpy(qw["codes"].astype(np.float64)) * s + b
+    ref = (W @ xn).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(logits, ref)
+    assert tok == int(torch.argmax(torch.from_numpy(ref)))  # torch: the first maximal index
+    assert logits[tok] == logits.max()
+
+
+def test_lm_head_greedy_ties_and_planted_winner():
+    cfg = synth.config("tiny")
+    x = O.bf16_to_f64(synth.x_in(6, 0, cfg))
+    base = _head_with_identical_rows(6, cfg, 64)
+    logits, tok = O.lm_head_greedy(cfg, base, x)
+    assert np.all(logits == logits[0]) and tok == 0  # all equal: the lowest index
+    # row 37 scaled by 2 (or 1/2) so that its logit is strictly the largest
+    factor = 2.0 if logits[0] > 0 else 0.5
+    win = _head_with_identical_rows(6, cfg, 64, winner=37, factor=factor)
+    logits2, tok2 = O.lm_head_greedy(cfg, win, x)
+    assert tok2 == 37
+    assert logits2[37] == logits[0] * factor
