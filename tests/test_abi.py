@@ -180,3 +180,21 @@ def test_lm_head_argument_errors_precede_launch():
     big["hidden"] = 12288 + 64
     wbig = B.qwen35_qweight(0x1000000, 0x2000000, 0x3000000, 1000, 12288 + 64)
     assert f(B.make_config(big), nw, wbig, x, logits, tok, S, 0) == B.QWEN35_ERR_UNSUPPORTED
+
+
+def test_well_formed_calls_without_a_device_fail_cleanly():
+    """With no CUDA device the runtime's device queries fail: a call that passes
+    every argument check returns QWEN35_ERR_CUDA (no crash, nothing launched)."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a CUDA device is present")
+    assert B.lib().qwen35_init() == B.QWEN35_ERR_CUDA
+    cfg = synth.config("tiny")
+    c = B.make_config(cfg)
+    kv = B.qwen35_kv_cache(0x5000000, 0x6000000, 16)
+    S = _FakeScratch(B.qwen35_scratch_bytes(c, 0))
+    assert B.qwen35_forward_full_attention(c, _fake_fa(cfg), S, kv, 0x8000000, 0x9000000, 3, 4, 0) == \
+        B.QWEN35_ERR_CUDA
+    w = B.qwen35_qweight(0x1000000, 0x2000000, 0x3000000, 1000, cfg["hidden"])
+    assert B.qwen35_lm_head_greedy(c, 0x4000000, w, 0x5000000, 0x6000000, 0x7000000, _FakeScratch(4096), 0) == \
+        B.QWEN35_ERR_CUDA
