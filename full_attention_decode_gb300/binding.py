@@ -112,7 +112,12 @@ _SIGS = {
     "qwen35_dequant": (C.c_int, [C.POINTER(qwen35_qweight), _P, _P]),
     "qwen35_lm_head_greedy": (C.c_int, [C.POINTER(qwen35_config), _P, C.POINTER(qwen35_qweight), _P, _P, _P, _P,
                                         C.c_size_t, _P]),
+    "qwen35_read_static_status": (C.c_int, [C.POINTER(C.c_int32), _P]),
     "qwen35_debug_scratch_offset": (C.c_size_t, [C.POINTER(qwen35_config), C.c_int, C.c_char_p]),
+    "qwen35_debug_stack_scratch_offset": (C.c_size_t, [C.POINTER(qwen35_config), C.c_char_p]),
+    "qwen35_debug_stage_dump": (C.c_int, [C.c_int]),
+    "qwen35_debug_set_wait_limit": (C.c_int, [C.c_ulonglong]),
+    "qwen35_debug_wait_probe": (C.c_int, [_P]),
     "qwen35_debug_trace": (C.c_int, [_P, C.c_uint32]),
 }
 
@@ -226,6 +231,13 @@ def qwen35_forward_linear_attention_static(cfg, layer, state, x_in, x_out, strea
                                                         _ptr(x_in), _ptr(x_out), _stream(stream))
 
 
+def qwen35_read_static_status(stream=None) -> int:
+    """The device status word of the static scratch (after a stream synchronise)."""
+    out = C.c_int32(0)
+    _check("qwen35_read_static_status", lib().qwen35_read_static_status(C.byref(out), _stream(stream)))
+    return out.value
+
+
 def qwen35_decode_step(cfg, layers, scratch, x_in, x_out, d_cache_pos, max_seq_len, stream=None):
     arr = (qwen35_layer * len(layers))(*layers)
     return lib().qwen35_decode_step(C.byref(cfg), arr, len(layers), _ptr(scratch), scratch.numel(), _ptr(x_in),
@@ -286,12 +298,42 @@ def qwen35_debug_scratch_offset(cfg, kind, name: str) -> int:
     return lib().qwen35_debug_scratch_offset(C.byref(cfg), kind, name.encode())
 
 
-def scratch_view(scratch: torch.Tensor, cfg, kind, name: str, n: int) -> torch.Tensor:
-    """The bf16 intermediate `name` (n elements) inside a layer's scratch, as int16 bits."""
-    off = qwen35_debug_scratch_offset(cfg, kind, name)
+def qwen35_debug_stack_scratch_offset(cfg, name: str) -> int:
+    return lib().qwen35_debug_stack_scratch_offset(C.byref(cfg), name.encode())
+
+
+# the fused steps' values, stored as plain bf16 while the stage dump is on; every
+# other named intermediate is a 32-bit word per element with the bf16 value in its
+# high half
+STAGE_DUMPS = ("x_norm", "x_norm2", "qkv_smooth", "y_norm")
+
+
+def scratch_view(scratch: torch.Tensor, cfg, kind, name: str, n: int, seq: int = 0, seq_stride: int = 0) -> torch.Tensor:
+    """The bf16 values of intermediate `name` (n elements) inside a scratch, as int16
+    bits (a copy for the tagged words, a view for the stage dumps). kind None: the
+    stack's layout; seq / seq_stride: sequence `seq` of a batch."""
+    off = qwen35_debug_stack_scratch_offset(cfg, name) if kind is None else qwen35_debug_scratch_offset(cfg, kind, name)
     if off == C.c_size_t(-1).value:
         raise KeyError(name)
-    return scratch[off:off + 2 * n].view(torch.int16)
+    off += seq * seq_stride
+    if name in STAGE_DUMPS:
+        return scratch[off:off + 2 * n].view(torch.int16)
+    words = scratch[off:off + 4 * n].view(torch.int32)
+    return (words >> 16).to(torch.int16)
+
+
+def qwen35_debug_stage_dump(on: bool):
+    return lib().qwen35_debug_stage_dump(1 if on else 0)
+
+
+def qwen35_debug_set_wait_limit(limit_ns: int):
+    """Bounded waits of later launches give up after limit_ns (0: the default, 1 s)."""
+    return lib().qwen35_debug_set_wait_limit(limit_ns)
+
+
+def qwen35_debug_wait_probe(flag):
+    """Later launches first wait (bounded) on the device word `flag` (None: off)."""
+    return lib().qwen35_debug_wait_probe(_ptr(flag))
 
 
 def qwen35_debug_trace(buf, max_phases: int):

@@ -4,14 +4,16 @@
 // Every forward is one launch of decode_kernel (decode.cu) over a program of
 // layers: one layer for qwen35_forward_full_attention / _dpos /
 // qwen35_forward_linear_attention, every layer of the stack for
-// qwen35_decode_step. A launch is preceded by a 4-byte memset of its grid-barrier
-// counter, so a captured decode step is two graph nodes.
+// qwen35_decode_step. A launch is preceded by a memset of the scratch's tagged
+// words (the results CTAs hand each other), so a captured decode step is two graph
+// nodes.
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
 #include <new>
 
 #include "qwen35_decode.h"  // include/ (on the include path)
+#include "common.cuh"
 #include "decode.h"
 
 using namespace q35;
@@ -78,7 +80,9 @@ bool qw_ok(const qwen35_qweight& w, uint32_t n, uint32_t k) {
 
 // ---------------------------------------------------------------- scratch layout
 
-// [0, 4) device status word; [4, 8) grid-barrier counter; intermediates from 256.
+// [0, 4) device status word; a sequence's block from 256: the tagged words other
+// CTAs read (32-bit words, zeroed before each launch), then the split-KV partials,
+// then the debug stage dumps (bf16).
 struct Layout {
   ScratchMap m;
   size_t total;
@@ -93,39 +97,49 @@ struct Bump {
   }
 };
 
-Layout layout(const Dims& d, int kind) {
+// Which layer kinds a layout serves (a stack of both kinds keeps both sets apart).
+constexpr int kHasFa = 1, kHasGdn = 2;
+
+Layout layout(const Dims& d, int kinds) {
   Layout L = {};
   Bump b;
-  L.m.x_resid = b.take(d.E * 2);
-  L.m.g = b.take(d.I * 2);
-  L.m.u = b.take(d.I * 2);
-  if (kind == QWEN35_LAYER_FULL_ATTENTION) {
-    L.m.q_full = b.take((size_t)2 * d.H * d.D * 2);
-    L.m.k = b.take((size_t)d.Hkv * d.D * 2);
-    L.m.v = b.take((size_t)d.Hkv * d.D * 2);
-    L.m.ga = b.take((size_t)d.H * d.D * 2);
-    L.m.o = b.take((size_t)d.E * 2);
+  auto words = [&](size_t n) { return b.take(n * 4); };
+  L.m.tag_begin = (uint32_t)b.off;
+  L.m.x_resid = words(d.E);
+  L.m.g = words(d.I);
+  L.m.u = words(d.I);
+  L.m.xa = words(d.E);
+  if (kinds & kHasFa) {
+    L.m.q_full = words((size_t)2 * d.H * d.D);
+    L.m.k = words((size_t)d.Hkv * d.D);
+    L.m.v = words((size_t)d.Hkv * d.D);
+    L.m.ga = words((size_t)d.H * d.D);
+    L.m.o = words(d.E);
+    L.m.flags = words(kDecMaxSplits);
+  }
+  if (kinds & kHasGdn) {
+    L.m.dt_raw = words(d.Hv);
+    L.m.b_raw = words(d.Hv);
+    L.m.qkv = words(d.C);
+    L.m.z = words(d.Z);
+    L.m.y = words(d.Z);
+    L.m.out = words(d.E);
+  }
+  L.m.tag_end = (uint32_t)b.off;
+  if (kinds & kHasFa) {
     L.m.part_o = b.take((size_t)kDecMaxSplits * d.H * d.D * 4);
     L.m.part_ml = b.take((size_t)kDecMaxSplits * d.H * 2 * 4);
-  } else {
-    L.m.dt_raw = b.take(d.Hv * 2);
-    L.m.b_raw = b.take(d.Hv * 2);
-    L.m.qkv = b.take((size_t)d.C * 2);
-    L.m.z = b.take((size_t)d.Z * 2);
-    L.m.y = b.take((size_t)d.Z * 2);
-    L.m.out = b.take((size_t)d.E * 2);
+  }
+  L.m.x_norm = b.take((size_t)d.E * 2);
+  L.m.x_norm2 = b.take((size_t)d.E * 2);
+  if (kinds & kHasGdn) {
+    L.m.qkv_smooth = b.take((size_t)d.C * 2);
+    L.m.y_norm = b.take((size_t)d.Z * 2);
   }
   L.total = b.off;
   return L;
 }
-
-// Both kinds' intermediates in one map (they share the buffer; the phases that use
-// them never overlap).
-ScratchMap stack_map(const Dims& d) {
-  ScratchMap a = layout(d, QWEN35_LAYER_FULL_ATTENTION).m, b = layout(d, QWEN35_LAYER_LINEAR_ATTENTION).m;
-  a.dt_raw = b.dt_raw; a.b_raw = b.b_raw; a.qkv = b.qkv; a.z = b.z; a.y = b.y; a.out = b.out;
-  return a;
-}
+int kinds_of(int layer_kind) { return layer_kind == QWEN35_LAYER_FULL_ATTENTION ? kHasFa : kHasGdn; }
 
 QMat qm(const qwen35_qweight& w) {
   QMat m;
@@ -199,7 +213,13 @@ void fill_gdn(LayerDesc& L, const qwen35_gdn_layer* l, const qwen35_gdn_state* s
   L.ssm = st->gdn_state;
 }
 
-// The program header shared by every call; the caller fills the layers.
+// Debug settings of the next launches (qwen35_debug_*).
+unsigned long long g_wait_ns = kWaitNs;
+const uint32_t* g_wait_probe = nullptr;
+uint32_t g_dump = 0;
+
+// The program header shared by every call; the caller fills the scratch map and
+// the layers.
 Program* new_program(const qwen35_config* cfg, const Dims& d, void* scratch) {
   Program* p = new (std::nothrow) Program();
   if (!p) return nullptr;
@@ -210,9 +230,10 @@ Program* new_program(const qwen35_config* cfg, const Dims& d, void* scratch) {
   p->gdn_out_scale = d.Dk ? (float)(1.0 / std::sqrt((double)d.Dk)) : 0.f;
   p->l2_eps = 1e-6f;
   p->scratch = static_cast<uint8_t*>(scratch);
-  p->sm = stack_map(d);
   p->status = reinterpret_cast<int*>(scratch);
-  p->barrier = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(scratch) + 4);
+  p->wait_ns = g_wait_ns;
+  p->wait_probe = g_wait_probe;
+  p->dump = g_dump;
   p->batch = 1;
   p->seq_stride = 0;
   // inv_freq[i] = theta^(-2i/R), computed in double and kept as fp32
@@ -252,7 +273,8 @@ int fa_forward(const qwen35_config* cfg, const qwen35_fa_layer* layer, void* scr
   if ((r = check_fa_layer(layer, d))) return r;
   if (!kv || !aligned16(kv->k) || !aligned16(kv->v) || kv->capacity == 0) return QWEN35_ERR_INVALID_ARGUMENT;
   if (!aligned16(x_in) || !aligned16(x_out) || !aligned16(scratch)) return QWEN35_ERR_INVALID_ARGUMENT;
-  if (scratch_bytes < layout(d, QWEN35_LAYER_FULL_ATTENTION).total) return QWEN35_ERR_INVALID_ARGUMENT;
+  const Layout lay = layout(d, kHasFa);
+  if (scratch_bytes < lay.total) return QWEN35_ERR_INVALID_ARGUMENT;
   if (d_pos) {
     if (max_seq == 0) return QWEN35_ERR_INVALID_ARGUMENT;
   } else if (cache_pos >= kv->capacity || seq_len == 0 || seq_len > cache_pos + 1) {
@@ -261,6 +283,7 @@ int fa_forward(const qwen35_config* cfg, const qwen35_fa_layer* layer, void* scr
   if (num_sms() <= 0) return QWEN35_ERR_CUDA;
   Program* p = new_program(cfg, d, scratch);
   if (!p) return QWEN35_ERR_CUDA;
+  p->sm = lay.m;
   p->n_layers = 1;
   p->x_in = x_in;
   p->x_out = x_out;
@@ -282,10 +305,12 @@ int gdn_forward(const qwen35_config* cfg, const qwen35_gdn_layer* layer, void* s
   if ((r = check_gdn_layer(layer, d))) return r;
   if (!state || !aligned16(state->conv_state) || !aligned16(state->gdn_state)) return QWEN35_ERR_INVALID_ARGUMENT;
   if (!aligned16(x_in) || !aligned16(x_out) || !aligned16(scratch)) return QWEN35_ERR_INVALID_ARGUMENT;
-  if (scratch_bytes < layout(d, QWEN35_LAYER_LINEAR_ATTENTION).total) return QWEN35_ERR_INVALID_ARGUMENT;
+  const Layout lay = layout(d, kHasGdn);
+  if (scratch_bytes < lay.total) return QWEN35_ERR_INVALID_ARGUMENT;
   if (num_sms() <= 0) return QWEN35_ERR_CUDA;
   Program* p = new_program(cfg, d, scratch);
   if (!p) return QWEN35_ERR_CUDA;
+  p->sm = lay.m;
   p->n_layers = 1;
   p->x_in = x_in;
   p->x_out = x_out;
@@ -341,14 +366,16 @@ size_t qwen35_scratch_bytes(const qwen35_config* cfg, int kind) {
   } else {
     return 0;
   }
-  return layout(d, kind).total;
+  return layout(d, kinds_of(kind)).total;
 }
 
 size_t qwen35_stack_scratch_bytes(const qwen35_config* cfg) {
-  const size_t a = qwen35_scratch_bytes(cfg, QWEN35_LAYER_FULL_ATTENTION);
-  const size_t b = qwen35_scratch_bytes(cfg, QWEN35_LAYER_LINEAR_ATTENTION);
-  if (a == 0 || b == 0) return 0;
-  return a > b ? a : b;
+  if (qwen35_scratch_bytes(cfg, QWEN35_LAYER_FULL_ATTENTION) == 0 ||
+      qwen35_scratch_bytes(cfg, QWEN35_LAYER_LINEAR_ATTENTION) == 0)
+    return 0;
+  Dims d;
+  check_config(cfg, d);
+  return layout(d, kHasFa | kHasGdn).total;
 }
 
 int qwen35_scratch_init(void* scratch, size_t scratch_bytes, void* stream) {
@@ -385,24 +412,41 @@ int qwen35_forward_linear_attention(const qwen35_config* cfg, const qwen35_gdn_l
   return gdn_forward(cfg, layer, scratch, scratch_bytes, state, x_in, x_out, (cudaStream_t)stream);
 }
 
+namespace {
+// The device address of the static array on the current device, looked up once per
+// device (with that device current) and cached; null on failure.
+void* static_scratch() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  if (!g_static_scratch_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return nullptr;
+    g_static_scratch_ptr[dev] = p;
+  }
+  return g_static_scratch_ptr[dev];
+}
+}  // namespace
+
 int qwen35_forward_linear_attention_static(const qwen35_config* cfg, const qwen35_gdn_layer* layer,
                                            const qwen35_gdn_state* state, const qwen35_bf16* x_in,
                                            qwen35_bf16* x_out, void* stream) {
   const size_t need = qwen35_scratch_bytes(cfg, QWEN35_LAYER_LINEAR_ATTENTION);
   if (need == 0) return QWEN35_ERR_INVALID_ARGUMENT;
   if (need > QWEN35_STATIC_SCRATCH_BYTES) return QWEN35_ERR_UNSUPPORTED;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QWEN35_ERR_CUDA;
-  if (!g_static_scratch_ptr[dev]) {  // once per device, with that device current
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return QWEN35_ERR_CUDA;
-    g_static_scratch_ptr[dev] = p;
-  }
-  void* scratch = g_static_scratch_ptr[dev];
+  void* scratch = static_scratch();
+  if (!scratch) return QWEN35_ERR_CUDA;
   cudaStream_t st = (cudaStream_t)stream;
   // the array keeps the previous call's contents: the status word must start at zero
   if (cudaMemsetAsync(scratch, 0, 256, st) != cudaSuccess) return QWEN35_ERR_CUDA;
   return gdn_forward(cfg, layer, scratch, QWEN35_STATIC_SCRATCH_BYTES, state, x_in, x_out, st);
+}
+
+int qwen35_read_static_status(int32_t* host_status, void* stream) {
+  if (!host_status) return QWEN35_ERR_INVALID_ARGUMENT;
+  void* scratch = static_scratch();
+  if (!scratch) return QWEN35_ERR_CUDA;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return QWEN35_ERR_CUDA;
+  return cudaMemcpy(host_status, scratch, 4, cudaMemcpyDeviceToHost) == cudaSuccess ? QWEN35_OK : QWEN35_ERR_CUDA;
 }
 
 namespace {
@@ -410,12 +454,8 @@ namespace {
 // Scratch of one sequence's intermediates in a stack program (both layer kinds'
 // maps share it), and of a batch: the status word and barrier counter, then one
 // block per sequence.
-size_t stack_need(const Dims& d, bool has_fa, bool has_gdn) {
-  size_t need = 256;
-  if (has_fa) need = layout(d, QWEN35_LAYER_FULL_ATTENTION).total;
-  if (has_gdn && layout(d, QWEN35_LAYER_LINEAR_ATTENTION).total > need)
-    need = layout(d, QWEN35_LAYER_LINEAR_ATTENTION).total;
-  return need;
+Layout stack_layout(const Dims& d, bool has_fa, bool has_gdn) {
+  return layout(d, (has_fa ? kHasFa : 0) | (has_gdn ? kHasGdn : 0));
 }
 size_t batch_need(size_t one, uint32_t batch) { return 256 + (size_t)batch * (one - 256); }
 
@@ -446,11 +486,13 @@ int decode_step(const qwen35_config* cfg, const qwen35_layer* layers, uint32_t n
     }
   }
   if (!aligned16(x_in) || !aligned16(x_out) || !aligned16(scratch)) return QWEN35_ERR_INVALID_ARGUMENT;
-  const size_t one = stack_need(d, has_fa, has_gdn);
+  const Layout lay = stack_layout(d, has_fa, has_gdn);
+  const size_t one = lay.total;
   if (scratch_bytes < batch_need(one, batch)) return QWEN35_ERR_INVALID_ARGUMENT;
   if (num_sms() <= 0) return QWEN35_ERR_CUDA;
   Program* p = new_program(cfg, d, scratch);
   if (!p) return QWEN35_ERR_CUDA;
+  p->sm = lay.m;
   p->n_layers = num_layers;
   p->x_in = x_in;
   p->x_out = x_out;
@@ -486,7 +528,7 @@ int qwen35_decode_step_batched(const qwen35_config* cfg, const qwen35_layer* lay
 size_t qwen35_stack_scratch_bytes_batched(const qwen35_config* cfg, uint32_t batch) {
   Dims d;
   if (!cfg || batch == 0 || batch > (uint32_t)kMaxBatch || check_config(cfg, d) != QWEN35_OK) return 0;
-  return batch_need(stack_need(d, true, true), batch);
+  return batch_need(stack_layout(d, true, true).total, batch);
 }
 
 struct qwen35_graph {
@@ -556,26 +598,55 @@ int qwen35_graph_destroy(qwen35_graph* graph) {
   return QWEN35_OK;
 }
 
-size_t qwen35_debug_scratch_offset(const qwen35_config* cfg, int kind, const char* name) {
-  const size_t none = (size_t)-1;
-  if (!name || qwen35_scratch_bytes(cfg, kind) == 0) return none;
-  Dims d;
-  check_config(cfg, d);
-  const ScratchMap m = layout(d, kind).m;
+namespace {
+// A named intermediate's offset in map m; kind -1 accepts either kind's names.
+size_t named_offset(const ScratchMap& m, int kind, const char* name) {
   struct Named {
     const char* n;
     uint32_t off;
     int kind;
   };
   const int F = QWEN35_LAYER_FULL_ATTENTION, G = QWEN35_LAYER_LINEAR_ATTENTION;
-  const Named tab[] = {{"q_full", m.q_full, F}, {"k", m.k, F},         {"v", m.v, F},
-                       {"gated_attn", m.ga, F}, {"o", m.o, F},         {"dt_raw", m.dt_raw, G},
-                       {"b_raw", m.b_raw, G},   {"qkv", m.qkv, G},     {"z", m.z, G},
-                       {"y", m.y, G},           {"out", m.out, G},     {"x_resid", m.x_resid, -1},
-                       {"gate_act", m.g, -1},   {"up_act", m.u, -1}};
+  const Named tab[] = {{"q_full", m.q_full, F},    {"k", m.k, F},          {"v", m.v, F},
+                       {"gated_attn", m.ga, F},    {"o", m.o, F},          {"dt_raw", m.dt_raw, G},
+                       {"b_raw", m.b_raw, G},      {"qkv", m.qkv, G},      {"z", m.z, G},
+                       {"y", m.y, G},              {"out", m.out, G},      {"x_resid", m.x_resid, -1},
+                       {"gate_act", m.g, -1},      {"up_act", m.u, -1},    {"x_norm", m.x_norm, -1},
+                       {"x_norm2", m.x_norm2, -1}, {"qkv_smooth", m.qkv_smooth, G}, {"y_norm", m.y_norm, G}};
   for (const Named& e : tab)
-    if ((e.kind == kind || e.kind == -1) && std::strcmp(e.n, name) == 0) return e.off;
-  return none;
+    if ((kind == -1 || e.kind == kind || e.kind == -1) && std::strcmp(e.n, name) == 0) return e.off;
+  return (size_t)-1;
+}
+}  // namespace
+
+size_t qwen35_debug_scratch_offset(const qwen35_config* cfg, int kind, const char* name) {
+  if (!name || qwen35_scratch_bytes(cfg, kind) == 0) return (size_t)-1;
+  Dims d;
+  check_config(cfg, d);
+  return named_offset(layout(d, kinds_of(kind)).m, kind, name);
+}
+
+size_t qwen35_debug_stack_scratch_offset(const qwen35_config* cfg, const char* name) {
+  if (!name || qwen35_stack_scratch_bytes(cfg) == 0) return (size_t)-1;
+  Dims d;
+  check_config(cfg, d);
+  return named_offset(layout(d, kHasFa | kHasGdn).m, -1, name);
+}
+
+int qwen35_debug_stage_dump(int on) {
+  g_dump = on ? 1u : 0u;
+  return QWEN35_OK;
+}
+
+int qwen35_debug_set_wait_limit(unsigned long long limit_ns) {
+  g_wait_ns = limit_ns ? limit_ns : kWaitNs;
+  return QWEN35_OK;
+}
+
+int qwen35_debug_wait_probe(const uint32_t* d_flag) {
+  if (d_flag && ((uintptr_t)d_flag % 4)) return QWEN35_ERR_INVALID_ARGUMENT;
+  g_wait_probe = d_flag;
+  return QWEN35_OK;
 }
 
 int qwen35_gemv(const qwen35_qweight* w, const qwen35_bf16* x, qwen35_bf16* y, void* scratch, size_t scratch_bytes,

@@ -1,6 +1,7 @@
 // Device helpers shared by the sm_103a kernels: bf16 conversions, mbarriers,
-// bulk (TMA-engine) copies global -> shared, programmatic dependent launch, and
-// waits bounded in time that report through the device status word.
+// bulk (TMA-engine) copies global -> shared, programmatic dependent launch, the
+// tagged words through which CTAs hand each other their results, and waits
+// bounded in time that report through the device status word.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -11,7 +12,7 @@ namespace q35 {
 
 constexpr int kStatusTimeout = 5;  // QWEN35_ERR_DEVICE_TIMEOUT
 constexpr int kStatusRange = 6;    // QWEN35_ERR_DEVICE_RANGE
-constexpr uint64_t kWaitNs = 1000000000ull;  // a bounded wait gives up after 1 s
+constexpr uint64_t kWaitNs = 1000000000ull;  // a bounded wait gives up after 1 s (the default)
 
 __device__ __forceinline__ float bf16f(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
 __device__ __forceinline__ uint16_t to_bf16(float f) { return __bfloat16_as_ushort(__float2bfloat16_rn(f)); }
@@ -98,15 +99,99 @@ __device__ __forceinline__ uint64_t global_ns() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
-// Wait for the phase with the given parity to complete; false after kWaitNs.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// Wait for the phase with the given parity to complete; false after limit_ns.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   while (!mbar_try_wait(bar, parity)) {
-    if (global_ns() - t0 > kWaitNs) return false;
+    if (global_ns() - t0 > limit_ns) return false;
   }
   return true;
 }
+
+// ---------------------------------------------------------------- tagged words
+//
+// A result that other CTAs read travels as 32-bit words, the bf16 value in the
+// high half and the writing phase's tag in the low half, stored and loaded at GPU
+// scope without going through L1 (a relaxed access: each 32-bit word is read or
+// written whole). A reader polls the words themselves until every tag is the one
+// it expects, so a result is usable one L2 round trip after it is stored; the
+// words are zeroed before each launch, and tags are never zero.
+__device__ __forceinline__ uint32_t tag_word(float v, uint32_t tag) { return ((uint32_t)to_bf16(v) << 16) | tag; }
+__device__ __forceinline__ uint32_t tag_word_bits(uint16_t b, uint32_t tag) { return ((uint32_t)b << 16) | tag; }
+__device__ __forceinline__ float tag_value(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ bool tag_is(uint32_t w, uint32_t tag) { return (w & 0xFFFFu) == tag; }
+__device__ __forceinline__ uint4 ld_tagged4(const uint32_t* p) {
+  uint4 r;
+  asm volatile("ld.relaxed.gpu.global.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p)
+               : "memory");
+  return r;
+}
+__device__ __forceinline__ uint32_t ld_tagged(const uint32_t* p) {
+  uint32_t r;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(r) : "l"(p) : "memory");
+  return r;
+}
+__device__ __forceinline__ void st_tagged(uint32_t* p, uint32_t w) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(w) : "memory");
+}
+__device__ __forceinline__ void st_tagged4(uint32_t* p, uint4 w) {
+  asm volatile("st.relaxed.gpu.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(w.x), "r"(w.y), "r"(w.z),
+               "r"(w.w)
+               : "memory");
+}
+__device__ __forceinline__ bool tags4_are(const uint4 w, uint32_t tag) {
+  return tag_is(w.x, tag) & tag_is(w.y, tag) & tag_is(w.z, tag) & tag_is(w.w, tag);
+}
+// A timeout already recorded in the status word: later waits give up at once
+// (the launch's results are meaningless anyway), so that a launch whose waits run
+// out ends after about one wait limit, not one per wait.
+__device__ __forceinline__ bool timed_out(const int* status) {
+  int v;
+  asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(status) : "memory");
+  return v == kStatusTimeout;
+}
+// Load 4 tagged words and poll them until all carry `tag` (bounded); false (and
+// whatever was last read) when the wait runs out.
+__device__ __forceinline__ bool ld_tagged4_wait(const uint32_t* p, uint32_t tag, uint4& w, uint64_t limit_ns,
+                                                const int* status) {
+  w = ld_tagged4(p);
+  if (tags4_are(w, tag)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t n = 1;; ++n) {
+    __nanosleep(64);
+    w = ld_tagged4(p);
+    if (tags4_are(w, tag)) return true;
+    if (global_ns() - t0 > limit_ns || ((n & 15) == 0 && timed_out(status))) return false;
+  }
+}
+__device__ __forceinline__ bool ld_tagged_wait(const uint32_t* p, uint32_t tag, uint32_t& w, uint64_t limit_ns,
+                                               const int* status) {
+  w = ld_tagged(p);
+  if (tag_is(w, tag)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t n = 1;; ++n) {
+    __nanosleep(64);
+    w = ld_tagged(p);
+    if (tag_is(w, tag)) return true;
+    if (global_ns() - t0 > limit_ns || ((n & 15) == 0 && timed_out(status))) return false;
+  }
+}
+// Acquire load / release store at GPU scope (a flag that publishes other data).
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
+  uint32_t r;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(r) : "l"(p) : "memory");
+  return r;
+}
+__device__ __forceinline__ void st_release(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Orders this thread's earlier memory accesses before its later ones at GPU scope
+// (both ways): placed after a phase has read its inputs and before it writes, it
+// makes the hand-over of tagged words a synchronisation.
+__device__ __forceinline__ void fence_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
 // ---------------------------------------------------------------- bulk copies
 

@@ -19,8 +19,9 @@
 // copies into a byte-addressed shared-memory ring, never waiting for a phase
 // boundary: weights and old cache rows do not depend on the phases before them.
 // It also stages each linear-attention layer's state block and conv inputs while
-// that layer's input projection streams. Consumers run the phases in order with
-// a grid barrier between dependent phases.
+// that layer's input projection streams. Consumers run the phases in order; a
+// phase's results reach the other CTAs as tagged words that the next phase polls
+// (no grid barrier, see "hand-over between CTAs" below).
 //
 // Phase functions are kept out of line (one call per phase) and read the
 // program header, the current layer and the current GEMV from static shared
@@ -40,6 +41,7 @@
 // terms ~128x larger than the result when b is close to -128 s). Each tile's row
 // is reduced across its warp into shared partial sums; one epilogue per phase
 // stores the rows.
+#include <algorithm>
 #include <cstddef>
 
 #include <cuda_fp16.h>
@@ -107,10 +109,20 @@ __device__ __forceinline__ void consumer_sync() { named_barrier(1, NCT); }
 // launch starts) and the current layer's description.
 constexpr uint32_t kHeadBytes = (offsetof(Program, layers) + 3) / 4 * 4;
 static_assert(offsetof(Program, layers) % 8 == 0, "layer table alignment");
+static_assert(sizeof(Program) <= 32764, "kernel parameter block");
 __shared__ __align__(16) uint8_t s_head[kHeadBytes];
-__shared__ LayerDesc s_layer;
-__shared__ LayerDesc s_layer0;  // the current layer as the program gives it (sequence 0's caches)
+// The descriptions the consumers work from, double-buffered so that the helper
+// warp forms the next phase's while the consumers run the current one:
+// the layer by layer parity (as the program gives it, s_lay0, and rebased to the
+// current sequence of a batch, s_lay), the GEMV by phase parity (s_gv, below).
+// s_sel: bit 0 the current phase's buffer, bit 1 the current layer's.
+__shared__ LayerDesc s_lay[2];
+__shared__ LayerDesc s_lay0[2];
+__shared__ uint32_t s_sel;
+__shared__ uint32_t s_dead_cta;  // a consumer wait on the helper ran out: no more ring reads
 __device__ __forceinline__ const Program& prog() { return *reinterpret_cast<const Program*>(s_head); }
+__device__ __forceinline__ LayerDesc& cur_layer() { return s_lay[(s_sel >> 1) & 1]; }
+__device__ __forceinline__ LayerDesc& cur_layer0() { return s_lay0[(s_sel >> 1) & 1]; }
 __device__ __forceinline__ Smem smem_map(uint8_t* base) { return smem_map(base, prog().ring_bytes); }
 
 // The sequence the consumers are working on (a batch runs each phase for its
@@ -144,39 +156,143 @@ __device__ __forceinline__ void seq_caches(const Program& P, LayerDesc& L, uint3
 // phase of the launch sees the same value although CTA 0 advances it at the end)
 __device__ __forceinline__ int32_t launch_pos(uint32_t b) { return s_pos[b]; }
 
-// ------------------------------------------------------------------ grid barrier
+// ------------------------------------------------------------------ hand-over between CTAs
+//
+// No grid barrier separates the phases. A phase's results that other CTAs read are
+// tagged words (common.cuh): each reader polls the words it needs until they carry
+// the tag of the phase that writes them, so it starts as soon as its own inputs
+// are in, one L2 round trip after they are stored. Every phase of a layer reads
+// results of all CTAs of the phase before it (the full input vector of a
+// projection, the partials of every split, every q-head's rows), so no CTA can be
+// more than one phase ahead of another, and a buffer is rewritten only after every
+// CTA has finished reading its previous contents: each phase's outputs are computed
+// from the values its loads return, so those loads have completed before any of its
+// stores is issued (no fence is needed for that order; one measured 0.4 us per
+// phase). Tags are the launch's phase index + 1.
 
-// All CTAs' consumers: arrive on a counter that starts at zero for the launch and
-// wait until it reaches `target` (G per barrier passed). Bounded to 1 s; on expiry
-// the status word records a timeout and the CTA continues (its results are then
-// meaningless, but nothing hangs).
-// The grid barrier in two halves, run by lane 0 of the last consumer warp (a warp
-// that issues none of the loads placed between the halves). Arrival is a release
-// add after the consumers' own barrier; it waits for that thread's earlier memory
-// operations, so loads that do not depend on the other CTAs go between the halves.
-constexpr uint32_t kBarThread = (NCW - 1) * 32;
-__device__ __forceinline__ void grid_arrive(const Program& P) {
-  consumer_sync();
-  if (threadIdx.x == kBarThread) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(P.barrier) : "memory");
+// The launch's limit for bounded waits (ns).
+__device__ __forceinline__ uint64_t wait_limit() { return prog().wait_ns; }
+// The limit for the producer's final drain of its copies in flight: at least the
+// default, so that no copy into shared memory outlives the CTA.
+__device__ __forceinline__ uint64_t drain_limit() { return prog().wait_ns > kWaitNs ? prog().wait_ns : kWaitNs; }
+
+__device__ __forceinline__ uint32_t phase_tag(uint32_t ph) { return ph + 1u; }
+
+// Poll N groups of 4 tagged words, w[i] loaded from p[i] and expected to carry
+// tag t[i] (t[i] == 0: nothing to poll), until every group carries its tag. Each
+// round re-loads all the groups still missing together, so a round costs one L2
+// round trip however many are missing. False when the wait runs out.
+template <int N>
+__device__ __forceinline__ bool settle4(const uint32_t* const (&p)[N], const uint32_t (&t)[N], uint4 (&w)[N]) {
+  uint32_t todo = 0;
+#pragma unroll
+  for (int i = 0; i < N; ++i)
+    if (t[i] && !tags4_are(w[i], t[i])) todo |= 1u << i;
+  if (!todo) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t n = 1;; ++n) {
+    __nanosleep(64);
+#pragma unroll
+    for (int i = 0; i < N; ++i)
+      if ((todo >> i) & 1u) w[i] = ld_tagged4(p[i]);
+#pragma unroll
+    for (int i = 0; i < N; ++i)
+      if (((todo >> i) & 1u) && tags4_are(w[i], t[i])) todo &= ~(1u << i);
+    if (!todo) return true;
+    if (global_ns() - t0 > wait_limit() || ((n & 15) == 0 && timed_out(prog().status))) return false;
+  }
 }
-__device__ __forceinline__ void grid_wait(const Program& P, uint32_t target) {
-  if (threadIdx.x == kBarThread) {
-    uint32_t v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(P.barrier) : "memory");
-    if (v < target) {
-      // back-to-back polls (each is an L2 round trip); the clock is read every 8th
-      const uint64_t t0 = global_ns();
-      for (uint32_t n = 1;; ++n) {
-        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(P.barrier) : "memory");
-        if (v >= target) break;
-        if ((n & 7) == 0 && global_ns() - t0 > kWaitNs) {
-          set_status(P.status, kStatusTimeout);
-          break;
-        }
-      }
+// The same for N single tagged words.
+template <int N>
+__device__ __forceinline__ bool settle1(const uint32_t* const (&p)[N], const uint32_t (&t)[N], uint32_t (&w)[N]) {
+  uint32_t todo = 0;
+#pragma unroll
+  for (int i = 0; i < N; ++i)
+    if (t[i] && !tag_is(w[i], t[i])) todo |= 1u << i;
+  if (!todo) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t n = 1;; ++n) {
+    __nanosleep(64);
+#pragma unroll
+    for (int i = 0; i < N; ++i)
+      if ((todo >> i) & 1u) w[i] = ld_tagged(p[i]);
+#pragma unroll
+    for (int i = 0; i < N; ++i)
+      if (((todo >> i) & 1u) && tag_is(w[i], t[i])) todo &= ~(1u << i);
+    if (!todo) return true;
+    if (global_ns() - t0 > wait_limit() || ((n & 15) == 0 && timed_out(prog().status))) return false;
+  }
+}
+
+// 16 input values of a chunk: tagged words (4 x uint4) or, for the caller's own
+// bf16 vectors (tag 0), 16 bf16 (2 x uint4). Issue, settle (settle4 over the
+// chunks' groups), then read out.
+struct Chunk16 {
+  uint4 w[4];
+};
+__device__ __forceinline__ void chunk_issue(const void* base, uint32_t tag, uint32_t c, Chunk16& ch) {
+  if (tag) {
+    const uint32_t* p = static_cast<const uint32_t*>(base) + (size_t)c * 16;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) ch.w[k] = ld_tagged4(p + 4 * k);
+  } else {
+    const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(base) + (size_t)c * 16);
+    ch.w[0] = p[0];
+    ch.w[1] = p[1];
+    ch.w[2] = ch.w[3] = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+// The poll list entries of chunk c (tag 0 or inactive: none), at index i0..i0+3.
+template <int N>
+__device__ __forceinline__ void chunk_pend(const void* base, uint32_t tag, uint32_t c, bool active,
+                                           const uint32_t* (&p)[N], uint32_t (&t)[N], int i0) {
+  const uint32_t* q = static_cast<const uint32_t*>(base) + (size_t)c * 16;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    p[i0 + k] = q + 4 * k;
+    t[i0 + k] = active ? tag : 0u;
+  }
+}
+__device__ __forceinline__ void chunk_values(const Chunk16& ch, uint32_t tag, float* x) {
+  if (tag) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      x[4 * k] = tag_value(ch.w[k].x);
+      x[4 * k + 1] = tag_value(ch.w[k].y);
+      x[4 * k + 2] = tag_value(ch.w[k].z);
+      x[4 * k + 3] = tag_value(ch.w[k].w);
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const uint4 u = ch.w[k];
+      x[8 * k] = bf16lo(u.x); x[8 * k + 1] = bf16hi(u.x);
+      x[8 * k + 2] = bf16lo(u.y); x[8 * k + 3] = bf16hi(u.y);
+      x[8 * k + 4] = bf16lo(u.z); x[8 * k + 5] = bf16hi(u.z);
+      x[8 * k + 6] = bf16lo(u.w); x[8 * k + 7] = bf16hi(u.w);
     }
   }
-  consumer_sync();
+}
+// One tagged value (polled); records a timeout in the status word.
+__device__ __forceinline__ float tagged_value(const uint32_t* p, uint32_t tag) {
+  uint32_t w;
+  if (!ld_tagged_wait(p, tag, w, wait_limit(), prog().status)) set_status(prog().status, kStatusTimeout);
+  return tag_value(w);
+}
+// Store 16 values of a chunk as tagged words (already rounded to bf16 or not).
+__device__ __forceinline__ void chunk_store_tagged(uint32_t* dst, const float* v, uint32_t tag) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    st_tagged4(dst + 4 * k, make_uint4(tag_word(v[4 * k], tag), tag_word(v[4 * k + 1], tag),
+                                       tag_word(v[4 * k + 2], tag), tag_word(v[4 * k + 3], tag)));
+}
+__device__ __forceinline__ void chunk_store_bf16(uint16_t* dst, const float* v) {
+  uint32_t pk[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) pk[j] = (uint32_t)to_bf16(v[2 * j]) | ((uint32_t)to_bf16(v[2 * j + 1]) << 16);
+  uint4* d = reinterpret_cast<uint4*>(dst);
+  d[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  d[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
 }
 
 // ------------------------------------------------------------------ bf16 helpers
@@ -347,13 +463,22 @@ __host__ __device__ inline uint32_t batch_teams(uint32_t span, uint32_t ntiles, 
 
 struct Gemv {
   QMat seg[4];
-  uint16_t* out[4];
+  uint8_t* out[4];   // each segment's output: tagged words, or bf16 (out_tag 0)
   uint32_t row0[5];  // prefix sums of the segments' rows
   uint32_t nseg, K;
   int pro, epi;
-  const uint16_t *a, *b, *nw;
-  uint16_t* resid_out;
-  const uint16_t* resid_in;
+  // inputs: tagged words expected to carry tag_a / tag_b / tag_r, or the caller's
+  // bf16 vectors when the tag is 0 (a, b, resid_in); nw: norm weights (bf16)
+  const void *a, *b, *resid_in;
+  uint32_t tag_a, tag_b, tag_r;
+  const uint16_t* nw;
+  uint32_t* resid_out;  // x_resid (tagged, written by CTA 0 with tag out_tag)
+  uint32_t out_tag;     // tag of the outputs; 0: bf16 into the caller's vector
+  uint16_t* dump;       // debug: CTA 0 stores the formed input here (bf16), or null
+  // the gate|up phase of a linear-attention layer also shifts the q/k channels' conv
+  // state (of sequence 0; a batch's others follow at C * Kc strides), qkv tagged conv_tag
+  float* conv_shift;
+  uint32_t conv_tag;
   uint32_t head_dim;
   uint32_t W, cpl, R, gstride, scale_off, bias_off;
   uint32_t rb, re, ntiles;  // this CTA's rows [rb, re) and its tile count
@@ -363,126 +488,246 @@ struct Gemv {
   uint32_t bs, npass, T;  // T: teams of warps per CTA (a batch)
 };
 
-__shared__ Gemv s_gemv;  // the current GEMV phase (written by thread 0 inside the barrier)
+__shared__ Gemv s_gv[2];  // GEMV descriptions by phase parity
+__device__ __forceinline__ Gemv& cur_gemv() { return s_gv[s_sel & 1]; }
 // Per ring slot: where a GEMV tile's first row is stored, as an element offset
 // from the phase's first output (a phase's outputs are consecutive buffers of one
 // scratch block in segment order, or a single output), written by the producer with
 // the tile's other words; the row loop stores whole rows without a segment lookup.
 __shared__ uint32_t s_tout[kDecSlots];
 
-__device__ __forceinline__ void gemv_add(Gemv& g, const QMat& m, uint16_t* out, uint32_t stride) {
+__device__ __forceinline__ uint32_t out_esz(const Gemv& g) { return g.out_tag ? 4u : 2u; }
+
+__device__ __forceinline__ void gemv_add(Gemv& g, const QMat& m, void* out, uint32_t stride) {
   g.seg[g.nseg] = m;
-  g.out[g.nseg] = out;
+  g.out[g.nseg] = static_cast<uint8_t*>(out);
   g.sout[g.nseg] = stride;
   g.row0[g.nseg + 1] = g.row0[g.nseg] + m.n;
   ++g.nseg;
 }
 
+// Store output element i of segment sg (sequence b of a batch) as a tagged word or
+// as bf16.
+__device__ __forceinline__ void gemv_store(const Gemv& g, uint32_t sg, size_t i, float y) {
+  if (g.out_tag) st_tagged(reinterpret_cast<uint32_t*>(g.out[sg]) + i, tag_word(y, g.out_tag));
+  else reinterpret_cast<uint16_t*>(g.out[sg])[i] = to_bf16(y);
+}
+
 // The GEMV of phase p of layer l, written into g (shared memory: a returned struct
-// would go through local memory).
-__device__ __noinline__ void gemv_of(const Program& P, const LayerDesc& L, uint32_t l, int p, uint32_t sq, Gemv& g) {
+// would go through local memory). ph0 is the launch's phase index of the layer's
+// phase 0 (for the tags); the last layer's down projection writes the caller's
+// x_out, the others a stack's internal output vector. The program's shape table
+// holds the split computed on the host, so this runs in a few hundred cycles on
+// the thread that fills it.
+__device__ __noinline__ void gemv_of(const Program& P, const LayerDesc& L, uint32_t l, int p, uint32_t sq,
+                                     uint32_t ph0, Gemv& g) {
   g.nseg = 0;
   g.row0[0] = 0;
   g.b = nullptr;
+  g.resid_in = nullptr;
   g.nw = nullptr;
   g.resid_out = nullptr;
-  g.resid_in = nullptr;
+  g.dump = nullptr;
   g.head_dim = 0;
   g.epi = 0;
+  g.tag_a = g.tag_b = g.tag_r = 0;
+  g.conv_shift = nullptr;
+  g.conv_tag = 0;
   g.sa = g.sb = g.sres_in = g.sres_out = 0;
   uint8_t* S = seq_scratch(P, sq);
   const ScratchMap& m = P.sm;
   const uint16_t* x_in = P.x_in + (size_t)sq * P.E;
   uint16_t* x_out = P.x_out + (size_t)sq * P.E;
-  const uint16_t* xin = l == 0 ? x_in : x_out;
-  auto at = [&](uint32_t off) { return reinterpret_cast<uint16_t*>(S + off); };
-  const uint32_t SS = P.seq_stride / 2, SX = P.E;  // per-sequence strides: scratch, vectors
+  auto tw = [&](uint32_t off) { return reinterpret_cast<uint32_t*>(S + off); };  // tagged words
+  auto dmp = [&](uint32_t off) { return P.dump && blockIdx.x == 0 ? reinterpret_cast<uint16_t*>(S + off) : nullptr; };
+  const uint32_t SS = P.seq_stride / 4, SX = P.E;  // per-sequence strides: scratch words, vectors
   const bool fa = L.kind == kLayerFA;
   const int mlp0 = fa ? 4 : 3;  // the gate|up phase
+  const uint32_t tag_out = phase_tag(ph0 + p);
+  // the layer's input: the caller's vector for layer 0, else the last layer's output
+  const void* xin = l == 0 ? static_cast<const void*>(x_in) : static_cast<const void*>(tw(m.xa));
+  const uint32_t tag_xin = l == 0 ? 0u : phase_tag(ph0 - 1);
+  const uint32_t sxin = l == 0 ? SX : SS;
+  g.out_tag = tag_out;
   if (L.kind == kLayerGemv || L.kind == kLayerHead) {
     g.K = P.E;
     g.pro = L.kind == kLayerHead ? kRms : kPlain;
     g.a = x_in;
     g.sa = SX;
     g.nw = L.input_ln;
+    g.out_tag = 0;
     gemv_add(g, L.m[0], x_out, SX);
   } else if (p == 0) {
     g.K = P.E;
     g.pro = kRms;
     g.a = xin;
-    g.sa = SX;
+    g.tag_a = tag_xin;
+    g.sa = sxin;
     g.nw = L.input_ln;
+    g.dump = dmp(m.x_norm);
     if (fa) {
-      gemv_add(g, L.m[0], at(m.q_full), SS);
-      gemv_add(g, L.m[1], at(m.k), SS);
-      gemv_add(g, L.m[2], at(m.v), SS);
+      gemv_add(g, L.m[0], tw(m.q_full), SS);
+      gemv_add(g, L.m[1], tw(m.k), SS);
+      gemv_add(g, L.m[2], tw(m.v), SS);
     } else {
-      gemv_add(g, L.m[0], at(m.dt_raw), SS);
-      gemv_add(g, L.m[1], at(m.b_raw), SS);
-      gemv_add(g, L.m[2], at(m.qkv), SS);
-      gemv_add(g, L.m[3], at(m.z), SS);
+      gemv_add(g, L.m[0], tw(m.dt_raw), SS);
+      gemv_add(g, L.m[1], tw(m.b_raw), SS);
+      gemv_add(g, L.m[2], tw(m.qkv), SS);
+      gemv_add(g, L.m[3], tw(m.z), SS);
     }
   } else if (p == mlp0) {
     g.K = P.E;
     g.pro = kAddRms;
     g.a = xin;
-    g.sa = SX;
-    g.b = at(fa ? m.o : m.out);
+    g.tag_a = tag_xin;
+    g.sa = sxin;
+    g.b = tw(fa ? m.o : m.out);
+    g.tag_b = phase_tag(ph0 + p - 1);
     g.sb = SS;
     g.nw = L.post_ln;
-    g.resid_out = at(m.x_resid);
+    g.resid_out = tw(m.x_resid);
     g.sres_out = SS;
-    gemv_add(g, L.m[4], at(m.g), SS);
-    gemv_add(g, L.m[5], at(m.u), SS);
+    g.dump = dmp(m.x_norm2);
+    if (!fa) {  // the q/k conv state: every linear-attention CTA has read it two phases back
+      g.conv_shift = L.conv_state;
+      g.conv_tag = phase_tag(ph0);
+    }
+    gemv_add(g, L.m[4], tw(m.g), SS);
+    gemv_add(g, L.m[5], tw(m.u), SS);
   } else if (p == mlp0 + 1) {
     g.K = P.I;
     g.pro = kSiluMul;
     g.epi = 1;
-    g.a = at(m.g);
+    g.a = tw(m.g);
+    g.tag_a = phase_tag(ph0 + p - 1);
     g.sa = SS;
-    g.b = at(m.u);
+    g.b = tw(m.u);
+    g.tag_b = g.tag_a;
     g.sb = SS;
-    g.resid_in = at(m.x_resid);
+    g.resid_in = tw(m.x_resid);
+    g.tag_r = g.tag_a;
     g.sres_in = SS;
-    gemv_add(g, L.m[6], x_out, SX);
+    if (l + 1 == P.n_layers) {
+      g.out_tag = 0;
+      gemv_add(g, L.m[6], x_out, SX);
+    } else {
+      gemv_add(g, L.m[6], tw(m.xa), SS);
+    }
   } else if (fa) {  // p == 3: o_proj
     g.K = P.H * P.D;
     g.pro = kPlain;
-    g.a = at(m.ga);
+    g.a = tw(m.ga);
+    g.tag_a = phase_tag(ph0 + 2);
     g.sa = SS;
-    gemv_add(g, L.m[3], at(m.o), SS);
+    gemv_add(g, L.m[3], tw(m.o), SS);
   } else {  // p == 2: out_proj on silu(z) * RMSNorm_head(y)
     g.K = P.Z;
     g.pro = kHeadNormSilu;
-    g.a = at(m.y);
+    g.a = tw(m.y);
+    g.tag_a = phase_tag(ph0 + 1);
     g.sa = SS;
-    g.b = at(m.z);
+    g.b = tw(m.z);
+    g.tag_b = phase_tag(ph0);
     g.sb = SS;
     g.nw = L.norm_weight;
     g.head_dim = P.Dv;
-    gemv_add(g, L.m[7], at(m.out), SS);
+    g.dump = dmp(m.y_norm);
+    gemv_add(g, L.m[7], tw(m.out), SS);
   }
-  pick_split(g.K / 16, g.W, g.cpl);
-  g.R = NCW / g.W;
-  if (P.batch > 1) g.R = batch_rows(g.K);  // tensor-core tiles
+  const GemvShape sh = P.shapes[L.kind < kShapeKinds ? L.kind : 0][p];
+  g.W = sh.W;
+  g.cpl = sh.cpl;
+  g.R = sh.R;
   g.gstride = ((g.K / 64 + 7) / 8) * 8;
   g.scale_off = (g.R * g.K + 15) / 16 * 16;
   g.bias_off = g.scale_off + g.R * g.gstride * 2;
-  // a balanced contiguous range of rows per CTA, cut into R-row tiles per segment
+  g.bs = sh.bs;
+  g.npass = sh.npass;
+  // a balanced contiguous range of rows per CTA (rows < 2^24, CTAs < 2^8: 32-bit
+  // products), cut into R-row tiles per segment
   const uint32_t total = g.row0[g.nseg];
-  g.rb = (uint32_t)(((uint64_t)total * blockIdx.x) / gridDim.x);
-  g.re = (uint32_t)(((uint64_t)total * (blockIdx.x + 1)) / gridDim.x);
+  g.rb = total * blockIdx.x / gridDim.x;
+  g.re = total * (blockIdx.x + 1) / gridDim.x;
   g.ntiles = 0;
   for (uint32_t sg = 0; sg < g.nseg; ++sg) {
     const uint32_t lo = max(g.rb, g.row0[sg]), hi = min(g.re, g.row0[sg + 1]);
     if (hi > lo) g.ntiles += (hi - lo + g.R - 1) / g.R;
   }
-  // a batch: as many sequences per pass over the weights as their staged inputs
-  // fit in the phase buffer beside the teams' partial sums
-  g.bs = P.batch > 1 ? min(P.batch, (P.union_bytes - kBatchPart) / batch_seq_bytes(g.K)) : 1u;
-  g.npass = (P.batch + g.bs - 1) / g.bs;
   g.T = P.batch > 1 ? batch_teams(g.bias_off + g.R * g.gstride * 2, g.ntiles, P.ring_bytes) : 1u;
 }
+
+// The shape-only part of every GEMV phase of the program (host).
+void fill_shapes(Program& P) {
+  for (int kind = 0; kind < kShapeKinds; ++kind)
+    for (int p = 0; p < kShapePhases; ++p) {
+      uint32_t K = 0;
+      if (kind == kLayerFA) K = p == 0 || p == 4 ? P.E : p == 3 ? P.H * P.D : p == 5 ? P.I : 0;
+      else if (kind == kLayerGDN) K = p == 0 || p == 3 ? P.E : p == 2 ? P.Z : p == 4 ? P.I : 0;
+      else K = p == 0 ? P.E : 0;
+      GemvShape& sh = P.shapes[kind][p];
+      sh = GemvShape{};
+      if (K == 0 || K % 64) continue;
+      uint32_t W = 0, cpl = 0;
+      pick_split(K / 16, W, cpl);
+      if (W == 0) continue;
+      const uint32_t R = P.batch > 1 ? batch_rows(K) : NCW / W;  // a batch: tensor-core tiles
+      // a batch: as many sequences per pass over the weights as their staged inputs
+      // fit in the phase buffer beside the teams' partial sums
+      uint32_t bs = P.batch > 1 ? std::min(P.batch, (P.union_bytes - kBatchPart) / batch_seq_bytes(K)) : 1u;
+      if (bs == 0) bs = 1;
+      sh.W = (uint8_t)W;
+      sh.cpl = (uint8_t)cpl;
+      sh.R = (uint8_t)R;
+      sh.bs = (uint8_t)bs;
+      sh.npass = (uint8_t)((P.batch + bs - 1) / bs);
+    }
+}
+
+// ------------------------------------------------------------------ phase descriptions
+
+// Where the consumers are and what the helper warp has prepared: `entered` = the
+// launch phase index the consumers are in + 1 (written by consumer thread 0 at the
+// phase's entry), `prepped` = the phases whose descriptions are formed (the helper
+// forms phase ph + 1's while the consumers run phase ph); the program's layer
+// table (parameter space).
+struct PhaseState {
+  const LayerDesc* layers;
+  uint32_t entered, prepped;
+};
+__shared__ PhaseState s_ph;
+
+__device__ __forceinline__ uint32_t ld_volatile_shared(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.volatile.shared.u32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_volatile_shared(uint32_t* p, uint32_t v) {
+  asm volatile("st.volatile.shared.u32 [%0], %1;" ::"r"(smem_addr(p)), "r"(v) : "memory");
+}
+
+// One warp: the descriptions of phase p of layer l (launch phase ph; the layer's
+// first phase ph0) into the buffers of their parity: the layer's (copied from the
+// parameter block at its first phase) and the GEMV's.
+__device__ __noinline__ void form_phase(uint32_t l, uint32_t p, uint32_t ph, uint32_t ph0) {
+  const Program& P = prog();
+  const uint32_t lane = threadIdx.x & 31;
+  if (p == 0) {  // a few words per lane
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(&s_ph.layers[l]);
+    uint32_t* d0 = reinterpret_cast<uint32_t*>(&s_lay0[l & 1]);
+    uint32_t* d1 = reinterpret_cast<uint32_t*>(&s_lay[l & 1]);
+    for (uint32_t i = lane; i < sizeof(LayerDesc) / 4; i += 32) {
+      const uint32_t v = src[i];
+      d0[i] = v;
+      d1[i] = v;
+    }
+    __syncwarp();
+  }
+  if (lane == 0 && phase_type(s_lay0[l & 1].kind, p) == kPhGemv) gemv_of(P, s_lay0[l & 1], l, p, 0, ph0, s_gv[ph & 1]);
+  __syncwarp();
+}
+
+// Forward declaration (defined with the linear-attention phase).
+__device__ __noinline__ void conv_shift_qk(float* conv_state, const uint8_t* scratch, uint32_t tag);
 
 // The CTA's partial row sums of a GEMV phase ([W][rows], one slice per K-part of
 // a row) and, for the down projection, its residual rows ([rows]): shared memory
@@ -493,9 +738,11 @@ __device__ __forceinline__ float* gemv_partials(const Smem& sh, uint32_t nch) {
 
 // Form the phase's input vector once per CTA and store it, quantised, in shared
 // memory: chunk c at hi[c], lo[c] (uint4 each) and aux[c] = {qsum128, scale, sum x}.
+// The inputs are polled until every word carries its expected tag; one fence
+// then orders the phase's reads before its writes (the hand-over above).
 __device__ __noinline__ void gemv_prologue(unsigned long long* tr) {
   const Program& P = prog();
-  const Gemv& g = s_gemv;
+  const Gemv& g = cur_gemv();
   const Smem sh = smem_map(smem_raw);
   const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t nch = g.K / 16;
@@ -505,21 +752,18 @@ __device__ __noinline__ void gemv_prologue(unsigned long long* tr) {
   const bool has_b = g.pro == kAddRms || g.pro == kSiluMul || g.pro == kHeadNormSilu;
   const bool has_w = g.pro == kAddRms || g.pro == kRms || g.pro == kHeadNormSilu;
   // every global load of the prologue is issued before any is used: one round trip
-  uint4 pa[2][2], pb[2][2], pw[2][2];
+  Chunk16 ca[2], cb[2];
+  uint4 pw[2][2];
 #pragma unroll
   for (int q = 0; q < 2; ++q) {
     const uint32_t c = tid + q * NCT;
     const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-    pa[q][0] = pa[q][1] = pb[q][0] = pb[q][1] = pw[q][0] = pw[q][1] = z;
+    ca[q].w[0] = ca[q].w[1] = ca[q].w[2] = ca[q].w[3] = z;
+    cb[q] = ca[q];
+    pw[q][0] = pw[q][1] = z;
     if (c < nch) {
-      const uint4* ap = reinterpret_cast<const uint4*>(g.a + c * 16);
-      pa[q][0] = ap[0];
-      pa[q][1] = ap[1];
-      if (has_b) {
-        const uint4* bp = reinterpret_cast<const uint4*>(g.b + c * 16);
-        pb[q][0] = bp[0];
-        pb[q][1] = bp[1];
-      }
+      chunk_issue(g.a, g.tag_a, c, ca[q]);
+      if (has_b) chunk_issue(g.b, g.tag_b, c, cb[q]);
       if (has_w) {
         const uint32_t wi = g.pro == kHeadNormSilu ? (c * 16) % g.head_dim : c * 16;
         const uint4* wp = reinterpret_cast<const uint4*>(g.nw + wi);
@@ -528,33 +772,59 @@ __device__ __noinline__ void gemv_prologue(unsigned long long* tr) {
       }
     }
   }
-  if (g.epi == 1) {  // the down projection's residual rows, for the epilogue
-    const uint32_t rb = g.rb, rows = g.re - g.rb;
-    float* resid = gemv_partials(sh, nch) + g.W * rows;
-    for (uint32_t i = tid; i < rows; i += NCT) resid[i] = bf16f(g.resid_in[rb + i]);
+  if (tr && tid == 0) tr[15] = global_ns();  // loads issued
+  // the down projection's residual rows (at most one per thread), for the epilogue:
+  // loaded in the same round
+  const uint32_t rrows = g.re - g.rb;
+  const bool has_r = g.epi == 1 && tid < rrows;
+  const uint32_t* rin = static_cast<const uint32_t*>(g.resid_in) + g.rb + tid;
+  uint32_t rw = has_r ? ld_tagged(rin) : 0u;
+  bool ok;
+  {  // the tagged inputs not there yet, polled together
+    const uint32_t* pp[16];
+    uint32_t pt[16];
+    uint4 pw4[16];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const uint32_t c = tid + q * NCT;
+      chunk_pend(g.a, g.tag_a, c < nch ? c : 0u, c < nch, pp, pt, 8 * q);
+      chunk_pend(g.b, g.tag_b, c < nch ? c : 0u, c < nch && has_b, pp, pt, 8 * q + 4);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        pw4[8 * q + k] = ca[q].w[k];
+        pw4[8 * q + 4 + k] = cb[q].w[k];
+      }
+    }
+    ok = settle4<16>(pp, pt, pw4);
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        ca[q].w[k] = pw4[8 * q + k];
+        cb[q].w[k] = pw4[8 * q + 4 + k];
+      }
   }
+  if (has_r) {
+    const uint32_t* pp1[1] = {rin};
+    const uint32_t pt1[1] = {g.tag_r};
+    uint32_t w1[1] = {rw};
+    ok &= settle1<1>(pp1, pt1, w1);
+    gemv_partials(sh, nch)[g.W * rrows + tid] = tag_value(w1[0]);
+  }
+  if (!ok) set_status(P.status, kStatusTimeout);
   float raw[2][16];
   float ss = 0.f;
 #pragma unroll
   for (int q = 0; q < 2; ++q) {
     const uint32_t c = tid + q * NCT;
-    unpack8(pa[q][0], raw[q]);
-    unpack8(pa[q][1], raw[q] + 8);
+    chunk_values(ca[q], g.tag_a, raw[q]);
     if (g.pro == kAddRms) {
       float xb[16];
-      unpack8(pb[q][0], xb);
-      unpack8(pb[q][1], xb + 8);
+      chunk_values(cb[q], g.tag_b, xb);
 #pragma unroll
       for (int j = 0; j < 16; ++j) raw[q][j] = round_bf16(raw[q][j] + xb[j]);
-      if (blockIdx.x == 0 && c < nch) {  // one CTA keeps x_resid for the down projection's residual
-        uint32_t pk[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          pk[j] = (uint32_t)to_bf16(raw[q][2 * j]) | ((uint32_t)to_bf16(raw[q][2 * j + 1]) << 16);
-        uint4* dst = reinterpret_cast<uint4*>(g.resid_out + c * 16);
-        dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-        dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-      }
+      if (blockIdx.x == 0 && c < nch)  // one CTA keeps x_resid for the down projection's residual
+        chunk_store_tagged(g.resid_out + c * 16, raw[q], g.out_tag);
     }
 #pragma unroll
     for (int j = 0; j < 16; ++j) ss = fmaf(raw[q][j], raw[q][j], ss);  // zero past the end
@@ -575,8 +845,7 @@ __device__ __noinline__ void gemv_prologue(unsigned long long* tr) {
     const uint32_t c = tid + q * NCT;
     if (q == 1 && NCT >= nch) break;  // (uniform) no second chunk anywhere
     float v[16], xb[16], w[16];
-    unpack8(pb[q][0], xb);
-    unpack8(pb[q][1], xb + 8);
+    chunk_values(cb[q], g.tag_b, xb);
     unpack8(pw[q][0], w);
     unpack8(pw[q][1], w + 8);
     if (g.pro == kHeadNormSilu) {
@@ -586,8 +855,12 @@ __device__ __noinline__ void gemv_prologue(unsigned long long* tr) {
       for (int j = 0; j < 16; ++j) hs = fmaf(raw[q][j], raw[q][j], hs);
       for (uint32_t o = 1; o < g.head_dim / 16; o <<= 1) hs += __shfl_xor_sync(FULLMASK, hs, o);
       const float hi = rsqrtf(hs / (float)g.head_dim + P.eps);
+      float yn[16];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) v[j] = silu_fast(xb[j]) * round_bf16(raw[q][j] * hi * w[j]);
+      for (int j = 0; j < 16; ++j) yn[j] = round_bf16(raw[q][j] * hi * w[j]);
+      if (g.dump && c < nch) chunk_store_bf16(g.dump + c * 16, yn);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[j] = silu_fast(xb[j]) * yn[j];
     } else if (g.pro == kPlain) {
 #pragma unroll
       for (int j = 0; j < 16; ++j) v[j] = raw[q][j];
@@ -597,6 +870,7 @@ __device__ __noinline__ void gemv_prologue(unsigned long long* tr) {
     } else {  // RMSNorm (plain or after the residual add)
 #pragma unroll
       for (int j = 0; j < 16; ++j) v[j] = round_bf16(raw[q][j] * inv * w[j]);
+      if (g.dump && c < nch) chunk_store_bf16(g.dump + c * 16, v);
     }
     if (c < nch) {
       XQ x;
@@ -656,15 +930,15 @@ __device__ __forceinline__ void gemv_tiles(const Gemv& g, const Smem& sh, uint32
   const uint32_t rb = g.rb, ntiles = g.ntiles;
   float* part = gemv_partials(sh, nch) + kp * (g.re - rb);  // indexed by row - rb
   const bool direct = gemv_direct(g);
-  uint16_t* const obase = g.out[0];
   int* status = prog().status;
+  const uint64_t limit = wait_limit();
   if (tr && threadIdx.x == 0) tr[11] = global_ns();
   float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;  // sums of the last tiles' rows
   // their places: in part, or for whole rows in the outputs from obase (~0u: none)
   uint32_t pr0 = ~0u, pr1 = ~0u, pr2 = ~0u, pr3 = ~0u;
   for (uint32_t t = 0; t < ntiles; ++t) {
     const uint32_t st = slot_of(it);
-    if (!dead && !mbar_wait(&sh.full[st], parity_of(it))) {
+    if (!dead && !mbar_wait(&sh.full[st], parity_of(it), limit)) {
       set_status(status, kStatusTimeout);
       dead = true;
     }
@@ -672,6 +946,8 @@ __device__ __forceinline__ void gemv_tiles(const Gemv& g, const Smem& sh, uint32
       if (t == 0) tr[4] = global_ns();
       if (t + 1 == ntiles) tr[5] = global_ns();
     }
+    // after a wait ran out nothing of the ring is read, and no slot is released
+    // (its copy may still be in flight)
     const uint32_t meta = dead ? 0u : sh.tmeta[st];
     const uint32_t tout = s_tout[st];
     const bool mine = rs < (meta >> 24);
@@ -700,7 +976,7 @@ __device__ __forceinline__ void gemv_tiles(const Gemv& g, const Smem& sh, uint32
       }
     } else {
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sh.empty[st]);
+      if (lane == 0 && !dead) mbar_arrive(&sh.empty[st]);
     }
     ++it;
     // the lanes' sums of the last four tiles' rows are reduced across the warp
@@ -713,7 +989,7 @@ __device__ __forceinline__ void gemv_tiles(const Gemv& g, const Smem& sh, uint32
       const uint32_t q = lane >> 3;
       const uint32_t pr = q == 0 ? pr0 : q == 1 ? pr1 : q == 2 ? pr2 : pr3;
       if ((lane & 7) == 0 && pr != ~0u) {
-        if (direct) obase[pr] = to_bf16(tot);  // a whole row: its output, straight from the loop
+        if (direct) gemv_store(g, 0, pr, tot);  // a whole row: its output, straight from the loop
         else part[pr] = tot;
       }
       acc0 = acc1 = acc2 = acc3 = 0.f;
@@ -723,7 +999,7 @@ __device__ __forceinline__ void gemv_tiles(const Gemv& g, const Smem& sh, uint32
 }
 
 __device__ __noinline__ uint32_t gemv_main(uint32_t itd, unsigned long long* tr) {
-  const Gemv& g = s_gemv;
+  const Gemv& g = cur_gemv();
   const Smem sh = smem_map(smem_raw);
   if (tr && threadIdx.x == 0) tr[10] = global_ns();
   uint32_t it = itd & ~kDeadBit;
@@ -744,10 +1020,10 @@ __device__ __noinline__ uint32_t gemv_main(uint32_t itd, unsigned long long* tr)
 // projection, bf16 stores by consecutive threads.
 __device__ uint32_t gemv_rows(uint32_t itd, unsigned long long* tr) {
   itd = gemv_main(itd, tr);
-  if (gemv_direct(s_gemv)) return itd;
+  if (gemv_direct(cur_gemv())) return itd;
   consumer_sync();
   if (tr && threadIdx.x == 0) tr[12] = global_ns();
-  const Gemv& g = s_gemv;
+  const Gemv& g = cur_gemv();
   const Smem sh = smem_map(smem_raw);
   const uint32_t rb = g.rb, rows = g.re - g.rb, W = g.W;
   const float* part = gemv_partials(sh, g.K / 16);
@@ -759,7 +1035,7 @@ __device__ uint32_t gemv_rows(uint32_t itd, unsigned long long* tr) {
     const uint32_t row = rb + i;
     uint32_t sg = 0;
     while (sg + 1 < g.nseg && row >= g.row0[sg + 1]) ++sg;
-    g.out[sg][row - g.row0[sg]] = to_bf16(y);
+    gemv_store(g, sg, row - g.row0[sg], y);
   }
   return itd;
 }
@@ -864,13 +1140,20 @@ __device__ __forceinline__ void stage16(const BatchBuf& bb, uint32_t ng, const f
 // round of NI items are issued before any is used (NI sized so that they stay in
 // registers). RMS kinds keep the raw rows (bf16) in the staging buffer until the
 // sums of squares are in.
+// Sequence b's copy of a projection input: tagged words (stride in words) or the
+// caller's bf16 vectors (tag 0, stride in elements).
+__device__ __forceinline__ const void* seq_vec(const void* base, uint32_t tag, uint32_t stride, uint32_t b) {
+  return tag ? static_cast<const void*>(static_cast<const uint32_t*>(base) + (size_t)b * stride)
+             : static_cast<const void*>(static_cast<const uint16_t*>(base) + (size_t)b * stride);
+}
+
 template <int PRO>
 __device__ __noinline__ void prologue_b_kind(uint32_t b0, uint32_t nb, unsigned long long* tr) {
   constexpr bool kTwo = PRO == kAddRms || PRO == kSiluMul || PRO == kHeadNormSilu;
   constexpr bool kRmsKind = PRO == kRms || PRO == kAddRms;
   constexpr uint32_t NI = kTwo ? 2 : 4;
   const Program& P = prog();
-  const Gemv& g = s_gemv;
+  const Gemv& g = cur_gemv();
   const Smem sh = smem_map(smem_raw);
   const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t K = g.K, nch = K / 16, ng = K / 64, items = nb * nch;
@@ -878,61 +1161,82 @@ __device__ __noinline__ void prologue_b_kind(uint32_t b0, uint32_t nb, unsigned 
   float ssb[kRmsKind ? kMaxBatch : 1];
 #pragma unroll
   for (int b = 0; b < (kRmsKind ? kMaxBatch : 1); ++b) ssb[b] = 0.f;
+  bool ok = true;
   for (uint32_t i0 = 0; i0 < items; i0 += NI * NCT) {
-    uint4 a[NI][2], x2[kTwo ? NI : 1][2];
+    Chunk16 a[NI], x2[kTwo ? NI : 1];
 #pragma unroll
     for (uint32_t u = 0; u < NI; ++u) {
       const uint32_t i = i0 + u * NCT + tid;
-      const bool ok = i < items;  // past the end: sequence 0's chunk 0 (valid memory, unused)
-      const uint32_t s = ok ? i / nch : 0, c = ok ? i % nch : 0;
-      const uint4* ap = reinterpret_cast<const uint4*>(g.a + (size_t)(b0 + s) * g.sa + c * 16);
-      a[u][0] = ap[0];
-      a[u][1] = ap[1];
-      if constexpr (kTwo) {
-        const uint4* bp = reinterpret_cast<const uint4*>(g.b + (size_t)(b0 + s) * g.sb + c * 16);
-        x2[u][0] = bp[0];
-        x2[u][1] = bp[1];
+      const bool ok_i = i < items;  // past the end: no load (its values are unused)
+      const uint32_t s = ok_i ? i / nch : 0, c = ok_i ? i % nch : 0;
+      a[u].w[0] = a[u].w[1] = a[u].w[2] = a[u].w[3] = make_uint4(0u, 0u, 0u, 0u);
+      if constexpr (kTwo) x2[u] = a[u];
+      if (ok_i) {
+        chunk_issue(seq_vec(g.a, g.tag_a, g.sa, b0 + s), g.tag_a, c, a[u]);
+        if constexpr (kTwo) chunk_issue(seq_vec(g.b, g.tag_b, g.sb, b0 + s), g.tag_b, c, x2[u]);
       }
     }
-    if (tr && tid == 0 && i0 == 0 && a[0][0].x != 0x12345678u) tr[8] = global_ns();  // loads landed
+    {  // the tagged inputs not there yet, polled together
+      constexpr int NP = kTwo ? 8 * NI : 4 * NI;
+      const uint32_t* pp[NP];
+      uint32_t pt[NP];
+      uint4 pw4[NP];
+#pragma unroll
+      for (uint32_t u = 0; u < NI; ++u) {
+        const uint32_t i = i0 + u * NCT + tid;
+        const bool in = i < items;
+        const uint32_t s = in ? i / nch : 0, c = in ? i % nch : 0;
+        chunk_pend(seq_vec(g.a, g.tag_a, g.sa, b0 + s), g.tag_a, c, in, pp, pt, (kTwo ? 8 : 4) * u);
+        if constexpr (kTwo) chunk_pend(seq_vec(g.b, g.tag_b, g.sb, b0 + s), g.tag_b, c, in, pp, pt, 8 * u + 4);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          pw4[(kTwo ? 8 : 4) * u + k] = a[u].w[k];
+          if constexpr (kTwo) pw4[8 * u + 4 + k] = x2[u].w[k];
+        }
+      }
+      ok &= settle4<NP>(pp, pt, pw4);
+#pragma unroll
+      for (uint32_t u = 0; u < NI; ++u)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          a[u].w[k] = pw4[(kTwo ? 8 : 4) * u + k];
+          if constexpr (kTwo) x2[u].w[k] = pw4[8 * u + 4 + k];
+        }
+    }
+    if (tr && tid == 0 && i0 == 0 && a[0].w[0].x != 0x12345678u) tr[8] = global_ns();  // loads landed
 #pragma unroll
     for (uint32_t u = 0; u < NI; ++u) {
       const uint32_t i = i0 + u * NCT + tid;
-      const bool ok = i < items;
-      const uint32_t s = ok ? i / nch : 0, c = ok ? i % nch : 0;
+      const bool ok_i = i < items;
+      const uint32_t s = ok_i ? i / nch : 0, c = ok_i ? i % nch : 0;
       float raw[16], v[16];
-      unpack8(a[u][0], raw);
-      unpack8(a[u][1], raw + 8);
+      chunk_values(a[u], g.tag_a, raw);
       if constexpr (kRmsKind) {
-        uint32_t pk[8] = {a[u][0].x, a[u][0].y, a[u][0].z, a[u][0].w, a[u][1].x, a[u][1].y, a[u][1].z, a[u][1].w};
         if constexpr (PRO == kAddRms) {
           float xb[16];
-          unpack8(x2[u][0], xb);
-          unpack8(x2[u][1], xb + 8);
+          chunk_values(x2[u], g.tag_b, xb);
 #pragma unroll
-          for (int k = 0; k < 8; ++k) pk[k] = pack_bf16x2(raw[2 * k] + xb[2 * k], raw[2 * k + 1] + xb[2 * k + 1]);
-          unpack_words(pk, raw);
+          for (int k = 0; k < 16; ++k) raw[k] = round_bf16(raw[k] + xb[k]);
+          if (ok_i && blockIdx.x == 0)  // one CTA stores x_resid
+            chunk_store_tagged(g.resid_out + (size_t)(b0 + s) * g.sres_out + c * 16, raw, g.out_tag);
         }
+        uint32_t pk[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) pk[k] = pack_bf16x2(raw[2 * k], raw[2 * k + 1]);  // exact: bf16 values
         float ss = 0.f;
 #pragma unroll
         for (int j = 0; j < 16; ++j) ss = fmaf(raw[j], raw[j], ss);
-        if (ok) {
+        if (ok_i) {
 #pragma unroll
           for (int b = 0; b < kMaxBatch; ++b) ssb[b] += s == (uint32_t)b ? ss : 0.f;
           uint4* dst = reinterpret_cast<uint4*>(bb.xf + s * bb.stride + c * 16);
           dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
           dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-          if (PRO == kAddRms && blockIdx.x == 0) {  // one CTA stores x_resid
-            uint4* rd = reinterpret_cast<uint4*>(g.resid_out + (size_t)(b0 + s) * g.sres_out + c * 16);
-            rd[0] = dst[0];
-            rd[1] = dst[1];
-          }
         }
       } else {
         if constexpr (PRO == kSiluMul) {
           float xb[16];
-          unpack8(x2[u][0], xb);
-          unpack8(x2[u][1], xb + 8);
+          chunk_values(x2[u], g.tag_b, xb);
 #pragma unroll
           for (int j = 0; j < 16; ++j) v[j] = silu_fast(raw[j]) * xb[j];
         } else if constexpr (PRO == kHeadNormSilu) {
@@ -942,8 +1246,7 @@ __device__ __noinline__ void prologue_b_kind(uint32_t b0, uint32_t nb, unsigned 
           for (uint32_t o = 1; o < g.head_dim / 16; o <<= 1) hs += __shfl_xor_sync(FULLMASK, hs, o);
           const float hi = rsqrtf(hs / (float)g.head_dim + P.eps);
           float xb[16], w[16];
-          unpack8(x2[u][0], xb);
-          unpack8(x2[u][1], xb + 8);
+          chunk_values(x2[u], g.tag_b, xb);
           const uint4* wp = reinterpret_cast<const uint4*>(g.nw + (c * 16) % g.head_dim);
           unpack8(wp[0], w);
           unpack8(wp[1], w + 8);
@@ -952,16 +1255,18 @@ __device__ __noinline__ void prologue_b_kind(uint32_t b0, uint32_t nb, unsigned 
           for (int k = 0; k < 8; ++k)
             pk[k] = pack_bf16x2(raw[2 * k] * hi * w[2 * k], raw[2 * k + 1] * hi * w[2 * k + 1]);
           unpack_words(pk, v);
+          if (g.dump && ok_i) chunk_store_bf16(g.dump + (size_t)(b0 + s) * (P.seq_stride / 2) + c * 16, v);
 #pragma unroll
           for (int j = 0; j < 16; ++j) v[j] *= silu_fast(xb[j]);
         } else {
 #pragma unroll
           for (int j = 0; j < 16; ++j) v[j] = raw[j];
         }
-        stage16(bb, ng, v, s, c, ok);
+        stage16(bb, ng, v, s, c, ok_i);
       }
     }
   }
+  if (!ok) set_status(P.status, kStatusTimeout);
   if (tr && tid == 0) tr[9] = global_ns();
   if constexpr (kRmsKind) {
     // each sequence's sum of squares: per thread, per warp, then over the warps in a
@@ -1013,6 +1318,7 @@ __device__ __noinline__ void prologue_b_kind(uint32_t b0, uint32_t nb, unsigned 
 #pragma unroll
         for (int k = 0; k < 8; ++k) pk[k] = pack_bf16x2(raw[2 * k] * inv * w[2 * k], raw[2 * k + 1] * inv * w[2 * k + 1]);
         unpack_words(pk, v);
+        if (g.dump && ok) chunk_store_bf16(g.dump + (size_t)(b0 + s) * (P.seq_stride / 2) + c * 16, v);
         stage16(bb, ng, v, s, c, ok);
       }
     }
@@ -1022,7 +1328,7 @@ __device__ __noinline__ void prologue_b_kind(uint32_t b0, uint32_t nb, unsigned 
 }
 
 __device__ __forceinline__ void gemv_prologue_b(uint32_t b0, uint32_t nb, unsigned long long* tr) {
-  switch (s_gemv.pro) {
+  switch (cur_gemv().pro) {
     case kRms: prologue_b_kind<kRms>(b0, nb, tr); break;
     case kAddRms: prologue_b_kind<kAddRms>(b0, nb, tr); break;
     case kSiluMul: prologue_b_kind<kSiluMul>(b0, nb, tr); break;
@@ -1118,7 +1424,7 @@ __device__ __forceinline__ void batch_tile_groups(const uint8_t* tile, uint32_t 
 // partial sums, and the team adds them in warp order and writes the rows of each
 // sequence (+ residual) as bf16. Tiles of other teams are skipped unread.
 __device__ __noinline__ uint32_t gemv_tiles_b(uint32_t itd, uint32_t b0, uint32_t nb, unsigned long long* tr) {
-  const Gemv& g = s_gemv;
+  const Gemv& g = cur_gemv();
   const Smem sh = smem_map(smem_raw);
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gq = lane >> 2, t = lane & 3;
   const uint32_t K = g.K, ng = K / 64, T = g.T, W = NCW / T;
@@ -1134,13 +1440,16 @@ __device__ __noinline__ uint32_t gemv_tiles_b(uint32_t itd, uint32_t b0, uint32_
   const float2* sqb = bb.xsq + (2 * t + 1 < nb ? 2 * t + 1 : 0) * ng;
   float* mine = bb.part + warp * 128;         // [16 rows][8 sequences]
   const float* tp = bb.part + team * W * 128;  // the team's partials
+  const uint64_t limit = wait_limit();
   for (uint32_t tl = 0; tl < g.ntiles; ++tl, ++it) {
-    if (tl % T != team) continue;
     const uint32_t st = slot_of(it);
-    if (!dead && !mbar_wait(&sh.full[st], parity_of(it))) {
+    // every warp waits for every tile, its team's or not: a warp that skipped a
+    // slot's phase could take a later phase of the slot for complete too early
+    if (!dead && !mbar_wait(&sh.full[st], parity_of(it), limit)) {
       set_status(status, kStatusTimeout);
       dead = true;
     }
+    if (tl % T != team) continue;
     if (tr && threadIdx.x == 0) {
       if (tl == 0) tr[4] = global_ns();
       if (tl + T >= g.ntiles) tr[5] = global_ns();
@@ -1156,7 +1465,7 @@ __device__ __noinline__ uint32_t gemv_tiles_b(uint32_t itd, uint32_t b0, uint32_
                                sqb, y);
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive_n(&sh.empty[st], T);
+    if (lane == 0 && !dead) mbar_arrive_n(&sh.empty[st], T);
     mine[gq * 8 + 2 * t] = y[0][0];
     mine[gq * 8 + 2 * t + 1] = y[0][1];
     mine[(gq + 8) * 8 + 2 * t] = y[1][0];
@@ -1166,10 +1475,11 @@ __device__ __noinline__ uint32_t gemv_tiles_b(uint32_t itd, uint32_t b0, uint32_
       const uint32_t rho = e / nb, s = e - rho * nb, row = r0 + rho;
       float acc = 0.f;
       for (uint32_t jj = 0; jj < W; ++jj) acc += tp[jj * 128 + rho * 8 + s];
-      if (g.epi == 1) acc += bf16f(g.resid_in[(size_t)(b0 + s) * g.sres_in + row]);
+      if (g.epi == 1)
+        acc += tagged_value(static_cast<const uint32_t*>(g.resid_in) + (size_t)(b0 + s) * g.sres_in + row, g.tag_r);
       uint32_t sg = 0;
       while (sg + 1 < g.nseg && row >= g.row0[sg + 1]) ++sg;
-      g.out[sg][(size_t)(b0 + s) * g.sout[sg] + row - g.row0[sg]] = to_bf16(acc);
+      gemv_store(g, sg, (size_t)(b0 + s) * g.sout[sg] + row - g.row0[sg], acc);
     }
     named_barrier(2 + team, W * 32);  // the partials are read before the next tile's
   }
@@ -1243,11 +1553,11 @@ __device__ __forceinline__ void norm_rope(float* x, const float* wv, const Progr
 // of head group w % NG (one kv-head) and every TI-th tile, TI = 12 / NG; the TI
 // partial softmax states of a head group are merged in shared memory at the end.
 template <int D, int HPW>
-__device__ __noinline__ uint32_t attn_consume(uint32_t itd, unsigned long long* tr) {
+__device__ __noinline__ uint32_t attn_consume(uint32_t itd, uint32_t ph, unsigned long long* tr) {
   uint32_t it = itd & ~kDeadBit;
   bool dead = (itd & kDeadBit) != 0;
   const Program& P = prog();
-  const LayerDesc& L = s_layer;
+  const LayerDesc& L = cur_layer();
   const Smem sh = smem_map(smem_raw);
   constexpr int EPL = D / 32;
   constexpr int NV = HPW * kTS;
@@ -1278,16 +1588,67 @@ __device__ __noinline__ uint32_t attn_consume(uint32_t itd, unsigned long long* 
   const bool active = ti < TI;
   const uint32_t h0 = hg * HPW, g = h0 / (H / Hkv);
   float q[HPW][EPL], m[HPW], l[HPW], acc[HPW][EPL], qw[EPL];
-  const uint16_t* qf = reinterpret_cast<const uint16_t*>(s_seq.scratch + P.sm.q_full);
-#pragma unroll
-  for (int j = 0; j < HPW; ++j) load_row<EPL>(qf + (size_t)(h0 + j) * 2 * D + lane * EPL, q[j]);
+  const uint32_t tin = phase_tag(ph - 1);  // q, k, v: the projection phase before
+  const uint32_t* qf = reinterpret_cast<const uint32_t*>(s_seq.scratch + P.sm.q_full);
   load_row<EPL>(L.q_norm + lane * EPL, qw);
   const bool kv_warp = appender && warp < Hkv;
   float kx[EPL], vx[EPL], kw[EPL];
-  if (kv_warp) {
-    load_row<EPL>(reinterpret_cast<const uint16_t*>(s_seq.scratch + P.sm.k) + warp * D + lane * EPL, kx);
-    load_row<EPL>(reinterpret_cast<const uint16_t*>(s_seq.scratch + P.sm.v) + warp * D + lane * EPL, vx);
-    load_row<EPL>(L.k_norm + lane * EPL, kw);
+  if (kv_warp) load_row<EPL>(L.k_norm + lane * EPL, kw);
+  {  // this warp's q-heads and, for the appending CTA, the new k and v: polled together
+    constexpr int NR = HPW + 2;  // rows of EPL tagged words per lane
+    const uint32_t* rows[NR];
+#pragma unroll
+    for (int j = 0; j < HPW; ++j) rows[j] = qf + (size_t)(h0 + j) * 2 * D + lane * EPL;
+    rows[HPW] = reinterpret_cast<const uint32_t*>(s_seq.scratch + P.sm.k) + warp * D + lane * EPL;
+    rows[HPW + 1] = reinterpret_cast<const uint32_t*>(s_seq.scratch + P.sm.v) + warp * D + lane * EPL;
+    bool ok;
+    if constexpr (EPL % 4 == 0) {
+      constexpr int G = EPL / 4, N = NR * G;
+      const uint32_t* pp[N];
+      uint32_t pt[N];
+      uint4 w[N];
+#pragma unroll
+      for (int r = 0; r < NR; ++r)
+#pragma unroll
+        for (int k = 0; k < G; ++k) {
+          pp[r * G + k] = rows[r] + 4 * k;
+          pt[r * G + k] = (r < HPW || kv_warp) ? tin : 0u;
+          w[r * G + k] = pt[r * G + k] ? ld_tagged4(pp[r * G + k]) : make_uint4(0u, 0u, 0u, 0u);
+        }
+      ok = settle4<N>(pp, pt, w);
+#pragma unroll
+      for (int r = 0; r < NR; ++r) {
+        float* dst = r < HPW ? q[r < HPW ? r : 0] : (r == HPW ? kx : vx);
+#pragma unroll
+        for (int k = 0; k < G; ++k) {
+          dst[4 * k] = tag_value(w[r * G + k].x);
+          dst[4 * k + 1] = tag_value(w[r * G + k].y);
+          dst[4 * k + 2] = tag_value(w[r * G + k].z);
+          dst[4 * k + 3] = tag_value(w[r * G + k].w);
+        }
+      }
+    } else {
+      constexpr int N = NR * EPL;
+      const uint32_t* pp[N];
+      uint32_t pt[N];
+      uint32_t w[N];
+#pragma unroll
+      for (int r = 0; r < NR; ++r)
+#pragma unroll
+        for (int k = 0; k < EPL; ++k) {
+          pp[r * EPL + k] = rows[r] + k;
+          pt[r * EPL + k] = (r < HPW || kv_warp) ? tin : 0u;
+          w[r * EPL + k] = pt[r * EPL + k] ? ld_tagged(pp[r * EPL + k]) : 0u;
+        }
+      ok = settle1<N>(pp, pt, w);
+#pragma unroll
+      for (int r = 0; r < NR; ++r) {
+        float* dst = r < HPW ? q[r < HPW ? r : 0] : (r == HPW ? kx : vx);
+#pragma unroll
+        for (int k = 0; k < EPL; ++k) dst[k] = tag_value(w[r * EPL + k]);
+      }
+    }
+    if (!ok) set_status(P.status, kStatusTimeout);
   }
   consumer_sync();  // the angle table
   if (kv_warp) {  // the new token's k (normed, rotated) and v: appended by exactly one CTA
@@ -1314,12 +1675,13 @@ __device__ __noinline__ uint32_t attn_consume(uint32_t itd, unsigned long long* 
   if (tr && threadIdx.x == 0) tr[3] = global_ns();
 
   const uint32_t midx = lane >> SH, mj = midx / kTS, mt = midx % kTS;
+  const uint64_t limit = wait_limit();
   for (uint32_t i = 0; i < sp.ntiles; ++i) {
     const uint32_t st = slot_of(it);
     const bool mine = active && (i % TI) == ti;
     // every warp waits for every tile before releasing it, so no warp can run a
     // ring round ahead and complete a slot's release early
-    if (!dead && !mbar_wait(&sh.full[st], parity_of(it))) {
+    if (!dead && !mbar_wait(&sh.full[st], parity_of(it), limit)) {
       set_status(P.status, kStatusTimeout);
       dead = true;
     }
@@ -1382,7 +1744,7 @@ __device__ __noinline__ uint32_t attn_consume(uint32_t itd, unsigned long long* 
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&sh.empty[st]);  // every warp releases every tile
+    if (lane == 0 && !dead) mbar_arrive(&sh.empty[st]);  // every warp releases every tile
     ++it;
   }
   if (sp.has_fresh && ti == 0) {
@@ -1455,38 +1817,78 @@ __device__ __noinline__ uint32_t attn_consume(uint32_t itd, unsigned long long* 
       }
     }
   }
-  consumer_sync();  // the merge space is free again
+  consumer_sync();  // the merge space is free again; every partial of the split is stored
+  if (threadIdx.x == 0) {  // publish them: the split's flag, released at GPU scope
+    uint32_t* flags = reinterpret_cast<uint32_t*>(s_seq.scratch + P.sm.flags);
+    st_release(flags + s, phase_tag(ph));
+  }
   return it | (dead ? kDeadBit : 0u);
 }
 
 // Merge of the P partials of (head h, 32 dims) per CTA, then the output gate:
-// ga = bf16(bf16(attn) * sigmoid(gate)).
-__device__ __noinline__ void combine_consume() {
+// ga = bf16(bf16(attn) * sigmoid(gate)). A split's partials are read once its flag
+// carries the attention phase's tag (acquire), through L2.
+__device__ __forceinline__ float ld_f32_l2(const float* p) {
+  float r;
+  asm volatile("ld.relaxed.gpu.global.f32 %0, [%1];" : "=f"(r) : "l"(p) : "memory");
+  return r;
+}
+__device__ __noinline__ void combine_consume(uint32_t ph) {
   const Program& P = prog();
-  const LayerDesc& L = s_layer;
+  const LayerDesc& L = cur_layer();
   const Smem sh = smem_map(smem_raw);
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t nd = P.D / 32, item = blockIdx.x;
   const Span sp = attn_span(P, L.capacity, s_seq.b);
   if (item >= P.H * nd) return;
   const uint32_t h = item / nd, d = (item % nd) * 32 + lane;
-  uint16_t* ga = reinterpret_cast<uint16_t*>(s_seq.scratch + P.sm.ga);
+  uint32_t* ga = reinterpret_cast<uint32_t*>(s_seq.scratch + P.sm.ga);
+  const uint32_t tag = phase_tag(ph);
   if (!sp.ok) {
-    if (warp == 0) ga[(size_t)h * P.D + d] = 0;
+    if (warp == 0) st_tagged(ga + (size_t)h * P.D + d, tag_word(0.f, tag));
     return;
   }
   const float* part_o = reinterpret_cast<const float*>(s_seq.scratch + P.sm.part_o);
   const float* part_ml = reinterpret_cast<const float*>(s_seq.scratch + P.sm.part_ml);
+  const uint32_t* flags = reinterpret_cast<const uint32_t*>(s_seq.scratch + P.sm.flags);
+  const uint32_t tflag = phase_tag(ph - 1);
+  const uint64_t limit = wait_limit();
+  bool ok = true;
   float M = -INFINITY, Ls = 0.f, O = 0.f;
   for (uint32_t base = 0; base < P.P; base += NCW * 4) {
     float ms[4], ls[4], os[4];
+    {  // the splits' flags first (polled together), then their partials
+      uint32_t todo = 0, f[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t sp_ = base + warp + NCW * k;
+        f[k] = sp_ < P.P ? ld_acquire(flags + sp_) : tflag;
+        if (f[k] != tflag) todo |= 1u << k;
+      }
+      if (todo) {
+        const uint64_t t0 = global_ns();
+        for (uint32_t n = 1; todo; ++n) {
+          __nanosleep(64);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            if ((todo >> k) & 1u) f[k] = ld_acquire(flags + base + warp + NCW * k);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            if (((todo >> k) & 1u) && f[k] == tflag) todo &= ~(1u << k);
+          if (todo && (global_ns() - t0 > limit || ((n & 15) == 0 && timed_out(P.status)))) {
+            ok = false;
+            break;
+          }
+        }
+      }
+    }
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const uint32_t sp_ = base + warp + NCW * k;
-      const bool ok = sp_ < P.P;
-      ms[k] = ok ? part_ml[((size_t)sp_ * P.H + h) * 2] : -INFINITY;
-      ls[k] = ok ? part_ml[((size_t)sp_ * P.H + h) * 2 + 1] : 0.f;
-      os[k] = ok ? part_o[((size_t)sp_ * P.H + h) * P.D + d] : 0.f;
+      const bool in = sp_ < P.P;
+      ms[k] = in ? ld_f32_l2(part_ml + ((size_t)sp_ * P.H + h) * 2) : -INFINITY;
+      ls[k] = in ? ld_f32_l2(part_ml + ((size_t)sp_ * P.H + h) * 2 + 1) : 0.f;
+      os[k] = in ? ld_f32_l2(part_o + ((size_t)sp_ * P.H + h) * P.D + d) : 0.f;
     }
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -1498,6 +1900,14 @@ __device__ __noinline__ void combine_consume() {
       M = mn;
     }
   }
+  float gate = 0.f;
+  if (warp == 0) {
+    uint32_t w;
+    ok &= ld_tagged_wait(reinterpret_cast<const uint32_t*>(s_seq.scratch + P.sm.q_full) + (size_t)h * 2 * P.D + P.D + d,
+                         phase_tag(ph - 2), w, limit, P.status);
+    gate = tag_value(w);
+  }
+  if (!ok) set_status(P.status, kStatusTimeout);
   float* part = reinterpret_cast<float*>(sh.uni);  // [3][16][32]
   part[(0 * NCW + warp) * 32 + lane] = M;
   part[(1 * NCW + warp) * 32 + lane] = Ls;
@@ -1518,9 +1928,7 @@ __device__ __noinline__ void combine_consume() {
       O = fmaf(part[(2 * NCW + w) * 32 + lane], c, O);
     }
     const float attn = round_bf16(O / Ls);
-    const uint16_t* qf = reinterpret_cast<const uint16_t*>(s_seq.scratch + P.sm.q_full);
-    const float gate = bf16f(qf[(size_t)h * 2 * P.D + P.D + d]);
-    ga[(size_t)h * P.D + d] = to_bf16(attn * sigmoidf_(gate));
+    st_tagged(ga + (size_t)h * P.D + d, tag_word(attn * sigmoidf_(gate), tag));
   }
   consumer_sync();
 }
@@ -1531,8 +1939,9 @@ __device__ __noinline__ void combine_consume() {
 // beta, state columns are independent:
 //   u_v = sum_i (g S[i][v]) k_i,  S[i][v] <- g S[i][v] + k_i beta (v_v - u_v),
 //   y_v = sum_i S[i][v] q_i / sqrt(Dk),
-// so the [Dk][32] fp32 slice is read into registers once (before the phase's grid
-// barrier: nothing before it writes the state), updated, and written once.
+// so the [Dk][32] fp32 slice is read into registers once (it arrives through the
+// ring while the layer's input projection streams: nothing before it in the step
+// writes the state), updated, and written once.
 constexpr int kGdnWarps = 8;  // warps holding state rows (Dk / 8 rows each)
 // The linear-attention phase's inputs that do not depend on the step's earlier
 // phases (the CTA's state block [Dk][32] fp32, its channels' convolution state
@@ -1558,19 +1967,21 @@ __device__ __forceinline__ GdnItem gdn_item(const Program& P) {
 
 // The convolution state of the q/k channels, shifted by one token (newest last):
 // the linear-attention phase reads it in every CTA of the channel's v-heads, so it
-// is written one grid barrier later, in the output projection phase, each CTA
-// taking a share of the channels (one warp).
-__device__ __noinline__ void conv_shift_qk(float* conv_state, const uint8_t* scratch) {
+// is written in the output projection phase, after that phase's input (the readout
+// of every linear-attention CTA, hence after all their reads of it) is in, each CTA
+// taking a share of the channels (one warp). tag: that of qkv.
+__device__ __noinline__ void conv_shift_qk(float* conv_state, const uint8_t* scratch, uint32_t tag) {
   const Program& P = prog();
   const uint32_t lane = threadIdx.x & 31, Kc = P.Kc;
   const uint32_t nqk = 2 * P.Hk * P.Dk, per = (nqk + gridDim.x - 1) / gridDim.x;
   const uint32_t c0 = blockIdx.x * per, c1 = min(nqk, c0 + per);
-  const uint16_t* qkv = reinterpret_cast<const uint16_t*>(scratch + P.sm.qkv);
+  const uint32_t* qkv = reinterpret_cast<const uint32_t*>(scratch + P.sm.qkv);
   for (uint32_t ch = c0 + lane; ch < c1; ch += 32) {
     float* cs = conv_state + (size_t)ch * Kc;
+    const float x = tagged_value(qkv + ch, tag);
     float v[kMaxKc];
 #pragma unroll
-    for (int t = 0; t < kMaxKc; ++t) v[t] = t + 1 < (int)Kc ? cs[t + 1] : bf16f(qkv[ch]);
+    for (int t = 0; t < kMaxKc; ++t) v[t] = t + 1 < (int)Kc ? cs[t + 1] : x;
 #pragma unroll
     for (int t = 0; t < kMaxKc; ++t)
       if (t < (int)Kc) cs[t] = v[t];
@@ -1578,9 +1989,9 @@ __device__ __noinline__ void conv_shift_qk(float* conv_state, const uint8_t* scr
 }
 
 template <int DK>
-__device__ __noinline__ uint32_t gdn_consume(uint32_t itd) {
+__device__ __noinline__ uint32_t gdn_consume(uint32_t itd, uint32_t ph) {
   const Program& P = prog();
-  const LayerDesc& L = s_layer;
+  const LayerDesc& L = cur_layer();
   const Smem sh = smem_map(smem_raw);
   constexpr int RPT = DK / kGdnWarps;
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
@@ -1589,32 +2000,49 @@ __device__ __noinline__ uint32_t gdn_consume(uint32_t itd) {
   const uint32_t h = w.h, v0 = w.v0, Kc = P.Kc;
   float* act = reinterpret_cast<float*>(sh.uni);  // [2 Dk + 32]
   float* red = act + 2 * DK + 32;                 // [2][NCW][32]
-  const uint32_t slot = slot_of(itd & ~kDeadBit);
-  if (!(itd & kDeadBit) && !mbar_wait(&sh.full[slot], parity_of(itd & ~kDeadBit))) {
-    set_status(P.status, kStatusTimeout);
-    itd |= kDeadBit;
-  }
-  const float* st_s = reinterpret_cast<const float*>(sh.ring + sh.toff[slot]);
-  const float* cs_s = st_s + DK * 32;
-  const uint16_t* cw_s = reinterpret_cast<const uint16_t*>(cs_s + (2 * DK + 32) * Kc);
-  const uint16_t* qkv = reinterpret_cast<const uint16_t*>(s_seq.scratch + P.sm.qkv);
+  const uint32_t tin = phase_tag(ph - 1);  // qkv, dt_raw, b_raw: the projection phase before
   // this channel (thread < 2 Dk + 32): q, k of the k-head, v of the slice
   const bool chan = tid < 2 * DK + 32;
   const uint32_t ch = tid < DK ? w.hk * DK + tid
                     : tid < 2 * DK ? P.Hk * DK + w.hk * DK + (tid - DK)
                                    : 2 * P.Hk * DK + h * P.Dv + v0 + (tid - 2 * DK);
-  const float x = chan ? bf16f(qkv[ch]) : 0.f;
-  float alog = 0.f, dtb = 0.f;
+  const uint32_t* qkv = reinterpret_cast<const uint32_t*>(s_seq.scratch + P.sm.qkv);
+  float x = 0.f;
+  {
+    const uint32_t* pp[1] = {qkv + (chan ? ch : 0u)};
+    const uint32_t pt[1] = {chan ? tin : 0u};
+    uint32_t w[1] = {chan ? ld_tagged(pp[0]) : 0u};
+    if (!settle1<1>(pp, pt, w)) set_status(P.status, kStatusTimeout);
+    x = tag_value(w[0]);
+  }
+  float alog = 0.f, dtb = 0.f, dtr = 0.f, brw = 0.f;
   if (tid == 0) {
     alog = L.a_log[h];
     dtb = bf16f(L.dt_bias[h]);
+    const uint32_t* pp[2] = {reinterpret_cast<const uint32_t*>(s_seq.scratch + P.sm.dt_raw) + h,
+                             reinterpret_cast<const uint32_t*>(s_seq.scratch + P.sm.b_raw) + h};
+    const uint32_t pt[2] = {tin, tin};
+    uint32_t w[2] = {ld_tagged(pp[0]), ld_tagged(pp[1])};
+    if (!settle1<2>(pp, pt, w)) set_status(P.status, kStatusTimeout);
+    dtr = tag_value(w[0]);
+    brw = tag_value(w[1]);
   }
+  const uint32_t slot = slot_of(itd & ~kDeadBit);
+  if (!(itd & kDeadBit) && !mbar_wait(&sh.full[slot], parity_of(itd & ~kDeadBit), wait_limit())) {
+    set_status(P.status, kStatusTimeout);
+    itd |= kDeadBit;
+  }
+  const bool dead = (itd & kDeadBit) != 0;
+  // after a wait ran out the tile is not read (it may still be arriving)
+  const float* st_s = reinterpret_cast<const float*>(sh.ring + (dead ? 0u : sh.toff[slot]));
+  const float* cs_s = st_s + DK * 32;
+  const uint16_t* cw_s = reinterpret_cast<const uint16_t*>(cs_s + (2 * DK + 32) * Kc);
   // causal conv update + SiLU
   if (chan) {
     // v channels belong to this CTA alone and are written here; the q/k channels of
     // a k-head are read by every CTA of its v-heads during this phase, so
     // conv_shift_qk shifts them in the next one
-    float* cnew = tid >= 2 * DK ? L.conv_state + (size_t)ch * Kc : nullptr;
+    float* cnew = tid >= 2 * DK && !dead ? L.conv_state + (size_t)ch * Kc : nullptr;
     float o = 0.f;
     for (uint32_t t = 0; t < Kc; ++t) {
       const float sv = t + 1 < Kc ? cs_s[tid * Kc + t + 1] : x;  // shift left, newest last
@@ -1623,14 +2051,12 @@ __device__ __noinline__ uint32_t gdn_consume(uint32_t itd) {
     }
     act[tid] = siluf_(o);
   }
-  const uint16_t* dtr = reinterpret_cast<const uint16_t*>(s_seq.scratch + P.sm.dt_raw);
-  const uint16_t* brw = reinterpret_cast<const uint16_t*>(s_seq.scratch + P.sm.b_raw);
   if (tid == 0) {
     // gate = exp(softplus(dt + dt_bias) * -exp(A_log)); beta = sigmoid(b)
-    const float xd = bf16f(dtr[h]) + dtb;
+    const float xd = dtr + dtb;
     const float spl = xd > 20.f ? xd : log1pf(expf(xd));
     sh.misc[0] = expf(spl * -expf(alog));
-    sh.misc[1] = sigmoidf_(bf16f(brw[h]));
+    sh.misc[1] = sigmoidf_(brw);
   }
   consumer_sync();
   // per-head L2 norm of q and k (eps 1e-6), then bf16 as qkv_smooth is
@@ -1659,6 +2085,11 @@ __device__ __noinline__ uint32_t gdn_consume(uint32_t itd) {
       const float v = act[i];
       act[i] = round_bf16(i < DK ? v * iq : (i < 2 * DK ? v * ik : v));
     }
+    if (P.dump && chan) {  // debug: qkv_smooth (q/k channels by the k-head's first CTA)
+      const bool first = w.j == 0 && w.h % (P.Hv / P.Hk) == 0;
+      if (tid >= 2 * DK || first)
+        reinterpret_cast<uint16_t*>(s_seq.scratch + P.sm.qkv_smooth)[ch] = to_bf16(act[tid]);
+    }
     consumer_sync();
   }
   // delta rule on the slice: thread (warp, lane) of the first 8 warps holds rows
@@ -1678,7 +2109,7 @@ __device__ __noinline__ uint32_t gdn_consume(uint32_t itd) {
     red[warp * 32 + lane] = u;
   }
   consumer_sync();
-  if (lane == 0) mbar_arrive(&sh.empty[slot]);  // the tile is read (every warp releases it)
+  if (lane == 0 && !dead) mbar_arrive(&sh.empty[slot]);  // the tile is read (every warp releases it)
   ++itd;
   u = 0.f;
 #pragma unroll
@@ -1692,8 +2123,10 @@ __device__ __noinline__ uint32_t gdn_consume(uint32_t itd) {
       y = fmaf(st[r], qv[warp * RPT + r], y);
     }
     float* sp = L.ssm + ((size_t)blockIdx.x * DK + warp * RPT) * 32 + lane;  // block (h, v0 / 32)
+    if (!dead) {
 #pragma unroll
-    for (int r = 0; r < RPT; ++r) sp[r * 32] = st[r];
+      for (int r = 0; r < RPT; ++r) sp[r * 32] = st[r];
+    }
     red[kGdnWarps * 32 + warp * 32 + lane] = y;
   }
   consumer_sync();
@@ -1701,8 +2134,8 @@ __device__ __noinline__ uint32_t gdn_consume(uint32_t itd) {
     y = 0.f;
 #pragma unroll
     for (int w = 0; w < kGdnWarps; ++w) y += red[kGdnWarps * 32 + w * 32 + lane];
-    uint16_t* yo = reinterpret_cast<uint16_t*>(s_seq.scratch + P.sm.y);
-    yo[(size_t)h * P.Dv + v0 + lane] = to_bf16(y * P.gdn_out_scale);
+    uint32_t* yo = reinterpret_cast<uint32_t*>(s_seq.scratch + P.sm.y);
+    st_tagged(yo + (size_t)h * P.Dv + v0 + lane, tag_word(y * P.gdn_out_scale, phase_tag(ph)));
   }
   consumer_sync();
   return itd;
@@ -1748,7 +2181,7 @@ __device__ __forceinline__ uint8_t* ring_claim(Ring& rg, const Smem& sh, uint32_
     ph = 0;
   }
   while (rg.tail < rg.i && (rg.i - rg.tail >= (uint32_t)kDecSlots || v + span - rg.vcons > rg.size)) {
-    if (!mbar_wait(&sh.empty[slot_of(rg.tail)], parity_of(rg.tail))) {
+    if (!mbar_wait(&sh.empty[slot_of(rg.tail)], parity_of(rg.tail), wait_limit())) {
       set_status(status, kStatusTimeout);
       rg.dead = true;
       return nullptr;
@@ -1768,7 +2201,9 @@ __device__ __forceinline__ uint8_t* ring_claim(Ring& rg, const Smem& sh, uint32_
 
 // The producer (one thread). Weights are read from HBM by a batch's first pass
 // over a phase and kept in L2 for the others (evict-last), the last pass marking
-// them evict-first.
+// them evict-first. Before it returns it waits (bounded) for every copy it issued
+// that the consumers have not released, so that none is in flight when the CTA
+// exits (consumers stop taking tiles after one of their waits has run out).
 __device__ __noinline__ void produce_all(const LayerDesc* layers) {
   const Program& P = prog();
   const Smem sh = smem_map(smem_raw);
@@ -1796,7 +2231,7 @@ __device__ __noinline__ void produce_all(const LayerDesc* layers) {
       fresh = true;
       const int ty = phase_type(L.kind, p);
       if (ty == kPhGemv) {
-        gemv_of(P, L, l, p, 0, s_prod.g);
+        gemv_of(P, L, l, p, 0, 0, s_prod.g);
         const Gemv& g = s_prod.g;
         const uint32_t K = g.K, gs = g.gstride, R = g.R, soff = g.scale_off, boff = g.bias_off;
         const uint32_t span = boff + R * gs * 2, rb = g.rb, re = g.re, nseg = g.nseg;
@@ -1806,7 +2241,7 @@ __device__ __noinline__ void produce_all(const LayerDesc* layers) {
           for (uint32_t sg = 0; sg < nseg; ++sg) {
             const uint32_t base = g.row0[sg], lo = max(rb, base), hi = min(re, g.row0[sg + 1]);
             if (lo >= hi) continue;
-            const uint32_t obase = (uint32_t)(g.out[sg] - g.out[0]);
+            const uint32_t obase = (uint32_t)((g.out[sg] - g.out[0]) / out_esz(g));
             const uint8_t* codes = g.seg[sg].codes;
             const uint16_t* scales = g.seg[sg].scales;
             const uint16_t* biases = g.seg[sg].biases;
@@ -1867,9 +2302,57 @@ __device__ __noinline__ void produce_all(const LayerDesc* layers) {
       }
     }
   }
-  return;
-drain:  // a wait ran out: let the copies still in flight land before the CTA can exit
-  for (uint32_t j = rg.tail; j < rg.i; ++j) mbar_wait(&sh.full[slot_of(j)], parity_of(j));
+drain:  // let the copies still in flight land before the CTA can exit
+  for (uint32_t j = rg.tail; j < rg.i; ++j) mbar_wait(&sh.full[slot_of(j)], parity_of(j), drain_limit());
+}
+
+// ------------------------------------------------------------------ the helper warp
+
+// The work between phases that no consumer should wait for, one phase ahead of the
+// consumers: while they run phase ph, the descriptions of phase ph + 1 (the layer's
+// and the GEMV's, formed on one thread, ~1 us), and in a linear-attention layer's
+// gate|up phase the shift of the q/k channels' conv state (every linear-attention
+// CTA has read it by then: the phase before waited for all their readouts). Its
+// waits use at least the default limit, so that the consumers never run on
+// descriptions it has not formed.
+__device__ __noinline__ void helper_loop() {
+  const Program& P = prog();
+  const uint32_t lane = threadIdx.x & 31;
+  const uint64_t limit = drain_limit();
+  // until the consumers are in phase ph (so phase ph - 1's buffers are free and
+  // phase ph's descriptions are in place); false when the wait runs out
+  auto wait_entered = [&](uint32_t ph) {
+    if (ld_volatile_shared(&s_ph.entered) > ph) return true;
+    const uint64_t t0 = global_ns();
+    while (ld_volatile_shared(&s_ph.entered) <= ph) {
+      if (global_ns() - t0 > limit) {
+        set_status(P.status, kStatusTimeout);
+        return false;
+      }
+      __nanosleep(128);
+    }
+    return true;
+  };
+  uint32_t ph = 0;
+  for (uint32_t l = 0; l < P.n_layers; ++l) {
+    const uint32_t ph0 = ph;
+    if (!wait_entered(ph0)) return;
+    const int kind = s_lay0[l & 1].kind;  // formed before the consumers entered phase ph0
+    const int np = n_phases(kind);
+    for (int p = 0; p < np; ++p, ++ph) {
+      if (p > 0 && !wait_entered(ph)) return;
+      if (p + 1 < np) form_phase(l, p + 1, ph + 1, ph0);
+      else if (l + 1 < P.n_layers) form_phase(l + 1, 0, ph + 1, ph + 1);
+      if (kind == kLayerGDN && p == 3) {  // gate|up of a linear-attention layer
+        const LayerDesc& L = s_lay0[l & 1];
+        for (uint32_t b = 0; b < P.batch; ++b)
+          conv_shift_qk(L.conv_state + (size_t)P.C * P.Kc * b, seq_scratch(P, b), phase_tag(ph0));
+      }
+      __syncwarp();
+      if (lane == 0) st_volatile_shared(&s_ph.prepped, ph + 2);  // phases 0 .. ph + 1 formed
+      __syncwarp();
+    }
+  }
 }
 
 // ------------------------------------------------------------------ the kernel
@@ -1889,6 +2372,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
       mbar_init(&sh.empty[s], NCW);
     }
     mbar_fence_init();
+    // the consumers/helper handshake starts before any phase: nothing entered, phase 0
+    // to be formed by consumer warp 0
+    s_ph.entered = 0u;
+    s_ph.prepped = 1u;
+    s_ph.layers = Pk.layers;
+    s_dead_cta = 0u;
   }
   if (threadIdx.x < Pk.batch) s_pos[threadIdx.x] = Pk.d_pos ? Pk.d_pos[threadIdx.x] : 0;
   __syncthreads();
@@ -1898,13 +2387,19 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
     if (lane == 0) produce_all(Pk.layers);
     return;
   }
+  if (warp == NCW + 1) {
+    // ------------------------------------------------ helper: descriptions, conv shift
+    // (phase 0's descriptions are formed by consumer warp 0 before the first phase)
+    if (P.n_layers > 0) helper_loop();
+    return;
+  }
 
   // -------------------------------------------------- consumers: the phases in order
-  // Each phase runs for the batch's sequences back to back (they are independent);
-  // dependent phases are separated by a grid barrier. Between its two halves
-  // thread 0 fetches the coming phase's descriptions (the layer's, rebased to the
-  // first sequence, and the GEMV's): they do not depend on the other CTAs.
-  uint32_t itd = 0, nbar = 0, ph = 0;  // ring position | kDeadBit
+  // Each phase runs for the batch's sequences back to back (they are independent).
+  // No grid barrier: each phase waits inside for the tagged inputs it reads. Between
+  // phases warp 0 fetches the coming phase's descriptions (the layer's, rebased to
+  // the first sequence, and the GEMV's) once every warp is done with the last.
+  uint32_t itd = 0, ph = 0;  // ring position | kDeadBit; the launch's phase index
   auto mark = [&](uint32_t k) {
     if (P.trace && threadIdx.x == 0 && ph < P.trace_phases)
       P.trace[((size_t)blockIdx.x * P.trace_phases + ph) * kTraceSlots + k] = global_ns();
@@ -1913,48 +2408,67 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
     return P.trace && ph < P.trace_phases ? P.trace + ((size_t)blockIdx.x * P.trace_phases + ph) * kTraceSlots
                                           : nullptr;
   };
-  auto set_seq = [&](uint32_t l, int p, uint32_t b) {  // warp 0
-    if (p == 0 && b == 0) {  // once per layer from the parameter block, a few words per lane
-      const uint32_t* src = reinterpret_cast<const uint32_t*>(&Pk.layers[l]);
-      uint32_t* d0 = reinterpret_cast<uint32_t*>(&s_layer0);
-      uint32_t* d1 = reinterpret_cast<uint32_t*>(&s_layer);
-      for (uint32_t i = lane; i < sizeof(LayerDesc) / 4; i += 32) {
-        const uint32_t v = src[i];
-        d0[i] = v;
-        d1[i] = v;
-      }
+  // warp 0: the consumers' view of sequence b (a batch's phases other than the
+  // projections run once per sequence): its scratch block and vectors, the layer's
+  // caches rebased to it
+  auto set_seq = [&](uint32_t b) {
+    if (BATCHED) {
+      const uint32_t* src = reinterpret_cast<const uint32_t*>(&cur_layer0());
+      uint32_t* dst = reinterpret_cast<uint32_t*>(&cur_layer());
+      for (uint32_t i = lane; i < sizeof(LayerDesc) / 4; i += 32) dst[i] = src[i];
       __syncwarp();
-    } else if (BATCHED && lane == 0) {
-      s_layer = s_layer0;
-      seq_caches(P, s_layer, b);
+      if (lane == 0 && b) seq_caches(P, cur_layer(), b);
     }
     if (lane == 0) {
       s_seq.scratch = seq_scratch(P, b);
       s_seq.x_in = P.x_in + (size_t)b * P.E;
       s_seq.x_out = P.x_out + (size_t)b * P.E;
       s_seq.b = b;
-      if (phase_type(s_layer.kind, p) == kPhGemv) gemv_of(P, s_layer, l, p, b, s_gemv);
     }
+    __syncwarp();
   };
-  if (warp == 0 && P.n_layers > 0) set_seq(0, 0, 0);
+  // warp 0 at a phase's entry: wait (bounded) until the helper has formed the
+  // phase's descriptions, select their buffers, tell the helper. A wait that runs
+  // out leaves the descriptions unusable: the CTA's consumers then touch no ring
+  // tile for the rest of the launch (dead).
+  auto enter = [&](uint32_t l, uint32_t ph_) {
+    if (lane == 0) {
+      bool ok = ld_volatile_shared(&s_ph.prepped) > ph_;
+      if (!ok) {
+        const uint64_t t0 = global_ns();
+        while (!(ok = ld_volatile_shared(&s_ph.prepped) > ph_) && global_ns() - t0 <= drain_limit()) __nanosleep(64);
+      }
+      if (!ok) {
+        set_status(P.status, kStatusTimeout);
+        s_dead_cta = 1u;
+      }
+      s_sel = (ph_ & 1u) | ((l & 1u) << 1);
+      st_volatile_shared(&s_ph.entered, ph_ + 1);
+    }
+    __syncwarp();
+    set_seq(0);
+  };
+  if (warp == 0 && P.n_layers > 0) {
+    form_phase(0, 0, 0, 0);
+    enter(0, 0);
+  }
   for (uint32_t l = 0; l < P.n_layers; ++l) {
+    const uint32_t ph0 = ph;
     for (int p = 0;; ++p, ++ph) {
       if (l > 0 || p > 0) {
         mark(0);
-        grid_arrive(P);
-        if (warp == 0) set_seq(l, p, 0);
-        grid_wait(P, ++nbar * gridDim.x);
-        mark(1);
-      } else {
-        consumer_sync();
-        mark(1);
+        consumer_sync();  // every warp is done with the last phase
+        mark(13);
+        if (warp == 0) enter(l, ph);
+        mark(14);
       }
-      const int ty = phase_type(s_layer.kind, p);
+      consumer_sync();
+      if (s_dead_cta) itd |= kDeadBit;
+      mark(1);
+      const int kind = cur_layer0().kind;
+      const int ty = phase_type(kind, p);
       if (BATCHED && ty == kPhGemv) {  // every sequence in passes over the weights, on tensor cores
-        if (s_layer.kind == kLayerGDN && p == 2 && warp == NCW - 1)
-          for (uint32_t b = 0; b < P.batch; ++b)
-            conv_shift_qk(s_layer0.conv_state + (size_t)P.C * P.Kc * b, seq_scratch(P, b));
-        const uint32_t bs = s_gemv.bs, npass = s_gemv.npass;
+        const uint32_t bs = cur_gemv().bs, npass = cur_gemv().npass;
         for (uint32_t pass = 0; pass < npass; ++pass) {
           const uint32_t b0 = pass * bs, nb = min(bs, P.batch - b0);
           if (pass > 0) consumer_sync();  // every team is done with the last pass's inputs
@@ -1963,35 +2477,29 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
           itd = gemv_tiles_b(itd, b0, nb, pass == 0 ? slots() : nullptr);
           if (pass == 0) mark(12);
         }
-        mark(2);
-        if (p + 1 >= n_phases(s_layer.kind)) {
-          ++ph;
-          break;
-        }
-        continue;
-      }
-      const uint32_t nb = BATCHED ? P.batch : 1u;
-      for (uint32_t b = 0; b < nb; ++b) {
-        if (b > 0) {  // the next sequence: its descriptions, once every warp is done with the last
-          consumer_sync();
-          if (warp == 0) set_seq(l, p, b);
-          consumer_sync();
-        }
-        if (s_layer.kind == kLayerGDN && p == 2 && warp == NCW - 1) conv_shift_qk(s_layer.conv_state, s_seq.scratch);
-        if (ty == kPhGemv) {
-          gemv_prologue(slots());
-          mark(3);
-          itd = gemv_rows(itd, slots());
-        } else if (ty == kPhAttn) {
-          itd = attn_consume<D, HPW>(itd, slots());
-        } else if (ty == kPhGdn) {
-          itd = gdn_consume<DK>(itd);
-        } else {
-          combine_consume();
+      } else {
+        const uint32_t nb = BATCHED ? P.batch : 1u;
+        for (uint32_t b = 0; b < nb; ++b) {
+          if (b > 0) {  // the next sequence: its descriptions, once every warp is done with the last
+            consumer_sync();
+            if (warp == 0) set_seq(b);
+            consumer_sync();
+          }
+          if (ty == kPhGemv) {
+            gemv_prologue(slots());
+            mark(3);
+            itd = gemv_rows(itd, slots());
+          } else if (ty == kPhAttn) {
+            itd = attn_consume<D, HPW>(itd, ph, slots());
+          } else if (ty == kPhGdn) {
+            itd = gdn_consume<DK>(itd, ph);
+          } else {
+            combine_consume(ph);
+          }
         }
       }
       mark(2);
-      if (p + 1 >= n_phases(s_layer.kind)) {
+      if (p + 1 >= n_phases(kind)) {
         ++ph;
         break;
       }
@@ -1999,6 +2507,16 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
   }
   consumer_sync();
   if (P.advance && blockIdx.x == 0 && threadIdx.x < P.batch) P.advance[threadIdx.x] += 1;
+  if (P.wait_probe && threadIdx.x == 0) {  // debug: a bounded wait on a word nothing may set,
+    const uint64_t t0 = global_ns();      // after the forward's work (nothing waits on it)
+    while (ld_acquire(P.wait_probe) == 0u) {
+      if (global_ns() - t0 > P.wait_ns) {
+        set_status(P.status, kStatusTimeout);
+        break;
+      }
+      __nanosleep(256);
+    }
+  }
 }
 
 using DecodeKernel = void (*)(Program);
@@ -2053,8 +2571,11 @@ bool decode_dims_ok(const Program& p, bool has_fa, bool has_gdn, int num_sms) {
   if (p.ring_bytes + p.union_bytes + kDecFixed != (uint32_t)kDecSmem || p.ring_bytes % 128 ||
       p.ring_bytes < (uint32_t)kDecTileMax)
     return false;
+  // a CTA's row range is computed in 32 bits (rows < 2^24, CTAs <= 256), and the
+  // down projection's residual rows of a CTA are one per consumer thread at most
+  if (num_sms <= 0 || num_sms > 256 || (p.E + num_sms - 1) / num_sms > (uint32_t)NCT) return false;
   auto gemv_ok = [&](uint32_t K, uint32_t N) {
-    if (K == 0 || K % 64 || K > 12288 || N == 0 || N >= (1u << 24) || num_sms <= 0) return false;
+    if (K == 0 || K % 64 || K > 12288 || N == 0 || N >= (1u << 24)) return false;
     if (p.batch > 1) {  // tensor-core passes: one sequence's staged input fits; a tile fits
       const uint32_t R = batch_rows(K), gs = ((K / 64 + 7) / 8) * 8;
       return batch_seq_bytes(K) + kBatchPart <= room &&
@@ -2113,14 +2634,19 @@ bool decode_dims_ok(const Program& p, bool has_fa, bool has_gdn, int num_sms) {
 }
 
 bool decode_pick_split(Program& p, bool has_fa, bool has_gdn, int num_sms) {
+  bool ok = false;
   if (p.batch <= 1) {
     p.ring_bytes = kDecRingLarge;
     p.union_bytes = kDecUnionSmall;
-    if (decode_dims_ok(p, has_fa, has_gdn, num_sms)) return true;
+    ok = decode_dims_ok(p, has_fa, has_gdn, num_sms);
   }
-  p.ring_bytes = kDecRing;
-  p.union_bytes = kDecUnion;
-  return decode_dims_ok(p, has_fa, has_gdn, num_sms);
+  if (!ok) {
+    p.ring_bytes = kDecRing;
+    p.union_bytes = kDecUnion;
+    ok = decode_dims_ok(p, has_fa, has_gdn, num_sms);
+  }
+  if (ok) fill_shapes(p);
+  return ok;
 }
 
 cudaError_t decode_set_attributes() {
@@ -2145,8 +2671,16 @@ cudaError_t decode_launch(const Program& p, int num_sms, cudaStream_t stream) {
   const uint32_t Dk = (p.Dk == 32 || p.Dk == 64 || p.Dk == 128) ? p.Dk : 128;
   DecodeKernel f = pick(D, hpw ? hpw : 1, Dk, p.batch > 1);
   if (!f) return cudaErrorInvalidValue;
-  cudaError_t e = cudaMemsetAsync(p.barrier, 0, sizeof(uint32_t), stream);
-  if (e != cudaSuccess) return e;
+  // every sequence's tagged words start the launch at zero (not written yet)
+  const uint32_t tb = p.sm.tag_begin, te = p.sm.tag_end;
+  if (te > tb) {
+    cudaError_t e;
+    if (p.batch <= 1)
+      e = cudaMemsetAsync(p.scratch + tb, 0, te - tb, stream);
+    else
+      e = cudaMemset2DAsync(p.scratch + tb, p.seq_stride, 0, te - tb, p.batch, stream);
+    if (e != cudaSuccess) return e;
+  }
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;

@@ -39,12 +39,30 @@ struct LayerDesc {
   float *conv_state, *ssm;
 };
 
-// Byte offsets of the intermediates inside the scratch buffer.
+// Byte offsets of the intermediates inside the scratch buffer (from the start of
+// a sequence's block). The ones other CTAs read are tagged words: one 32-bit word
+// per element, the bf16 value in the high half and, in the low half, the tag of
+// the phase that wrote it (the launch's phase index + 1); the launch starts with
+// these words zeroed (tag 0: not written yet). They sit first in the block,
+// [tag_begin, tag_end); the attention partials (fp32, released by a per-split
+// flag word, also tagged) and the debug stage dumps (plain bf16) follow.
 struct ScratchMap {
-  uint32_t q_full, k, v, ga, o, part_o, part_ml;  // full attention
-  uint32_t dt_raw, b_raw, qkv, z, y, out;         // linear attention
-  uint32_t x_resid, g, u;                         // both
+  uint32_t q_full, k, v, ga, o, flags;        // full attention (tagged)
+  uint32_t dt_raw, b_raw, qkv, z, y, out;     // linear attention (tagged)
+  uint32_t x_resid, g, u, xa;                 // both (tagged); xa: a layer's output inside a stack
+  uint32_t tag_begin, tag_end;
+  uint32_t part_o, part_ml;                   // split-KV partials (fp32)
+  uint32_t x_norm, x_norm2, qkv_smooth, y_norm;  // debug stage dumps (bf16)
 };
+
+// The split of a GEMV phase's work that depends only on its shape (the layer kind
+// and phase), computed once per launch on the host: K-parts per row W, chunks per
+// lane cpl, rows per tile R, a batch's sequences per pass bs and passes npass. It
+// travels in the program header, which every CTA keeps in shared memory.
+struct GemvShape {
+  uint8_t W, cpl, R, bs, npass, pad[3];
+};
+constexpr int kShapeKinds = 4, kShapePhases = 6;
 
 struct Program {
   // dims
@@ -56,7 +74,11 @@ struct Program {
   uint8_t* scratch;
   ScratchMap sm;
   int* status;
-  uint32_t* barrier;  // grid-barrier counter, zero at launch
+  // bounded waits give up after wait_ns; wait_probe (debug) is a word that thread
+  // 0 of every CTA waits on at the start (bounded) until it is nonzero
+  unsigned long long wait_ns;
+  const uint32_t* wait_probe;
+  uint32_t dump;  // debug: the fused steps also store x_norm, x_norm2, qkv_smooth, y_norm
   // position: host values, or d_pos[b] (seq_len = d_pos[b] + 1) bounded by max_seq
   uint32_t pos, S, max_seq, P;
   const int32_t* d_pos;
@@ -66,22 +88,26 @@ struct Program {
   uint32_t batch, seq_stride;
   float inv_freq[128];
   // optional phase timeline: trace[(cta * trace_phases + phase) * kTraceSlots + k],
-  // k = 0 barrier arrival, 1 barrier release, 2 phase end, 3 GEMV input formed,
+  // k = 0 previous phase done, 1 phase entered, 2 phase end, 3 GEMV input formed,
   // 4 first tile in shared memory, 5 last tile in shared memory, 6 rows done
   // (globaltimer ns, thread 0), 7 first tile issued (the producer), 8 input loads
   // landed, 9 input stored, 10 row loop entered, 11 tile loop entered, 12 rows
-  // reduced; null = off
+  // reduced, 13 the previous phase done in every warp, 14 the phase's descriptions
+  // formed, 15 the GEMV input loads issued; null = off
   unsigned long long* trace;
   uint32_t trace_phases;
   // shared memory split of this launch: the tile ring's bytes and the per-phase
   // buffer's (ring_bytes + union_bytes + kDecFixed = kDecSmem)
   uint32_t ring_bytes, union_bytes;
+  // GEMV shapes by [layer kind][phase], filled by decode_pick_split
+  GemvShape shapes[kShapeKinds][kShapePhases];
   LayerDesc layers[kMaxLayers];
 };
 
 // Launch geometry and attributes.
 constexpr int kDecConsumerWarps = 12;
-constexpr int kDecThreads = (kDecConsumerWarps + 1) * 32;
+// consumers, then the producer warp, then the helper warp
+constexpr int kDecThreads = (kDecConsumerWarps + 2) * 32;
 // The tile ring: tiles of any size up to kDecTileMax sit at increasing offsets of
 // one circular buffer, at most kDecSlots in flight (one full/empty barrier pair
 // and one offset word per slot).
@@ -93,7 +119,7 @@ constexpr int kDecThreads = (kDecConsumerWarps + 1) * 32;
 constexpr int kDecRing = 174080;    // 170 KiB
 constexpr int kDecTileMax = 45056;  // 44 KiB
 constexpr int kDecSlots = 16;
-constexpr int kDecUnion = 53248;
+constexpr int kDecUnion = 51200;
 constexpr int kDecFixed = 2 * kDecSlots * 8 + 16 + 2 * kDecSlots * 4 + 1024;  // barriers, slot words, misc
 constexpr int kDecSmem = kDecRing + kDecFixed + kDecUnion;
 constexpr int kDecRingLarge = 195840;
@@ -106,13 +132,14 @@ cudaError_t dequant_launch(const uint8_t* codes, const uint16_t* scales, const u
 // Index of the largest of n bf16 values (the lowest index among equal ones) into
 // *out: one block of 1024 threads.
 cudaError_t argmax_bf16_launch(const uint16_t* v, uint32_t n, int32_t* out, cudaStream_t stream);
-// Zeroes the barrier counter, then launches the program (cooperative, one CTA per SM).
+// Zeroes the tagged words of every sequence's block, then launches the program
+// (cooperative, one CTA per SM).
 cudaError_t decode_launch(const Program& p, int num_sms, cudaStream_t stream);
 // Host check of the dims the kernel supports on a grid of num_sms CTAs; false if
 // unsupported.
 bool decode_dims_ok(const Program& p, bool has_fa, bool has_gdn, int num_sms);
 // Picks the launch's shared-memory split (the larger ring when every phase fits the
-// smaller buffer), then checks the dims; false if unsupported.
+// smaller buffer), checks the dims and fills the GEMV shapes; false if unsupported.
 bool decode_pick_split(Program& p, bool has_fa, bool has_gdn, int num_sms);
 
 }  // namespace q35

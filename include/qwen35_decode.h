@@ -214,7 +214,7 @@ QWEN35_API int qwen35_forward_linear_attention(const qwen35_config* cfg, const q
  * latency-critical path where cudaMalloc's device-wide synchronisation is not
  * acceptable. No counterpart on the pages (their forwards take caller-owned
  * scratch); it exists for those callers only.
- * Instead of caller scratch it uses one static device array of 128 KiB inside
+ * Instead of caller scratch it uses one static device array of 256 KiB inside
  * the library (QWEN35_STATIC_SCRATCH_BYTES), which every GPU that loads the
  * library keeps until the process exits. Configs whose linear-attention scratch
  * (qwen35_scratch_bytes) exceeds it are rejected with QWEN35_ERR_UNSUPPORTED.
@@ -224,12 +224,17 @@ QWEN35_API int qwen35_forward_linear_attention(const qwen35_config* cfg, const q
  * first, so calls whose work overlaps on the GPU (other streams, other host
  * threads) race on it: serialise them. Arguments and errors otherwise as
  * qwen35_forward_linear_attention. Allocates nothing (no cudaMalloc/cudaFree). */
-#define QWEN35_STATIC_SCRATCH_BYTES (128u * 1024u)
+#define QWEN35_STATIC_SCRATCH_BYTES (256u * 1024u)
 QWEN35_API int qwen35_forward_linear_attention_static(const qwen35_config* cfg,
                                                       const qwen35_gdn_layer* layer,
                                                       const qwen35_gdn_state* state,
                                                       const qwen35_bf16* x_in, qwen35_bf16* x_out,
                                                       void* stream);
+/* The device status word of that static array (as qwen35_read_device_status is
+ * for caller scratch): synchronises `stream`, then copies the status the last
+ * qwen35_forward_linear_attention_static call on the current device left (0 if
+ * none ran) into *host_status (host pointer). Allocates nothing. */
+QWEN35_API int qwen35_read_static_status(int32_t* host_status, void* stream);
 
 /* One decode step of a layer stack: layer i's output is layer i+1's input (the
  * caller's layer loop, which the module page leaves to the caller). Full-attention
@@ -310,18 +315,45 @@ QWEN35_API int qwen35_lm_head_greedy(const qwen35_config* cfg, const qwen35_bf16
 /* Byte offset inside a layer's scratch of a named intermediate the last forward of
  * that kind left there, or (size_t)-1 for an unknown name: the counterpart of the
  * intra_dump hook of "linear_attention.rs" (named buffers readable after a stream
- * synchronise). bf16 buffers, by kind:
+ * synchronise). For a stack (qwen35_decode_step) the offsets of
+ * qwen35_debug_stack_scratch_offset apply instead; both hold the last layer of
+ * that kind's values.
+ * Results handed between the kernel's CTAs are 32-bit words, one per element, the
+ * bf16 value in the HIGH 16 bits (the low 16 bits are internal):
  *   full attention:   q_full [2*H*D], k, v [Hkv*D], gated_attn [H*D], o, x_resid [hidden],
  *                     gate_act, up_act [intermediate]
  *   linear attention: dt_raw, b_raw [Hv], qkv [C], z, y [Hv*Dv], out, x_resid [hidden],
  *                     gate_act, up_act [intermediate]
- * (x_norm, x_norm2 and qkv_smooth exist only inside the fused kernels.) */
+ * The steps fused inside the kernel store plain bf16 values, and only while
+ * qwen35_debug_stage_dump is on (the page's intra_dump names): x_norm, x_norm2
+ * [hidden] (both kinds), qkv_smooth [C] and y_norm [Hv*Dv] (linear attention). */
 QWEN35_API size_t qwen35_debug_scratch_offset(const qwen35_config* cfg, int layer_kind, const char* name);
+QWEN35_API size_t qwen35_debug_stack_scratch_offset(const qwen35_config* cfg, const char* name);
+
+/* Debug: while on (nonzero), the forwards launched after this call also store the
+ * fused steps' values named above (x_norm, x_norm2, qkv_smooth, y_norm). Off by
+ * default; not thread-safe. */
+QWEN35_API int qwen35_debug_stage_dump(int on);
+
+/* Debug: every bounded wait inside the kernels of the forwards launched after this
+ * call gives up after limit_ns nanoseconds (0 restores the default of 1 s),
+ * records QWEN35_ERR_DEVICE_TIMEOUT in the status word and lets the kernel run to
+ * its end (its results are then meaningless). Copies into shared memory are always
+ * waited for at least 1 s before a CTA exits. Not thread-safe; for tests. */
+QWEN35_API int qwen35_debug_set_wait_limit(unsigned long long limit_ns);
+
+/* Debug: with a non-null device pointer d_flag (4-byte aligned), the forwards
+ * launched after this call run as usual, then thread 0 of every CTA waits (bounded
+ * by the wait limit) for *d_flag to become nonzero before the kernel exits; a flag
+ * that nothing sets makes that wait run out (QWEN35_ERR_DEVICE_TIMEOUT in the
+ * status word) while the forward's results stay valid. NULL turns it off. Not
+ * thread-safe; for tests. */
+QWEN35_API int qwen35_debug_wait_probe(const uint32_t* d_flag);
 
 /* Debug timeline of the forwards launched after this call (until it is called
  * again with NULL, 0): each CTA c (one per SM) writes, for phase f of a launch,
  * globaltimer readings (ns) at d_trace[(c * max_phases + f) * 16 + k]: k = 0
- * when it reaches the grid barrier before the phase, 1 when it leaves it, 2 when
+ * when it is done with the phase before, 1 when it enters the phase, 2 when
  * it finishes the phase; projection phases also write 3 when the phase's input
  * vector is formed and quantised, 4 and 5 when the first and the last of the
  * CTA's weight tiles is in shared memory, 6 when its rows are done; phases

@@ -66,7 +66,8 @@ def test_scratch_sizes():
     fa = B.qwen35_scratch_bytes(c4, B.QWEN35_LAYER_FULL_ATTENTION)
     gdn = B.qwen35_scratch_bytes(c4, B.QWEN35_LAYER_LINEAR_ATTENTION)
     assert fa > 0 and gdn > 0
-    assert B.qwen35_stack_scratch_bytes(c4) == max(fa, gdn)
+    # a stack keeps both kinds' intermediates apart: more than either kind alone
+    assert max(fa, gdn) < B.qwen35_stack_scratch_bytes(c4) < fa + gdn
     assert B.qwen35_scratch_bytes(c4, 7) == 0
     bad = synth.config("4b")
     bad["group_size"] = 32
@@ -86,6 +87,19 @@ def test_debug_offsets():
         assert B.qwen35_debug_scratch_offset(c, 1, n) != none, n
     assert B.qwen35_debug_scratch_offset(c, 0, "qkv") == none
     assert B.qwen35_debug_scratch_offset(c, 1, "nope") == none
+    # the fused steps' stage dumps (the page's intra_dump names)
+    for n in ["x_norm", "x_norm2"]:
+        assert B.qwen35_debug_scratch_offset(c, 0, n) != none, n
+    for n in ["x_norm", "x_norm2", "qkv_smooth", "y_norm"]:
+        assert B.qwen35_debug_scratch_offset(c, 1, n) != none, n
+    assert B.qwen35_debug_scratch_offset(c, 0, "y_norm") == none
+    # a stack's layout holds both kinds' names at distinct offsets, inside its scratch
+    names = ["q_full", "k", "v", "gated_attn", "o", "dt_raw", "b_raw", "qkv", "z", "y", "out", "x_resid",
+             "gate_act", "up_act", "x_norm", "x_norm2", "qkv_smooth", "y_norm"]
+    offs = [B.qwen35_debug_stack_scratch_offset(c, n) for n in names]
+    assert none not in offs and len(set(offs)) == len(offs)
+    assert max(offs) < B.qwen35_stack_scratch_bytes(c)
+    assert B.qwen35_debug_stack_scratch_offset(c, "nope") == none
 
 
 # ---- argument validation with fake (never dereferenced) aligned pointers
