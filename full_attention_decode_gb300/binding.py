@@ -106,6 +106,12 @@ _SIGS = {
                                              C.c_size_t, _P, _P, _P, _U, _P]),
     "qwen35_graph_create_batched": (C.c_int, [C.POINTER(qwen35_config), C.POINTER(qwen35_layer), _U, _U, _P,
                                               C.c_size_t, _P, _P, _P, _U, _P, C.POINTER(C.c_void_p)]),
+    "qwen35_forward_full_attention_batched": (C.c_int, [C.POINTER(qwen35_config), C.POINTER(qwen35_fa_layer), _U,
+                                                        _P, C.c_size_t, C.POINTER(qwen35_kv_cache), _P, _P, _P,
+                                                        _U, _P]),
+    "qwen35_forward_linear_attention_batched": (C.c_int, [C.POINTER(qwen35_config), C.POINTER(qwen35_gdn_layer),
+                                                          _U, _P, C.c_size_t, C.POINTER(qwen35_gdn_state), _P, _P,
+                                                          _P]),
     "qwen35_graph_launch": (C.c_int, [_P, _P]),
     "qwen35_graph_destroy": (C.c_int, [_P]),
     "qwen35_gemv": (C.c_int, [C.POINTER(qwen35_qweight), _P, _P, _P, C.c_size_t, _P]),
@@ -249,6 +255,19 @@ def qwen35_decode_step_batched(cfg, layers, batch, scratch, x_in, x_out, d_cache
     return lib().qwen35_decode_step_batched(C.byref(cfg), arr, len(layers), batch, _ptr(scratch), scratch.numel(),
                                             _ptr(x_in), _ptr(x_out), _ptr(d_cache_pos), max_seq_len,
                                             _stream(stream))
+
+
+def qwen35_forward_full_attention_batched(cfg, layer, batch, scratch, kv, x_in, x_out, d_cache_pos, max_seq_len,
+                                          stream=None):
+    return lib().qwen35_forward_full_attention_batched(C.byref(cfg), C.byref(layer), batch, _ptr(scratch),
+                                                       scratch.numel(), C.byref(kv), _ptr(x_in), _ptr(x_out),
+                                                       _ptr(d_cache_pos), max_seq_len, _stream(stream))
+
+
+def qwen35_forward_linear_attention_batched(cfg, layer, batch, scratch, state, x_in, x_out, stream=None):
+    return lib().qwen35_forward_linear_attention_batched(C.byref(cfg), C.byref(layer), batch, _ptr(scratch),
+                                                         scratch.numel(), C.byref(state), _ptr(x_in), _ptr(x_out),
+                                                         _stream(stream))
 
 
 class Graph:

@@ -459,12 +459,23 @@ Layout stack_layout(const Dims& d, bool has_fa, bool has_gdn) {
 }
 size_t batch_need(size_t one, uint32_t batch) { return 256 + (size_t)batch * (one - 256); }
 
+// A program of layers over a batch of sequences. `advance`: the kernel advances
+// every sequence's device position after the last layer (a decode step); the
+// per-layer batched forwards leave the positions alone, and a program without a
+// full-attention layer reads none (d_cache_pos may then be null).
 int decode_step(const qwen35_config* cfg, const qwen35_layer* layers, uint32_t num_layers, uint32_t batch,
                 void* scratch, size_t scratch_bytes, const qwen35_bf16* x_in, qwen35_bf16* x_out,
-                int32_t* d_cache_pos, uint32_t max_seq_len, cudaStream_t stream) {
-  if (!layers || num_layers == 0 || num_layers > (uint32_t)kMaxLayers || !d_cache_pos ||
-      ((uintptr_t)d_cache_pos % 4) || max_seq_len == 0 || batch == 0 || batch > (uint32_t)kMaxBatch)
+                int32_t* d_cache_pos, uint32_t max_seq_len, cudaStream_t stream, bool advance = true) {
+  if (!layers || num_layers == 0 || num_layers > (uint32_t)kMaxLayers || batch == 0 ||
+      batch > (uint32_t)kMaxBatch)
     return QWEN35_ERR_INVALID_ARGUMENT;
+  bool any_fa = false;
+  for (uint32_t i = 0; i < num_layers; ++i) any_fa |= layers[i].kind == QWEN35_LAYER_FULL_ATTENTION;
+  if (advance || any_fa) {
+    if (!d_cache_pos || ((uintptr_t)d_cache_pos % 4) || max_seq_len == 0) return QWEN35_ERR_INVALID_ARGUMENT;
+  } else if (d_cache_pos && ((uintptr_t)d_cache_pos % 4)) {
+    return QWEN35_ERR_INVALID_ARGUMENT;
+  }
   Dims d;
   int r = check_config(cfg, d);
   if (r) return r;
@@ -496,10 +507,10 @@ int decode_step(const qwen35_config* cfg, const qwen35_layer* layers, uint32_t n
   p->n_layers = num_layers;
   p->x_in = x_in;
   p->x_out = x_out;
-  p->d_pos = d_cache_pos;
-  p->max_seq = max_seq_len;
-  p->P = splits_for(max_seq_len);
-  p->advance = d_cache_pos;
+  p->d_pos = any_fa ? d_cache_pos : nullptr;
+  p->max_seq = max_seq_len ? max_seq_len : 1;
+  p->P = splits_for(p->max_seq);
+  p->advance = advance ? d_cache_pos : nullptr;
   p->batch = batch;
   p->seq_stride = (uint32_t)(one - 256);
   for (uint32_t i = 0; i < num_layers; ++i) {
@@ -523,6 +534,24 @@ int qwen35_decode_step_batched(const qwen35_config* cfg, const qwen35_layer* lay
                                qwen35_bf16* x_out, int32_t* d_cache_pos, uint32_t max_seq_len, void* stream) {
   return decode_step(cfg, layers, num_layers, batch, scratch, scratch_bytes, x_in, x_out, d_cache_pos, max_seq_len,
                      (cudaStream_t)stream);
+}
+
+int qwen35_forward_full_attention_batched(const qwen35_config* cfg, const qwen35_fa_layer* layer, uint32_t batch,
+                                          void* scratch, size_t scratch_bytes, const qwen35_kv_cache* kv,
+                                          const qwen35_bf16* x_in, qwen35_bf16* x_out, const int32_t* d_cache_pos,
+                                          uint32_t max_seq_len, void* stream) {
+  if (!layer || !kv || !d_cache_pos) return QWEN35_ERR_INVALID_ARGUMENT;
+  qwen35_layer l = {QWEN35_LAYER_FULL_ATTENTION, layer, kv, nullptr, nullptr};
+  return decode_step(cfg, &l, 1, batch, scratch, scratch_bytes, x_in, x_out, const_cast<int32_t*>(d_cache_pos),
+                     max_seq_len, (cudaStream_t)stream, false);
+}
+
+int qwen35_forward_linear_attention_batched(const qwen35_config* cfg, const qwen35_gdn_layer* layer, uint32_t batch,
+                                            void* scratch, size_t scratch_bytes, const qwen35_gdn_state* state,
+                                            const qwen35_bf16* x_in, qwen35_bf16* x_out, void* stream) {
+  if (!layer || !state) return QWEN35_ERR_INVALID_ARGUMENT;
+  qwen35_layer l = {QWEN35_LAYER_LINEAR_ATTENTION, nullptr, nullptr, layer, state};
+  return decode_step(cfg, &l, 1, batch, scratch, scratch_bytes, x_in, x_out, nullptr, 0, (cudaStream_t)stream, false);
 }
 
 size_t qwen35_stack_scratch_bytes_batched(const qwen35_config* cfg, uint32_t batch) {

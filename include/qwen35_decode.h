@@ -281,6 +281,29 @@ QWEN35_API int qwen35_decode_step_batched(const qwen35_config* cfg, const qwen35
                        uint32_t num_layers, uint32_t batch, void* scratch, size_t scratch_bytes,
                        const qwen35_bf16* x_in, qwen35_bf16* x_out,
                        int32_t* d_cache_pos, uint32_t max_seq_len, void* stream);
+/* One layer for a batch of independent sequences (the per-layer forwards above,
+ * several sequences at once; the layer's weights are streamed once, the batch's
+ * projections run on the tensor cores): sequence b computes exactly what the
+ * single-sequence forward computes for it.
+ *  - batch: 1..8; x_in, x_out [batch][hidden] (x_out may equal x_in);
+ *  - full attention: kv->k, kv->v [batch][capacity][Hkv][D]; d_cache_pos [batch]
+ *    int32 in device memory, sequence b appending at d_cache_pos[b] and attending
+ *    over d_cache_pos[b] + 1 tokens (read when the kernel runs, not advanced); a
+ *    position outside [0, min(capacity, max_seq_len)) sets QWEN35_ERR_DEVICE_RANGE
+ *    in the status word and that sequence's attention is skipped;
+ *  - linear attention: conv_state [batch][C][conv_kernel_size], gdn_state
+ *    [batch][Hv][Dv/32][Dk][32];
+ *  - scratch: qwen35_stack_scratch_bytes_batched(cfg, batch) suffices.
+ * Errors as the single-sequence forwards; batch outside 1..8 is INVALID_ARGUMENT. */
+QWEN35_API int qwen35_forward_full_attention_batched(const qwen35_config* cfg, const qwen35_fa_layer* layer,
+                                                     uint32_t batch, void* scratch, size_t scratch_bytes,
+                                                     const qwen35_kv_cache* kv, const qwen35_bf16* x_in,
+                                                     qwen35_bf16* x_out, const int32_t* d_cache_pos,
+                                                     uint32_t max_seq_len, void* stream);
+QWEN35_API int qwen35_forward_linear_attention_batched(const qwen35_config* cfg, const qwen35_gdn_layer* layer,
+                                                       uint32_t batch, void* scratch, size_t scratch_bytes,
+                                                       const qwen35_gdn_state* state, const qwen35_bf16* x_in,
+                                                       qwen35_bf16* x_out, void* stream);
 /* A CUDA graph of one qwen35_decode_step_batched (as qwen35_graph_create). */
 QWEN35_API int qwen35_graph_create_batched(const qwen35_config* cfg, const qwen35_layer* layers,
                         uint32_t num_layers, uint32_t batch, void* scratch, size_t scratch_bytes,

@@ -212,3 +212,27 @@ def test_well_formed_calls_without_a_device_fail_cleanly():
     w = B.qwen35_qweight(0x1000000, 0x2000000, 0x3000000, 1000, cfg["hidden"])
     assert B.qwen35_lm_head_greedy(c, 0x4000000, w, 0x5000000, 0x6000000, 0x7000000, _FakeScratch(4096), 0) == \
         B.QWEN35_ERR_CUDA
+
+
+def test_batched_layer_forwards_argument_errors():
+    cfg = synth.config("tiny")
+    c = B.make_config(cfg)
+    fa = _fake_fa(cfg)
+    kv = B.qwen35_kv_cache(_FAKE * 5, _FAKE * 6, 16)
+    scr = _FakeScratch(B.qwen35_stack_scratch_bytes_batched(c, 2))
+    L = B.lib()
+    import ctypes as C
+    # batch outside 1..8, missing positions, a misaligned vector: rejected before any launch
+    for batch, dpos, x in [(0, _FAKE * 9, _FAKE * 7), (9, _FAKE * 9, _FAKE * 7), (2, None, _FAKE * 7),
+                           (2, _FAKE * 9, _FAKE * 7 + 2)]:
+        rc = L.qwen35_forward_full_attention_batched(C.byref(c), C.byref(fa), batch, scr.data_ptr(), scr.numel(),
+                                                     C.byref(kv), x, _FAKE * 8, dpos, 16, None)
+        assert rc == B.QWEN35_ERR_INVALID_ARGUMENT, (batch, dpos, x)
+    # scratch too small for the batch
+    small = _FakeScratch(B.qwen35_stack_scratch_bytes_batched(c, 1))
+    rc = L.qwen35_forward_full_attention_batched(C.byref(c), C.byref(fa), 2, small.data_ptr(), small.numel(),
+                                                 C.byref(kv), _FAKE * 7, _FAKE * 8, _FAKE * 9, 16, None)
+    assert rc == B.QWEN35_ERR_INVALID_ARGUMENT
+    rc = L.qwen35_forward_linear_attention_batched(C.byref(c), None, 2, scr.data_ptr(), scr.numel(), None,
+                                                   _FAKE * 7, _FAKE * 8, None)
+    assert rc == B.QWEN35_ERR_INVALID_ARGUMENT

@@ -522,6 +522,7 @@ def _batch_case(cfg_name, n_layers, positions, cap, seeds):
 
 @pytest.mark.parametrize("cfg_name,n_layers,positions,use_graph",
                          [("tiny", 2, [0, 5, 11], False), ("tiny", 2, [3, 0, 7], True),
+                          ("tiny", 2, [0, 5, 11, 2, 7, 1, 9, 4], True),
                           ("4b", 4, [1000, 3100, 257, 2048], False)])
 def test_batch_matches_single_sequence_decodes(cfg_name, n_layers, positions, use_graph):
     # the batch's projections run on tensor cores with inputs quantised per 64
@@ -606,14 +607,18 @@ def test_batch_matches_single_sequence_decodes(cfg_name, n_layers, positions, us
         g.close()
 
 
-def test_batch_4b_teacher_forced_per_layer():
+@pytest.mark.parametrize("positions", [[1000, 3100, 257, 2048],
+                                       # the multi-sequence workload: 8 sequences, positions U{1024..65536}
+                                       [int(p) for p in synth.cache_positions(0, 8)]])
+def test_batch_4b_teacher_forced_per_layer(positions):
     """One batched step of a 4-layer 4B-shape stack (3 linear-attention layers, then
-    full attention), 4 sequences at their own positions, checked layer by layer:
-    the GPU runs the prefixes [0, i] from the same caches; the oracle applies layer i
-    to each sequence's GPU input of that layer; output, new state or appended row
-    must match at the per-layer tolerances."""
+    full attention), each sequence at its own position, checked layer by layer: the
+    GPU runs the prefixes [0, i] from the same caches; the oracle applies layer i to
+    each sequence's GPU input of that layer; output, new state or appended row must
+    match at the per-layer tolerances. With 8 sequences every n-column of the
+    tensor-core products (one per sequence) and every per-sequence cache and
+    scratch stride up to b = 7 is checked."""
     init()
-    positions = [1000, 3100, 257, 2048]
     nb, cap = len(positions), max(positions) + 8
     seeds = [30 + s for s in range(nb)]
     cfg, kinds, layers, dev, per_seq = _batch_case("4b", 4, positions, cap, seeds)
@@ -689,3 +694,71 @@ def test_batch_sequence_matches_oracle():
         assert rel_l2(O.bf16_to_f64(bits(bx_out).reshape(nb, E)[s]), ref) <= TOL_X, t
     assert rel_l2(f32(bcaches[0].ssm_matrix(s)), oc[0]["ssm"]) <= TOL_STATE
     assert B.qwen35_read_device_status(bscr) == 0
+
+
+# ------------------------------------------------------------------ per-layer batched forwards
+
+
+@pytest.mark.parametrize("cfg_name,nb", [("tiny", 3), ("4b", 8)])
+def test_linear_attention_batched_forward(cfg_name, nb):
+    """qwen35_forward_linear_attention_batched: each of nb sequences (own state, own
+    input) against the oracle's single-sequence forward, output and state."""
+    init()
+    cfg = synth.config(cfg_name)
+    c = B.make_config(cfg)
+    E = cfg["hidden"]
+    layer = synth.gdn_layer(2, 0, cfg)
+    dev = B.DeviceGdnLayer(layer)
+    states = [synth.gdn_state(40 + s, 0, cfg, std=0.1) for s in range(nb)]
+    bst = B.DeviceStateBatch([cs for cs, _ in states], [ss for _, ss in states])
+    ost = [O.state_from_arrays(cs, ss) for cs, ss in states]
+    scratch = B.new_scratch(B.qwen35_stack_scratch_bytes_batched(c, nb))
+    x_in = torch.empty(nb * E, dtype=torch.int16, device="cuda")
+    x_out = torch.empty_like(x_in)
+    for t in range(2):
+        xs = [synth.x_in(40 + s, t, cfg) for s in range(nb)]
+        x_in.copy_(B.to_device(np.concatenate(xs)))
+        assert B.qwen35_forward_linear_attention_batched(c, dev.struct, nb, scratch, bst.struct, x_in, x_out) == 0
+        torch.cuda.synchronize()
+        got = O.bf16_to_f64(bits(x_out).reshape(nb, E))
+        for s in range(nb):
+            ref = O.forward_linear_attention(cfg, layer, ost[s], O.bf16_to_f64(xs[s]))
+            assert rel_l2(got[s], ref) <= TOL_X, (t, s)
+    for s in range(nb):
+        assert rel_l2(f32(bst.ssm_matrix(s)), ost[s]["ssm"]) <= TOL_STATE, s
+        assert rel_l2(f32(bst.conv[s]), ost[s]["conv"]) <= TOL_STATE, s
+    assert B.qwen35_read_device_status(scratch) == 0
+
+
+@pytest.mark.parametrize("cfg_name,positions", [("tiny", [0, 5, 11]), ("4b", [300, 4095, 1024, 2047, 17, 999, 3000, 511])])
+def test_full_attention_batched_forward(cfg_name, positions):
+    """qwen35_forward_full_attention_batched: each sequence at its own device position
+    against the oracle's single-sequence forward (output, appended row), and the
+    positions left as they were."""
+    init()
+    cfg = synth.config(cfg_name)
+    c = B.make_config(cfg)
+    E, D = cfg["hidden"], cfg["head_dim"]
+    nb, cap = len(positions), max(positions) + 4
+    layer = synth.fa_layer(3, 1, cfg)
+    dev = B.DeviceFaLayer(layer)
+    kvs = [synth.kv_cache(50 + s, 1, cfg, cap, p) for s, p in enumerate(positions)]
+    bkv = B.DeviceKvBatch([k for k, _ in kvs], [v for _, v in kvs])
+    scratch = B.new_scratch(B.qwen35_stack_scratch_bytes_batched(c, nb))
+    x_in = torch.empty(nb * E, dtype=torch.int16, device="cuda")
+    x_out = torch.empty_like(x_in)
+    dpos = torch.tensor(positions, dtype=torch.int32, device="cuda")
+    xs = [synth.x_in(50 + s, 0, cfg) for s in range(nb)]
+    x_in.copy_(B.to_device(np.concatenate(xs)))
+    assert B.qwen35_forward_full_attention_batched(c, dev.struct, nb, scratch, bkv.struct, x_in, x_out, dpos, cap) == 0
+    torch.cuda.synchronize()
+    got = O.bf16_to_f64(bits(x_out).reshape(nb, E))
+    for s, p in enumerate(positions):
+        tr = {}
+        ref = O.forward_full_attention(cfg, layer, O.kv_from_bits(*kvs[s]), O.bf16_to_f64(xs[s]), p, p + 1, tr)
+        assert rel_l2(got[s], ref) <= TOL_X, s
+        assert rel_l2(f64(bkv.k)[s][p], tr["k_rope"]) <= TOL_X, s
+        assert rel_l2(f64(bkv.v)[s][p], tr["v"].reshape(-1, D)) <= TOL_X, s
+        assert not np.any(bits(bkv.k)[s][p + 1:])  # nothing above the append
+    assert dpos.tolist() == positions  # a per-layer forward does not advance the positions
+    assert B.qwen35_read_device_status(scratch) == 0
