@@ -177,6 +177,27 @@ def kv_cache(seed: int, layer: int, cfg: dict, capacity: int, n_prefill: int, se
     return k, v
 
 
+def kv_cache_turbo8(seed: int, layer: int, cfg: dict, capacity: int, n_prefill: int, seq: int = 0):
+    """A Turbo8 KV cache (FP8 E4M3 codes [capacity][Hkv][D], bf16 scales
+    [capacity][Hkv][D/16] for K and for V) with rows [0, n_prefill) drawn at random:
+    codes U over the 254 finite E4M3 codes, scales bf16(U(0.5, 1.5) * 2 / 448) (the
+    size a group of N(0, 1) values gets); zero above. Returns (k_codes, k_scales,
+    v_codes, v_scales)."""
+    Hkv, D = cfg["num_kv_heads"], cfg["head_dim"]
+    out = []
+    for part in ("k", "v"):
+        codes = np.zeros((capacity, Hkv, D), dtype=np.uint8)
+        scales = np.zeros((capacity, Hkv, D // 16), dtype=np.uint16)
+        if n_prefill:
+            r = _rng(seed, "kv_turbo8", part, seq, layer)
+            c = r.integers(0, 254, size=(n_prefill, Hkv, D), dtype=np.int64)
+            c = np.where(c >= 0x7F, c + 1, c)  # skip 0x7F (not a number); 0xFF is never drawn
+            codes[:n_prefill] = c.astype(np.uint8)
+            scales[:n_prefill] = to_bf16_bits(r.uniform(0.5, 1.5, size=(n_prefill, Hkv, D // 16)) * (2.0 / 448.0))
+        out += [codes, scales]
+    return tuple(out)
+
+
 def gdn_state(seed: int, layer: int, cfg: dict, std: float = 0.0, seq: int = 0):
     """(conv_state fp32 [C][Kc] zero, gdn_state fp32 [Hv][Dk][Dv] N(0, std))."""
     Hk, Hv = cfg["num_k_heads_lin"], cfg["num_v_heads_lin"]

@@ -15,8 +15,9 @@ where the pages keep it in a bf16 buffer, and to fp32 where they keep it fp32
 (gate, beta, conv1d_state, gdn_state). Where the pages leave a step open, the
 reading taken is named in the docstring ("Reading: ...").
 
-Pins (see tests/test_oracle_pins.py): every function below is checked against
-closed forms, special cases, library routines or brute force. None is unpinned.
+Pins (see tests/test_oracle_pins.py, tests/test_oracle_composition.py and
+tests/test_oracle_turbo8.py): every function below is checked against closed
+forms, special cases, library routines or brute force. None is unpinned.
 """
 
 from __future__ import annotations
@@ -254,6 +255,107 @@ def gated_delta_rule(state, q, k, v, g, beta, Dk: int):
 
 
 # ----------------------------------------------------------------------------
+# Turbo8 KV cache (mod.rs: MetalKvDtype::Turbo8; full_attention.rs: Turbo path)
+# ----------------------------------------------------------------------------
+
+E4M3_MAX = 448.0  # the largest finite FP8 E4M3 value, 1.75 * 2^8
+
+
+def wht(x) -> np.ndarray:
+    """Orthonormal Walsh-Hadamard transform along the last axis (length a power of 2).
+
+    full_attention.rs rotates K and V before the Turbo append, Q before attention
+    and the attention output back after it (wht / wht_inv). Reading: the Sylvester
+    ordering H_2n = [[H, H], [H, -H]] with the orthonormal factor 1/sqrt(n), so the
+    transform is its own inverse and keeps dot products (the pages name no
+    normalisation; this is the one under which rotating both q and K leaves the
+    scores unchanged). Written as the butterfly: each stage pairs elements h apart.
+    """
+    y = np.array(x, dtype=np.float64, copy=True)
+    n = y.shape[-1]
+    h = 1
+    while h < n:
+        a = y.reshape(y.shape[:-1] + (n // (2 * h), 2, h))
+        lo = a[..., 0, :].copy()
+        hi = a[..., 1, :].copy()
+        a[..., 0, :] = lo + hi
+        a[..., 1, :] = lo - hi
+        h *= 2
+    return y / np.sqrt(np.float64(n))
+
+
+def e4m3_round(x) -> np.ndarray:
+    """Round to the nearest FP8 E4M3 value, ties to even, saturating at +-448.
+
+    E4M3: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits; normal values
+    (1 + m/8) 2^(e-7) for e = 1..15 (e = 15, m = 7 is not a number, so 448 is the
+    largest finite value), subnormal values (m/8) 2^-6. Reading (the pages print
+    the format, not its rounding): round to nearest even with saturation to the
+    largest finite value (no infinities or NaN from finite inputs).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    _, e = np.frexp(a)                 # a = f 2^e, 0.5 <= f < 1; the binade's step is 2^(e-4)
+    step = np.ldexp(1.0, np.maximum(e - 4, -9))   # subnormal step 2^-9
+    r = np.rint(a / step) * step
+    r = np.minimum(r, E4M3_MAX)
+    return np.copysign(r, x)
+
+
+def e4m3_bits(x) -> np.ndarray:
+    """E4M3 values (already representable) -> their 8-bit codes."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    sign = (np.signbit(x)).astype(np.uint8) << 7
+    _, e = np.frexp(a)
+    exp = np.clip(e - 1 + 7, 0, 15)              # biased exponent of a normal value
+    normal = (a >= 2.0 ** -6)
+    mant_n = np.where(normal, np.rint((a / np.ldexp(1.0, e - 1) - 1.0) * 8), 0)
+    mant_s = np.rint(a / 2.0 ** -9)              # subnormal: a = m 2^-9
+    code = np.where(normal, (exp.astype(np.int64) << 3) | mant_n.astype(np.int64), mant_s.astype(np.int64))
+    return (code.astype(np.uint8) | sign).astype(np.uint8)
+
+
+def e4m3_value(bits) -> np.ndarray:
+    """8-bit E4M3 codes -> values (code 0x7F / 0xFF, not a number, never produced here)."""
+    b = np.asarray(bits, dtype=np.uint8).astype(np.int64)
+    s = np.where(b & 0x80, -1.0, 1.0)
+    e = (b >> 3) & 0xF
+    m = b & 7
+    v = np.where(e == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * np.ldexp(1.0, e - 7))
+    return s * v
+
+
+def turbo8_quantize(x):
+    """Quantise rows of bf16 values in groups of 16: (E4M3 codes, bf16 scales).
+
+    mod.rs, Turbo8: FP8 E4M3 data and a BF16 scale per group of 16 (1.125 bytes per
+    element). Reading (the pages do not print the kernel): the group's scale is
+    bf16(fp32(amax / 448)), so that the largest element maps to the top of the E4M3
+    range, and each element's code is the E4M3 rounding of the fp32 quotient
+    fp32(x / scale); a group of zeros has scale 0 and codes 0. The quotient is
+    formed in fp32 because that is the precision the kernel decides the code in.
+    Returns (codes uint8 [..., n], scales float64 [..., n / 16] holding bf16 values).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    g = x.reshape(x.shape[:-1] + (x.shape[-1] // 16, 16))
+    amax = np.max(np.abs(g), axis=-1)
+    scale = bf16_round(f32_round(amax / E4M3_MAX))
+    safe = np.where(scale > 0, scale, 1.0)
+    q = f32_round(g.astype(np.float32).astype(np.float64) / safe[..., None])
+    q = np.where(scale[..., None] > 0, q, 0.0)
+    codes = e4m3_bits(e4m3_round(q))
+    return codes.reshape(x.shape), scale
+
+
+def turbo8_dequantize(codes, scales) -> np.ndarray:
+    """codes [..., n] and bf16 scales [..., n / 16] -> values code * scale (exact in float64)."""
+    v = e4m3_value(codes)
+    s = np.asarray(scales, dtype=np.float64)
+    return (v.reshape(s.shape + (16,)) * s[..., None]).reshape(v.shape)
+
+
+# ----------------------------------------------------------------------------
 # The two layer forwards
 # ----------------------------------------------------------------------------
 
@@ -295,10 +397,28 @@ def forward_full_attention(cfg: dict, layer: dict, kv: dict, x_in, cache_pos: in
     inv_freq = rope_inv_freq(cfg["rope_theta"], R)
     q_r = bf16_round(rope_apply(q_n, cache_pos, inv_freq, R))
     k_r = bf16_round(rope_apply(k_n, cache_pos, inv_freq, R))
-    # KV append at cache_pos (bf16 cache), then attention over seq_len_attn tokens
-    kv["k"][cache_pos] = k_r
-    kv["v"][cache_pos] = v.reshape(Hkv, D)
-    attn = bf16_round(attention_decode(q_r, kv["k"], kv["v"], seq_len_attn, Hkv))
+    if kv.get("dtype") == "turbo8":
+        # Turbo path: K and V rotated (bf16, in place on the page) before the
+        # quantising append, Q rotated before attention; the dequantising attention
+        # runs in the rotated basis and its output is rotated back (bf16 each time).
+        # Reading: no sparse-V gate (the page's threshold 0.0 disables it).
+        k_rot = bf16_round(wht(k_r))
+        v_rot = bf16_round(wht(v.reshape(Hkv, D)))
+        kc, ks = turbo8_quantize(k_rot)
+        vc, vs = turbo8_quantize(v_rot)
+        kv["k_codes"][cache_pos], kv["k_scales"][cache_pos] = kc, ks
+        kv["v_codes"][cache_pos], kv["v_scales"][cache_pos] = vc, vs
+        q_rot = bf16_round(wht(q_r))
+        K = turbo8_dequantize(kv["k_codes"][:seq_len_attn], kv["k_scales"][:seq_len_attn])
+        V = turbo8_dequantize(kv["v_codes"][:seq_len_attn], kv["v_scales"][:seq_len_attn])
+        attn_rot = bf16_round(attention_decode(q_rot, K, V, seq_len_attn, Hkv))
+        attn = bf16_round(wht(attn_rot))
+        t.update(k_rot=k_rot, v_rot=v_rot, q_rot=q_rot, attn_rot=attn_rot)
+    else:
+        # KV append at cache_pos (bf16 cache), then attention over seq_len_attn tokens
+        kv["k"][cache_pos] = k_r
+        kv["v"][cache_pos] = v.reshape(Hkv, D)
+        attn = bf16_round(attention_decode(q_r, kv["k"], kv["v"], seq_len_attn, Hkv))
     # sigmoid gate
     gated = bf16_round(attn * sigmoid(gate))
     # o_proj
@@ -428,6 +548,13 @@ def lm_head_greedy(cfg: dict, head: dict, x_in, rows_per_chunk: int = 4096) -> t
 
 def kv_from_bits(k_bits, v_bits) -> dict:
     return {"k": bf16_to_f64(k_bits), "v": bf16_to_f64(v_bits)}
+
+
+def turbo8_kv(k_codes, k_scale_bits, v_codes, v_scale_bits) -> dict:
+    """A Turbo8 cache for the oracle: codes uint8 [cap][Hkv][D], scales as float64
+    [cap][Hkv][D / 16] (bf16 values)."""
+    return {"dtype": "turbo8", "k_codes": np.array(k_codes, dtype=np.uint8), "v_codes": np.array(v_codes, dtype=np.uint8),
+            "k_scales": bf16_to_f64(k_scale_bits), "v_scales": bf16_to_f64(v_scale_bits)}
 
 
 def state_from_arrays(conv, ssm) -> dict:
