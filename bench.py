@@ -81,7 +81,7 @@ def _peaks():
         return 6800.0, "fallback"
 
 
-def algorithmic_bytes(cfg: dict, seq_len: int, kinds: list | None = None) -> dict:
+def algorithmic_bytes(cfg: dict, seq_len: int, kinds: list | None = None, kv_dtype: str = "bf16") -> dict:
     """Bytes a decode step must move: every weight, scale and bias once, K/V rows
     [0, seq_len) once per full-attention layer plus the appended row, GDN and conv
     state read and written once, norm vectors and the small per-head vectors."""
@@ -99,7 +99,9 @@ def algorithmic_bytes(cfg: dict, seq_len: int, kinds: list | None = None) -> dic
     gdn_w = q(Hv, E) * 2 + q(C, E) + q(Hv * Dv, E) + q(E, Hv * Dv) + mlp + 2 * (2 * E + Dv) + \
         Hv * (4 + 2) + C * Kc * 2
     gdn_state = 2 * (Hv * Dk * Dv * 4 + C * Kc * 4)
-    kv = lambda S: 2 * S * Hkv * D * 2 + 2 * Hkv * D * 2  # noqa: E731
+    # per token and kv-head: bf16 rows, or Turbo8 codes plus one bf16 scale per 16
+    row = D * 2 if kv_dtype == "bf16" else D + D // 8
+    kv = lambda S: 2 * S * Hkv * row + 2 * Hkv * row  # noqa: E731
     kinds = kinds if kinds is not None else synth.layer_kinds(cfg)
     n_fa = kinds.count("fa")
     n_gdn = kinds.count("gdn")
@@ -224,10 +226,24 @@ def run_gpu(args) -> dict | None:
     gen = torch.Generator(device="cuda")
     gen.manual_seed(seed)
     device_fill = nb > 1 or args.prefill != PREFILL  # large caches: filled on the device (seeded)
+    t8 = args.kv == "turbo8"
     for i, kind in enumerate(kinds):
         if kind == "fa":
             dl = B.DeviceFaLayer(synth.fa_layer(seed, i, cfg))
-            if device_fill:
+            if t8:  # Turbo8 caches filled on the device: finite E4M3 codes, scales of N(0, 1) groups
+                Hkv, D = cfg["num_kv_heads"], cfg["head_dim"]
+                cc = B.DeviceKvBatch.__new__(B.DeviceKvBatch)
+                codes = []
+                for _ in range(2):
+                    c8 = torch.randint(0, 254, (nb, cap, Hkv, D), generator=gen, device="cuda", dtype=torch.int16)
+                    codes.append(torch.where(c8 >= 0x7F, c8 + 1, c8).to(torch.uint8))
+                ss = B.turbo8_sstride(cfg)
+                scl = [(torch.rand((nb, cap, ss), generator=gen, device="cuda") + 0.5) * (2.0 / 448.0) for _ in range(2)]
+                cc.k, cc.v = codes
+                cc.ks, cc.vs = [x.to(torch.bfloat16).view(torch.int16) for x in scl]
+                cc.struct = B.qwen35_kv_cache(cc.k.data_ptr(), cc.v.data_ptr(), cap, B.QWEN35_KV_TURBO8,
+                                              cc.ks.data_ptr(), cc.vs.data_ptr())
+            elif device_fill:
                 shape = (nb, cap, cfg["num_kv_heads"], cfg["head_dim"])
                 cc = B.DeviceKvBatch.__new__(B.DeviceKvBatch)
                 cc.k = torch.randn(shape, generator=gen, device="cuda", dtype=torch.bfloat16).view(torch.int16)
@@ -355,12 +371,13 @@ def run_gpu(args) -> dict | None:
 
     peak, peak_kind = _peaks()
     mid = args.warmup + args.steps // 2 + 1  # tokens each sequence gained by mid-run
-    per_seq = [algorithmic_bytes(cfg, p + mid, kinds) for p in positions]
+    per_seq = [algorithmic_bytes(cfg, p + mid, kinds, args.kv) for p in positions]
     kv_seq = [a["step"] - a["weights"] - a["gdn_state_all"] for a in per_seq]
     ab = dict(per_seq[0])
     ab["step"] = per_seq[0]["weights"] + sum(kv_seq) + nb * per_seq[0]["gdn_state_all"]
     seq_mid = positions[0] + mid
-    traffic, traffic_note = profiled_traffic(ab["step"]) if nb == 1 and args.prefill == PREFILL else (None, "not captured")
+    traffic, traffic_note = profiled_traffic(ab["step"]) if nb == 1 and args.prefill == PREFILL and not t8 \
+        else (None, "not captured")
     tok_s = job_tok_s(ms, world, nb)
     step_gbs = ab["step"] / (ms * 1e-3) / 1e9
     gemv_gbs = gemv_bytes / (gemv_ms * 1e-3) / 1e9
@@ -369,8 +386,10 @@ def run_gpu(args) -> dict | None:
         "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int8-weight/bf16-act/fp32-acc", "data": "synthetic",
         "config": {"workload": ("qwen3.5-4b-shape 32-layer decode stack, batch 1, KV prefilled to 8192" if nb == 1
-                                and args.prefill == PREFILL else
-                                f"qwen3.5-4b-shape 32-layer decode stack, batch {nb}, KV prefilled to {positions}"),
+                                and args.prefill == PREFILL and not t8 else
+                                f"qwen3.5-4b-shape 32-layer decode stack, batch {nb}, KV prefilled to {positions}"
+                                + (", Turbo8 KV cache" if t8 else "")),
+                   "kv_dtype": args.kv,
                    "batch": nb, "positions": positions,
                    "layers": "24 gated-deltanet + 8 full-attention (i % 4 == 3)",
                    "context": [pos0 + 1, pos0 + args.steps], "global_batch": world, "seq_len": seq_mid,
@@ -496,6 +515,7 @@ def main():
     ap.add_argument("--stack-only", action="store_true", help="graph replays only (for ncu captures)")
     ap.add_argument("--batch", type=int, default=1, help="sequences per step (multi-sequence workload)")
     ap.add_argument("--prefill", type=int, default=PREFILL, help="KV tokens before the first step (batch 1)")
+    ap.add_argument("--kv", choices=["bf16", "turbo8"], default="bf16", help="KV cache format")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -67,8 +67,13 @@ class qwen35_gdn_layer(C.Structure):
                 ("up_proj", qwen35_qweight), ("down_proj", qwen35_qweight)]
 
 
+QWEN35_KV_BF16 = 0
+QWEN35_KV_TURBO8 = 1
+
+
 class qwen35_kv_cache(C.Structure):
-    _fields_ = [("k", C.c_void_p), ("v", C.c_void_p), ("capacity", C.c_uint32)]
+    _fields_ = [("k", C.c_void_p), ("v", C.c_void_p), ("capacity", C.c_uint32), ("dtype", C.c_uint32),
+                ("k_scales", C.c_void_p), ("v_scales", C.c_void_p)]
 
 
 class qwen35_gdn_state(C.Structure):
@@ -324,7 +329,7 @@ def qwen35_debug_stack_scratch_offset(cfg, name: str) -> int:
 # the fused steps' values, stored as plain bf16 while the stage dump is on; every
 # other named intermediate is a 32-bit word per element with the bf16 value in its
 # high half
-STAGE_DUMPS = ("x_norm", "x_norm2", "qkv_smooth", "y_norm")
+STAGE_DUMPS = ("x_norm", "x_norm2", "qkv_smooth", "y_norm", "k_rot", "v_rot")
 
 
 def scratch_view(scratch: torch.Tensor, cfg, kind, name: str, n: int, seq: int = 0, seq_stride: int = 0) -> torch.Tensor:
@@ -442,6 +447,42 @@ class DeviceState:
         """The state as [Hv][Dk][Dv] (a device tensor)."""
         hv, dk, dv = self.shape
         return self.ssm.view(hv, dv // 32, dk, 32).permute(0, 2, 1, 3).reshape(hv, dk, dv)
+
+
+def turbo8_sstride(cfg: dict) -> int:
+    """Row stride, in bf16 elements, of a Turbo8 cache's scale arrays."""
+    return ((cfg["num_kv_heads"] * cfg["head_dim"] // 16 + 7) // 8) * 8
+
+
+def _pad_scales(s: np.ndarray, sstride: int) -> np.ndarray:
+    """[..., cap, Hkv, D/16] bf16 scales -> [..., cap, sstride] (padded rows)."""
+    flat = s.reshape(s.shape[:-2] + (-1,))
+    out = np.zeros(flat.shape[:-1] + (sstride,), dtype=np.uint16)
+    out[..., :flat.shape[-1]] = flat
+    return out
+
+
+class DeviceKvTurbo8:
+    """A Turbo8 cache on the device from (k_codes, k_scales, v_codes, v_scales) with
+    codes [cap][Hkv][D] and scales [cap][Hkv][D/16]; the scales are stored in rows
+    padded to the library's stride."""
+
+    def __init__(self, k_codes, k_scales, v_codes, v_scales, cfg: dict, device="cuda"):
+        ss = turbo8_sstride(cfg)
+        self.shape = k_scales.shape
+        self.k = to_device(np.ascontiguousarray(k_codes), device)
+        self.v = to_device(np.ascontiguousarray(v_codes), device)
+        self.ks = to_device(_pad_scales(k_scales, ss), device)
+        self.vs = to_device(_pad_scales(v_scales, ss), device)
+        self.struct = qwen35_kv_cache(self.k.data_ptr(), self.v.data_ptr(), k_codes.shape[-3], QWEN35_KV_TURBO8,
+                                      self.ks.data_ptr(), self.vs.data_ptr())
+
+    def scales(self, which: str) -> np.ndarray:
+        """The scales back as [..., cap, Hkv, D/16] bf16 bits."""
+        t = self.ks if which == "k" else self.vs
+        a = t.cpu().numpy().view(np.uint16)
+        n = self.shape[-2] * self.shape[-1]
+        return a[..., :n].reshape(a.shape[:-1] + self.shape[-2:])
 
 
 class DeviceKvBatch:

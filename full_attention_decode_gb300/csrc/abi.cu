@@ -132,6 +132,10 @@ Layout layout(const Dims& d, int kinds) {
   }
   L.m.x_norm = b.take((size_t)d.E * 2);
   L.m.x_norm2 = b.take((size_t)d.E * 2);
+  if (kinds & kHasFa) {
+    L.m.k_rot = b.take((size_t)d.Hkv * d.D * 2);
+    L.m.v_rot = b.take((size_t)d.Hkv * d.D * 2);
+  }
   if (kinds & kHasGdn) {
     L.m.qkv_smooth = b.take((size_t)d.C * 2);
     L.m.y_norm = b.take((size_t)d.Z * 2);
@@ -149,6 +153,15 @@ QMat qm(const qwen35_qweight& w) {
   m.n = w.n;
   m.pad = 0;
   return m;
+}
+
+// The cache of a full-attention layer: aligned pointers, a known format (Turbo8:
+// scale arrays too).
+bool kv_ok(const qwen35_kv_cache* kv) {
+  if (!kv || !aligned16(kv->k) || !aligned16(kv->v) || kv->capacity == 0) return false;
+  if (kv->dtype == QWEN35_KV_BF16) return true;
+  if (kv->dtype == QWEN35_KV_TURBO8) return aligned16(kv->k_scales) && aligned16(kv->v_scales);
+  return false;
 }
 
 int check_fa_layer(const qwen35_fa_layer* l, const Dims& d) {
@@ -189,8 +202,11 @@ void fill_fa(LayerDesc& L, const qwen35_fa_layer* l, const qwen35_kv_cache* kv) 
   L.post_ln = l->post_ln;
   L.q_norm = l->q_norm;
   L.k_norm = l->k_norm;
-  L.kc = kv->k;
-  L.vc = kv->v;
+  L.kc = static_cast<uint8_t*>(kv->k);
+  L.vc = static_cast<uint8_t*>(kv->v);
+  L.kv_dtype = kv->dtype;
+  L.ks = kv->k_scales;
+  L.vs = kv->v_scales;
 }
 
 void fill_gdn(LayerDesc& L, const qwen35_gdn_layer* l, const qwen35_gdn_state* st) {
@@ -271,7 +287,7 @@ int fa_forward(const qwen35_config* cfg, const qwen35_fa_layer* layer, void* scr
   if (r) return r;
   if ((r = check_fa_dims(cfg, d))) return r;
   if ((r = check_fa_layer(layer, d))) return r;
-  if (!kv || !aligned16(kv->k) || !aligned16(kv->v) || kv->capacity == 0) return QWEN35_ERR_INVALID_ARGUMENT;
+  if (!kv_ok(kv)) return QWEN35_ERR_INVALID_ARGUMENT;
   if (!aligned16(x_in) || !aligned16(x_out) || !aligned16(scratch)) return QWEN35_ERR_INVALID_ARGUMENT;
   const Layout lay = layout(d, kHasFa);
   if (scratch_bytes < lay.total) return QWEN35_ERR_INVALID_ARGUMENT;
@@ -483,8 +499,7 @@ int decode_step(const qwen35_config* cfg, const qwen35_layer* layers, uint32_t n
   for (uint32_t i = 0; i < num_layers; ++i) {
     const qwen35_layer& l = layers[i];
     if (l.kind == QWEN35_LAYER_FULL_ATTENTION) {
-      if (!l.fa || !l.kv || !aligned16(l.kv->k) || !aligned16(l.kv->v) || l.kv->capacity == 0)
-        return QWEN35_ERR_INVALID_ARGUMENT;
+      if (!l.fa || !kv_ok(l.kv)) return QWEN35_ERR_INVALID_ARGUMENT;
       if ((r = check_fa_dims(cfg, d)) || (r = check_fa_layer(l.fa, d))) return r;
       has_fa = true;
     } else if (l.kind == QWEN35_LAYER_LINEAR_ATTENTION) {
@@ -641,7 +656,8 @@ size_t named_offset(const ScratchMap& m, int kind, const char* name) {
                        {"b_raw", m.b_raw, G},      {"qkv", m.qkv, G},      {"z", m.z, G},
                        {"y", m.y, G},              {"out", m.out, G},      {"x_resid", m.x_resid, -1},
                        {"gate_act", m.g, -1},      {"up_act", m.u, -1},    {"x_norm", m.x_norm, -1},
-                       {"x_norm2", m.x_norm2, -1}, {"qkv_smooth", m.qkv_smooth, G}, {"y_norm", m.y_norm, G}};
+                       {"x_norm2", m.x_norm2, -1}, {"qkv_smooth", m.qkv_smooth, G}, {"y_norm", m.y_norm, G},
+                       {"k_rot", m.k_rot, F},      {"v_rot", m.v_rot, F}};
   for (const Named& e : tab)
     if ((kind == -1 || e.kind == kind || e.kind == -1) && std::strcmp(e.n, name) == 0) return e.off;
   return (size_t)-1;

@@ -59,7 +59,9 @@ constexpr int kTS = 8;      // tokens per attention tile
 constexpr int kMaxKc = 8;
 
 enum PhaseType { kPhGemv = 0, kPhAttn = 1, kPhCombine = 2, kPhGdn = 3 };
-enum Pro { kPlain = 0, kRms = 1, kAddRms = 2, kSiluMul = 3, kHeadNormSilu = 4 };
+// kWhtGate: a Turbo8 layer's o_proj input: the attention output, in the cache's
+// rotated basis, rotated back per head (bf16), times sigmoid(gate) (bf16)
+enum Pro { kPlain = 0, kRms = 1, kAddRms = 2, kSiluMul = 3, kHeadNormSilu = 4, kWhtGate = 5 };
 
 __device__ __forceinline__ int n_phases(int kind) { return kind == kLayerFA ? 6 : kind == kLayerGDN ? 5 : 1; }
 __device__ __forceinline__ int phase_type(int kind, int p) {
@@ -137,15 +139,25 @@ struct SeqCtx {
 __shared__ SeqCtx s_seq;
 __shared__ int32_t s_pos[kMaxBatch];  // each sequence's device position, read at launch
 
+// Row stride, in bf16 elements, of a Turbo8 cache's scales: one per 16 elements of
+// a token's row, padded to 16 bytes.
+__host__ __device__ inline uint32_t turbo8_sstride(uint32_t Hkv, uint32_t D) { return (Hkv * D / 16 + 7) / 8 * 8; }
+
 // Sequence b's scratch block and its caches in layer L (the caller's [B][...] arrays).
 __device__ __forceinline__ uint8_t* seq_scratch(const Program& P, uint32_t b) {
   return P.scratch + (size_t)b * P.seq_stride;
 }
 __device__ __forceinline__ void seq_caches(const Program& P, LayerDesc& L, uint32_t b) {
   if (L.kind == kLayerFA) {
-    const size_t kv = (size_t)L.capacity * P.Hkv * P.D * b;
+    const bool t8 = L.kv_dtype == kKvTurbo8;
+    const size_t kv = (size_t)L.capacity * P.Hkv * P.D * (t8 ? 1 : 2) * b;  // bytes
     L.kc += kv;
     L.vc += kv;
+    if (t8) {
+      const size_t sc = (size_t)L.capacity * turbo8_sstride(P.Hkv, P.D) * b;
+      L.ks += sc;
+      L.vs += sc;
+    }
   } else if (L.kind == kLayerGDN) {
     L.conv_state += (size_t)P.C * P.Kc * b;
     L.ssm += (size_t)P.Hv * P.Dk * P.Dv * b;
@@ -619,6 +631,13 @@ __device__ __noinline__ void gemv_of(const Program& P, const LayerDesc& L, uint3
     g.a = tw(m.ga);
     g.tag_a = phase_tag(ph0 + 2);
     g.sa = SS;
+    if (L.kv_dtype == kKvTurbo8) {  // the attention output is still rotated: back, then the gate
+      g.pro = kWhtGate;
+      g.b = tw(m.q_full);  // head h's gate at q_full[h * 2D + D + d]
+      g.tag_b = phase_tag(ph0);
+      g.sb = SS;
+      g.head_dim = P.D;
+    }
     gemv_add(g, L.m[3], tw(m.o), SS);
   } else {  // p == 2: out_proj on silu(z) * RMSNorm_head(y)
     g.K = P.Z;
@@ -749,8 +768,12 @@ __device__ __noinline__ void gemv_prologue(unsigned long long* tr) {
   uint4* qhi = reinterpret_cast<uint4*>(sh.uni);
   uint4* qlo = qhi + nch;
   float4* aux = reinterpret_cast<float4*>(qlo + nch);
-  const bool has_b = g.pro == kAddRms || g.pro == kSiluMul || g.pro == kHeadNormSilu;
+  const bool has_b = g.pro == kAddRms || g.pro == kSiluMul || g.pro == kHeadNormSilu || g.pro == kWhtGate;
   const bool has_w = g.pro == kAddRms || g.pro == kRms || g.pro == kHeadNormSilu;
+  // chunk c of input b (kWhtGate: head h's gate chunk sits at q_full[h * 2D + D + ...])
+  auto bchunk = [&](uint32_t c) {
+    return g.pro == kWhtGate ? c + ((16 * c) / g.head_dim + 1) * (g.head_dim / 16) : c;
+  };
   // every global load of the prologue is issued before any is used: one round trip
   Chunk16 ca[2], cb[2];
   uint4 pw[2][2];
@@ -763,7 +786,7 @@ __device__ __noinline__ void gemv_prologue(unsigned long long* tr) {
     pw[q][0] = pw[q][1] = z;
     if (c < nch) {
       chunk_issue(g.a, g.tag_a, c, ca[q]);
-      if (has_b) chunk_issue(g.b, g.tag_b, c, cb[q]);
+      if (has_b) chunk_issue(g.b, g.tag_b, bchunk(c), cb[q]);
       if (has_w) {
         const uint32_t wi = g.pro == kHeadNormSilu ? (c * 16) % g.head_dim : c * 16;
         const uint4* wp = reinterpret_cast<const uint4*>(g.nw + wi);
@@ -788,7 +811,7 @@ __device__ __noinline__ void gemv_prologue(unsigned long long* tr) {
     for (int q = 0; q < 2; ++q) {
       const uint32_t c = tid + q * NCT;
       chunk_pend(g.a, g.tag_a, c < nch ? c : 0u, c < nch, pp, pt, 8 * q);
-      chunk_pend(g.b, g.tag_b, c < nch ? c : 0u, c < nch && has_b, pp, pt, 8 * q + 4);
+      chunk_pend(g.b, g.tag_b, c < nch ? bchunk(c) : 0u, c < nch && has_b, pp, pt, 8 * q + 4);
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         pw4[8 * q + k] = ca[q].w[k];
@@ -864,6 +887,30 @@ __device__ __noinline__ void gemv_prologue(unsigned long long* tr) {
     } else if (g.pro == kPlain) {
 #pragma unroll
       for (int j = 0; j < 16; ++j) v[j] = raw[q][j];
+    } else if (g.pro == kWhtGate) {
+      // a head's D/16 chunks sit on adjacent lanes: the WHT's strides below 16 stay
+      // in the chunk, larger ones pair lane with lane ^ (stride / 16)
+      float x[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) x[j] = raw[q][j];
+#pragma unroll
+      for (int h = 1; h < 16; h <<= 1)
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          if (!(j & h)) {
+            const float a0 = x[j], a1 = x[j + h];
+            x[j] = a0 + a1;
+            x[j + h] = a0 - a1;
+          }
+      for (uint32_t m = 1; m < g.head_dim / 16; m <<= 1)
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float pv = __shfl_xor_sync(FULLMASK, x[j], m);
+          x[j] = (lane & m) ? pv - x[j] : x[j] + pv;
+        }
+      const float wn = rsqrtf((float)g.head_dim);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[j] = round_bf16(round_bf16(x[j] * wn) * sigmoidf_(xb[j]));
     } else if (g.pro == kSiluMul) {
 #pragma unroll
       for (int j = 0; j < 16; ++j) v[j] = silu_fast(raw[q][j]) * xb[j];
@@ -1149,7 +1196,7 @@ __device__ __forceinline__ const void* seq_vec(const void* base, uint32_t tag, u
 
 template <int PRO>
 __device__ __noinline__ void prologue_b_kind(uint32_t b0, uint32_t nb, unsigned long long* tr) {
-  constexpr bool kTwo = PRO == kAddRms || PRO == kSiluMul || PRO == kHeadNormSilu;
+  constexpr bool kTwo = PRO == kAddRms || PRO == kSiluMul || PRO == kHeadNormSilu || PRO == kWhtGate;
   constexpr bool kRmsKind = PRO == kRms || PRO == kAddRms;
   constexpr uint32_t NI = kTwo ? 2 : 4;
   const Program& P = prog();
@@ -1158,6 +1205,10 @@ __device__ __noinline__ void prologue_b_kind(uint32_t b0, uint32_t nb, unsigned 
   const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t K = g.K, nch = K / 16, ng = K / 64, items = nb * nch;
   const BatchBuf bb = batch_buf(sh, K, g.bs);
+  // chunk c of input b (kWhtGate: head h's gate chunk sits at q_full[h * 2D + D + ...])
+  auto bchunk = [&](uint32_t c) {
+    return PRO == kWhtGate ? c + ((16 * c) / g.head_dim + 1) * (g.head_dim / 16) : c;
+  };
   float ssb[kRmsKind ? kMaxBatch : 1];
 #pragma unroll
   for (int b = 0; b < (kRmsKind ? kMaxBatch : 1); ++b) ssb[b] = 0.f;
@@ -1173,7 +1224,7 @@ __device__ __noinline__ void prologue_b_kind(uint32_t b0, uint32_t nb, unsigned 
       if constexpr (kTwo) x2[u] = a[u];
       if (ok_i) {
         chunk_issue(seq_vec(g.a, g.tag_a, g.sa, b0 + s), g.tag_a, c, a[u]);
-        if constexpr (kTwo) chunk_issue(seq_vec(g.b, g.tag_b, g.sb, b0 + s), g.tag_b, c, x2[u]);
+        if constexpr (kTwo) chunk_issue(seq_vec(g.b, g.tag_b, g.sb, b0 + s), g.tag_b, bchunk(c), x2[u]);
       }
     }
     {  // the tagged inputs not there yet, polled together
@@ -1187,7 +1238,7 @@ __device__ __noinline__ void prologue_b_kind(uint32_t b0, uint32_t nb, unsigned 
         const bool in = i < items;
         const uint32_t s = in ? i / nch : 0, c = in ? i % nch : 0;
         chunk_pend(seq_vec(g.a, g.tag_a, g.sa, b0 + s), g.tag_a, c, in, pp, pt, (kTwo ? 8 : 4) * u);
-        if constexpr (kTwo) chunk_pend(seq_vec(g.b, g.tag_b, g.sb, b0 + s), g.tag_b, c, in, pp, pt, 8 * u + 4);
+        if constexpr (kTwo) chunk_pend(seq_vec(g.b, g.tag_b, g.sb, b0 + s), g.tag_b, bchunk(c), in, pp, pt, 8 * u + 4);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           pw4[(kTwo ? 8 : 4) * u + k] = a[u].w[k];
@@ -1258,6 +1309,30 @@ __device__ __noinline__ void prologue_b_kind(uint32_t b0, uint32_t nb, unsigned 
           if (g.dump && ok_i) chunk_store_bf16(g.dump + (size_t)(b0 + s) * (P.seq_stride / 2) + c * 16, v);
 #pragma unroll
           for (int j = 0; j < 16; ++j) v[j] *= silu_fast(xb[j]);
+        } else if constexpr (PRO == kWhtGate) {
+          // a head's chunks sit on an aligned group of adjacent lanes (nch is a
+          // multiple of the head's D / 16 chunks): strides below 16 in the chunk,
+          // larger ones across lanes
+          float xb[16];
+          chunk_values(x2[u], g.tag_b, xb);
+#pragma unroll
+          for (int h = 1; h < 16; h <<= 1)
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (!(j & h)) {
+                const float a0 = raw[j], a1 = raw[j + h];
+                raw[j] = a0 + a1;
+                raw[j + h] = a0 - a1;
+              }
+          for (uint32_t m = 1; m < g.head_dim / 16; m <<= 1)
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float pv = __shfl_xor_sync(FULLMASK, raw[j], m);
+              raw[j] = (lane & m) ? pv - raw[j] : raw[j] + pv;
+            }
+          const float wn = rsqrtf((float)g.head_dim);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] = round_bf16(round_bf16(raw[j] * wn) * sigmoidf_(xb[j]));
         } else {
 #pragma unroll
           for (int j = 0; j < 16; ++j) v[j] = raw[j];
@@ -1333,6 +1408,7 @@ __device__ __forceinline__ void gemv_prologue_b(uint32_t b0, uint32_t nb, unsign
     case kAddRms: prologue_b_kind<kAddRms>(b0, nb, tr); break;
     case kSiluMul: prologue_b_kind<kSiluMul>(b0, nb, tr); break;
     case kHeadNormSilu: prologue_b_kind<kHeadNormSilu>(b0, nb, tr); break;
+    case kWhtGate: prologue_b_kind<kWhtGate>(b0, nb, tr); break;
     default: prologue_b_kind<kPlain>(b0, nb, tr); break;
   }
 }
@@ -1549,6 +1625,92 @@ __device__ __forceinline__ void norm_rope(float* x, const float* wv, const Progr
 }
 
 
+// ------------------------------------------------------------------ Turbo8 helpers
+
+// Orthonormal Walsh-Hadamard transform (Sylvester order) of one head's row, held
+// EPL consecutive elements per lane: butterflies of stride h pair elements i and
+// i + h (bit h of i clear) into (x_i + x_{i+h}, x_i - x_{i+h}); strides below EPL
+// stay in the lane, larger ones pair lane with lane ^ (h / EPL). Then x 1/sqrt(D).
+template <int EPL>
+__device__ __forceinline__ void wht_row(float* x, uint32_t lane, float norm) {
+#pragma unroll
+  for (int h = 1; h < EPL; h <<= 1)
+#pragma unroll
+    for (int e = 0; e < EPL; ++e)
+      if (!(e & h)) {
+        const float a = x[e], b = x[e + h];
+        x[e] = a + b;
+        x[e + h] = a - b;
+      }
+#pragma unroll
+  for (uint32_t m = 1; m < 32; m <<= 1)
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+      const float p = __shfl_xor_sync(FULLMASK, x[e], m);
+      x[e] = (lane & m) ? p - x[e] : x[e] + p;
+    }
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) x[e] *= norm;
+}
+
+// Two fp32 values as FP8 E4M3 (round to nearest even, saturating), x0 in the low
+// byte; and two E4M3 codes (low byte first) back to fp32 (exact through f16).
+__device__ __forceinline__ uint32_t e4m3x2_of(float x0, float x1) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(x1), "f"(x0));
+  return r;
+}
+__device__ __forceinline__ float2 e4m3x2_value(uint32_t two) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)two));
+  return __half22float2(*reinterpret_cast<const __half2*>(&h2));
+}
+// EPL codes (little-endian bytes) of a lane, as a word pair
+template <int EPL>
+__device__ __forceinline__ uint2 load_codes(const uint8_t* p) {
+  if constexpr (EPL == 8) return *reinterpret_cast<const uint2*>(p);
+  else if constexpr (EPL == 4) return make_uint2(*reinterpret_cast<const uint32_t*>(p), 0u);
+  else return make_uint2(*reinterpret_cast<const uint16_t*>(p), 0u);
+}
+template <int EPL>
+__device__ __forceinline__ void store_codes(uint8_t* p, uint2 c) {
+  if constexpr (EPL == 8) *reinterpret_cast<uint2*>(p) = c;
+  else if constexpr (EPL == 4) *reinterpret_cast<uint32_t*>(p) = c.x;
+  else *reinterpret_cast<uint16_t*>(p) = (uint16_t)c.x;
+}
+template <int EPL>
+__device__ __forceinline__ void dequant_codes(uint2 c, float s, float* x) {
+#pragma unroll
+  for (int e = 0; e < EPL; e += 2) {
+    const uint32_t w = e < 4 ? c.x : c.y;
+    const float2 v = e4m3x2_value(w >> (8 * (e % 4)));
+    x[e] = v.x * s;
+    x[e + 1] = v.y * s;
+  }
+}
+// Turbo8 quantisation of a row held EPL per lane (groups of 16 on 16 / EPL lanes):
+// scale = bf16(amax / 448), codes = E4M3(x / scale); returns the codes and the
+// group's scale, and leaves the dequantised values (code * scale, exact) in x.
+template <int EPL>
+__device__ __forceinline__ uint2 turbo8_quant(float* x, float& scale) {
+  float amax = 0.f;
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) amax = fmaxf(amax, fabsf(x[e]));
+#pragma unroll
+  for (int o = 1; o < 16 / EPL; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(FULLMASK, amax, o));
+  const float s = round_bf16(amax / 448.f);
+  uint2 c = make_uint2(0u, 0u);
+#pragma unroll
+  for (int e = 0; e < EPL; e += 2) {
+    const uint32_t two = s > 0.f ? e4m3x2_of(x[e] / s, x[e + 1] / s) : 0u;
+    if (e < 4) c.x |= two << (8 * e);
+    else c.y |= two << (8 * (e - 4));
+  }
+  dequant_codes<EPL>(c, s, x);
+  scale = s;
+  return c;
+}
+
 // Split-KV attention of one split (CTA). Warp w serves the HPW consecutive q-heads
 // of head group w % NG (one kv-head) and every TI-th tile, TI = 12 / NG; the TI
 // partial softmax states of a head group are merged in shared memory at the end.
@@ -1565,7 +1727,10 @@ __device__ __noinline__ uint32_t attn_consume(uint32_t itd, uint32_t ph, unsigne
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t s = blockIdx.x;
   const Span sp = attn_span(P, L.capacity, s_seq.b);
-  const uint32_t H = P.H, Hkv = P.Hkv, rowh = Hkv * D, rowbytes = rowh * 2;
+  const bool t8 = L.kv_dtype == kKvTurbo8;
+  const uint32_t H = P.H, Hkv = P.Hkv, rowh = Hkv * D, rowbytes = rowh * (t8 ? 1 : 2);
+  const uint32_t sstride = turbo8_sstride(Hkv, D), srow = t8 ? sstride * 2 : 0u;
+  const uint32_t part = kTS * (rowbytes + srow);  // a tile's K part (rows, then Turbo8 scales); V follows
   const uint32_t NG = H / HPW, TI = NCW / NG;  // warps beyond NG * TI only keep the ring moving
   if (!sp.ok) {
     if (s == 0 && threadIdx.x == 0) set_status(P.status, kStatusRange);
@@ -1651,16 +1816,53 @@ __device__ __noinline__ uint32_t attn_consume(uint32_t itd, uint32_t ph, unsigne
     if (!ok) set_status(P.status, kStatusTimeout);
   }
   consumer_sync();  // the angle table
+  const float wnorm = rsqrtf((float)D);  // the WHT's 1/sqrt(D)
   if (kv_warp) {  // the new token's k (normed, rotated) and v: appended by exactly one CTA
     norm_rope<EPL>(kx, kw, P, cs, buf + warp * D, lane);
-    uint16_t* kd = L.kc + (size_t)sp.pos * rowh + warp * D + lane * EPL;
-    uint16_t* vd = L.vc + (size_t)sp.pos * rowh + warp * D + lane * EPL;
+    if (t8) {
+      // Turbo8: k and v rotated (bf16), quantised per 16, appended as codes and
+      // scales; the fresh row keeps the dequantised values every split reads
+      wht_row<EPL>(kx, lane, wnorm);
+      wht_row<EPL>(vx, lane, wnorm);
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) {
-      fresh[warp * D + lane * EPL + e] = kx[e];
-      fresh[rowh + warp * D + lane * EPL + e] = vx[e];
-      kd[e] = to_bf16(kx[e]);
-      vd[e] = to_bf16(vx[e]);
+      for (int e = 0; e < EPL; ++e) {
+        kx[e] = round_bf16(kx[e]);
+        vx[e] = round_bf16(vx[e]);
+      }
+      if (P.dump) {
+        uint16_t* kr = reinterpret_cast<uint16_t*>(s_seq.scratch + P.sm.k_rot) + warp * D + lane * EPL;
+        uint16_t* vr = reinterpret_cast<uint16_t*>(s_seq.scratch + P.sm.v_rot) + warp * D + lane * EPL;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) {
+          kr[e] = to_bf16(kx[e]);
+          vr[e] = to_bf16(vx[e]);
+        }
+      }
+      float sk, sv;
+      const uint2 ck = turbo8_quant<EPL>(kx, sk), cv = turbo8_quant<EPL>(vx, sv);
+      const size_t row = (size_t)sp.pos * rowh + warp * D + lane * EPL;
+      store_codes<EPL>(L.kc + row, ck);
+      store_codes<EPL>(L.vc + row, cv);
+      if ((lane * EPL) % 16 == 0) {
+        const size_t si = (size_t)sp.pos * sstride + (warp * D + lane * EPL) / 16;
+        L.ks[si] = to_bf16(sk);
+        L.vs[si] = to_bf16(sv);
+      }
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) {
+        fresh[warp * D + lane * EPL + e] = kx[e];
+        fresh[rowh + warp * D + lane * EPL + e] = vx[e];
+      }
+    } else {
+      uint16_t* kd = reinterpret_cast<uint16_t*>(L.kc) + (size_t)sp.pos * rowh + warp * D + lane * EPL;
+      uint16_t* vd = reinterpret_cast<uint16_t*>(L.vc) + (size_t)sp.pos * rowh + warp * D + lane * EPL;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) {
+        fresh[warp * D + lane * EPL + e] = kx[e];
+        fresh[rowh + warp * D + lane * EPL + e] = vx[e];
+        kd[e] = to_bf16(kx[e]);
+        vd[e] = to_bf16(vx[e]);
+      }
     }
   }
 #pragma unroll
@@ -1669,7 +1871,14 @@ __device__ __noinline__ uint32_t attn_consume(uint32_t itd, uint32_t ph, unsigne
     l[j] = 0.f;
 #pragma unroll
     for (int e = 0; e < EPL; ++e) acc[j][e] = 0.f;
-    if (active) norm_rope<EPL>(q[j], qw, P, cs, buf + warp * D, lane);
+    if (active) {
+      norm_rope<EPL>(q[j], qw, P, cs, buf + warp * D, lane);
+      if (t8) {  // q rotated into the cache's basis (bf16)
+        wht_row<EPL>(q[j], lane, wnorm);
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) q[j][e] = round_bf16(q[j][e]);
+      }
+    }
   }
   consumer_sync();  // the fresh row is visible to every warp; the RoPE buffers are free
   if (tr && threadIdx.x == 0) tr[3] = global_ns();
@@ -1693,10 +1902,15 @@ __device__ __noinline__ uint32_t attn_consume(uint32_t itd, uint32_t ph, unsigne
       const uint8_t* base = sh.ring + sh.toff[st];
       const uint32_t n = min((uint32_t)kTS, sp.tc_end - (sp.t0 + i * kTS));
       float d[NV];
+      const uint32_t sidx = (g * D + lane * EPL) / 16;  // this lane's group in a token's scale row
 #pragma unroll
       for (int t = 0; t < kTS; ++t) {  // rows t >= n hold stale data: their scores are masked
         float kf[EPL];
-        load_row<EPL>(reinterpret_cast<const uint16_t*>(base + t * rowbytes) + g * D + lane * EPL, kf);
+        if (t8)
+          dequant_codes<EPL>(load_codes<EPL>(base + t * rowbytes + g * D + lane * EPL),
+                             bf16f(reinterpret_cast<const uint16_t*>(base + kTS * rowbytes + t * srow)[sidx]), kf);
+        else
+          load_row<EPL>(reinterpret_cast<const uint16_t*>(base + t * rowbytes) + g * D + lane * EPL, kf);
 #pragma unroll
         for (int j = 0; j < HPW; ++j) {
           float x = 0.f;
@@ -1733,7 +1947,12 @@ __device__ __noinline__ uint32_t attn_consume(uint32_t itd, uint32_t ph, unsigne
 #pragma unroll
       for (uint32_t t = 0; t < (uint32_t)kTS; ++t) {
         float vf[EPL];
-        load_row<EPL>(reinterpret_cast<const uint16_t*>(base + (kTS + t) * rowbytes) + g * D + lane * EPL, vf);
+        if (t8)
+          dequant_codes<EPL>(load_codes<EPL>(base + part + t * rowbytes + g * D + lane * EPL),
+                             bf16f(reinterpret_cast<const uint16_t*>(base + part + kTS * rowbytes + t * srow)[sidx]),
+                             vf);
+        else
+          load_row<EPL>(reinterpret_cast<const uint16_t*>(base + part + t * rowbytes) + g * D + lane * EPL, vf);
         const bool live = t < n;
 #pragma unroll
         for (int j = 0; j < HPW; ++j) {
@@ -1928,7 +2147,9 @@ __device__ __noinline__ void combine_consume(uint32_t ph) {
       O = fmaf(part[(2 * NCW + w) * 32 + lane], c, O);
     }
     const float attn = round_bf16(O / Ls);
-    st_tagged(ga + (size_t)h * P.D + d, tag_word(attn * sigmoidf_(gate), tag));
+    // a Turbo8 layer's output is still in the rotated basis: the o_proj prologue
+    // rotates each head back and applies the gate there
+    st_tagged(ga + (size_t)h * P.D + d, tag_word(L.kv_dtype == kKvTurbo8 ? attn : attn * sigmoidf_(gate), tag));
   }
   consumer_sync();
 }
@@ -2258,20 +2479,30 @@ __device__ __noinline__ void produce_all(const LayerDesc* layers) {
           }
         }
       } else if (ty == kPhAttn) {
-        const uint32_t rowh = P.Hkv * P.D, rowbytes = rowh * 2;
+        const bool t8 = L.kv_dtype == kKvTurbo8;
+        const uint32_t rowh = P.Hkv * P.D, rowbytes = rowh * (t8 ? 1 : 2);
+        const uint32_t ss = turbo8_sstride(P.Hkv, P.D), srow = ss * 2;  // Turbo8 scales per token
         for (uint32_t b = 0; b < batch; ++b) {
-          const size_t seq_off = (size_t)L.capacity * rowh * b;
-          const uint16_t* kc = L.kc + seq_off;
-          const uint16_t* vc = L.vc + seq_off;
+          const size_t seq_off = (size_t)L.capacity * rowbytes * b;
+          const uint8_t* kc = L.kc + seq_off;
+          const uint8_t* vc = L.vc + seq_off;
+          const uint16_t* ks = t8 ? L.ks + (size_t)L.capacity * ss * b : nullptr;
+          const uint16_t* vs = t8 ? L.vs + (size_t)L.capacity * ss * b : nullptr;
           const Span sp = attn_span(P, L.capacity, b);
           for (uint32_t t = 0; t < sp.ntiles; ++t) {
             const uint32_t tt = sp.t0 + t * kTS, n = min((uint32_t)kTS, sp.tc_end - tt);
-            // rows past n are read (masked) by the consumers
-            uint8_t* dst = ring_claim(rg, sh, 2 * kTS * rowbytes, 2 * n * rowbytes, 0u, 0u, status);
+            // rows past n are read (masked) by the consumers. A tile: K rows, then
+            // (Turbo8) K scales, V rows, V scales, each part kTS tokens long.
+            const uint32_t part = kTS * (rowbytes + (t8 ? srow : 0u));
+            uint8_t* dst = ring_claim(rg, sh, 2 * part, 2 * n * (rowbytes + (t8 ? srow : 0u)), 0u, 0u, status);
             if (!dst) goto drain;
             uint64_t* fb = &sh.full[slot_of(rg.i)];
-            bulk_g2s(dst, kc + (size_t)tt * rowh, n * rowbytes, fb);
-            bulk_g2s(dst + kTS * rowbytes, vc + (size_t)tt * rowh, n * rowbytes, fb);
+            bulk_g2s(dst, kc + (size_t)tt * rowbytes, n * rowbytes, fb);
+            bulk_g2s(dst + part, vc + (size_t)tt * rowbytes, n * rowbytes, fb);
+            if (t8) {
+              bulk_g2s(dst + kTS * rowbytes, ks + (size_t)tt * ss, n * srow, fb);
+              bulk_g2s(dst + part + kTS * rowbytes, vs + (size_t)tt * ss, n * srow, fb);
+            }
             issued();
           }
         }

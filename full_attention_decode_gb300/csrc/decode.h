@@ -29,13 +29,19 @@ enum LayerKind : int32_t { kLayerFA = 0, kLayerGDN = 1, kLayerGemv = 2, kLayerHe
 //   full attention:   0 q_proj, 1 k_proj, 2 v_proj, 3 o_proj, 4 gate, 5 up, 6 down
 //   linear attention: 0 in_proj_a, 1 in_proj_b, 2 in_proj_qkv, 3 in_proj_z, 4 gate,
 //                     5 up, 6 down, 7 out_proj
+// KV formats (qwen35_kv_dtype): bf16 rows, or Turbo8 (E4M3 codes + bf16 scales per
+// 16, rotated basis).
+enum KvDtype : uint32_t { kKvBf16 = 0, kKvTurbo8 = 1 };
+
 struct LayerDesc {
   int32_t kind;
   uint32_t capacity;  // KV rows (full attention)
   QMat m[8];
   const uint16_t *input_ln, *post_ln, *q_norm, *k_norm, *norm_weight, *dt_bias, *conv_w;
   const float* a_log;
-  uint16_t *kc, *vc;
+  uint8_t *kc, *vc;     // bf16 rows or Turbo8 codes
+  uint16_t *ks, *vs;    // Turbo8 scales [capacity][sstride]
+  uint32_t kv_dtype, pad;
   float *conv_state, *ssm;
 };
 
@@ -53,6 +59,7 @@ struct ScratchMap {
   uint32_t tag_begin, tag_end;
   uint32_t part_o, part_ml;                   // split-KV partials (fp32)
   uint32_t x_norm, x_norm2, qkv_smooth, y_norm;  // debug stage dumps (bf16)
+  uint32_t k_rot, v_rot;                         // debug: a Turbo8 layer's rotated new k, v (bf16)
 };
 
 // The split of a GEMV phase's work that depends only on its shape (the layer kind

@@ -113,13 +113,31 @@ typedef struct qwen35_gdn_layer {
     qwen35_qweight gate_proj, up_proj, down_proj;
 } qwen35_gdn_layer;
 
-/* bf16 KV cache of one full-attention layer and one sequence (LayerKvCache with
- * the Bf16 format, "mod.rs"): k and v are [capacity][num_kv_heads][head_dim]. A
- * forward writes exactly row cache_pos of each and reads rows [0, seq_len_attn). */
+/* KV cache of one full-attention layer and one sequence (LayerKvCache, "mod.rs"),
+ * in one of two formats (MetalKvDtype there):
+ *  - QWEN35_KV_BF16 (0): k and v are bf16 [capacity][num_kv_heads][head_dim];
+ *    k_scales, v_scales unused (may be NULL).
+ *  - QWEN35_KV_TURBO8 (1): the Turbo8 format, in the WHT-rotated basis (the
+ *    forward rotates k and v before the append, q before attention and the output
+ *    back after it): k and v are FP8 E4M3 codes, uint8 [capacity][num_kv_heads]
+ *    [head_dim]; k_scales and v_scales are bf16 [capacity][sstride], one scale per
+ *    16 consecutive elements of a token's row (element j of kv-head g uses scale
+ *    g * head_dim / 16 + j / 16), sstride = round_up(num_kv_heads * head_dim / 16, 8)
+ *    (the pages keep the scales unpadded; the padding keeps every token's row of
+ *    scales 16-byte aligned for the bulk copies). 1.125 bytes per element.
+ * A forward writes exactly row cache_pos of each array and reads rows
+ * [0, seq_len_attn). All pointers 16-byte aligned. */
+enum qwen35_kv_dtype {
+    QWEN35_KV_BF16 = 0,
+    QWEN35_KV_TURBO8 = 1
+};
 typedef struct qwen35_kv_cache {
-    qwen35_bf16* k;
-    qwen35_bf16* v;
+    void* k;
+    void* v;
     uint32_t capacity;
+    uint32_t dtype;
+    qwen35_bf16* k_scales;
+    qwen35_bf16* v_scales;
 } qwen35_kv_cache;
 
 /* Persistent state of one linear-attention layer (LinearAttentionState,
