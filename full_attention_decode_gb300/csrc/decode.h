@@ -132,6 +132,14 @@ constexpr int kDecSmem = kDecRing + kDecFixed + kDecUnion;
 constexpr int kDecRingLarge = 195840;
 constexpr int kDecUnionSmall = kDecSmem - kDecFixed - kDecRingLarge;
 
+// The decode kernel for a program's dims: attention head dim (one function per
+// supported D, each in its own translation unit), q-heads per attention warp, GDN
+// key head dim, batched or not; nullptr for an unsupported combination.
+using DecodeKernel = void (*)(Program);
+DecodeKernel decode_kernel_d64(uint32_t hpw, uint32_t Dk, bool batched);
+DecodeKernel decode_kernel_d128(uint32_t hpw, uint32_t Dk, bool batched);
+DecodeKernel decode_kernel_d256(uint32_t hpw, uint32_t Dk, bool batched);
+
 cudaError_t decode_set_attributes();
 // Dequantise one matrix to fp32 [n][k]: fmaf(scale, code, bias), one rounding.
 cudaError_t dequant_launch(const uint8_t* codes, const uint16_t* scales, const uint16_t* biases,
