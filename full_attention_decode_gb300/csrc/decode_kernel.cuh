@@ -311,6 +311,12 @@ __device__ __forceinline__ void chunk_store_bf16(uint16_t* dst, const float* v) 
 
 // ------------------------------------------------------------------ bf16 helpers
 
+// bf16 pair {lo, hi} (round to nearest).
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
 __device__ __forceinline__ void unpack8(const uint4 u, float* x) {
   x[0] = bf16lo(u.x); x[1] = bf16hi(u.x);
   x[2] = bf16lo(u.y); x[3] = bf16hi(u.y);
@@ -759,9 +765,12 @@ __device__ __forceinline__ float* gemv_partials(const Smem& sh, uint32_t nch) {
 
 // Form the phase's input vector once per CTA and store it, quantised, in shared
 // memory: chunk c at hi[c], lo[c] (uint4 each) and aux[c] = {qsum128, scale, sum x}.
-// The inputs are polled until every word carries its expected tag; one fence
-// then orders the phase's reads before its writes (the hand-over above).
-__device__ __noinline__ void gemv_prologue(unsigned long long* tr) {
+// The inputs are polled until every word carries its expected tag. This form gives
+// each thread whole 16-element chunks (a head's chunks on adjacent lanes for the
+// per-head norm and the Turbo8 rotation); the RMSNorm inputs take the
+// four-threads-per-chunk form below, which measured faster for them and slower
+// for the wider inputs of the down and output projections.
+__device__ __noinline__ void gemv_prologue_chunks(unsigned long long* tr) {
   const Program& P = prog();
   const Gemv& g = cur_gemv();
   const Smem sh = smem_map(smem_raw);
@@ -934,6 +943,169 @@ __device__ __noinline__ void gemv_prologue(unsigned long long* tr) {
   }
   if (tr && tid == 0) tr[9] = global_ns();
   consumer_sync();
+}
+
+// An RMSNorm input (kRms, kAddRms) with four consecutive elements per thread:
+// thread t of round r holds elements 4 (t + 384 r) .. 4 (t + 384 r) + 3, so the
+// loads of a warp are 512 contiguous bytes, every consumer thread takes part, and a
+// chunk's four threads are adjacent lanes (its largest magnitude, quantised sum and
+// sum are reduced across them). The arithmetic per element is that of the chunk
+// form, so the stored chunks are the same bits. R rounds cover K <= 1536 R.
+__device__ __forceinline__ uint4 quad_issue(const void* base, uint32_t tag, uint32_t e) {
+  if (tag) return ld_tagged4(static_cast<const uint32_t*>(base) + e);
+  const uint2 u = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(base) + e);
+  return make_uint4(u.x, u.y, 0u, 0u);
+}
+__device__ __forceinline__ void quad_values(const uint4 w, uint32_t tag, float* x) {
+  if (tag) {
+    x[0] = tag_value(w.x); x[1] = tag_value(w.y); x[2] = tag_value(w.z); x[3] = tag_value(w.w);
+  } else {
+    x[0] = bf16lo(w.x); x[1] = bf16hi(w.x); x[2] = bf16lo(w.y); x[3] = bf16hi(w.y);
+  }
+}
+// Quantise the four values of this thread as part of chunk c (lanes 4m .. 4m + 3
+// of a warp hold one chunk): the same scale, codes and sums as quantize16 over
+// the whole chunk. Every lane takes part in the shuffles; `store` selects the
+// chunks that exist.
+__device__ __forceinline__ void quantize_quad(const float* v, uint32_t c, bool store, uint32_t* qhi, uint32_t* qlo,
+                                              float4* aux) {
+  const uint32_t j = threadIdx.x & 3;
+  float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+  amax = fmaxf(amax, __shfl_xor_sync(FULLMASK, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(FULLMASK, amax, 2));
+  const uint32_t E = __float_as_uint(amax) >> 23;
+  const bool nz = E >= 15;
+  const float up = nz ? __uint_as_float((268u - E) << 23) : 0.f;  // 2^(15-e)
+  const float scale = nz ? __uint_as_float((E - 14u) << 23) : 0.f;
+  int t[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) t[i] = sat16(v[i] * up);
+  int qs = t[0] + t[1] + t[2] + t[3];
+  float sx = v[0] + v[1] + v[2] + v[3];
+  qs += __shfl_xor_sync(FULLMASK, qs, 1);
+  sx += __shfl_xor_sync(FULLMASK, sx, 1);
+  qs += __shfl_xor_sync(FULLMASK, qs, 2);
+  sx += __shfl_xor_sync(FULLMASK, sx, 2);
+  if (store) {
+    qlo[4 * c + j] = __byte_perm(__byte_perm(t[0], t[1], 0x0040), __byte_perm(t[2], t[3], 0x0040), 0x5410);
+    qhi[4 * c + j] = __byte_perm(__byte_perm(t[0], t[1], 0x0051), __byte_perm(t[2], t[3], 0x0051), 0x5410);
+    if (j == 0) aux[c] = make_float4(__int_as_float(128 * qs), scale, sx, 0.f);
+  }
+}
+template <int R>
+__device__ __noinline__ void gemv_prologue_quads(unsigned long long* tr) {
+  const Program& P = prog();
+  const Gemv& g = cur_gemv();
+  const Smem sh = smem_map(smem_raw);
+  const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t K = g.K, nch = K / 16;
+  uint32_t* qhi = reinterpret_cast<uint32_t*>(sh.uni);
+  uint32_t* qlo = qhi + 4 * nch;
+  float4* aux = reinterpret_cast<float4*>(qlo + 4 * nch);
+  const bool add = g.pro == kAddRms;  // else kRms
+  const uint32_t tag_a = g.tag_a, tag_b = add ? g.tag_b : 0u;
+  // every global load of the prologue is issued before any is used: one round trip
+  uint4 A[R], Bq[R];
+  uint2 Wq[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const uint32_t e = 4u * (tid + (uint32_t)NCT * r);
+    A[r] = Bq[r] = make_uint4(0u, 0u, 0u, 0u);
+    Wq[r] = make_uint2(0u, 0u);
+    if (e < K) {
+      A[r] = quad_issue(g.a, tag_a, e);
+      if (add) Bq[r] = quad_issue(g.b, tag_b, e);
+      Wq[r] = *reinterpret_cast<const uint2*>(g.nw + e);
+    }
+  }
+  if (tr && tid == 0) tr[15] = global_ns();  // loads issued
+  // the tagged inputs not there yet, polled together until every word has its tag
+  uint32_t todo = 0;
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const uint32_t e = 4u * (tid + (uint32_t)NCT * r);
+    if (e < K && ((tag_a && !tags4_are(A[r], tag_a)) || (tag_b && !tags4_are(Bq[r], tag_b)))) todo |= 1u << r;
+  }
+  if (todo) {
+    const uint64_t t0 = global_ns(), limit = wait_limit();
+    for (uint32_t n = 1; todo; ++n) {
+      __nanosleep(64);
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+        if ((todo >> r) & 1u) {
+          const uint32_t e = 4u * (tid + (uint32_t)NCT * r);
+          if (tag_a) A[r] = quad_issue(g.a, tag_a, e);
+          if (tag_b) Bq[r] = quad_issue(g.b, tag_b, e);
+        }
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+        if (((todo >> r) & 1u) && (!tag_a || tags4_are(A[r], tag_a)) && (!tag_b || tags4_are(Bq[r], tag_b)))
+          todo &= ~(1u << r);
+      if (todo && (global_ns() - t0 > limit || ((n & 15) == 0 && timed_out(P.status)))) {
+        set_status(P.status, kStatusTimeout);
+        break;
+      }
+    }
+  }
+  // the values before the norm (kept in A as float bits) and their sum of squares
+  float ss = 0.f;
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const uint32_t e = 4u * (tid + (uint32_t)NCT * r);
+    float x[4];
+    quad_values(A[r], tag_a, x);
+    if (add) {
+      float xb[4];
+      quad_values(Bq[r], tag_b, xb);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) x[i] = round_bf16(x[i] + xb[i]);
+      if (blockIdx.x == 0 && e < K)  // one CTA keeps x_resid for the down projection's residual
+        st_tagged4(g.resid_out + e, make_uint4(tag_word(x[0], g.out_tag), tag_word(x[1], g.out_tag),
+                                                tag_word(x[2], g.out_tag), tag_word(x[3], g.out_tag)));
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) ss = fmaf(x[i], x[i], ss);  // zero past the end
+    A[r] = make_uint4(__float_as_uint(x[0]), __float_as_uint(x[1]), __float_as_uint(x[2]), __float_as_uint(x[3]));
+  }
+  if (tr && tid == 0 && ss != 12345.f) tr[8] = global_ns();  // thread 0's loads have landed
+  ss = warp_sum(ss);
+  if (lane == 0) sh.misc[warp] = ss;
+  consumer_sync();
+  float tot = 0.f;
+#pragma unroll
+  for (int w = 0; w < NCW; ++w) tot += sh.misc[w];
+  const float inv = rsqrtf(tot / (float)K + P.eps);
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    if (4u * (uint32_t)NCT * r >= K) break;  // (uniform) no thread has this round
+    const uint32_t e = 4u * (tid + (uint32_t)NCT * r);
+    const bool in = e < K;
+    const float w[4] = {bf16lo(Wq[r].x), bf16hi(Wq[r].x), bf16lo(Wq[r].y), bf16hi(Wq[r].y)};
+    float v[4];
+    v[0] = round_bf16(__uint_as_float(A[r].x) * inv * w[0]);
+    v[1] = round_bf16(__uint_as_float(A[r].y) * inv * w[1]);
+    v[2] = round_bf16(__uint_as_float(A[r].z) * inv * w[2]);
+    v[3] = round_bf16(__uint_as_float(A[r].w) * inv * w[3]);
+    if (g.dump && in)
+      *reinterpret_cast<uint2*>(g.dump + e) = make_uint2(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]));
+    if (!in) v[0] = v[1] = v[2] = v[3] = 0.f;
+    quantize_quad(v, e / 16, in, qhi, qlo, aux);
+  }
+  if (tr && tid == 0) tr[9] = global_ns();
+  consumer_sync();
+}
+// The phase's input vector: the RMSNorm inputs in the four-threads-per-chunk form,
+// the others in whole chunks per thread.
+__device__ __noinline__ void gemv_prologue(unsigned long long* tr) {
+  const Gemv& g = cur_gemv();
+  if (g.pro != kRms && g.pro != kAddRms) return gemv_prologue_chunks(tr);
+  const uint32_t rounds = (g.K + 4 * NCT - 1) / (4 * NCT);
+  if (rounds <= 1) return gemv_prologue_quads<1>(tr);
+  if (rounds <= 2) return gemv_prologue_quads<2>(tr);
+  if (rounds <= 3) return gemv_prologue_quads<3>(tr);
+  if (rounds <= 4) return gemv_prologue_quads<4>(tr);
+  if (rounds <= 6) return gemv_prologue_quads<6>(tr);
+  return gemv_prologue_quads<8>(tr);
 }
 
 // Rows computed whole by one warp with nothing added after the sum (one K-part, no
@@ -1124,12 +1296,6 @@ constexpr uint32_t kLoPair = 0x5140u, kHiPair = 0x5342u;  // bytes 0,1 and 2,3 o
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-// bf16 pair {lo, hi} (round to nearest).
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  uint32_t r;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
 __device__ __forceinline__ void unpack_words(const uint32_t (&pk)[8], float* x) {
@@ -2303,9 +2469,9 @@ __device__ __noinline__ uint32_t gdn_consume(uint32_t itd, uint32_t ph) {
     consumer_sync();
     float tq = 0.f, tk = 0.f;
 #pragma unroll
-    for (int w = 0; w < NCW; ++w) {
-      tq += red[w];
-      tk += red[32 + w];
+    for (int i = 0; i < NCW; ++i) {
+      tq += red[i];
+      tk += red[32 + i];
     }
     const float iq = rsqrtf(tq + P.l2_eps), ik = rsqrtf(tk + P.l2_eps);
     consumer_sync();
@@ -2691,7 +2857,6 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
     enter(0, 0);
   }
   for (uint32_t l = 0; l < P.n_layers; ++l) {
-    const uint32_t ph0 = ph;
     for (int p = 0;; ++p, ++ph) {
       if (l > 0 || p > 0) {
         mark(0);
