@@ -109,6 +109,8 @@ Layout layout(const Dims& d, int kinds) {
   L.m.g = words(d.I);
   L.m.u = words(d.I);
   L.m.xa = words(d.E);
+  L.m.hq = words(d.I);
+  L.m.he = words(d.I / 16);
   if (kinds & kHasFa) {
     L.m.q_full = words((size_t)2 * d.H * d.D);
     L.m.k = words((size_t)d.Hkv * d.D);

@@ -56,6 +56,9 @@ struct ScratchMap {
   uint32_t q_full, k, v, ga, o, flags;        // full attention (tagged)
   uint32_t dt_raw, b_raw, qkv, z, y, out;     // linear attention (tagged)
   uint32_t x_resid, g, u, xa;                 // both (tagged); xa: a layer's output inside a stack
+  // a single sequence's SiLU(gate) * up, formed by the gate|up phase and quantised
+  // as the down projection's input (tagged): 16-bit codes [I], chunk exponents [I/16]
+  uint32_t hq, he;
   uint32_t tag_begin, tag_end;
   uint32_t part_o, part_ml;                   // split-KV partials (fp32)
   uint32_t x_norm, x_norm2, qkv_smooth, y_norm;  // debug stage dumps (bf16)

@@ -63,7 +63,9 @@ constexpr int kMaxKc = 8;
 enum PhaseType { kPhGemv = 0, kPhAttn = 1, kPhCombine = 2, kPhGdn = 3 };
 // kWhtGate: a Turbo8 layer's o_proj input: the attention output, in the cache's
 // rotated basis, rotated back per head (bf16), times sigmoid(gate) (bf16)
-enum Pro { kPlain = 0, kRms = 1, kAddRms = 2, kSiluMul = 3, kHeadNormSilu = 4, kWhtGate = 5 };
+// kQuantized: the input arrives already quantised (16-bit codes and chunk exponents
+// formed by the phase that produced it)
+enum Pro { kPlain = 0, kRms = 1, kAddRms = 2, kSiluMul = 3, kHeadNormSilu = 4, kWhtGate = 5, kQuantized = 6 };
 
 __device__ __forceinline__ int n_phases(int kind) { return kind == kLayerFA ? 6 : kind == kLayerGDN ? 5 : 1; }
 __device__ __forceinline__ int phase_type(int kind, int p) {
@@ -506,6 +508,9 @@ struct Gemv {
   // (elements), bs sequences per pass over the weights, npass passes
   uint32_t sa, sb, sres_in, sres_out, sout[4];
   uint32_t bs, npass, T;  // T: teams of warps per CTA (a batch)
+  // epi 3 (a single sequence's gate|up): rows pr0 .. pr0 + pn - 1 of gate and of up
+  // (whole 16-row chunks), partial sums [gate rows | up rows]
+  uint32_t pr0, pn;
 };
 
 __shared__ Gemv s_gv[2];  // GEMV descriptions by phase parity
@@ -612,8 +617,14 @@ __device__ __noinline__ void gemv_of(const Program& P, const LayerDesc& L, uint3
       g.conv_shift = L.conv_state;
       g.conv_tag = phase_tag(ph0);
     }
-    gemv_add(g, L.m[4], tw(m.g), SS);
-    gemv_add(g, L.m[5], tw(m.u), SS);
+    if (P.batch <= 1) {  // matching gate and up rows per CTA; h = SiLU(gate) * up, quantised
+      g.epi = 3;
+      gemv_add(g, L.m[4], tw(m.hq), SS);
+      gemv_add(g, L.m[5], tw(m.he), SS);
+    } else {
+      gemv_add(g, L.m[4], tw(m.g), SS);
+      gemv_add(g, L.m[5], tw(m.u), SS);
+    }
   } else if (p == mlp0 + 1) {
     g.K = P.I;
     g.pro = kSiluMul;
@@ -624,6 +635,11 @@ __device__ __noinline__ void gemv_of(const Program& P, const LayerDesc& L, uint3
     g.b = tw(m.u);
     g.tag_b = g.tag_a;
     g.sb = SS;
+    if (P.batch <= 1) {  // h's codes and chunk exponents from the gate|up phase
+      g.pro = kQuantized;
+      g.a = tw(m.hq);
+      g.b = tw(m.he);
+    }
     g.resid_in = tw(m.x_resid);
     g.tag_r = g.tag_a;
     g.sres_in = SS;
@@ -676,9 +692,19 @@ __device__ __noinline__ void gemv_of(const Program& P, const LayerDesc& L, uint3
   g.rb = total * blockIdx.x / gridDim.x;
   g.re = total * (blockIdx.x + 1) / gridDim.x;
   g.ntiles = 0;
-  for (uint32_t sg = 0; sg < g.nseg; ++sg) {
-    const uint32_t lo = max(g.rb, g.row0[sg]), hi = min(g.re, g.row0[sg + 1]);
-    if (hi > lo) g.ntiles += (hi - lo + g.R - 1) / g.R;
+  g.pr0 = g.pn = 0;
+  if (g.epi == 3) {  // a balanced range of whole 16-row chunks of gate, the same of up
+    const uint32_t nch = g.seg[0].n / 16, c0 = nch * blockIdx.x / gridDim.x, c1 = nch * (blockIdx.x + 1) / gridDim.x;
+    g.pr0 = 16 * c0;
+    g.pn = 16 * (c1 - c0);
+    g.rb = 0;
+    g.re = 2 * g.pn;
+    g.ntiles = 2 * ((g.pn + g.R - 1) / g.R);
+  } else {
+    for (uint32_t sg = 0; sg < g.nseg; ++sg) {
+      const uint32_t lo = max(g.rb, g.row0[sg]), hi = min(g.re, g.row0[sg + 1]);
+      if (hi > lo) g.ntiles += (hi - lo + g.R - 1) / g.R;
+    }
   }
   g.T = P.batch > 1 ? batch_teams(g.bias_off + g.R * g.gstride * 2, g.ntiles, P.ring_bytes) : 1u;
 }
@@ -761,6 +787,89 @@ __device__ __noinline__ void conv_shift_qk(float* conv_state, const uint8_t* scr
 // after the input chunks.
 __device__ __forceinline__ float* gemv_partials(const Smem& sh, uint32_t nch) {
   return reinterpret_cast<float*>(sh.uni + nch * 48);
+}
+
+// The down projection's input when the gate|up phase has already quantised it
+// (kQuantized): chunk c's 16-bit codes are tagged words hq[16c .. 16c + 15] (code
+// in the high half) and its exponent the tagged word he[c]; the chunks go into
+// shared memory in the layout the row loop reads, with the same bits quantize16
+// would have given (the gate|up phase ran it on the same values).
+__device__ __noinline__ void gemv_prologue_quantized(unsigned long long* tr) {
+  const Program& P = prog();
+  const Gemv& g = cur_gemv();
+  const Smem sh = smem_map(smem_raw);
+  const uint32_t tid = threadIdx.x, nch = g.K / 16, tag = g.tag_a;
+  uint4* qhi = reinterpret_cast<uint4*>(sh.uni);
+  uint4* qlo = qhi + nch;
+  float4* aux = reinterpret_cast<float4*>(qlo + nch);
+  const uint32_t* hq = static_cast<const uint32_t*>(g.a);
+  const uint32_t* he = static_cast<const uint32_t*>(g.b);
+  Chunk16 ca[2];
+  uint32_t ew[2];
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const uint32_t c = tid + q * NCT;
+    ca[q].w[0] = ca[q].w[1] = ca[q].w[2] = ca[q].w[3] = make_uint4(0u, 0u, 0u, 0u);
+    ew[q] = 0u;
+    if (c < nch) {
+      chunk_issue(hq, tag, c, ca[q]);
+      ew[q] = ld_tagged(he + c);
+    }
+  }
+  if (tr && tid == 0) tr[15] = global_ns();  // loads issued
+  const uint32_t rrows = g.re - g.rb;
+  const bool has_r = g.epi == 1 && tid < rrows;
+  const uint32_t* rin = static_cast<const uint32_t*>(g.resid_in) + g.rb + tid;
+  const uint32_t rw0 = has_r ? ld_tagged(rin) : 0u;
+  bool ok;
+  {
+    const uint32_t* pp[8];
+    uint32_t pt[8];
+    uint4 pw4[8];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const uint32_t c = tid + q * NCT;
+      chunk_pend(hq, tag, c < nch ? c : 0u, c < nch, pp, pt, 4 * q);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) pw4[4 * q + k] = ca[q].w[k];
+    }
+    ok = settle4<8>(pp, pt, pw4);
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) ca[q].w[k] = pw4[4 * q + k];
+    const uint32_t c1 = tid + NCT;
+    const uint32_t* pp1[3] = {he + (tid < nch ? tid : 0u), he + (c1 < nch ? c1 : 0u), rin};
+    const uint32_t pt1[3] = {tid < nch ? tag : 0u, c1 < nch ? tag : 0u, has_r ? g.tag_r : 0u};
+    uint32_t w1[3] = {ew[0], ew[1], rw0};
+    ok &= settle1<3>(pp1, pt1, w1);
+    ew[0] = w1[0];
+    ew[1] = w1[1];
+    if (has_r) gemv_partials(sh, nch)[g.W * rrows + tid] = tag_value(w1[2]);
+  }
+  if (!ok) set_status(P.status, kStatusTimeout);
+  if (tr && tid == 0 && ca[0].w[0].x != 0x12345678u) tr[8] = global_ns();
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const uint32_t c = tid + q * NCT;
+    if (c >= nch) continue;
+    uint4 h, l;
+    int qs = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint4 w = ca[q].w[k];  // codes of elements 4k .. 4k + 3 in bytes 2 (low) and 3 (high)
+      (&l.x)[k] = __byte_perm(__byte_perm(w.x, w.y, 0x0062), __byte_perm(w.z, w.w, 0x0062), 0x5410);
+      (&h.x)[k] = __byte_perm(__byte_perm(w.x, w.y, 0x0073), __byte_perm(w.z, w.w, 0x0073), 0x5410);
+      qs += (int)(int16_t)(w.x >> 16) + (int)(int16_t)(w.y >> 16) + (int)(int16_t)(w.z >> 16) +
+            (int)(int16_t)(w.w >> 16);
+    }
+    const uint32_t E = ew[q] >> 16;
+    qhi[c] = h;
+    qlo[c] = l;
+    aux[c] = make_float4(__int_as_float(128 * qs), E >= 15 ? __uint_as_float((E - 14u) << 23) : 0.f, 0.f, 0.f);
+  }
+  if (tr && tid == 0) tr[9] = global_ns();
+  consumer_sync();
 }
 
 // Form the phase's input vector once per CTA and store it, quantised, in shared
@@ -1098,6 +1207,7 @@ __device__ __noinline__ void gemv_prologue_quads(unsigned long long* tr) {
 // the others in whole chunks per thread.
 __device__ __noinline__ void gemv_prologue(unsigned long long* tr) {
   const Gemv& g = cur_gemv();
+  if (g.pro == kQuantized) return gemv_prologue_quantized(tr);
   if (g.pro != kRms && g.pro != kAddRms) return gemv_prologue_chunks(tr);
   const uint32_t rounds = (g.K + 4 * NCT - 1) / (4 * NCT);
   if (rounds <= 1) return gemv_prologue_quads<1>(tr);
@@ -1248,6 +1358,43 @@ __device__ uint32_t gemv_rows(uint32_t itd, unsigned long long* tr) {
   const Smem sh = smem_map(smem_raw);
   const uint32_t rb = g.rb, rows = g.re - g.rb, W = g.W;
   const float* part = gemv_partials(sh, g.K / 16);
+  if (g.epi == 3) {
+    // a single sequence's gate|up: h = SiLU(gate) * up for the CTA's rows (gate and
+    // up rounded to bf16, as their stored outputs would be), quantised per 16-row
+    // chunk exactly as the down projection's prologue would (quantize16 on a chunk
+    // held by four lanes), stored as codes and chunk exponents
+    const uint32_t n = g.pn, lane = threadIdx.x & 31, warp = threadIdx.x >> 5, tag = g.out_tag;
+    uint32_t* hq = reinterpret_cast<uint32_t*>(g.out[0]);
+    uint32_t* he = reinterpret_cast<uint32_t*>(g.out[1]);
+    for (uint32_t base = 64 * warp; base < n; base += 64 * NCW) {  // 64 rows per warp, lanes 0..15
+      const uint32_t r0 = base + 4 * lane;
+      const bool in = lane < 16 && r0 < n;
+      float v[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float gs = 0.f, us = 0.f;
+        if (in)
+          for (uint32_t w = 0; w < W; ++w) {
+            gs += part[w * rows + r0 + i];
+            us += part[w * rows + n + r0 + i];
+          }
+        v[i] = in ? silu_fast(round_bf16(gs)) * round_bf16(us) : 0.f;
+      }
+      float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+      amax = fmaxf(amax, __shfl_xor_sync(FULLMASK, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(FULLMASK, amax, 2));
+      const uint32_t E = __float_as_uint(amax) >> 23;
+      const float up = E >= 15 ? __uint_as_float((268u - E) << 23) : 0.f;  // 2^(15-e)
+      if (in) {
+        uint32_t t[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) t[i] = ((uint32_t)(uint16_t)sat16(v[i] * up) << 16) | tag;
+        st_tagged4(hq + g.pr0 + r0, make_uint4(t[0], t[1], t[2], t[3]));
+        if ((lane & 3) == 0) st_tagged(he + (g.pr0 + r0) / 16, (E << 16) | tag);
+      }
+    }
+    return itd;
+  }
   const float* resid = part + W * rows;
   for (uint32_t i = threadIdx.x; i < rows; i += NCT) {
     float y = 0.f;
@@ -2630,6 +2777,22 @@ __device__ __noinline__ void produce_all(const LayerDesc* layers) {
         const uint32_t K = g.K, gs = g.gstride, R = g.R, soff = g.scale_off, boff = g.bias_off;
         const uint32_t span = boff + R * gs * 2, rb = g.rb, re = g.re, nseg = g.nseg;
         const uint32_t npass = batch > 1 ? g.npass : 1u;
+        if (g.epi == 3) {  // a single sequence's gate|up: the CTA's gate rows, then the same up rows
+          const uint32_t lo = g.pr0, n = g.pn;
+          for (uint32_t sg = 0; sg < 2; ++sg)
+            for (uint32_t r = lo; r < lo + n; r += R) {
+              const uint32_t nr = min(R, lo + n - r), cb = nr * K, sb = nr * gs * 2;
+              // the tile's first row as its place in the partial sums: gate 0 .. n-1, up n .. 2n-1
+              uint8_t* dst = ring_claim(rg, sh, span, cb + 2 * sb, (sg * n + r - lo) | (nr << 24), 0u, status);
+              if (!dst) goto drain;
+              uint64_t* fb = &sh.full[slot_of(rg.i)];
+              bulk_g2s_stream(dst, g.seg[sg].codes + (size_t)r * K, cb, fb, stream);
+              bulk_g2s_stream(dst + soff, g.seg[sg].scales + (size_t)r * gs, sb, fb, stream);
+              bulk_g2s_stream(dst + boff, g.seg[sg].biases + (size_t)r * gs, sb, fb, stream);
+              issued();
+            }
+          continue;
+        }
         for (uint32_t pass = 0; pass < npass; ++pass) {
           const uint64_t pol = pass + 1 < npass ? keep : stream;
           for (uint32_t sg = 0; sg < nseg; ++sg) {
