@@ -29,7 +29,9 @@ PREFILL = 8192
 SEED = 0
 
 
-KERNEL_SOURCES = ["full_attention_decode_gb300/csrc/decode.cu", "full_attention_decode_gb300/csrc/decode.h",
+KERNEL_SOURCES = ["full_attention_decode_gb300/csrc/decode_kernel.cuh", "full_attention_decode_gb300/csrc/decode.cu",
+                  "full_attention_decode_gb300/csrc/decode_d64.cu", "full_attention_decode_gb300/csrc/decode_d128.cu",
+                  "full_attention_decode_gb300/csrc/decode_d256.cu", "full_attention_decode_gb300/csrc/decode.h",
                   "full_attention_decode_gb300/csrc/common.cuh"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_kernel_stack_dram_traffic.txt")
 

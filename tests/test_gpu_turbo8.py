@@ -110,6 +110,20 @@ def test_turbo8_layer_4b(stage_dump, cache_pos):
     assert B.qwen35_read_device_status(r.scratch) == 0
 
 
+def test_turbo8_layer_4b_long_context(stage_dump):
+    """131072 tokens of Turbo8 context (config 4a's length): the layer output, the
+    appended codes and scales, and the prefilled rows untouched."""
+    cache_pos = 131071
+    r = TurboFa("4b", cache_pos + 8, cache_pos)
+    tr = {}
+    got, ref = r.step(0, cache_pos, trace=tr)
+    assert rel_l2(got, ref) <= TOL_X
+    check_append(r, cache_pos, tr)
+    kc0, _, _, _ = synth.kv_cache_turbo8(0, 1, r.cfg, cache_pos + 8, cache_pos)
+    np.testing.assert_array_equal(r.kv.k.cpu().numpy().view(np.uint8)[:cache_pos], kc0[:cache_pos])
+    assert B.qwen35_read_device_status(r.scratch) == 0
+
+
 @pytest.mark.parametrize("use_graph", [False, True])
 def test_turbo8_tiny_stack(use_graph):
     init()
