@@ -32,7 +32,9 @@ bool decode_dims_ok(const Program& p, bool has_fa, bool has_gdn, int num_sms) {
   if (num_sms <= 0 || num_sms > 256 || (p.E + num_sms - 1) / num_sms > (uint32_t)NCT) return false;
   auto gemv_ok = [&](uint32_t K, uint32_t N) {
     if (K == 0 || K % 64 || K > 12288 || N == 0 || N >= (1u << 24)) return false;
-    if (p.batch > 1) {  // tensor-core passes: one sequence's staged input fits; a tile fits
+    if (p.batch > 1) {  // tensor-core passes: one sequence's staged input fits; a tile fits;
+      // the down projection's residual rows of a pass fit their buffer
+      if ((p.E + num_sms - 1) / num_sms * kMaxBatch * 4 > kBatchResid) return false;
       const uint32_t R = batch_rows(K), gs = ((K / 64 + 7) / 8) * 8;
       return batch_seq_bytes(K) + kBatchPart <= room &&
              (R * K + 15) / 16 * 16 + 4 * R * gs <= (uint32_t)kDecTileMax;

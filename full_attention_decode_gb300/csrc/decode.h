@@ -123,13 +123,15 @@ constexpr int kDecThreads = (kDecConsumerWarps + 2) * 32;
 // and one offset word per slot).
 // Two splits of the same dynamic shared memory between the ring and the per-phase
 // buffer (x chunks + partial sums / attention / GDN work area): a batch's
-// tensor-core passes stage several sequences' inputs in the larger buffer; a single
-// sequence needs at most about 28 KiB there and takes the larger ring (six 4B-shape
-// 12-row tiles of 2560 columns, ten 2-row tiles of 9216).
-constexpr int kDecRing = 174080;    // 170 KiB
+// tensor-core passes stage several sequences' inputs in a 90 KiB buffer beside a
+// 130 KiB ring (at 4B dims 8, 8 and 4 sequences per pass at K = 2560, 4096, 9216;
+// fewer passes over the down projection measured faster than a larger ring); a
+// single sequence needs at most about 28 KiB there and takes the larger ring (six
+// 4B-shape 12-row tiles of 2560 columns, ten 2-row tiles of 9216).
+constexpr int kDecRing = 133120;    // 130 KiB
 constexpr int kDecTileMax = 45056;  // 44 KiB
 constexpr int kDecSlots = 16;
-constexpr int kDecUnion = 51200;
+constexpr int kDecUnion = 92160;
 constexpr int kDecFixed = 2 * kDecSlots * 8 + 16 + 2 * kDecSlots * 4 + 1024;  // barriers, slot words, misc
 constexpr int kDecSmem = kDecRing + kDecFixed + kDecUnion;
 constexpr int kDecRingLarge = 195840;

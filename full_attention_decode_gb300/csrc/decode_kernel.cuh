@@ -459,7 +459,10 @@ __host__ __device__ inline void pick_split(uint32_t nch, uint32_t& W, uint32_t& 
 // team share a tile's column groups and add their row sums in a fixed order.
 constexpr uint32_t kBatchRowsMax = 16;
 constexpr uint32_t kXPadH = 8;
-constexpr uint32_t kBatchPart = NCW * 128 * 4;  // each warp's 16 x 8 partial sums
+// each warp's 16 x 8 partial sums, then the down projection's residual rows of the
+// pass's sequences ([CTA rows][bs], at most 1 KiB: rows <= 32)
+constexpr uint32_t kBatchResid = 1024;
+constexpr uint32_t kBatchPart = NCW * 128 * 4 + kBatchResid;
 #ifndef QWEN35_TEAM_SLACK
 #define QWEN35_TEAM_SLACK 1
 #endif
@@ -1832,6 +1835,18 @@ __device__ __noinline__ uint32_t gemv_tiles_b(uint32_t itd, uint32_t b0, uint32_
   float* mine = bb.part + warp * 128;         // [16 rows][8 sequences]
   const float* tp = bb.part + team * W * 128;  // the team's partials
   const uint64_t limit = wait_limit();
+  // the down projection's residual rows of the pass's sequences, polled together
+  // once (one L2 round trip) instead of per output inside the tile loop
+  float* resid = bb.part + NCW * 128;  // [row - rb][nb]
+  if (g.epi == 1) {
+    const uint32_t rows = g.re - g.rb;
+    for (uint32_t e = threadIdx.x; e < rows * nb; e += NCT) {
+      const uint32_t rho = e / nb, sq = e - rho * nb;
+      resid[e] = tagged_value(static_cast<const uint32_t*>(g.resid_in) + (size_t)(b0 + sq) * g.sres_in + g.rb + rho,
+                              g.tag_r);
+    }
+    consumer_sync();
+  }
   for (uint32_t tl = 0; tl < g.ntiles; ++tl, ++it) {
     const uint32_t st = slot_of(it);
     // every warp waits for every tile, its team's or not: a warp that skipped a
@@ -1866,8 +1881,7 @@ __device__ __noinline__ uint32_t gemv_tiles_b(uint32_t itd, uint32_t b0, uint32_
       const uint32_t rho = e / nb, s = e - rho * nb, row = r0 + rho;
       float acc = 0.f;
       for (uint32_t jj = 0; jj < W; ++jj) acc += tp[jj * 128 + rho * 8 + s];
-      if (g.epi == 1)
-        acc += tagged_value(static_cast<const uint32_t*>(g.resid_in) + (size_t)(b0 + s) * g.sres_in + row, g.tag_r);
+      if (g.epi == 1) acc += resid[(row - g.rb) * nb + s];
       uint32_t sg = 0;
       while (sg + 1 < g.nseg && row >= g.row0[sg + 1]) ++sg;
       gemv_store(g, sg, (size_t)(b0 + s) * g.sout[sg] + row - g.row0[sg], acc);
