@@ -245,6 +245,16 @@ def run_gpu(args) -> dict | None:
                 cc.ks, cc.vs = [x.to(torch.bfloat16).view(torch.int16) for x in scl]
                 cc.struct = B.qwen35_kv_cache(cc.k.data_ptr(), cc.v.data_ptr(), cap, B.QWEN35_KV_TURBO8,
                                               cc.ks.data_ptr(), cc.vs.data_ptr())
+            elif args.paged:  # one pool of 16-token blocks placed by a shuffled table, filled on the device
+                bt = 16
+                nbl = nb * ((cap + bt - 1) // bt)
+                shape = (nbl, bt, cfg["num_kv_heads"], cfg["head_dim"])
+                cc = B.DeviceKvBatch.__new__(B.DeviceKvBatch)
+                cc.k = torch.randn(shape, generator=gen, device="cuda", dtype=torch.bfloat16).view(torch.int16)
+                cc.v = torch.randn(shape, generator=gen, device="cuda", dtype=torch.bfloat16).view(torch.int16)
+                cc.table = torch.randperm(nbl, generator=gen, device="cuda").to(torch.int32)
+                cc.struct = B.qwen35_kv_cache(cc.k.data_ptr(), cc.v.data_ptr(), nbl // nb * bt, B.QWEN35_KV_BF16,
+                                              None, None, cc.table.data_ptr(), bt, 0)
             elif device_fill:
                 shape = (nb, cap, cfg["num_kv_heads"], cfg["head_dim"])
                 cc = B.DeviceKvBatch.__new__(B.DeviceKvBatch)
@@ -379,6 +389,7 @@ def run_gpu(args) -> dict | None:
     ab["step"] = per_seq[0]["weights"] + sum(kv_seq) + nb * per_seq[0]["gdn_state_all"]
     seq_mid = positions[0] + mid
     traffic, traffic_note = profiled_traffic(ab["step"]) if nb == 1 and args.prefill == PREFILL and not t8 \
+        and not args.paged \
         else (None, "not captured")
     tok_s = job_tok_s(ms, world, nb)
     step_gbs = ab["step"] / (ms * 1e-3) / 1e9
@@ -388,10 +399,11 @@ def run_gpu(args) -> dict | None:
         "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int8-weight/bf16-act/fp32-acc", "data": "synthetic",
         "config": {"workload": ("qwen3.5-4b-shape 32-layer decode stack, batch 1, KV prefilled to 8192" if nb == 1
-                                and args.prefill == PREFILL and not t8 else
+                                and args.prefill == PREFILL and not t8 and not args.paged else
                                 f"qwen3.5-4b-shape 32-layer decode stack, batch {nb}, KV prefilled to {positions}"
-                                + (", Turbo8 KV cache" if t8 else "")),
-                   "kv_dtype": args.kv,
+                                + (", Turbo8 KV cache" if t8 else "") + (", paged KV (16-token blocks)"
+                                                                          if args.paged else "")),
+                   "kv_dtype": args.kv, "paged": bool(args.paged),
                    "batch": nb, "positions": positions,
                    "layers": "24 gated-deltanet + 8 full-attention (i % 4 == 3)",
                    "context": [pos0 + 1, pos0 + args.steps], "global_batch": world, "seq_len": seq_mid,
@@ -518,6 +530,7 @@ def main():
     ap.add_argument("--batch", type=int, default=1, help="sequences per step (multi-sequence workload)")
     ap.add_argument("--prefill", type=int, default=PREFILL, help="KV tokens before the first step (batch 1)")
     ap.add_argument("--kv", choices=["bf16", "turbo8"], default="bf16", help="KV cache format")
+    ap.add_argument("--paged", action="store_true", help="paged bf16 KV (16-token blocks, shuffled table)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -73,7 +73,8 @@ QWEN35_KV_TURBO8 = 1
 
 class qwen35_kv_cache(C.Structure):
     _fields_ = [("k", C.c_void_p), ("v", C.c_void_p), ("capacity", C.c_uint32), ("dtype", C.c_uint32),
-                ("k_scales", C.c_void_p), ("v_scales", C.c_void_p)]
+                ("k_scales", C.c_void_p), ("v_scales", C.c_void_p), ("block_table", C.c_void_p),
+                ("block_tokens", C.c_uint32), ("reserved", C.c_uint32)]
 
 
 class qwen35_gdn_state(C.Structure):
@@ -492,6 +493,33 @@ class DeviceKvBatch:
         self.k = to_device(np.stack(ks), device)
         self.v = to_device(np.stack(vs), device)
         self.struct = qwen35_kv_cache(self.k.data_ptr(), self.v.data_ptr(), ks[0].shape[0])
+
+
+class DeviceKvPaged:
+    """Paged bf16 caches on the device: the logical caches ks[b], vs[b] ([cap][Hkv][D]
+    bf16 bits) cut into blocks of `block_tokens` rows, placed in one pool of
+    `n_blocks` blocks at the blocks `table` names ([B][cap / block_tokens]); the
+    pool's other blocks hold `fill`."""
+
+    def __init__(self, ks: list, vs: list, block_tokens: int, table, n_blocks: int, fill: int = 0x7FC0,
+                 device="cuda"):
+        from . import synth
+        self.block_tokens = block_tokens
+        self.table_np = np.ascontiguousarray(np.asarray(table, dtype=np.int32).reshape(len(ks), -1))
+        self.k = to_device(synth.paged_pool(ks, block_tokens, self.table_np, n_blocks, fill), device)
+        self.v = to_device(synth.paged_pool(vs, block_tokens, self.table_np, n_blocks, fill), device)
+        self.table = torch.from_numpy(self.table_np).to(device)
+        self.capacity = ks[0].shape[0]
+        self.struct = qwen35_kv_cache(self.k.data_ptr(), self.v.data_ptr(), self.capacity, QWEN35_KV_BF16, None,
+                                      None, self.table.data_ptr(), block_tokens, 0)
+
+    def pool(self, which: str) -> np.ndarray:
+        t = self.k if which == "k" else self.v
+        return t.cpu().numpy().view(np.uint16)
+
+    def logical(self, which: str, b: int = 0) -> np.ndarray:
+        from . import synth
+        return synth.paged_gather(self.pool(which), self.table_np[b], self.block_tokens)
 
 
 class DeviceStateBatch:

@@ -161,6 +161,13 @@ QMat qm(const qwen35_qweight& w) {
 // scale arrays too).
 bool kv_ok(const qwen35_kv_cache* kv) {
   if (!kv || !aligned16(kv->k) || !aligned16(kv->v) || kv->capacity == 0) return false;
+  if (kv->block_table) {  // paged: bf16 blocks of a power of two >= 8 rows dividing the capacity
+    const uint32_t bt = kv->block_tokens;
+    if (kv->dtype != QWEN35_KV_BF16 || ((uintptr_t)kv->block_table % 4) || bt < 8 || (bt & (bt - 1)) ||
+        kv->capacity % bt)
+      return false;
+    return true;
+  }
   if (kv->dtype == QWEN35_KV_BF16) return true;
   if (kv->dtype == QWEN35_KV_TURBO8) return aligned16(kv->k_scales) && aligned16(kv->v_scales);
   return false;
@@ -209,6 +216,10 @@ void fill_fa(LayerDesc& L, const qwen35_fa_layer* l, const qwen35_kv_cache* kv) 
   L.kv_dtype = kv->dtype;
   L.ks = kv->k_scales;
   L.vs = kv->v_scales;
+  L.btab = kv->block_table;
+  L.bt_shift = 0;
+  if (kv->block_table)
+    while ((1u << L.bt_shift) < kv->block_tokens) ++L.bt_shift;
 }
 
 void fill_gdn(LayerDesc& L, const qwen35_gdn_layer* l, const qwen35_gdn_state* st) {

@@ -39,9 +39,13 @@ struct LayerDesc {
   QMat m[8];
   const uint16_t *input_ln, *post_ln, *q_norm, *k_norm, *norm_weight, *dt_bias, *conv_w;
   const float* a_log;
-  uint8_t *kc, *vc;     // bf16 rows or Turbo8 codes
+  uint8_t *kc, *vc;     // bf16 rows or Turbo8 codes (paged: the block pools)
   uint16_t *ks, *vs;    // Turbo8 scales [capacity][sstride]
   uint32_t kv_dtype, pad;
+  // paged KV: token t in row t & (2^bt_shift - 1) of pool block btab[t >> bt_shift];
+  // null: contiguous rows
+  const int32_t* btab;
+  uint32_t bt_shift, pad2;
   float *conv_state, *ssm;
 };
 

@@ -152,7 +152,9 @@ __device__ __forceinline__ uint8_t* seq_scratch(const Program& P, uint32_t b) {
   return P.scratch + (size_t)b * P.seq_stride;
 }
 __device__ __forceinline__ void seq_caches(const Program& P, LayerDesc& L, uint32_t b) {
-  if (L.kind == kLayerFA) {
+  if (L.kind == kLayerFA && L.btab) {  // paged: one shared pool, a table per sequence
+    L.btab += (size_t)(L.capacity >> L.bt_shift) * b;
+  } else if (L.kind == kLayerFA) {
     const bool t8 = L.kv_dtype == kKvTurbo8;
     const size_t kv = (size_t)L.capacity * P.Hkv * P.D * (t8 ? 1 : 2) * b;  // bytes
     L.kc += kv;
@@ -166,6 +168,14 @@ __device__ __forceinline__ void seq_caches(const Program& P, LayerDesc& L, uint3
     L.conv_state += (size_t)P.C * P.Kc * b;
     L.ssm += (size_t)P.Hv * P.Dk * P.Dv * b;
   }
+}
+
+// The cache row holding logical token t: t itself, or for a paged cache its row in
+// the pool block the table names.
+__device__ __forceinline__ size_t kv_row(const LayerDesc& L, uint32_t t) {
+  if (!L.btab) return t;
+  const uint32_t mask = (1u << L.bt_shift) - 1u;
+  return ((size_t)(uint32_t)__ldg(L.btab + (t >> L.bt_shift)) << L.bt_shift) | (t & mask);
 }
 
 // misc[255]: the device position, read once per CTA when the launch starts (every
@@ -1901,7 +1911,9 @@ struct Span {
 
 // The device position as this CTA read it at kernel start (shared memory).
 
-__device__ __forceinline__ Span attn_span(const Program& P, uint32_t capacity, uint32_t b) {
+// A paged cache's splits start at multiples of 8 tokens, so that no 8-token tile
+// straddles two pool blocks.
+__device__ __forceinline__ Span attn_span(const Program& P, uint32_t capacity, uint32_t b, bool paged) {
   Span sp;
   if (P.d_pos) {
     const int32_t p = launch_pos(b);
@@ -1916,8 +1928,12 @@ __device__ __forceinline__ Span attn_span(const Program& P, uint32_t capacity, u
   }
   const uint32_t s = blockIdx.x;
   const bool mine = s < P.P && sp.ok;
-  sp.t0 = mine ? (uint32_t)(((uint64_t)sp.S * s) / P.P) : 0;
-  sp.t1 = mine ? (uint32_t)(((uint64_t)sp.S * (s + 1)) / P.P) : 0;
+  auto cut = [&](uint32_t k) {
+    const uint32_t t = (uint32_t)(((uint64_t)sp.S * k) / P.P);
+    return paged && k < P.P ? t & ~7u : t;
+  };
+  sp.t0 = mine ? cut(s) : 0;
+  sp.t1 = mine ? cut(s + 1) : 0;
   sp.has_fresh = mine && sp.S == sp.pos + 1 && sp.pos >= sp.t0 && sp.pos < sp.t1;
   sp.tc_end = sp.has_fresh ? sp.pos : sp.t1;
   sp.ntiles = (mine && sp.tc_end > sp.t0) ? (sp.tc_end - sp.t0 + kTS - 1) / kTS : 0;
@@ -2055,7 +2071,7 @@ __device__ __noinline__ uint32_t attn_consume(uint32_t itd, uint32_t ph, unsigne
   constexpr int SH = NV == 8 ? 2 : NV == 16 ? 1 : 0;
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t s = blockIdx.x;
-  const Span sp = attn_span(P, L.capacity, s_seq.b);
+  const Span sp = attn_span(P, L.capacity, s_seq.b, L.btab != nullptr);
   constexpr bool t8 = T8;  // the cache's format: Turbo8 (rotated basis) or bf16
   const uint32_t H = P.H, Hkv = P.Hkv, rowh = Hkv * D, rowbytes = rowh * (t8 ? 1 : 2);
   const uint32_t sstride = turbo8_sstride(Hkv, D), srow = t8 ? sstride * 2 : 0u;
@@ -2183,8 +2199,9 @@ __device__ __noinline__ uint32_t attn_consume(uint32_t itd, uint32_t ph, unsigne
         fresh[rowh + warp * D + lane * EPL + e] = vx[e];
       }
     } else {
-      uint16_t* kd = reinterpret_cast<uint16_t*>(L.kc) + (size_t)sp.pos * rowh + warp * D + lane * EPL;
-      uint16_t* vd = reinterpret_cast<uint16_t*>(L.vc) + (size_t)sp.pos * rowh + warp * D + lane * EPL;
+      const size_t prow = kv_row(L, sp.pos);  // paged: the row in the pool
+      uint16_t* kd = reinterpret_cast<uint16_t*>(L.kc) + prow * rowh + warp * D + lane * EPL;
+      uint16_t* vd = reinterpret_cast<uint16_t*>(L.vc) + prow * rowh + warp * D + lane * EPL;
 #pragma unroll
       for (int e = 0; e < EPL; ++e) {
         fresh[warp * D + lane * EPL + e] = kx[e];
@@ -2392,7 +2409,7 @@ __device__ __noinline__ void combine_consume(uint32_t ph) {
   const Smem sh = smem_map(smem_raw);
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t nd = P.D / 32, item = blockIdx.x;
-  const Span sp = attn_span(P, L.capacity, s_seq.b);
+  const Span sp = attn_span(P, L.capacity, s_seq.b, L.btab != nullptr);
   if (item >= P.H * nd) return;
   const uint32_t h = item / nd, d = (item % nd) * 32 + lane;
   uint32_t* ga = reinterpret_cast<uint32_t*>(s_seq.scratch + P.sm.ga);
@@ -2833,22 +2850,41 @@ __device__ __noinline__ void produce_all(const LayerDesc* layers) {
         const uint32_t rowh = P.Hkv * P.D, rowbytes = rowh * (t8 ? 1 : 2);
         const uint32_t ss = turbo8_sstride(P.Hkv, P.D), srow = ss * 2;  // Turbo8 scales per token
         for (uint32_t b = 0; b < batch; ++b) {
-          const size_t seq_off = (size_t)L.capacity * rowbytes * b;
+          // paged: one pool, sequence b's table; the entry of the next block is loaded
+          // while the current block's tiles are issued
+          const bool paged = L.btab != nullptr;
+          const int32_t* btab = paged ? L.btab + (size_t)(L.capacity >> L.bt_shift) * b : nullptr;
+          const uint32_t bsh = L.bt_shift, bmask = (1u << bsh) - 1u;
+          uint32_t lb_cur = ~0u, lb_nxt = ~0u;
+          int32_t pb_cur = 0, pb_nxt = 0;
+          const size_t seq_off = paged ? 0 : (size_t)L.capacity * rowbytes * b;
           const uint8_t* kc = L.kc + seq_off;
           const uint8_t* vc = L.vc + seq_off;
           const uint16_t* ks = t8 ? L.ks + (size_t)L.capacity * ss * b : nullptr;
           const uint16_t* vs = t8 ? L.vs + (size_t)L.capacity * ss * b : nullptr;
-          const Span sp = attn_span(P, L.capacity, b);
+          const Span sp = attn_span(P, L.capacity, b, L.btab != nullptr);
           for (uint32_t t = 0; t < sp.ntiles; ++t) {
             const uint32_t tt = sp.t0 + t * kTS, n = min((uint32_t)kTS, sp.tc_end - tt);
             // rows past n are read (masked) by the consumers. A tile: K rows, then
             // (Turbo8) K scales, V rows, V scales, each part kTS tokens long.
             const uint32_t part = kTS * (rowbytes + (t8 ? srow : 0u));
+            size_t row = tt;
+            if (paged) {  // the tile lies in one block (splits and tiles start at multiples of 8)
+              const uint32_t lb = tt >> bsh;
+              if (lb != lb_cur) {
+                pb_cur = lb == lb_nxt ? pb_nxt : __ldg(btab + lb);
+                lb_cur = lb;
+                lb_nxt = lb + 1;
+                if ((lb_nxt << bsh) < sp.tc_end) pb_nxt = __ldg(btab + lb_nxt);
+                else lb_nxt = ~0u;
+              }
+              row = ((size_t)(uint32_t)pb_cur << bsh) | (tt & bmask);
+            }
             uint8_t* dst = ring_claim(rg, sh, 2 * part, 2 * n * (rowbytes + (t8 ? srow : 0u)), 0u, 0u, status);
             if (!dst) goto drain;
             uint64_t* fb = &sh.full[slot_of(rg.i)];
-            bulk_g2s(dst, kc + (size_t)tt * rowbytes, n * rowbytes, fb);
-            bulk_g2s(dst + part, vc + (size_t)tt * rowbytes, n * rowbytes, fb);
+            bulk_g2s(dst, kc + row * rowbytes, n * rowbytes, fb);
+            bulk_g2s(dst + part, vc + row * rowbytes, n * rowbytes, fb);
             if (t8) {
               bulk_g2s(dst + kTS * rowbytes, ks + (size_t)tt * ss, n * srow, fb);
               bulk_g2s(dst + part + kTS * rowbytes, vs + (size_t)tt * ss, n * srow, fb);

@@ -214,3 +214,34 @@ def gdn_state(seed: int, layer: int, cfg: dict, std: float = 0.0, seq: int = 0):
 def cache_positions(seed: int, batch: int, lo: int = 1024, hi: int = 65536) -> np.ndarray:
     """Per-sequence prefill lengths U{lo..hi} for the independent-sequences stack."""
     return _rng(seed, "cache_pos").integers(lo, hi + 1, size=batch).astype(np.int64)
+
+
+# ---------------------------------------------------------------- paged KV layout
+
+
+def block_table(seed: int, batch: int, n_logical: int, n_blocks: int) -> np.ndarray:
+    """[batch][n_logical] distinct pool blocks drawn from [0, n_blocks), seeded (a
+    shuffled placement, as a pool allocator would leave it)."""
+    assert batch * n_logical <= n_blocks
+    perm = _rng(seed, "block_table").permutation(n_blocks)[:batch * n_logical]
+    return perm.reshape(batch, n_logical).astype(np.int32)
+
+
+def paged_pool(caches: list, block_tokens: int, table: np.ndarray, n_blocks: int, fill: int) -> np.ndarray:
+    """One pool [n_blocks][block_tokens][...] holding each logical cache caches[b]
+    ([capacity][...], any dtype) block i at pool block table[b][i]; other blocks
+    filled with `fill`."""
+    c0 = np.asarray(caches[0])
+    cap = c0.shape[0]
+    assert cap % block_tokens == 0
+    pool = np.full((n_blocks, block_tokens) + c0.shape[1:], fill, dtype=c0.dtype)
+    for b, c in enumerate(caches):
+        c = np.asarray(c).reshape((cap // block_tokens, block_tokens) + c0.shape[1:])
+        pool[np.asarray(table[b])] = c
+    return pool
+
+
+def paged_gather(pool: np.ndarray, table_row, block_tokens: int) -> np.ndarray:
+    """The logical cache [capacity][...] of one sequence back from a pool."""
+    t = np.asarray(table_row)
+    return pool[t].reshape((len(t) * block_tokens,) + pool.shape[2:])

@@ -126,7 +126,18 @@ typedef struct qwen35_gdn_layer {
  *    (the pages keep the scales unpadded; the padding keeps every token's row of
  *    scales 16-byte aligned for the bulk copies). 1.125 bytes per element.
  * A forward writes exactly row cache_pos of each array and reads rows
- * [0, seq_len_attn). All pointers 16-byte aligned. */
+ * [0, seq_len_attn). All pointers 16-byte aligned.
+ *
+ * Paged (optional; the production decode path the module page names, whose format
+ * the pages do not print): with block_table non-NULL, k and v are pools of blocks
+ * of block_tokens token rows, bf16 [num_blocks][block_tokens][num_kv_heads]
+ * [head_dim], and logical token t lives in row t % block_tokens of pool block
+ * block_table[t / block_tokens] (int32, in [0, num_blocks); the caller keeps it
+ * valid for every block a forward touches: [0, seq_len_attn) and cache_pos).
+ * capacity counts logical tokens and is a multiple of block_tokens; block_tokens
+ * is a power of two, at least 8. bf16 only. A batch of caches shares one pool:
+ * sequence b's table is block_table + b * (capacity / block_tokens). With
+ * block_table NULL (block_tokens ignored) the rows are contiguous as above. */
 enum qwen35_kv_dtype {
     QWEN35_KV_BF16 = 0,
     QWEN35_KV_TURBO8 = 1
@@ -138,6 +149,9 @@ typedef struct qwen35_kv_cache {
     uint32_t dtype;
     qwen35_bf16* k_scales;
     qwen35_bf16* v_scales;
+    const int32_t* block_table;
+    uint32_t block_tokens;
+    uint32_t reserved;
 } qwen35_kv_cache;
 
 /* Persistent state of one linear-attention layer (LinearAttentionState,
@@ -289,7 +303,8 @@ QWEN35_API int qwen35_graph_destroy(qwen35_graph* graph);
  *    one after the last layer); max_seq_len bounds every sequence's position.
  *  - layers: as for qwen35_decode_step, with every cache holding the batch's
  *    sequences contiguously, sequence b at the given pointer plus b times one
- *    sequence's size: kv->k and kv->v [batch][capacity][Hkv][D] (capacity shared);
+ *    sequence's size: kv->k and kv->v [batch][capacity][Hkv][D] (capacity shared;
+ *    a paged cache: one shared pool, tables [batch][capacity / block_tokens]);
  *    conv_state [batch][C][conv_kernel_size]; gdn_state [batch][Hv][Dv/32][Dk][32].
  *  - scratch: qwen35_stack_scratch_bytes_batched(cfg, batch).
  * Errors as qwen35_decode_step; batch outside 1..8 is INVALID_ARGUMENT. Sequence b
@@ -304,7 +319,8 @@ QWEN35_API int qwen35_decode_step_batched(const qwen35_config* cfg, const qwen35
  * projections run on the tensor cores): sequence b computes exactly what the
  * single-sequence forward computes for it.
  *  - batch: 1..8; x_in, x_out [batch][hidden] (x_out may equal x_in);
- *  - full attention: kv->k, kv->v [batch][capacity][Hkv][D]; d_cache_pos [batch]
+ *  - full attention: kv->k, kv->v [batch][capacity][Hkv][D] (paged: one pool,
+ *    tables [batch][capacity / block_tokens]); d_cache_pos [batch]
  *    int32 in device memory, sequence b appending at d_cache_pos[b] and attending
  *    over d_cache_pos[b] + 1 tokens (read when the kernel runs, not advanced); a
  *    position outside [0, min(capacity, max_seq_len)) sets QWEN35_ERR_DEVICE_RANGE
