@@ -516,6 +516,104 @@ def decode_step(cfg: dict, kinds: list, layers: list, caches: list, x_in, cache_
 
 
 # ----------------------------------------------------------------------------
+# Multi-token prefill
+# ----------------------------------------------------------------------------
+
+
+def prefill_full_attention(cfg: dict, layer: dict, kv: dict, X, cache_pos: int,
+                           traces: list | None = None) -> np.ndarray:
+    """A prompt of T tokens (X [T][E], bf16 values) through a full-attention layer.
+
+    Reading: the pages keep prefill out of the single-token path (page "Module
+    qwen3_5", non-goals: multi-token prefill) and print no prefill kernel, so its
+    result is fixed by the decode forward itself: token t of the prompt sits at
+    position cache_pos + t, appends its K/V row there and attends over
+    cache_pos + t + 1 tokens, after tokens 0 .. t-1 have done the same. The prompt
+    is that forward applied token after token. Returns x_out [T][E].
+    """
+    X = np.asarray(X, dtype=np.float64)
+    out = np.empty_like(X)
+    for t in range(X.shape[0]):
+        tr = {} if traces is not None else None
+        out[t] = forward_full_attention(cfg, layer, kv, X[t], cache_pos + t, cache_pos + t + 1, tr)
+        if traces is not None:
+            traces.append(tr)
+    return out
+
+
+def prefill_linear_attention(cfg: dict, layer: dict, state: dict, X, traces: list | None = None) -> np.ndarray:
+    """A prompt of T tokens through a linear-attention layer: the single-token forward
+    token after token, the conv and delta-rule states carried from one to the next
+    (the same reading as prefill_full_attention). Returns x_out [T][E]."""
+    X = np.asarray(X, dtype=np.float64)
+    out = np.empty_like(X)
+    for t in range(X.shape[0]):
+        tr = {} if traces is not None else None
+        out[t] = forward_linear_attention(cfg, layer, state, X[t], tr)
+        if traces is not None:
+            traces.append(tr)
+    return out
+
+
+def prefill_step(cfg: dict, kinds: list, layers: list, caches: list, X, cache_pos: int,
+                 layer_outputs: list | None = None) -> np.ndarray:
+    """A prompt through a stack, layer by layer over all T tokens: layer i's outputs
+    for the prompt are layer i+1's inputs. Token t of layer i depends only on token t
+    of layer i-1 and tokens < t of layer i, so this equals T decode_step calls at
+    positions cache_pos .. cache_pos + T - 1 (a pinned identity)."""
+    x = np.asarray(X, dtype=np.float64)
+    for kind, layer, c in zip(kinds, layers, caches):
+        if kind == "fa":
+            x = prefill_full_attention(cfg, layer, c, x, cache_pos)
+        else:
+            x = prefill_linear_attention(cfg, layer, c, x)
+        if layer_outputs is not None:
+            layer_outputs.append(x.copy())
+    return x
+
+
+def gated_delta_rule_chunk(state, q, k, v, g, beta, Dk: int):
+    """The gated delta rule over a chunk of L tokens at once (the chunked form of the
+    recurrence a prefill uses); returns (new_state, y [L][Hv][Dv]).
+
+    q, k [L][Hk][Dk]; v [L][Hv][Dv]; g, beta [L][Hv]. Per v-head with cumulative
+    decays G_t = g_1 ... g_t, the step S_t = g_t S_(t-1) + k_t d_t^T with
+    d_t = beta_t (v_t - (g_t S_(t-1))^T k_t) unrolls to
+    S_t = G_t S_0 + sum_(s<=t) (G_t / G_s) k_s d_s^T, so the d_t solve one
+    lower-triangular system
+      d_t + beta_t sum_(s<t) (G_t / G_s) (k_s . k_t) d_s = beta_t (v_t - G_t S_0^T k_t),
+    and y_t = (G_t S_0^T q_t + sum_(s<=t) (G_t / G_s) (k_s . q_t) d_s) / sqrt(Dk).
+    Solved here with a library linear solve, independently of gated_delta_rule's
+    token loop, which it must reproduce.
+    """
+    S0 = np.asarray(state, dtype=np.float64)
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    g = np.asarray(g, dtype=np.float64)
+    beta = np.asarray(beta, dtype=np.float64)
+    L, Hk = q.shape[0], q.shape[1]
+    Hv = S0.shape[0]
+    grp = Hv // Hk
+    S_new = np.empty_like(S0)
+    y = np.zeros((L, Hv, S0.shape[2]))
+    for h in range(Hv):
+        j = h // grp
+        K, Q, V = k[:, j, :], q[:, j, :], v[:, h, :]
+        lg = np.cumsum(np.log(g[:, h]))
+        ratio = np.exp(lg[:, None] - lg[None, :])          # G_t / G_s
+        G = np.exp(lg)
+        low = np.tril(np.ones((L, L)), -1)
+        A = np.eye(L) + beta[:, h][:, None] * ratio * (K @ K.T) * low
+        rhs = beta[:, h][:, None] * (V - G[:, None] * (K @ S0[h]))
+        d = np.linalg.solve(A, rhs)
+        S_new[h] = G[-1] * S0[h] + (ratio[-1][:, None] * K).T @ d
+        incl = np.tril(np.ones((L, L)))
+        y[:, h, :] = (G[:, None] * (Q @ S0[h]) + (ratio * (Q @ K.T) * incl) @ d) / np.sqrt(np.float64(Dk))
+    return S_new, y
+
+
+# ----------------------------------------------------------------------------
 # Output head
 # ----------------------------------------------------------------------------
 
