@@ -436,6 +436,156 @@ def run_gpu(args) -> dict | None:
     return res
 
 
+# ---------------------------------------------------------------------- prompt prefill
+
+
+def prefill_flops(cfg: dict, T: int, kinds: list) -> dict:
+    """Tensor-core FLOPs of one prefill of T tokens from position 0: 2 T N K per
+    projection, plus the causal attention's 4 D per (token, head, key) (keys 0..t)."""
+    E, I, H, Hkv, D = cfg["hidden"], cfg["intermediate"], cfg["num_heads"], cfg["num_kv_heads"], cfg["head_dim"]
+    Hk, Hv, Dk, Dv = cfg["num_k_heads_lin"], cfg["num_v_heads_lin"], cfg["k_head_dim_lin"], cfg["v_head_dim_lin"]
+    C = 2 * Hk * Dk + Hv * Dv
+    mlp = 3 * E * I
+    fa = 2 * H * D * E + 2 * Hkv * D * E + H * D * E + mlp
+    gdn = 2 * Hv * E + C * E + Hv * Dv * E + Hv * Dv * E + mlp
+    gemm = 2 * T * (kinds.count("fa") * fa + kinds.count("gdn") * gdn)
+    attn = kinds.count("fa") * 4 * D * H * T * (T + 1) // 2
+    return {"gemm": gemm, "attention": attn, "gate_proj_one": 2 * T * I * E}
+
+
+def run_prompt(args) -> dict | None:
+    """The multi-token prefill of a T-token prompt through the 32-layer stack from
+    position 0 (qwen35_prefill_step): one step = the whole prompt through every
+    layer; K steps timed after W warm-up steps (each rewrites the same cache rows;
+    the linear-attention states keep advancing)."""
+    import numpy as np
+    import torch
+
+    from full_attention_decode_gb300 import binding as B
+    from full_attention_decode_gb300 import synth
+
+    rank = int(os.environ.get("RANK", "0"))
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    B.qwen35_init()
+    cfg = synth.config("4b")
+    kinds = synth.layer_kinds(cfg)[:args.layers]
+    cfg = dict(cfg, num_layers=len(kinds))
+    c = B.make_config(cfg)
+    T, E = args.prompt, cfg["hidden"]
+    seed = replica_seed(rank)
+    t0 = time.time()
+    dev_layers, caches, entries = [], [], []
+    for i, kind in enumerate(kinds):
+        if kind == "fa":
+            dl = B.DeviceFaLayer(synth.fa_layer(seed, i, cfg))
+            kb, vb = synth.kv_cache(seed, i, cfg, T, 0)
+            cc = B.DeviceKv(kb, vb)
+        else:
+            dl = B.DeviceGdnLayer(synth.gdn_layer(seed, i, cfg))
+            conv, ssm = synth.gdn_state(seed, i, cfg, std=0.1)
+            cc = B.DeviceState(conv, ssm)
+        dev_layers.append(dl)
+        caches.append(cc)
+        entries.append(B.stack_layer(kind, dl, cc))
+    setup_s = time.time() - t0
+    stream = torch.cuda.Stream()
+    scratch = B.new_scratch(B.qwen35_prefill_scratch_bytes(c, T), stream=stream)
+    X = np.stack([synth.x_in(seed, 5000 + t, cfg) for t in range(T)])
+    x_in = B.to_device(X)
+    x_out = torch.empty_like(x_in)
+    torch.cuda.synchronize()
+
+    def step():
+        assert B.qwen35_prefill_step(c, entries, scratch, x_in, x_out, 0, T, stream) == 0
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    stream.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with Clocks(int(os.environ.get("LOCAL_RANK", "0"))) as clk:
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for _ in range(args.steps):
+                step()
+            ev1.record(stream)
+        stream.synchronize()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    status = B.qwen35_read_device_status(scratch, stream)
+
+    # end to end: the prompt from pinned host memory, the outputs back, every step
+    h_in = torch.from_numpy(X.view(np.int16)).pin_memory()
+    h_out = torch.empty_like(x_out, device="cpu").pin_memory()
+    torch.cuda.synchronize()
+    t_e0 = time.perf_counter()
+    for _ in range(args.steps):
+        with torch.cuda.stream(stream):
+            x_in.copy_(h_in, non_blocking=True)
+            step()
+            h_out.copy_(x_out, non_blocking=True)
+        stream.synchronize()
+    e2e_ms = (time.perf_counter() - t_e0) * 1e3 / args.steps
+
+    # the projection alone: every layer's gate_proj (9216 x 2560) over the T tokens
+    gs = B.new_scratch(4096, stream=stream)
+    xs = torch.zeros((T, E), dtype=torch.int16, device="cuda")
+    ys = torch.empty((T, cfg["intermediate"]), dtype=torch.int16, device="cuda")
+    cw = [dl.m["gate_proj"].c() for dl in dev_layers]
+    gemm_ms = {}
+    for exact in (False, True):
+        with torch.cuda.stream(stream):
+            for w in cw:
+                assert B.qwen35_prefill_gemm(w, xs, ys, T, gs, stream, exact) == 0
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            reps = 4
+            for _ in range(reps):
+                for w in cw:
+                    assert B.qwen35_prefill_gemm(w, xs, ys, T, gs, stream, exact) == 0
+            e1.record(stream)
+        stream.synchronize()
+        gemm_ms[exact] = e0.elapsed_time(e1) / (reps * len(cw))
+    if rank != 0:
+        return None
+    fl = prefill_flops(cfg, T, kinds)
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        peak_burst, peak_sus, peak_kind = float(pk["bf16_tflops"]), float(pk["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        peak_burst, peak_sus, peak_kind = 1900.0, 1700.0, "fallback"
+    step_tf = fl["gemm"] / (ms * 1e-3) / 1e12
+    gemm_tf = fl["gate_proj_one"] / (gemm_ms[False] * 1e-3) / 1e12
+    gemm_tf_x = fl["gate_proj_one"] / (gemm_ms[True] * 1e-3) / 1e12
+    n_fa, n_gdn = kinds.count("fa"), kinds.count("gdn")
+    return {
+        "metric": "prefill tok/s (32-layer 4B-shape stack, one prompt from position 0); tensor TFLOP/s vs peak",
+        "value": round(T / (ms * 1e-3), 1), "unit": "tok/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16-dequantised-weight/bf16-act/fp32-acc", "data": "synthetic",
+        "config": {"workload": f"qwen3.5-4b-shape 32-layer prefill of a {T}-token prompt from position 0",
+                   "prompt_tokens": T, "layers": "24 gated-deltanet + 8 full-attention (i % 4 == 3)",
+                   "l2": "inputs larger than L2: 3.79 GB of weights per step",
+                   "flops_per_step": fl, "device_status": status, "setup_s": round(setup_s, 1),
+                   "gemm_alone": {"matrix": "9216x2560", "tokens": T, "us": round(gemm_ms[False] * 1e3, 2),
+                                  "tflops": round(gemm_tf, 1), "frac_of_burst_peak": round(gemm_tf / peak_burst, 4),
+                                  "exact_us": round(gemm_ms[True] * 1e3, 2),
+                                  "exact_tflops": round(gemm_tf_x, 1),
+                                  "exact_note": "hi + lo bf16 weights: two MMAs per weight; the tensor work is "
+                                                "twice the useful FLOPs counted here"}},
+        "roofline": {"bound": "tensor", "achieved": round(gemm_tf, 1), "peak": peak_burst, "unit": "TFLOP/s",
+                     "frac": round(gemm_tf / peak_burst, 4), "traffic": None,
+                     "kernel": f"gemm_kernel alone: the 9216x2560 gate_proj over the {T}-token prompt (bf16 "
+                               "weights), 2 T N K FLOPs per launch over its CUDA-event time",
+                     "peak_kind": peak_kind + " (burst bf16)",
+                     "step_tflops": round(step_tf, 1), "step_frac_of_sustained": round(step_tf / peak_sus, 4)},
+        "e2e": {"value": round(T / (e2e_ms * 1e-3), 1), "unit": "tok/s", "ms_per_step": round(e2e_ms, 4),
+                "h2d_bytes_per_step": T * E * 2, "d2h_bytes_per_step": T * E * 2},
+        "gpu_launches": args.steps * (12 * n_fa + 15 * n_gdn),
+        "clocks": clk.summary(),
+    }
+
+
 # ---------------------------------------------------------------------- CPU oracle
 
 
@@ -531,6 +681,8 @@ def main():
     ap.add_argument("--prefill", type=int, default=PREFILL, help="KV tokens before the first step (batch 1)")
     ap.add_argument("--kv", choices=["bf16", "turbo8"], default="bf16", help="KV cache format")
     ap.add_argument("--paged", action="store_true", help="paged bf16 KV (16-token blocks, shuffled table)")
+    ap.add_argument("--prompt", type=int, default=0,
+                    help="time the multi-token prefill of a prompt of this many tokens instead of decode")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -554,6 +706,18 @@ def main():
         print(json.dumps(res))
         return
 
+    if args.prompt > 0:
+        res = run_prompt(args)
+        if res is None:
+            return
+        if args.cpu_steps > 0:  # the oracle's prefill is its single-token forward per token
+            cb = cpu_baseline(args.cpu_steps)
+            cb["sample"] = "the oracle's prefill runs its single-token forward token after token: " + cb["sample"]
+            res["cpu_baseline"] = cb
+        else:
+            res["cpu_baseline"] = None
+        print(json.dumps(res))
+        return
     res = run_gpu(args)
     if res is None:
         return

@@ -125,6 +125,14 @@ _SIGS = {
     "qwen35_lm_head_greedy": (C.c_int, [C.POINTER(qwen35_config), _P, C.POINTER(qwen35_qweight), _P, _P, _P, _P,
                                         C.c_size_t, _P]),
     "qwen35_read_static_status": (C.c_int, [C.POINTER(C.c_int32), _P]),
+    "qwen35_prefill_scratch_bytes": (C.c_size_t, [C.POINTER(qwen35_config), _U]),
+    "qwen35_prefill_gemm": (C.c_int, [C.POINTER(qwen35_qweight), _P, _P, _U, C.c_int, _P, C.c_size_t, _P]),
+    "qwen35_prefill_full_attention": (C.c_int, [C.POINTER(qwen35_config), C.POINTER(qwen35_fa_layer), _P,
+                                                C.c_size_t, C.POINTER(qwen35_kv_cache), _P, _P, _U, _U, _P]),
+    "qwen35_prefill_linear_attention": (C.c_int, [C.POINTER(qwen35_config), C.POINTER(qwen35_gdn_layer), _P,
+                                                  C.c_size_t, C.POINTER(qwen35_gdn_state), _P, _P, _U, _P]),
+    "qwen35_prefill_step": (C.c_int, [C.POINTER(qwen35_config), C.POINTER(qwen35_layer), _U, _P, C.c_size_t,
+                                      _P, _P, _U, _U, _P]),
     "qwen35_debug_scratch_offset": (C.c_size_t, [C.POINTER(qwen35_config), C.c_int, C.c_char_p]),
     "qwen35_debug_stack_scratch_offset": (C.c_size_t, [C.POINTER(qwen35_config), C.c_char_p]),
     "qwen35_debug_stage_dump": (C.c_int, [C.c_int]),
@@ -308,6 +316,33 @@ class Graph:
             self.close()
         except Exception:
             pass
+
+
+def qwen35_prefill_gemm(w, X, Y, n_tokens, scratch, stream=None, exact: bool = True):
+    return lib().qwen35_prefill_gemm(C.byref(w), _ptr(X), _ptr(Y), n_tokens, 1 if exact else 0, _ptr(scratch),
+                                     scratch.numel(), _stream(stream))
+
+
+def qwen35_prefill_scratch_bytes(cfg: qwen35_config, max_tokens: int) -> int:
+    return lib().qwen35_prefill_scratch_bytes(C.byref(cfg), max_tokens)
+
+
+def qwen35_prefill_full_attention(cfg, layer, scratch, kv, x_in, x_out, cache_pos, n_tokens, stream=None):
+    return lib().qwen35_prefill_full_attention(C.byref(cfg), C.byref(layer), _ptr(scratch), scratch.numel(),
+                                               C.byref(kv), _ptr(x_in), _ptr(x_out), cache_pos, n_tokens,
+                                               _stream(stream))
+
+
+def qwen35_prefill_linear_attention(cfg, layer, scratch, state, x_in, x_out, n_tokens, stream=None):
+    return lib().qwen35_prefill_linear_attention(C.byref(cfg), C.byref(layer), _ptr(scratch), scratch.numel(),
+                                                 C.byref(state), _ptr(x_in), _ptr(x_out), n_tokens,
+                                                 _stream(stream))
+
+
+def qwen35_prefill_step(cfg, layers, scratch, x_in, x_out, cache_pos, n_tokens, stream=None):
+    arr = (qwen35_layer * len(layers))(*layers)
+    return lib().qwen35_prefill_step(C.byref(cfg), arr, len(layers), _ptr(scratch), scratch.numel(), _ptr(x_in),
+                                     _ptr(x_out), cache_pos, n_tokens, _stream(stream))
 
 
 def qwen35_gemv(w, x, y, scratch, stream=None):

@@ -15,6 +15,7 @@
 #include "qwen35_decode.h"  // include/ (on the include path)
 #include "common.cuh"
 #include "decode.h"
+#include "prefill.h"
 
 using namespace q35;
 
@@ -771,6 +772,291 @@ int qwen35_dequant(const qwen35_qweight* w, float* out, void* stream) {
                         (cudaStream_t)stream) == cudaSuccess
              ? QWEN35_OK
              : QWEN35_ERR_CUDA;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------- prefill
+
+namespace {
+
+// Scratch of a prefill of up to T tokens after the status word: per-token buffers
+// (bf16 unless noted), each 256-byte aligned; both layer kinds' buffers, so one
+// scratch serves a stack.
+struct PfLayout {
+  size_t xn, xr, o, g, u;                                // [T][E] x3, [T][I] x2
+  size_t qf, k, v, qr, ga;                               // full attention
+  size_t dt, bb, qkv, z, qs, gb, act, y, yin;            // linear attention (gb, act fp32)
+  size_t total;
+};
+PfLayout pf_layout(const Dims& d, uint32_t T) {
+  PfLayout L = {};
+  size_t off = 256;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += (bytes + 255) / 256 * 256;
+    return o;
+  };
+  const size_t t = T;
+  L.xn = take(t * d.E * 2);
+  L.xr = take(t * d.E * 2);
+  L.o = take(t * d.E * 2);
+  L.g = take(t * d.I * 2);
+  L.u = take(t * d.I * 2);
+  L.qf = take(t * 2 * d.H * d.D * 2);
+  L.k = take(t * d.Hkv * d.D * 2);
+  L.v = take(t * d.Hkv * d.D * 2);
+  L.qr = take(t * d.H * d.D * 2);
+  L.ga = take(t * d.H * d.D * 2);
+  L.dt = take(t * d.Hv * 2);
+  L.bb = take(t * d.Hv * 2);
+  L.qkv = take(t * d.C * 2);
+  L.z = take(t * d.Z * 2);
+  L.qs = take(t * d.C * 2);
+  L.gb = take(t * d.Hv * 2 * 4);
+  L.act = take(t * d.C * 4);
+  L.y = take(t * d.Z * 2);
+  L.yin = take(t * d.Z * 2);
+  L.total = off;
+  return L;
+}
+
+constexpr uint32_t kMaxPrefillTokens = 65536;
+
+struct PfCtx {
+  const qwen35_config* cfg;
+  Dims d;
+  uint8_t* s;  // scratch
+  PfLayout L;
+  uint32_t T;
+  cudaStream_t st;
+  uint16_t* b16(size_t off) const { return reinterpret_cast<uint16_t*>(s + off); }
+  float* f32(size_t off) const { return reinterpret_cast<float*>(s + off); }
+  int* status() const { return reinterpret_cast<int*>(s); }
+};
+
+// The checks every prefill entry shares: config, scratch size, token count, x.
+int pf_begin(PfCtx& c, const qwen35_config* cfg, void* scratch, size_t scratch_bytes, const void* x_in,
+             const void* x_out, uint32_t T, cudaStream_t st) {
+  int r = check_config(cfg, c.d);
+  if (r) return r;
+  if (T == 0 || T > kMaxPrefillTokens || !aligned16(scratch) || !aligned16(x_in) || !aligned16(x_out))
+    return QWEN35_ERR_INVALID_ARGUMENT;
+  c.cfg = cfg;
+  c.L = pf_layout(c.d, T);
+  if (scratch_bytes < c.L.total) return QWEN35_ERR_INVALID_ARGUMENT;
+  c.s = static_cast<uint8_t*>(scratch);
+  c.T = T;
+  c.st = st;
+  return QWEN35_OK;
+}
+
+int cu(cudaError_t e) { return e == cudaSuccess ? QWEN35_OK : QWEN35_ERR_CUDA; }
+
+// A prefill projection. exact: the weights to 2^-16 (the projections whose outputs
+// are kept: k_proj and v_proj fill the KV cache, in_proj_qkv/a/b drive the conv and
+// delta-rule states); otherwise bf16-rounded weights.
+int pf_gemm(const PfCtx& c, const qwen35_qweight& w, const uint16_t* X, uint16_t* Y, const uint16_t* R,
+            bool exact) {
+  q35pf::Gemm g;
+  g.X = X;
+  g.codes = w.codes;
+  g.scales = w.scales;
+  g.biases = w.biases;
+  g.Y = Y;
+  g.R = R;
+  g.ldx = w.k;
+  g.ldy = w.n;
+  g.gstride = gstride_of(w.k);
+  g.N = w.n;
+  g.K = w.k;
+  g.T = c.T;
+  g.status = c.status();
+  g.wait_ns = g_wait_ns;
+  g.exact = exact;
+  return cu(q35pf::gemm(g, c.st));
+}
+
+// x_out = x_resid + down(SiLU(gate) * up) with x_resid = bf16(x_in + delta) and
+// the MLP input RMSNorm(x_resid) * post_ln. x_in is last read before x_out is
+// written, so the two may be one buffer.
+int pf_mlp(const PfCtx& c, const uint16_t* x_in, const uint16_t* delta, const uint16_t* post_ln,
+           const qwen35_qweight& gate, const qwen35_qweight& up, const qwen35_qweight& down, uint16_t* x_out) {
+  const Dims& d = c.d;
+  uint16_t *xn = c.b16(c.L.xn), *xr = c.b16(c.L.xr), *g = c.b16(c.L.g), *u = c.b16(c.L.u);
+  int r = cu(q35pf::rmsnorm(x_in, delta, xr, post_ln, xn, c.T, d.E, c.cfg->rms_eps, c.st));
+  if (!r) r = pf_gemm(c, gate, xn, g, nullptr, false);
+  if (!r) r = pf_gemm(c, up, xn, u, nullptr, false);
+  if (!r) r = cu(q35pf::silu_mul(g, u, g, (size_t)c.T * d.I, c.st));
+  if (!r) r = pf_gemm(c, down, g, x_out, xr, false);
+  return r;
+}
+
+int pf_fa(const PfCtx& c, const qwen35_fa_layer* l, const qwen35_kv_cache* kv, const uint16_t* x_in,
+          uint16_t* x_out, uint32_t p0) {
+  const Dims& d = c.d;
+  uint16_t *xn = c.b16(c.L.xn), *qf = c.b16(c.L.qf), *k = c.b16(c.L.k), *v = c.b16(c.L.v);
+  int r = cu(q35pf::rmsnorm(x_in, nullptr, nullptr, l->input_ln, xn, c.T, d.E, c.cfg->rms_eps, c.st));
+  if (!r) r = pf_gemm(c, l->q_proj, xn, qf, nullptr, false);
+  if (!r) r = pf_gemm(c, l->k_proj, xn, k, nullptr, true);
+  if (!r) r = pf_gemm(c, l->v_proj, xn, v, nullptr, true);
+  if (r) return r;
+  q35pf::Attn a = {};
+  a.qf = qf;
+  a.k = k;
+  a.v = v;
+  a.q_norm = l->q_norm;
+  a.k_norm = l->k_norm;
+  a.qr = c.b16(c.L.qr);
+  a.kc = static_cast<uint16_t*>(kv->k);
+  a.vc = static_cast<uint16_t*>(kv->v);
+  a.ga = c.b16(c.L.ga);
+  a.T = c.T;
+  a.p0 = p0;
+  a.H = d.H;
+  a.Hkv = d.Hkv;
+  a.D = d.D;
+  a.R = d.R;
+  a.eps = c.cfg->rms_eps;
+  for (uint32_t i = 0; i < d.R / 2 && i < 128; ++i)  // theta^(-2i/R) in double, kept fp32
+    a.inv_freq[i] = (float)std::pow((double)c.cfg->rope_theta, -2.0 * (double)i / (double)d.R);
+  r = cu(q35pf::attention(a, c.st));
+  if (!r) r = pf_gemm(c, l->o_proj, a.ga, c.b16(c.L.o), nullptr, false);
+  if (!r) r = pf_mlp(c, x_in, c.b16(c.L.o), l->post_ln, l->gate_proj, l->up_proj, l->down_proj, x_out);
+  return r;
+}
+
+int pf_gdn(const PfCtx& c, const qwen35_gdn_layer* l, const qwen35_gdn_state* st, const uint16_t* x_in,
+           uint16_t* x_out) {
+  const Dims& d = c.d;
+  uint16_t* xn = c.b16(c.L.xn);
+  q35pf::Gdn g = {};
+  g.qkv = c.b16(c.L.qkv);
+  g.z = c.b16(c.L.z);
+  g.dt_raw = c.b16(c.L.dt);
+  g.b_raw = c.b16(c.L.bb);
+  int r = cu(q35pf::rmsnorm(x_in, nullptr, nullptr, l->input_ln, xn, c.T, d.E, c.cfg->rms_eps, c.st));
+  if (!r) r = pf_gemm(c, l->in_proj_a, xn, c.b16(c.L.dt), nullptr, true);
+  if (!r) r = pf_gemm(c, l->in_proj_b, xn, c.b16(c.L.bb), nullptr, true);
+  if (!r) r = pf_gemm(c, l->in_proj_qkv, xn, c.b16(c.L.qkv), nullptr, true);
+  if (!r) r = pf_gemm(c, l->in_proj_z, xn, c.b16(c.L.z), nullptr, false);
+  if (r) return r;
+  g.conv_w = l->conv1d_weight;
+  g.a_log = l->a_log;
+  g.dt_bias = l->dt_bias;
+  g.norm_w = l->norm_weight;
+  g.conv_state = st->conv_state;
+  g.ssm = st->gdn_state;
+  g.qs = c.b16(c.L.qs);
+  g.act = c.f32(c.L.act);
+  g.gb = c.f32(c.L.gb);
+  g.y = c.b16(c.L.y);
+  g.yin = c.b16(c.L.yin);
+  g.T = c.T;
+  g.Hk = d.Hk;
+  g.Hv = d.Hv;
+  g.Dk = d.Dk;
+  g.Dv = d.Dv;
+  g.Kc = d.Kc;
+  g.C = d.C;
+  g.eps = c.cfg->rms_eps;
+  r = cu(q35pf::gdn(g, c.st));
+  if (!r) r = pf_gemm(c, l->out_proj, g.yin, c.b16(c.L.o), nullptr, false);
+  if (!r) r = pf_mlp(c, x_in, c.b16(c.L.o), l->post_ln, l->gate_proj, l->up_proj, l->down_proj, x_out);
+  return r;
+}
+
+// A prefill's KV cache: bf16, contiguous rows, room for positions [p0, p0 + T).
+int pf_kv_ok(const qwen35_kv_cache* kv, uint32_t p0, uint32_t T) {
+  if (!kv_ok(kv)) return QWEN35_ERR_INVALID_ARGUMENT;
+  if (kv->dtype != QWEN35_KV_BF16 || kv->block_table) return QWEN35_ERR_UNSUPPORTED;
+  if ((uint64_t)p0 + T > kv->capacity) return QWEN35_ERR_OUT_OF_RANGE;
+  return QWEN35_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int qwen35_prefill_gemm(const qwen35_qweight* w, const qwen35_bf16* X, qwen35_bf16* Y, uint32_t n_tokens,
+                        int exact, void* scratch, size_t scratch_bytes, void* stream) {
+  if (!w || !aligned16(X) || !aligned16(Y) || !aligned16(scratch) || scratch_bytes < 256)
+    return QWEN35_ERR_INVALID_ARGUMENT;
+  if (!qw_ok(*w, w->n, w->k) || w->n == 0 || w->k == 0 || w->k % 64 || n_tokens == 0 ||
+      n_tokens > kMaxPrefillTokens)
+    return QWEN35_ERR_INVALID_ARGUMENT;
+  if (num_sms() <= 0) return QWEN35_ERR_CUDA;
+  PfCtx c = {};
+  c.s = static_cast<uint8_t*>(scratch);
+  c.T = n_tokens;
+  c.st = (cudaStream_t)stream;
+  return pf_gemm(c, *w, X, Y, nullptr, exact != 0);
+}
+
+size_t qwen35_prefill_scratch_bytes(const qwen35_config* cfg, uint32_t max_tokens) {
+  Dims d;
+  if (check_config(cfg, d) || max_tokens == 0 || max_tokens > kMaxPrefillTokens) return 0;
+  return pf_layout(d, max_tokens).total;
+}
+
+int qwen35_prefill_full_attention(const qwen35_config* cfg, const qwen35_fa_layer* layer, void* scratch,
+                                  size_t scratch_bytes, const qwen35_kv_cache* kv, const qwen35_bf16* x_in,
+                                  qwen35_bf16* x_out, uint32_t cache_pos, uint32_t n_tokens, void* stream) {
+  PfCtx c;
+  int r = pf_begin(c, cfg, scratch, scratch_bytes, x_in, x_out, n_tokens, (cudaStream_t)stream);
+  if (!r) r = check_fa_dims(cfg, c.d);
+  if (!r) r = check_fa_layer(layer, c.d);
+  if (!r) r = pf_kv_ok(kv, cache_pos, n_tokens);
+  if (r) return r;
+  if (num_sms() <= 0) return QWEN35_ERR_CUDA;
+  return pf_fa(c, layer, kv, x_in, x_out, cache_pos);
+}
+
+int qwen35_prefill_linear_attention(const qwen35_config* cfg, const qwen35_gdn_layer* layer, void* scratch,
+                                    size_t scratch_bytes, const qwen35_gdn_state* state, const qwen35_bf16* x_in,
+                                    qwen35_bf16* x_out, uint32_t n_tokens, void* stream) {
+  PfCtx c;
+  int r = pf_begin(c, cfg, scratch, scratch_bytes, x_in, x_out, n_tokens, (cudaStream_t)stream);
+  if (!r) r = check_gdn_dims(c.d);
+  if (!r) r = check_gdn_layer(layer, c.d);
+  if (!r && (!state || !aligned16(state->conv_state) || !aligned16(state->gdn_state)))
+    r = QWEN35_ERR_INVALID_ARGUMENT;
+  if (r) return r;
+  if (num_sms() <= 0) return QWEN35_ERR_CUDA;
+  return pf_gdn(c, layer, state, x_in, x_out);
+}
+
+int qwen35_prefill_step(const qwen35_config* cfg, const qwen35_layer* layers, uint32_t num_layers, void* scratch,
+                        size_t scratch_bytes, const qwen35_bf16* x_in, qwen35_bf16* x_out, uint32_t cache_pos,
+                        uint32_t n_tokens, void* stream) {
+  PfCtx c;
+  int r = pf_begin(c, cfg, scratch, scratch_bytes, x_in, x_out, n_tokens, (cudaStream_t)stream);
+  if (r) return r;
+  if (!layers || num_layers == 0) return QWEN35_ERR_INVALID_ARGUMENT;
+  for (uint32_t i = 0; i < num_layers && !r; ++i) {  // every layer checked before anything is enqueued
+    const qwen35_layer& L = layers[i];
+    if (L.kind == QWEN35_LAYER_FULL_ATTENTION) {
+      r = check_fa_dims(cfg, c.d);
+      if (!r) r = check_fa_layer(L.fa, c.d);
+      if (!r) r = pf_kv_ok(L.kv, cache_pos, n_tokens);
+    } else if (L.kind == QWEN35_LAYER_LINEAR_ATTENTION) {
+      r = check_gdn_dims(c.d);
+      if (!r) r = check_gdn_layer(L.gdn, c.d);
+      if (!r && (!L.state || !aligned16(L.state->conv_state) || !aligned16(L.state->gdn_state)))
+        r = QWEN35_ERR_INVALID_ARGUMENT;
+    } else {
+      r = QWEN35_ERR_INVALID_ARGUMENT;
+    }
+  }
+  if (r) return r;
+  if (num_sms() <= 0) return QWEN35_ERR_CUDA;
+  for (uint32_t i = 0; i < num_layers && !r; ++i) {
+    const uint16_t* xi = i == 0 ? x_in : x_out;
+    const qwen35_layer& L = layers[i];
+    r = L.kind == QWEN35_LAYER_FULL_ATTENTION ? pf_fa(c, L.fa, L.kv, xi, x_out, cache_pos)
+                                              : pf_gdn(c, L.gdn, L.state, xi, x_out);
+  }
+  return r;
 }
 
 }  // extern "C"

@@ -345,6 +345,62 @@ QWEN35_API int qwen35_graph_create_batched(const qwen35_config* cfg, const qwen3
                         int32_t* d_cache_pos, uint32_t max_seq_len, void* stream,
                         qwen35_graph** out_graph);
 
+/* Multi-token prefill: the n_tokens tokens of a prompt through a layer (or a
+ * stack) in one call, the step before decode that the module page "Module
+ * qwen3_5" leaves out of the single-token path (its non-goals: multi-token
+ * prefill). Token t of the prompt sits at position cache_pos + t and computes
+ * exactly what the single-token forward computes for it after tokens 0 .. t-1
+ * (full attention: append at cache_pos + t, attention over cache_pos + t + 1
+ * tokens; linear attention: the conv and delta-rule states advanced token by
+ * token), so a prefill of n tokens equals n single-token calls in order, up to
+ * the rounding below.
+ *  - x_in, x_out: bf16 [n_tokens][hidden] (x_out may equal x_in); every token's
+ *    output is written.
+ *  - Projections run as tensor-core GEMMs over all tokens at once, each GEMM
+ *    input a bf16 vector. The projections whose outputs are kept (k_proj and
+ *    v_proj fill the KV cache; in_proj_qkv, in_proj_a, in_proj_b drive the conv
+ *    and delta-rule states) multiply each dequantised weight w = scale * code +
+ *    bias as the sum of two bf16 values (bf16(w) + bf16(w - bf16(w)): w to 2^-16
+ *    relative), so the caches and states match the single-token path's; the
+ *    others multiply bf16(w) (relative 2^-9 per weight). The inputs the
+ *    single-token path keeps unrounded inside its fused kernels (SiLU(gate) * up
+ *    before down_proj, SiLU(z) * y_norm before out_proj) are rounded to bf16
+ *    here. Both stay far inside the layer tolerance.
+ *  - KV cache: bf16, contiguous rows only (no Turbo8, no block table:
+ *    QWEN35_ERR_UNSUPPORTED); rows [cache_pos, cache_pos + n_tokens) are
+ *    written, rows [0, cache_pos) read; cache_pos + n_tokens > capacity is
+ *    QWEN35_ERR_OUT_OF_RANGE.
+ *  - Scratch: qwen35_prefill_scratch_bytes(cfg, max_tokens) for any n_tokens up to
+ *    max_tokens (its first 4 bytes are the device status word, as for decode);
+ *    at most 65536 tokens per call.
+ *  - The stack form runs layer i on layer i-1's output, all at positions
+ *    cache_pos .. cache_pos + n_tokens - 1 (nothing is advanced in device memory).
+ * Errors: INVALID_ARGUMENT (null or misaligned pointer, n_tokens 0 or above 65536,
+ * scratch too small, shape mismatch), OUT_OF_RANGE, UNSUPPORTED, CUDA. Calls only
+ * enqueue work on `stream`. */
+QWEN35_API size_t qwen35_prefill_scratch_bytes(const qwen35_config* cfg, uint32_t max_tokens);
+QWEN35_API int qwen35_prefill_full_attention(const qwen35_config* cfg, const qwen35_fa_layer* layer,
+                                             void* scratch, size_t scratch_bytes, const qwen35_kv_cache* kv,
+                                             const qwen35_bf16* x_in, qwen35_bf16* x_out, uint32_t cache_pos,
+                                             uint32_t n_tokens, void* stream);
+QWEN35_API int qwen35_prefill_linear_attention(const qwen35_config* cfg, const qwen35_gdn_layer* layer,
+                                               void* scratch, size_t scratch_bytes, const qwen35_gdn_state* state,
+                                               const qwen35_bf16* x_in, qwen35_bf16* x_out, uint32_t n_tokens,
+                                               void* stream);
+QWEN35_API int qwen35_prefill_step(const qwen35_config* cfg, const qwen35_layer* layers, uint32_t num_layers,
+                                   void* scratch, size_t scratch_bytes, const qwen35_bf16* x_in,
+                                   qwen35_bf16* x_out, uint32_t cache_pos, uint32_t n_tokens, void* stream);
+
+/* The prefill's projection on its own: Y[t][r] = bf16(sum_c W[r][c] X[t][c]) for
+ * t < n_tokens, r < w->n, with w = scales[r][c/64] * codes[r][c] + biases[r][c/64]
+ * taken as W = bf16(w) + bf16(w - bf16(w)) (w to 2^-16 relative) when exact is
+ * nonzero, else as W = bf16(w); fp32 accumulation on the tensor cores. X bf16
+ * [n_tokens][k], Y bf16 [n_tokens][n], device pointers, 16-byte aligned; scratch:
+ * at least 256 bytes (its status word). Errors: INVALID_ARGUMENT, CUDA. */
+QWEN35_API int qwen35_prefill_gemm(const qwen35_qweight* w, const qwen35_bf16* X, qwen35_bf16* Y,
+                                   uint32_t n_tokens, int exact, void* scratch, size_t scratch_bytes,
+                                   void* stream);
+
 /* The quantised GEMV on its own (QuantWeights::gemv): y[n] = bf16(W x), x bf16 [k]. */
 QWEN35_API int qwen35_gemv(const qwen35_qweight* w, const qwen35_bf16* x, qwen35_bf16* y, void* scratch,
                 size_t scratch_bytes, void* stream);

@@ -236,3 +236,37 @@ def test_batched_layer_forwards_argument_errors():
     rc = L.qwen35_forward_linear_attention_batched(C.byref(c), None, 2, scr.data_ptr(), scr.numel(), None,
                                                    _FAKE * 7, _FAKE * 8, None)
     assert rc == B.QWEN35_ERR_INVALID_ARGUMENT
+
+
+def test_prefill_argument_errors_precede_launch():
+    """Prefill entries: scratch sized per token count, range and format checks
+    before anything is enqueued; a well-formed call without a device is a CUDA error."""
+    import torch
+    cfg = synth.config("tiny")
+    c = B.make_config(cfg)
+    s8, s16 = B.qwen35_prefill_scratch_bytes(c, 8), B.qwen35_prefill_scratch_bytes(c, 16)
+    assert 0 < s8 < s16
+    assert B.qwen35_prefill_scratch_bytes(c, 0) == 0 and B.qwen35_prefill_scratch_bytes(c, 65537) == 0
+    fa = _fake_fa(cfg)
+    kv = B.qwen35_kv_cache(_FAKE * 5, _FAKE * 6, 16)
+    S = _FakeScratch(s8)
+    x, y = _FAKE * 7, _FAKE * 8
+    f = B.qwen35_prefill_full_attention
+    assert f(c, fa, S, kv, x, y, 9, 8, 0) == B.QWEN35_ERR_OUT_OF_RANGE        # rows 9..16 past capacity 16
+    assert f(c, fa, S, kv, x, y, 0, 9, 0) == B.QWEN35_ERR_INVALID_ARGUMENT    # scratch for 8 tokens
+    assert f(c, fa, S, kv, x, y, 0, 0, 0) == B.QWEN35_ERR_INVALID_ARGUMENT    # no tokens
+    assert f(c, fa, S, kv, x + 2, y, 0, 8, 0) == B.QWEN35_ERR_INVALID_ARGUMENT
+    t8 = B.qwen35_kv_cache(_FAKE * 5, _FAKE * 6, 16, 1, _FAKE * 3, _FAKE * 4)
+    assert f(c, fa, S, t8, x, y, 0, 8, 0) == B.QWEN35_ERR_UNSUPPORTED         # Turbo8 cache
+    paged = B.qwen35_kv_cache(_FAKE * 5, _FAKE * 6, 16, 0, None, None, _FAKE * 2, 8)
+    assert f(c, fa, S, paged, x, y, 0, 8, 0) == B.QWEN35_ERR_UNSUPPORTED      # block table
+    g = B.qwen35_gdn_layer()
+    st = B.qwen35_gdn_state(_FAKE * 5, _FAKE * 6)
+    assert B.qwen35_prefill_linear_attention(c, g, S, st, x, y, 8, 0) == B.QWEN35_ERR_INVALID_ARGUMENT
+    bad_layer = B.qwen35_layer(9, None, None, None, None)
+    assert B.qwen35_prefill_step(c, [bad_layer], S, x, y, 0, 8, 0) == B.QWEN35_ERR_INVALID_ARGUMENT
+    w = B.qwen35_qweight(_FAKE * 1, _FAKE * 2, _FAKE * 3, 100, 256)
+    assert B.qwen35_prefill_gemm(w, x, y, 0, S, 0, True) == B.QWEN35_ERR_INVALID_ARGUMENT
+    if not torch.cuda.is_available():
+        assert f(c, fa, S, kv, x, y, 0, 8, 0) == B.QWEN35_ERR_CUDA
+        assert B.qwen35_prefill_gemm(w, x, y, 4, S, 0, False) == B.QWEN35_ERR_CUDA
