@@ -581,7 +581,7 @@ def run_prompt(args) -> dict | None:
                      "step_tflops": round(step_tf, 1), "step_frac_of_sustained": round(step_tf / peak_sus, 4)},
         "e2e": {"value": round(T / (e2e_ms * 1e-3), 1), "unit": "tok/s", "ms_per_step": round(e2e_ms, 4),
                 "h2d_bytes_per_step": T * E * 2, "d2h_bytes_per_step": T * E * 2},
-        "gpu_launches": args.steps * (12 * n_fa + 15 * n_gdn),
+        "gpu_launches": args.steps * (12 * n_fa + 16 * n_gdn),
         "clocks": clk.summary(),
     }
 

@@ -33,14 +33,18 @@ namespace {
 // engine (the token tile and the raw codes, 128 rows of 64 bytes, both swizzled
 // by the copy itself), filled kAhead blocks ahead, and two stages of dequantised weight
 // tiles (hi, lo) written by the CTA's threads.
-constexpr uint32_t kBM = 128, kBN = 256, kGemmThreads = 256;
+constexpr uint32_t kBM = 128, kBN = 256, kDqThreads = 256, kGemmThreads = kDqThreads + 32;
 constexpr uint32_t kRaw = 4, kAhead = kRaw - 2;
 constexpr uint32_t kTileBytes = kBM * 64 * 2;  // a weight tile (hi or lo)
 constexpr uint32_t kXBytes = kBN * 64 * 2;     // a token tile
 constexpr uint32_t kCodeBytes = kBM * 64;
 constexpr uint32_t kRawBytes = kXBytes + kCodeBytes;
-constexpr uint32_t kWBytes = 2 * kTileBytes;
-constexpr uint32_t kGemmSmem = kRaw * kRawBytes + 2 * kWBytes + 1024;  // + alignment slack
+// weight stages: two of hi + lo (exact form) or four of hi (plain form), 64 KiB
+template <bool EXACT>
+struct WStages {
+  static constexpr uint32_t n = EXACT ? 2 : 4, bytes = EXACT ? 2 * kTileBytes : kTileBytes;
+};
+constexpr uint32_t kGemmSmem = kRaw * kRawBytes + 4 * kTileBytes + 1024;  // + alignment slack
 
 __device__ __forceinline__ uint32_t sw_off(uint32_t r, uint32_t j) { return r * 128 + ((j ^ (r & 7)) << 4); }
 
@@ -161,30 +165,34 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
-// One CTA: rows [n0, n0 + 128) x tokens [t0, t0 + 256). Thread 0 copies each
-// K-block's token tile and codes kAhead blocks ahead (one barrier per raw slot,
-// completed by the copies' byte count) and issues the block's eight K=16 MMAs (hi
-// and lo weights), committed to the slot's second barrier. Thread (r, half)
-// dequantises half of weight row n0 + r's codes of the current block into the
-// weight stage. The commit's arrival frees both the raw slot (refilled kAhead
-// blocks later) and the weight stage (rewritten two blocks later).
+// One CTA: rows [n0, n0 + 128) x tokens [t0, t0 + 256), nine warps. Warps 0-7
+// dequantise: thread (r, half) turns half of weight row n0 + r's codes of each
+// K-block into the block's weight stage and arrives on the stage's barrier. Lane 0
+// of warp 8 copies each K-block's token tile and codes kAhead blocks ahead (one
+// barrier per raw slot, completed by the copies' byte count) and, once a block's
+// copies have landed and its weight stage is complete, issues its K=16 MMAs (hi,
+// and lo in the exact form) and commits them to the raw slot's second barrier,
+// whose arrival frees the raw slot (refilled kAhead blocks later) and the weight
+// stage (rewritten WStages::n blocks later). No barrier of the whole CTA inside the
+// loop: the dequantising warps run ahead of the MMAs as far as the stages allow.
 template <bool EXACT>
 __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_constant__ GemmArgs A) {
+  using WS = WStages<EXACT>;
   const Gemm& g = A.g;
   extern __shared__ __align__(16) uint8_t smem[];
-  __shared__ uint64_t full[kRaw], done[kRaw];
+  __shared__ uint64_t full[kRaw], done[kRaw], wready[4];
   __shared__ uint32_t s_tmem;
   const uint32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t n0 = blockIdx.x * kBM, t0 = blockIdx.y * kBN;
-  const uint32_t r = tid & 127, half = tid >> 7;
   if (tid == 0) {
     for (uint32_t s = 0; s < kRaw; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&done[s], 1);
     }
+    for (uint32_t s = 0; s < 4; ++s) mbar_init(&wready[s], kDqThreads);
     mbar_fence_init();
   }
-  if (warp == 0) {
+  if (warp == 8) {
     tmem_alloc(&s_tmem, kBN);
     tmem_relinquish();
   }
@@ -193,102 +201,110 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   tc_after_sync();
   const uint32_t tmem = s_tmem;
   const uint32_t nk = g.K / 64;
-  const uint32_t n = n0 + r;
-  const bool nin = n < g.N;
-  const uint16_t* srow = g.scales + (size_t)(nin ? n : 0) * g.gstride;
-  const uint16_t* brow = g.biases + (size_t)(nin ? n : 0) * g.gstride;
-  const uint32_t j0 = 4 * half;
   // the tiles from the first 1024-byte boundary of the dynamic shared memory
   const uint32_t sraw = smem_addr(smem), sbase = (sraw + 1023u) & ~1023u;
   uint8_t* raw = smem + (sbase - sraw);
   uint8_t* wst = raw + kRaw * kRawBytes;
-  auto issue = [&](uint32_t kb) {  // thread 0: K-block kb into its raw slot
-    uint8_t* X = raw + (kb % kRaw) * kRawBytes;
-    uint64_t* bar = &full[kb % kRaw];
-    mbar_arrive_expect_tx(bar, kXBytes + kCodeBytes);
-    tma_load_2d(X, &A.tx, (int32_t)(kb * 64), (int32_t)t0, bar);
-    tma_load_2d(X + kXBytes, &A.tc, (int32_t)(kb * 64), (int32_t)n0, bar);
-  };
-  if (tid == 0)
-    for (uint32_t kb = 0; kb < kAhead && kb < nk; ++kb) issue(kb);
-  // scale and bias of the row, two blocks ahead in registers
-  uint16_t sc0 = 0, bi0 = 0, sc1 = 0, bi1 = 0;
-  if (nin) {
-    sc0 = __ldg(srow);
-    bi0 = __ldg(brow);
-    if (nk > 1) {
-      sc1 = __ldg(srow + 1);
-      bi1 = __ldg(brow + 1);
-    }
-  }
-  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
   bool ok = true;
-  for (uint32_t kb = 0; kb < nk; ++kb) {
-    const float fs = bf16f(sc0), fb = bf16f(bi0);
-    sc0 = sc1;
-    bi0 = bi1;
-    if (nin && kb + 2 < nk) {
-      sc1 = __ldg(srow + kb + 2);
-      bi1 = __ldg(brow + kb + 2);
-    }
-    // MMA(kb - 2) read the raw slot refilled now and the weight stage written now
-    if (kb >= 2 && ok && !mbar_wait_bounded(&done[(kb - 2) % kRaw], ((kb - 2) / kRaw) & 1, g.wait_ns)) {
+  auto wait = [&](uint64_t* bar, uint32_t parity) {
+    if (ok && !mbar_wait_bounded(bar, parity, g.wait_ns)) {
       set_status(g.status, kStatusTimeout);
       ok = false;
     }
-    if (tid == 0 && kb + kAhead < nk) issue(kb + kAhead);
-    if (ok && !mbar_wait_bounded(&full[kb % kRaw], (kb / kRaw) & 1, g.wait_ns)) {
-      set_status(g.status, kStatusTimeout);
-      ok = false;
-    }
-    // the codes tile arrives with the 64-byte swizzle: 16-byte chunk c of row r at
-    // chunk position c ^ ((r / 2) % 4), so a warp's 32 rows read one chunk each
-    // without bank conflicts
-    const uint8_t* Cs = raw + (kb % kRaw) * kRawBytes + kXBytes + r * 64;
-    const uint32_t sw = (r >> 1) & 3;
-    uint8_t* Wh = wst + (kb & 1) * kWBytes;
-    uint8_t* Wl = Wh + kTileBytes;
-    {
-      const uint4 a0 = *reinterpret_cast<const uint4*>(Cs + (((2 * half) ^ sw) << 4));
-      const uint4 a1 = *reinterpret_cast<const uint4*>(Cs + (((2 * half + 1) ^ sw) << 4));
-      uint4 h[4], l[4];
-      dequant8<EXACT>(a0.x, a0.y, fs, fb, h[0], l[0]);
-      dequant8<EXACT>(a0.z, a0.w, fs, fb, h[1], l[1]);
-      dequant8<EXACT>(a1.x, a1.y, fs, fb, h[2], l[2]);
-      dequant8<EXACT>(a1.z, a1.w, fs, fb, h[3], l[3]);
+  };
+  if (warp == 8) {
+    if (lane == 0) {
+      auto issue = [&](uint32_t kb) {  // K-block kb into its raw slot
+        uint8_t* X = raw + (kb % kRaw) * kRawBytes;
+        uint64_t* bar = &full[kb % kRaw];
+        mbar_arrive_expect_tx(bar, kXBytes + kCodeBytes);
+        tma_load_2d(X, &A.tx, (int32_t)(kb * 64), (int32_t)t0, bar);
+        tma_load_2d(X + kXBytes, &A.tc, (int32_t)(kb * 64), (int32_t)n0, bar);
+      };
+      for (uint32_t kb = 0; kb < kAhead && kb < nk; ++kb) issue(kb);
+      for (uint32_t kb = 0; kb < nk; ++kb) {
+        if (kb + kAhead < nk) {  // the slot's last reader was MMA(kb + kAhead - kRaw)
+          if (kb + kAhead >= kRaw) wait(&done[(kb + kAhead) % kRaw], ((kb + kAhead - kRaw) / kRaw) & 1);
+          issue(kb + kAhead);
+        }
+        wait(&full[kb % kRaw], (kb / kRaw) & 1);
+        wait(&wready[kb % WS::n], (kb / WS::n) & 1);
+        tc_after_sync();
+        const uint32_t sx = sbase + (kb % kRaw) * kRawBytes;
+        const uint32_t sh = sbase + kRaw * kRawBytes + (kb % WS::n) * WS::bytes, sl = sh + kTileBytes;
 #pragma unroll
-      for (uint32_t i = 0; i < 4; ++i) {
-        *reinterpret_cast<uint4*>(Wh + sw_off(r, j0 + i)) = nin ? h[i] : zero;
-        if (EXACT) *reinterpret_cast<uint4*>(Wl + sw_off(r, j0 + i)) = nin ? l[i] : zero;
+        for (uint32_t kk = 0; kk < 4; ++kk) {  // K = 16 per MMA: 32 bytes of each row
+          mma_bf16(tmem, smem_desc(sh + kk * 32), smem_desc(sx + kk * 32), (kb | kk) != 0);
+          if (EXACT) mma_bf16(tmem, smem_desc(sl + kk * 32), smem_desc(sx + kk * 32), 1u);
+        }
+        mma_commit(&done[kb % kRaw]);
       }
     }
-    fence_async_shared();  // the weight stores, for the tensor core
-    __syncthreads();
-    if (tid == 0) {
-      tc_after_sync();
-      const uint32_t sx = sbase + (kb % kRaw) * kRawBytes;
-      const uint32_t sh = sbase + kRaw * kRawBytes + (kb & 1) * kWBytes, sl = sh + kTileBytes;
-#pragma unroll
-      for (uint32_t kk = 0; kk < 4; ++kk) {  // K = 16 per MMA: 32 bytes of each row
-        mma_bf16(tmem, smem_desc(sh + kk * 32), smem_desc(sx + kk * 32), (kb | kk) != 0);
-        if (EXACT) mma_bf16(tmem, smem_desc(sl + kk * 32), smem_desc(sx + kk * 32), 1u);
+  } else {
+    const uint32_t r = tid & 127, half = tid >> 7;
+    const uint32_t n = n0 + r;
+    const bool nin = n < g.N;
+    const uint16_t* srow = g.scales + (size_t)(nin ? n : 0) * g.gstride;
+    const uint16_t* brow = g.biases + (size_t)(nin ? n : 0) * g.gstride;
+    const uint32_t j0 = 4 * half;
+    // scale and bias of the row, two blocks ahead in registers
+    uint16_t sc0 = 0, bi0 = 0, sc1 = 0, bi1 = 0;
+    if (nin) {
+      sc0 = __ldg(srow);
+      bi0 = __ldg(brow);
+      if (nk > 1) {
+        sc1 = __ldg(srow + 1);
+        bi1 = __ldg(brow + 1);
       }
-      mma_commit(&done[kb % kRaw]);
+    }
+    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+    for (uint32_t kb = 0; kb < nk; ++kb) {
+      const float fs = bf16f(sc0), fb = bf16f(bi0);
+      sc0 = sc1;
+      bi0 = bi1;
+      if (nin && kb + 2 < nk) {
+        sc1 = __ldg(srow + kb + 2);
+        bi1 = __ldg(brow + kb + 2);
+      }
+      // the weight stage's last reader was MMA(kb - WS::n)
+      if (kb >= WS::n) wait(&done[(kb - WS::n) % kRaw], ((kb - WS::n) / kRaw) & 1);
+      wait(&full[kb % kRaw], (kb / kRaw) & 1);
+      // the codes tile arrives with the 64-byte swizzle: 16-byte chunk c of row r at
+      // chunk position c ^ ((r / 2) % 4), so a warp's 32 rows read one chunk each
+      // without bank conflicts
+      const uint8_t* Cs = raw + (kb % kRaw) * kRawBytes + kXBytes + r * 64;
+      const uint32_t sw = (r >> 1) & 3;
+      uint8_t* Wh = wst + (kb % WS::n) * WS::bytes;
+      uint8_t* Wl = Wh + kTileBytes;
+      {
+        const uint4 a0 = *reinterpret_cast<const uint4*>(Cs + (((2 * half) ^ sw) << 4));
+        const uint4 a1 = *reinterpret_cast<const uint4*>(Cs + (((2 * half + 1) ^ sw) << 4));
+        uint4 h[4], l[4];
+        dequant8<EXACT>(a0.x, a0.y, fs, fb, h[0], l[0]);
+        dequant8<EXACT>(a0.z, a0.w, fs, fb, h[1], l[1]);
+        dequant8<EXACT>(a1.x, a1.y, fs, fb, h[2], l[2]);
+        dequant8<EXACT>(a1.z, a1.w, fs, fb, h[3], l[3]);
+#pragma unroll
+        for (uint32_t i = 0; i < 4; ++i) {
+          *reinterpret_cast<uint4*>(Wh + sw_off(r, j0 + i)) = nin ? h[i] : zero;
+          if (EXACT) *reinterpret_cast<uint4*>(Wl + sw_off(r, j0 + i)) = nin ? l[i] : zero;
+        }
+      }
+      fence_async_shared();  // the weight stores, for the tensor core
+      mbar_arrive(&wready[kb % WS::n]);
     }
   }
-  // every MMA is done when the last commit has arrived
+  // every MMA is done when the last commit has arrived; warps 0-7 read TMEM lanes
+  // 32 (w % 4) .. (their weight rows) over tokens [128 (w / 4), +128)
   const uint32_t last = nk - 1;
-  if (!mbar_wait_bounded(&done[last % kRaw], (last / kRaw) & 1, g.wait_ns)) {
-    set_status(g.status, kStatusTimeout);
-    ok = false;
+  if (warp < 8) {
+    wait(&done[last % kRaw], (last / kRaw) & 1);
+    tc_after_sync();
   }
-  tc_after_sync();
-  // epilogue: warp w reads TMEM lanes 32 (w % 4) .. (its weight rows) over tokens
-  // [128 (w / 4), +128)
   const uint32_t q = warp & 3, ch = warp >> 2;
   const uint32_t row = n0 + 32 * q + lane;
 #pragma unroll 1
-  for (uint32_t c = 0; c < kBN / 2; c += 16) {
+  for (uint32_t c = 0; warp < 8 && c < kBN / 2; c += 16) {
     float v[16];
     tmem_ld16(tmem + ((32 * q) << 16) + (kBN / 2) * ch + c, v);
     if (ok && row < g.N) {
@@ -305,7 +321,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   }
   tc_before_sync();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == 8) {
     tc_after_sync();
     tmem_dealloc(tmem, kBN);
   }
