@@ -406,6 +406,14 @@ __global__ void silu_mul_kernel(const uint16_t* g, const uint16_t* u, uint16_t* 
 
 // ------------------------------------------------------------------ full attention
 
+// The cache row (in units of token rows) of logical token t: itself, or its row in
+// the pool block the table names.
+__device__ __forceinline__ size_t cache_row(const Attn& a, uint32_t t) {
+  if (!a.btab) return t;
+  const uint32_t m = (1u << a.bt_shift) - 1u;
+  return ((size_t)(uint32_t)a.btab[t >> a.bt_shift] << a.bt_shift) | (t & m);
+}
+
 // Per (token, head slot) one warp: slots [0, H) are the q-heads (RMSNorm with
 // q_norm, RoPE, into qr), [H, H + Hkv) the k-heads (RMSNorm with k_norm, RoPE,
 // appended to the K cache), [H + Hkv, H + 2 Hkv) the v-heads (appended to the V
@@ -417,7 +425,7 @@ __global__ void __launch_bounds__(128) qk_rope_kernel(const Attn a) {
   const uint32_t item = blockIdx.x * 4 + warp;
   if (item >= a.T * slots) return;
   const uint32_t t = item / slots, sl = item % slots, D = a.D, pos = a.p0 + t;
-  const uint32_t kvrow = (pos * a.Hkv) * D;
+  const size_t kvrow = cache_row(a, pos) * a.Hkv * D;
   float* x = buf[warp];
   if (sl >= a.H + a.Hkv) {  // v: a copy into the cache
     const uint32_t g = sl - a.H - a.Hkv;
@@ -493,7 +501,7 @@ __global__ void __launch_bounds__(256) attn_kernel(const Attn a) {
       const uint32_t j = i / (D / 8), d8 = i % (D / 8);
       uint4 kv = make_uint4(0u, 0u, 0u, 0u), vv = kv;
       if (k0 + j < nkeys) {
-        const size_t off = (size_t)(k0 + j) * kvw + g * D + 8 * d8;
+        const size_t off = cache_row(a, k0 + j) * kvw + g * D + 8 * d8;
         kv = *reinterpret_cast<const uint4*>(a.kc + off);
         vv = *reinterpret_cast<const uint4*>(a.vc + off);
       }

@@ -48,9 +48,10 @@ struct Attn {
   const uint16_t* v;   // v_proj outputs [T][Hkv*D]
   const uint16_t *q_norm, *k_norm;
   uint16_t* qr;        // roped q [T][H][D] (written)
-  uint16_t *kc, *vc;   // bf16 caches [capacity][Hkv][D]
+  uint16_t *kc, *vc;   // bf16 caches [capacity][Hkv][D], or pools of 2^bt_shift-row blocks
+  const int32_t* btab; // paged: logical token t in row t % 2^bt_shift of block btab[t >> bt_shift]
   uint16_t* ga;        // gated attention [T][H*D] (written)
-  uint32_t T, p0, H, Hkv, D, R;
+  uint32_t T, p0, H, Hkv, D, R, bt_shift;
   float eps;
   float inv_freq[128];
 };

@@ -258,8 +258,8 @@ def test_prefill_argument_errors_precede_launch():
     assert f(c, fa, S, kv, x + 2, y, 0, 8, 0) == B.QWEN35_ERR_INVALID_ARGUMENT
     t8 = B.qwen35_kv_cache(_FAKE * 5, _FAKE * 6, 16, 1, _FAKE * 3, _FAKE * 4)
     assert f(c, fa, S, t8, x, y, 0, 8, 0) == B.QWEN35_ERR_UNSUPPORTED         # Turbo8 cache
-    paged = B.qwen35_kv_cache(_FAKE * 5, _FAKE * 6, 16, 0, None, None, _FAKE * 2, 8)
-    assert f(c, fa, S, paged, x, y, 0, 8, 0) == B.QWEN35_ERR_UNSUPPORTED      # block table
+    badpaged = B.qwen35_kv_cache(_FAKE * 5, _FAKE * 6, 16, 0, None, None, _FAKE * 2, 12)
+    assert f(c, fa, S, badpaged, x, y, 0, 8, 0) == B.QWEN35_ERR_INVALID_ARGUMENT  # blocks not a power of 2
     g = B.qwen35_gdn_layer()
     st = B.qwen35_gdn_state(_FAKE * 5, _FAKE * 6)
     assert B.qwen35_prefill_linear_attention(c, g, S, st, x, y, 8, 0) == B.QWEN35_ERR_INVALID_ARGUMENT

@@ -241,3 +241,56 @@ def test_prefill_argument_errors():
     assert B.qwen35_prefill_full_attention(c, dev.struct, big, kv.struct, x, y, 0, 0) == B.QWEN35_ERR_INVALID_ARGUMENT
     assert B.qwen35_prefill_full_attention(c, dev.struct, big, kv.struct, x, y, 8, 8) == 0
     torch.cuda.synchronize()
+
+
+# ------------------------------------------------------------------ paged caches, long context
+
+
+@pytest.mark.parametrize("cfg_name,capacity,n_filled,T,bt", [("tiny", 64, 5, 37, 8), ("4b", 512, 300, 150, 16)])
+def test_prefill_fa_paged_equals_contiguous(cfg_name, capacity, n_filled, T, bt):
+    """The prompt over a paged cache (blocks placed by a shuffled table, every block
+    the table does not name filled with bf16 NaN) gives the contiguous cache's
+    outputs and rows bit for bit, and the oracle's within the layer tolerance."""
+    r = PrefillFa(cfg_name, capacity=capacity, n_filled=n_filled, T=T)
+    nl = capacity // bt
+    table = synth.block_table(11, 1, nl, nl + 3)
+    paged = B.DeviceKvPaged([r.k0], [r.v0], bt, table, nl + 3, fill=0x7FC0)
+    out_p = torch.empty_like(r.x_out)
+    scr_p = B.new_scratch(B.qwen35_prefill_scratch_bytes(r.c, T))
+    assert B.qwen35_prefill_full_attention(r.c, r.dev.struct, scr_p, paged.struct, r.x_in, out_p, n_filled, T) == 0
+    got, ref = r.run(n_filled)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(bits(out_p), bits(r.x_out))
+    for t in range(T):
+        assert rel_l2(got[t], ref[t]) <= TOL_X, t
+    for w, flat in (("k", r.kv.k), ("v", r.kv.v)):
+        np.testing.assert_array_equal(paged.logical(w), bits(flat))
+        pool = paged.pool(w)
+        unused = sorted(set(range(pool.shape[0])) - set(table.reshape(-1).tolist()))
+        assert np.all(pool[unused] == 0x7FC0)
+    assert B.qwen35_read_device_status(scr_p) == 0
+
+
+def test_prefill_fa_4b_after_long_context():
+    """A 64-token prompt after 8192 cached rows at the 4B dims: each token attends
+    over 8193 .. 8256 rows."""
+    r = PrefillFa("4b", capacity=8320, n_filled=8192, T=64)
+    traces = []
+    got, ref = r.run(8192, traces)
+    _check_fa(r, 8192, got, ref, traces)
+
+
+def test_prefill_fa_one_token_equals_decode():
+    """A one-token prompt is the single-token forward: against the oracle and the
+    decode path on the same cache."""
+    r = PrefillFa("4b", capacity=512, n_filled=200, T=1)
+    traces = []
+    got, ref = r.run(200, traces)
+    _check_fa(r, 200, got, ref, traces)
+    # the decode path on a fresh copy of the same cache and input
+    kv2 = B.DeviceKv(r.k0, r.v0)
+    scr = B.new_scratch(B.qwen35_scratch_bytes(r.c, B.QWEN35_LAYER_FULL_ATTENTION))
+    xo = torch.empty(r.cfg["hidden"], dtype=torch.int16, device="cuda")
+    assert B.qwen35_forward_full_attention(r.c, r.dev.struct, scr, kv2.struct, r.x_in[0], xo, 200, 201) == 0
+    torch.cuda.synchronize()
+    assert rel_l2(got[0], f64(xo)) <= TOL_X
