@@ -33,7 +33,7 @@ namespace {
 // engine (the token tile and the raw codes, 128 rows of 64 bytes, both swizzled
 // by the copy itself), filled kAhead blocks ahead, and two stages of dequantised weight
 // tiles (hi, lo) written by the CTA's threads.
-constexpr uint32_t kBM = 128, kBN = 256, kDqThreads = 256, kGemmThreads = kDqThreads + 32;
+constexpr uint32_t kBM = 128, kBN = 256, kDqThreads = 256, kGemmThreads = kDqThreads + 64;
 constexpr uint32_t kRaw = 4, kAhead = kRaw - 2;
 constexpr uint32_t kTileBytes = kBM * 64 * 2;  // a weight tile (hi or lo)
 constexpr uint32_t kXBytes = kBN * 64 * 2;     // a token tile
@@ -165,13 +165,14 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
-// One CTA: rows [n0, n0 + 128) x tokens [t0, t0 + 256), nine warps. Warps 0-7
+// One CTA: rows [n0, n0 + 128) x tokens [t0, t0 + 256), ten warps. Warps 0-7
 // dequantise: thread (r, half) turns half of weight row n0 + r's codes of each
 // K-block into the block's weight stage and arrives on the stage's barrier. Lane 0
 // of warp 8 copies each K-block's token tile and codes kAhead blocks ahead (one
-// barrier per raw slot, completed by the copies' byte count) and, once a block's
-// copies have landed and its weight stage is complete, issues its K=16 MMAs (hi,
-// and lo in the exact form) and commits them to the raw slot's second barrier,
+// barrier per raw slot, completed by the copies' byte count); lane 0 of warp 9,
+// once a block's copies have landed and its weight stage is complete, issues its
+// K=16 MMAs (hi, and lo in the exact form) and commits them to the raw slot's
+// second barrier,
 // whose arrival frees the raw slot (refilled kAhead blocks later) and the weight
 // stage (rewritten WStages::n blocks later). No barrier of the whole CTA inside the
 // loop: the dequantising warps run ahead of the MMAs as far as the stages allow.
@@ -192,7 +193,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     for (uint32_t s = 0; s < 4; ++s) mbar_init(&wready[s], kDqThreads);
     mbar_fence_init();
   }
-  if (warp == 8) {
+  if (warp == 9) {
     tmem_alloc(&s_tmem, kBN);
     tmem_relinquish();
   }
@@ -213,7 +214,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     }
   };
   if (warp == 8) {
-    if (lane == 0) {
+    if (lane == 0) {  // the copies
       auto issue = [&](uint32_t kb) {  // K-block kb into its raw slot
         uint8_t* X = raw + (kb % kRaw) * kRawBytes;
         uint64_t* bar = &full[kb % kRaw];
@@ -222,11 +223,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         tma_load_2d(X + kXBytes, &A.tc, (int32_t)(kb * 64), (int32_t)n0, bar);
       };
       for (uint32_t kb = 0; kb < kAhead && kb < nk; ++kb) issue(kb);
+      for (uint32_t kb = 0; kb + kAhead < nk; ++kb) {  // the slot's last reader was MMA(kb + kAhead - kRaw)
+        if (kb + kAhead >= kRaw) wait(&done[(kb + kAhead) % kRaw], ((kb + kAhead - kRaw) / kRaw) & 1);
+        issue(kb + kAhead);
+      }
+    }
+  } else if (warp == 9) {
+    if (lane == 0) {  // the MMAs
       for (uint32_t kb = 0; kb < nk; ++kb) {
-        if (kb + kAhead < nk) {  // the slot's last reader was MMA(kb + kAhead - kRaw)
-          if (kb + kAhead >= kRaw) wait(&done[(kb + kAhead) % kRaw], ((kb + kAhead - kRaw) / kRaw) & 1);
-          issue(kb + kAhead);
-        }
         wait(&full[kb % kRaw], (kb / kRaw) & 1);
         wait(&wready[kb % WS::n], (kb / WS::n) & 1);
         tc_after_sync();
@@ -321,7 +325,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   }
   tc_before_sync();
   __syncthreads();
-  if (warp == 8) {
+  if (warp == 9) {
     tc_after_sync();
     tmem_dealloc(tmem, kBN);
   }
