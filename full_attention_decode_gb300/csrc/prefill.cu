@@ -2,10 +2,10 @@
 // every projection, so the projections are dense contractions and run on the
 // fifth-generation tensor cores: tcgen05.mma with bf16 operands in shared memory
 // and fp32 accumulators in tensor memory. The int8 group-64 weights are
-// dequantised by the CTA's threads on their way into shared memory, each as the
-// sum of two bf16 values (exact to 2^-16 relative); the
-// attention and the Gated DeltaNet recurrence keep the single-token forward's
-// arithmetic, token after token where the method is sequential.
+// dequantised by the CTA's threads on their way into shared memory (as bf16, or
+// as the sum of two bf16 values, exact to 2^-16). The attention and the Gated
+// DeltaNet recurrence keep the single-token forward's arithmetic, token after
+// token where the method is sequential.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -21,18 +21,19 @@ namespace {
 // ------------------------------------------------------------------ tcgen05
 
 // A GEMM tile: 128 weight rows (the MMA's M) x 256 tokens (its N), K in blocks of
-// one quantisation group (64). Each operand tile of a K-block is rows x 64 bf16
-// (128 weight rows, 256 token rows) in the K-major layout with the 128-byte swizzle: row r at r * 128, its
-// 16-byte chunk j at chunk position j ^ (r % 8) (the tile 1024-byte aligned), so
-// eight consecutive rows' copies of one chunk fall in different banks; rows are
-// 128 bytes apart and 8-row groups 1024 (the descriptor's stride offset).
-// In the exact form the weights enter the MMA as the bf16 sum hi + lo (hi = bf16(w),
-// lo = bf16(w - hi), so hi + lo is w to 2^-16 relative): both weight tiles multiply
-// the same token tile into one accumulator. The plain form takes hi alone.
+// one quantisation group (64). Each operand tile of a K-block (128 weight rows or
+// 256 token rows of 64 bf16) is in the K-major layout with the 128-byte swizzle:
+// row r at r * 128, its 16-byte chunk j at chunk position j ^ (r % 8) (the tile
+// 1024-byte aligned), so eight consecutive rows' copies of one chunk fall in
+// different banks; 8-row groups are 1024 bytes apart (the descriptor's stride
+// offset). In the exact form the weights enter the MMA as the bf16 sum hi + lo
+// (hi = bf16(w), lo = bf16(w - hi), so hi + lo is w to 2^-16 relative): both
+// weight tiles multiply the same token tile into one accumulator. The plain form
+// takes hi alone.
 // Shared memory: a ring of kRaw K-blocks as loaded by the tensor-memory-access
-// engine (the token tile and the raw codes, 128 rows of 64 bytes, both swizzled
-// by the copy itself), filled kAhead blocks ahead, and two stages of dequantised weight
-// tiles (hi, lo) written by the CTA's threads.
+// engine (the token tile and the raw codes, 128 rows of 64 bytes, both swizzled by
+// the copy itself), filled kAhead blocks ahead, and the stages of dequantised
+// weight tiles written by the CTA's threads.
 constexpr uint32_t kBM = 128, kBN = 256, kDqThreads = 256, kGemmThreads = kDqThreads + 64;
 constexpr uint32_t kRaw = 4, kAhead = kRaw - 2;
 constexpr uint32_t kTileBytes = kBM * 64 * 2;  // a weight tile (hi or lo)
@@ -149,8 +150,7 @@ __device__ __forceinline__ void dequant8(uint32_t c0, uint32_t c1, float s, floa
 
 // The GEMM's operands as tensor maps (tokens: bf16 [T][ldx], boxes of 64 x 256
 // with the 128-byte swizzle; codes: u8 [N][K], boxes of 64 x 128 with the 64-byte
-// swizzle), zero-filled
-// outside the matrices.
+// swizzle), zero-filled outside the matrices.
 struct GemmArgs {
   CUtensorMap tx;
   CUtensorMap tc;
@@ -172,10 +172,10 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
 // barrier per raw slot, completed by the copies' byte count); lane 0 of warp 9,
 // once a block's copies have landed and its weight stage is complete, issues its
 // K=16 MMAs (hi, and lo in the exact form) and commits them to the raw slot's
-// second barrier,
-// whose arrival frees the raw slot (refilled kAhead blocks later) and the weight
-// stage (rewritten WStages::n blocks later). No barrier of the whole CTA inside the
-// loop: the dequantising warps run ahead of the MMAs as far as the stages allow.
+// second barrier, whose arrival frees the raw slot (refilled kAhead blocks later)
+// and the weight stage (rewritten WStages::n blocks later). No barrier of the whole
+// CTA inside the loop: the dequantising warps run ahead of the MMAs as far as the
+// stages allow.
 template <bool EXACT>
 __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_constant__ GemmArgs A) {
   using WS = WStages<EXACT>;
