@@ -910,6 +910,10 @@ int pf_fa(const PfCtx& c, const qwen35_fa_layer* l, const qwen35_kv_cache* kv, c
   a.qr = c.b16(c.L.qr);
   a.kc = static_cast<uint16_t*>(kv->k);
   a.vc = static_cast<uint16_t*>(kv->v);
+  a.turbo8 = kv->dtype == QWEN35_KV_TURBO8;
+  a.ks = kv->k_scales;
+  a.vs = kv->v_scales;
+  a.sstride = (d.Hkv * d.D / 16 + 7) / 8 * 8;  // scale rows padded to 16 bytes
   a.btab = kv->block_table;
   a.bt_shift = 0;
   if (kv->block_table)
@@ -970,10 +974,10 @@ int pf_gdn(const PfCtx& c, const qwen35_gdn_layer* l, const qwen35_gdn_state* st
   return r;
 }
 
-// A prefill's KV cache: bf16 (contiguous or paged), room for positions [p0, p0 + T).
+// A prefill's KV cache: bf16 (contiguous or paged) or Turbo8, room for positions
+// [p0, p0 + T).
 int pf_kv_ok(const qwen35_kv_cache* kv, uint32_t p0, uint32_t T) {
   if (!kv_ok(kv)) return QWEN35_ERR_INVALID_ARGUMENT;
-  if (kv->dtype != QWEN35_KV_BF16) return QWEN35_ERR_UNSUPPORTED;
   if ((uint64_t)p0 + T > kv->capacity) return QWEN35_ERR_OUT_OF_RANGE;
   return QWEN35_OK;
 }

@@ -13,6 +13,9 @@
 #include "prefill.h"
 
 #include <algorithm>
+#include <type_traits>
+
+#include <cuda_fp16.h>
 
 namespace q35pf {
 using namespace q35;
@@ -410,6 +413,61 @@ __global__ void silu_mul_kernel(const uint16_t* g, const uint16_t* u, uint16_t* 
 
 // ------------------------------------------------------------------ full attention
 
+// Turbo8 (WHT-rotated FP8 E4M3 codes, a bf16 scale per 16 elements). A warp holds
+// a head's D-vector with lane L holding elements [L EPL, L EPL + EPL), EPL = D / 32.
+// The orthonormal Walsh-Hadamard transform in Sylvester order: butterflies over the
+// element index's low bits inside the lane, then over the lane bits by shuffles,
+// scaled by 1 / sqrt(D).
+template <int EPL>
+__device__ __forceinline__ void wht_lanes(float* x, uint32_t lane, float norm) {
+#pragma unroll
+  for (int hb = 1; hb < EPL; hb <<= 1)
+#pragma unroll
+    for (int e = 0; e < EPL; ++e)
+      if (!(e & hb)) {
+        const float u = x[e], w = x[e + hb];
+        x[e] = u + w;
+        x[e + hb] = u - w;
+      }
+#pragma unroll
+  for (uint32_t m = 1; m < 32; m <<= 1)
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+      const float o = __shfl_xor_sync(0xffffffffu, x[e], m);
+      x[e] = (lane & m) ? o - x[e] : x[e] + o;
+    }
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) x[e] *= norm;
+}
+__device__ __forceinline__ uint32_t e4m3_pair(float x0, float x1) {  // x0 in the low byte
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(x1), "f"(x0));
+  return r;
+}
+__device__ __forceinline__ float2 e4m3_pair_value(uint32_t two) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)two));
+  return __half22float2(*reinterpret_cast<const __half2*>(&h2));
+}
+// Quantise the warp's row (bf16 values in x): per group of 16 elements (16 / EPL
+// lanes) scale = bf16(amax / 448), code = E4M3(x / scale) rounded to nearest even
+// and saturated; a zero group keeps scale 0 and codes 0. Stores the lane's EPL
+// codes at codes[L EPL ..] and each group's scale at scales[group].
+template <int EPL>
+__device__ __forceinline__ void turbo8_store(const float* x, uint32_t lane, uint8_t* codes, uint16_t* scales) {
+  float amax = 0.f;
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) amax = fmaxf(amax, fabsf(x[e]));
+#pragma unroll
+  for (int o = 1; o < 16 / EPL; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const float sc = round_bf16(amax / 448.f);
+#pragma unroll
+  for (int e = 0; e < EPL; e += 2)
+    *reinterpret_cast<uint16_t*>(codes + lane * EPL + e) =
+        (uint16_t)(sc > 0.f ? e4m3_pair(x[e] / sc, x[e + 1] / sc) : 0u);
+  if ((lane * EPL) % 16 == 0) scales[lane * EPL / 16] = to_bf16(sc);
+}
+
 // The cache row (in units of token rows) of logical token t: itself, or its row in
 // the pool block the table names.
 __device__ __forceinline__ size_t cache_row(const Attn& a, uint32_t t) {
@@ -421,46 +479,72 @@ __device__ __forceinline__ size_t cache_row(const Attn& a, uint32_t t) {
 // Per (token, head slot) one warp: slots [0, H) are the q-heads (RMSNorm with
 // q_norm, RoPE, into qr), [H, H + Hkv) the k-heads (RMSNorm with k_norm, RoPE,
 // appended to the K cache), [H + Hkv, H + 2 Hkv) the v-heads (appended to the V
-// cache). Each value is rounded to bf16 after the norm and after the rotation.
+// cache). Each value is rounded to bf16 after the norm and after the rotation. For
+// a Turbo8 cache the rows are then rotated by the WHT and rounded to bf16 again:
+// q kept so in qr, k and v quantised into the cache's codes and scales.
+template <int EPL>
 __global__ void __launch_bounds__(128) qk_rope_kernel(const Attn a) {
-  __shared__ float buf[4][256];
+  constexpr int D = 32 * EPL;
+  __shared__ float buf[4][2][D];
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t slots = a.H + 2 * a.Hkv;
   const uint32_t item = blockIdx.x * 4 + warp;
   if (item >= a.T * slots) return;
-  const uint32_t t = item / slots, sl = item % slots, D = a.D, pos = a.p0 + t;
-  const size_t kvrow = cache_row(a, pos) * a.Hkv * D;
-  float* x = buf[warp];
-  if (sl >= a.H + a.Hkv) {  // v: a copy into the cache
-    const uint32_t g = sl - a.H - a.Hkv;
-    for (uint32_t d = lane; d < D; d += 32) a.vc[kvrow + g * D + d] = a.v[((size_t)t * a.Hkv + g) * D + d];
+  const uint32_t t = item / slots, sl = item % slots, pos = a.p0 + t;
+  const size_t crow = cache_row(a, pos);
+  const size_t kvrow = crow * a.Hkv * D;
+  float* x = buf[warp][0];
+  float* y = buf[warp][1];
+  const bool isv = sl >= a.H + a.Hkv, isq = sl < a.H;
+  const uint32_t hd = isq ? sl : isv ? sl - a.H - a.Hkv : sl - a.H;
+  if (isv) {  // v: as projected
+    const uint16_t* src = a.v + ((size_t)t * a.Hkv + hd) * D;
+    for (uint32_t d = lane; d < D; d += 32) y[d] = bf16f(src[d]);
+  } else {
+    const uint16_t* src = isq ? a.qf + ((size_t)t * a.H + hd) * 2 * D : a.k + ((size_t)t * a.Hkv + hd) * D;
+    const uint16_t* nw = isq ? a.q_norm : a.k_norm;
+    float ss = 0.f;
+    for (uint32_t d = lane; d < D; d += 32) {
+      const float v = bf16f(src[d]);
+      x[d] = v;
+      ss = fmaf(v, v, ss);
+    }
+    const float inv = rsqrtf(warp_sum(ss) / (float)D + a.eps);
+    for (uint32_t d = lane; d < D; d += 32) x[d] = round_bf16(x[d] * inv * bf16f(nw[d]));
+    __syncwarp();
+    const uint32_t half = a.R / 2;
+    for (uint32_t d = lane; d < D; d += 32) {
+      float v = x[d];
+      if (d < a.R) {
+        const uint32_t i = d < half ? d : d - half;
+        float sn, cs;
+        sincosf((float)pos * a.inv_freq[i], &sn, &cs);
+        v = d < half ? x[d] * cs - x[d + half] * sn : x[d] * cs + x[d - half] * sn;
+      }
+      y[d] = round_bf16(v);
+    }
+  }
+  __syncwarp();
+  if (!a.turbo8) {
+    uint16_t* dst = isq ? a.qr + ((size_t)t * a.H + hd) * D : (isv ? a.vc : a.kc) + kvrow + hd * D;
+    for (uint32_t d = lane; d < D; d += 32) dst[d] = to_bf16(y[d]);
     return;
   }
-  const bool isq = sl < a.H;
-  const uint32_t hd = isq ? sl : sl - a.H;
-  const uint16_t* src = isq ? a.qf + ((size_t)t * a.H + hd) * 2 * D : a.k + ((size_t)t * a.Hkv + hd) * D;
-  const uint16_t* nw = isq ? a.q_norm : a.k_norm;
-  float ss = 0.f;
-  for (uint32_t d = lane; d < D; d += 32) {
-    const float v = bf16f(src[d]);
-    x[d] = v;
-    ss = fmaf(v, v, ss);
+  float r[EPL];
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) r[e] = y[lane * EPL + e];
+  wht_lanes<EPL>(r, lane, rsqrtf((float)D));
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) r[e] = round_bf16(r[e]);
+  if (isq) {
+    uint16_t* dst = a.qr + ((size_t)t * a.H + hd) * D + lane * EPL;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) dst[e] = to_bf16(r[e]);
+    return;
   }
-  const float inv = rsqrtf(warp_sum(ss) / (float)D + a.eps);
-  for (uint32_t d = lane; d < D; d += 32) x[d] = round_bf16(x[d] * inv * bf16f(nw[d]));
-  __syncwarp();
-  const uint32_t half = a.R / 2;
-  uint16_t* dst = isq ? a.qr + ((size_t)t * a.H + hd) * D : a.kc + kvrow + hd * D;
-  for (uint32_t d = lane; d < D; d += 32) {
-    float y = x[d];
-    if (d < a.R) {
-      const uint32_t i = d < half ? d : d - half;
-      float sn, cs;
-      sincosf((float)pos * a.inv_freq[i], &sn, &cs);
-      y = d < half ? x[d] * cs - x[d + half] * sn : x[d] * cs + x[d - half] * sn;
-    }
-    dst[d] = to_bf16(y);
-  }
+  uint8_t* codes = reinterpret_cast<uint8_t*>(isv ? a.vc : a.kc) + kvrow + hd * D;
+  uint16_t* scales = (isv ? a.vs : a.ks) + crow * a.sstride + hd * (D / 16);
+  turbo8_store<EPL>(r, lane, codes, scales);
 }
 
 // Causal attention: one CTA per (kv-head g, 8 consecutive tokens), warp w for token
@@ -468,12 +552,16 @@ __global__ void __launch_bounds__(128) qk_rope_kernel(const Attn a) {
 // and V (rows [0, p0 + t] for token t) are staged in shared memory, K rows padded
 // by 16 bytes. Scores: lane j takes key j of the tile over all D dims; the online
 // softmax runs in the log2 domain; P V: lane L holds dims [DPL L, DPL L + DPL).
-template <int D, int HPG>
+// A Turbo8 cache: the tiles are decoded (E4M3 code times its group's scale, exact
+// in fp32) into fp32 tiles (K rows padded by 4 elements), q is the rotated q, and the
+// output is rotated back by the WHT before the gate (each step rounded to bf16).
+template <int D, int HPG, bool T8>
 __global__ void __launch_bounds__(256) attn_kernel(const Attn a) {
-  constexpr int KT = 32, KS = D + 8, DPL = D / 32;
+  constexpr int KT = 32, KS = T8 ? D + 4 : D + 8, DPL = D / 32;
+  using TE = typename std::conditional<T8, float, uint16_t>::type;  // tile element
   extern __shared__ __align__(16) uint8_t dsm[];
-  uint16_t* Ks = reinterpret_cast<uint16_t*>(dsm);  // [KT][KS]
-  uint16_t* Vs = Ks + KT * KS;                      // [KT][D]
+  TE* Ks = reinterpret_cast<TE*>(dsm);  // [KT][KS]
+  TE* Vs = Ks + KT * KS;                // [KT][D]
   uint16_t (*Qs)[HPG][D] = reinterpret_cast<uint16_t (*)[HPG][D]>(Vs + KT * D);  // [8][HPG][D]
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t g = blockIdx.y, tb = blockIdx.x * 8;
@@ -503,14 +591,41 @@ __global__ void __launch_bounds__(256) attn_kernel(const Attn a) {
     __syncthreads();  // the last tile is consumed
     for (uint32_t i = threadIdx.x; i < KT * D / 8; i += blockDim.x) {
       const uint32_t j = i / (D / 8), d8 = i % (D / 8);
-      uint4 kv = make_uint4(0u, 0u, 0u, 0u), vv = kv;
-      if (k0 + j < nkeys) {
-        const size_t off = cache_row(a, k0 + j) * kvw + g * D + 8 * d8;
-        kv = *reinterpret_cast<const uint4*>(a.kc + off);
-        vv = *reinterpret_cast<const uint4*>(a.vc + off);
+      if constexpr (T8) {
+        float kx[8], vx[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) kx[e] = vx[e] = 0.f;
+        if (k0 + j < nkeys) {
+          const size_t row = cache_row(a, k0 + j);
+          const size_t off = row * kvw + g * D + 8 * d8;
+          const uint2 kc = *reinterpret_cast<const uint2*>(reinterpret_cast<const uint8_t*>(a.kc) + off);
+          const uint2 vc = *reinterpret_cast<const uint2*>(reinterpret_cast<const uint8_t*>(a.vc) + off);
+          const size_t sidx = row * a.sstride + g * (D / 16) + d8 / 2;
+          const float ksc = bf16f(a.ks[sidx]), vsc = bf16f(a.vs[sidx]);
+#pragma unroll
+          for (int e = 0; e < 8; e += 2) {
+            const uint32_t kw = e < 4 ? kc.x : kc.y, vw = e < 4 ? vc.x : vc.y;
+            const float2 kf = e4m3_pair_value(kw >> (8 * (e % 4))), vf = e4m3_pair_value(vw >> (8 * (e % 4)));
+            kx[e] = kf.x * ksc;
+            kx[e + 1] = kf.y * ksc;
+            vx[e] = vf.x * vsc;
+            vx[e + 1] = vf.y * vsc;
+          }
+        }
+        *reinterpret_cast<float4*>(&Ks[j * KS + 8 * d8]) = make_float4(kx[0], kx[1], kx[2], kx[3]);
+        *reinterpret_cast<float4*>(&Ks[j * KS + 8 * d8 + 4]) = make_float4(kx[4], kx[5], kx[6], kx[7]);
+        *reinterpret_cast<float4*>(&Vs[j * D + 8 * d8]) = make_float4(vx[0], vx[1], vx[2], vx[3]);
+        *reinterpret_cast<float4*>(&Vs[j * D + 8 * d8 + 4]) = make_float4(vx[4], vx[5], vx[6], vx[7]);
+      } else {
+        uint4 kv = make_uint4(0u, 0u, 0u, 0u), vv = kv;
+        if (k0 + j < nkeys) {
+          const size_t off = cache_row(a, k0 + j) * kvw + g * D + 8 * d8;
+          kv = *reinterpret_cast<const uint4*>(a.kc + off);
+          vv = *reinterpret_cast<const uint4*>(a.vc + off);
+        }
+        *reinterpret_cast<uint4*>(&Ks[j * KS + 8 * d8]) = kv;
+        *reinterpret_cast<uint4*>(&Vs[j * D + 8 * d8]) = vv;
       }
-      *reinterpret_cast<uint4*>(&Ks[j * KS + 8 * d8]) = kv;
-      *reinterpret_cast<uint4*>(&Vs[j * D + 8 * d8]) = vv;
     }
     __syncthreads();
     if (k0 >= mykeys) continue;  // (warp-uniform) past this token's keys
@@ -521,7 +636,14 @@ __global__ void __launch_bounds__(256) attn_kernel(const Attn a) {
 #pragma unroll 4
     for (uint32_t d8 = 0; d8 < D / 8; ++d8) {
       float kx[8];
-      unpack8(*reinterpret_cast<const uint4*>(&Ks[lane * KS + 8 * d8]), kx);
+      if constexpr (T8) {
+        const float4 k0v = *reinterpret_cast<const float4*>(&Ks[lane * KS + 8 * d8]);
+        const float4 k1v = *reinterpret_cast<const float4*>(&Ks[lane * KS + 8 * d8 + 4]);
+        kx[0] = k0v.x; kx[1] = k0v.y; kx[2] = k0v.z; kx[3] = k0v.w;
+        kx[4] = k1v.x; kx[5] = k1v.y; kx[6] = k1v.z; kx[7] = k1v.w;
+      } else {
+        unpack8(*reinterpret_cast<const uint4*>(&Ks[lane * KS + 8 * d8]), kx);
+      }
 #pragma unroll
       for (int h = 0; h < HPG; ++h) {
         float qx[8];
@@ -546,7 +668,10 @@ __global__ void __launch_bounds__(256) attn_kernel(const Attn a) {
     const uint32_t jn = min((uint32_t)KT, mykeys - k0);
     for (uint32_t j = 0; j < jn; ++j) {
       float vx[DPL];
-      if constexpr (DPL == 8) {
+      if constexpr (T8) {
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) vx[i] = Vs[j * D + DPL * lane + i];
+      } else if constexpr (DPL == 8) {
         unpack8(*reinterpret_cast<const uint4*>(&Vs[j * D + 8 * lane]), vx);
       } else if constexpr (DPL == 4) {
         const uint2 u = *reinterpret_cast<const uint2*>(&Vs[j * D + 4 * lane]);
@@ -564,17 +689,25 @@ __global__ void __launch_bounds__(256) attn_kernel(const Attn a) {
     }
   }
   if (!live) return;
-  // attn = bf16(o / l); gated = bf16(attn * sigmoid(gate))
+  // attn = bf16(o / l) (Turbo8: rotated back, bf16 again); gated = bf16(attn * sigmoid(gate))
 #pragma unroll
   for (int h = 0; h < HPG; ++h) {
     const uint32_t hh = g * HPG + h;
     const float inv = 1.0f / l[h];
     const uint16_t* gate = a.qf + ((size_t)t * a.H + hh) * 2 * D + D;
     uint16_t* out = a.ga + ((size_t)t * a.H + hh) * D;
+    float at[DPL];
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) at[i] = round_bf16(o[h][i] * inv);
+    if constexpr (T8) {
+      wht_lanes<DPL>(at, lane, rsqrtf((float)D));
+#pragma unroll
+      for (int i = 0; i < DPL; ++i) at[i] = round_bf16(at[i]);
+    }
 #pragma unroll
     for (int i = 0; i < DPL; ++i) {
       const uint32_t d = DPL * lane + i;
-      out[d] = to_bf16(round_bf16(o[h][i] * inv) * sigmoidf_(bf16f(gate[d])));
+      out[d] = to_bf16(at[i] * sigmoidf_(bf16f(gate[d])));
     }
   }
 }
@@ -817,11 +950,21 @@ cudaError_t silu_mul(const uint16_t* g, const uint16_t* u, uint16_t* h, size_t n
 namespace {
 template <int D, int HPG>
 cudaError_t attn_launch(const Attn& a, dim3 grid, cudaStream_t st) {
-  // key and value tiles (32 rows, K rows padded by 8 elements) and 8 tokens' q rows
-  const uint32_t bytes = (32 * (D + 8) + 32 * D + 8 * HPG * D) * 2;
-  cudaError_t e = cudaFuncSetAttribute(attn_kernel<D, HPG>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e != cudaSuccess) return e;
-  attn_kernel<D, HPG><<<grid, 256, bytes, st>>>(a);
+  // key and value tiles (32 rows; bf16, K rows padded by 8, or fp32 decoded Turbo8
+  // rows, K rows padded by 4) and 8 tokens' q rows
+  if (a.turbo8) {
+    const uint32_t bytes = (32 * (D + 4) + 32 * D) * 4 + 8 * HPG * D * 2;
+    cudaError_t e =
+        cudaFuncSetAttribute(attn_kernel<D, HPG, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    attn_kernel<D, HPG, true><<<grid, 256, bytes, st>>>(a);
+  } else {
+    const uint32_t bytes = (32 * (D + 8) + 32 * D + 8 * HPG * D) * 2;
+    cudaError_t e =
+        cudaFuncSetAttribute(attn_kernel<D, HPG, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    attn_kernel<D, HPG, false><<<grid, 256, bytes, st>>>(a);
+  }
   return cudaGetLastError();
 }
 template <int D>
@@ -838,8 +981,13 @@ cudaError_t attn_for(const Attn& a, dim3 grid, cudaStream_t st) {
 
 cudaError_t attention(const Attn& a, cudaStream_t st) {
   if (a.T == 0) return cudaSuccess;
-  const uint32_t items = a.T * (a.H + 2 * a.Hkv);
-  qk_rope_kernel<<<(items + 3) / 4, 128, 0, st>>>(a);
+  const uint32_t items = a.T * (a.H + 2 * a.Hkv), blocks = (items + 3) / 4;
+  switch (a.D) {
+    case 64: qk_rope_kernel<2><<<blocks, 128, 0, st>>>(a); break;
+    case 128: qk_rope_kernel<4><<<blocks, 128, 0, st>>>(a); break;
+    case 256: qk_rope_kernel<8><<<blocks, 128, 0, st>>>(a); break;
+    default: return cudaErrorInvalidValue;
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const dim3 grid((a.T + 7) / 8, a.Hkv);

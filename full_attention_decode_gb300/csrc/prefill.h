@@ -48,10 +48,13 @@ struct Attn {
   const uint16_t* v;   // v_proj outputs [T][Hkv*D]
   const uint16_t *q_norm, *k_norm;
   uint16_t* qr;        // roped q [T][H][D] (written)
-  uint16_t *kc, *vc;   // bf16 caches [capacity][Hkv][D], or pools of 2^bt_shift-row blocks
+  uint16_t *kc, *vc;   // bf16 caches [capacity][Hkv][D], or pools of 2^bt_shift-row blocks;
+                       // Turbo8: E4M3 codes, u8 [capacity][Hkv][D]
+  uint16_t *ks, *vs;   // Turbo8: bf16 scales [capacity][sstride], one per 16 elements
   const int32_t* btab; // paged: logical token t in row t % 2^bt_shift of block btab[t >> bt_shift]
   uint16_t* ga;        // gated attention [T][H*D] (written)
   uint32_t T, p0, H, Hkv, D, R, bt_shift;
+  uint32_t turbo8, sstride;  // Turbo8 cache (rows rotated by the normalised WHT, quantised)
   float eps;
   float inv_freq[128];
 };

@@ -366,11 +366,11 @@ QWEN35_API int qwen35_graph_create_batched(const qwen35_config* cfg, const qwen3
  *    single-token path keeps unrounded inside its fused kernels (SiLU(gate) * up
  *    before down_proj, SiLU(z) * y_norm before out_proj) are rounded to bf16
  *    here. Both stay far inside the layer tolerance.
- *  - KV cache: bf16, contiguous or paged (a Turbo8 cache is
- *    QWEN35_ERR_UNSUPPORTED); logical rows [cache_pos, cache_pos + n_tokens) are
- *    written, rows [0, cache_pos) read (a paged cache's table must name every
- *    block of [0, cache_pos + n_tokens)); cache_pos + n_tokens > capacity is
- *    QWEN35_ERR_OUT_OF_RANGE.
+ *  - KV cache: bf16 (contiguous or paged) or Turbo8 (rows rotated and quantised
+ *    as the single-token forward does); logical rows [cache_pos, cache_pos +
+ *    n_tokens) are written, rows [0, cache_pos) read (a paged cache's table must
+ *    name every block of [0, cache_pos + n_tokens)); cache_pos + n_tokens >
+ *    capacity is QWEN35_ERR_OUT_OF_RANGE.
  *  - Scratch: qwen35_prefill_scratch_bytes(cfg, max_tokens) for any n_tokens up to
  *    max_tokens (its first 4 bytes are the device status word, as for decode);
  *    at most 65536 tokens per call.

@@ -256,8 +256,8 @@ def test_prefill_argument_errors_precede_launch():
     assert f(c, fa, S, kv, x, y, 0, 9, 0) == B.QWEN35_ERR_INVALID_ARGUMENT    # scratch for 8 tokens
     assert f(c, fa, S, kv, x, y, 0, 0, 0) == B.QWEN35_ERR_INVALID_ARGUMENT    # no tokens
     assert f(c, fa, S, kv, x + 2, y, 0, 8, 0) == B.QWEN35_ERR_INVALID_ARGUMENT
-    t8 = B.qwen35_kv_cache(_FAKE * 5, _FAKE * 6, 16, 1, _FAKE * 3, _FAKE * 4)
-    assert f(c, fa, S, t8, x, y, 0, 8, 0) == B.QWEN35_ERR_UNSUPPORTED         # Turbo8 cache
+    t8 = B.qwen35_kv_cache(_FAKE * 5, _FAKE * 6, 16, 1, None, _FAKE * 4)
+    assert f(c, fa, S, t8, x, y, 0, 8, 0) == B.QWEN35_ERR_INVALID_ARGUMENT    # Turbo8 without k scales
     badpaged = B.qwen35_kv_cache(_FAKE * 5, _FAKE * 6, 16, 0, None, None, _FAKE * 2, 12)
     assert f(c, fa, S, badpaged, x, y, 0, 8, 0) == B.QWEN35_ERR_INVALID_ARGUMENT  # blocks not a power of 2
     g = B.qwen35_gdn_layer()

@@ -294,3 +294,84 @@ def test_prefill_fa_one_token_equals_decode():
     assert B.qwen35_forward_full_attention(r.c, r.dev.struct, scr, kv2.struct, r.x_in[0], xo, 200, 201) == 0
     torch.cuda.synchronize()
     assert rel_l2(got[0], f64(xo)) <= TOL_X
+
+
+# ------------------------------------------------------------------ Turbo8 caches
+
+
+@pytest.mark.parametrize("cfg_name,capacity,n_filled,T", [("tiny", 64, 5, 37), ("4b", 512, 300, 150)])
+def test_prefill_fa_turbo8(cfg_name, capacity, n_filled, T):
+    """A prompt appended to a Turbo8 cache (rows WHT-rotated, FP8 E4M3 codes with a
+    bf16 scale per 16) and attending over it: every token's output within the layer
+    tolerance; the appended rows decode to the oracle's within it (a code can move
+    one E4M3 step where the two sides' rotated rows differ in the last bf16 bit), and
+    most codes are the oracle's; the rows outside the prompt untouched."""
+    init()
+    cfg = synth.config(cfg_name)
+    c = B.make_config(cfg)
+    layer = synth.fa_layer(0, 1, cfg)
+    dev = B.DeviceFaLayer(layer)
+    kc, ks, vc, vs = synth.kv_cache_turbo8(0, 1, cfg, capacity, n_filled)
+    kv = B.DeviceKvTurbo8(kc, ks, vc, vs, cfg)
+    okv = O.turbo8_kv(kc, ks, vc, vs)
+    X = _prompt(0, T, cfg)
+    x_in = B.to_device(X)
+    x_out = torch.empty_like(x_in)
+    scratch = B.new_scratch(B.qwen35_prefill_scratch_bytes(c, T))
+    assert B.qwen35_prefill_full_attention(c, dev.struct, scratch, kv.struct, x_in, x_out, n_filled, T) == 0
+    ref = O.prefill_full_attention(cfg, layer, okv, O.bf16_to_f64(X), n_filled)
+    torch.cuda.synchronize()
+    got = f64(x_out)
+    for t in range(T):
+        assert rel_l2(got[t], ref[t]) <= TOL_X, t
+    end = n_filled + T
+    for w, codes0 in (("k", kc), ("v", vc)):
+        gc = (kv.k if w == "k" else kv.v).cpu().numpy().view(np.uint8)
+        gs = O.bf16_to_f64(kv.scales(w))
+        oc, osc = okv[w + "_codes"], okv[w + "_scales"]
+        deq_g = O.turbo8_dequantize(gc[n_filled:end], gs[n_filled:end])
+        deq_o = O.turbo8_dequantize(oc[n_filled:end], osc[n_filled:end])
+        assert rel_l2(deq_g, deq_o) <= TOL_X, w
+        assert np.mean(gc[n_filled:end] == oc[n_filled:end]) >= 0.9, w
+        np.testing.assert_array_equal(gc[:n_filled], codes0[:n_filled])
+        assert not gc[end:].any()
+    assert B.qwen35_read_device_status(scratch) == 0
+
+
+def test_prefill_stack_turbo8_then_decode():
+    """A 20-token prompt through the tiny stack with a Turbo8 cache, then 4 decode
+    steps on what it left, against the oracle."""
+    init()
+    cfg = synth.config("tiny")
+    c = B.make_config(cfg)
+    kinds = synth.layer_kinds(cfg)
+    layers = [synth.gdn_layer(0, 0, cfg), synth.fa_layer(0, 1, cfg)]
+    conv, ssm = synth.gdn_state(0, 0, cfg, 0.1)
+    kc, ks, vc, vs = synth.kv_cache_turbo8(0, 1, cfg, 32, 0)
+    dev = [B.DeviceGdnLayer(layers[0]), B.DeviceFaLayer(layers[1])]
+    caches = [B.DeviceState(conv, ssm), B.DeviceKvTurbo8(kc, ks, vc, vs, cfg)]
+    ocaches = [O.state_from_arrays(conv, ssm), O.turbo8_kv(kc, ks, vc, vs)]
+    entries = [B.stack_layer(k, l, cc) for k, l, cc in zip(kinds, dev, caches)]
+    T = 20
+    X = _prompt(0, T, cfg)
+    x_in = B.to_device(X)
+    x_out = torch.empty_like(x_in)
+    pscr = B.new_scratch(B.qwen35_prefill_scratch_bytes(c, T))
+    assert B.qwen35_prefill_step(c, entries, pscr, x_in, x_out, 0, T) == 0
+    ref = O.prefill_step(cfg, kinds, layers, ocaches, O.bf16_to_f64(X), 0)
+    torch.cuda.synchronize()
+    got = f64(x_out)
+    for t in range(T):
+        assert rel_l2(got[t], ref[t]) <= TOL_X, t
+    scratch = B.new_scratch(B.qwen35_stack_scratch_bytes(c))
+    xi = torch.empty(cfg["hidden"], dtype=torch.int16, device="cuda")
+    xo = torch.empty_like(xi)
+    d_pos = torch.full((1,), T, dtype=torch.int32, device="cuda")
+    for s in range(4):
+        x = synth.x_in(0, s, cfg)
+        xi.copy_(B.to_device(x))
+        assert B.qwen35_decode_step(c, entries, scratch, xi, xo, d_pos, 32) == 0
+        ref = O.decode_step(cfg, kinds, layers, ocaches, O.bf16_to_f64(x), T + s)
+        torch.cuda.synchronize()
+        assert rel_l2(f64(xo), ref) <= TOL_X, s
+    assert B.qwen35_read_device_status(pscr) == 0 and B.qwen35_read_device_status(scratch) == 0
