@@ -21,6 +21,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_lib", "libqwen35_decode.so")
 
 QWEN35_OK = 0
+QWEN35_PREFILL_GEMM_SPLIT_SCRATCH = 256 + 152 * 128 * 256 * 4  # include/qwen35_decode.h
 QWEN35_ERR_INVALID_ARGUMENT = 1
 QWEN35_ERR_OUT_OF_RANGE = 2
 QWEN35_ERR_UNSUPPORTED = 3

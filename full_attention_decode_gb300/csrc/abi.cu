@@ -787,6 +787,7 @@ struct PfLayout {
   size_t xn, xr, o, g, u;                                // [T][E] x3, [T][I] x2
   size_t qf, k, v, qr, ga;                               // full attention
   size_t dt, bb, qkv, z, qs, gb, act, y, yin;            // linear attention (gb, act fp32)
+  size_t ws;                                             // split-K partial sums (fp32)
   size_t total;
 };
 PfLayout pf_layout(const Dims& d, uint32_t T) {
@@ -817,6 +818,7 @@ PfLayout pf_layout(const Dims& d, uint32_t T) {
   L.act = take(t * d.C * 4);
   L.y = take(t * d.Z * 2);
   L.yin = take(t * d.Z * 2);
+  L.ws = take(q35pf::kGemmWorkspace);
   L.total = off;
   return L;
 }
@@ -830,6 +832,7 @@ struct PfCtx {
   PfLayout L;
   uint32_t T;
   cudaStream_t st;
+  float* ws;  // split-K workspace, or null
   uint16_t* b16(size_t off) const { return reinterpret_cast<uint16_t*>(s + off); }
   float* f32(size_t off) const { return reinterpret_cast<float*>(s + off); }
   int* status() const { return reinterpret_cast<int*>(s); }
@@ -848,6 +851,7 @@ int pf_begin(PfCtx& c, const qwen35_config* cfg, void* scratch, size_t scratch_b
   c.s = static_cast<uint8_t*>(scratch);
   c.T = T;
   c.st = st;
+  c.ws = c.f32(c.L.ws);
   return QWEN35_OK;
 }
 
@@ -874,6 +878,7 @@ int pf_gemm(const PfCtx& c, const qwen35_qweight& w, const uint16_t* X, uint16_t
   g.status = c.status();
   g.wait_ns = g_wait_ns;
   g.exact = exact;
+  g.ws = c.ws;
   return cu(q35pf::gemm(g, c.st));
 }
 
@@ -998,6 +1003,9 @@ int qwen35_prefill_gemm(const qwen35_qweight* w, const qwen35_bf16* X, qwen35_bf
   c.s = static_cast<uint8_t*>(scratch);
   c.T = n_tokens;
   c.st = (cudaStream_t)stream;
+  // a scratch with room for the split-K workspace after its first 256 bytes lets a
+  // GEMM of few tiles split K
+  c.ws = scratch_bytes >= 256 + q35pf::kGemmWorkspace ? reinterpret_cast<float*>(c.s + 256) : nullptr;
   return pf_gemm(c, *w, X, Y, nullptr, exact != 0);
 }
 

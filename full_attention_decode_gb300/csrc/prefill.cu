@@ -204,7 +204,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   __syncthreads();
   tc_after_sync();
   const uint32_t tmem = s_tmem;
-  const uint32_t nk = g.K / 64;
+  // this CTA's K-blocks (split K: the z-th of gridDim.z equal ranges); kb below counts
+  // from the range's start
+  const uint32_t nkt = g.K / 64, kb0 = blockIdx.z * nkt / gridDim.z;
+  const uint32_t nk = (blockIdx.z + 1) * nkt / gridDim.z - kb0;
   // the tiles from the first 1024-byte boundary of the dynamic shared memory
   const uint32_t sraw = smem_addr(smem), sbase = (sraw + 1023u) & ~1023u;
   uint8_t* raw = smem + (sbase - sraw);
@@ -222,8 +225,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         uint8_t* X = raw + (kb % kRaw) * kRawBytes;
         uint64_t* bar = &full[kb % kRaw];
         mbar_arrive_expect_tx(bar, kXBytes + kCodeBytes);
-        tma_load_2d(X, &A.tx, (int32_t)(kb * 64), (int32_t)t0, bar);
-        tma_load_2d(X + kXBytes, &A.tc, (int32_t)(kb * 64), (int32_t)n0, bar);
+        tma_load_2d(X, &A.tx, (int32_t)((kb0 + kb) * 64), (int32_t)t0, bar);
+        tma_load_2d(X + kXBytes, &A.tc, (int32_t)((kb0 + kb) * 64), (int32_t)n0, bar);
       };
       for (uint32_t kb = 0; kb < kAhead && kb < nk; ++kb) issue(kb);
       for (uint32_t kb = 0; kb + kAhead < nk; ++kb) {  // the slot's last reader was MMA(kb + kAhead - kRaw)
@@ -251,8 +254,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     const uint32_t r = tid & 127, half = tid >> 7;
     const uint32_t n = n0 + r;
     const bool nin = n < g.N;
-    const uint16_t* srow = g.scales + (size_t)(nin ? n : 0) * g.gstride;
-    const uint16_t* brow = g.biases + (size_t)(nin ? n : 0) * g.gstride;
+    const uint16_t* srow = g.scales + (size_t)(nin ? n : 0) * g.gstride + kb0;
+    const uint16_t* brow = g.biases + (size_t)(nin ? n : 0) * g.gstride + kb0;
     const uint32_t j0 = 4 * half;
     // scale and bias of the row, two blocks ahead in registers
     uint16_t sc0 = 0, bi0 = 0, sc1 = 0, bi1 = 0;
@@ -319,9 +322,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       for (int i = 0; i < 16; ++i) {
         const uint32_t tt = t0 + (kBN / 2) * ch + c + i;
         if (tt < g.T) {
-          float y = v[i];
-          if (g.R) y += bf16f(g.R[(size_t)tt * g.ldy + row]);
-          g.Y[(size_t)tt * g.ldy + row] = to_bf16(y);
+          if (gridDim.z > 1) {  // a split's partial sum, added up by the finishing kernel
+            g.ws[((size_t)blockIdx.z * g.T + tt) * g.N + row] = v[i];
+          } else {
+            float y = v[i];
+            if (g.R) y += bf16f(g.R[(size_t)tt * g.ldy + row]);
+            g.Y[(size_t)tt * g.ldy + row] = to_bf16(y);
+          }
         }
       }
     }
@@ -331,6 +338,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   if (warp == 9) {
     tc_after_sync();
     tmem_dealloc(tmem, kBN);
+  }
+}
+
+// The split-K sum: Y[t][n] = bf16(sum_z ws[z][t][n] (+ R[t][n])), splits added in
+// order.
+__global__ void gemm_finish_kernel(const Gemm g, uint32_t splits) {
+  const size_t total = (size_t)g.T * g.N;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+    const size_t t = i / g.N, n = i % g.N;
+    float y = 0.f;
+    for (uint32_t z = 0; z < splits; ++z) y += g.ws[z * total + i];
+    if (g.R) y += bf16f(g.R[t * g.ldy + n]);
+    g.Y[t * g.ldy + n] = to_bf16(y);
   }
 }
 
@@ -927,8 +947,18 @@ cudaError_t gemm(const Gemm& g, cudaStream_t st) {
   const auto k = g.exact ? gemm_kernel<true> : gemm_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
   if (e != cudaSuccess) return e;
-  const dim3 grid((g.N + kBM - 1) / kBM, (g.T + kBN - 1) / kBN);
+  const uint32_t tiles = ((g.N + kBM - 1) / kBM) * ((g.T + kBN - 1) / kBN), nk = g.K / 64;
+  // split K while the tiles would leave more than half of the 152 SMs idle
+  uint32_t splits = 1;
+  if (g.ws && tiles * 2 <= 152) splits = std::min(std::min(152u / tiles, 8u), nk);
+  if (splits < 2) a.g.ws = nullptr, splits = 1;
+  const dim3 grid((g.N + kBM - 1) / kBM, (g.T + kBN - 1) / kBN, splits);
   k<<<grid, kGemmThreads, kGemmSmem, st>>>(a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || splits == 1) return e;
+  const size_t total = (size_t)g.T * g.N;
+  const uint32_t blocks = (uint32_t)std::min<size_t>((total + 255) / 256, 152 * 8);
+  gemm_finish_kernel<<<blocks, 256, 0, st>>>(a.g, splits);
   return cudaGetLastError();
 }
 

@@ -28,7 +28,13 @@ struct Gemm {
   int* status;
   unsigned long long wait_ns;
   bool exact;
+  float* ws;  // split-K partial sums (kGemmWorkspace bytes), or null: no split
 };
+// Workspace for a GEMM whose tiles leave SMs idle: K is split so that tiles x
+// splits fill the GPU, each split's fp32 partial sums land here and a second
+// kernel adds them in split order (deterministic). splits x T x N <= 152 x 128 x
+// 256, so the bound does not depend on the shape.
+constexpr size_t kGemmWorkspace = (size_t)152 * 128 * 256 * 4;
 cudaError_t gemm(const Gemm& g, cudaStream_t st);
 
 // out[t] = bf16(RMSNorm(v[t]) * w) over E values, v = a (b null) or

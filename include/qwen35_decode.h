@@ -397,7 +397,11 @@ QWEN35_API int qwen35_prefill_step(const qwen35_config* cfg, const qwen35_layer*
  * taken as W = bf16(w) + bf16(w - bf16(w)) (w to 2^-16 relative) when exact is
  * nonzero, else as W = bf16(w); fp32 accumulation on the tensor cores. X bf16
  * [n_tokens][k], Y bf16 [n_tokens][n], device pointers, 16-byte aligned; scratch:
- * at least 256 bytes (its status word). Errors: INVALID_ARGUMENT, CUDA. */
+ * at least 256 bytes (its status word); with QWEN35_PREFILL_GEMM_SPLIT_SCRATCH
+ * bytes or more, a GEMM whose 128-row x 256-token tiles would leave SMs idle
+ * splits K over more CTAs (fp32 partial sums in the scratch, added in a fixed
+ * order). Errors: INVALID_ARGUMENT, CUDA. */
+#define QWEN35_PREFILL_GEMM_SPLIT_SCRATCH (256u + 152u * 128u * 256u * 4u)
 QWEN35_API int qwen35_prefill_gemm(const qwen35_qweight* w, const qwen35_bf16* X, qwen35_bf16* Y,
                                    uint32_t n_tokens, int exact, void* scratch, size_t scratch_bytes,
                                    void* stream);

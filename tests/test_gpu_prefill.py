@@ -42,10 +42,11 @@ def _ulp(v):
     return np.where(a > 0, 2.0 ** (e - 7), 0.0)
 
 
+@pytest.mark.parametrize("split", [False, True])
 @pytest.mark.parametrize("exact", [True, False])
 @pytest.mark.parametrize("n,k,T", [(300, 320, 200), (128, 64, 1), (37, 256, 129), (9216, 2560, 256),
                                    (32, 2560, 77), (2560, 9216, 300)])
-def test_prefill_gemm_matches_weight_product(n, k, T, exact):
+def test_prefill_gemm_matches_weight_product(n, k, T, exact, split):
     """Rows past a 128-row tile and tokens past a 256-token tile (ragged tails), K
     past the 4-slot ring. Against bf16(X W^T) with the weights the form defines (the
     exact dequantised weights, or each rounded to bf16): a misplaced operand or a
@@ -53,14 +54,15 @@ def test_prefill_gemm_matches_weight_product(n, k, T, exact):
     rows or tokens; here every output is within one bf16 unit of the reference plus
     1e-3 of the rms (the tensor cores' fp32 accumulation and, exact, the weights'
     2^-16 split, which move only outputs near a rounding boundary or near zero),
-    and 99.9% are within one unit."""
+    and 99.9% are within one unit. With the split-K workspace, shapes of few tiles
+    sum K in up to eight ranges (the same bounds hold)."""
     init()
     qw = synth.qweight(3, ("pf", n, k), n, k)
     w = B.DeviceQWeight(qw)
     X = synth.to_bf16_bits(np.random.default_rng(n + k + T).standard_normal((T, k)))
     x = B.to_device(X)
     y = torch.empty((T, n), dtype=torch.int16, device="cuda")
-    scratch = B.new_scratch(256)
+    scratch = B.new_scratch(B.QWEN35_PREFILL_GEMM_SPLIT_SCRATCH if split else 256)
     assert B.qwen35_prefill_gemm(w.c(), x, y, T, scratch, exact=exact) == 0
     wt = O.dequant(qw) if exact else O.bf16_round(O.dequant(qw))
     ref = O.bf16_round(O.bf16_to_f64(X) @ wt.T)
@@ -70,7 +72,7 @@ def test_prefill_gemm_matches_weight_product(n, k, T, exact):
     err = np.abs(got - ref)
     excess = np.maximum(err - _ulp(ref), 0.0)
     ulps = bf16_ulps(got, ref)
-    print(f"n={n} k={k} T={T} exact={exact}: max err / rms {err.max() / rms:.3e}, beyond one unit / rms "
+    print(f"n={n} k={k} T={T} exact={exact} split={split}: max err / rms {err.max() / rms:.3e}, beyond one unit / rms "
           f"{excess.max() / rms:.3e}, rel-L2 {rel_l2(got, ref):.3e}, within 1 unit {np.mean(ulps <= 1):.6f}")
     assert excess.max() <= 1e-3 * rms
     assert np.mean(ulps <= 1) >= 0.999
@@ -375,3 +377,41 @@ def test_prefill_stack_turbo8_then_decode():
         torch.cuda.synchronize()
         assert rel_l2(f64(xo), ref) <= TOL_X, s
     assert B.qwen35_read_device_status(pscr) == 0 and B.qwen35_read_device_status(scratch) == 0
+
+
+def test_prefill_step_captured_in_a_graph():
+    """A stack prefill captured once as a CUDA graph and replayed computes what the
+    call computes eagerly, bit for bit (outputs, caches and states)."""
+    init()
+    cfg = synth.config("tiny")
+    c = B.make_config(cfg)
+    kinds = synth.layer_kinds(cfg)
+    layers = [synth.gdn_layer(0, 0, cfg), synth.fa_layer(0, 1, cfg)]
+    conv, ssm = synth.gdn_state(0, 0, cfg, 0.1)
+    kb, vb = synth.kv_cache(0, 1, cfg, 32, 0)
+    T = 20
+    X = _prompt(3, T, cfg)
+    runs = []
+    for use_graph in (False, True):
+        dev = [B.DeviceGdnLayer(layers[0]), B.DeviceFaLayer(layers[1])]
+        caches = [B.DeviceState(conv, ssm), B.DeviceKv(kb, vb)]
+        entries = [B.stack_layer(k, l, cc) for k, l, cc in zip(kinds, dev, caches)]
+        x_in = B.to_device(X)
+        x_out = torch.empty_like(x_in)
+        scr = B.new_scratch(B.qwen35_prefill_scratch_bytes(c, T))
+        stream = torch.cuda.Stream()
+        torch.cuda.synchronize()
+        if use_graph:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+                assert B.qwen35_prefill_step(c, entries, scr, x_in, x_out, 0, T, stream) == 0
+            with torch.cuda.stream(stream):
+                g.replay()
+        else:
+            with torch.cuda.stream(stream):
+                assert B.qwen35_prefill_step(c, entries, scr, x_in, x_out, 0, T, stream) == 0
+        stream.synchronize()
+        runs.append((bits(x_out), f32(caches[0].ssm_matrix()), bits(caches[1].k), bits(caches[1].v)))
+        assert B.qwen35_read_device_status(scr) == 0
+    for a, b in zip(*runs):
+        np.testing.assert_array_equal(a, b)
