@@ -326,15 +326,24 @@ int fa_forward(const qwen35_config* cfg, const qwen35_fa_layer* layer, void* scr
   return launch(p, true, false, st);
 }
 
-int gdn_forward(const qwen35_config* cfg, const qwen35_gdn_layer* layer, void* scratch, size_t scratch_bytes,
-                const qwen35_gdn_state* state, const uint16_t* x_in, uint16_t* x_out, cudaStream_t st) {
-  Dims d;
+// The linear-attention forward's checks of everything but the scratch.
+int gdn_check(const qwen35_config* cfg, const qwen35_gdn_layer* layer, const qwen35_gdn_state* state,
+              const uint16_t* x_in, const uint16_t* x_out, Dims& d) {
   int r = check_config(cfg, d);
   if (r) return r;
   if ((r = check_gdn_dims(d))) return r;
   if ((r = check_gdn_layer(layer, d))) return r;
   if (!state || !aligned16(state->conv_state) || !aligned16(state->gdn_state)) return QWEN35_ERR_INVALID_ARGUMENT;
-  if (!aligned16(x_in) || !aligned16(x_out) || !aligned16(scratch)) return QWEN35_ERR_INVALID_ARGUMENT;
+  if (!aligned16(x_in) || !aligned16(x_out)) return QWEN35_ERR_INVALID_ARGUMENT;
+  return QWEN35_OK;
+}
+
+int gdn_forward(const qwen35_config* cfg, const qwen35_gdn_layer* layer, void* scratch, size_t scratch_bytes,
+                const qwen35_gdn_state* state, const uint16_t* x_in, uint16_t* x_out, cudaStream_t st) {
+  Dims d;
+  const int r = gdn_check(cfg, layer, state, x_in, x_out, d);
+  if (r) return r;
+  if (!aligned16(scratch)) return QWEN35_ERR_INVALID_ARGUMENT;
   const Layout lay = layout(d, kHasGdn);
   if (scratch_bytes < lay.total) return QWEN35_ERR_INVALID_ARGUMENT;
   if (num_sms() <= 0) return QWEN35_ERR_CUDA;
@@ -460,9 +469,12 @@ void* static_scratch() {
 int qwen35_forward_linear_attention_static(const qwen35_config* cfg, const qwen35_gdn_layer* layer,
                                            const qwen35_gdn_state* state, const qwen35_bf16* x_in,
                                            qwen35_bf16* x_out, void* stream) {
-  const size_t need = qwen35_scratch_bytes(cfg, QWEN35_LAYER_LINEAR_ATTENTION);
-  if (need == 0) return QWEN35_ERR_INVALID_ARGUMENT;
-  if (need > QWEN35_STATIC_SCRATCH_BYTES) return QWEN35_ERR_UNSUPPORTED;
+  // every argument is checked before the device is touched: a rejected call leaves
+  // the array (and the previous call's status word) as it was
+  Dims d;
+  const int r = gdn_check(cfg, layer, state, x_in, x_out, d);
+  if (r) return r;
+  if (layout(d, kHasGdn).total > QWEN35_STATIC_SCRATCH_BYTES) return QWEN35_ERR_UNSUPPORTED;
   void* scratch = static_scratch();
   if (!scratch) return QWEN35_ERR_CUDA;
   cudaStream_t st = (cudaStream_t)stream;

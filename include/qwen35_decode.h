@@ -252,9 +252,11 @@ QWEN35_API int qwen35_forward_linear_attention(const qwen35_config* cfg, const q
  * (qwen35_scratch_bytes) exceeds it are rejected with QWEN35_ERR_UNSUPPORTED.
  * The first call on a device looks the array's device address up (once per
  * device, with that device current); make that first call before any stream
- * capture. Every call shares the array and each call clears its status word
- * first, so calls whose work overlaps on the GPU (other streams, other host
- * threads) race on it: serialise them. Arguments and errors otherwise as
+ * capture. Every call shares the array and each accepted call clears its status
+ * word first, so calls whose work overlaps on the GPU (other streams, other host
+ * threads) race on it: serialise them. Every argument is checked before the
+ * device is touched: a rejected call enqueues nothing and leaves the previous
+ * call's status word as it was. Arguments and errors otherwise as
  * qwen35_forward_linear_attention. Allocates nothing (no cudaMalloc/cudaFree). */
 #define QWEN35_STATIC_SCRATCH_BYTES (256u * 1024u)
 QWEN35_API int qwen35_forward_linear_attention_static(const qwen35_config* cfg,
