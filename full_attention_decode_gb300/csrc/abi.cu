@@ -470,11 +470,14 @@ int qwen35_forward_linear_attention_static(const qwen35_config* cfg, const qwen3
                                            const qwen35_gdn_state* state, const qwen35_bf16* x_in,
                                            qwen35_bf16* x_out, void* stream) {
   // every argument is checked before the device is touched: a rejected call leaves
-  // the array (and the previous call's status word) as it was
+  // the array (and the previous call's status word) as it was. The config first:
+  // one that needs more scratch than the array is unsupported whatever the pointers.
   Dims d;
-  const int r = gdn_check(cfg, layer, state, x_in, x_out, d);
+  int r = check_config(cfg, d);
   if (r) return r;
+  if ((r = check_gdn_dims(d))) return r;
   if (layout(d, kHasGdn).total > QWEN35_STATIC_SCRATCH_BYTES) return QWEN35_ERR_UNSUPPORTED;
+  if ((r = gdn_check(cfg, layer, state, x_in, x_out, d))) return r;
   void* scratch = static_scratch();
   if (!scratch) return QWEN35_ERR_CUDA;
   cudaStream_t st = (cudaStream_t)stream;

@@ -102,6 +102,10 @@ def test_static_forward_rejects_configs_larger_than_the_array():
     st = B.qwen35_gdn_state(0xA0000000, 0xB0000000)
     assert B.qwen35_forward_linear_attention_static(c, _fake_gdn(cfg), st, X, Y, _NO_STREAM) == \
         B.QWEN35_ERR_UNSUPPORTED
+    # the size is judged on the config alone, before the pointers: an empty layer
+    # and null state are still unsupported, not invalid
+    assert B.qwen35_forward_linear_attention_static(c, B.qwen35_gdn_layer(), B.qwen35_gdn_state(0, 0), 0, 0,
+                                                    _NO_STREAM) == B.QWEN35_ERR_UNSUPPORTED
     # the 4B shape fits
     c4 = B.make_config(synth.config("4b"))
     assert B.qwen35_scratch_bytes(c4, B.QWEN35_LAYER_LINEAR_ATTENTION) <= _STATIC_BYTES
