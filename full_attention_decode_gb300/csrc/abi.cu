@@ -507,10 +507,12 @@ size_t batch_need(size_t one, uint32_t batch) { return 256 + (size_t)batch * (on
 // A program of layers over a batch of sequences. `advance`: the kernel advances
 // every sequence's device position after the last layer (a decode step); the
 // per-layer batched forwards leave the positions alone, and a program without a
-// full-attention layer reads none (d_cache_pos may then be null).
+// full-attention layer reads none (d_cache_pos may then be null). `check_only`:
+// return after the argument checks, before any CUDA call.
 int decode_step(const qwen35_config* cfg, const qwen35_layer* layers, uint32_t num_layers, uint32_t batch,
                 void* scratch, size_t scratch_bytes, const qwen35_bf16* x_in, qwen35_bf16* x_out,
-                int32_t* d_cache_pos, uint32_t max_seq_len, cudaStream_t stream, bool advance = true) {
+                int32_t* d_cache_pos, uint32_t max_seq_len, cudaStream_t stream, bool advance = true,
+                bool check_only = false) {
   if (!layers || num_layers == 0 || num_layers > (uint32_t)kMaxLayers || batch == 0 ||
       batch > (uint32_t)kMaxBatch)
     return QWEN35_ERR_INVALID_ARGUMENT;
@@ -544,6 +546,7 @@ int decode_step(const qwen35_config* cfg, const qwen35_layer* layers, uint32_t n
   const Layout lay = stack_layout(d, has_fa, has_gdn);
   const size_t one = lay.total;
   if (scratch_bytes < batch_need(one, batch)) return QWEN35_ERR_INVALID_ARGUMENT;
+  if (check_only) return QWEN35_OK;
   if (num_sms() <= 0) return QWEN35_ERR_CUDA;
   Program* p = new_program(cfg, d, scratch);
   if (!p) return QWEN35_ERR_CUDA;
@@ -617,9 +620,12 @@ int graph_create(const qwen35_config* cfg, const qwen35_layer* layers, uint32_t 
   *out_graph = nullptr;
   cudaStream_t st = (cudaStream_t)stream;
   if (st == nullptr) return QWEN35_ERR_INVALID_ARGUMENT;  // the legacy stream cannot be captured
-  if (cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal) != cudaSuccess) return QWEN35_ERR_CUDA;
+  // argument errors before the capture begins: the caller's stream is left alone
   int r = decode_step(cfg, layers, num_layers, batch, scratch, scratch_bytes, x_in, x_out, d_cache_pos, max_seq_len,
-                      st);
+                      st, true, true);
+  if (r != QWEN35_OK) return r;
+  if (cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal) != cudaSuccess) return QWEN35_ERR_CUDA;
+  r = decode_step(cfg, layers, num_layers, batch, scratch, scratch_bytes, x_in, x_out, d_cache_pos, max_seq_len, st);
   cudaGraph_t g = nullptr;
   cudaError_t e = cudaStreamEndCapture(st, &g);
   if (r != QWEN35_OK) {

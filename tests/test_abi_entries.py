@@ -193,8 +193,8 @@ def test_stack_forms_without_a_device_fail_cleanly():
 
 
 def test_graph_entries_argument_errors():
-    """Graph creation checks its handle and stream before it begins a capture;
-    launch and destroy reject a null graph."""
+    """Graph creation checks its handle, its stream and the whole step before it
+    begins a capture; launch and destroy reject a null graph."""
     cfg = synth.config("tiny")
     c = B.make_config(cfg)
     layers, _keep = _stack(cfg)
@@ -208,6 +208,18 @@ def test_graph_entries_argument_errors():
     assert L.qwen35_graph_create(C.byref(c), arr, 2, S.addr, S.n, X, Y, 0xC0000000, 16, 0x5000, None) == INV
     assert L.qwen35_graph_create_batched(C.byref(c), arr, 2, 2, S.addr, S.n, X, Y, 0xC0000000, 16, None,
                                          C.byref(h)) == INV
+    # a malformed step is rejected before the capture begins: the stream (a fake
+    # handle here) is never used
+    fake_stream = 0x5000
+    small = _Scratch(S.n - 16)
+    assert L.qwen35_graph_create(C.byref(c), arr, 2, small.addr, small.n, X, Y, 0xC0000000, 16, fake_stream,
+                                 C.byref(h)) == INV
+    assert L.qwen35_graph_create(C.byref(c), arr, 2, S.addr, S.n, X + 2, Y, 0xC0000000, 16, fake_stream,
+                                 C.byref(h)) == INV
+    assert L.qwen35_graph_create(C.byref(c), arr, 2, S.addr, S.n, X, Y, None, 16, fake_stream, C.byref(h)) == INV
+    assert L.qwen35_graph_create_batched(C.byref(c), arr, 2, 9, S.addr, S.n, X, Y, 0xC0000000, 16, fake_stream,
+                                         C.byref(h)) == INV
+    assert h.value is None
     assert L.qwen35_graph_launch(None, None) == INV
     assert L.qwen35_graph_destroy(None) == INV
 
