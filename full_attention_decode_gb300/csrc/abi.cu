@@ -1000,6 +1000,15 @@ int pf_gdn(const PfCtx& c, const qwen35_gdn_layer* l, const qwen35_gdn_state* st
   return r;
 }
 
+// The prefill's causal attention holds one kv-head's group of q-heads per CTA, in
+// groups of 1, 2, 4 or 8 q-heads (the single-token forward takes any group).
+int pf_fa_dims(const qwen35_config* cfg, const Dims& d) {
+  const int r = check_fa_dims(cfg, d);
+  if (r) return r;
+  const uint32_t g = d.H / d.Hkv;
+  return g == 1 || g == 2 || g == 4 || g == 8 ? QWEN35_OK : QWEN35_ERR_UNSUPPORTED;
+}
+
 // A prefill's KV cache: bf16 (contiguous or paged) or Turbo8, room for positions
 // [p0, p0 + T).
 int pf_kv_ok(const qwen35_kv_cache* kv, uint32_t p0, uint32_t T) {
@@ -1041,7 +1050,7 @@ int qwen35_prefill_full_attention(const qwen35_config* cfg, const qwen35_fa_laye
                                   qwen35_bf16* x_out, uint32_t cache_pos, uint32_t n_tokens, void* stream) {
   PfCtx c;
   int r = pf_begin(c, cfg, scratch, scratch_bytes, x_in, x_out, n_tokens, (cudaStream_t)stream);
-  if (!r) r = check_fa_dims(cfg, c.d);
+  if (!r) r = pf_fa_dims(cfg, c.d);
   if (!r) r = check_fa_layer(layer, c.d);
   if (!r) r = pf_kv_ok(kv, cache_pos, n_tokens);
   if (r) return r;
@@ -1073,7 +1082,7 @@ int qwen35_prefill_step(const qwen35_config* cfg, const qwen35_layer* layers, ui
   for (uint32_t i = 0; i < num_layers && !r; ++i) {  // every layer checked before anything is enqueued
     const qwen35_layer& L = layers[i];
     if (L.kind == QWEN35_LAYER_FULL_ATTENTION) {
-      r = check_fa_dims(cfg, c.d);
+      r = pf_fa_dims(cfg, c.d);
       if (!r) r = check_fa_layer(L.fa, c.d);
       if (!r) r = pf_kv_ok(L.kv, cache_pos, n_tokens);
     } else if (L.kind == QWEN35_LAYER_LINEAR_ATTENTION) {

@@ -379,8 +379,10 @@ QWEN35_API int qwen35_graph_create_batched(const qwen35_config* cfg, const qwen3
  *  - The stack form runs layer i on layer i-1's output, all at positions
  *    cache_pos .. cache_pos + n_tokens - 1 (nothing is advanced in device memory).
  * Errors: INVALID_ARGUMENT (null or misaligned pointer, n_tokens 0 or above 65536,
- * scratch too small, shape mismatch), OUT_OF_RANGE, UNSUPPORTED, CUDA. Calls only
- * enqueue work on `stream`. */
+ * scratch too small, shape mismatch), OUT_OF_RANGE, UNSUPPORTED (as for the
+ * single-token forwards, and for full attention num_heads / num_kv_heads other
+ * than 1, 2, 4 or 8), CUDA. Every argument is checked before anything is enqueued;
+ * calls only enqueue work on `stream`. */
 QWEN35_API size_t qwen35_prefill_scratch_bytes(const qwen35_config* cfg, uint32_t max_tokens);
 QWEN35_API int qwen35_prefill_full_attention(const qwen35_config* cfg, const qwen35_fa_layer* layer,
                                              void* scratch, size_t scratch_bytes, const qwen35_kv_cache* kv,

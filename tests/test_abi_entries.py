@@ -289,3 +289,37 @@ def test_debug_hooks_check_arguments_and_accept_their_defaults():
     assert L.qwen35_debug_stage_dump(0) == B.QWEN35_OK
     assert L.qwen35_status_string(B.QWEN35_ERR_DEVICE_TIMEOUT) == b"device wait timed out"
     assert L.qwen35_status_string(12345) == b"unknown status"
+
+
+# ------------------------------------------------ prefill head groups
+
+
+@pytest.mark.parametrize("H,Hkv", [(3, 1), (16, 1), (12, 4)])
+def test_prefill_rejects_head_groups_its_attention_lacks(H, Hkv):
+    """The prefill's causal attention takes 1, 2, 4 or 8 q-heads per kv-head; other
+    groups, which the single-token forward accepts, are unsupported before anything
+    is enqueued (the layer and the stack form)."""
+    cfg = synth.config("tiny")
+    cfg["num_heads"], cfg["num_kv_heads"] = H, Hkv
+    c = B.make_config(cfg)
+    assert B.qwen35_scratch_bytes(c, B.QWEN35_LAYER_FULL_ATTENTION) > 0  # a valid decode config
+    fa = _fake_fa(cfg)
+    kv = B.qwen35_kv_cache(0xA0000000, 0xB0000000, 64)
+    S = _Scratch(B.qwen35_prefill_scratch_bytes(c, 16))
+    assert B.qwen35_prefill_full_attention(c, fa, S, kv, X, Y, 0, 16, _NO_STREAM) == B.QWEN35_ERR_UNSUPPORTED
+    layers = [B.qwen35_layer(B.QWEN35_LAYER_FULL_ATTENTION, C.pointer(fa), C.pointer(kv), None, None)]
+    arr = (B.qwen35_layer * 1)(*layers)
+    assert B.lib().qwen35_prefill_step(C.byref(c), arr, 1, S.addr, S.n, X, Y, 0, 16, None) == \
+        B.QWEN35_ERR_UNSUPPORTED
+
+
+@_no_device
+def test_prefill_accepts_supported_head_groups():
+    for H, Hkv in [(4, 1), (8, 4), (8, 1), (4, 4)]:
+        cfg = synth.config("tiny")
+        cfg["num_heads"], cfg["num_kv_heads"] = H, Hkv
+        c = B.make_config(cfg)
+        kv = B.qwen35_kv_cache(0xA0000000, 0xB0000000, 64)
+        S = _Scratch(B.qwen35_prefill_scratch_bytes(c, 16))
+        assert B.qwen35_prefill_full_attention(c, _fake_fa(cfg), S, kv, X, Y, 0, 16, _NO_STREAM) == \
+            B.QWEN35_ERR_CUDA, (H, Hkv)
