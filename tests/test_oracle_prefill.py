@@ -76,12 +76,15 @@ def test_prefill_stack_equals_decode_steps():
     assert np.array_equal(c1[1]["k"], c2[1]["k"]) and np.array_equal(c1[1]["v"], c2[1]["v"])
 
 
-def test_prefill_attention_is_offset_causal_attention():
+@pytest.mark.parametrize("H,Hkv,D,R", [(4, 1, 64, 16), (3, 1, 128, 32), (6, 2, 64, 64), (2, 2, 128, 16)])
+def test_prefill_attention_is_offset_causal_attention(H, Hkv, D, R):
     """Token t of a prompt at cache_pos p0 attends over cache rows [0, p0 + t]:
     every token's attention output equals a library scaled-dot-product attention
     over the final cache with the offset causal mask j <= p0 + t (GQA heads
-    expanded), rounded to bf16."""
+    expanded: q-head h reads kv-head h // (H / Hkv)), rounded to bf16. Group sizes
+    4, 3 and 1 and head dims 64 and 128."""
     cfg = synth.config("tiny")
+    cfg.update(num_heads=H, num_kv_heads=Hkv, head_dim=D, rotary_dim=R)
     layer = synth.fa_layer(2, 1, cfg)
     T, p0, cap = 7, 5, 16
     kb, vb = synth.kv_cache(2, 1, cfg, cap, p0)
