@@ -41,12 +41,18 @@ def gstride(k: int) -> int:
 
 
 # Dimensions (the "Qwen35ForwardConfig" struct of the mod.rs page). "4b" is that
-# page's qwen3_5_4b_mlx_int8 preset; "tiny" is the small correctness case.
+# page's qwen3_5_4b_mlx_int8 preset; "tiny" is the small correctness case;
+# "tiny_alt" is a second small case with the other head dims the kernels are built
+# for (attention 128 with one q-head per kv-head, linear attention 64).
 CONFIGS = {
     "tiny": dict(hidden=256, intermediate=512, num_layers=2, vocab=0, group_size=64,
                  rms_eps=1e-6, num_heads=4, num_kv_heads=1, head_dim=64,
                  rope_theta=1e7, rotary_dim=16, num_k_heads_lin=2, num_v_heads_lin=4,
                  k_head_dim_lin=32, v_head_dim_lin=32, conv_kernel_size=4),
+    "tiny_alt": dict(hidden=256, intermediate=512, num_layers=2, vocab=0, group_size=64,
+                     rms_eps=1e-6, num_heads=3, num_kv_heads=3, head_dim=128,
+                     rope_theta=1e7, rotary_dim=32, num_k_heads_lin=2, num_v_heads_lin=4,
+                     k_head_dim_lin=64, v_head_dim_lin=64, conv_kernel_size=4),
     "4b": dict(hidden=2560, intermediate=9216, num_layers=32, vocab=248320, group_size=64,
                rms_eps=1e-6, num_heads=16, num_kv_heads=4, head_dim=256,
                rope_theta=1e7, rotary_dim=64, num_k_heads_lin=16, num_v_heads_lin=32,

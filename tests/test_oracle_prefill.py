@@ -51,8 +51,8 @@ def test_chunked_delta_rule_detects_a_dropped_decay():
     assert not np.allclose(Sc, S, rtol=1e-3)
 
 
-def _tiny_stack(cache_rows=4, capacity=32):
-    cfg = synth.config("tiny")
+def _tiny_stack(cache_rows=4, capacity=32, name="tiny"):
+    cfg = synth.config(name)
     kinds = synth.layer_kinds(cfg)
     layers = [synth.gdn_layer(0, 0, cfg), synth.fa_layer(0, 1, cfg)]
     conv, ssm = synth.gdn_state(0, 0, cfg, 0.1)
@@ -61,11 +61,12 @@ def _tiny_stack(cache_rows=4, capacity=32):
     return cfg, kinds, layers, caches
 
 
-def test_prefill_stack_equals_decode_steps():
+@pytest.mark.parametrize("name", ["tiny", "tiny_alt"])
+def test_prefill_stack_equals_decode_steps(name):
     """Layer-major over the prompt (prefill_step) equals token-major through the
     stack (decode_step per token at cache_pos + t): outputs, caches and states bit
     for bit."""
-    cfg, kinds, layers, caches = _tiny_stack()
+    cfg, kinds, layers, caches = _tiny_stack(name=name)
     T, p0 = 6, 4
     X = O.bf16_to_f64(np.stack([synth.x_in(1, t, cfg) for t in range(T)]))
     c1, c2 = caches(), caches()
