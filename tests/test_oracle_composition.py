@@ -19,13 +19,19 @@ closed form in which the swapped or missing operand gives a different number.
 """
 
 import numpy as np
+import pytest
 import torch
 import torch.nn.functional as F
 
 from full_attention_decode_gb300 import synth
 from oracle import qwen35_oracle as O
 
-CFG = synth.config("tiny")
+
+@pytest.fixture(params=["tiny", "tiny_alt"])
+def CFG(request):
+    """The small configs: 4 q-heads of dim 64 over one kv-head and linear heads of
+    dim 32, and 3 q-heads of dim 128 over 3 kv-heads and linear heads of dim 64."""
+    return synth.config(request.param)
 
 
 def _t(x):
@@ -69,7 +75,7 @@ def _scale(qw, r, c):
 
 # ---------------------------------------------------------------- full attention
 
-def _fa_run(lay, pos=5, seed=0):
+def _fa_run(CFG, lay, pos=5, seed=0):
     k, v = synth.kv_cache(seed, 1, CFG, 16, pos)
     kv = O.kv_from_bits(k, v)
     x = O.bf16_to_f64(synth.x_in(seed, 2, CFG))
@@ -78,12 +84,12 @@ def _fa_run(lay, pos=5, seed=0):
     return x, out, tr
 
 
-def test_fa_mlp_matches_library_composition():
+def test_fa_mlp_matches_library_composition(CFG):
     """x_out = bf16(x_resid + W_down (silu(bf16(W_gate xn2)) * bf16(W_up xn2))) with
     x_resid = bf16(x_in + o) and xn2 = bf16(RMSNorm(x_resid) * post_ln); o is the
     layer's own o_proj output (nonzero, so x_in and x_resid differ)."""
     lay = synth.fa_layer(4, 1, CFG)
-    x, out, tr = _fa_run(lay)
+    x, out, tr = _fa_run(CFG, lay)
     o = _t(tr["o"])
     assert torch.count_nonzero(o) > 0
     x_resid = _bf(_t(x) + o)
@@ -100,7 +106,7 @@ def test_fa_mlp_matches_library_composition():
     assert not np.array_equal(out, from_x_in.numpy())
 
 
-def test_fa_mlp_one_hot_closed_form():
+def test_fa_mlp_one_hot_closed_form(CFG):
     """One-hot gate/up/down rows: gate_j = s_g,j * xn2[0], up_j = s_u,j * xn2[1], and
     x_out[j] = x_resid[j] + s_d,j * silu(gate_j) * up_j for j < hidden."""
     E, I = CFG["hidden"], CFG["intermediate"]
@@ -110,7 +116,7 @@ def test_fa_mlp_one_hot_closed_form():
     _one_hot_rows(lay["up_proj"], lambda r: 1, scale=0.75)
     _one_hot_rows(lay["down_proj"], lambda r: r, scale=1.0)  # row j reads h_j (E <= I)
     assert I >= E
-    x, out, tr = _fa_run(lay)
+    x, out, tr = _fa_run(CFG, lay)
     xn2 = tr["x_norm2"]
     x_resid = tr["x_resid"]
     g = float(O.bf16_round(2.0 * xn2[0]))
@@ -126,13 +132,13 @@ def test_fa_mlp_one_hot_closed_form():
     assert not np.array_equal(out, O.bf16_round(x + h))  # the residual is x_resid, not x_in
 
 
-def test_fa_qk_norm_then_rope():
+def test_fa_qk_norm_then_rope(CFG):
     """q_rope = bf16(rope(bf16(RMSNorm_head(q) * q_norm))), with non-uniform norm
     weights at a nonzero position; the other order (rotate, then normalise) differs."""
     H, Hkv, D, R = CFG["num_heads"], CFG["num_kv_heads"], CFG["head_dim"], CFG["rotary_dim"]
     lay = synth.fa_layer(6, 1, CFG)
     pos = 7
-    x, out, tr = _fa_run(lay, pos=pos)
+    x, out, tr = _fa_run(CFG, lay, pos=pos)
     q = _t(tr["q_full"]).reshape(H, 2 * D)[:, :D]
     k = _t(tr["k"]).reshape(Hkv, D)
     wq, wk = _bits(lay["q_norm"]), _bits(lay["k_norm"])
@@ -159,7 +165,7 @@ def test_fa_qk_norm_then_rope():
 
 # ---------------------------------------------------------------- linear attention
 
-def _gdn_run(lay, seed=0, steps=2):
+def _gdn_run(CFG, lay, seed=0, steps=2):
     conv, ssm = synth.gdn_state(seed, 0, CFG, std=0.1)
     st = O.state_from_arrays(conv, ssm)
     tr = {}
@@ -170,12 +176,12 @@ def _gdn_run(lay, seed=0, steps=2):
     return x, out, tr
 
 
-def test_gdn_output_gate_matches_library_composition():
+def test_gdn_output_gate_matches_library_composition(CFG):
     """out = bf16(W_out (silu(z) * y_norm)), y_norm = bf16(RMSNorm_head(y) * norm_weight),
     then x_out = bf16(x_resid + MLP) with x_resid = bf16(x_in + out)."""
     Hv, Dv = CFG["num_v_heads_lin"], CFG["v_head_dim_lin"]
     lay = synth.gdn_layer(7, 0, CFG)
-    x, out, tr = _gdn_run(lay)
+    x, out, tr = _gdn_run(CFG, lay)
     y = _t(tr["y"]).reshape(Hv, Dv)
     z = _t(tr["z"])
     y_norm = _bf(F.rms_norm(y, (Dv,), _bits(lay["norm_weight"]), eps=CFG["rms_eps"])).reshape(-1)
@@ -195,12 +201,12 @@ def test_gdn_output_gate_matches_library_composition():
     assert not np.array_equal(tr["out"], no_silu.numpy())
 
 
-def test_gdn_output_gate_one_hot_closed_form():
+def test_gdn_output_gate_one_hot_closed_form(CFG):
     """One-hot out_proj rows: out[j] = s_j * silu(z[c_j]) * y_norm[c_j] with c_j = j mod Z."""
     Z = CFG["num_v_heads_lin"] * CFG["v_head_dim_lin"]
     lay = synth.gdn_layer(8, 0, CFG)
     _one_hot_rows(lay["out_proj"], lambda r: r % Z, scale=1.0)
-    x, out, tr = _gdn_run(lay)
+    x, out, tr = _gdn_run(CFG, lay)
     z, yn = tr["z"], tr["y_norm"]
     c = np.arange(CFG["hidden"]) % Z
     want = O.bf16_round(z[c] / (1.0 + np.exp(-z[c])) * yn[c])
