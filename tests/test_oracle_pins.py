@@ -325,14 +325,16 @@ def test_delta_rule_columns_independent():
 
 # ---------------------------------------------------------------- whole layers
 
-CFG = synth.config("tiny")
+@pytest.fixture(params=["tiny", "tiny_alt"])
+def CFG(request):
+    return synth.config(request.param)
 
 
 def _zero_matrix(qw):
     qw["codes"][:] = 128  # synthetic bias is -128 * scale, so every weight is 0
 
 
-def test_fa_layer_seq1_returns_gated_v():
+def test_fa_layer_seq1_returns_gated_v(CFG):
     lay = synth.fa_layer(0, 1, CFG)
     k, v = synth.kv_cache(0, 1, CFG, 16, 0)
     kv = O.kv_from_bits(k, v)
@@ -351,7 +353,7 @@ def test_fa_layer_seq1_returns_gated_v():
     assert not kv["k"][1:].any() and not kv["v"][1:].any()
 
 
-def test_fa_layer_zero_projections_are_identity_residuals():
+def test_fa_layer_zero_projections_are_identity_residuals(CFG):
     lay = synth.fa_layer(0, 1, CFG)
     _zero_matrix(lay["o_proj"])
     _zero_matrix(lay["down_proj"])
@@ -363,7 +365,7 @@ def test_fa_layer_zero_projections_are_identity_residuals():
     np.testing.assert_array_equal(out, x)
 
 
-def test_gdn_layer_zero_projections_and_state_update():
+def test_gdn_layer_zero_projections_and_state_update(CFG):
     lay = synth.gdn_layer(0, 0, CFG)
     _zero_matrix(lay["out_proj"])
     _zero_matrix(lay["down_proj"])
@@ -382,14 +384,14 @@ def test_gdn_layer_zero_projections_and_state_update():
     kk = tr["qkv_smooth"][nqk:2 * nqk].reshape(Hk, Dk)
     vv = tr["qkv_smooth"][2 * nqk:].reshape(Hv, -1)
     for h in range(Hv):
-        np.testing.assert_allclose(st["ssm"][h], O.f32_round(np.outer(kk[h // 2], tr["beta"][h] * vv[h])),
+        np.testing.assert_allclose(st["ssm"][h], O.f32_round(np.outer(kk[h // (Hv // Hk)], tr["beta"][h] * vv[h])),
                                    rtol=1e-7)
     # the Q and K heads of qkv_smooth are unit vectors (up to bf16 rounding)
     qs = tr["qkv_smooth"][:2 * nqk].reshape(2 * Hk, Dk)
     np.testing.assert_allclose(np.linalg.norm(qs, axis=1), 1.0, atol=1e-2)
 
 
-def test_stack_step_chains_layers():
+def test_stack_step_chains_layers(CFG):
     kinds = synth.layer_kinds(CFG)
     assert kinds == ["gdn", "fa"]
     layers = [synth.gdn_layer(0, 0, CFG), synth.fa_layer(0, 1, CFG)]
@@ -424,7 +426,7 @@ def _head_with_identical_rows(seed, cfg, vocab, winner=None, factor=1.0):
     return h
 
 
-def test_lm_head_greedy_against_library_and_brute_force():
+def test_lm_head_greedy_against_library_and_brute_force(CFG):
     cfg = synth.config("tiny")
     head = synth.head(5, cfg, 300)
     x = O.bf16_to_f64(synth.x_in(5, 0, cfg)) * 3.0
@@ -444,7 +446,7 @@ def test_lm_head_greedy_against_library_and_brute_force():
     assert logits[tok] == logits.max()
 
 
-def test_lm_head_greedy_ties_and_planted_winner():
+def test_lm_head_greedy_ties_and_planted_winner(CFG):
     cfg = synth.config("tiny")
     x = O.bf16_to_f64(synth.x_in(6, 0, cfg))
     base = _head_with_identical_rows(6, cfg, 64)
