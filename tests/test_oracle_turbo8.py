@@ -17,12 +17,15 @@ import torch
 from full_attention_decode_gb300 import synth
 from oracle import qwen35_oracle as O
 
-CFG = synth.config("tiny")
+
+@pytest.fixture(params=["tiny", "tiny_alt"])
+def CFG(request):
+    return synth.config(request.param)
 
 
 # ---------------------------------------------------------------- WHT
 
-@pytest.mark.parametrize("n", [16, 64, 256])
+@pytest.mark.parametrize("n", [16, 64, 128, 256])
 def test_wht_is_the_orthonormal_sylvester_hadamard(n):
     x = np.random.default_rng(n).standard_normal((5, n))
     H = scipy.linalg.hadamard(n) / np.sqrt(n)  # Sylvester order: H_2n = [[H, H], [H, -H]]
@@ -100,7 +103,7 @@ def test_turbo8_quantize_round_trips_representable_groups():
 
 # ---------------------------------------------------------------- the layer's Turbo path
 
-def _turbo_layer_run(pos, seed=0):
+def _turbo_layer_run(CFG, pos, seed=0):
     lay = synth.fa_layer(seed, 1, CFG)
     kc, ks, vc, vs = synth.kv_cache_turbo8(seed, 1, CFG, 16, pos)
     kv = O.turbo8_kv(kc, ks, vc, vs)
@@ -110,12 +113,12 @@ def _turbo_layer_run(pos, seed=0):
     return lay, kv, (kc, ks, vc, vs), tr, out
 
 
-def test_turbo8_one_token_attention_returns_the_rotated_back_v():
+def test_turbo8_one_token_attention_returns_the_rotated_back_v(CFG):
     """At one token the softmax weight is 1: the rotated-basis output is the
     dequantised rotated v (bf16), and the layer's attention output is its inverse
     rotation. Without the inverse rotation, or with q rotated twice, it is not."""
     H, Hkv, D = CFG["num_heads"], CFG["num_kv_heads"], CFG["head_dim"]
-    lay, kv, _, tr, _ = _turbo_layer_run(0)
+    lay, kv, _, tr, _ = _turbo_layer_run(CFG, 0)
     vdeq = O.turbo8_dequantize(*O.turbo8_quantize(tr["v_rot"]))
     for h in range(H):
         np.testing.assert_array_equal(tr["attn_rot"][h], O.bf16_round(vdeq[h // (H // Hkv)]))
@@ -126,9 +129,9 @@ def test_turbo8_one_token_attention_returns_the_rotated_back_v():
     assert np.linalg.norm(O.wht(vdeq) - v) <= 0.05 * np.linalg.norm(v)
 
 
-def test_turbo8_append_writes_row_cache_pos_only():
+def test_turbo8_append_writes_row_cache_pos_only(CFG):
     pos = 6
-    lay, kv, before, tr, _ = _turbo_layer_run(pos)
+    lay, kv, before, tr, _ = _turbo_layer_run(CFG, pos)
     kc, ks, vc, vs = before
     # the rows written are the quantised rotated k (after norm and RoPE) and v
     ck, sk = O.turbo8_quantize(tr["k_rot"])
@@ -145,14 +148,14 @@ def test_turbo8_append_writes_row_cache_pos_only():
     np.testing.assert_array_equal(kv["k_scales"][rows], O.bf16_to_f64(ks[rows]))
 
 
-def test_turbo8_attention_equals_plain_attention_on_the_rotated_back_cache():
+def test_turbo8_attention_equals_plain_attention_on_the_rotated_back_cache(CFG):
     """Rotating q and every cached K row by the same orthonormal transform leaves the
     scores unchanged, and rotating the V-weighted sum back equals weighting the
     rotated-back V rows: the Turbo attention output (before its bf16 roundings)
     equals the plain attention on wht(dequantised rows) with the un-rotated q."""
     pos = 9
     H, Hkv, D = CFG["num_heads"], CFG["num_kv_heads"], CFG["head_dim"]
-    lay, kv, _, tr, _ = _turbo_layer_run(pos)
+    lay, kv, _, tr, _ = _turbo_layer_run(CFG, pos)
     K = O.turbo8_dequantize(kv["k_codes"][:pos + 1], kv["k_scales"][:pos + 1])
     V = O.turbo8_dequantize(kv["v_codes"][:pos + 1], kv["v_scales"][:pos + 1])
     plain = O.attention_decode(O.wht(tr["q_rot"]), O.wht(K), O.wht(V), pos + 1, Hkv)
