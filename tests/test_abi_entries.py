@@ -3,9 +3,10 @@ malformed call is rejected before anything touches the device (the pointers here
 are fake, aligned or deliberately misaligned, and never dereferenced), and a
 well-formed call with no device present fails with QWEN35_ERR_CUDA.
 
-Only the rejected calls run when a CUDA device is present: they return before any
-CUDA call. The debug setters are only ever called with their default values, so
-the library's global state is left as it was for whatever runs next in the process.
+The whole file is skipped where a CUDA device is present: a check lost in a later
+change would otherwise let a fake address reach a kernel on a real GPU. The debug
+setters are only ever called with their default values, so the library's global
+state is left as it was for whatever runs next in the process.
 """
 
 import ctypes as C
@@ -19,6 +20,7 @@ from full_attention_decode_gb300 import synth
 _BASE = 0x10000000  # fake device addresses, 16-byte aligned
 _NO_STREAM = 0
 _no_device = pytest.mark.skipif(torch.cuda.is_available(), reason="a CUDA device is present")
+pytestmark = _no_device
 
 
 def _qw(n, k, i):

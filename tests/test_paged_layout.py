@@ -28,6 +28,9 @@ def test_pool_and_gather_round_trip():
 
 
 def test_paged_cache_argument_errors_precede_launch():
+    import torch
+    if torch.cuda.is_available():  # fake device addresses: a lost check must not reach a real GPU
+        pytest.skip("a CUDA device is present")
     cfg = synth.config("tiny")
     c = B.make_config(cfg)
     lay = _fake_fa(cfg)
@@ -48,8 +51,5 @@ def test_paged_cache_argument_errors_precede_launch():
            kv(block_table=tab + 2)]        # misaligned table
     for k in bad:
         assert f(c, lay, S, k, x, y, 3, 4, 0) == B.QWEN35_ERR_INVALID_ARGUMENT
-    import torch
-    if not torch.cuda.is_available():  # well formed: past every check, then no device
-        assert f(c, lay, S, kv(), x, y, 3, 4, 0) == B.QWEN35_ERR_CUDA
-    else:
-        pytest.skip("a CUDA device is present")
+    # well formed: past every check, then no device
+    assert f(c, lay, S, kv(), x, y, 3, 4, 0) == B.QWEN35_ERR_CUDA
